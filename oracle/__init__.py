@@ -1,0 +1,262 @@
+"""CPU oracle for the per-frame decode hot path (test infrastructure only).
+
+A plain, slow, single-threaded restatement of what each step of the hot path
+computes, compiled from ``oracle.cpp`` with the host compiler and called through
+ctypes on numpy arrays.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may import this package; the CUDA library never
+does, and this package imports nothing from the CUDA library.
+
+Steps and the passages they follow (page titles as printed on the pages):
+
+* ``frame_embed`` -- "qwentts.cpp ... src/pipeline-tts.h", on-device AR input
+  assembly: 16 code-embedding rows gathered and summed with the trailing text/pad
+  overlay; the code predictor gathers one sub-code from its own group table.
+* ``rms_norm_rope`` -- "minicpm-o-4.5 ... docs/optimizations.md", core table, fused
+  "q/k norm + RoPE" (norm, then rotation).
+* ``kv_set_rows`` -- "qwentts.cpp ... src/pipeline-tts.h", fixed topology section:
+  KV writes through set_rows with destination rows carried as data; bf16 rounding by
+  integer round-to-nearest-even as in the optimizations table.
+* ``decode_attn`` -- "qwentts.cpp ... src/pipeline-tts.h", persistent arenas and KV
+  cache sections: decode reads the [0, cur_len+1) window, padded tail masked by -inf.
+* ``decode_step`` / ``predictor_frame`` -- compositions of the above in the order the
+  KV cache section gives (norm+RoPE, write the new row, attend; the predictor resets
+  its 16-slot cache, prefills T=2 and then decodes 14 single tokens).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.cpp")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+CFLAGS = ["-O2", "-std=c++17", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared"]
+
+
+def build(force: bool = False) -> str:
+    """Compile ``oracle.cpp`` into ``_build/liboracle.so`` (host compiler, no GPU)."""
+    os.makedirs(_BUILD, exist_ok=True)
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        subprocess.check_call(["g++", *CFLAGS, _SRC, "-o", tmp])
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            P, I, L, D = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_double
+            lib.oracle_bf16_rne.argtypes = [ctypes.c_float]
+            lib.oracle_bf16_rne.restype = ctypes.c_uint16
+            lib.oracle_frame_embed.argtypes = [P, I, I, I, P, L, P, L, P, I]
+            lib.oracle_frame_embed.restype = I
+            lib.oracle_rms_norm_rope.argtypes = [P, L, P, L, I, I, I, P, ctypes.c_float, P, D]
+            lib.oracle_rms_norm_rope.restype = None
+            lib.oracle_rope_angle.argtypes = [I, I, I, D, P]
+            lib.oracle_rope_angle.restype = None
+            lib.oracle_kv_set_rows.argtypes = [P, P, L, P, P, I, I, I, I, I, I, I, I, P, I, P]
+            lib.oracle_kv_set_rows.restype = I
+            lib.oracle_decode_attn.argtypes = [P, L, P, P, I, I, I, I, I, I, I, I, I, P, I, P, D, P, P]
+            lib.oracle_decode_attn.restype = I
+            _lib = lib
+    return _lib
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data
+
+
+def _c(a, dtype):
+    """Contiguous array of the given dtype (no copy when already so)."""
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+# ---------------------------------------------------------------------------
+# bf16 helpers
+# ---------------------------------------------------------------------------
+def bf16_rne(x: float) -> int:
+    """bf16 bit pattern of one f32 value, integer round-to-nearest-even."""
+    return int(_load().oracle_bf16_rne(ctypes.c_float(float(np.float32(x)))))
+
+
+def bf16_rne_array(x) -> np.ndarray:
+    """Elementwise bf16 RNE of an f32 array, as uint16 (one oracle call per element)."""
+    x = _c(x, np.float32)
+    lib = _load()
+    out = np.empty(x.shape, np.uint16)
+    flat_in, flat_out = x.reshape(-1), out.reshape(-1)
+    for i in range(flat_in.size):
+        flat_out[i] = lib.oracle_bf16_rne(ctypes.c_float(float(flat_in[i])))
+    return out
+
+
+def bf16_bits_to_f32(h) -> np.ndarray:
+    """Exact widening of bf16 bit patterns (uint16) to f32."""
+    h = np.asarray(h, dtype=np.uint16)
+    return (h.astype(np.uint32) << 16).view(np.float32)
+
+
+# ---------------------------------------------------------------------------
+# a1: frame-input composition
+# ---------------------------------------------------------------------------
+def frame_embed(tables, ids, overlay=None):
+    """out[b] = ((E_0[c_b0] + E_1[c_b1]) + ... ) + overlay[b], f32, fixed order.
+
+    tables: list of [vocab][hidden] f32 arrays; ids: [B][n_tables] int32;
+    overlay: [B][hidden] f32 or None.  Returns (out [B][hidden] f32, clamped flag).
+    """
+    tabs = [_c(t, np.float32) for t in tables]
+    ids = _c(ids, np.int32)
+    B, n = ids.shape
+    vocab, hidden = tabs[0].shape
+    arr = (ctypes.c_void_p * n)(*[t.ctypes.data for t in tabs])
+    ov = None if overlay is None else _c(overlay, np.float32)
+    out = np.empty((B, hidden), np.float32)
+    flag = _load().oracle_frame_embed(arr, n, vocab, hidden, _ptr(ids), n, _ptr(ov),
+                                      hidden, _ptr(out), B)
+    return out, int(flag)
+
+
+# ---------------------------------------------------------------------------
+# a2: per-head RMSNorm + RoPE
+# ---------------------------------------------------------------------------
+def rms_norm_rope(x, gamma, eps, pos, base):
+    """x: [B][H][D] f32 -> normed and rotated copy (f32), per the a2 definition."""
+    x = _c(x, np.float32)
+    B, H, D = x.shape
+    gamma = _c(gamma, np.float32)
+    pos = _c(pos, np.int32)
+    y = np.empty_like(x)
+    _load().oracle_rms_norm_rope(_ptr(x), H * D, _ptr(y), H * D, B, H, D, _ptr(gamma),
+                                 ctypes.c_float(eps), _ptr(pos), float(base))
+    return y
+
+
+def rope_angle(pos: int, i: int, head_dim: int, base: float):
+    cs = np.empty(2, np.float64)
+    _load().oracle_rope_angle(int(pos), int(i), int(head_dim), float(base), _ptr(cs))
+    return float(cs[0]), float(cs[1])
+
+
+# ---------------------------------------------------------------------------
+# Cache descriptor shared by a3/a4 on the oracle side
+# ---------------------------------------------------------------------------
+class KvLayout:
+    """Geometry of one layer's K/V cache, head-major (see ``oracle.cpp``)."""
+
+    def __init__(self, B, n_kv_heads, head_dim, capacity, kv_dtype="f32", paged=False,
+                 page_size=16, n_pages=0, block_table=None):
+        self.B, self.n_kv_heads, self.head_dim, self.capacity = B, n_kv_heads, head_dim, capacity
+        self.kv_dtype = kv_dtype
+        self.paged = bool(paged)
+        self.page_size = page_size
+        self.n_pages = n_pages
+        self.block_table = None if block_table is None else _c(block_table, np.int32)
+
+    @property
+    def dtype_code(self):
+        return 0 if self.kv_dtype == "f32" else 1
+
+    @property
+    def bt_stride(self):
+        return 0 if self.block_table is None else self.block_table.shape[1]
+
+
+def kv_set_rows(k, v, k_cache, v_cache, layout: KvLayout, dst_pos):
+    """Write k[b], v[b] ([B][Hkv][D] f32) into the caches at dst_pos[b], in place.
+
+    Caches are numpy arrays (f32, or uint16 holding bf16 bits).  Returns the
+    skipped-write flag.
+    """
+    k = _c(k, np.float32)
+    v = _c(v, np.float32)
+    B = k.shape[0]
+    row = k.shape[1] * k.shape[2]
+    dst_pos = _c(dst_pos, np.int32)
+    assert k_cache.flags.c_contiguous and v_cache.flags.c_contiguous
+    L = layout
+    return int(_load().oracle_kv_set_rows(
+        _ptr(k), _ptr(v), row, _ptr(k_cache), _ptr(v_cache), L.dtype_code, B, L.n_kv_heads,
+        L.head_dim, L.capacity, int(L.paged), L.page_size, L.n_pages, _ptr(L.block_table),
+        L.bt_stride, _ptr(dst_pos)))
+
+
+def decode_attn(q, k_cache, v_cache, layout: KvLayout, n_valid, scale, want_weights=False):
+    """Single-query GQA attention over [0, n_valid[b]) per stream, double precision.
+
+    q: [B][Hq][D] f32.  Returns (out [B][Hq][D] f32, weights or None, clamped flag).
+    """
+    q = _c(q, np.float32)
+    B, Hq, D = q.shape
+    n_valid = _c(n_valid, np.int32)
+    L = layout
+    out = np.empty((B, Hq, D), np.float32)
+    w = np.empty((B, Hq, L.capacity), np.float64) if want_weights else None
+    flag = _load().oracle_decode_attn(
+        _ptr(q), Hq * D, _ptr(k_cache), _ptr(v_cache), L.dtype_code, B, Hq, L.n_kv_heads, D,
+        L.capacity, int(L.paged), L.page_size, L.n_pages, _ptr(L.block_table), L.bt_stride,
+        _ptr(n_valid), float(scale), _ptr(out), _ptr(w))
+    return out, w, int(flag)
+
+
+# ---------------------------------------------------------------------------
+# Compositions
+# ---------------------------------------------------------------------------
+def decode_step(q, k, v, gamma_q, gamma_k, eps, base, k_cache, v_cache, layout: KvLayout,
+                cur_len, scale):
+    """One layer of one decode step for B streams, in the order the pages give:
+    q/k RMSNorm + RoPE at position cur_len, write the new K/V row at cur_len, attend
+    over [0, cur_len + 1).  Mutates the caches; returns the attention output."""
+    cur_len = _c(cur_len, np.int32)
+    qn = rms_norm_rope(q, gamma_q, eps, cur_len, base)
+    kn = rms_norm_rope(k, gamma_k, eps, cur_len, base)
+    kv_set_rows(kn, v, k_cache, v_cache, layout, cur_len)
+    out, _, _ = decode_attn(qn, k_cache, v_cache, layout, cur_len + 1, scale)
+    return out
+
+
+def predictor_frame(group_tables, codes, bridge, qkv_per_substep, gammas, eps, base,
+                    caches, layout: KvLayout, scale):
+    """One code-predictor frame for B streams ("qwentts.cpp", KV cache section).
+
+    The 16-slot cache is reset (cur_len = 0; stale rows are masked, not cleared), the
+    T=2 prefill writes rows 0 and 1 causally, then 14 single-token decodes write rows
+    2..15.  Sub-step j gathers code j from group table j (the bridge row stands in
+    front of the c0 row in the prefill).  The QKV projection between the gathered row
+    and q/k/v is outside this path, so q/k/v per sub-step and layer are inputs.
+
+    group_tables: 15 arrays [vocab][hidden]; codes: [B][15] int32; bridge: [B][hidden];
+    qkv_per_substep[t][l] = (q, k, v) for sub-step t in 0..15 (t=0,1 the prefill rows);
+    gammas[l] = (gamma_q, gamma_k); caches[l] = (k_cache, v_cache).
+    Returns (embeds, outs): embeds[j] the gathered row for sub-step j (j = 0..14),
+    outs[t][l] the attention output of sub-step t at layer l.
+    """
+    codes = _c(codes, np.int32)
+    B = codes.shape[0]
+    embeds = []
+    for j in range(15):
+        e, _ = frame_embed([group_tables[j]], codes[:, j:j + 1], None)
+        embeds.append(e)
+    outs = []
+    n_layers = len(caches)
+    for t in range(16):
+        cur = np.full(B, t, np.int32)
+        per_layer = []
+        for l in range(n_layers):
+            q, k, v = qkv_per_substep[t][l]
+            gq, gk = gammas[l]
+            kc, vc = caches[l]
+            per_layer.append(decode_step(q, k, v, gq, gk, eps, base, kc, vc, layout, cur, scale))
+        outs.append(per_layer)
+    return embeds, outs

@@ -1,0 +1,447 @@
+"""Pins of the CPU oracle against things other than itself.
+
+Each test checks the oracle against a closed form, a hand-derived value (golden
+fixtures under tests/golden/), a library routine (torch's rms_norm and
+scaled_dot_product_attention in float64, torch's bf16 conversion, sympy's
+high-precision cos/sin), or an invariant that the definition implies.  The cases are
+chosen so that a plausible slip in the oracle (wrong table or row, wrong summation
+order, a dropped eps, a sign or index error in the rotation, a transposed or
+mis-mapped head, a softmax over the padded tail) fails at least one of them.
+"""
+import math
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import sympy as sp
+import torch
+
+import oracle
+from conftest import read_golden
+
+F = torch.nn.functional
+
+
+def f32_from_bits(u):
+    return np.array([u], dtype=np.uint32).view(np.float32)[0]
+
+
+# ---------------------------------------------------------------------------
+# a1: frame-input composition
+# ---------------------------------------------------------------------------
+def test_embed_exact_closed_form():
+    """Entries chosen so every partial sum is exact in f32: the result must equal the
+    exact rational sum of the addressed rows, which pins table/row/column indexing."""
+    n, vocab, hidden, B = 16, 64, 32, 3
+    tabs = []
+    for g in range(n):
+        c = np.arange(vocab)[:, None]
+        i = np.arange(hidden)[None, :]
+        tabs.append((2.0 * g + c * 2.0 ** -6 + i * 2.0 ** -12).astype(np.float32))
+    rng = np.random.default_rng(1)
+    ids = rng.integers(0, vocab, size=(B, n)).astype(np.int32)
+    ov = (np.arange(B)[:, None] * 2.0 ** -8 + np.zeros((1, hidden))).astype(np.float32)
+    out, flag = oracle.frame_embed(tabs, ids, ov)
+    assert flag == 0
+    for b in range(B):
+        for i in range(hidden):
+            exact = sum(Fraction(2 * g) + Fraction(int(ids[b, g]), 64) + Fraction(i, 4096)
+                        for g in range(n)) + Fraction(b, 256)
+            assert Fraction(float(out[b, i])) == exact
+
+
+def test_embed_left_to_right_order_and_overlay_last():
+    """Hand-derived: 1.0 followed by fifteen 2^-24 terms, added left to right in f32,
+    stays exactly 1.0 (each addition is a tie that rounds to even); the overlay -1.0
+    then gives exactly 0.  Any other order (pairwise, reversed, overlay first) keeps
+    some of the small terms and gives a nonzero result."""
+    vocab, hidden = 4, 8
+    tabs = [np.full((vocab, hidden), 2.0 ** -24, np.float32) for _ in range(16)]
+    tabs[0][:] = 1.0
+    ids = np.zeros((1, 16), np.int32)
+    out, _ = oracle.frame_embed(tabs, ids, np.full((1, hidden), -1.0, np.float32))
+    assert np.all(out == 0.0)
+    out_no_ov, _ = oracle.frame_embed(tabs, ids, None)
+    assert np.all(out_no_ov == 1.0)
+
+
+def test_embed_single_table_is_a_row_copy():
+    """Predictor sub-steps gather one row from one group table, no overlay."""
+    rng = np.random.default_rng(2)
+    tab = rng.standard_normal((50, 16)).astype(np.float32)
+    ids = np.array([[7], [49], [0]], np.int32)
+    out, _ = oracle.frame_embed([tab], ids, None)
+    assert np.array_equal(out, tab[[7, 49, 0]])
+
+
+def test_embed_clamps_out_of_range_ids():
+    tab = np.arange(12, dtype=np.float32).reshape(4, 3)
+    out, flag = oracle.frame_embed([tab], np.array([[-1], [4], [2]], np.int32), None)
+    assert flag == 1
+    assert np.array_equal(out, tab[[0, 3, 2]])
+
+
+# ---------------------------------------------------------------------------
+# a2: RMSNorm + RoPE
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("D", [4, 64, 128])
+def test_norm_matches_torch_rms_norm_at_position_zero(D):
+    """At position 0 every angle is 0, so the output is the RMSNorm alone; compare with
+    torch's rms_norm in float64 (weight = gamma, eps inside the root)."""
+    rng = np.random.default_rng(D)
+    x = rng.standard_normal((3, 5, D)).astype(np.float32)
+    gam = rng.uniform(0.5, 1.5, D).astype(np.float32)
+    eps = np.float32(1e-6)
+    y = oracle.rms_norm_rope(x, gam, eps, np.zeros(3, np.int32), 1e6)
+    ref = F.rms_norm(torch.from_numpy(x).double(), (D,), weight=torch.from_numpy(gam).double(),
+                     eps=float(eps)).numpy().astype(np.float32)
+    np.testing.assert_array_max_ulp(y, ref, maxulp=1)
+
+
+def test_norm_constant_row_closed_form():
+    """x = c everywhere, gamma = 1, pos 0: every output equals c / sqrt(c^2 + eps)."""
+    D = 128
+    for c in [3.0, -0.25, 1e-3]:
+        x = np.full((1, 1, D), c, np.float32)
+        eps = np.float32(1e-6)
+        y = oracle.rms_norm_rope(x, np.ones(D, np.float32), eps, np.zeros(1, np.int32), 1e6)
+        expect = np.float32(np.float32(c) / math.sqrt(float(np.float32(c)) ** 2 + float(eps)))
+        np.testing.assert_array_max_ulp(y, np.full_like(y, expect), maxulp=1)
+
+
+def test_rope_angles_hand_derived():
+    for pos, i, D, base, c, s in read_golden("rope_angles.txt"):
+        got = oracle.rope_angle(int(pos), int(i), int(D), float(base))
+        assert got[0] == pytest.approx(float(c), abs=1e-15)
+        assert got[1] == pytest.approx(float(s), abs=1e-15)
+
+
+@pytest.mark.parametrize("pos", [1, 37, 255, 4095])
+def test_rope_angles_against_sympy(pos):
+    """theta_i = pos * base^(-2i/D) evaluated by sympy to 40 digits, base 1e6, D 128,
+    at the first, a middle and the last frequency."""
+    D, base = 128, 10 ** 6
+    for i in [0, 1, 17, 63]:
+        theta = sp.Integer(pos) * sp.Integer(base) ** sp.Rational(-2 * i, D)
+        c = float(sp.N(sp.cos(theta), 40))
+        s = float(sp.N(sp.sin(theta), 40))
+        got = oracle.rope_angle(pos, i, D, float(base))
+        assert got[0] == pytest.approx(c, abs=1e-12)
+        assert got[1] == pytest.approx(s, abs=1e-12)
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_rope_is_complex_rotation_of_the_normed_halves(D):
+    """Rotate-half RoPE equals multiplying t_i + i t_{i+D/2} by exp(i theta_i).  The
+    normed t comes from torch's rms_norm (float64), the angles from sympy."""
+    rng = np.random.default_rng(10 + D)
+    B, H = 2, 3
+    x = rng.standard_normal((B, H, D)).astype(np.float32)
+    gam = rng.uniform(0.5, 1.5, D).astype(np.float32)
+    pos = np.array([5, 4095], np.int32)
+    eps = np.float32(1e-6)
+    y = oracle.rms_norm_rope(x, gam, eps, pos, 1e6)
+    t = F.rms_norm(torch.from_numpy(x).double(), (D,), weight=torch.from_numpy(gam).double(),
+                   eps=float(eps)).numpy()
+    for b in range(B):
+        ang = np.array([complex(sp.N(sp.exp(sp.I * sp.Integer(int(pos[b])) *
+                                            sp.Integer(10 ** 6) ** sp.Rational(-2 * i, D)), 30))
+                        for i in range(D // 2)])
+        z = (t[b, :, :D // 2] + 1j * t[b, :, D // 2:]) * ang[None, :]
+        ref = np.concatenate([z.real, z.imag], axis=-1).astype(np.float32)
+        np.testing.assert_allclose(y[b], ref, rtol=0, atol=2e-7 * np.abs(ref).max())
+
+
+def test_rope_preserves_pair_norms():
+    rng = np.random.default_rng(3)
+    D = 128
+    x = rng.standard_normal((1, 4, D)).astype(np.float32)
+    g1 = np.ones(D, np.float32)
+    y0 = oracle.rms_norm_rope(x, g1, np.float32(1e-6), np.zeros(1, np.int32), 1e6).astype(np.float64)
+    y = oracle.rms_norm_rope(x, g1, np.float32(1e-6), np.array([3001], np.int32), 1e6).astype(np.float64)
+    n0 = y0[..., :D // 2] ** 2 + y0[..., D // 2:] ** 2
+    n1 = y[..., :D // 2] ** 2 + y[..., D // 2:] ** 2
+    np.testing.assert_allclose(n1, n0, rtol=1e-6, atol=1e-12)
+
+
+# ---------------------------------------------------------------------------
+# a3: set_rows and bf16 rounding
+# ---------------------------------------------------------------------------
+def test_bf16_rne_hand_derived_cases():
+    for f_bits, h_bits in read_golden("bf16_rne_cases.txt"):
+        assert oracle.bf16_rne(f32_from_bits(int(f_bits, 16))) == int(h_bits, 16), f_bits
+
+
+def test_bf16_rne_matches_torch_conversion():
+    """torch's f32 -> bf16 conversion is round-to-nearest-even; compare on random
+    values plus constructed ties (low half exactly 0x8000)."""
+    rng = np.random.default_rng(4)
+    x = rng.standard_normal(20000).astype(np.float32) * np.float32(10.0) ** rng.integers(-30, 30, 20000).astype(np.float32)
+    ties = (rng.integers(0, 2 ** 31, 5000).astype(np.uint32) & np.uint32(0xFFFF0000)) | np.uint32(0x8000)
+    x = np.concatenate([x, ties.view(np.float32)])
+    x = x[np.isfinite(x)]
+    got = oracle.bf16_rne_array(x)
+    ref = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(got, ref)
+
+
+@pytest.mark.parametrize("layout_name", ["contiguous", "paged"])
+@pytest.mark.parametrize("kv_dtype", ["f32", "bf16"])
+def test_set_rows_hand_derived_offsets(layout_name, kv_dtype):
+    """Rows land at the hand-derived flat offsets of the documented layouts; every
+    other element keeps its canary value."""
+    B, Hkv, D, cap = 2, 2, 2, 4
+    paged = layout_name == "paged"
+    bt = np.array([[3, 1], [0, 4]], np.int32)
+    lay = oracle.KvLayout(B, Hkv, D, cap, kv_dtype, paged=paged, page_size=2, n_pages=5,
+                          block_table=bt if paged else None)
+    n_el = (5 * Hkv * 2 * D) if paged else (B * Hkv * cap * D)
+    dt = np.float32 if kv_dtype == "f32" else np.uint16
+    canary = np.float32(-7.0) if kv_dtype == "f32" else np.uint16(0xDEAD)
+    kc = np.full(n_el, canary, dt)
+    vc = np.full(n_el, canary, dt)
+    k = np.array([[[1, 2], [3, 4]], [[5, 6], [7, 8]]], np.float32)
+    v = k + np.float32(10)
+    flag = oracle.kv_set_rows(k, v, kc, vc, lay, np.array([3, 0], np.int32))
+    assert flag == 0
+    touched = set()
+    for lay_name, b, pos, g, off in read_golden("paged_offsets.txt"):
+        if lay_name != layout_name:
+            continue
+        b, g, off = int(b), int(g), int(off)
+        for d in range(D):
+            want_k, want_v = k[b, g, d], v[b, g, d]
+            if kv_dtype == "bf16":
+                want_k = oracle.bf16_rne(want_k)
+                want_v = oracle.bf16_rne(want_v)
+            assert kc[off + d] == want_k and vc[off + d] == want_v
+            touched.add(off + d)
+    rest = np.array([i for i in range(n_el) if i not in touched])
+    assert np.all(kc[rest] == canary) and np.all(vc[rest] == canary)
+
+
+def test_set_rows_skips_out_of_range_positions():
+    lay = oracle.KvLayout(2, 1, 4, 8, "f32")
+    kc = np.zeros(2 * 8 * 4, np.float32)
+    vc = np.zeros_like(kc)
+    k = np.ones((2, 1, 4), np.float32)
+    flag = oracle.kv_set_rows(k, k, kc, vc, lay, np.array([8, -1], np.int32))
+    assert flag == 1 and np.all(kc == 0)
+
+
+# ---------------------------------------------------------------------------
+# a4: decode attention
+# ---------------------------------------------------------------------------
+def _rand_case(rng, B, Hq, Hkv, D, cap, kv_dtype="f32"):
+    q = rng.standard_normal((B, Hq, D)).astype(np.float32)
+    kc = rng.standard_normal((B, Hkv, cap, D)).astype(np.float32)
+    vc = rng.standard_normal((B, Hkv, cap, D)).astype(np.float32)
+    if kv_dtype == "bf16":
+        kc = torch.from_numpy(kc).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+        vc = torch.from_numpy(vc).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    return q, kc, vc
+
+
+def _as_f64(c, kv_dtype):
+    return c.astype(np.float64) if kv_dtype == "f32" else oracle.bf16_bits_to_f32(c).astype(np.float64)
+
+
+@pytest.mark.parametrize("kv_dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("Hq,Hkv", [(16, 8), (4, 1), (8, 8)])
+def test_attn_matches_torch_sdpa(kv_dtype, Hq, Hkv):
+    """torch scaled_dot_product_attention in float64 with enable_gqa (q head h reads kv
+    head h // (Hq/Hkv)) and its default 1/sqrt(D) scale, over the valid rows only."""
+    rng = np.random.default_rng(5)
+    B, D, cap = 3, 16, 40
+    q, kc, vc = _rand_case(rng, B, Hq, Hkv, D, cap, kv_dtype)
+    n_valid = np.array([1, 17, 40], np.int32)
+    lay = oracle.KvLayout(B, Hkv, D, cap, kv_dtype)
+    out, _, flag = oracle.decode_attn(q, kc, vc, lay, n_valid, 1.0 / math.sqrt(D))
+    assert flag == 0
+    K, V = _as_f64(kc, kv_dtype), _as_f64(vc, kv_dtype)
+    for b in range(B):
+        n = int(n_valid[b])
+        ref = F.scaled_dot_product_attention(
+            torch.from_numpy(q[b:b + 1].astype(np.float64))[:, :, None, :],
+            torch.from_numpy(K[b:b + 1, :, :n]), torch.from_numpy(V[b:b + 1, :, :n]),
+            enable_gqa=True)[0, :, 0, :].numpy()
+        np.testing.assert_allclose(out[b], ref, rtol=1e-6, atol=1e-7)
+
+
+def test_attn_weights_sum_to_one_and_tail_is_exactly_zero():
+    rng = np.random.default_rng(6)
+    B, Hq, Hkv, D, cap = 2, 4, 2, 8, 64
+    q, kc, vc = _rand_case(rng, B, Hq, Hkv, D, cap)
+    n_valid = np.array([5, 64], np.int32)
+    _, w, _ = oracle.decode_attn(q, kc, vc, oracle.KvLayout(B, Hkv, D, cap), n_valid, 0.3,
+                                 want_weights=True)
+    assert np.all(np.abs(w.sum(-1) - 1.0) < 1e-12)
+    assert np.all(w[0, :, 5:] == 0.0)
+    assert np.all(w[0, :, :5] > 0.0)
+
+
+def test_attn_ignores_poisoned_tail_and_window_padding():
+    """Whatever sits past n_valid (NaN, +-1e30) and however far the cache extends, the
+    result is bit-identical: the padded tail is never read."""
+    rng = np.random.default_rng(7)
+    B, Hq, Hkv, D = 1, 4, 2, 8
+    q, kc, vc = _rand_case(rng, B, Hq, Hkv, D, 256)
+    n_valid = np.array([38], np.int32)
+    base, _, _ = oracle.decode_attn(q, kc, vc, oracle.KvLayout(B, Hkv, D, 256), n_valid, 0.35)
+    for poison in [np.nan, 1e30, -1e30]:
+        kp, vp = kc.copy(), vc.copy()
+        kp[:, :, 38:] = poison
+        vp[:, :, 38:] = poison
+        out, _, _ = oracle.decode_attn(q, kp, vp, oracle.KvLayout(B, Hkv, D, 256), n_valid, 0.35)
+        assert np.array_equal(out, base)
+    for cap in [38, 64, 512]:
+        kp = np.full((B, Hkv, cap, D), np.nan, np.float32)
+        vp = kp.copy()
+        kp[:, :, :38] = kc[:, :, :38]
+        vp[:, :, :38] = vc[:, :, :38]
+        out, _, _ = oracle.decode_attn(q, kp, vp, oracle.KvLayout(B, Hkv, D, cap), n_valid, 0.35)
+        assert np.array_equal(out, base)
+
+
+def test_attn_closed_forms():
+    rng = np.random.default_rng(8)
+    B, Hq, Hkv, D, cap = 1, 2, 1, 8, 32
+    q = rng.standard_normal((B, Hq, D)).astype(np.float32)
+    V = rng.standard_normal((B, Hkv, cap, D)).astype(np.float32)
+    lay = oracle.KvLayout(B, Hkv, D, cap)
+    # All keys equal: uniform weights, output = mean of the valid V rows.
+    K = np.repeat(rng.standard_normal((B, Hkv, 1, D)).astype(np.float32), cap, axis=2)
+    out, _, _ = oracle.decode_attn(q, K, V, lay, np.array([20], np.int32), 0.5)
+    mean = V[0, 0, :20].astype(np.float64).mean(0)
+    np.testing.assert_allclose(out[0], np.broadcast_to(mean, (Hq, D)), rtol=1e-6, atol=1e-7)
+    # One key dominates by 60 in score: the output is its V row to ~exp(-60).
+    K2 = np.zeros((B, Hkv, cap, D), np.float32)
+    q2 = np.zeros((B, Hq, D), np.float32)
+    q2[..., 0] = 1.0
+    K2[0, 0, 3, 0] = 60.0
+    out, _, _ = oracle.decode_attn(q2, K2, V, lay, np.array([32], np.int32), 1.0)
+    np.testing.assert_allclose(out[0], np.broadcast_to(V[0, 0, 3], (Hq, D)), rtol=1e-6, atol=1e-7)
+    # A single valid row: the output is that V row exactly.
+    out, _, _ = oracle.decode_attn(q, K, V, lay, np.array([1], np.int32), 0.5)
+    assert np.array_equal(out[0], np.broadcast_to(V[0, 0, 0], (Hq, D)))
+
+
+def test_attn_scale_enters_as_multiplier_of_the_scores():
+    """Doubling the scale equals doubling q (the score is scale * q.K)."""
+    rng = np.random.default_rng(9)
+    q, kc, vc = _rand_case(rng, 1, 2, 1, 8, 16)
+    lay = oracle.KvLayout(1, 1, 8, 16)
+    a, _, _ = oracle.decode_attn(q, kc, vc, lay, np.array([16], np.int32), 0.4)
+    b, _, _ = oracle.decode_attn(q * np.float32(2), kc, vc, lay, np.array([16], np.int32), 0.2)
+    np.testing.assert_allclose(a, b, rtol=1e-12, atol=0)
+
+
+@pytest.mark.parametrize("kv_dtype", ["f32", "bf16"])
+def test_attn_paged_equals_contiguous(kv_dtype):
+    """Scatter each stream's logical rows into shuffled pages through set_rows; the
+    paged result must equal the contiguous one bit for bit."""
+    rng = np.random.default_rng(11)
+    B, Hq, Hkv, D, ps, pages_per = 2, 4, 2, 8, 16, 4
+    cap = ps * pages_per
+    n_pages = 11
+    bt = np.array([[7, 2, 9, 0], [3, 10, 5, 1]], np.int32)
+    q = rng.standard_normal((B, Hq, D)).astype(np.float32)
+    kl = rng.standard_normal((B, cap, Hkv, D)).astype(np.float32)
+    vl = rng.standard_normal((B, cap, Hkv, D)).astype(np.float32)
+    dt = np.float32 if kv_dtype == "f32" else np.uint16
+    cont = oracle.KvLayout(B, Hkv, D, cap, kv_dtype)
+    pag = oracle.KvLayout(B, Hkv, D, cap, kv_dtype, paged=True, page_size=ps, n_pages=n_pages,
+                          block_table=bt)
+    kc = np.zeros(B * Hkv * cap * D, dt)
+    vc = np.zeros_like(kc)
+    kp = np.zeros(n_pages * Hkv * ps * D, dt)
+    vp = np.zeros_like(kp)
+    n_valid = np.array([37, 64], np.int32)
+    for j in range(cap):
+        pos = np.full(B, j, np.int32)
+        oracle.kv_set_rows(kl[:, j], vl[:, j], kc, vc, cont, pos)
+        oracle.kv_set_rows(kl[:, j], vl[:, j], kp, vp, pag, pos)
+    a, _, _ = oracle.decode_attn(q, kc, vc, cont, n_valid, 0.3)
+    b, _, _ = oracle.decode_attn(q, kp, vp, pag, n_valid, 0.3)
+    assert np.array_equal(a, b)
+
+
+def test_attn_clamps_invalid_n_valid():
+    rng = np.random.default_rng(12)
+    q, kc, vc = _rand_case(rng, 2, 2, 1, 8, 16)
+    lay = oracle.KvLayout(2, 1, 8, 16)
+    out, _, flag = oracle.decode_attn(q, kc, vc, lay, np.array([0, 99], np.int32), 0.3)
+    ref, _, flag2 = oracle.decode_attn(q, kc, vc, lay, np.array([1, 16], np.int32), 0.3)
+    assert flag == 1 and flag2 == 0 and np.array_equal(out, ref)
+
+
+# ---------------------------------------------------------------------------
+# Compositions
+# ---------------------------------------------------------------------------
+def test_decode_step_batched_equals_per_stream():
+    rng = np.random.default_rng(13)
+    B, Hq, Hkv, D, cap = 3, 4, 2, 16, 32
+    q = rng.standard_normal((B, Hq, D)).astype(np.float32)
+    k = rng.standard_normal((B, Hkv, D)).astype(np.float32)
+    v = rng.standard_normal((B, Hkv, D)).astype(np.float32)
+    gq = rng.uniform(0.5, 1.5, D).astype(np.float32)
+    gk = rng.uniform(0.5, 1.5, D).astype(np.float32)
+    kc0 = rng.standard_normal((B, Hkv, cap, D)).astype(np.float32)
+    vc0 = rng.standard_normal((B, Hkv, cap, D)).astype(np.float32)
+    cur = np.array([0, 13, 31], np.int32)
+    kc, vc = kc0.copy(), vc0.copy()
+    out = oracle.decode_step(q, k, v, gq, gk, np.float32(1e-6), 1e6, kc, vc,
+                             oracle.KvLayout(B, Hkv, D, cap), cur, 0.25)
+    for b in range(B):
+        kb, vb = kc0[b:b + 1].copy(), vc0[b:b + 1].copy()
+        ob = oracle.decode_step(q[b:b + 1], k[b:b + 1], v[b:b + 1], gq, gk, np.float32(1e-6),
+                                1e6, kb, vb, oracle.KvLayout(1, Hkv, D, cap), cur[b:b + 1], 0.25)
+        assert np.array_equal(ob[0], out[b])
+        assert np.array_equal(kb[0], kc[b]) and np.array_equal(vb[0], vc[b])
+
+
+def test_decode_step_at_position_zero_attends_to_its_own_value_row():
+    """cur_len = 0: the window is the single new row, so the output is v itself."""
+    rng = np.random.default_rng(14)
+    Hq, Hkv, D = 4, 2, 16
+    q = rng.standard_normal((1, Hq, D)).astype(np.float32)
+    k = rng.standard_normal((1, Hkv, D)).astype(np.float32)
+    v = rng.standard_normal((1, Hkv, D)).astype(np.float32)
+    kc = np.full((1, Hkv, 16, D), np.nan, np.float32)
+    vc = kc.copy()
+    out = oracle.decode_step(q, k, v, np.ones(D, np.float32), np.ones(D, np.float32),
+                             np.float32(1e-6), 1e6, kc, vc, oracle.KvLayout(1, Hkv, D, 16),
+                             np.array([0], np.int32), 0.25)
+    assert np.array_equal(out[0], np.repeat(v[0], Hq // Hkv, axis=0))
+
+
+def test_predictor_frame_reset_masks_the_previous_frame():
+    """Two predictor frames through the same cache: the second frame's outputs equal
+    those of the same frame on a fresh (NaN-filled) cache, so stale rows from the
+    previous frame never leak (the cache reset is cur_len = 0, not a clear)."""
+    rng = np.random.default_rng(15)
+    B, L, Hq, Hkv, D, cap, hidden, vocab = 2, 2, 4, 2, 8, 16, 8, 32
+    lay = oracle.KvLayout(B, Hkv, D, cap)
+    tabs = [rng.standard_normal((vocab, hidden)).astype(np.float32) for _ in range(15)]
+    gam = [(np.ones(D, np.float32), np.ones(D, np.float32)) for _ in range(L)]
+
+    def frame_inputs():
+        codes = rng.integers(0, vocab, (B, 15)).astype(np.int32)
+        qkv = [[tuple(rng.standard_normal(s).astype(np.float32)
+                      for s in [(B, Hq, D), (B, Hkv, D), (B, Hkv, D)]) for _ in range(L)]
+               for _ in range(16)]
+        return codes, qkv
+
+    used = [tuple(rng.standard_normal((B, Hkv, cap, D)).astype(np.float32) for _ in range(2))
+            for _ in range(L)]
+    c1, qkv1 = frame_inputs()
+    oracle.predictor_frame(tabs, c1, None, qkv1, gam, np.float32(1e-6), 1e6, used, lay, 0.3)
+    c2, qkv2 = frame_inputs()
+    e2, o2 = oracle.predictor_frame(tabs, c2, None, qkv2, gam, np.float32(1e-6), 1e6, used, lay, 0.3)
+    fresh = [tuple(np.full((B, Hkv, cap, D), np.nan, np.float32) for _ in range(2)) for _ in range(L)]
+    e3, o3 = oracle.predictor_frame(tabs, c2, None, qkv2, gam, np.float32(1e-6), 1e6, fresh, lay, 0.3)
+    for t in range(16):
+        for l in range(L):
+            assert np.array_equal(o2[t][l], o3[t][l])
+    for j in range(15):
+        assert np.array_equal(e2[j], tabs[j][c2[:, j]])
