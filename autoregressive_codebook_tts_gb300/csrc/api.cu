@@ -1,0 +1,338 @@
+// C ABI of the decode hot path: argument validation on the host, then kernel launches
+// on the caller's stream.  Declarations and the full contract are in
+// include/tts_decode.h.
+#include <cmath>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "kernels.h"
+
+using namespace tts;
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
+int log2i(int x) {
+  int s = 0;
+  while ((1 << s) < x) ++s;
+  return s;
+}
+cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
+tts_status from_cuda(cudaError_t e) { return e == cudaSuccess ? TTS_OK : TTS_ERR_CUDA; }
+
+bool head_dim_ok(int d) { return d == 64 || d == 128; }
+bool group_ok(int hq, int hkv) {
+  if (hq <= 0 || hkv <= 0 || hq % hkv != 0) return false;
+  const int g = hq / hkv;
+  return g == 1 || g == 2 || g == 4;
+}
+
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 152;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+    cudaGetLastError();  // clear the sticky-free error this query may leave
+    return 152;
+  }
+  return n;
+}
+
+tts_status check_desc(const tts_kv_desc* d) {
+  if (d == nullptr) return TTS_ERR_NULL;
+  if (d->B < 1 || d->capacity < 1 || !head_dim_ok(d->head_dim) || !group_ok(d->n_q_heads, d->n_kv_heads))
+    return TTS_ERR_SHAPE;
+  if (d->window_quantum < 1 || d->capacity % d->window_quantum != 0) return TTS_ERR_SHAPE;
+  if (d->kv_dtype != TTS_F32 && d->kv_dtype != TTS_BF16) return TTS_ERR_DTYPE;
+  if (d->paged != 0 && d->paged != 1) return TTS_ERR_LAYOUT;
+  if (d->paged) {
+    if (d->block_table == nullptr) return TTS_ERR_NULL;
+    if (!is_pow2(d->page_size) || d->page_size > 256 || d->capacity % d->page_size != 0 ||
+        d->n_pages < 1 || d->bt_stride < d->capacity / d->page_size)
+      return TTS_ERR_LAYOUT;
+  }
+  return TTS_OK;
+}
+
+// Positions per split: a multiple of the tile, covering capacity in n_splits pieces.
+int split_len_for(const tts_kv_desc* d, int n_splits, int tile) {
+  int per = (d->capacity + n_splits - 1) / n_splits;
+  per = ((per + tile - 1) / tile) * tile;
+  return per;
+}
+
+struct WsLayout {
+  size_t o_off, ml_off, cnt_off, total;
+};
+
+size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+WsLayout ws_layout(const tts_kv_desc* d, int n_splits) {
+  WsLayout w;
+  const size_t slots = static_cast<size_t>(d->B) * d->n_q_heads * n_splits;
+  w.o_off = 0;
+  w.ml_off = round256(slots * d->head_dim * sizeof(float));
+  w.cnt_off = w.ml_off + round256(slots * 2 * sizeof(float));
+  w.total = w.cnt_off + round256(static_cast<size_t>(d->B) * d->n_kv_heads * sizeof(int));
+  return w;
+}
+
+// Shared preparation of the attention launch (standalone and fused).
+tts_status prepare_attn(const tts_kv_desc* d, const void* k_cache, const void* v_cache,
+                        void* workspace, size_t ws_bytes, int32_t n_splits_req, AttnParams& p,
+                        int& n_splits_out) {
+  tts_status st = check_desc(d);
+  if (st != TTS_OK) return st;
+  if (k_cache == nullptr || v_cache == nullptr) return TTS_ERR_NULL;
+  if (!aligned16(k_cache) || !aligned16(v_cache)) return TTS_ERR_ALIGN;
+  const int bf16 = d->kv_dtype == TTS_BF16;
+  const AttnGeometry geo = attn_geometry(bf16, d->head_dim);
+  int n_splits = n_splits_req == 0 ? tts_decode_attn_default_splits(d) : n_splits_req;
+  if (n_splits < 1) return TTS_ERR_SHAPE;
+  const int max_splits = (d->capacity + geo.tile_rows - 1) / geo.tile_rows;
+  if (n_splits > max_splits) n_splits = max_splits;
+  const int split_len = split_len_for(d, n_splits, geo.tile_rows);
+  const int used = (d->capacity + split_len - 1) / split_len;  // splits actually launched
+  if (used > 65535 || d->n_kv_heads > 65535 || d->B > 65535) return TTS_ERR_SHAPE;
+  if (used > 1) {
+    const WsLayout w = ws_layout(d, used);
+    if (workspace == nullptr) return TTS_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return TTS_ERR_ALIGN;
+    if (ws_bytes < w.total) return TTS_ERR_WORKSPACE;
+    unsigned char* ws = static_cast<unsigned char*>(workspace);
+    p.ws_o = reinterpret_cast<float*>(ws + w.o_off);
+    p.ws_ml = reinterpret_cast<float*>(ws + w.ml_off);
+    p.ws_cnt = reinterpret_cast<int*>(ws + w.cnt_off);
+  } else {
+    p.ws_o = nullptr;
+    p.ws_ml = nullptr;
+    p.ws_cnt = nullptr;
+  }
+  const int tiles_per_split = split_len / geo.tile_rows;
+  p.n_stages = tiles_per_split < geo.max_stages ? tiles_per_split : geo.max_stages;
+  if (p.n_stages < 1) p.n_stages = 1;
+  p.k_cache = k_cache;
+  p.v_cache = v_cache;
+  p.B = d->B;
+  p.n_q_heads = d->n_q_heads;
+  p.n_kv_heads = d->n_kv_heads;
+  p.capacity = d->capacity;
+  p.paged = d->paged;
+  p.page_size = d->paged ? d->page_size : 1;
+  p.page_shift = d->paged ? log2i(d->page_size) : 0;
+  p.n_pages = d->paged ? d->n_pages : 0;
+  p.bt_stride = d->paged ? d->bt_stride : 0;
+  p.block_table = d->paged ? d->block_table : nullptr;
+  p.flags = d->flags;
+  p.n_splits = used;
+  p.split_len = split_len;
+  n_splits_out = used;
+  return TTS_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t tts_abi_version(void) { return TTS_ABI_VERSION; }
+int32_t tts_abi_min_version(void) { return TTS_ABI_MIN_VERSION; }
+
+const char* tts_status_str(int32_t s) {
+  switch (s) {
+    case TTS_OK: return "TTS_OK";
+    case TTS_ERR_NULL: return "TTS_ERR_NULL";
+    case TTS_ERR_SHAPE: return "TTS_ERR_SHAPE";
+    case TTS_ERR_DTYPE: return "TTS_ERR_DTYPE";
+    case TTS_ERR_LAYOUT: return "TTS_ERR_LAYOUT";
+    case TTS_ERR_ALIGN: return "TTS_ERR_ALIGN";
+    case TTS_ERR_WORKSPACE: return "TTS_ERR_WORKSPACE";
+    case TTS_ERR_CUDA: return "TTS_ERR_CUDA";
+    case TTS_ERR_ABI: return "TTS_ERR_ABI";
+    default: return "TTS_ERR_UNKNOWN";
+  }
+}
+
+tts_status tts_frame_embed(const tts_tables* t, const int32_t* ids, int64_t ids_stride,
+                           const float* overlay, int64_t overlay_stride, float* out, int32_t B,
+                           int32_t* err_flag, void* stream) {
+  if (t == nullptr || ids == nullptr || out == nullptr) return TTS_ERR_NULL;
+  if (t->n_tables < 1 || t->n_tables > TTS_MAX_TABLES || t->vocab < 1 || t->hidden < 4 ||
+      t->hidden % 4 != 0 || B < 1 || B > 65535 || ids_stride < t->n_tables)
+    return TTS_ERR_SHAPE;
+  EmbedParams p = {};
+  for (int i = 0; i < t->n_tables; ++i) {
+    if (t->tab[i] == nullptr) return TTS_ERR_NULL;
+    if (!aligned16(t->tab[i])) return TTS_ERR_ALIGN;
+    p.tab[i] = t->tab[i];
+  }
+  if (!aligned16(out)) return TTS_ERR_ALIGN;
+  if (overlay != nullptr && (!aligned16(overlay) || overlay_stride < t->hidden || overlay_stride % 4 != 0))
+    return overlay_stride < t->hidden ? TTS_ERR_SHAPE : TTS_ERR_ALIGN;
+  p.n_tables = t->n_tables;
+  p.vocab = t->vocab;
+  p.hidden = t->hidden;
+  p.ids = ids;
+  p.ids_stride = ids_stride;
+  p.overlay = overlay;
+  p.overlay_stride = overlay_stride;
+  p.out = out;
+  p.B = B;
+  p.err = err_flag;
+  return from_cuda(launch_frame_embed(p, as_stream(stream)));
+}
+
+tts_status tts_rope_table(float* cs, int32_t max_pos, int32_t head_dim, double base, void* stream) {
+  if (cs == nullptr) return TTS_ERR_NULL;
+  if (max_pos < 1 || !head_dim_ok(head_dim) || !(base > 1.0) || !std::isfinite(base)) return TTS_ERR_SHAPE;
+  if (!aligned16(cs)) return TTS_ERR_ALIGN;
+  return from_cuda(launch_rope_table(cs, max_pos, head_dim, base, as_stream(stream)));
+}
+
+tts_status tts_qk_norm_rope(float* q, int64_t q_row_stride, float* k, int64_t k_row_stride,
+                            const float* gamma_q, const float* gamma_k, const int32_t* pos,
+                            int32_t B, int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim,
+                            float eps, const float* rope_cs, int32_t rope_max_pos,
+                            int32_t* err_flag, void* stream) {
+  if (q == nullptr || k == nullptr || gamma_q == nullptr || gamma_k == nullptr || pos == nullptr ||
+      rope_cs == nullptr)
+    return TTS_ERR_NULL;
+  if (B < 1 || B > 65535 || !head_dim_ok(head_dim) || n_q_heads < 1 || n_kv_heads < 1 ||
+      rope_max_pos < 1 || !(eps >= 0.f) || q_row_stride < static_cast<int64_t>(n_q_heads) * head_dim ||
+      k_row_stride < static_cast<int64_t>(n_kv_heads) * head_dim)
+    return TTS_ERR_SHAPE;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(gamma_q) || !aligned16(gamma_k) ||
+      !aligned16(rope_cs) || q_row_stride % 4 != 0 || k_row_stride % 4 != 0)
+    return TTS_ERR_ALIGN;
+  NormRopeParams p = {q, q_row_stride, k, k_row_stride, gamma_q, gamma_k, pos, B, n_q_heads,
+                      n_kv_heads, head_dim, eps, reinterpret_cast<const float2*>(rope_cs),
+                      rope_max_pos, err_flag};
+  return from_cuda(launch_qk_norm_rope(p, as_stream(stream)));
+}
+
+tts_status tts_kv_set_rows(const float* k, const float* v, int64_t kv_row_stride, void* k_cache,
+                           void* v_cache, const tts_kv_desc* d, const int32_t* dst_pos,
+                           int32_t* err_flag, void* stream) {
+  tts_status st = check_desc(d);
+  if (st != TTS_OK) return st;
+  if (k == nullptr || v == nullptr || k_cache == nullptr || v_cache == nullptr || dst_pos == nullptr)
+    return TTS_ERR_NULL;
+  if (kv_row_stride < static_cast<int64_t>(d->n_kv_heads) * d->head_dim) return TTS_ERR_SHAPE;
+  if (!aligned16(k) || !aligned16(v) || !aligned16(k_cache) || !aligned16(v_cache) || kv_row_stride % 4 != 0)
+    return TTS_ERR_ALIGN;
+  SetRowsParams p = {};
+  p.k = k;
+  p.v = v;
+  p.row_stride = kv_row_stride;
+  p.k_cache = k_cache;
+  p.v_cache = v_cache;
+  p.B = d->B;
+  p.n_kv_heads = d->n_kv_heads;
+  p.head_dim = d->head_dim;
+  p.capacity = d->capacity;
+  p.kv_bf16 = d->kv_dtype == TTS_BF16;
+  p.paged = d->paged;
+  p.page_size = d->paged ? d->page_size : 1;
+  p.n_pages = d->n_pages;
+  p.bt_stride = d->bt_stride;
+  p.block_table = d->block_table;
+  p.pos = dst_pos;
+  p.err = err_flag;
+  return from_cuda(launch_set_rows(p, as_stream(stream)));
+}
+
+int32_t tts_decode_attn_default_splits(const tts_kv_desc* d) {
+  if (check_desc(d) != TTS_OK) return 1;
+  const AttnGeometry geo = attn_geometry(d->kv_dtype == TTS_BF16, d->head_dim);
+  const int max_splits = (d->capacity + geo.tile_rows - 1) / geo.tile_rows;
+  const int pairs = d->B * d->n_kv_heads;
+  // Aim for about two resident CTAs per SM over the whole grid, and cut long windows
+  // into pieces of at most 512 positions so ragged streams still balance.
+  int s = (2 * sm_count() + pairs - 1) / pairs;
+  const int by_len = (d->capacity + 511) / 512;
+  if (s < by_len) s = by_len;
+  if (s > max_splits) s = max_splits;
+  if (s < 1) s = 1;
+  return s;
+}
+
+size_t tts_decode_attn_workspace_size(const tts_kv_desc* d, int32_t n_splits) {
+  if (check_desc(d) != TTS_OK) return 0;
+  if (n_splits == 0) n_splits = tts_decode_attn_default_splits(d);
+  if (n_splits < 1) return 0;
+  const AttnGeometry geo = attn_geometry(d->kv_dtype == TTS_BF16, d->head_dim);
+  const int max_splits = (d->capacity + geo.tile_rows - 1) / geo.tile_rows;
+  if (n_splits > max_splits) n_splits = max_splits;
+  const int split_len = split_len_for(d, n_splits, geo.tile_rows);
+  const int used = (d->capacity + split_len - 1) / split_len;
+  return ws_layout(d, used).total;
+}
+
+tts_status tts_workspace_init(void* workspace, size_t ws_bytes, void* stream) {
+  if (workspace == nullptr) return TTS_ERR_NULL;
+  if (!aligned16(workspace)) return TTS_ERR_ALIGN;
+  return from_cuda(launch_zero(workspace, ws_bytes & ~static_cast<size_t>(15), as_stream(stream)));
+}
+
+tts_status tts_decode_attn(const float* q, int64_t q_row_stride, const void* k_cache,
+                           const void* v_cache, const tts_kv_desc* d, const int32_t* n_valid,
+                           float scale, float* out, void* workspace, size_t ws_bytes,
+                           int32_t n_splits, int32_t* err_flag, void* stream) {
+  if (q == nullptr || n_valid == nullptr || out == nullptr) return TTS_ERR_NULL;
+  AttnParams p = {};
+  int used = 0;
+  tts_status st = prepare_attn(d, k_cache, v_cache, workspace, ws_bytes, n_splits, p, used);
+  if (st != TTS_OK) return st;
+  if (q_row_stride < static_cast<int64_t>(d->n_q_heads) * d->head_dim) return TTS_ERR_SHAPE;
+  if (!aligned16(q) || !aligned16(out) || q_row_stride % 4 != 0) return TTS_ERR_ALIGN;
+  if (!std::isfinite(scale)) return TTS_ERR_SHAPE;
+  p.q = q;
+  p.q_stride = q_row_stride;
+  p.lens = n_valid;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.out = out;
+  p.err = err_flag;
+  p.flags &= ~TTS_KV_PREFETCH_BEFORE_WAIT;  // only meaningful for the fused step
+  return from_cuda(launch_decode_attn(p, d->kv_dtype == TTS_BF16, d->head_dim,
+                                      d->n_q_heads / d->n_kv_heads, false, as_stream(stream)));
+}
+
+tts_status tts_decode_step(const float* q, const float* k, const float* v, int64_t row_stride,
+                           const float* gamma_q, const float* gamma_k, float eps,
+                           const float* rope_cs, int32_t rope_max_pos, void* k_cache,
+                           void* v_cache, const tts_kv_desc* d, const int32_t* cur_len,
+                           float scale, float* out, void* workspace, size_t ws_bytes,
+                           int32_t n_splits, int32_t* err_flag, void* stream) {
+  if (q == nullptr || k == nullptr || v == nullptr || gamma_q == nullptr || gamma_k == nullptr ||
+      rope_cs == nullptr || cur_len == nullptr || out == nullptr)
+    return TTS_ERR_NULL;
+  AttnParams p = {};
+  int used = 0;
+  tts_status st = prepare_attn(d, k_cache, v_cache, workspace, ws_bytes, n_splits, p, used);
+  if (st != TTS_OK) return st;
+  if (row_stride < static_cast<int64_t>(d->n_q_heads) * d->head_dim || rope_max_pos < 1 || !(eps >= 0.f))
+    return TTS_ERR_SHAPE;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(gamma_q) ||
+      !aligned16(gamma_k) || !aligned16(rope_cs) || row_stride % 4 != 0)
+    return TTS_ERR_ALIGN;
+  if (!std::isfinite(scale)) return TTS_ERR_SHAPE;
+  p.q = q;
+  p.q_stride = row_stride;
+  p.k_new = k;
+  p.v_new = v;
+  p.kv_new_stride = row_stride;
+  p.gamma_q = gamma_q;
+  p.gamma_k = gamma_k;
+  p.eps = eps;
+  p.cs = reinterpret_cast<const float2*>(rope_cs);
+  p.max_pos = rope_max_pos;
+  p.k_cache_w = k_cache;
+  p.v_cache_w = v_cache;
+  p.lens = cur_len;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.out = out;
+  p.err = err_flag;
+  return from_cuda(launch_decode_attn(p, d->kv_dtype == TTS_BF16, d->head_dim,
+                                      d->n_q_heads / d->n_kv_heads, true, as_stream(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,181 @@
+// Device helpers shared by the decode-path kernels (sm_103a): error flag, bounded
+// mbarrier waits, 1-D bulk (TMA) copies global -> shared, programmatic dependent
+// launch controls, 16-byte vector loads and bf16 unpacking.
+#pragma once
+
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "../../include/tts_decode.h"
+
+namespace tts {
+
+constexpr unsigned kFull = 0xffffffffu;
+
+// Upper bound on any in-kernel wait, in SM clock cycles (about a second at the
+// GB300's clocks).  A wait that runs out sets TTS_EFLAG_TIMEOUT and the kernel winds
+// down instead of hanging.
+constexpr long long kWaitLimitCycles = 2000000000LL;
+
+__device__ __forceinline__ void set_err(int32_t* flag, int bits) {
+  if (flag != nullptr) atomicOr(flag, bits);
+}
+
+// ---------------------------------------------------------------------------
+// Programmatic dependent launch.  `grid_wait` blocks until the preceding kernel on
+// the stream has completed and its writes are visible (a no-op when the kernel was
+// launched without the programmatic-serialisation attribute); `grid_launch_dependents`
+// lets the next kernel be scheduled early.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void grid_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
+// Shared-memory mbarriers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+// Makes barrier initialisation visible to the async (bulk-copy) proxy.
+__device__ __forceinline__ void mbar_init_fence() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  uint64_t state;
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 %0, [%1], %2;"
+               : "=l"(state) : "r"(smem_u32(bar)), "r"(bytes) : "memory");
+  (void)state;
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  uint64_t state;
+  asm volatile("mbarrier.arrive.shared::cta.b64 %0, [%1];" : "=l"(state) : "r"(smem_u32(bar)) : "memory");
+  (void)state;
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
+  return ok != 0;
+}
+
+// Waits until the phase with the given parity has completed.  Bounded: returns false
+// after kWaitLimitCycles.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long start = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (clock64() - start > kWaitLimitCycles) return false;
+  }
+  return true;
+}
+
+// ---------------------------------------------------------------------------
+// 1-D bulk copy global -> shared (TMA engine), completion counted in bytes on an
+// mbarrier.  Addresses 16-byte aligned, size a multiple of 16.  The L2 policy marks
+// the streamed KV lines evict-first: each is read once per step.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+__device__ __forceinline__ void bulk_g2s(void* smem_dst, const void* gmem_src, uint32_t bytes,
+                                         uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1], %2, [%3], %4;"
+      ::"r"(smem_u32(smem_dst)), "l"(gmem_src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
+// Named barrier over a subset of the CTA's warps (id 0 is __syncthreads).
+__device__ __forceinline__ void named_barrier(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// Vector loads and bf16 unpacking
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint4 lds128(const void* p) {
+  return *reinterpret_cast<const uint4*>(p);
+}
+
+// Eight bf16 packed in a uint4 (element 0 in the low half of .x) -> eight floats.
+// Widening bf16 -> f32 is exact: the bf16 bits become the high half of the f32.
+__device__ __forceinline__ void unpack_bf16x8(const uint4 v, float (&f)[8]) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+  }
+}
+
+__device__ __forceinline__ void unpack_f32x4(const uint4 v, float (&f)[4]) {
+  f[0] = __uint_as_float(v.x);
+  f[1] = __uint_as_float(v.y);
+  f[2] = __uint_as_float(v.z);
+  f[3] = __uint_as_float(v.w);
+}
+
+template <typename KvT> struct KvVec;
+template <> struct KvVec<float> {
+  static constexpr int kElems = 4;
+  static __device__ __forceinline__ void unpack(const uint4 v, float (&f)[4]) { unpack_f32x4(v, f); }
+};
+template <> struct KvVec<__nv_bfloat16> {
+  static constexpr int kElems = 8;
+  static __device__ __forceinline__ void unpack(const uint4 v, float (&f)[8]) { unpack_bf16x8(v, f); }
+};
+
+// f32 -> cache element, round-to-nearest-even for bf16.
+__device__ __forceinline__ float to_cache(float x, float*) { return x; }
+__device__ __forceinline__ __nv_bfloat16 to_cache(float x, __nv_bfloat16*) { return __float2bfloat16_rn(x); }
+
+// ---------------------------------------------------------------------------
+// Per-head RMSNorm + rotate-half RoPE on a row held by a group of LPR lanes, each
+// with EPL consecutive elements starting at e0 = (lane % LPR) * EPL.  The partner of
+// element i (i +- D/2) lives in lane ^ (LPR/2).  All lanes of the warp must call it.
+//   t = x * (mean(x^2) + eps)^(-1/2) * gamma;  rotate (t_i, t_{i+D/2}) by theta_i.
+// ---------------------------------------------------------------------------
+template <int EPL, int LPR>
+__device__ __forceinline__ void norm_rope_lanes(float (&x)[EPL], const float* __restrict__ gamma,
+                                                const float2* __restrict__ cs_row, float eps,
+                                                int e0, int D) {
+  float ss = 0.f;
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) ss = fmaf(x[i], x[i], ss);
+#pragma unroll
+  for (int o = LPR / 2; o >= 1; o >>= 1) ss += __shfl_xor_sync(kFull, ss, o);
+  const float r = 1.0f / sqrtf(ss / static_cast<float>(D) + eps);
+  float t[EPL];
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) t[i] = x[i] * r * __ldg(gamma + e0 + i);
+  const int half = D / 2;
+  const bool lo = e0 < half;
+  const int f0 = lo ? e0 : e0 - half;
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) {
+    const float pt = __shfl_xor_sync(kFull, t[i], LPR / 2);
+    const float2 cs = __ldg(cs_row + f0 + i);
+    // lower half: t*c - partner*s ; upper half: partner*s + t*c
+    x[i] = lo ? fmaf(t[i], cs.x, -pt * cs.y) : fmaf(pt, cs.y, t[i] * cs.x);
+  }
+}
+
+}  // namespace tts

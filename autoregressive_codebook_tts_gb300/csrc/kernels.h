@@ -1,0 +1,104 @@
+// Internal launch interface between the C-ABI layer (api.cu) and the kernels.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/tts_decode.h"
+
+namespace tts {
+
+struct EmbedParams {
+  const float* tab[TTS_MAX_TABLES];
+  int n_tables, vocab, hidden;
+  const int32_t* ids;
+  int64_t ids_stride;
+  const float* overlay;
+  int64_t overlay_stride;
+  float* out;
+  int B;
+  int32_t* err;
+};
+
+struct NormRopeParams {
+  float* q;
+  int64_t q_stride;
+  float* k;
+  int64_t k_stride;
+  const float* gamma_q;
+  const float* gamma_k;
+  const int32_t* pos;
+  int B, n_q_heads, n_kv_heads, head_dim;
+  float eps;
+  const float2* cs;
+  int max_pos;
+  int32_t* err;
+};
+
+struct SetRowsParams {
+  const float* k;
+  const float* v;
+  int64_t row_stride;
+  void* k_cache;
+  void* v_cache;
+  int B, n_kv_heads, head_dim, capacity, kv_bf16;
+  int paged, page_size, n_pages, bt_stride;
+  const int32_t* block_table;
+  const int32_t* pos;
+  int32_t* err;
+};
+
+// Decode attention, standalone (q already normed) or fused with norm+RoPE and the
+// new-row write.
+struct AttnParams {
+  const float* q;       // standalone: normed q; fused: raw projection q
+  int64_t q_stride;
+  const float* k_new;   // fused only
+  const float* v_new;   // fused only
+  int64_t kv_new_stride;
+  const float* gamma_q;
+  const float* gamma_k;
+  float eps;
+  const float2* cs;
+  int max_pos;
+  const void* k_cache;
+  const void* v_cache;
+  void* k_cache_w;      // fused: where the new row goes
+  void* v_cache_w;
+  int B, n_q_heads, n_kv_heads, capacity;
+  int paged, page_size, page_shift, n_pages, bt_stride;
+  const int32_t* block_table;
+  const int32_t* lens;  // standalone: n_valid; fused: cur_len
+  float scale_log2;     // softmax scale * log2(e)
+  float* out;
+  float* ws_o;          // [B][Hq][n_splits][D]
+  float* ws_ml;         // [B][Hq][n_splits][2]
+  int* ws_cnt;          // [B][Hkv]
+  int n_splits;         // grid.x
+  int split_len;        // positions per split, a multiple of the tile
+  int n_stages;         // pipeline depth actually used (<= the kernel's maximum)
+  uint32_t flags;
+  int32_t* err;
+};
+
+// Launch helpers (return a cudaError_t from the launch).
+cudaError_t launch_frame_embed(const EmbedParams& p, cudaStream_t s);
+cudaError_t launch_rope_table(float* cs, int max_pos, int head_dim, double base, cudaStream_t s);
+cudaError_t launch_qk_norm_rope(const NormRopeParams& p, cudaStream_t s);
+cudaError_t launch_set_rows(const SetRowsParams& p, cudaStream_t s);
+cudaError_t launch_zero(void* ptr, size_t bytes, cudaStream_t s);
+
+// Tile geometry of the attention kernel for a (dtype, head_dim) pair.
+struct AttnGeometry {
+  int tile_rows;     // positions per pipeline stage
+  int max_stages;    // ring depth the kernel is compiled for
+  int stage_bytes;   // K tile + V tile
+  int threads;       // consumer warps + one producer warp
+};
+AttnGeometry attn_geometry(int kv_bf16, int head_dim);
+size_t attn_smem_bytes(int kv_bf16, int head_dim, int group, int n_stages);
+cudaError_t launch_decode_attn(const AttnParams& p, int kv_bf16, int head_dim, int group,
+                               bool fused, cudaStream_t s);
+
+}  // namespace tts

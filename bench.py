@@ -1,0 +1,540 @@
+"""Benchmark of the per-frame decode hot path on one GB300 (or N replicas).
+
+Workload (default): the talker single-stream configuration -- 1 stream, 28 layers,
+hidden 2048, 16 q / 8 kv heads, head_dim 128, f32 KV cache of 4096 positions per layer
+(896 MiB), 16 codebooks of 2048 x 2048 f32, cur_len 4095 (window 4096).  One step is
+one frame: the frame-input composition plus 28 fused decode steps (q/k norm + RoPE,
+set_rows of the new K/V row, split-KV decode attention), captured once in a CUDA graph
+from the public C-ABI calls and replayed.  The KV working set (896 MiB) is larger than
+L2, so no flush is needed between steps.
+
+Printed: one JSON line (rank 0).  ``value`` = algorithmic bytes per frame (KV window
+read + new-row write + activations + embedding rows) x frames / device time, in GB/s.
+``--impl reference`` times the CPU oracle on the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode-attn KV GB/s (% of HBM peak); frame steps/sec at B streams, 1 GB300"
+FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 7900.0
+ATTN_SRC = os.path.join(ROOT, "autoregressive_codebook_tts_gb300", "csrc", "attn.cu")
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "decode_step_talker_f32_cur4095.txt")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["native", "reference"], default="native")
+    ap.add_argument("--workload", default="talker", choices=["talker", "batched", "paged"])
+    ap.add_argument("--cur-len", type=int, default=4095)
+    ap.add_argument("--n-splits", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--sweep", action="store_true", help="also time cur_len 255/1023/2047")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# Algorithmic bytes
+# ---------------------------------------------------------------------------
+def step_bytes(w, cur_lens):
+    """Per-layer and per-frame algorithmic bytes (see the module docstring)."""
+    e = w.elem_bytes
+    Hq, Hkv, D = w.n_q_heads, w.n_kv_heads, w.head_dim
+    per_layer = 0
+    kv_layer = 0
+    for c in cur_lens:
+        kv = (c + 1) * Hkv * D * e * 2           # window rows read + new row written
+        act = (Hq + 2 * Hkv) * D * 4 + Hq * D * 4  # q, k, v in; out
+        const = 2 * D * 4 + (D // 2) * 8           # gammas, RoPE row
+        per_layer += kv + act + const
+        kv_layer += kv
+    embed = len(cur_lens) * (w.n_tables * w.hidden * 4 + 2 * w.hidden * 4 + w.n_tables * 4)
+    return per_layer, kv_layer, embed
+
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            with open(path) as f:
+                d = json.load(f)
+            for key in ("hbm_gbs", "hbm_GBps", "hbm"):
+                if key in d and isinstance(d[key], (int, float)):
+                    return float(d[key]), "measured"
+        except Exception:
+            pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def profiled_traffic():
+    """dram bytes per launch of the dominant kernel from the committed ncu summary,
+    or None when the summary is absent or was taken on a different attn.cu."""
+    if not os.path.exists(PROFILE_SUMMARY):
+        return None
+    src_hash = hashlib.sha256(open(ATTN_SRC, "rb").read()).hexdigest()[:16]
+    vals = {}
+    for line in open(PROFILE_SUMMARY):
+        if ":" in line:
+            k, v = line.split(":", 1)
+            vals[k.strip()] = v.strip()
+    if vals.get("attn_cu_sha256_16") != src_hash:
+        return None
+    try:
+        return float(vals["traffic_bytes_per_launch_full"])
+    except (KeyError, ValueError):
+        return None
+
+
+# ---------------------------------------------------------------------------
+# Clock sampling during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"tts_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        sms, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sms.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        os.unlink(self.path)
+        if not sms:
+            return None
+        return {"sm_mhz": statistics.median(sms), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sms)}
+
+
+# ---------------------------------------------------------------------------
+# Native arm
+# ---------------------------------------------------------------------------
+def build_frame(tts, W, w, cur_len, n_splits, dev, seed=0):
+    """Device-resident inputs of one frame and the closure that enqueues it."""
+    import torch
+    B, L = w.B, w.layers
+    g = torch.Generator(device=dev)
+    g.manual_seed(seed)
+    tabs = [torch.randn(w.vocab, w.hidden, generator=g, device=dev) * w.table_std for _ in range(w.n_tables)]
+    ids = torch.randint(0, w.vocab, (B, w.n_tables), generator=g, device=dev, dtype=torch.int32)
+    overlay = torch.randn(B, w.hidden, generator=g, device=dev) * w.table_std
+    width = (w.n_q_heads + 2 * w.n_kv_heads) * w.head_dim
+    qkv = torch.randn(L, B, width, generator=g, device=dev)
+    gq = torch.rand(L, w.head_dim, generator=g, device=dev) + 0.5
+    gk = torch.rand(L, w.head_dim, generator=g, device=dev) + 0.5
+    if isinstance(cur_len, int):
+        cur = torch.full((B,), cur_len, dtype=torch.int32, device=dev)
+    else:
+        cur = cur_len.to(dev)
+    kv_dt = torch.float32 if w.kv_dtype == "f32" else torch.bfloat16
+    if w.paged:
+        pages_per = w.capacity // w.page_size
+        bt = torch.randperm(w.n_pages, generator=g, device=dev)[:B * pages_per].reshape(B, pages_per).to(torch.int32).contiguous()
+        shape = (w.n_pages, w.n_kv_heads, w.page_size, w.head_dim)
+    else:
+        bt = None
+        shape = (B, w.n_kv_heads, w.capacity, w.head_dim)
+    caches = []
+    for _ in range(L):
+        K = torch.empty(shape, dtype=kv_dt, device=dev)
+        V = torch.empty(shape, dtype=kv_dt, device=dev)
+        K.normal_(generator=g)
+        V.normal_(generator=g)
+        caches.append((K, V))
+    cs = torch.empty(w.capacity, w.head_dim // 2, 2, device=dev)
+    tts.tts_rope_table(cs, w.capacity, w.head_dim, w.rope_base)
+    desc = tts.kv_desc(B, w.n_q_heads, w.n_kv_heads, w.head_dim, w.capacity, w.kv_dtype,
+                       window_quantum=w.window_quantum, paged=w.paged, page_size=w.page_size,
+                       n_pages=w.n_pages, block_table=bt, flags=tts.TTS_KV_PREFETCH_BEFORE_WAIT)
+    ws = tts.workspace(desc, n_splits, device=dev)
+    emb = torch.empty(B, w.hidden, device=dev)
+    outs = torch.empty(L, B, w.n_q_heads, w.head_dim, device=dev)
+    ef = torch.zeros(1, dtype=torch.int32, device=dev)
+    qd, kd = w.n_q_heads * w.head_dim, w.n_kv_heads * w.head_dim
+    scale = 1.0 / math.sqrt(w.head_dim)
+    tabs_struct = tts.tables(tabs)
+
+    def layers():
+        for l in range(L):
+            K, V = caches[l]
+            rows = qkv[l]
+            tts.tts_decode_step(rows[:, :qd], rows[:, qd:qd + kd], rows[:, qd + kd:], gq[l], gk[l],
+                                w.eps, cs, w.capacity, K, V, desc, cur, scale, outs[l], ws,
+                                n_splits, ef)
+
+    def frame():
+        tts.tts_frame_embed(tabs_struct, ids, overlay, emb, ef)
+        layers()
+
+    state = dict(tabs=tabs, ids=ids, overlay=overlay, qkv=qkv, cur=cur, caches=caches, emb=emb,
+                 outs=outs, ef=ef, cs=cs, ws=ws, bt=bt, gq=gq, gk=gk, desc=desc)
+    return frame, layers, state
+
+
+def capture(fn, torch):
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        fn()  # warm (sets kernel attributes outside capture)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        fn()
+    torch.cuda.synchronize()
+    return g
+
+
+def timed_replays(g, steps, torch, stream=None):
+    st = stream or torch.cuda.current_stream()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(st)
+    with torch.cuda.stream(st):
+        for _ in range(steps):
+            g.replay()
+    e1.record(st)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / 1e3
+
+
+def cpu_oracle_sample(state, w, cur_len, seconds):
+    """The oracle as it stands, single-threaded, on a bounded sample of the workload:
+    the frame-input composition and the fused decode step of layer 0 (same bytes as on
+    the device), repeated for about `seconds`.  Returns (GB/s, sample description)."""
+    import numpy as np
+    import oracle
+    K, V = state["caches"][0]
+    hk = K.cpu().numpy()
+    hv = V.cpu().numpy()
+    hk0, hv0 = hk.copy(), hv.copy()
+    tabs = [t.cpu().numpy() for t in state["tabs"]]
+    ids = state["ids"].cpu().numpy()
+    ov = state["overlay"].cpu().numpy()
+    rows = state["qkv"][0].cpu().numpy()
+    qd, kd = w.n_q_heads * w.head_dim, w.n_kv_heads * w.head_dim
+    B = w.B
+    q = rows[:, :qd].reshape(B, w.n_q_heads, w.head_dim)
+    k = rows[:, qd:qd + kd].reshape(B, w.n_kv_heads, w.head_dim)
+    v = rows[:, qd + kd:].reshape(B, w.n_kv_heads, w.head_dim)
+    gq = state["gq"][0].cpu().numpy()
+    gk = state["gk"][0].cpu().numpy()
+    cur = state["cur"].cpu().numpy()
+    bt = None if state["bt"] is None else state["bt"].cpu().numpy()
+    lay = oracle.KvLayout(B, w.n_kv_heads, w.head_dim, w.capacity, w.kv_dtype, paged=w.paged,
+                          page_size=w.page_size, n_pages=w.n_pages, block_table=bt)
+    if w.kv_dtype == "bf16":
+        hk = hk0 = K.cpu().view(__import__("torch").int16).numpy().view(np.uint16).copy()
+        hv = hv0 = V.cpu().view(__import__("torch").int16).numpy().view(np.uint16).copy()
+    per_layer, _, embed = step_bytes(w, [int(c) for c in cur])
+    done_bytes = 0
+    reps = 0
+    t0 = time.perf_counter()
+    while True:
+        oracle.frame_embed(tabs, ids, ov)
+        oracle.decode_step(q, k, v, gq, gk, np.float32(w.eps), w.rope_base, hk, hv, lay, cur,
+                           1.0 / math.sqrt(w.head_dim))
+        done_bytes += embed + per_layer
+        reps += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    dt = time.perf_counter() - t0
+    return done_bytes / dt / 1e9, (f"{reps} x (frame-input composition + layer-0 fused decode step) "
+                                   f"of the {w.name} workload at cur_len {cur_len}, {dt:.1f} s")
+
+
+def run_native(args, rank, world):
+    import torch
+    from autoregressive_codebook_tts_gb300 import build as b
+    b.build()
+    from autoregressive_codebook_tts_gb300 import tts
+    from autoregressive_codebook_tts_gb300 import workloads as W
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    w = W.workload(args.workload)
+    if args.workload == "talker":
+        cur_arg = args.cur_len
+        cur_list = [args.cur_len] * w.B
+    else:
+        cur_t = W.cur_lens(w, seed=0)
+        cur_arg = cur_t
+        cur_list = [int(c) for c in cur_t]
+    frame, layers, state = build_frame(tts, W, w, cur_arg, args.n_splits, dev, seed=rank)
+    per_layer, kv_layer, embed = step_bytes(w, cur_list)
+    frame_bytes = embed + w.layers * per_layer
+
+    g_frame = capture(frame, torch)
+    g_layers = capture(layers, torch)
+    for _ in range(args.warmup):
+        g_frame.replay()
+    torch.cuda.synchronize()
+    if state["ef"].item() != 0:
+        raise RuntimeError(f"device error flag {state['ef'].item()}")
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t_frame = timed_replays(g_frame, args.steps, torch)
+    if world > 1:
+        torch.distributed.barrier()
+    # dominant kernel alone: the 28 fused decode-step launches of the same frame
+    t_layers = timed_replays(g_layers, args.steps, torch)
+    clk = clocks.stop()
+
+    # end to end through the public calls with host buffers: upload this frame's
+    # inputs from pinned memory, run the frame, read back every layer's output
+    h_ids = state["ids"].cpu().pin_memory()
+    h_ov = state["overlay"].cpu().pin_memory()
+    h_qkv = state["qkv"].cpu().pin_memory()
+    h_cur = state["cur"].cpu().pin_memory()
+    h_out = torch.empty_like(state["outs"], device="cpu").pin_memory()
+    h_emb = torch.empty_like(state["emb"], device="cpu").pin_memory()
+    h_ef = torch.empty(1, dtype=torch.int32).pin_memory()
+    s = torch.cuda.current_stream()
+
+    def e2e_step():
+        state["ids"].copy_(h_ids, non_blocking=True)
+        state["overlay"].copy_(h_ov, non_blocking=True)
+        state["qkv"].copy_(h_qkv, non_blocking=True)
+        state["cur"].copy_(h_cur, non_blocking=True)
+        g_frame.replay()
+        h_out.copy_(state["outs"], non_blocking=True)
+        h_emb.copy_(state["emb"], non_blocking=True)
+        h_ef.copy_(state["ef"], non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_steps = max(10, args.steps // 4)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(s)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(s)
+    torch.cuda.synchronize()
+    t_e2e = e0.elapsed_time(e1) / 1e3
+    h2d = sum(t.numel() * t.element_size() for t in (h_ids, h_ov, h_qkv, h_cur))
+    d2h = sum(t.numel() * t.element_size() for t in (h_out, h_emb, h_ef))
+    if int(h_ef.item()) != 0:
+        raise RuntimeError(f"device error flag {int(h_ef.item())}")
+
+    if world > 1:
+        tt = torch.tensor([t_frame, t_layers, t_e2e], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        t_frame, t_layers, t_e2e = [float(x) for x in tt.tolist()]
+
+    sweep = None
+    if args.sweep and args.workload == "talker" and rank == 0:
+        sweep = {}
+        for c in (255, 1023, 2047):
+            fr, ly, st = build_frame(tts, W, w, c, args.n_splits, dev, seed=1)
+            pl, _, em = step_bytes(w, [c])
+            gf = capture(fr, torch)
+            for _ in range(args.warmup):
+                gf.replay()
+            # working set below L2: flush L2 (write 2x its size) before every timed frame
+            flush = torch.empty(2 * 130 * 2 ** 20, dtype=torch.uint8, device=dev)
+            tot = 0.0
+            for _ in range(min(args.steps, 200)):
+                flush.fill_(1)
+                tot += timed_replays(gf, 1, torch)
+            n = min(args.steps, 200)
+            sweep[str(c)] = {"GB_s": round((em + w.layers * pl) * n / tot / 1e9, 1),
+                             "ms_per_step": round(tot / n * 1e3, 4), "l2": "flushed"}
+            del fr, ly, st, gf, flush
+
+    peak, peak_kind = hbm_peak()
+    value = world * frame_bytes * args.steps / t_frame / 1e9
+    dom_bytes = per_layer
+    dom_time = t_layers / (args.steps * w.layers)
+    achieved = dom_bytes / dom_time / 1e9
+    traffic = profiled_traffic()
+    res = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(t_frame / args.steps * 1e3, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32" if w.kv_dtype == "f32" else "bf16-kv/f32",
+        "data": "synthetic (seeded, device-generated; random-init, no weights)",
+        "config": {"workload": (f"{w.name}: B={w.B} streams, {w.layers} layers, hidden {w.hidden}, "
+                                f"{w.n_q_heads} q / {w.n_kv_heads} kv heads, head_dim {w.head_dim}, "
+                                f"{w.kv_dtype} KV, capacity {w.capacity}"
+                                + (f", paged {w.page_size}-token pages" if w.paged else "")
+                                + (f", cur_len {args.cur_len}" if args.workload == 'talker' else ", ragged cur_len")),
+                   "B": w.B, "layers": w.layers, "window_rows_per_layer": sum(c + 1 for c in cur_list),
+                   "l2": "inputs larger than L2 (KV working set per frame %.0f MiB)" % (w.layers * kv_layer / 2 ** 20),
+                   "frame_step": "graph replay of tts_frame_embed + %d x tts_decode_step" % w.layers,
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "pct_of_hbm_peak": round(100 * value / world / peak, 2),
+        "pct_of_nominal_hbm": round(100 * value / world / NOMINAL_HBM_GBS, 2),
+        "frame_steps_per_s": round(world * w.B * args.steps / t_frame, 1),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "kernel": "decode_attn_kernel<fused> (tts_decode_step)",
+                     "peak_source": f"{peak_kind} HBM copy bandwidth",
+                     "bytes_per_launch": dom_bytes, "us_per_launch": round(dom_time * 1e6, 3)},
+        "e2e": {"value": round(world * frame_bytes * e2e_steps / t_e2e / 1e9, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": round(t_e2e / e2e_steps * 1e3, 5)},
+        "gpu_launches": args.steps * (1 + w.layers),
+        "clocks": clk,
+    }
+    if sweep is not None:
+        res["sweep_cur_len"] = sweep
+    if rank == 0 and not args.no_cpu_baseline:
+        gbs, sample = cpu_oracle_sample(state, w, args.cur_len, args.cpu_seconds)
+        res["cpu_baseline"] = {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                               "sample": sample}
+    return res
+
+
+def run_reference(args, rank, world):
+    """The CPU oracle timed as the reference arm, on the same workload and metric."""
+    import numpy as np
+    import torch
+    from autoregressive_codebook_tts_gb300 import workloads as W
+    import oracle
+    oracle.build()
+    w = W.workload(args.workload)
+    cur_list = [args.cur_len] * w.B if args.workload == "talker" else [int(c) for c in W.cur_lens(w, 0)]
+    cur = np.array(cur_list, np.int32)
+    tabs = [t.numpy() for t in W.tables(w.n_tables, w.vocab, w.hidden, seed=0)]
+    ids = W.code_ids(w.B, w.n_tables, w.vocab, seed=1).numpy()
+    ov = W.overlay(w.B, w.hidden, seed=2).numpy()
+    rows, q, k, v = W.qkv(w.B, w.n_q_heads, w.n_kv_heads, w.head_dim, seed=3)
+    q = q.numpy().reshape(w.B, w.n_q_heads, w.head_dim)
+    k = k.numpy().reshape(w.B, w.n_kv_heads, w.head_dim)
+    v = v.numpy().reshape(w.B, w.n_kv_heads, w.head_dim)
+    gq, gk = W.gamma(w.head_dim, 4).numpy(), W.gamma(w.head_dim, 5).numpy()
+    bt = None
+    if w.paged:
+        bt = W.block_table(w.B, w.capacity // w.page_size, w.n_pages, seed=6)
+    K, V = W.cache(w, cur_list, seed=7, block_tab=bt, poison=False)
+    if w.kv_dtype == "bf16":
+        hk = K.view(torch.int16).numpy().view(np.uint16).copy()
+        hv = V.view(torch.int16).numpy().view(np.uint16).copy()
+    else:
+        hk, hv = K.numpy().copy(), V.numpy().copy()
+    lay = oracle.KvLayout(w.B, w.n_kv_heads, w.head_dim, w.capacity, w.kv_dtype, paged=w.paged,
+                          page_size=w.page_size, n_pages=w.n_pages,
+                          block_table=None if bt is None else bt.numpy())
+    per_layer, _, embed = step_bytes(w, cur_list)
+    # one step = the frame-input composition + one layer's fused decode step (a bounded
+    # sample of the frame; the metric is bytes per second, so it carries over)
+    sample_bytes = embed + per_layer
+
+    def step():
+        oracle.frame_embed(tabs, ids, ov)
+        oracle.decode_step(q, k, v, gq, gk, np.float32(w.eps), w.rope_base, hk, hv, lay, cur,
+                           1.0 / math.sqrt(w.head_dim))
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = time.perf_counter() - t0
+    value = sample_bytes * args.steps / dt / 1e9
+    sample = (f"each step: frame-input composition + one layer's fused decode step of the "
+              f"{w.name} workload (1 of {w.layers} layers)")
+    return {
+        "impl": "reference",
+        "metric": METRIC, "value": round(value, 5), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)",
+        "data": "synthetic (seeded)",
+        "config": {"workload": f"{w.name} (same shapes as the native arm)", "B": w.B,
+                   "layers": w.layers, "parallelism": "single host thread"},
+        "cpu_baseline": {"value": round(value, 5), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 5), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        if args.steps > 50:
+            args.steps = 20   # each oracle step is a whole layer in double precision
+        if args.warmup > 3:
+            args.warmup = 3
+        print(json.dumps(run_reference(args, rank, world)))
+        return
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    res = run_native(args, rank, world)
+    if rank == 0:
+        print(json.dumps(res))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

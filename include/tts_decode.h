@@ -1,0 +1,245 @@
+/*
+ * tts_decode.h -- C ABI of the GB300 (sm_103a) per-frame decode hot path of a
+ * multi-codebook autoregressive TTS transformer (talker + 16-slot code predictor).
+ *
+ * The operations and where they are defined (page titles as printed on the pages):
+ *   [P-pipeline] "qwentts.cpp ... src/pipeline-tts.h" commit page
+ *       - fixed-topology section: KV writes through set_rows with the destination rows
+ *         carried as data, so every decode graph keeps fixed tensor addresses; per
+ *         frame the host uploads 16 code ids and one overlay row and reads back only
+ *         results;
+ *       - on-device AR input assembly section: the talker gathers and sums the 16 frame
+ *         code embeddings plus the trailing text/pad overlay; the code predictor
+ *         gathers c0 and each sampled sub-code from its own group table;
+ *       - persistent-arenas section: talker attention window padded to 256, predictor
+ *         window fixed to the frame cache size, causal mask carrying -inf over the
+ *         padded tail;
+ *       - KV-cache section: a per-layer K/V buffer sized at init (talker 4096
+ *         positions, predictor 16 positions reset every frame); decode appends one
+ *         position and reads the [0, cur_len+1) window; the predictor runs a T=2
+ *         prefill then 14 single-token decodes.
+ *   [P-engine] "minicpm-o-4.5-single-gpu-engine ... docs/optimizations.md",
+ *       core-optimisation table: fused q/k norm + RoPE kernels, integer
+ *       round-to-nearest-even rounding, paged KV per model; "Lean Talker frame"
+ *       option row: q/k/v read as strided views of one projection output.
+ *
+ * Conventions shared by every call
+ *   - Every buffer pointer is a DEVICE pointer owned by the caller (allocated, e.g.,
+ *     through PyTorch).  The library never allocates device memory and keeps no state
+ *     between calls; descriptor structs are read on the host during the call only.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).
+ *     Every call is asynchronous and stream-ordered; the launch configuration depends
+ *     only on shapes and capacity, never on device data such as cur_len, so a
+ *     sequence of calls can be captured in a CUDA graph and replayed with fixed
+ *     addresses.
+ *   - Kernels are launched with programmatic stream serialisation: each kernel waits
+ *     for the previous kernel on the stream before touching its inputs (one
+ *     documented opt-in exception, TTS_KV_PREFETCH_BEFORE_WAIT below).
+ *   - The returned tts_status reports errors found on the host, before any launch
+ *     (null pointers, bad shapes, misalignment, short workspace, launch failure).
+ *     Nothing is launched when it is not TTS_OK.
+ *   - Errors only visible on the device (a code id outside the table, a position
+ *     outside the cache, a bad page id, an n_valid outside [1, capacity], a bounded
+ *     wait that ran out) never trap: the offending index is clamped or the write is
+ *     skipped as stated per call, and a bit (TTS_EFLAG_*) is OR-ed into the caller's
+ *     int32 `err_flag` (device memory; may be NULL to ignore).  Read it after the
+ *     stream synchronises; clear it yourself.
+ *   - Alignment: every device pointer must be 16-byte aligned; row strides are given
+ *     in elements and must keep each row 16-byte aligned (a multiple of 4 floats).
+ *   - head_dim is 64 or 128; n_q_heads / n_kv_heads (the GQA group) is 1, 2 or 4.
+ */
+#ifndef TTS_DECODE_H
+#define TTS_DECODE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ABI version range ([P-pipeline]-style ABI probe): a caller built against version V
+ * may use this library iff tts_abi_min_version() <= V <= tts_abi_version(). */
+#define TTS_ABI_VERSION 1
+#define TTS_ABI_MIN_VERSION 1
+int32_t tts_abi_version(void);
+int32_t tts_abi_min_version(void);
+
+typedef enum {
+  TTS_OK = 0,
+  TTS_ERR_NULL = 1,       /* a required pointer is NULL */
+  TTS_ERR_SHAPE = 2,      /* a size or head count outside the supported set */
+  TTS_ERR_DTYPE = 3,      /* unknown dtype code */
+  TTS_ERR_LAYOUT = 4,     /* inconsistent cache layout (page size, pool, strides) */
+  TTS_ERR_ALIGN = 5,      /* a pointer or stride breaks the 16-byte rule */
+  TTS_ERR_WORKSPACE = 6,  /* workspace NULL or smaller than required */
+  TTS_ERR_CUDA = 7,       /* the CUDA runtime refused the launch */
+  TTS_ERR_ABI = 8         /* reserved for version mismatches */
+} tts_status;
+
+/* Human-readable name of a status code (static string). */
+const char* tts_status_str(int32_t status);
+
+/* Device-side error bits OR-ed into *err_flag. */
+#define TTS_EFLAG_ID_RANGE 1    /* code id outside [0, vocab): clamped into range   */
+#define TTS_EFLAG_POS_RANGE 2   /* position outside the cache/RoPE table: see call  */
+#define TTS_EFLAG_PAGE 4        /* block-table entry outside [0, n_pages): see call */
+#define TTS_EFLAG_NVALID 8      /* n_valid outside [1, capacity]: clamped into it   */
+#define TTS_EFLAG_TIMEOUT 16    /* a bounded in-kernel wait ran out; output invalid */
+
+typedef enum { TTS_F32 = 0, TTS_BF16 = 1 } tts_dtype;
+
+#define TTS_MAX_TABLES 16
+
+/* Codebook tables for the frame-input composition.  tab[g] points to a dense row-major
+ * [vocab][hidden] f32 table; only the first n_tables entries are read. */
+typedef struct {
+  const float* tab[TTS_MAX_TABLES];
+  int32_t n_tables; /* 1..16 */
+  int32_t vocab;    /* rows per table */
+  int32_t hidden;   /* row length in floats, a multiple of 4 */
+} tts_tables;
+
+/* Flags of tts_kv_desc.flags */
+/* TTS_KV_PREFETCH_BEFORE_WAIT: tts_decode_step may start streaming this layer's cache
+ * rows before the previous kernel on the stream has finished.  Set it only when the
+ * work enqueued immediately before the call writes neither this cache, nor its block
+ * table, nor cur_len (true for a layer loop whose layers own distinct caches). */
+#define TTS_KV_PREFETCH_BEFORE_WAIT 1u
+
+/* One layer's K/V cache for B streams, "head-major" so that one kv head's positions
+ * are contiguous:
+ *   contiguous (paged = 0): K[b][g][j][d], j < capacity, dense; V likewise.
+ *   paged      (paged = 1): a pool K[page][g][slot][d], page < n_pages,
+ *                           slot < page_size; position j of stream b lives in page
+ *                           block_table[b * bt_stride + j / page_size], slot
+ *                           j % page_size.  capacity = page_size * pages per stream.
+ * Element type f32 or bf16 (kv_dtype).  The window seen by a decode query is
+ * [0, n_valid); conceptually it is padded to W = ceil(n_valid / window_quantum) *
+ * window_quantum with -inf scores over [n_valid, W), i.e. those rows get weight
+ * exactly 0 and are never read, so results do not depend on window_quantum or on what
+ * the tail holds. */
+typedef struct {
+  int32_t B;              /* streams */
+  int32_t n_q_heads;      /* Hq */
+  int32_t n_kv_heads;     /* Hkv; Hq / Hkv in {1, 2, 4} */
+  int32_t head_dim;       /* D in {64, 128} */
+  int32_t capacity;       /* positions per stream, >= 1 */
+  int32_t window_quantum; /* 256 talker, 16 predictor; divides capacity */
+  int32_t kv_dtype;       /* tts_dtype */
+  int32_t paged;          /* 0 contiguous, 1 paged */
+  int32_t page_size;      /* paged: power of two in [1, 256] */
+  int32_t n_pages;        /* paged: pages in the pool */
+  int32_t bt_stride;      /* paged: block-table row stride (entries), >= capacity/page_size */
+  uint32_t flags;         /* TTS_KV_* */
+  const int32_t* block_table; /* paged: device int32 [B][bt_stride]; else NULL */
+} tts_kv_desc;
+
+/* ---------------------------------------------------------------------------
+ * Step 1: frame-input composition.  [P-pipeline], on-device AR input assembly.
+ *   out[b] = ((tab[0][ids[b][0]] + tab[1][ids[b][1]]) + ... ) + overlay[b]
+ * in f32, codebooks in ascending order, the overlay added last; the result is
+ * bit-identical to that sequence of single f32 additions.  For a code-predictor
+ * sub-step pass one group table (n_tables = 1) and overlay = NULL.
+ *   ids:     device int32 [B][ids_stride], first n_tables entries per row read.
+ *   overlay: device f32 rows of `hidden`, row stride overlay_stride; or NULL.
+ *   out:     device f32 [B][hidden], dense.
+ * An id outside [0, vocab) is clamped into range and sets TTS_EFLAG_ID_RANGE.
+ * ------------------------------------------------------------------------- */
+tts_status tts_frame_embed(const tts_tables* tables, const int32_t* ids, int64_t ids_stride,
+                           const float* overlay, int64_t overlay_stride, float* out, int32_t B,
+                           int32_t* err_flag, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * RoPE table.  Fills cs[p][i] = (cos theta, sin theta) as float pairs with
+ * theta = p * base^(-2i/head_dim), for p < max_pos, i < head_dim/2; the angle and its
+ * cos/sin are evaluated in double on the device and rounded to f32 once.  Built once
+ * per model (like a model's inverse-frequency buffer) and read by the norm+RoPE calls.
+ *   cs: device f32 [max_pos][head_dim/2][2].
+ * ------------------------------------------------------------------------- */
+tts_status tts_rope_table(float* cs, int32_t max_pos, int32_t head_dim, double base, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Step 2: per-head q/k RMSNorm then rotate-half RoPE, in place.  [P-engine], core
+ * table, fused q/k norm + RoPE.  For every head row x of q (Hq heads) and k (Hkv
+ * heads) of stream b:
+ *   t_d = x_d * (mean_d(x_d^2) + eps)^(-1/2) * gamma_d
+ *   y_i = t_i c_i - t_{i+D/2} s_i,  y_{i+D/2} = t_i s_i + t_{i+D/2} c_i
+ * with (c_i, s_i) = rope_cs[pos[b]][i].  gamma_q / gamma_k: device f32 [D], shared by
+ * the heads.  q rows: stream b at q + b*q_row_stride, heads contiguous (same for k).
+ * q and k may be strided views into one fused projection row.  A pos outside
+ * [0, rope_max_pos) is clamped and sets TTS_EFLAG_POS_RANGE.
+ * ------------------------------------------------------------------------- */
+tts_status tts_qk_norm_rope(float* q, int64_t q_row_stride, float* k, int64_t k_row_stride,
+                            const float* gamma_q, const float* gamma_k, const int32_t* pos,
+                            int32_t B, int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim,
+                            float eps, const float* rope_cs, int32_t rope_max_pos,
+                            int32_t* err_flag, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Step 3: KV write by set_rows.  [P-pipeline], fixed-topology section; KV-cache section.
+ * For stream b and kv head g the row k[b][g][:] (f32) is written to the K cache at
+ * position dst_pos[b] (device data), converted to the cache dtype (identity for f32;
+ * bf16 round-to-nearest-even), and likewise v into the V cache.  k/v rows: stream b at
+ * k + b*kv_row_stride, heads contiguous.  A position outside [0, capacity) or a page id
+ * outside [0, n_pages) skips that stream's write and sets TTS_EFLAG_POS_RANGE /
+ * TTS_EFLAG_PAGE.  Nothing else in the caches is touched.
+ * ------------------------------------------------------------------------- */
+tts_status tts_kv_set_rows(const float* k, const float* v, int64_t kv_row_stride, void* k_cache,
+                           void* v_cache, const tts_kv_desc* desc, const int32_t* dst_pos,
+                           int32_t* err_flag, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Step 4: single-query GQA decode attention with split-KV partitions.
+ * [P-pipeline], persistent-arenas and KV-cache sections.  For stream b and q head h
+ * (kv head g = h / (Hq/Hkv)):
+ *   s_j = scale * q_h . K[b][g][j],  j < n_valid[b];   rows j >= n_valid[b]: -inf
+ *   out[b][h] = sum_j softmax(s)_j V[b][g][j]
+ * f32 accumulation.  Each kv head's window is cut into n_splits position ranges that
+ * are processed in parallel and merged with a log-sum-exp combine inside the same
+ * launch (the last range to finish merges; no kernel waits on another).
+ *   q:   device f32, stream b at q + b*q_row_stride, heads contiguous.
+ *   out: device f32 [B][Hq][D], dense.
+ *   n_valid: device int32 [B] (= cur_len + 1 after the new row is written); an entry
+ *        outside [1, capacity] is clamped and sets TTS_EFLAG_NVALID.  In a paged cache
+ *        a page id outside [0, n_pages) inside the window reads page 0 instead and sets
+ *        TTS_EFLAG_PAGE.
+ *   workspace: device scratch of at least tts_decode_attn_workspace_size() bytes,
+ *        256-byte aligned, zeroed once before its first use (tts_workspace_init or a
+ *        memset); every call leaves it ready for the next.  Calls that overlap in time
+ *        on the GPU must not share a workspace.
+ *   n_splits: ranges per kv head, >= 1; 0 picks tts_decode_attn_default_splits().
+ * ------------------------------------------------------------------------- */
+size_t tts_decode_attn_workspace_size(const tts_kv_desc* desc, int32_t n_splits);
+int32_t tts_decode_attn_default_splits(const tts_kv_desc* desc);
+tts_status tts_workspace_init(void* workspace, size_t ws_bytes, void* stream);
+
+tts_status tts_decode_attn(const float* q, int64_t q_row_stride, const void* k_cache,
+                           const void* v_cache, const tts_kv_desc* desc, const int32_t* n_valid,
+                           float scale, float* out, void* workspace, size_t ws_bytes,
+                           int32_t n_splits, int32_t* err_flag, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Steps 2+3+4 fused: one layer of one decode step for B streams, in the order of the
+ * [P-pipeline] KV-cache section.  For stream b with position p = cur_len[b]:
+ *   q' = norm_rope(q[b], gamma_q, p), k' = norm_rope(k[b], gamma_k, p)   (as step 2)
+ *   K[b][.][p] = cvt(k'), V[b][.][p] = cvt(v[b])                         (as step 3)
+ *   out[b] = attention of q' over [0, p + 1)                             (as step 4)
+ * q, k, v are read only (they may be strided views of one projection row; each row of
+ * stream b starts at ptr + b*row_stride).  The attention uses the converted new row,
+ * exactly as if it had been read back from the cache.  Workspace and n_splits as in
+ * tts_decode_attn.  The frame-input composition (step 1) is a separate call made once
+ * per frame, because the QKV projection sits between it and this step.
+ * ------------------------------------------------------------------------- */
+tts_status tts_decode_step(const float* q, const float* k, const float* v, int64_t row_stride,
+                           const float* gamma_q, const float* gamma_k, float eps,
+                           const float* rope_cs, int32_t rope_max_pos, void* k_cache,
+                           void* v_cache, const tts_kv_desc* desc, const int32_t* cur_len,
+                           float scale, float* out, void* workspace, size_t ws_bytes,
+                           int32_t n_splits, int32_t* err_flag, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TTS_DECODE_H */

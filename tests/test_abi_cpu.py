@@ -1,0 +1,121 @@
+"""Host-side checks of the C ABI that need no GPU: the library builds and loads, it
+exports every function that include/tts_decode.h declares, the ABI version range
+behaves like the probe described on the "qwentts.cpp" tests page (ABI bump section:
+both bounds of [min, max] reject), and argument validation rejects bad calls before
+any launch."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+# The validation tests pass fake device addresses that must be rejected on the host.
+# They only run where no GPU is visible, so that a validation bug can never turn into
+# a launch on fake pointers.
+no_gpu = pytest.mark.skipif(
+    __import__("torch").cuda.is_available(), reason="host-only validation checks")
+
+
+@pytest.fixture(scope="module")
+def tts():
+    from autoregressive_codebook_tts_gb300 import build
+    build.build()
+    from autoregressive_codebook_tts_gb300 import tts as mod
+    return mod
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "tts_decode.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(tts_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_library_exports_every_declared_function(tts):
+    names = declared_functions()
+    assert len(names) >= 12
+    lib = ctypes.CDLL(tts.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+    assert sorted(tts.EXPORTED) == names
+
+
+def test_abi_version_probe(tts):
+    lo, hi = tts.abi_min_version(), tts.abi_version()
+    assert 1 <= lo <= hi
+
+    def compatible(v):
+        return lo <= v <= hi
+    assert compatible(hi) and compatible(lo)
+    assert not compatible(lo - 1) and not compatible(hi + 1)
+
+
+def test_status_strings(tts):
+    assert tts.status_str(0) == "TTS_OK"
+    assert tts.status_str(6) == "TTS_ERR_WORKSPACE"
+    assert tts.status_str(99) == "TTS_ERR_UNKNOWN"
+
+
+def _call_attn(tts, desc, q=16, k=16, v=16, nv=16, out=16, ws=256, ws_bytes=1 << 20, n_splits=0):
+    P = ctypes.c_void_p
+    return tts._lib.tts_decode_attn(P(q) if q else None, desc.n_q_heads * desc.head_dim,
+                                    P(k) if k else None, P(v) if v else None, ctypes.byref(desc),
+                                    P(nv) if nv else None, 0.1, P(out) if out else None,
+                                    P(ws) if ws else None, ws_bytes, n_splits, None, None)
+
+
+@no_gpu
+def test_validation_rejects_before_launch(tts):
+    d = tts.kv_desc(1, 16, 8, 128, 4096)
+    assert _call_attn(tts, d, q=0) == 1                    # NULL
+    assert _call_attn(tts, d, k=0) == 1
+    assert _call_attn(tts, tts.kv_desc(1, 16, 8, 96, 4096)) == 2   # head_dim
+    assert _call_attn(tts, tts.kv_desc(1, 16, 3, 128, 4096)) == 2  # group
+    assert _call_attn(tts, tts.kv_desc(1, 16, 2, 128, 4096)) == 2  # group 8
+    assert _call_attn(tts, tts.kv_desc(1, 16, 8, 128, 4000)) == 2  # quantum
+    bad = tts.kv_desc(1, 16, 8, 128, 4096)
+    bad.kv_dtype = 7
+    assert _call_attn(tts, bad) == 3
+    assert _call_attn(tts, d, k=24) == 5                   # misaligned cache
+    assert _call_attn(tts, d, ws=0) == 6                   # no workspace with splits
+    assert _call_attn(tts, d, ws_bytes=16) == 6            # short workspace
+    assert _call_attn(tts, d, ws=272) == 5                 # workspace not 256-aligned
+    paged = tts.kv_desc(1, 16, 8, 128, 4096, paged=True, page_size=16, n_pages=4)
+    assert _call_attn(tts, paged) == 1                     # paged without block table
+    paged.block_table = 4096
+    paged.bt_stride = 256
+    paged.page_size = 12
+    assert _call_attn(tts, paged) == 4                     # page size not a power of two
+
+
+def test_workspace_size_grows_with_splits(tts):
+    d = tts.kv_desc(32, 16, 8, 128, 4096, kv_dtype="bf16")
+    s1 = tts.tts_decode_attn_workspace_size(d, 1)
+    s8 = tts.tts_decode_attn_workspace_size(d, 8)
+    s16 = tts.tts_decode_attn_workspace_size(d, 16)
+    assert 0 < s1 < s8 < s16
+    # o partials + (m, l) + tickets, each rounded to 256 bytes
+    assert s8 >= 32 * 16 * 8 * (128 + 2) * 4 + 32 * 8 * 4
+    assert tts.tts_decode_attn_default_splits(d) >= 1
+
+
+@no_gpu
+def test_other_entry_points_validate(tts):
+    P = ctypes.c_void_p
+    t = tts.TtsTables()
+    t.n_tables, t.vocab, t.hidden = 16, 2048, 1024
+    assert tts._lib.tts_frame_embed(ctypes.byref(t), P(16), 16, None, 0, P(16), 1, None, None) == 1
+    t.n_tables = 17
+    assert tts._lib.tts_frame_embed(ctypes.byref(t), P(16), 16, None, 0, P(16), 1, None, None) == 2
+    assert tts._lib.tts_rope_table(None, 16, 128, 1e6, None) == 1
+    assert tts._lib.tts_rope_table(P(16), 16, 100, 1e6, None) == 2
+    assert tts._lib.tts_rope_table(P(8), 16, 128, 1e6, None) == 5
+    d = tts.kv_desc(1, 16, 8, 128, 4096)
+    assert tts._lib.tts_kv_set_rows(P(16), P(16), 1024, P(16), P(16), ctypes.byref(d), None, None, None) == 1
+    assert tts._lib.tts_kv_set_rows(P(16), P(16), 1000, P(16), P(16), ctypes.byref(d), P(16), None, None) == 2
+    assert tts._lib.tts_qk_norm_rope(P(16), 2048, P(16), 1024, P(16), P(16), None, 1, 16, 8, 128,
+                                     1e-6, P(16), 4096, None, None) == 1
+    assert tts._lib.tts_qk_norm_rope(P(16), 1000, P(16), 1024, P(16), P(16), P(16), 1, 16, 8, 128,
+                                     1e-6, P(16), 4096, None, None) == 2
