@@ -77,6 +77,21 @@ WsLayout ws_layout(const tts_kv_desc* d, int n_splits) {
   return w;
 }
 
+// Splits actually launched for a requested count (0 = default): at most one per tile
+// and at most kMaxSplits; each split covers split_len positions, a multiple of the tile.
+constexpr int kMaxSplits = 256;
+tts_status resolve_splits(const tts_kv_desc* d, int32_t n_splits_req, int& split_len, int& used) {
+  const AttnGeometry geo = attn_geometry(d->kv_dtype == TTS_BF16, d->head_dim);
+  int n_splits = n_splits_req == 0 ? tts_decode_attn_default_splits(d) : n_splits_req;
+  if (n_splits < 1) return TTS_ERR_SHAPE;
+  const int max_splits = (d->capacity + geo.tile_rows - 1) / geo.tile_rows;
+  if (n_splits > max_splits) n_splits = max_splits;
+  if (n_splits > kMaxSplits) n_splits = kMaxSplits;
+  split_len = split_len_for(d, n_splits, geo.tile_rows);
+  used = (d->capacity + split_len - 1) / split_len;
+  return TTS_OK;
+}
+
 // Shared preparation of the attention launch (standalone and fused).
 tts_status prepare_attn(const tts_kv_desc* d, const void* k_cache, const void* v_cache,
                         void* workspace, size_t ws_bytes, int32_t n_splits_req, AttnParams& p,
@@ -85,14 +100,10 @@ tts_status prepare_attn(const tts_kv_desc* d, const void* k_cache, const void* v
   if (st != TTS_OK) return st;
   if (k_cache == nullptr || v_cache == nullptr) return TTS_ERR_NULL;
   if (!aligned16(k_cache) || !aligned16(v_cache)) return TTS_ERR_ALIGN;
-  const int bf16 = d->kv_dtype == TTS_BF16;
-  const AttnGeometry geo = attn_geometry(bf16, d->head_dim);
-  int n_splits = n_splits_req == 0 ? tts_decode_attn_default_splits(d) : n_splits_req;
-  if (n_splits < 1) return TTS_ERR_SHAPE;
-  const int max_splits = (d->capacity + geo.tile_rows - 1) / geo.tile_rows;
-  if (n_splits > max_splits) n_splits = max_splits;
-  const int split_len = split_len_for(d, n_splits, geo.tile_rows);
-  const int used = (d->capacity + split_len - 1) / split_len;  // splits actually launched
+  const AttnGeometry geo = attn_geometry(d->kv_dtype == TTS_BF16, d->head_dim);
+  int split_len = 0, used = 0;
+  st = resolve_splits(d, n_splits_req, split_len, used);
+  if (st != TTS_OK) return st;
   if (used > 65535 || d->n_kv_heads > 65535 || d->B > 65535) return TTS_ERR_SHAPE;
   if (used > 1) {
     const WsLayout w = ws_layout(d, used);
@@ -257,13 +268,8 @@ int32_t tts_decode_attn_default_splits(const tts_kv_desc* d) {
 
 size_t tts_decode_attn_workspace_size(const tts_kv_desc* d, int32_t n_splits) {
   if (check_desc(d) != TTS_OK) return 0;
-  if (n_splits == 0) n_splits = tts_decode_attn_default_splits(d);
-  if (n_splits < 1) return 0;
-  const AttnGeometry geo = attn_geometry(d->kv_dtype == TTS_BF16, d->head_dim);
-  const int max_splits = (d->capacity + geo.tile_rows - 1) / geo.tile_rows;
-  if (n_splits > max_splits) n_splits = max_splits;
-  const int split_len = split_len_for(d, n_splits, geo.tile_rows);
-  const int used = (d->capacity + split_len - 1) / split_len;
+  int split_len = 0, used = 0;
+  if (resolve_splits(d, n_splits, split_len, used) != TTS_OK) return 0;
   return ws_layout(d, used).total;
 }
 

@@ -14,24 +14,103 @@
 //     (the TMA engine) of whole K and V tiles; the cache is head-major, so a tile of a
 //     contiguous cache is one copy (a paged cache: one copy per page piece).  Copies
 //     complete on per-stage mbarriers; consumer warps release stages on a second set.
-//   * Four consumer warps split each tile's rows.  A row is covered by LPR lanes with
-//     16 bytes each (4 f32 or 8 bf16 elements); q.k is reduced across those lanes with
-//     xor shuffles; each warp keeps its own online-softmax state (running max in
-//     log2 units, running sum, unnormalised output), merged at the end through
-//     shared memory.
+//     The ring is kept small (64 KB) so that three CTAs share an SM and the next
+//     launch's CTAs find room while this one drains.
+//   * Consumer warps split each tile's rows.  A row is covered by LPR lanes with 16
+//     bytes each (4 f32 or 8 bf16 elements); q.k is reduced across those lanes with
+//     xor shuffles; each warp keeps its own online-softmax state (running max in log2
+//     units, running sum, unnormalised output), merged at the end in shared memory.
 //   * Rows at or past n_valid are never copied or read: the -inf of the padded tail
 //     is realised as "not there", so poison in the tail cannot leak.
-//   * Split-KV: every split writes (o, m, l) to the workspace and takes a ticket; the
-//     last split of a (stream, kv head) merges all partials with a log-sum-exp combine
-//     and resets the ticket.  No CTA ever waits for another.
+//   * Split-KV: every split writes (o, m, l) to the workspace and takes a ticket (one
+//     acquire-release atomic per CTA); the last split of a (stream, kv head) merges all
+//     partials with a log-sum-exp combine whose loads are all issued up front, and
+//     resets the ticket.  No CTA ever waits for another.
 //   * Launch configuration depends only on capacity; splits past the window exit early.
+//   * Programmatic dependent launch: each launch lets the next one be scheduled as soon
+//     as its own consumers pass their dependency wait.  With TTS_KV_PREFETCH_BEFORE_WAIT
+//     the producer starts streaming cache tiles (and the consumers load gamma and the
+//     RoPE row) before the preceding kernel has finished.
 //   * Every mbarrier wait is bounded (kWaitLimitCycles); on expiry TTS_EFLAG_TIMEOUT is
 //     set, the copies already issued are waited for (bounded), and the CTA finishes.
 #include "common.cuh"
 #include "kernels.h"
 
+// Tile geometry per (cache dtype, head_dim): rows per stage (T), ring stages (NS),
+// consumer warps (NC).  Overridable at build time for tuning sweeps.
+#ifndef TTS_F32_128_T
+#define TTS_F32_128_T 16
+#endif
+#ifndef TTS_F32_128_NS
+#define TTS_F32_128_NS 4
+#endif
+#ifndef TTS_F32_128_NC
+#define TTS_F32_128_NC 4
+#endif
+#ifndef TTS_BF16_128_T
+#define TTS_BF16_128_T 32
+#endif
+#ifndef TTS_BF16_128_NS
+#define TTS_BF16_128_NS 4
+#endif
+#ifndef TTS_BF16_128_NC
+#define TTS_BF16_128_NC 4
+#endif
+#ifndef TTS_F32_64_T
+#define TTS_F32_64_T 32
+#endif
+#ifndef TTS_F32_64_NS
+#define TTS_F32_64_NS 4
+#endif
+#ifndef TTS_F32_64_NC
+#define TTS_F32_64_NC 4
+#endif
+#ifndef TTS_BF16_64_T
+#define TTS_BF16_64_T 64
+#endif
+#ifndef TTS_BF16_64_NS
+#define TTS_BF16_64_NS 4
+#endif
+#ifndef TTS_BF16_64_NC
+#define TTS_BF16_64_NC 4
+#endif
+#ifndef TTS_ATTN_MIN_BLOCKS
+#define TTS_ATTN_MIN_BLOCKS 3
+#endif
+
 namespace tts {
+
+#ifdef TTS_TRACE
+// Optional timeline of the most recent attention launch (build with -DTTS_TRACE):
+// per CTA, %globaltimer stamps at fixed points; read with tts_trace_read().
+constexpr int kTraceSlots = 8;
+constexpr int kTraceCtas = 8192;
+__device__ unsigned long long g_trace[kTraceCtas][kTraceSlots];
+__device__ __forceinline__ unsigned long long gtime() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+#define TTS_STAMP(slot)                                                                    \
+  do {                                                                                     \
+    const int cta_ = (blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;       \
+    if (cta_ < kTraceCtas) g_trace[cta_][slot] = gtime();                                  \
+  } while (0)
+#else
+#define TTS_STAMP(slot) do {} while (0)
+#endif
+
 namespace {
+
+template <int T_, int NS_, int NC_>
+struct TuneOf {
+  static constexpr int T = T_, NS = NS_, NC = NC_;
+};
+template <typename KvT, int D> struct Tune;
+template <> struct Tune<float, 128> : TuneOf<TTS_F32_128_T, TTS_F32_128_NS, TTS_F32_128_NC> {};
+template <> struct Tune<__nv_bfloat16, 128> : TuneOf<TTS_BF16_128_T, TTS_BF16_128_NS, TTS_BF16_128_NC> {};
+template <> struct Tune<float, 64> : TuneOf<TTS_F32_64_T, TTS_F32_64_NS, TTS_F32_64_NC> {};
+template <> struct Tune<__nv_bfloat16, 64> : TuneOf<TTS_BF16_64_T, TTS_BF16_64_NS, TTS_BF16_64_NC> {};
 
 template <typename KvT, int D_, int G_>
 struct Cfg {
@@ -42,16 +121,19 @@ struct Cfg {
   static constexpr int LPR = D / EPL;         // lanes per row
   static constexpr int RPI = 32 / LPR;        // rows per warp step
   static constexpr int ROW_BYTES = D * kElem;
-  static constexpr int NC = 4;                // consumer warps
-  static constexpr int T = (ROW_BYTES >= 512) ? 32 : 64;  // rows per stage
-  static constexpr int NS = 3;                // maximum ring depth
+  static constexpr int T = Tune<KvT, D>::T;   // rows per stage
+  static constexpr int NS = Tune<KvT, D>::NS; // maximum ring depth
+  static constexpr int NC = Tune<KvT, D>::NC; // consumer warps
+  static constexpr int NT = NC * 32;          // consumer threads
   static constexpr int RPW = T / NC;          // rows per warp per tile
   static constexpr int STEPS = RPW / RPI;
   static constexpr int TILE_BYTES = T * ROW_BYTES;
   static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
-  static constexpr int THREADS = (NC + 1) * 32;
-  static_assert(RPW % RPI == 0, "tile rows must split evenly over warp steps");
+  static constexpr int THREADS = NT + 32;
+  static constexpr int Q4 = G * D / 4;        // float4 columns of one (stream, kv head) output
+  static_assert(RPW % RPI == 0 && STEPS >= 1, "tile rows must split evenly over warp steps");
   static_assert(LPR >= 2 && LPR <= 32, "row must span 2..32 lanes");
+  static_assert(NT % Q4 == 0 || Q4 % NT == 0, "combine layout");
 
   static constexpr size_t bar_off(int ns) { return static_cast<size_t>(ns) * STAGE_BYTES; }
   static constexpr size_t fresh_off(int ns) { return bar_off(ns) + 2 * NS * sizeof(uint64_t); }
@@ -62,7 +144,7 @@ struct Cfg {
   static constexpr size_t smem_bytes(int ns) { return flag_off(ns) + 16; }
 };
 
-// 16 bytes of f32 row data starting at element e0 of a global row.
+// f32 row data starting at element e0 of a global row (EPL floats, 16-byte loads).
 template <int EPL>
 __device__ __forceinline__ void load_row_f32(const float* row, int e0, float (&x)[EPL]) {
 #pragma unroll
@@ -85,18 +167,22 @@ __device__ __forceinline__ uint4 pack_row(const float (&x)[8], __nv_bfloat16*) {
                     pack2_bf16(x[6], x[7]));
 }
 
-// Consume one tile (nrows valid rows) for this warp: scores, online softmax, P.V.
+// 2^x on the MUFU unit (ex2.approx, relative error about 2^-22; -inf gives +0).
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Phase 1 of a tile for this warp: q.K scores of its rows (log2 units), reduced over
+// the LPR lanes of each row; rows at or past nrows get -inf.
 template <class C, typename KvT, bool PARTIAL>
-__device__ __forceinline__ void consume_tile(const unsigned char* __restrict__ kt,
-                                             const unsigned char* __restrict__ vt, int nrows,
-                                             int warp, int lane, const float (&q)[C::G][C::EPL],
-                                             float (&m_run)[C::G], float (&l_run)[C::G],
-                                             float (&o)[C::G][C::EPL]) {
+__device__ __forceinline__ void tile_scores(const unsigned char* __restrict__ kt, int nrows,
+                                            int warp, int lane, const float (&q)[C::G][C::EPL],
+                                            float (&s)[C::STEPS][C::G]) {
   constexpr int G = C::G, EPL = C::EPL, LPR = C::LPR, STEPS = C::STEPS;
   const int lr = lane % LPR;
-  const int rg = lane / LPR;
-  const int row_base = warp * C::RPW + rg;
-  float s[STEPS][G];
+  const int row_base = warp * C::RPW + lane / LPR;
 #pragma unroll
   for (int st = 0; st < STEPS; ++st) {
     const int row = row_base + st * C::RPI;
@@ -109,18 +195,22 @@ __device__ __forceinline__ void consume_tile(const unsigned char* __restrict__ k
     }
 #pragma unroll
     for (int h = 0; h < G; ++h) {
-      float a = 0.f;
+      // two partial sums halve the FMA dependency chain
+      float a0 = 0.f, a1 = 0.f;
 #pragma unroll
-      for (int i = 0; i < EPL; ++i) a = fmaf(q[h][i], kf[i], a);
-      s[st][h] = a;
+      for (int i = 0; i < EPL; i += 2) {
+        a0 = fmaf(q[h][i], kf[i], a0);
+        a1 = fmaf(q[h][i + 1], kf[i + 1], a1);
+      }
+      s[st][h] = a0 + a1;
     }
   }
 #pragma unroll
-  for (int st = 0; st < STEPS; ++st)
+  for (int off = LPR / 2; off >= 1; off >>= 1)
 #pragma unroll
-    for (int h = 0; h < G; ++h)
+    for (int st = 0; st < STEPS; ++st)
 #pragma unroll
-      for (int off = LPR / 2; off >= 1; off >>= 1) s[st][h] += __shfl_xor_sync(kFull, s[st][h], off);
+      for (int h = 0; h < G; ++h) s[st][h] += __shfl_xor_sync(kFull, s[st][h], off);
   if (PARTIAL) {
 #pragma unroll
     for (int st = 0; st < STEPS; ++st)
@@ -128,6 +218,17 @@ __device__ __forceinline__ void consume_tile(const unsigned char* __restrict__ k
 #pragma unroll
         for (int h = 0; h < G; ++h) s[st][h] = -INFINITY;
   }
+}
+
+// Phase 2 of a tile: online-softmax update with the tile's scores, then P.V.
+template <class C, typename KvT, bool PARTIAL>
+__device__ __forceinline__ void tile_softmax_pv(const unsigned char* __restrict__ vt, int nrows,
+                                                int warp, int lane, float (&s)[C::STEPS][C::G],
+                                                float (&m_run)[C::G], float (&l_run)[C::G],
+                                                float (&o)[C::G][C::EPL]) {
+  constexpr int G = C::G, EPL = C::EPL, LPR = C::LPR, STEPS = C::STEPS;
+  const int lr = lane % LPR;
+  const int row_base = warp * C::RPW + lane / LPR;
 #pragma unroll
   for (int h = 0; h < G; ++h) {
     float mx = s[0][h];
@@ -137,14 +238,14 @@ __device__ __forceinline__ void consume_tile(const unsigned char* __restrict__ k
     for (int off = LPR; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, off));
     const float m_new = fmaxf(m_run[h], mx);
     const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-    const float alpha = exp2f(m_run[h] - m_use);
+    const float alpha = fast_exp2(m_run[h] - m_use);
     m_run[h] = m_new;
     l_run[h] *= alpha;
 #pragma unroll
     for (int i = 0; i < EPL; ++i) o[h][i] *= alpha;
 #pragma unroll
     for (int st = 0; st < STEPS; ++st) {
-      s[st][h] = exp2f(s[st][h] - m_use);
+      s[st][h] = fast_exp2(s[st][h] - m_use);
       l_run[h] += s[st][h];
     }
   }
@@ -165,11 +266,112 @@ __device__ __forceinline__ void consume_tile(const unsigned char* __restrict__ k
   }
 }
 
+// Log-sum-exp merge of the n_act split partials of one (stream, kv head), run by the
+// NT consumer threads of the CTA that took the last ticket.  The (m, l) pairs and the
+// first batch of output partials are requested together; per-head maxima and sums use
+// warp reductions.  `smem` is free shared memory (the ring).
+template <class C>
+__device__ __forceinline__ void combine_splits(const AttnParams& p, int b, int g, int n_act,
+                                               int tid, unsigned char* smem) {
+  constexpr int G = C::G, D = C::D, NT = C::NT, Q4 = C::Q4;
+  constexpr int R = (NT >= Q4) ? NT / Q4 : 1;  // split groups working side by side
+  constexpr int BATCH = 16;                    // partial rows in flight per thread
+  const int Hq = p.n_q_heads;
+  const int lane = tid & 31, warp = tid >> 5;
+  float* sm_w = reinterpret_cast<float*>(smem);  // [G][n_act]: m, then the weights
+  float* sm_l = sm_w + G * n_act;                // [G][n_act]
+  float* sm_L = sm_l + G * n_act;                // [G]
+  float4* sm_acc = reinterpret_cast<float4*>(smem + ((2 * G * n_act + G) * sizeof(float) + 15) / 16 * 16);
+  const int64_t head0 = static_cast<int64_t>(b) * Hq + g * G;  // first q head of the group
+
+  const int qi = tid % Q4;
+  const int r = tid / Q4;
+  const int h = qi / (D / 4);
+  const int d4 = qi - h * (D / 4);
+  const float4* op = reinterpret_cast<const float4*>(p.ws_o) + (head0 + h) * p.n_splits * (D / 4) + d4;
+  float4 v[BATCH];
+#pragma unroll
+  for (int k = 0; k < BATCH; ++k) {
+    const int s = r + k * R;
+    v[k] = (s < n_act) ? __ldcg(op + static_cast<int64_t>(s) * (D / 4)) : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  for (int i = tid; i < G * n_act; i += NT) {
+    const int hh = i / n_act;
+    const int s = i - hh * n_act;
+    const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.ws_ml) + (head0 + hh) * p.n_splits + s);
+    sm_w[i] = ml.x;
+    sm_l[i] = ml.y;
+  }
+  named_barrier(1, NT);
+  // warp hh < G: M = max m, w_s = 2^(m_s - M), L = sum l_s w_s
+  for (int hh = warp; hh < G; hh += C::NC) {
+    float M = -INFINITY;
+    for (int s = lane; s < n_act; s += 32) M = fmaxf(M, sm_w[hh * n_act + s]);
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, off));
+    float L = 0.f;
+    for (int s = lane; s < n_act; s += 32) {
+      const float w = fast_exp2(sm_w[hh * n_act + s] - M);
+      sm_w[hh * n_act + s] = w;
+      L = fmaf(sm_l[hh * n_act + s], w, L);
+    }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) L += __shfl_xor_sync(kFull, L, off);
+    if (lane == 0) sm_L[hh] = L;
+  }
+  named_barrier(1, NT);
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  const float* wh = sm_w + h * n_act;
+#pragma unroll
+  for (int k = 0; k < BATCH; ++k) {
+    const int s = r + k * R;
+    if (s < n_act) {
+      const float w = wh[s];
+      acc.x = fmaf(w, v[k].x, acc.x);
+      acc.y = fmaf(w, v[k].y, acc.y);
+      acc.z = fmaf(w, v[k].z, acc.z);
+      acc.w = fmaf(w, v[k].w, acc.w);
+    }
+  }
+  for (int s0 = r + BATCH * R; s0 < n_act; s0 += BATCH * R) {  // only for very many splits
+#pragma unroll
+    for (int k = 0; k < BATCH; ++k) {
+      const int s = s0 + k * R;
+      v[k] = (s < n_act) ? __ldcg(op + static_cast<int64_t>(s) * (D / 4)) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int k = 0; k < BATCH; ++k) {
+      const int s = s0 + k * R;
+      if (s < n_act) {
+        const float w = wh[s];
+        acc.x = fmaf(w, v[k].x, acc.x);
+        acc.y = fmaf(w, v[k].y, acc.y);
+        acc.z = fmaf(w, v[k].z, acc.z);
+        acc.w = fmaf(w, v[k].w, acc.w);
+      }
+    }
+  }
+  if (R > 1) {
+    sm_acc[r * Q4 + qi] = acc;
+    named_barrier(1, NT);
+  }
+  if (tid < Q4) {
+#pragma unroll 1
+    for (int rr = 1; rr < R; ++rr) {
+      const float4 a = sm_acc[rr * Q4 + qi];
+      acc.x += a.x; acc.y += a.y; acc.z += a.z; acc.w += a.w;
+    }
+    const float L = sm_L[h];
+    reinterpret_cast<float4*>(p.out + (head0 + h) * D)[d4] =
+        make_float4(acc.x / L, acc.y / L, acc.z / L, acc.w / L);
+  }
+}
+
 template <typename KvT, int D, int G, bool FUSED>
-__global__ void __launch_bounds__(Cfg<KvT, D, G>::THREADS, 2)
+__global__ void __launch_bounds__(Cfg<KvT, D, G>::THREADS, (G >= 4 ? 2 : TTS_ATTN_MIN_BLOCKS))
 decode_attn_kernel(const AttnParams p) {
   using C = Cfg<KvT, D, G>;
-  constexpr int EPL = C::EPL, LPR = C::LPR, NC = C::NC, T = C::T;
+  constexpr int EPL = C::EPL, LPR = C::LPR, NC = C::NC, NT = C::NT, T = C::T;
   extern __shared__ __align__(128) unsigned char smem[];
 
   const int split = blockIdx.x;
@@ -189,6 +391,7 @@ decode_attn_kernel(const AttnParams p) {
   int* s_last = reinterpret_cast<int*>(smem + C::flag_off(ns));
 
   if (threadIdx.x == 0) {
+    TTS_STAMP(0);
     for (int s = 0; s < ns; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], NC);
@@ -197,11 +400,11 @@ decode_attn_kernel(const AttnParams p) {
   }
   __syncthreads();
 
-  // The producer may stream cache rows before the preceding kernel finishes only when
-  // the caller has promised that kernel does not write them (TTS_KV_PREFETCH_BEFORE_WAIT).
+  // With TTS_KV_PREFETCH_BEFORE_WAIT the caller has promised that the preceding kernel
+  // writes neither this cache, its block table, cur_len, gamma nor the RoPE table, so
+  // those may be read before the dependency wait.
   const bool early = FUSED && (p.flags & TTS_KV_PREFETCH_BEFORE_WAIT);
-  if (!early || warp < NC) grid_wait();
-  if (warp < NC) grid_launch_dependents();
+  if (!early) grid_wait();
 
   const bool reporter = (split == 0 && g == 0 && threadIdx.x == 0);
   int nv, cache_end;
@@ -210,7 +413,6 @@ decode_attn_kernel(const AttnParams p) {
   if (FUSED) {
     cur = __ldcg(p.lens + b);
     fresh_ok = (cur >= 0 && cur < p.capacity);
-    if (!fresh_ok && reporter) set_err(p.err, TTS_EFLAG_POS_RANGE);
     nv = min(max(cur + 1, 1), p.capacity);
     cache_end = fresh_ok ? cur : nv;
   } else {
@@ -284,25 +486,40 @@ decode_attn_kernel(const AttnParams p) {
   }
 
   // -------------------------------------------------------------------- consumers
-  const int tid = threadIdx.x;  // < NC * 32
+  const int tid = threadIdx.x;  // < NT
   const int lr = lane % LPR;
   const int e0 = lr * EPL;
   const int half = D / 2;
 
-  if (active) {
-    int rope_pos = 0;
-    if (FUSED) {
-      rope_pos = min(max(cur, 0), p.max_pos - 1);
-      if ((cur < 0 || cur >= p.max_pos) && reporter) set_err(p.err, TTS_EFLAG_POS_RANGE);
+  float gq[EPL], gk[EPL];
+  float2 csr[EPL];
+  int rope_pos = 0;
+  if (FUSED) {
+    rope_pos = min(max(cur, 0), p.max_pos - 1);
+    if (early && active) {
+      const float2* cs_row = p.cs + static_cast<int64_t>(rope_pos) * half;
+      load_norm_consts<EPL>(p.gamma_q, cs_row, e0, D, gq, csr);
+      if (has_fresh) load_norm_consts<EPL>(p.gamma_k, cs_row, e0, D, gk, csr);
     }
-    const float2* cs_row = p.cs + static_cast<int64_t>(rope_pos) * half;
+    if (early) grid_wait();
+    if (!fresh_ok && reporter) set_err(p.err, TTS_EFLAG_POS_RANGE);
+    if ((cur < 0 || cur >= p.max_pos) && reporter) set_err(p.err, TTS_EFLAG_POS_RANGE);
+  }
+  grid_launch_dependents();
+  if (tid == 0) TTS_STAMP(1);
 
+  if (active) {
+    if (FUSED && !early) {
+      const float2* cs_row = p.cs + static_cast<int64_t>(rope_pos) * half;
+      load_norm_consts<EPL>(p.gamma_q, cs_row, e0, D, gq, csr);
+      if (has_fresh) load_norm_consts<EPL>(p.gamma_k, cs_row, e0, D, gk, csr);
+    }
     float q[G][EPL];
 #pragma unroll
     for (int h = 0; h < G; ++h) {
       load_row_f32<EPL>(p.q + static_cast<int64_t>(b) * p.q_stride + static_cast<int64_t>(g * G + h) * D,
                         e0, q[h]);
-      if (FUSED) norm_rope_lanes<EPL, LPR>(q[h], p.gamma_q, cs_row, p.eps, e0, D);
+      if (FUSED) norm_rope_regs<EPL, LPR>(q[h], gq, csr, p.eps, e0, D);
 #pragma unroll
       for (int i = 0; i < EPL; ++i) q[h][i] *= p.scale_log2;
     }
@@ -314,7 +531,7 @@ decode_attn_kernel(const AttnParams p) {
       const int64_t roff = static_cast<int64_t>(b) * p.kv_new_stride + static_cast<int64_t>(g) * D;
       load_row_f32<EPL>(p.k_new + roff, e0, kr);
       load_row_f32<EPL>(p.v_new + roff, e0, vr);
-      norm_rope_lanes<EPL, LPR>(kr, p.gamma_k, cs_row, p.eps, e0, D);
+      norm_rope_regs<EPL, LPR>(kr, gk, csr, p.eps, e0, D);
       if (lane < LPR) {
         const uint4 kp = pack_row(kr, static_cast<KvT*>(nullptr));
         const uint4 vp = pack_row(vr, static_cast<KvT*>(nullptr));
@@ -348,31 +565,63 @@ decode_attn_kernel(const AttnParams p) {
       for (int i = 0; i < EPL; ++i) o[h][i] = 0.f;
     }
 
+    if (tid == 0) TTS_STAMP(2);
+    // Tiles are consumed in a two-deep software pipeline: the scores of tile t+1 are
+    // computed in the same basic block as the softmax and P.V of tile t, so the two
+    // dependency chains overlap.  Only the last tile may be partial.
+    constexpr int STEPS = C::STEPS;
+    const int n_full = n_rows / T;
+    const int tail = n_rows - n_full * T;
     bool ok = true;
-    int stage = 0;
-    uint32_t round = 0;
-    for (int t = 0; t < ntiles; ++t) {
-      if (!mbar_wait(&full[stage], round & 1u)) {
-        set_err(p.err, TTS_EFLAG_TIMEOUT);
+    float s_cur[STEPS][G], s_nxt[STEPS][G];
+    if (n_full > 0) {
+      ok = mbar_wait(&full[0], 0u);
+      if (tid == 0) TTS_STAMP(3);
+      if (ok) tile_scores<C, KvT, false>(ring, T, warp, lane, q, s_cur);
+    }
+    for (int t = 0; ok && t + 1 < n_full; ++t) {
+      const int sc = t % ns;
+      const int sn = (t + 1) % ns;
+      if (!mbar_wait(&full[sn], static_cast<uint32_t>((t + 1) / ns) & 1u)) {
         ok = false;
         break;
       }
-      const unsigned char* kt = ring + stage * C::STAGE_BYTES;
-      const unsigned char* vt = kt + C::TILE_BYTES;
-      const int rows = min(T, n_rows - t * T);
-      if (rows == T)
-        consume_tile<C, KvT, false>(kt, vt, T, warp, lane, q, m_run, l_run, o);
-      else
-        consume_tile<C, KvT, true>(kt, vt, rows, warp, lane, q, m_run, l_run, o);
+      tile_scores<C, KvT, false>(ring + sn * C::STAGE_BYTES, T, warp, lane, q, s_nxt);
+      tile_softmax_pv<C, KvT, false>(ring + sc * C::STAGE_BYTES + C::TILE_BYTES, T, warp, lane,
+                                     s_cur, m_run, l_run, o);
       __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[stage]);
-      if (++stage == ns) {
-        stage = 0;
-        ++round;
+      if (lane == 0) mbar_arrive(&empty[sc]);
+#pragma unroll
+      for (int st = 0; st < STEPS; ++st)
+#pragma unroll
+        for (int h = 0; h < G; ++h) s_cur[st][h] = s_nxt[st][h];
+    }
+    if (ok && n_full > 0) {
+      const int sc = (n_full - 1) % ns;
+      tile_softmax_pv<C, KvT, false>(ring + sc * C::STAGE_BYTES + C::TILE_BYTES, T, warp, lane,
+                                     s_cur, m_run, l_run, o);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[sc]);
+    }
+    if (ok && tail > 0) {
+      const int sc = n_full % ns;
+      if (mbar_wait(&full[sc], static_cast<uint32_t>(n_full / ns) & 1u)) {
+        if (n_full == 0 && tid == 0) TTS_STAMP(3);
+        tile_scores<C, KvT, true>(ring + sc * C::STAGE_BYTES, tail, warp, lane, q, s_cur);
+        tile_softmax_pv<C, KvT, true>(ring + sc * C::STAGE_BYTES + C::TILE_BYTES, tail, warp,
+                                      lane, s_cur, m_run, l_run, o);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[sc]);
+      } else {
+        ok = false;
       }
     }
-    if (FUSED && has_fresh && ok)
-      consume_tile<C, KvT, true>(fresh_k, fresh_v, 1, warp, lane, q, m_run, l_run, o);
+    if (!ok) set_err(p.err, TTS_EFLAG_TIMEOUT);
+    if (FUSED && has_fresh && ok) {
+      tile_scores<C, KvT, true>(fresh_k, 1, warp, lane, q, s_cur);
+      tile_softmax_pv<C, KvT, true>(fresh_v, 1, warp, lane, s_cur, m_run, l_run, o);
+    }
+    if (tid == 0) TTS_STAMP(4);
 
     // Merge the row groups of this warp, then the warps of this CTA.
 #pragma unroll
@@ -396,9 +645,9 @@ decode_attn_kernel(const AttnParams p) {
         }
       }
     }
-    named_barrier(1, NC * 32);
+    named_barrier(1, NT);
 
-    for (int idx = tid; idx < G * D; idx += NC * 32) {
+    for (int idx = tid; idx < G * D; idx += NT) {
       const int h = idx / D;
       const int d = idx - h * D;
       float M = -INFINITY;
@@ -418,43 +667,29 @@ decode_attn_kernel(const AttnParams p) {
       } else {
         const int64_t slot = (static_cast<int64_t>(b) * Hq + hq) * p.n_splits + split;
         p.ws_o[slot * D + d] = O;
-        if (d == 0) {
-          p.ws_ml[slot * 2] = M;
-          p.ws_ml[slot * 2 + 1] = L;
-        }
+        if (d == 0) reinterpret_cast<float2*>(p.ws_ml)[slot] = make_float2(M, L);
       }
     }
   }
 
+  if (tid == 0) TTS_STAMP(5);
   if (p.n_splits == 1) return;
 
   // Ticket: the last split of this (stream, kv head) to finish merges all partials.
-  __threadfence();
-  named_barrier(1, NC * 32);
+  named_barrier(1, NT);
   if (tid == 0) {
-    const int prev = atomicAdd(p.ws_cnt + b * Hkv + g, 1);
+    const int prev = atomic_add_acq_rel_gpu(p.ws_cnt + b * Hkv + g, 1);
     *s_last = (prev == p.n_splits - 1) ? 1 : 0;
   }
-  named_barrier(1, NC * 32);
+  named_barrier(1, NT);
+  if (tid == 0) TTS_STAMP(6);
   if (*s_last == 0) return;
-  __threadfence();
   const int n_act = min(p.n_splits, (nv + p.split_len - 1) / p.split_len);
-  for (int idx = tid; idx < G * D; idx += NC * 32) {
-    const int h = idx / D;
-    const int d = idx - h * D;
-    const int hq = g * G + h;
-    const int64_t base = (static_cast<int64_t>(b) * Hq + hq) * p.n_splits;
-    float M = -INFINITY;
-    for (int s = 0; s < n_act; ++s) M = fmaxf(M, __ldcg(p.ws_ml + (base + s) * 2));
-    float L = 0.f, O = 0.f;
-    for (int s = 0; s < n_act; ++s) {
-      const float f = exp2f(__ldcg(p.ws_ml + (base + s) * 2) - M);
-      L = fmaf(__ldcg(p.ws_ml + (base + s) * 2 + 1), f, L);
-      O = fmaf(__ldcg(p.ws_o + (base + s) * D + d), f, O);
-    }
-    p.out[(static_cast<int64_t>(b) * Hq + hq) * D + d] = O / L;
+  combine_splits<C>(p, b, g, n_act, tid, ring);
+  if (tid == 0) {
+    p.ws_cnt[b * Hkv + g] = 0;
+    TTS_STAMP(7);
   }
-  if (tid == 0) p.ws_cnt[b * Hkv + g] = 0;
 }
 
 template <typename KvT, int D, int G, bool FUSED>
@@ -536,5 +771,17 @@ cudaError_t launch_decode_attn(const AttnParams& p, int kv_bf16, int head_dim, i
   }
   return cudaErrorInvalidValue;
 }
+
+#ifdef TTS_TRACE
+// Copies the timeline of the last traced launch to host memory (n_ctas x 8 stamps).
+extern "C" int tts_trace_read(unsigned long long* host, int n_ctas) {
+  if (n_ctas > kTraceCtas) n_ctas = kTraceCtas;
+  return static_cast<int>(cudaMemcpyFromSymbol(host, g_trace, sizeof(unsigned long long) * kTraceSlots * n_ctas));
+}
+extern "C" int tts_trace_clear(void) {
+  static unsigned long long zeros[kTraceCtas][kTraceSlots];
+  return static_cast<int>(cudaMemcpyToSymbol(g_trace, zeros, sizeof(zeros)));
+}
+#endif
 
 }  // namespace tts

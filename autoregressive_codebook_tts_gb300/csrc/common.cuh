@@ -152,11 +152,27 @@ __device__ __forceinline__ __nv_bfloat16 to_cache(float x, __nv_bfloat16*) { ret
 // with EPL consecutive elements starting at e0 = (lane % LPR) * EPL.  The partner of
 // element i (i +- D/2) lives in lane ^ (LPR/2).  All lanes of the warp must call it.
 //   t = x * (mean(x^2) + eps)^(-1/2) * gamma;  rotate (t_i, t_{i+D/2}) by theta_i.
+// gam[i] = gamma[e0 + i]; cs[i] = (cos, sin) of frequency (e0 + i) mod D/2.
 // ---------------------------------------------------------------------------
+template <int EPL>
+__device__ __forceinline__ void load_norm_consts(const float* gamma, const float2* cs_row, int e0,
+                                                 int D, float (&gam)[EPL], float2 (&cs)[EPL]) {
+  const int half = D / 2;
+  const int f0 = e0 < half ? e0 : e0 - half;
+#pragma unroll
+  for (int i = 0; i < EPL; i += 4) {
+    const float4 gv = __ldcg(reinterpret_cast<const float4*>(gamma + e0 + i));
+    gam[i] = gv.x; gam[i + 1] = gv.y; gam[i + 2] = gv.z; gam[i + 3] = gv.w;
+    const float4 c0 = __ldcg(reinterpret_cast<const float4*>(cs_row + f0 + i));
+    const float4 c1 = __ldcg(reinterpret_cast<const float4*>(cs_row + f0 + i + 2));
+    cs[i] = make_float2(c0.x, c0.y); cs[i + 1] = make_float2(c0.z, c0.w);
+    cs[i + 2] = make_float2(c1.x, c1.y); cs[i + 3] = make_float2(c1.z, c1.w);
+  }
+}
+
 template <int EPL, int LPR>
-__device__ __forceinline__ void norm_rope_lanes(float (&x)[EPL], const float* __restrict__ gamma,
-                                                const float2* __restrict__ cs_row, float eps,
-                                                int e0, int D) {
+__device__ __forceinline__ void norm_rope_regs(float (&x)[EPL], const float (&gam)[EPL],
+                                               const float2 (&cs)[EPL], float eps, int e0, int D) {
   float ss = 0.f;
 #pragma unroll
   for (int i = 0; i < EPL; ++i) ss = fmaf(x[i], x[i], ss);
@@ -165,17 +181,22 @@ __device__ __forceinline__ void norm_rope_lanes(float (&x)[EPL], const float* __
   const float r = 1.0f / sqrtf(ss / static_cast<float>(D) + eps);
   float t[EPL];
 #pragma unroll
-  for (int i = 0; i < EPL; ++i) t[i] = x[i] * r * __ldg(gamma + e0 + i);
-  const int half = D / 2;
-  const bool lo = e0 < half;
-  const int f0 = lo ? e0 : e0 - half;
+  for (int i = 0; i < EPL; ++i) t[i] = x[i] * r * gam[i];
+  const bool lo = e0 < D / 2;
 #pragma unroll
   for (int i = 0; i < EPL; ++i) {
     const float pt = __shfl_xor_sync(kFull, t[i], LPR / 2);
-    const float2 cs = __ldg(cs_row + f0 + i);
     // lower half: t*c - partner*s ; upper half: partner*s + t*c
-    x[i] = lo ? fmaf(t[i], cs.x, -pt * cs.y) : fmaf(pt, cs.y, t[i] * cs.x);
+    x[i] = lo ? fmaf(t[i], cs[i].x, -pt * cs[i].y) : fmaf(pt, cs[i].y, t[i] * cs[i].x);
   }
+}
+
+// Ticket counter with acquire-release semantics at GPU scope.  Called by one thread
+// after a CTA barrier, it publishes every store the CTA made before the barrier.
+__device__ __forceinline__ int atomic_add_acq_rel_gpu(int* p, int v) {
+  int old;
+  asm volatile("atom.add.acq_rel.gpu.global.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
 }
 
 }  // namespace tts

@@ -121,8 +121,11 @@ __global__ void __launch_bounds__(kNormWarps * 32) qk_norm_rope_kernel(const Nor
     x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
   }
   // Dead row groups run the same shuffles on zeros (gamma/cs reads stay in bounds).
-  norm_rope_lanes<EPL, LPR>(x, live ? gamma : p.gamma_q, p.cs + static_cast<int64_t>(pos) * (D / 2),
-                            p.eps, e0, D);
+  float gam[EPL];
+  float2 cs[EPL];
+  load_norm_consts<EPL>(live ? gamma : p.gamma_q, p.cs + static_cast<int64_t>(pos) * (D / 2), e0, D,
+                        gam, cs);
+  norm_rope_regs<EPL, LPR>(x, gam, cs, p.eps, e0, D);
   if (live) *reinterpret_cast<float4*>(ptr + e0) = make_float4(x[0], x[1], x[2], x[3]);
 }
 

@@ -14,7 +14,7 @@ import os
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "_build", "libttsdecode.so")
+LIB_PATH = os.environ.get("TTS_LIBRARY") or os.path.join(_HERE, "_build", "libttsdecode.so")
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(
