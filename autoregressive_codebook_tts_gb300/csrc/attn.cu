@@ -77,6 +77,11 @@
 #ifndef TTS_ATTN_MIN_BLOCKS
 #define TTS_ATTN_MIN_BLOCKS 3
 #endif
+// Lanes that share one K/V row (8: a quarter warp per row, 16 bytes per lane per
+// vector, so a row reduction takes three shuffle levels).
+#ifndef TTS_ATTN_LPR
+#define TTS_ATTN_LPR 8
+#endif
 
 namespace tts {
 
@@ -117,8 +122,13 @@ struct Cfg {
   static constexpr int D = D_;
   static constexpr int G = G_;
   static constexpr int kElem = sizeof(KvT);
-  static constexpr int EPL = 16 / kElem;      // elements per lane per 16-byte vector
-  static constexpr int LPR = D / EPL;         // lanes per row
+  static constexpr int VE = 16 / kElem;       // elements per 16-byte vector
+  // lanes per row: a quarter warp by default; half a warp for groups of four q heads
+  // (whose per-lane q and output arrays would otherwise not fit in registers)
+  static constexpr int LPR_WANT = (G_ >= 4 && TTS_ATTN_LPR < 16) ? 16 : TTS_ATTN_LPR;
+  static constexpr int LPR = (LPR_WANT < D / VE) ? LPR_WANT : D / VE;
+  static constexpr int EPL = D / LPR;         // elements per lane per row
+  static constexpr int VEC = EPL / VE;        // 16-byte vectors per lane per row
   static constexpr int RPI = 32 / LPR;        // rows per warp step
   static constexpr int ROW_BYTES = D * kElem;
   static constexpr int T = Tune<KvT, D>::T;   // rows per stage
@@ -132,29 +142,39 @@ struct Cfg {
   static constexpr int THREADS = NT + 32;
   static constexpr int Q4 = G * D / 4;        // float4 columns of one (stream, kv head) output
   static_assert(RPW % RPI == 0 && STEPS >= 1, "tile rows must split evenly over warp steps");
-  static_assert(LPR >= 2 && LPR <= 32, "row must span 2..32 lanes");
+  static_assert(LPR >= 2 && LPR <= 32 && EPL % VE == 0, "row must span 2..32 lanes");
   static_assert(NT % Q4 == 0 || Q4 % NT == 0, "combine layout");
 
+  // Shared memory: the ring of ns stages, mbarriers (full[NS], empty[NS], gather),
+  // the fresh K/V row, the per-warp merge scratch, a flag word, and (cluster mode)
+  // the gather area where the cluster's splits deposit their partials in rank 0.
+  static constexpr int PART = G * (D + 2);    // floats of one split's partial (o, m, l per head)
   static constexpr size_t bar_off(int ns) { return static_cast<size_t>(ns) * STAGE_BYTES; }
-  static constexpr size_t fresh_off(int ns) { return bar_off(ns) + 2 * NS * sizeof(uint64_t); }
+  static constexpr size_t fresh_off(int ns) { return bar_off(ns) + ((2 * NS + 1) * sizeof(uint64_t) + 15) / 16 * 16; }
   static constexpr size_t scratch_off(int ns) { return fresh_off(ns) + 2 * ROW_BYTES; }
   static constexpr size_t flag_off(int ns) {
-    return scratch_off(ns) + static_cast<size_t>(NC) * G * (D + 2) * sizeof(float);
+    return scratch_off(ns) + static_cast<size_t>(NC) * PART * sizeof(float);
   }
-  static constexpr size_t smem_bytes(int ns) { return flag_off(ns) + 16; }
+  static constexpr size_t gather_off(int ns) { return flag_off(ns) + 16; }
+  static constexpr size_t smem_bytes(int ns, int cluster) {
+    return gather_off(ns) + static_cast<size_t>(cluster > 1 ? cluster : 0) * PART * sizeof(float);
+  }
 };
 
-// f32 row data starting at element e0 of a global row (EPL floats, 16-byte loads).
-template <int EPL>
-__device__ __forceinline__ void load_row_f32(const float* row, int e0, float (&x)[EPL]) {
+// The lane's elements of an f32 global row, in the lane layout of the cache rows:
+// element e of vector j is row element (j * LPR + lr) * VE + e.
+template <int VE, int VEC, int LPR>
+__device__ __forceinline__ void load_row_f32(const float* row, int lr, float (&x)[VE * VEC]) {
 #pragma unroll
-  for (int i = 0; i < EPL; i += 4) {
-    const float4 v = __ldcg(reinterpret_cast<const float4*>(row + e0 + i));
-    x[i] = v.x; x[i + 1] = v.y; x[i + 2] = v.z; x[i + 3] = v.w;
-  }
+  for (int j = 0; j < VEC; ++j)
+#pragma unroll
+    for (int e = 0; e < VE; e += 4) {
+      const float4 v = __ldcg(reinterpret_cast<const float4*>(row + (j * LPR + lr) * VE + e));
+      x[j * VE + e] = v.x; x[j * VE + e + 1] = v.y; x[j * VE + e + 2] = v.z; x[j * VE + e + 3] = v.w;
+    }
 }
 
-__device__ __forceinline__ uint4 pack_row(const float (&x)[4], float*) {
+__device__ __forceinline__ uint4 pack_vec(const float* x, float*) {
   return make_uint4(__float_as_uint(x[0]), __float_as_uint(x[1]), __float_as_uint(x[2]),
                     __float_as_uint(x[3]));
 }
@@ -162,7 +182,7 @@ __device__ __forceinline__ uint32_t pack2_bf16(float a, float b) {
   const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);  // .x = a (low half), round-to-nearest-even
   return *reinterpret_cast<const uint32_t*>(&h);
 }
-__device__ __forceinline__ uint4 pack_row(const float (&x)[8], __nv_bfloat16*) {
+__device__ __forceinline__ uint4 pack_vec(const float* x, __nv_bfloat16*) {
   return make_uint4(pack2_bf16(x[0], x[1]), pack2_bf16(x[2], x[3]), pack2_bf16(x[4], x[5]),
                     pack2_bf16(x[6], x[7]));
 }
@@ -172,6 +192,25 @@ __device__ __forceinline__ float fast_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+// The lane's elements of one staged K or V row (zeros for rows at or past nrows).
+template <class C, typename KvT, bool PARTIAL>
+__device__ __forceinline__ void load_smem_row(const unsigned char* __restrict__ tile, int row,
+                                              int nrows, int lr, float (&f)[C::EPL]) {
+  constexpr int VE = C::VE;
+  if (!PARTIAL || row < nrows) {
+#pragma unroll
+    for (int j = 0; j < C::VEC; ++j) {
+      float part[VE];
+      KvVec<KvT>::unpack(lds128(tile + row * C::ROW_BYTES + (j * C::LPR + lr) * 16), part);
+#pragma unroll
+      for (int e = 0; e < VE; ++e) f[j * VE + e] = part[e];
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < C::EPL; ++i) f[i] = 0.f;
+  }
 }
 
 // Phase 1 of a tile for this warp: q.K scores of its rows (log2 units), reduced over
@@ -187,12 +226,7 @@ __device__ __forceinline__ void tile_scores(const unsigned char* __restrict__ kt
   for (int st = 0; st < STEPS; ++st) {
     const int row = row_base + st * C::RPI;
     float kf[EPL];
-    if (!PARTIAL || row < nrows) {
-      KvVec<KvT>::unpack(lds128(kt + row * C::ROW_BYTES + lr * 16), kf);
-    } else {
-#pragma unroll
-      for (int i = 0; i < EPL; ++i) kf[i] = 0.f;
-    }
+    load_smem_row<C, KvT, PARTIAL>(kt, row, nrows, lr, kf);
 #pragma unroll
     for (int h = 0; h < G; ++h) {
       // two partial sums halve the FMA dependency chain
@@ -253,12 +287,7 @@ __device__ __forceinline__ void tile_softmax_pv(const unsigned char* __restrict_
   for (int st = 0; st < STEPS; ++st) {
     const int row = row_base + st * C::RPI;
     float vf[EPL];
-    if (!PARTIAL || row < nrows) {
-      KvVec<KvT>::unpack(lds128(vt + row * C::ROW_BYTES + lr * 16), vf);
-    } else {
-#pragma unroll
-      for (int i = 0; i < EPL; ++i) vf[i] = 0.f;
-    }
+    load_smem_row<C, KvT, PARTIAL>(vt, row, nrows, lr, vf);
 #pragma unroll
     for (int h = 0; h < G; ++h)
 #pragma unroll
@@ -385,10 +414,15 @@ decode_attn_kernel(const AttnParams p) {
   unsigned char* ring = smem;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::bar_off(ns));
   uint64_t* empty = full + C::NS;
+  uint64_t* gbar = empty + C::NS;
   unsigned char* fresh_k = smem + C::fresh_off(ns);
   unsigned char* fresh_v = fresh_k + C::ROW_BYTES;
   float* scratch = reinterpret_cast<float*>(smem + C::scratch_off(ns));
   int* s_last = reinterpret_cast<int*>(smem + C::flag_off(ns));
+  float* gather = reinterpret_cast<float*>(smem + C::gather_off(ns));
+  // Cluster mode: the n_splits CTAs of one (stream, kv head) form a cluster and merge
+  // their partials in rank 0's shared memory (rank == split).
+  const bool clustered = p.cluster > 1;
 
   if (threadIdx.x == 0) {
     TTS_STAMP(0);
@@ -396,9 +430,12 @@ decode_attn_kernel(const AttnParams p) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], NC);
     }
+    if (clustered) mbar_init(gbar, p.cluster - 1);
     mbar_init_fence();
   }
-  __syncthreads();
+  // every CTA's gather barrier is initialised before any peer can arrive on it
+  if (clustered) cluster_sync_all();
+  else __syncthreads();
 
   // With TTS_KV_PREFETCH_BEFORE_WAIT the caller has promised that the preceding kernel
   // writes neither this cache, its block table, cur_len, gamma nor the RoPE table, so
@@ -487,8 +524,8 @@ decode_attn_kernel(const AttnParams p) {
 
   // -------------------------------------------------------------------- consumers
   const int tid = threadIdx.x;  // < NT
+  constexpr int VE = C::VE, VEC = C::VEC;
   const int lr = lane % LPR;
-  const int e0 = lr * EPL;
   const int half = D / 2;
 
   float gq[EPL], gk[EPL];
@@ -498,8 +535,8 @@ decode_attn_kernel(const AttnParams p) {
     rope_pos = min(max(cur, 0), p.max_pos - 1);
     if (early && active) {
       const float2* cs_row = p.cs + static_cast<int64_t>(rope_pos) * half;
-      load_norm_consts<EPL>(p.gamma_q, cs_row, e0, D, gq, csr);
-      if (has_fresh) load_norm_consts<EPL>(p.gamma_k, cs_row, e0, D, gk, csr);
+      load_norm_consts<VE, VEC, LPR>(p.gamma_q, cs_row, lr, D, gq, csr);
+      if (has_fresh) load_norm_consts<VE, VEC, LPR>(p.gamma_k, cs_row, lr, D, gk, csr);
     }
     if (early) grid_wait();
     if (!fresh_ok && reporter) set_err(p.err, TTS_EFLAG_POS_RANGE);
@@ -511,15 +548,15 @@ decode_attn_kernel(const AttnParams p) {
   if (active) {
     if (FUSED && !early) {
       const float2* cs_row = p.cs + static_cast<int64_t>(rope_pos) * half;
-      load_norm_consts<EPL>(p.gamma_q, cs_row, e0, D, gq, csr);
-      if (has_fresh) load_norm_consts<EPL>(p.gamma_k, cs_row, e0, D, gk, csr);
+      load_norm_consts<VE, VEC, LPR>(p.gamma_q, cs_row, lr, D, gq, csr);
+      if (has_fresh) load_norm_consts<VE, VEC, LPR>(p.gamma_k, cs_row, lr, D, gk, csr);
     }
     float q[G][EPL];
 #pragma unroll
     for (int h = 0; h < G; ++h) {
-      load_row_f32<EPL>(p.q + static_cast<int64_t>(b) * p.q_stride + static_cast<int64_t>(g * G + h) * D,
-                        e0, q[h]);
-      if (FUSED) norm_rope_regs<EPL, LPR>(q[h], gq, csr, p.eps, e0, D);
+      load_row_f32<VE, VEC, LPR>(
+          p.q + static_cast<int64_t>(b) * p.q_stride + static_cast<int64_t>(g * G + h) * D, lr, q[h]);
+      if (FUSED) norm_rope_regs<VE, VEC, LPR>(q[h], gq, csr, p.eps, lr, D);
 #pragma unroll
       for (int i = 0; i < EPL; ++i) q[h][i] *= p.scale_log2;
     }
@@ -529,14 +566,18 @@ decode_attn_kernel(const AttnParams p) {
     if (FUSED && has_fresh && warp == 0) {
       float kr[EPL], vr[EPL];
       const int64_t roff = static_cast<int64_t>(b) * p.kv_new_stride + static_cast<int64_t>(g) * D;
-      load_row_f32<EPL>(p.k_new + roff, e0, kr);
-      load_row_f32<EPL>(p.v_new + roff, e0, vr);
-      norm_rope_regs<EPL, LPR>(kr, gk, csr, p.eps, e0, D);
+      load_row_f32<VE, VEC, LPR>(p.k_new + roff, lr, kr);
+      load_row_f32<VE, VEC, LPR>(p.v_new + roff, lr, vr);
+      norm_rope_regs<VE, VEC, LPR>(kr, gk, csr, p.eps, lr, D);
       if (lane < LPR) {
-        const uint4 kp = pack_row(kr, static_cast<KvT*>(nullptr));
-        const uint4 vp = pack_row(vr, static_cast<KvT*>(nullptr));
-        *reinterpret_cast<uint4*>(fresh_k + lr * 16) = kp;
-        *reinterpret_cast<uint4*>(fresh_v + lr * 16) = vp;
+        uint4 kp[VEC], vp[VEC];
+#pragma unroll
+        for (int j = 0; j < VEC; ++j) {
+          kp[j] = pack_vec(kr + j * VE, static_cast<KvT*>(nullptr));
+          vp[j] = pack_vec(vr + j * VE, static_cast<KvT*>(nullptr));
+          *reinterpret_cast<uint4*>(fresh_k + (j * LPR + lr) * 16) = kp[j];
+          *reinterpret_cast<uint4*>(fresh_v + (j * LPR + lr) * 16) = vp[j];
+        }
         size_t off;
         bool write = true;
         if (!p.paged) {
@@ -549,8 +590,12 @@ decode_attn_kernel(const AttnParams p) {
                  (cur & (p.page_size - 1))) * C::ROW_BYTES;
         }
         if (write) {
-          *reinterpret_cast<uint4*>(static_cast<unsigned char*>(p.k_cache_w) + off + lr * 16) = kp;
-          *reinterpret_cast<uint4*>(static_cast<unsigned char*>(p.v_cache_w) + off + lr * 16) = vp;
+#pragma unroll
+          for (int j = 0; j < VEC; ++j) {
+            const size_t o16 = off + (j * LPR + lr) * 16;
+            *reinterpret_cast<uint4*>(static_cast<unsigned char*>(p.k_cache_w) + o16) = kp[j];
+            *reinterpret_cast<uint4*>(static_cast<unsigned char*>(p.v_cache_w) + o16) = vp[j];
+          }
         }
       }
       __syncwarp();
@@ -638,7 +683,9 @@ decode_attn_kernel(const AttnParams p) {
       for (int h = 0; h < G; ++h) {
         float* dst = scratch + (warp * G + h) * (D + 2);
 #pragma unroll
-        for (int i = 0; i < EPL; ++i) dst[e0 + i] = o[h][i];
+        for (int j = 0; j < VEC; ++j)
+#pragma unroll
+          for (int e = 0; e < VE; ++e) dst[(j * LPR + lr) * VE + e] = o[h][j * VE + e];
         if (lane == 0) {
           dst[D] = m_run[h];
           dst[D + 1] = l_run[h];
@@ -664,6 +711,21 @@ decode_attn_kernel(const AttnParams p) {
       const int hq = g * G + h;
       if (p.n_splits == 1) {
         p.out[(static_cast<int64_t>(b) * Hq + hq) * D + d] = O / L;
+      } else if (clustered) {
+        float* slot = gather + (split * G + h) * (D + 2);
+        if (split == 0) {
+          slot[d] = O;
+          if (d == 0) {
+            slot[D] = M;
+            slot[D + 1] = L;
+          }
+        } else {
+          st_cluster_f32(map_shared_rank(slot + d, 0), O);
+          if (d == 0) {
+            st_cluster_f32(map_shared_rank(slot + D, 0), M);
+            st_cluster_f32(map_shared_rank(slot + D + 1, 0), L);
+          }
+        }
       } else {
         const int64_t slot = (static_cast<int64_t>(b) * Hq + hq) * p.n_splits + split;
         p.ws_o[slot * D + d] = O;
@@ -674,6 +736,38 @@ decode_attn_kernel(const AttnParams p) {
 
   if (tid == 0) TTS_STAMP(5);
   if (p.n_splits == 1) return;
+
+  if (clustered) {
+    // Partials travel over distributed shared memory; rank 0 waits (bounded) for the
+    // other ranks' arrivals, which release their stores, and merges from its own smem.
+    named_barrier(1, NT);
+    if (split != 0) {
+      if (tid == 0) mbar_arrive_remote(map_shared_rank(gbar, 0));
+      return;
+    }
+    if (!mbar_wait_cluster(gbar, 0u, 8 * kWaitLimitCycles)) {
+      if (tid == 0) set_err(p.err, TTS_EFLAG_TIMEOUT);
+      return;
+    }
+    if (tid == 0) TTS_STAMP(6);
+    const int n_act = min(p.n_splits, (nv + p.split_len - 1) / p.split_len);
+    for (int idx = tid; idx < G * D; idx += NT) {
+      const int h = idx / D;
+      const int d = idx - h * D;
+      float M = -INFINITY;
+      for (int s2 = 0; s2 < n_act; ++s2) M = fmaxf(M, gather[(s2 * G + h) * (D + 2) + D]);
+      float L = 0.f, O = 0.f;
+      for (int s2 = 0; s2 < n_act; ++s2) {
+        const float* src = gather + (s2 * G + h) * (D + 2);
+        const float f = fast_exp2(src[D] - M);
+        L = fmaf(src[D + 1], f, L);
+        O = fmaf(src[d], f, O);
+      }
+      p.out[(static_cast<int64_t>(b) * Hq + g * G + h) * D + d] = O / L;
+    }
+    if (tid == 0) TTS_STAMP(7);
+    return;
+  }
 
   // Ticket: the last split of this (stream, kv head) to finish merges all partials.
   named_barrier(1, NT);
@@ -692,31 +786,60 @@ decode_attn_kernel(const AttnParams p) {
   }
 }
 
+constexpr int kMaxCluster = 16;
+
 template <typename KvT, int D, int G, bool FUSED>
-cudaError_t launch_one(const AttnParams& p, cudaStream_t s) {
+cudaError_t launch_one(const AttnParams& p_in, cudaStream_t s) {
   using C = Cfg<KvT, D, G>;
   auto kern = decode_attn_kernel<KvT, D, G, FUSED>;
-  const size_t smem = C::smem_bytes(p.n_stages);
-  static int configured_for = -1;  // device whose max-dynamic-smem attribute is set
+  // Per device: the kernel attributes, and the largest cluster of this kernel the GPU
+  // can co-schedule (cluster mode is used only up to that size).
+  static int configured_for = -1;
+  static int max_cluster = 1;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (configured_for != dev) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(C::smem_bytes(C::NS)));
+                             static_cast<int>(C::smem_bytes(C::NS, kMaxCluster)));
     if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t q = {};
+    q.gridDim = dim3(kMaxCluster, 1, 1);
+    q.blockDim = dim3(C::THREADS);
+    q.dynamicSmemBytes = C::smem_bytes(C::NS, kMaxCluster);
+    cudaLaunchAttribute qa[1];
+    qa[0].id = cudaLaunchAttributeClusterDimension;
+    qa[0].val.clusterDim.x = kMaxCluster;
+    qa[0].val.clusterDim.y = 1;
+    qa[0].val.clusterDim.z = 1;
+    q.attrs = qa;
+    q.numAttrs = 1;
+    int mc = 1;
+    if (cudaOccupancyMaxPotentialClusterSize(&mc, kern, &q) != cudaSuccess) {
+      cudaGetLastError();
+      mc = 8;  // portable cluster size
+    }
+    max_cluster = mc < 1 ? 1 : (mc > kMaxCluster ? kMaxCluster : mc);
     configured_for = dev;
   }
+  AttnParams p = p_in;
+  p.cluster = (p.n_splits > 1 && p.n_splits <= max_cluster && p.ws_o != nullptr) ? p.n_splits : 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.n_splits, p.n_kv_heads, p.B);
   cfg.blockDim = dim3(C::THREADS);
-  cfg.dynamicSmemBytes = smem;
+  cfg.dynamicSmemBytes = C::smem_bytes(p.n_stages, p.cluster);
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = p.cluster > 1 ? p.cluster : 1;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = p.cluster > 1 ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
@@ -739,9 +862,9 @@ AttnGeometry geometry_of() {
 template <typename KvT, int D>
 size_t smem_of(int group, int ns) {
   switch (group) {
-    case 1: return Cfg<KvT, D, 1>::smem_bytes(ns);
-    case 2: return Cfg<KvT, D, 2>::smem_bytes(ns);
-    case 4: return Cfg<KvT, D, 4>::smem_bytes(ns);
+    case 1: return Cfg<KvT, D, 1>::smem_bytes(ns, kMaxCluster);
+    case 2: return Cfg<KvT, D, 2>::smem_bytes(ns, kMaxCluster);
+    case 4: return Cfg<KvT, D, 4>::smem_bytes(ns, kMaxCluster);
     default: return 0;
   }
 }

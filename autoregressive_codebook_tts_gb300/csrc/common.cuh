@@ -148,31 +148,44 @@ __device__ __forceinline__ float to_cache(float x, float*) { return x; }
 __device__ __forceinline__ __nv_bfloat16 to_cache(float x, __nv_bfloat16*) { return __float2bfloat16_rn(x); }
 
 // ---------------------------------------------------------------------------
-// Per-head RMSNorm + rotate-half RoPE on a row held by a group of LPR lanes, each
-// with EPL consecutive elements starting at e0 = (lane % LPR) * EPL.  The partner of
-// element i (i +- D/2) lives in lane ^ (LPR/2).  All lanes of the warp must call it.
-//   t = x * (mean(x^2) + eps)^(-1/2) * gamma;  rotate (t_i, t_{i+D/2}) by theta_i.
-// gam[i] = gamma[e0 + i]; cs[i] = (cos, sin) of frequency (e0 + i) mod D/2.
+// Per-head RMSNorm + rotate-half RoPE on a row of D elements held by a group of LPR
+// lanes.  Lane lr of the group holds VEC vectors of VE elements; element e of vector
+// j is row element (j * LPR + lr) * VE + e, so D = VEC * LPR * VE.  All lanes of the
+// warp must call it (the sum of squares is reduced over the group with shuffles).
+//   t = x * (mean(x^2) + eps)^(-1/2) * gamma
+//   (t_i, t_{i+D/2}) -> (t_i c - t_{i+D/2} s, t_i s + t_{i+D/2} c),  (c, s) of theta_i
+// With VEC >= 2 the partner i + D/2 of element i sits in the same lane (vector
+// j + VEC/2); with VEC == 1 it sits in lane lr ^ (LPR/2).
+// gam[k] = gamma of the lane's element k; cs[k] = (cos, sin) of frequency
+// (row index of element k) mod D/2.
 // ---------------------------------------------------------------------------
-template <int EPL>
-__device__ __forceinline__ void load_norm_consts(const float* gamma, const float2* cs_row, int e0,
-                                                 int D, float (&gam)[EPL], float2 (&cs)[EPL]) {
+template <int VE, int VEC, int LPR>
+__device__ __forceinline__ void load_norm_consts(const float* gamma, const float2* cs_row, int lr,
+                                                 int D, float (&gam)[VE * VEC],
+                                                 float2 (&cs)[VE * VEC]) {
   const int half = D / 2;
-  const int f0 = e0 < half ? e0 : e0 - half;
 #pragma unroll
-  for (int i = 0; i < EPL; i += 4) {
-    const float4 gv = __ldcg(reinterpret_cast<const float4*>(gamma + e0 + i));
-    gam[i] = gv.x; gam[i + 1] = gv.y; gam[i + 2] = gv.z; gam[i + 3] = gv.w;
-    const float4 c0 = __ldcg(reinterpret_cast<const float4*>(cs_row + f0 + i));
-    const float4 c1 = __ldcg(reinterpret_cast<const float4*>(cs_row + f0 + i + 2));
-    cs[i] = make_float2(c0.x, c0.y); cs[i + 1] = make_float2(c0.z, c0.w);
-    cs[i + 2] = make_float2(c1.x, c1.y); cs[i + 3] = make_float2(c1.z, c1.w);
+  for (int j = 0; j < VEC; ++j) {
+    const int idx = (j * LPR + lr) * VE;
+    const int f = idx < half ? idx : idx - half;
+#pragma unroll
+    for (int e = 0; e < VE; e += 4) {
+      const float4 gv = __ldcg(reinterpret_cast<const float4*>(gamma + idx + e));
+      gam[j * VE + e] = gv.x; gam[j * VE + e + 1] = gv.y;
+      gam[j * VE + e + 2] = gv.z; gam[j * VE + e + 3] = gv.w;
+      const float4 c0 = __ldcg(reinterpret_cast<const float4*>(cs_row + f + e));
+      const float4 c1 = __ldcg(reinterpret_cast<const float4*>(cs_row + f + e + 2));
+      cs[j * VE + e] = make_float2(c0.x, c0.y); cs[j * VE + e + 1] = make_float2(c0.z, c0.w);
+      cs[j * VE + e + 2] = make_float2(c1.x, c1.y); cs[j * VE + e + 3] = make_float2(c1.z, c1.w);
+    }
   }
 }
 
-template <int EPL, int LPR>
-__device__ __forceinline__ void norm_rope_regs(float (&x)[EPL], const float (&gam)[EPL],
-                                               const float2 (&cs)[EPL], float eps, int e0, int D) {
+template <int VE, int VEC, int LPR>
+__device__ __forceinline__ void norm_rope_regs(float (&x)[VE * VEC], const float (&gam)[VE * VEC],
+                                               const float2 (&cs)[VE * VEC], float eps, int lr,
+                                               int D) {
+  constexpr int EPL = VE * VEC;
   float ss = 0.f;
 #pragma unroll
   for (int i = 0; i < EPL; ++i) ss = fmaf(x[i], x[i], ss);
@@ -182,13 +195,75 @@ __device__ __forceinline__ void norm_rope_regs(float (&x)[EPL], const float (&ga
   float t[EPL];
 #pragma unroll
   for (int i = 0; i < EPL; ++i) t[i] = x[i] * r * gam[i];
-  const bool lo = e0 < D / 2;
+  if (VEC >= 2) {
 #pragma unroll
-  for (int i = 0; i < EPL; ++i) {
-    const float pt = __shfl_xor_sync(kFull, t[i], LPR / 2);
-    // lower half: t*c - partner*s ; upper half: partner*s + t*c
-    x[i] = lo ? fmaf(t[i], cs[i].x, -pt * cs[i].y) : fmaf(pt, cs[i].y, t[i] * cs[i].x);
+    for (int j = 0; j < VEC / 2; ++j)
+#pragma unroll
+      for (int e = 0; e < VE; ++e) {
+        const int a = j * VE + e, c = (j + VEC / 2) * VE + e;
+        x[a] = fmaf(t[a], cs[a].x, -t[c] * cs[a].y);
+        x[c] = fmaf(t[a], cs[a].y, t[c] * cs[a].x);
+      }
+  } else {
+    const bool lo = lr < LPR / 2;
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+      const float pt = __shfl_xor_sync(kFull, t[i], LPR / 2);
+      // lower half: t*c - partner*s ; upper half: partner*s + t*c
+      x[i] = lo ? fmaf(t[i], cs[i].x, -pt * cs[i].y) : fmaf(pt, cs[i].y, t[i] * cs[i].x);
+    }
   }
+}
+
+// ---------------------------------------------------------------------------
+// Thread-block clusters: rank, cluster-wide barrier, distributed shared memory.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// All threads of all CTAs of the cluster; also a barrier for this CTA.
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t map_shared_rank(const void* local, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(local)), "r"(rank));
+  return r;
+}
+
+__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+
+// Arrive on an mbarrier of another CTA of the cluster, releasing this CTA's prior
+// shared-memory writes (ordered before this call by a CTA barrier) at cluster scope.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
+  return ok != 0;
+}
+
+// Bounded wait for a phase completed by other CTAs of the cluster (acquire).
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, long long limit) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const long long start = clock64();
+  while (!mbar_try_wait_cluster(bar, parity)) {
+    if (clock64() - start > limit) return false;
+  }
+  return true;
 }
 
 // Ticket counter with acquire-release semantics at GPU scope.  Called by one thread

@@ -78,6 +78,7 @@ struct AttnParams {
   int n_splits;         // grid.x
   int split_len;        // positions per split, a multiple of the tile
   int n_stages;         // pipeline depth actually used (<= the kernel's maximum)
+  int cluster;          // set by the launcher: splits per cluster (>1 = cluster merge)
   uint32_t flags;
   int32_t* err;
 };

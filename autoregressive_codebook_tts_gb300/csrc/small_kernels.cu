@@ -123,9 +123,9 @@ __global__ void __launch_bounds__(kNormWarps * 32) qk_norm_rope_kernel(const Nor
   // Dead row groups run the same shuffles on zeros (gamma/cs reads stay in bounds).
   float gam[EPL];
   float2 cs[EPL];
-  load_norm_consts<EPL>(live ? gamma : p.gamma_q, p.cs + static_cast<int64_t>(pos) * (D / 2), e0, D,
-                        gam, cs);
-  norm_rope_regs<EPL, LPR>(x, gam, cs, p.eps, e0, D);
+  load_norm_consts<EPL, 1, LPR>(live ? gamma : p.gamma_q, p.cs + static_cast<int64_t>(pos) * (D / 2),
+                                lane % LPR, D, gam, cs);
+  norm_rope_regs<EPL, 1, LPR>(x, gam, cs, p.eps, lane % LPR, D);
   if (live) *reinterpret_cast<float4*>(ptr + e0) = make_float4(x[0], x[1], x[2], x[3]);
 }
 
