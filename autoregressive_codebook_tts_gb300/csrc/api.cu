@@ -258,11 +258,11 @@ int32_t tts_decode_attn_default_splits(const tts_kv_desc* d) {
   const int pairs = d->B * d->n_kv_heads;
   // About four CTAs' worth of window per SM over the grid, at most 16 splits so that a
   // (stream, kv head) fits one thread-block cluster and merges through distributed
-  // shared memory, and windows cut into pieces of at most 1024 positions so ragged
+  // shared memory, and windows cut into pieces of at most 512 positions so ragged
   // batches still balance.
   int s = (4 * sm_count() + pairs - 1) / pairs;
   if (s > 16) s = 16;
-  const int by_len = (d->capacity + 1023) / 1024;
+  const int by_len = (d->capacity + 511) / 512;
   if (s < by_len) s = by_len;
   if (s > max_splits) s = max_splits;
   if (s < 1) s = 1;

@@ -42,7 +42,7 @@
 #define TTS_F32_128_T 16
 #endif
 #ifndef TTS_F32_128_NS
-#define TTS_F32_128_NS 4
+#define TTS_F32_128_NS 8
 #endif
 #ifndef TTS_F32_128_NC
 #define TTS_F32_128_NC 4
@@ -51,7 +51,7 @@
 #define TTS_BF16_128_T 32
 #endif
 #ifndef TTS_BF16_128_NS
-#define TTS_BF16_128_NS 4
+#define TTS_BF16_128_NS 8
 #endif
 #ifndef TTS_BF16_128_NC
 #define TTS_BF16_128_NC 4
@@ -60,7 +60,7 @@
 #define TTS_F32_64_T 32
 #endif
 #ifndef TTS_F32_64_NS
-#define TTS_F32_64_NS 4
+#define TTS_F32_64_NS 8
 #endif
 #ifndef TTS_F32_64_NC
 #define TTS_F32_64_NC 4
@@ -69,7 +69,16 @@
 #define TTS_BF16_64_T 64
 #endif
 #ifndef TTS_BF16_64_NS
-#define TTS_BF16_64_NS 4
+#define TTS_BF16_64_NS 8
+#endif
+// Ring stages actually used: a grid of many CTAs keeps three per SM (64 KB rings);
+// a single-wave cluster grid keeps one per SM plus room for the next launch's CTA, and
+// needs the deeper ring to keep enough bytes in flight on its own.
+#ifndef TTS_STAGES_WAVES
+#define TTS_STAGES_WAVES 4
+#endif
+#ifndef TTS_STAGES_CLUSTER
+#define TTS_STAGES_CLUSTER 5
 #endif
 #ifndef TTS_BF16_64_NC
 #define TTS_BF16_64_NC 4
@@ -751,19 +760,28 @@ decode_attn_kernel(const AttnParams p) {
     }
     if (tid == 0) TTS_STAMP(6);
     const int n_act = min(p.n_splits, (nv + p.split_len - 1) / p.split_len);
+    // per head: weights 2^(m_s - M) and the sum L, one warp per head (lanes over splits)
+    float* sm_w = scratch;  // [G][16] weights, then [G] sums (the merge scratch is free now)
+    for (int h = warp; h < G; h += NC) {
+      const float m = lane < n_act ? gather[(lane * G + h) * (D + 2) + D] : -INFINITY;
+      float M = m;
+#pragma unroll
+      for (int off = 16; off >= 1; off >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, off));
+      const float w = lane < n_act ? fast_exp2(m - M) : 0.f;
+      float L = lane < n_act ? w * gather[(lane * G + h) * (D + 2) + D + 1] : 0.f;
+#pragma unroll
+      for (int off = 16; off >= 1; off >>= 1) L += __shfl_xor_sync(kFull, L, off);
+      if (lane < 16) sm_w[h * 16 + lane] = w;
+      if (lane == 0) sm_w[G * 16 + h] = L;
+    }
+    named_barrier(1, NT);
     for (int idx = tid; idx < G * D; idx += NT) {
       const int h = idx / D;
       const int d = idx - h * D;
-      float M = -INFINITY;
-      for (int s2 = 0; s2 < n_act; ++s2) M = fmaxf(M, gather[(s2 * G + h) * (D + 2) + D]);
-      float L = 0.f, O = 0.f;
-      for (int s2 = 0; s2 < n_act; ++s2) {
-        const float* src = gather + (s2 * G + h) * (D + 2);
-        const float f = fast_exp2(src[D] - M);
-        L = fmaf(src[D + 1], f, L);
-        O = fmaf(src[d], f, O);
-      }
-      p.out[(static_cast<int64_t>(b) * Hq + g * G + h) * D + d] = O / L;
+      float O = 0.f;
+#pragma unroll 4
+      for (int s2 = 0; s2 < n_act; ++s2) O = fmaf(gather[(s2 * G + h) * (D + 2) + d], sm_w[h * 16 + s2], O);
+      p.out[(static_cast<int64_t>(b) * Hq + g * G + h) * D + d] = O / sm_w[G * 16 + h];
     }
     if (tid == 0) TTS_STAMP(7);
     return;
@@ -825,7 +843,18 @@ cudaError_t launch_one(const AttnParams& p_in, cudaStream_t s) {
     configured_for = dev;
   }
   AttnParams p = p_in;
-  p.cluster = (p.n_splits > 1 && p.n_splits <= max_cluster && p.ws_o != nullptr) ? p.n_splits : 0;
+  // Clusters pay off when the whole grid is one wave of one CTA per SM (few streams);
+  // ragged multi-wave grids keep the ticket merge, which schedules CTAs freely.
+  static int n_sm = 0;
+  if (n_sm == 0 && cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    cudaGetLastError();
+    n_sm = 1;
+  }
+  const long long ctas = static_cast<long long>(p.n_splits) * p.n_kv_heads * p.B;
+  const bool one_wave = ctas <= n_sm;
+  p.cluster = (p.n_splits > 1 && p.n_splits <= max_cluster && p.ws_o != nullptr && one_wave) ? p.n_splits : 0;
+  const int want = p.cluster > 1 ? TTS_STAGES_CLUSTER : TTS_STAGES_WAVES;
+  if (p.n_stages > want) p.n_stages = want;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.n_splits, p.n_kv_heads, p.B);
   cfg.blockDim = dim3(C::THREADS);
