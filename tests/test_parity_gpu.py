@@ -261,6 +261,10 @@ def test_decode_attn_paged_equals_contiguous(tts):
 
 
 def test_decode_attn_batched_equals_per_stream(tts):
+    """Stream b of a batched call equals a call on stream b alone.  The two launches may
+    take different split-merge paths (a one-stream grid fits one wave and merges in a
+    thread-block cluster; the batched grid merges through the workspace), which differ
+    only in the f32 rounding order of the merge, so the bound is 1e-6 per row."""
     w = W.workload("batched", B=5, layers=1)
     L = Layer(w, seed=43, poison=False)
     desc = L.desc(tts)
@@ -276,7 +280,7 @@ def test_decode_attn_batched_equals_per_stream(tts):
         tts.tts_decode_attn(L.d_q[b:b + 1], L.d_K[b:b + 1], L.d_V[b:b + 1], d1, nv[b:b + 1],
                             scale_of(w1), o1, ws1, 8)
         torch.cuda.synchronize()
-        assert torch.equal(o1[0].cpu(), out[b].cpu())
+        assert row_rel_err(o1[0].cpu().numpy(), out[b].cpu().numpy()) <= 1e-6
 
 
 def test_decode_attn_flags_bad_n_valid_and_pages(tts):
