@@ -279,13 +279,18 @@ __device__ __forceinline__ void tile_softmax_pv(const unsigned char* __restrict_
     for (int st = 1; st < STEPS; ++st) mx = fmaxf(mx, s[st][h]);
 #pragma unroll
     for (int off = LPR; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, off));
-    const float m_new = fmaxf(m_run[h], mx);
-    const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-    const float alpha = fast_exp2(m_run[h] - m_use);
-    m_run[h] = m_new;
-    l_run[h] *= alpha;
+    // Lazy rescaling: the reference maximum m_run moves only when the tile maximum
+    // exceeds it by more than 8 (log2 units), so the o/l rescale is rare; until then the
+    // weights 2^(s - m_run) stay below 2^8.  m_run and mx are warp-uniform, so is the
+    // branch.  The result is exact up to rounding: o and l share the reference.
+    if (mx > m_run[h] + 8.0f) {
+      const float alpha = fast_exp2(m_run[h] - mx);  // 0 on the first tile (m_run = -inf)
+      m_run[h] = mx;
+      l_run[h] *= alpha;
 #pragma unroll
-    for (int i = 0; i < EPL; ++i) o[h][i] *= alpha;
+      for (int i = 0; i < EPL; ++i) o[h][i] *= alpha;
+    }
+    const float m_use = (m_run[h] == -INFINITY) ? 0.f : m_run[h];
 #pragma unroll
     for (int st = 0; st < STEPS; ++st) {
       s[st][h] = fast_exp2(s[st][h] - m_use);
@@ -628,15 +633,21 @@ decode_attn_kernel(const AttnParams p) {
     const int tail = n_rows - n_full * T;
     bool ok = true;
     float s_cur[STEPS][G], s_nxt[STEPS][G];
+    int sc = 0;          // ring stage of the current tile
+    uint32_t pc = 0u;    // parity of its phase
     if (n_full > 0) {
       ok = mbar_wait(&full[0], 0u);
       if (tid == 0) TTS_STAMP(3);
       if (ok) tile_scores<C, KvT, false>(ring, T, warp, lane, q, s_cur);
     }
     for (int t = 0; ok && t + 1 < n_full; ++t) {
-      const int sc = t % ns;
-      const int sn = (t + 1) % ns;
-      if (!mbar_wait(&full[sn], static_cast<uint32_t>((t + 1) / ns) & 1u)) {
+      int sn = sc + 1;
+      uint32_t pn = pc;
+      if (sn == ns) {
+        sn = 0;
+        pn ^= 1u;
+      }
+      if (!mbar_wait(&full[sn], pn)) {
         ok = false;
         break;
       }
@@ -649,17 +660,21 @@ decode_attn_kernel(const AttnParams p) {
       for (int st = 0; st < STEPS; ++st)
 #pragma unroll
         for (int h = 0; h < G; ++h) s_cur[st][h] = s_nxt[st][h];
+      sc = sn;
+      pc = pn;
     }
     if (ok && n_full > 0) {
-      const int sc = (n_full - 1) % ns;
       tile_softmax_pv<C, KvT, false>(ring + sc * C::STAGE_BYTES + C::TILE_BYTES, T, warp, lane,
                                      s_cur, m_run, l_run, o);
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[sc]);
+      if (++sc == ns) {
+        sc = 0;
+        pc ^= 1u;
+      }
     }
     if (ok && tail > 0) {
-      const int sc = n_full % ns;
-      if (mbar_wait(&full[sc], static_cast<uint32_t>(n_full / ns) & 1u)) {
+      if (mbar_wait(&full[sc], pc)) {
         if (n_full == 0 && tid == 0) TTS_STAMP(3);
         tile_scores<C, KvT, true>(ring + sc * C::STAGE_BYTES, tail, warp, lane, q, s_cur);
         tile_softmax_pv<C, KvT, true>(ring + sc * C::STAGE_BYTES + C::TILE_BYTES, tail, warp,
