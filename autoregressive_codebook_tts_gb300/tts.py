@@ -37,6 +37,7 @@ EXPORTED = [
     "tts_abi_version", "tts_abi_min_version", "tts_status_str", "tts_frame_embed",
     "tts_rope_table", "tts_qk_norm_rope", "tts_kv_set_rows", "tts_decode_attn_workspace_size",
     "tts_decode_attn_default_splits", "tts_workspace_init", "tts_decode_attn", "tts_decode_step",
+    "tts_decode_step_noalloc",
 ]
 
 
@@ -73,6 +74,8 @@ _sigs = {
                          _P, _P], _I32),
     "tts_decode_step": ([_P, _P, _P, _I64, _P, _P, _F, _P, _I32, _P, _P,
                          ctypes.POINTER(TtsKvDesc), _P, _F, _P, _P, _SZ, _I32, _P, _P], _I32),
+    "tts_decode_step_noalloc": ([_P, _P, _P, _I64, _P, _P, _F, _P, _I32, _P, _P,
+                                 ctypes.POINTER(TtsKvDesc), _P, _F, _P, _I32, _P, _P], _I32),
 }
 for _name, (_args, _ret) in _sigs.items():
     _fn = getattr(_lib, _name)
@@ -215,6 +218,20 @@ def tts_decode_step(q, k, v, gamma_q, gamma_k, eps, cs, max_pos, k_cache, v_cach
                                 ctypes.byref(desc), _ptr(cur_len), float(scale), _ptr(out),
                                 _ptr(ws), 0 if ws is None else ws.numel() * ws.element_size(),
                                 n_splits, _ptr(err_flag), _stream(stream)), "tts_decode_step")
+
+
+def tts_decode_step_noalloc(q, k, v, gamma_q, gamma_k, eps, cs, max_pos, k_cache, v_cache,
+                            desc: TtsKvDesc, cur_len, scale, out, n_splits=0, err_flag=None,
+                            stream=None):
+    """tts_decode_step with the library's built-in scratch instead of a workspace (for
+    callers that cannot allocate device memory); see include/tts_decode.h."""
+    stride = _row_stride(q)
+    assert k.stride(0) == stride and v.stride(0) == stride, "q, k, v rows must share one stride"
+    _check(_lib.tts_decode_step_noalloc(_ptr(q), _ptr(k), _ptr(v), stride, _ptr(gamma_q),
+                                        _ptr(gamma_k), float(eps), _ptr(cs), max_pos,
+                                        _ptr(k_cache), _ptr(v_cache), ctypes.byref(desc),
+                                        _ptr(cur_len), float(scale), _ptr(out), n_splits,
+                                        _ptr(err_flag), _stream(stream)), "tts_decode_step_noalloc")
 
 
 def default_scale(head_dim: int) -> float:

@@ -238,6 +238,29 @@ tts_status tts_decode_step(const float* q, const float* k, const float* v, int64
                            float scale, float* out, void* workspace, size_t ws_bytes,
                            int32_t n_splits, int32_t* err_flag, void* stream);
 
+/* ---------------------------------------------------------------------------
+ * tts_decode_step without a workspace argument.  The pages have no counterpart: this
+ * is a convenience of this library for callers that cannot allocate device memory when
+ * they run a step -- e.g. a real-time audio callback that must not enter an allocator,
+ * or a host framework that only lends out the tensors it owns.  The caller still passes
+ * every input and output; the split-KV scratch comes from a fixed 4 MiB device array
+ * inside the library (held on every GPU that loads the library until the process
+ * exits), so a configuration needing more (tts_decode_attn_workspace_size() > 4 MiB)
+ * is rejected with TTS_ERR_WORKSPACE.  The first call on a device looks the array's
+ * device address up (a synchronous runtime call), so make that first call before any
+ * stream capture.  Each call first clears the part of the array it uses (one small
+ * kernel on `stream`) and then runs the step.  All calls share the one array: calls
+ * that can overlap on the GPU (different streams, or different threads) race on it and
+ * must be serialised by the caller.  Arguments and results are otherwise those of
+ * tts_decode_step.
+ * ------------------------------------------------------------------------- */
+tts_status tts_decode_step_noalloc(const float* q, const float* k, const float* v,
+                                   int64_t row_stride, const float* gamma_q,
+                                   const float* gamma_k, float eps, const float* rope_cs,
+                                   int32_t rope_max_pos, void* k_cache, void* v_cache,
+                                   const tts_kv_desc* desc, const int32_t* cur_len, float scale,
+                                   float* out, int32_t n_splits, int32_t* err_flag, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
