@@ -10,12 +10,13 @@
 //   * grid = (split, kv head, stream).  One CTA streams a contiguous range of one kv
 //     head's positions and serves all Hq/Hkv q heads of the group from the same bytes,
 //     so each K/V element is read from HBM once.
-//   * One producer warp feeds a ring of shared-memory stages with 1-D bulk copies
+//   * Two producer warps feed a ring of shared-memory stages with 1-D bulk copies
 //     (the TMA engine) of whole K and V tiles; the cache is head-major, so a tile of a
 //     contiguous cache is one copy (a paged cache: one copy per page piece).  Copies
 //     complete on per-stage mbarriers; consumer warps release stages on a second set.
-//     The ring is kept small (64 KB) so that three CTAs share an SM and the next
-//     launch's CTAs find room while this one drains.
+//     One bulk copy costs about the same time whatever its size up to tens of KB and
+//     copies issued by one thread run one after another, so tiles are 16 KB per copy
+//     and K and V are issued by two producer warps side by side.
 //   * Consumer warps split each tile's rows.  A row is covered by LPR lanes with 16
 //     bytes each (4 f32 or 8 bf16 elements); q.k is reduced across those lanes with
 //     xor shuffles; each warp keeps its own online-softmax state (running max in log2
@@ -39,28 +40,28 @@
 // Tile geometry per (cache dtype, head_dim): rows per stage (T), ring stages (NS),
 // consumer warps (NC).  Overridable at build time for tuning sweeps.
 #ifndef TTS_F32_128_T
-#define TTS_F32_128_T 16
+#define TTS_F32_128_T 32
 #endif
 #ifndef TTS_F32_128_NS
-#define TTS_F32_128_NS 8
+#define TTS_F32_128_NS 4
 #endif
 #ifndef TTS_F32_128_NC
 #define TTS_F32_128_NC 4
 #endif
 #ifndef TTS_BF16_128_T
-#define TTS_BF16_128_T 32
+#define TTS_BF16_128_T 64
 #endif
 #ifndef TTS_BF16_128_NS
-#define TTS_BF16_128_NS 8
+#define TTS_BF16_128_NS 4
 #endif
 #ifndef TTS_BF16_128_NC
 #define TTS_BF16_128_NC 4
 #endif
 #ifndef TTS_F32_64_T
-#define TTS_F32_64_T 32
+#define TTS_F32_64_T 64
 #endif
 #ifndef TTS_F32_64_NS
-#define TTS_F32_64_NS 8
+#define TTS_F32_64_NS 4
 #endif
 #ifndef TTS_F32_64_NC
 #define TTS_F32_64_NC 4
@@ -69,22 +70,22 @@
 #define TTS_BF16_64_T 64
 #endif
 #ifndef TTS_BF16_64_NS
-#define TTS_BF16_64_NS 8
+#define TTS_BF16_64_NS 4
 #endif
-// Ring stages actually used: a grid of many CTAs keeps three per SM (64 KB rings);
-// a single-wave cluster grid keeps one per SM plus room for the next launch's CTA, and
-// needs the deeper ring to keep enough bytes in flight on its own.
+// Ring stages actually used (each stage is a 16 KB K tile plus a 16 KB V tile for the
+// 128-wide heads): three in a grid of many CTAs (two CTAs per SM); two in a single-wave
+// cluster grid, so that the next launch's CTA fits beside each running one.
 #ifndef TTS_STAGES_WAVES
-#define TTS_STAGES_WAVES 4
+#define TTS_STAGES_WAVES 3
 #endif
 #ifndef TTS_STAGES_CLUSTER
-#define TTS_STAGES_CLUSTER 5
+#define TTS_STAGES_CLUSTER 2
 #endif
 #ifndef TTS_BF16_64_NC
 #define TTS_BF16_64_NC 4
 #endif
 #ifndef TTS_ATTN_MIN_BLOCKS
-#define TTS_ATTN_MIN_BLOCKS 3
+#define TTS_ATTN_MIN_BLOCKS 2
 #endif
 // Lanes that share one K/V row (8: a quarter warp per row, 16 bytes per lane per
 // vector, so a row reduction takes three shuffle levels).
@@ -148,7 +149,7 @@ struct Cfg {
   static constexpr int STEPS = RPW / RPI;
   static constexpr int TILE_BYTES = T * ROW_BYTES;
   static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
-  static constexpr int THREADS = NT + 32;
+  static constexpr int THREADS = NT + 64;      // consumers + two producer warps
   static constexpr int Q4 = G * D / 4;        // float4 columns of one (stream, kv head) output
   static_assert(RPW % RPI == 0 && STEPS >= 1, "tile rows must split evenly over warp steps");
   static_assert(LPR >= 2 && LPR <= 32 && EPL % VE == 0, "row must span 2..32 lanes");
@@ -441,7 +442,7 @@ decode_attn_kernel(const AttnParams p) {
   if (threadIdx.x == 0) {
     TTS_STAMP(0);
     for (int s = 0; s < ns; ++s) {
-      mbar_init(&full[s], 1);
+      mbar_init(&full[s], 2);  // one arrival from each producer warp, plus the bytes
       mbar_init(&empty[s], NC);
     }
     if (clustered) mbar_init(gbar, p.cluster - 1);
@@ -478,49 +479,56 @@ decode_attn_kernel(const AttnParams p) {
   const bool active = r0 < nv;
   const int ntiles = (n_rows + T - 1) / T;
 
-  if (warp == NC) {
-    // ------------------------------------------------------------------ producer
-    if (lane == 0 && ntiles > 0) {
+  if (warp >= NC) {
+    // ----------------------------------------------------------------- producers
+    // Warp NC streams the K tiles, warp NC+1 the V tiles: bulk copies issued by
+    // different warps proceed side by side, while one thread's copies run one after
+    // another.  A paged tile's page pieces are issued by consecutive lanes.
+    const int pw = warp - NC;
+    if (ntiles > 0) {
       const uint64_t pol = l2_evict_first_policy();
-      const unsigned char* kc = static_cast<const unsigned char*>(p.k_cache);
-      const unsigned char* vc = static_cast<const unsigned char*>(p.v_cache);
+      const unsigned char* src = static_cast<const unsigned char*>(pw == 0 ? p.k_cache : p.v_cache);
       const int32_t* bt = p.paged ? p.block_table + static_cast<int64_t>(b) * p.bt_stride : nullptr;
       int issued = 0;
       int stage = 0;
       uint32_t round = 0;
       for (int t = 0; t < ntiles; ++t) {
-        if (t >= ns && !mbar_wait(&empty[stage], (round & 1u) ^ 1u)) {
-          set_err(p.err, TTS_EFLAG_TIMEOUT);
-          break;
+        if (t >= ns) {
+          int ok = 1;
+          if (lane == 0) ok = mbar_wait(&empty[stage], (round & 1u) ^ 1u) ? 1 : 0;
+          if (__shfl_sync(kFull, ok, 0) == 0) {
+            if (lane == 0) set_err(p.err, TTS_EFLAG_TIMEOUT);
+            break;
+          }
         }
         const int row0 = r0 + t * T;
         const int rows = min(T, r0 + n_rows - row0);
-        const uint32_t bytes = static_cast<uint32_t>(rows) * C::ROW_BYTES;
-        unsigned char* kd = ring + stage * C::STAGE_BYTES;
-        unsigned char* vd = kd + C::TILE_BYTES;
-        mbar_arrive_expect_tx(&full[stage], 2u * bytes);
+        unsigned char* dst = ring + stage * C::STAGE_BYTES + pw * C::TILE_BYTES;
+        if (lane == 0) mbar_arrive_expect_tx(&full[stage], static_cast<uint32_t>(rows) * C::ROW_BYTES);
+        __syncwarp();
         if (!p.paged) {
-          const size_t off =
-              ((static_cast<size_t>(b) * Hkv + g) * p.capacity + row0) * C::ROW_BYTES;
-          bulk_g2s(kd, kc + off, bytes, &full[stage], pol);
-          bulk_g2s(vd, vc + off, bytes, &full[stage], pol);
+          if (lane == 0) {
+            const size_t off =
+                ((static_cast<size_t>(b) * Hkv + g) * p.capacity + row0) * C::ROW_BYTES;
+            bulk_g2s(dst, src + off, static_cast<uint32_t>(rows) * C::ROW_BYTES, &full[stage], pol);
+          }
         } else {
-          int r = row0;
           const int re = row0 + rows;
-          while (r < re) {
-            int page = __ldcg(bt + (r >> p.page_shift));
+          const int page0 = row0 & ~(p.page_size - 1);
+          for (int i = lane;; i += 32) {
+            const int start = (i == 0) ? row0 : page0 + i * p.page_size;
+            if (start >= re) break;
+            int page = __ldcg(bt + (start >> p.page_shift));
             if (page < 0 || page >= p.n_pages) {
               set_err(p.err, TTS_EFLAG_PAGE);
               page = 0;
             }
-            const int slot = r & (p.page_size - 1);
-            const int n = min(p.page_size - slot, re - r);
+            const int slot = start & (p.page_size - 1);
+            const int n = min(p.page_size - slot, re - start);
             const size_t off =
                 ((static_cast<size_t>(page) * Hkv + g) * p.page_size + slot) * C::ROW_BYTES;
-            const uint32_t nb = static_cast<uint32_t>(n) * C::ROW_BYTES;
-            bulk_g2s(kd + (r - row0) * C::ROW_BYTES, kc + off, nb, &full[stage], pol);
-            bulk_g2s(vd + (r - row0) * C::ROW_BYTES, vc + off, nb, &full[stage], pol);
-            r += n;
+            bulk_g2s(dst + (start - row0) * C::ROW_BYTES, src + off,
+                     static_cast<uint32_t>(n) * C::ROW_BYTES, &full[stage], pol);
           }
         }
         ++issued;
@@ -530,8 +538,9 @@ decode_attn_kernel(const AttnParams p) {
         }
       }
       // Do not leave while copies into this CTA's shared memory may be in flight.
-      for (int t = max(0, issued - ns); t < issued; ++t)
-        mbar_wait(&full[t % ns], static_cast<uint32_t>(t / ns) & 1u);
+      if (lane == 0)
+        for (int t = max(0, issued - ns); t < issued; ++t)
+          mbar_wait(&full[t % ns], static_cast<uint32_t>(t / ns) & 1u);
     }
     return;
   }
