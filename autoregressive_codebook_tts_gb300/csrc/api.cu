@@ -256,14 +256,20 @@ int32_t tts_decode_attn_default_splits(const tts_kv_desc* d) {
   const AttnGeometry geo = attn_geometry(d->kv_dtype == TTS_BF16, d->head_dim);
   const int max_splits = (d->capacity + geo.tile_rows - 1) / geo.tile_rows;
   const int pairs = d->B * d->n_kv_heads;
-  // About four CTAs' worth of window per SM over the grid, at most 16 splits so that a
-  // (stream, kv head) fits one thread-block cluster and merges through distributed
-  // shared memory, and windows cut into pieces of at most 512 positions so ragged
-  // batches still balance.
-  int s = (4 * sm_count() + pairs - 1) / pairs;
-  if (s > 16) s = 16;
-  const int by_len = (d->capacity + 511) / 512;
-  if (s < by_len) s = by_len;
+  const int sms = sm_count();
+  int s;
+  if (pairs <= 16) {
+    // Few (stream, kv head) pairs: one thread-block cluster per pair, sized to leave
+    // about 40% of the SMs free so the next launch's CTAs can start streaming there.
+    s = (6 * sms) / (10 * pairs);
+    if (s > 16) s = 16;
+    if (s < 2) s = 2;
+  } else {
+    // Many pairs: windows cut into pieces of at most 512 positions (ragged batches
+    // balance; the partials merge through the workspace).
+    s = (d->capacity + 511) / 512;
+    if (s < 1) s = 1;
+  }
   if (s > max_splits) s = max_splits;
   if (s < 1) s = 1;
   return s;

@@ -73,13 +73,13 @@
 #define TTS_BF16_64_NS 4
 #endif
 // Ring stages actually used (each stage is a 16 KB K tile plus a 16 KB V tile for the
-// 128-wide heads): three in a grid of many CTAs (two CTAs per SM); two in a single-wave
-// cluster grid, so that the next launch's CTA fits beside each running one.
+// 128-wide heads): three in a grid of many CTAs (two CTAs per SM); four in a cluster
+// grid, which has fewer CTAs than SMs, so the next launch's CTAs start on the idle SMs.
 #ifndef TTS_STAGES_WAVES
 #define TTS_STAGES_WAVES 3
 #endif
 #ifndef TTS_STAGES_CLUSTER
-#define TTS_STAGES_CLUSTER 2
+#define TTS_STAGES_CLUSTER 4
 #endif
 #ifndef TTS_BF16_64_NC
 #define TTS_BF16_64_NC 4
