@@ -165,9 +165,18 @@ struct Cfg {
   static constexpr size_t flag_off(int ns) {
     return scratch_off(ns) + static_cast<size_t>(NC) * PART * sizeof(float);
   }
-  static constexpr size_t gather_off(int ns) { return flag_off(ns) + 16; }
-  static constexpr size_t smem_bytes(int ns, int cluster) {
+  // merge of up to kCombSplits partials (workspace path) or 16 (cluster path)
+  static constexpr int kCombSplits = 256;
+  static constexpr size_t COMB_BYTES =
+      ((2 * G * kCombSplits + G) * sizeof(float) + 15) / 16 * 16 + NT * 16;
+  static constexpr size_t comb_off(int ns) { return flag_off(ns) + 16; }
+  static constexpr size_t gather_off(int ns) { return comb_off(ns) + COMB_BYTES; }
+  static constexpr size_t list_off(int ns, int cluster) {
     return gather_off(ns) + static_cast<size_t>(cluster > 1 ? cluster : 0) * PART * sizeof(float);
+  }
+  // persistent mode: prefix sums of the work list, B + 1 ints
+  static constexpr size_t smem_bytes(int ns, int cluster, int list_ints = 0) {
+    return list_off(ns, cluster) + static_cast<size_t>(list_ints) * sizeof(int);
   }
 };
 
@@ -411,16 +420,56 @@ __device__ __forceinline__ void combine_splits(const AttnParams& p, int b, int g
   }
 }
 
+// One unit of work: the rows [r0, r0 + split_len) of one (stream, kv head).
+struct Item {
+  int b, g, split;
+  int nv;         // window length (clamped)
+  int cur;        // fused: position of the new row
+  bool fresh_ok;  // fused: cur is a valid position
+  int r0, n_rows, ntiles;
+  bool has_fresh;
+  int n_act;      // splits of this stream that hold rows of the window
+};
+
+template <bool FUSED>
+__device__ __forceinline__ Item make_item(const AttnParams& p, int T, int b, int g, int split, int raw) {
+  Item it;
+  it.b = b;
+  it.g = g;
+  it.split = split;
+  int cache_end;
+  if (FUSED) {
+    it.cur = raw;
+    it.fresh_ok = raw >= 0 && raw < p.capacity;
+    it.nv = min(max(raw + 1, 1), p.capacity);
+    cache_end = it.fresh_ok ? raw : it.nv;
+  } else {
+    it.cur = 0;
+    it.fresh_ok = false;
+    it.nv = min(max(raw, 1), p.capacity);
+    cache_end = it.nv;
+  }
+  it.r0 = split * p.split_len;
+  it.n_rows = max(0, min(it.r0 + p.split_len, cache_end) - it.r0);
+  it.has_fresh = FUSED && it.fresh_ok && it.cur >= it.r0 && it.cur < it.r0 + p.split_len;
+  it.ntiles = (it.n_rows + T - 1) / T;
+  it.n_act = min(p.n_splits, (it.nv + p.split_len - 1) / p.split_len);
+  return it;
+}
+
+__device__ __forceinline__ int n_active(const AttnParams& p, int raw, bool fused) {
+  const int nv = fused ? min(max(raw + 1, 1), p.capacity) : min(max(raw, 1), p.capacity);
+  return min(p.n_splits, (nv + p.split_len - 1) / p.split_len);
+}
+
 template <typename KvT, int D, int G, bool FUSED>
 __global__ void __launch_bounds__(Cfg<KvT, D, G>::THREADS, (G >= 4 ? 2 : TTS_ATTN_MIN_BLOCKS))
 decode_attn_kernel(const AttnParams p) {
   using C = Cfg<KvT, D, G>;
   constexpr int EPL = C::EPL, LPR = C::LPR, NC = C::NC, NT = C::NT, T = C::T;
+  constexpr int VE = C::VE, VEC = C::VEC, STEPS = C::STEPS;
   extern __shared__ __align__(128) unsigned char smem[];
 
-  const int split = blockIdx.x;
-  const int g = blockIdx.y;
-  const int b = blockIdx.z;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int ns = p.n_stages;
@@ -434,10 +483,14 @@ decode_attn_kernel(const AttnParams p) {
   unsigned char* fresh_v = fresh_k + C::ROW_BYTES;
   float* scratch = reinterpret_cast<float*>(smem + C::scratch_off(ns));
   int* s_last = reinterpret_cast<int*>(smem + C::flag_off(ns));
+  unsigned char* comb = smem + C::comb_off(ns);
+  int* s_pre = reinterpret_cast<int*>(smem + C::list_off(ns, p.cluster));  // persistent: [B+1]
   float* gather = reinterpret_cast<float*>(smem + C::gather_off(ns));
   // Cluster mode: the n_splits CTAs of one (stream, kv head) form a cluster and merge
   // their partials in rank 0's shared memory (rank == split).
   const bool clustered = p.cluster > 1;
+  // Persistent mode: a fixed grid whose CTAs walk a list of the active items only.
+  const bool persistent = p.persistent != 0;
 
   if (threadIdx.x == 0) {
     TTS_STAMP(0);
@@ -458,65 +511,96 @@ decode_attn_kernel(const AttnParams p) {
   const bool early = FUSED && (p.flags & TTS_KV_PREFETCH_BEFORE_WAIT);
   if (!early) grid_wait();
 
-  const bool reporter = (split == 0 && g == 0 && threadIdx.x == 0);
-  int nv, cache_end;
-  bool fresh_ok = false;
-  int cur = 0;
-  if (FUSED) {
-    cur = __ldcg(p.lens + b);
-    fresh_ok = (cur >= 0 && cur < p.capacity);
-    nv = min(max(cur + 1, 1), p.capacity);
-    cache_end = fresh_ok ? cur : nv;
+  // Work list.  Persistent: item i -> (stream b, kv head g, split) over the active
+  // splits only, prefix sums of Hkv * n_act[b] in shared memory.  Otherwise one item,
+  // the CTA's own (split, g, b).
+  int n_items;
+  if (persistent) {
+    if (warp == 0) {
+      int carry = 0;
+      for (int b0 = 0; b0 < p.B; b0 += 32) {
+        const int bb = b0 + lane;
+        int v = bb < p.B ? Hkv * n_active(p, __ldcg(p.lens + bb), FUSED) : 0;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+          const int u = __shfl_up_sync(kFull, v, off);
+          if (lane >= off) v += u;
+        }
+        if (bb < p.B) s_pre[bb + 1] = carry + v;
+        carry += __shfl_sync(kFull, v, 31);
+      }
+      if (lane == 0) s_pre[0] = 0;
+    }
+    __syncthreads();
+    n_items = s_pre[p.B];
   } else {
-    nv = __ldcg(p.lens + b);
-    if ((nv < 1 || nv > p.capacity) && reporter) set_err(p.err, TTS_EFLAG_NVALID);
-    nv = min(max(nv, 1), p.capacity);
-    cache_end = nv;
+    n_items = 1;
   }
-  const int r0 = split * p.split_len;
-  const int n_rows = max(0, min(r0 + p.split_len, cache_end) - r0);
-  const bool has_fresh = FUSED && fresh_ok && cur >= r0 && cur < r0 + p.split_len;
-  const bool active = r0 < nv;
-  const int ntiles = (n_rows + T - 1) / T;
+  auto item_at = [&](int i) -> Item {
+    int b, g, split;
+    if (persistent) {
+      int lo = 0, hi = p.B;  // largest b with s_pre[b] <= i
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (s_pre[mid] <= i) lo = mid; else hi = mid;
+      }
+      b = lo;
+      const int r = i - s_pre[b];
+      g = r % Hkv;
+      split = r / Hkv;
+    } else {
+      b = blockIdx.z;
+      g = blockIdx.y;
+      split = blockIdx.x;
+    }
+    return make_item<FUSED>(p, T, b, g, split, __ldcg(p.lens + b));
+  };
+  const int i_first = persistent ? blockIdx.x : 0;
+  const int i_step = persistent ? gridDim.x : 1;
 
   if (warp >= NC) {
     // ----------------------------------------------------------------- producers
     // Warp NC streams the K tiles, warp NC+1 the V tiles: bulk copies issued by
     // different warps proceed side by side, while one thread's copies run one after
-    // another.  A paged tile's page pieces are issued by consecutive lanes.
+    // another.  A paged tile's page pieces are issued by consecutive lanes.  The ring
+    // runs on across items, so the next item's tiles stream in while this one drains.
     const int pw = warp - NC;
-    if (ntiles > 0) {
-      const uint64_t pol = l2_evict_first_policy();
-      const unsigned char* src = static_cast<const unsigned char*>(pw == 0 ? p.k_cache : p.v_cache);
-      const int32_t* bt = p.paged ? p.block_table + static_cast<int64_t>(b) * p.bt_stride : nullptr;
-      int issued = 0;
-      int stage = 0;
-      uint32_t round = 0;
-      for (int t = 0; t < ntiles; ++t) {
-        if (t >= ns) {
-          int ok = 1;
-          if (lane == 0) ok = mbar_wait(&empty[stage], (round & 1u) ^ 1u) ? 1 : 0;
-          if (__shfl_sync(kFull, ok, 0) == 0) {
+    const uint64_t pol = l2_evict_first_policy();
+    const unsigned char* src = static_cast<const unsigned char*>(pw == 0 ? p.k_cache : p.v_cache);
+    int issued = 0;
+    int stage = 0;
+    uint32_t round = 0;
+    bool ok = true;
+    for (int i = i_first; ok && i < n_items; i += i_step) {
+      const Item it = item_at(i);
+      if (!persistent && it.split >= it.n_act) break;  // outside the window
+      const int32_t* bt = p.paged ? p.block_table + static_cast<int64_t>(it.b) * p.bt_stride : nullptr;
+      for (int t = 0; t < it.ntiles; ++t) {
+        if (issued >= ns) {
+          int w = 1;
+          if (lane == 0) w = mbar_wait(&empty[stage], (round & 1u) ^ 1u) ? 1 : 0;
+          if (__shfl_sync(kFull, w, 0) == 0) {
             if (lane == 0) set_err(p.err, TTS_EFLAG_TIMEOUT);
+            ok = false;
             break;
           }
         }
-        const int row0 = r0 + t * T;
-        const int rows = min(T, r0 + n_rows - row0);
+        const int row0 = it.r0 + t * T;
+        const int rows = min(T, it.r0 + it.n_rows - row0);
         unsigned char* dst = ring + stage * C::STAGE_BYTES + pw * C::TILE_BYTES;
         if (lane == 0) mbar_arrive_expect_tx(&full[stage], static_cast<uint32_t>(rows) * C::ROW_BYTES);
         __syncwarp();
         if (!p.paged) {
           if (lane == 0) {
             const size_t off =
-                ((static_cast<size_t>(b) * Hkv + g) * p.capacity + row0) * C::ROW_BYTES;
+                ((static_cast<size_t>(it.b) * Hkv + it.g) * p.capacity + row0) * C::ROW_BYTES;
             bulk_g2s(dst, src + off, static_cast<uint32_t>(rows) * C::ROW_BYTES, &full[stage], pol);
           }
         } else {
           const int re = row0 + rows;
           const int page0 = row0 & ~(p.page_size - 1);
-          for (int i = lane;; i += 32) {
-            const int start = (i == 0) ? row0 : page0 + i * p.page_size;
+          for (int k = lane;; k += 32) {
+            const int start = (k == 0) ? row0 : page0 + k * p.page_size;
             if (start >= re) break;
             int page = __ldcg(bt + (start >> p.page_shift));
             if (page < 0 || page >= p.n_pages) {
@@ -526,7 +610,7 @@ decode_attn_kernel(const AttnParams p) {
             const int slot = start & (p.page_size - 1);
             const int n = min(p.page_size - slot, re - start);
             const size_t off =
-                ((static_cast<size_t>(page) * Hkv + g) * p.page_size + slot) * C::ROW_BYTES;
+                ((static_cast<size_t>(page) * Hkv + it.g) * p.page_size + slot) * C::ROW_BYTES;
             bulk_g2s(dst + (start - row0) * C::ROW_BYTES, src + off,
                      static_cast<uint32_t>(n) * C::ROW_BYTES, &full[stage], pol);
           }
@@ -537,42 +621,57 @@ decode_attn_kernel(const AttnParams p) {
           ++round;
         }
       }
-      // Do not leave while copies into this CTA's shared memory may be in flight.
-      if (lane == 0)
-        for (int t = max(0, issued - ns); t < issued; ++t)
-          mbar_wait(&full[t % ns], static_cast<uint32_t>(t / ns) & 1u);
     }
+    // Do not leave while copies into this CTA's shared memory may be in flight.
+    if (lane == 0)
+      for (int t = max(0, issued - ns); t < issued; ++t)
+        mbar_wait(&full[t % ns], static_cast<uint32_t>(t / ns) & 1u);
     return;
   }
 
   // -------------------------------------------------------------------- consumers
   const int tid = threadIdx.x;  // < NT
-  constexpr int VE = C::VE, VEC = C::VEC;
   const int lr = lane % LPR;
   const int half = D / 2;
-
-  float gq[EPL], gk[EPL];
-  float2 csr[EPL];
-  int rope_pos = 0;
-  if (FUSED) {
-    rope_pos = min(max(cur, 0), p.max_pos - 1);
-    if (early && active) {
-      const float2* cs_row = p.cs + static_cast<int64_t>(rope_pos) * half;
-      load_norm_consts<VE, VEC, LPR>(p.gamma_q, cs_row, lr, D, gq, csr);
-      if (has_fresh) load_norm_consts<VE, VEC, LPR>(p.gamma_k, cs_row, lr, D, gk, csr);
-    }
-    if (early) grid_wait();
-    if (!fresh_ok && reporter) set_err(p.err, TTS_EFLAG_POS_RANGE);
-    if ((cur < 0 || cur >= p.max_pos) && reporter) set_err(p.err, TTS_EFLAG_POS_RANGE);
-  }
+  if (early) grid_wait();
   grid_launch_dependents();
   if (tid == 0) TTS_STAMP(1);
 
-  if (active) {
-    if (FUSED && !early) {
+  int sc = 0;          // ring stage of the next tile
+  uint32_t pc = 0u;    // parity of its phase
+  bool ok = true;
+  for (int i = i_first; i < n_items; i += i_step) {
+    const Item it = item_at(i);
+    const bool active = it.split < it.n_act;
+    if (!persistent && !active) {
+      // Outside the window: nothing to stream.  A cluster peer still reports in when
+      // rank 0 waits for the cluster (more than one active split); when the window
+      // fits in split 0, rank 0 writes the output alone and does not wait.
+      if (clustered && it.n_act > 1) {
+        named_barrier(1, NT);
+        if (tid == 0) mbar_arrive_remote(map_shared_rank(gbar, 0));
+      }
+      return;
+    }
+    const int b = it.b, g = it.g, split = it.split;
+    const bool reporter = (split == 0 && g == 0 && tid == 0);
+    if (reporter) {
+      if (FUSED) {
+        if (!it.fresh_ok) set_err(p.err, TTS_EFLAG_POS_RANGE);
+        if (it.cur < 0 || it.cur >= p.max_pos) set_err(p.err, TTS_EFLAG_POS_RANGE);
+      } else {
+        const int raw = __ldcg(p.lens + b);
+        if (raw < 1 || raw > p.capacity) set_err(p.err, TTS_EFLAG_NVALID);
+      }
+    }
+
+    float gq[EPL], gk[EPL];
+    float2 csr[EPL];
+    if (FUSED) {
+      const int rope_pos = min(max(it.cur, 0), p.max_pos - 1);
       const float2* cs_row = p.cs + static_cast<int64_t>(rope_pos) * half;
       load_norm_consts<VE, VEC, LPR>(p.gamma_q, cs_row, lr, D, gq, csr);
-      if (has_fresh) load_norm_consts<VE, VEC, LPR>(p.gamma_k, cs_row, lr, D, gk, csr);
+      if (it.has_fresh) load_norm_consts<VE, VEC, LPR>(p.gamma_k, cs_row, lr, D, gk, csr);
     }
     float q[G][EPL];
 #pragma unroll
@@ -581,12 +680,12 @@ decode_attn_kernel(const AttnParams p) {
           p.q + static_cast<int64_t>(b) * p.q_stride + static_cast<int64_t>(g * G + h) * D, lr, q[h]);
       if (FUSED) norm_rope_regs<VE, VEC, LPR>(q[h], gq, csr, p.eps, lr, D);
 #pragma unroll
-      for (int i = 0; i < EPL; ++i) q[h][i] *= p.scale_log2;
+      for (int k = 0; k < EPL; ++k) q[h][k] *= p.scale_log2;
     }
 
     // Fused: build the new K/V row (norm + RoPE on k, v as is), convert it to the cache
     // type, store it to the cache and keep a copy in shared memory for this CTA.
-    if (FUSED && has_fresh && warp == 0) {
+    if (FUSED && it.has_fresh && warp == 0) {
       float kr[EPL], vr[EPL];
       const int64_t roff = static_cast<int64_t>(b) * p.kv_new_stride + static_cast<int64_t>(g) * D;
       load_row_f32<VE, VEC, LPR>(p.k_new + roff, lr, kr);
@@ -604,13 +703,13 @@ decode_attn_kernel(const AttnParams p) {
         size_t off;
         bool write = true;
         if (!p.paged) {
-          off = ((static_cast<size_t>(b) * Hkv + g) * p.capacity + cur) * C::ROW_BYTES;
+          off = ((static_cast<size_t>(b) * Hkv + g) * p.capacity + it.cur) * C::ROW_BYTES;
         } else {
-          const int page = __ldcg(p.block_table + static_cast<int64_t>(b) * p.bt_stride + (cur >> p.page_shift));
+          const int page = __ldcg(p.block_table + static_cast<int64_t>(b) * p.bt_stride + (it.cur >> p.page_shift));
           write = page >= 0 && page < p.n_pages;
           if (!write && lane == 0) set_err(p.err, TTS_EFLAG_PAGE);
           off = ((static_cast<size_t>(write ? page : 0) * Hkv + g) * p.page_size +
-                 (cur & (p.page_size - 1))) * C::ROW_BYTES;
+                 (it.cur & (p.page_size - 1))) * C::ROW_BYTES;
         }
         if (write) {
 #pragma unroll
@@ -630,24 +729,20 @@ decode_attn_kernel(const AttnParams p) {
       m_run[h] = -INFINITY;
       l_run[h] = 0.f;
 #pragma unroll
-      for (int i = 0; i < EPL; ++i) o[h][i] = 0.f;
+      for (int k = 0; k < EPL; ++k) o[h][k] = 0.f;
     }
 
     if (tid == 0) TTS_STAMP(2);
     // Tiles are consumed in a two-deep software pipeline: the scores of tile t+1 are
     // computed in the same basic block as the softmax and P.V of tile t, so the two
-    // dependency chains overlap.  Only the last tile may be partial.
-    constexpr int STEPS = C::STEPS;
-    const int n_full = n_rows / T;
-    const int tail = n_rows - n_full * T;
-    bool ok = true;
+    // dependency chains overlap.  Only the last tile of an item may be partial.
+    const int n_full = it.n_rows / T;
+    const int tail = it.n_rows - n_full * T;
     float s_cur[STEPS][G], s_nxt[STEPS][G];
-    int sc = 0;          // ring stage of the current tile
-    uint32_t pc = 0u;    // parity of its phase
-    if (n_full > 0) {
-      ok = mbar_wait(&full[0], 0u);
+    if (ok && n_full > 0) {
+      ok = mbar_wait(&full[sc], pc);
       if (tid == 0) TTS_STAMP(3);
-      if (ok) tile_scores<C, KvT, false>(ring, T, warp, lane, q, s_cur);
+      if (ok) tile_scores<C, KvT, false>(ring + sc * C::STAGE_BYTES, T, warp, lane, q, s_cur);
     }
     for (int t = 0; ok && t + 1 < n_full; ++t) {
       int sn = sc + 1;
@@ -690,12 +785,16 @@ decode_attn_kernel(const AttnParams p) {
                                       lane, s_cur, m_run, l_run, o);
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[sc]);
+        if (++sc == ns) {
+          sc = 0;
+          pc ^= 1u;
+        }
       } else {
         ok = false;
       }
     }
     if (!ok) set_err(p.err, TTS_EFLAG_TIMEOUT);
-    if (FUSED && has_fresh && ok) {
+    if (FUSED && it.has_fresh && ok) {
       tile_scores<C, KvT, true>(fresh_k, 1, warp, lane, q, s_cur);
       tile_softmax_pv<C, KvT, true>(fresh_v, 1, warp, lane, s_cur, m_run, l_run, o);
     }
@@ -708,7 +807,7 @@ decode_attn_kernel(const AttnParams p) {
       for (int off = LPR; off < 32; off <<= 1) {
         l_run[h] += __shfl_xor_sync(kFull, l_run[h], off);
 #pragma unroll
-        for (int i = 0; i < EPL; ++i) o[h][i] += __shfl_xor_sync(kFull, o[h][i], off);
+        for (int k = 0; k < EPL; ++k) o[h][k] += __shfl_xor_sync(kFull, o[h][k], off);
       }
     }
     if (lane < LPR) {
@@ -727,6 +826,7 @@ decode_attn_kernel(const AttnParams p) {
     }
     named_barrier(1, NT);
 
+    const bool direct = it.n_act == 1;  // the window lies in one split: final output here
     for (int idx = tid; idx < G * D; idx += NT) {
       const int h = idx / D;
       const int d = idx - h * D;
@@ -736,13 +836,13 @@ decode_attn_kernel(const AttnParams p) {
       float L = 0.f, O = 0.f;
 #pragma unroll
       for (int w = 0; w < NC; ++w) {
-        const float* src = scratch + (w * G + h) * (D + 2);
-        const float f = (src[D] == -INFINITY) ? 0.f : exp2f(src[D] - M);
-        L = fmaf(src[D + 1], f, L);
-        O = fmaf(src[d], f, O);
+        const float* srcp = scratch + (w * G + h) * (D + 2);
+        const float f = (srcp[D] == -INFINITY) ? 0.f : exp2f(srcp[D] - M);
+        L = fmaf(srcp[D + 1], f, L);
+        O = fmaf(srcp[d], f, O);
       }
       const int hq = g * G + h;
-      if (p.n_splits == 1) {
+      if (direct) {
         p.out[(static_cast<int64_t>(b) * Hq + hq) * D + d] = O / L;
       } else if (clustered) {
         float* slot = gather + (split * G + h) * (D + 2);
@@ -765,85 +865,94 @@ decode_attn_kernel(const AttnParams p) {
         if (d == 0) reinterpret_cast<float2*>(p.ws_ml)[slot] = make_float2(M, L);
       }
     }
-  }
+    if (tid == 0) TTS_STAMP(5);
 
-  if (tid == 0) TTS_STAMP(5);
-  if (p.n_splits == 1) return;
-
-  if (clustered) {
-    // Partials travel over distributed shared memory; rank 0 waits (bounded) for the
-    // other ranks' arrivals, which release their stores, and merges from its own smem.
-    named_barrier(1, NT);
-    if (split != 0) {
-      if (tid == 0) mbar_arrive_remote(map_shared_rank(gbar, 0));
-      return;
-    }
-    if (!mbar_wait_cluster(gbar, 0u, 8 * kWaitLimitCycles)) {
-      if (tid == 0) set_err(p.err, TTS_EFLAG_TIMEOUT);
-      return;
-    }
-    if (tid == 0) TTS_STAMP(6);
-    const int n_act = min(p.n_splits, (nv + p.split_len - 1) / p.split_len);
-    // per head: weights 2^(m_s - M) and the sum L, one warp per head (lanes over splits)
-    float* sm_w = scratch;  // [G][16] weights, then [G] sums (the merge scratch is free now)
-    for (int h = warp; h < G; h += NC) {
-      const float m = lane < n_act ? gather[(lane * G + h) * (D + 2) + D] : -INFINITY;
-      float M = m;
+    if (clustered) {
+      // Partials travel over distributed shared memory; rank 0 waits (bounded) for the
+      // other ranks' arrivals, which release their stores, and merges from its own smem.
+      named_barrier(1, NT);
+      if (split != 0) {
+        if (tid == 0) mbar_arrive_remote(map_shared_rank(gbar, 0));
+        return;
+      }
+      if (!direct) {
+        if (!mbar_wait_cluster(gbar, 0u, 8 * kWaitLimitCycles)) {
+          if (tid == 0) set_err(p.err, TTS_EFLAG_TIMEOUT);
+          return;
+        }
+        if (tid == 0) TTS_STAMP(6);
+        const int n_act = it.n_act;
+        // per head: weights 2^(m_s - M) and the sum L, one warp per head (lanes over splits)
+        float* sm_w = reinterpret_cast<float*>(comb);  // [G][16] weights, then [G] sums
+        for (int h = warp; h < G; h += NC) {
+          const float m = lane < n_act ? gather[(lane * G + h) * (D + 2) + D] : -INFINITY;
+          float M = m;
 #pragma unroll
-      for (int off = 16; off >= 1; off >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, off));
-      const float w = lane < n_act ? fast_exp2(m - M) : 0.f;
-      float L = lane < n_act ? w * gather[(lane * G + h) * (D + 2) + D + 1] : 0.f;
+          for (int off = 16; off >= 1; off >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, off));
+          const float w = lane < n_act ? fast_exp2(m - M) : 0.f;
+          float L = lane < n_act ? w * gather[(lane * G + h) * (D + 2) + D + 1] : 0.f;
 #pragma unroll
-      for (int off = 16; off >= 1; off >>= 1) L += __shfl_xor_sync(kFull, L, off);
-      if (lane < 16) sm_w[h * 16 + lane] = w;
-      if (lane == 0) sm_w[G * 16 + h] = L;
-    }
-    named_barrier(1, NT);
-    for (int idx = tid; idx < G * D; idx += NT) {
-      const int h = idx / D;
-      const int d = idx - h * D;
-      float O = 0.f;
+          for (int off = 16; off >= 1; off >>= 1) L += __shfl_xor_sync(kFull, L, off);
+          if (lane < 16) sm_w[h * 16 + lane] = w;
+          if (lane == 0) sm_w[G * 16 + h] = L;
+        }
+        named_barrier(1, NT);
+        for (int idx = tid; idx < G * D; idx += NT) {
+          const int h = idx / D;
+          const int d = idx - h * D;
+          float O = 0.f;
 #pragma unroll 4
-      for (int s2 = 0; s2 < n_act; ++s2) O = fmaf(gather[(s2 * G + h) * (D + 2) + d], sm_w[h * 16 + s2], O);
-      p.out[(static_cast<int64_t>(b) * Hq + g * G + h) * D + d] = O / sm_w[G * 16 + h];
+          for (int s2 = 0; s2 < n_act; ++s2) O = fmaf(gather[(s2 * G + h) * (D + 2) + d], sm_w[h * 16 + s2], O);
+          p.out[(static_cast<int64_t>(b) * Hq + g * G + h) * D + d] = O / sm_w[G * 16 + h];
+        }
+        if (tid == 0) TTS_STAMP(7);
+      }
+      return;
     }
-    if (tid == 0) TTS_STAMP(7);
-    return;
-  }
 
-  // Ticket: the last split of this (stream, kv head) to finish merges all partials.
-  named_barrier(1, NT);
-  if (tid == 0) {
-    const int prev = atomic_add_acq_rel_gpu(p.ws_cnt + b * Hkv + g, 1);
-    *s_last = (prev == p.n_splits - 1) ? 1 : 0;
-  }
-  named_barrier(1, NT);
-  if (tid == 0) TTS_STAMP(6);
-  if (*s_last == 0) return;
-  const int n_act = min(p.n_splits, (nv + p.split_len - 1) / p.split_len);
-  combine_splits<C>(p, b, g, n_act, tid, ring);
-  if (tid == 0) {
-    p.ws_cnt[b * Hkv + g] = 0;
-    TTS_STAMP(7);
+    if (!direct) {
+      // Ticket: the last of this (stream, kv head)'s active splits merges all partials.
+      named_barrier(1, NT);
+      if (tid == 0) {
+        const int prev = atomic_add_acq_rel_gpu(p.ws_cnt + b * Hkv + g, 1);
+        *s_last = (prev == it.n_act - 1) ? 1 : 0;
+      }
+      named_barrier(1, NT);
+      if (tid == 0) TTS_STAMP(6);
+      if (*s_last != 0) {
+        combine_splits<C>(p, b, g, it.n_act, tid, comb);
+        if (tid == 0) {
+          p.ws_cnt[b * Hkv + g] = 0;
+          TTS_STAMP(7);
+        }
+      }
+    }
+    // the merge scratch and flag are reused by the next item
+    named_barrier(1, NT);
   }
 }
 
 constexpr int kMaxCluster = 16;
 
+constexpr int kMaxListStreams = 2048;  // persistent mode keeps B + 1 prefix sums in smem
+
 template <typename KvT, int D, int G, bool FUSED>
 cudaError_t launch_one(const AttnParams& p_in, cudaStream_t s) {
   using C = Cfg<KvT, D, G>;
   auto kern = decode_attn_kernel<KvT, D, G, FUSED>;
-  // Per device: the kernel attributes, and the largest cluster of this kernel the GPU
-  // can co-schedule (cluster mode is used only up to that size).
+  // Per device: the kernel attributes, the largest cluster of this kernel the GPU can
+  // co-schedule (cluster mode is used only up to that size), the SM count and how many
+  // CTAs of the persistent configuration fit on one SM.
   static int configured_for = -1;
   static int max_cluster = 1;
+  static int n_sm = 1;
+  static int per_sm = 1;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (configured_for != dev) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(C::smem_bytes(C::NS, kMaxCluster)));
+    const size_t max_smem = C::smem_bytes(C::NS, kMaxCluster, kMaxListStreams + 1);
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(max_smem));
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
@@ -864,25 +973,39 @@ cudaError_t launch_one(const AttnParams& p_in, cudaStream_t s) {
       mc = 8;  // portable cluster size
     }
     max_cluster = mc < 1 ? 1 : (mc > kMaxCluster ? kMaxCluster : mc);
+    if (cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n_sm < 1) {
+      cudaGetLastError();
+      n_sm = 1;
+    }
+    int occ = 0;
+    const size_t wave_smem = C::smem_bytes(TTS_STAGES_WAVES < C::NS ? TTS_STAGES_WAVES : C::NS, 0, 64);
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, C::THREADS, wave_smem) != cudaSuccess || occ < 1) {
+      cudaGetLastError();
+      occ = 1;
+    }
+    per_sm = occ;
     configured_for = dev;
   }
   AttnParams p = p_in;
-  // Clusters pay off when the whole grid is one wave of one CTA per SM (few streams);
-  // ragged multi-wave grids keep the ticket merge, which schedules CTAs freely.
-  static int n_sm = 0;
-  if (n_sm == 0 && cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
-    cudaGetLastError();
-    n_sm = 1;
-  }
+  // Clusters pay off when the whole grid is one wave of one CTA per SM (few streams).
+  // A grid larger than what fits at once becomes persistent: as many CTAs as fit, each
+  // walking the list of active (stream, kv head, split) items.
   const long long ctas = static_cast<long long>(p.n_splits) * p.n_kv_heads * p.B;
   const bool one_wave = ctas <= n_sm;
   p.cluster = (p.n_splits > 1 && p.n_splits <= max_cluster && p.ws_o != nullptr && one_wave) ? p.n_splits : 0;
+  const long long resident = static_cast<long long>(n_sm) * per_sm;
+  p.persistent = (p.cluster == 0 && ctas > resident && p.B <= kMaxListStreams) ? 1 : 0;
   const int want = p.cluster > 1 ? TTS_STAGES_CLUSTER : TTS_STAGES_WAVES;
   if (p.n_stages > want) p.n_stages = want;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.n_splits, p.n_kv_heads, p.B);
+  if (p.persistent) {
+    cfg.gridDim = dim3(static_cast<unsigned>(resident), 1, 1);
+    cfg.dynamicSmemBytes = C::smem_bytes(p.n_stages, 0, p.B + 1);
+  } else {
+    cfg.gridDim = dim3(p.n_splits, p.n_kv_heads, p.B);
+    cfg.dynamicSmemBytes = C::smem_bytes(p.n_stages, p.cluster);
+  }
   cfg.blockDim = dim3(C::THREADS);
-  cfg.dynamicSmemBytes = C::smem_bytes(p.n_stages, p.cluster);
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -915,9 +1038,9 @@ AttnGeometry geometry_of() {
 template <typename KvT, int D>
 size_t smem_of(int group, int ns) {
   switch (group) {
-    case 1: return Cfg<KvT, D, 1>::smem_bytes(ns, kMaxCluster);
-    case 2: return Cfg<KvT, D, 2>::smem_bytes(ns, kMaxCluster);
-    case 4: return Cfg<KvT, D, 4>::smem_bytes(ns, kMaxCluster);
+    case 1: return Cfg<KvT, D, 1>::smem_bytes(ns, kMaxCluster, kMaxListStreams + 1);
+    case 2: return Cfg<KvT, D, 2>::smem_bytes(ns, kMaxCluster, kMaxListStreams + 1);
+    case 4: return Cfg<KvT, D, 4>::smem_bytes(ns, kMaxCluster, kMaxListStreams + 1);
     default: return 0;
   }
 }

@@ -79,6 +79,7 @@ struct AttnParams {
   int split_len;        // positions per split, a multiple of the tile
   int n_stages;         // pipeline depth actually used (<= the kernel's maximum)
   int cluster;          // set by the launcher: splits per cluster (>1 = cluster merge)
+  int persistent;       // set by the launcher: 1 = fixed grid walking the active items
   uint32_t flags;
   int32_t* err;
 };
