@@ -73,7 +73,8 @@ WsLayout ws_layout(const tts_kv_desc* d, int n_splits) {
   w.o_off = 0;
   w.ml_off = round256(slots * d->head_dim * sizeof(float));
   w.cnt_off = w.ml_off + round256(slots * 2 * sizeof(float));
-  w.total = w.cnt_off + round256(static_cast<size_t>(d->B) * d->n_kv_heads * sizeof(int));
+  // split tickets [B][Hkv], then the persistent scheduler's two counters
+  w.total = w.cnt_off + round256((static_cast<size_t>(d->B) * d->n_kv_heads + 2) * sizeof(int));
   return w;
 }
 
@@ -114,10 +115,12 @@ tts_status prepare_attn(const tts_kv_desc* d, const void* k_cache, const void* v
     p.ws_o = reinterpret_cast<float*>(ws + w.o_off);
     p.ws_ml = reinterpret_cast<float*>(ws + w.ml_off);
     p.ws_cnt = reinterpret_cast<int*>(ws + w.cnt_off);
+    p.ws_sched = p.ws_cnt + static_cast<size_t>(d->B) * d->n_kv_heads;
   } else {
     p.ws_o = nullptr;
     p.ws_ml = nullptr;
     p.ws_cnt = nullptr;
+    p.ws_sched = nullptr;
   }
   const int tiles_per_split = split_len / geo.tile_rows;
   p.n_stages = tiles_per_split < geo.max_stages ? tiles_per_split : geo.max_stages;

@@ -111,8 +111,14 @@ __device__ __forceinline__ unsigned long long gtime() {
     const int cta_ = (blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;       \
     if (cta_ < kTraceCtas) g_trace[cta_][slot] = gtime();                                  \
   } while (0)
+// per work item (persistent mode) rather than per CTA
+#define TTS_STAMP_ITEM(slot, item)                                                         \
+  do {                                                                                     \
+    if ((item) < kTraceCtas) g_trace[(item)][slot] = gtime();                              \
+  } while (0)
 #else
 #define TTS_STAMP(slot) do {} while (0)
+#define TTS_STAMP_ITEM(slot, item) do {} while (0)
 #endif
 
 namespace {
@@ -160,7 +166,8 @@ struct Cfg {
   // the gather area where the cluster's splits deposit their partials in rank 0.
   static constexpr int PART = G * (D + 2);    // floats of one split's partial (o, m, l per head)
   static constexpr size_t bar_off(int ns) { return static_cast<size_t>(ns) * STAGE_BYTES; }
-  static constexpr size_t fresh_off(int ns) { return bar_off(ns) + ((2 * NS + 1) * sizeof(uint64_t) + 15) / 16 * 16; }
+  // barriers: full[NS], empty[NS], gather, item-ready[4], item-free[4]
+  static constexpr size_t fresh_off(int ns) { return bar_off(ns) + ((2 * NS + 9) * sizeof(uint64_t) + 15) / 16 * 16; }
   static constexpr size_t scratch_off(int ns) { return fresh_off(ns) + 2 * ROW_BYTES; }
   static constexpr size_t flag_off(int ns) {
     return scratch_off(ns) + static_cast<size_t>(NC) * PART * sizeof(float);
@@ -169,7 +176,7 @@ struct Cfg {
   static constexpr int kCombSplits = 256;
   static constexpr size_t COMB_BYTES =
       ((2 * G * kCombSplits + G) * sizeof(float) + 15) / 16 * 16 + NT * 16;
-  static constexpr size_t comb_off(int ns) { return flag_off(ns) + 16; }
+  static constexpr size_t comb_off(int ns) { return flag_off(ns) + 32; }  // flag + item queue[4]
   static constexpr size_t gather_off(int ns) { return comb_off(ns) + COMB_BYTES; }
   static constexpr size_t list_off(int ns, int cluster) {
     return gather_off(ns) + static_cast<size_t>(cluster > 1 ? cluster : 0) * PART * sizeof(float);
@@ -479,17 +486,21 @@ decode_attn_kernel(const AttnParams p) {
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::bar_off(ns));
   uint64_t* empty = full + C::NS;
   uint64_t* gbar = empty + C::NS;
+  uint64_t* ibar = gbar + 1;   // persistent: item published in queue slot j
+  uint64_t* ifree = ibar + 4;  // persistent: queue slot j read by every reader
   unsigned char* fresh_k = smem + C::fresh_off(ns);
   unsigned char* fresh_v = fresh_k + C::ROW_BYTES;
   float* scratch = reinterpret_cast<float*>(smem + C::scratch_off(ns));
   int* s_last = reinterpret_cast<int*>(smem + C::flag_off(ns));
+  volatile int* s_item = reinterpret_cast<volatile int*>(smem + C::flag_off(ns) + 16);
   unsigned char* comb = smem + C::comb_off(ns);
   int* s_pre = reinterpret_cast<int*>(smem + C::list_off(ns, p.cluster));  // persistent: [B+1]
   float* gather = reinterpret_cast<float*>(smem + C::gather_off(ns));
   // Cluster mode: the n_splits CTAs of one (stream, kv head) form a cluster and merge
   // their partials in rank 0's shared memory (rank == split).
   const bool clustered = p.cluster > 1;
-  // Persistent mode: a fixed grid whose CTAs walk a list of the active items only.
+  // Persistent mode: a fixed grid whose CTAs take the active items one after another:
+  // item blockIdx.x first, then whatever an atomic work counter hands out.
   const bool persistent = p.persistent != 0;
 
   if (threadIdx.x == 0) {
@@ -499,6 +510,12 @@ decode_attn_kernel(const AttnParams p) {
       mbar_init(&empty[s], NC);
     }
     if (clustered) mbar_init(gbar, p.cluster - 1);
+    if (persistent) {
+      for (int j = 0; j < 4; ++j) {
+        mbar_init(&ibar[j], 1);        // the scheduler publishes
+        mbar_init(&ifree[j], NC + 1);  // the V producer and every consumer warp read
+      }
+    }
     mbar_init_fence();
   }
   // every CTA's gather barrier is initialised before any peer can arrive on it
@@ -555,8 +572,18 @@ decode_attn_kernel(const AttnParams p) {
     }
     return make_item<FUSED>(p, T, b, g, split, __ldcg(p.lens + b));
   };
-  const int i_first = persistent ? blockIdx.x : 0;
-  const int i_step = persistent ? gridDim.x : 1;
+  // Persistent mode: queue slot j = k % 4 carries this CTA's k-th item from the
+  // scheduler (the K producer's lane 0) to the V producer and the consumer warps;
+  // -1 ends the list.  Returns false if a bounded wait ran out.
+  auto next_item = [&](int& k, int& item) -> bool {
+    const int j = k & 3;
+    if (!mbar_wait(&ibar[j], static_cast<uint32_t>(k >> 2) & 1u)) return false;
+    item = s_item[j];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&ifree[j]);
+    ++k;
+    return true;
+  };
 
   if (warp >= NC) {
     // ----------------------------------------------------------------- producers
@@ -571,7 +598,31 @@ decode_attn_kernel(const AttnParams p) {
     int stage = 0;
     uint32_t round = 0;
     bool ok = true;
-    for (int i = i_first; ok && i < n_items; i += i_step) {
+    int k = 0;  // items taken so far
+    int i = persistent ? (static_cast<int>(blockIdx.x) < n_items ? static_cast<int>(blockIdx.x) : -1) : 0;
+    for (;;) {
+      if (persistent) {
+        if (pw == 0) {
+          // scheduler: publish item i in queue slot k % 4 once every reader is done with it
+          const int j = k & 3;
+          int w = 1;
+          if (k >= 4 && lane == 0) w = mbar_wait(&ifree[j], static_cast<uint32_t>((k >> 2) - 1) & 1u) ? 1 : 0;
+          if (__shfl_sync(kFull, w, 0) == 0) {
+            if (lane == 0) set_err(p.err, TTS_EFLAG_TIMEOUT);
+            break;
+          }
+          if (lane == 0) {
+            s_item[j] = i;
+            mbar_arrive(&ibar[j]);
+          }
+          __syncwarp();
+          ++k;
+        } else if (!next_item(k, i)) {
+          if (lane == 0) set_err(p.err, TTS_EFLAG_TIMEOUT);
+          break;
+        }
+        if (i < 0) break;
+      }
       const Item it = item_at(i);
       if (!persistent && it.split >= it.n_act) break;  // outside the window
       const int32_t* bt = p.paged ? p.block_table + static_cast<int64_t>(it.b) * p.bt_stride : nullptr;
@@ -621,6 +672,18 @@ decode_attn_kernel(const AttnParams p) {
           ++round;
         }
       }
+      if (!ok || !persistent) break;
+      if (pw == 0) {
+        // next item from the work counter (after the dependency wait: the counter is
+        // reset by the preceding launch on this workspace when it finishes)
+        if (k == 1 && early) grid_wait();
+        int nxt = -1;
+        if (lane == 0) {
+          const int v = static_cast<int>(gridDim.x) + atomicAdd(p.ws_sched, 1);
+          nxt = v < n_items ? v : -1;
+        }
+        i = __shfl_sync(kFull, nxt, 0);
+      }
     }
     // Do not leave while copies into this CTA's shared memory may be in flight.
     if (lane == 0)
@@ -640,7 +703,18 @@ decode_attn_kernel(const AttnParams p) {
   int sc = 0;          // ring stage of the next tile
   uint32_t pc = 0u;    // parity of its phase
   bool ok = true;
-  for (int i = i_first; i < n_items; i += i_step) {
+  int kq = 0;  // items taken from the queue so far (persistent)
+  for (int round_item = 0;; ++round_item) {
+    int i = 0;
+    if (persistent) {
+      if (!next_item(kq, i)) {
+        set_err(p.err, TTS_EFLAG_TIMEOUT);
+        break;
+      }
+      if (i < 0) break;
+    } else if (round_item > 0) {
+      break;
+    }
     const Item it = item_at(i);
     const bool active = it.split < it.n_act;
     if (!persistent && !active) {
@@ -654,6 +728,7 @@ decode_attn_kernel(const AttnParams p) {
       return;
     }
     const int b = it.b, g = it.g, split = it.split;
+    if (persistent && tid == 0) { TTS_STAMP_ITEM(0, i); TTS_STAMP_ITEM(1, blockIdx.x * 0 + i); }
     const bool reporter = (split == 0 && g == 0 && tid == 0);
     if (reporter) {
       if (FUSED) {
@@ -732,7 +807,7 @@ decode_attn_kernel(const AttnParams p) {
       for (int k = 0; k < EPL; ++k) o[h][k] = 0.f;
     }
 
-    if (tid == 0) TTS_STAMP(2);
+    if (tid == 0) { if (persistent) TTS_STAMP_ITEM(2, i); else TTS_STAMP(2); }
     // Tiles are consumed in a two-deep software pipeline: the scores of tile t+1 are
     // computed in the same basic block as the softmax and P.V of tile t, so the two
     // dependency chains overlap.  Only the last tile of an item may be partial.
@@ -741,7 +816,7 @@ decode_attn_kernel(const AttnParams p) {
     float s_cur[STEPS][G], s_nxt[STEPS][G];
     if (ok && n_full > 0) {
       ok = mbar_wait(&full[sc], pc);
-      if (tid == 0) TTS_STAMP(3);
+      if (tid == 0) { if (persistent) TTS_STAMP_ITEM(3, i); else TTS_STAMP(3); }
       if (ok) tile_scores<C, KvT, false>(ring + sc * C::STAGE_BYTES, T, warp, lane, q, s_cur);
     }
     for (int t = 0; ok && t + 1 < n_full; ++t) {
@@ -779,7 +854,7 @@ decode_attn_kernel(const AttnParams p) {
     }
     if (ok && tail > 0) {
       if (mbar_wait(&full[sc], pc)) {
-        if (n_full == 0 && tid == 0) TTS_STAMP(3);
+        if (n_full == 0 && tid == 0) { if (persistent) TTS_STAMP_ITEM(3, i); else TTS_STAMP(3); }
         tile_scores<C, KvT, true>(ring + sc * C::STAGE_BYTES, tail, warp, lane, q, s_cur);
         tile_softmax_pv<C, KvT, true>(ring + sc * C::STAGE_BYTES + C::TILE_BYTES, tail, warp,
                                       lane, s_cur, m_run, l_run, o);
@@ -798,7 +873,7 @@ decode_attn_kernel(const AttnParams p) {
       tile_scores<C, KvT, true>(fresh_k, 1, warp, lane, q, s_cur);
       tile_softmax_pv<C, KvT, true>(fresh_v, 1, warp, lane, s_cur, m_run, l_run, o);
     }
-    if (tid == 0) TTS_STAMP(4);
+    if (tid == 0) { if (persistent) TTS_STAMP_ITEM(4, i); else TTS_STAMP(4); }
 
     // Merge the row groups of this warp, then the warps of this CTA.
 #pragma unroll
@@ -865,7 +940,7 @@ decode_attn_kernel(const AttnParams p) {
         if (d == 0) reinterpret_cast<float2*>(p.ws_ml)[slot] = make_float2(M, L);
       }
     }
-    if (tid == 0) TTS_STAMP(5);
+    if (tid == 0) { if (persistent) TTS_STAMP_ITEM(5, i); else TTS_STAMP(5); }
 
     if (clustered) {
       // Partials travel over distributed shared memory; rank 0 waits (bounded) for the
@@ -880,7 +955,7 @@ decode_attn_kernel(const AttnParams p) {
           if (tid == 0) set_err(p.err, TTS_EFLAG_TIMEOUT);
           return;
         }
-        if (tid == 0) TTS_STAMP(6);
+        if (tid == 0) { if (persistent) TTS_STAMP_ITEM(6, i); else TTS_STAMP(6); }
         const int n_act = it.n_act;
         // per head: weights 2^(m_s - M) and the sum L, one warp per head (lanes over splits)
         float* sm_w = reinterpret_cast<float*>(comb);  // [G][16] weights, then [G] sums
@@ -905,7 +980,7 @@ decode_attn_kernel(const AttnParams p) {
           for (int s2 = 0; s2 < n_act; ++s2) O = fmaf(gather[(s2 * G + h) * (D + 2) + d], sm_w[h * 16 + s2], O);
           p.out[(static_cast<int64_t>(b) * Hq + g * G + h) * D + d] = O / sm_w[G * 16 + h];
         }
-        if (tid == 0) TTS_STAMP(7);
+        if (tid == 0) { if (persistent) TTS_STAMP_ITEM(7, i); else TTS_STAMP(7); }
       }
       return;
     }
@@ -918,17 +993,25 @@ decode_attn_kernel(const AttnParams p) {
         *s_last = (prev == it.n_act - 1) ? 1 : 0;
       }
       named_barrier(1, NT);
-      if (tid == 0) TTS_STAMP(6);
+      if (tid == 0) { if (persistent) TTS_STAMP_ITEM(6, i); else TTS_STAMP(6); }
       if (*s_last != 0) {
         combine_splits<C>(p, b, g, it.n_act, tid, comb);
         if (tid == 0) {
           p.ws_cnt[b * Hkv + g] = 0;
-          TTS_STAMP(7);
+          { if (persistent) TTS_STAMP_ITEM(7, i); else TTS_STAMP(7); }
         }
       }
     }
     // the merge scratch and flag are reused by the next item
     named_barrier(1, NT);
+  }
+  if (persistent && tid == 0) {
+    // the last CTA to finish resets the work counter for the next launch
+    const int prev = atomic_add_acq_rel_gpu(p.ws_sched + 1, 1);
+    if (prev == static_cast<int>(gridDim.x) - 1) {
+      p.ws_sched[0] = 0;
+      p.ws_sched[1] = 0;
+    }
   }
 }
 

@@ -74,7 +74,8 @@ struct AttnParams {
   float* out;
   float* ws_o;          // [B][Hq][n_splits][D]
   float* ws_ml;         // [B][Hq][n_splits][2]
-  int* ws_cnt;          // [B][Hkv]
+  int* ws_cnt;          // [B][Hkv] split tickets
+  int* ws_sched;        // [2] persistent mode: work counter, finished-CTA counter
   int n_splits;         // grid.x
   int split_len;        // positions per split, a multiple of the tile
   int n_stages;         // pipeline depth actually used (<= the kernel's maximum)
