@@ -262,17 +262,14 @@ int32_t tts_decode_attn_default_splits(const tts_kv_desc* d) {
   const int sms = sm_count();
   int s;
   if (pairs <= 16) {
-    // Few (stream, kv head) pairs: one thread-block cluster per pair, sized to leave
-    // about 40% of the SMs free so the next launch's CTAs can start streaming there.
-    s = (6 * sms) / (10 * pairs);
-    if (s > 16) s = 16;
-    if (s < 2) s = 2;
+    // Few (stream, kv head) pairs: about two CTAs per SM over the grid.
+    s = (2 * sms + pairs - 1) / pairs;
   } else {
     // Many pairs: windows cut into pieces of at most 512 positions (ragged batches
     // balance; the partials merge through the workspace).
     s = (d->capacity + 511) / 512;
-    if (s < 1) s = 1;
   }
+  if (s < 1) s = 1;
   if (s > max_splits) s = max_splits;
   if (s < 1) s = 1;
   return s;
