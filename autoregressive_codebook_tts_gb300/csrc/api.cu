@@ -54,10 +54,12 @@ tts_status check_desc(const tts_kv_desc* d) {
   return TTS_OK;
 }
 
-// Positions per split: a multiple of the tile, covering capacity in n_splits pieces.
-int split_len_for(const tts_kv_desc* d, int n_splits, int tile) {
+// Positions per split: a multiple of kSplitQuantum, covering capacity in n_splits
+// pieces.  A split's last tile may be partial.
+constexpr int kSplitQuantum = 16;
+int split_len_for(const tts_kv_desc* d, int n_splits) {
   int per = (d->capacity + n_splits - 1) / n_splits;
-  per = ((per + tile - 1) / tile) * tile;
+  per = ((per + kSplitQuantum - 1) / kSplitQuantum) * kSplitQuantum;
   return per;
 }
 
@@ -78,17 +80,16 @@ WsLayout ws_layout(const tts_kv_desc* d, int n_splits) {
   return w;
 }
 
-// Splits actually launched for a requested count (0 = default): at most one per tile
-// and at most kMaxSplits; each split covers split_len positions, a multiple of the tile.
+// Splits actually launched for a requested count (0 = default): at most one per
+// kSplitQuantum positions and at most kMaxSplits; each split covers split_len positions.
 constexpr int kMaxSplits = 256;
 tts_status resolve_splits(const tts_kv_desc* d, int32_t n_splits_req, int& split_len, int& used) {
-  const AttnGeometry geo = attn_geometry(d->kv_dtype == TTS_BF16, d->head_dim);
   int n_splits = n_splits_req == 0 ? tts_decode_attn_default_splits(d) : n_splits_req;
   if (n_splits < 1) return TTS_ERR_SHAPE;
-  const int max_splits = (d->capacity + geo.tile_rows - 1) / geo.tile_rows;
+  const int max_splits = (d->capacity + kSplitQuantum - 1) / kSplitQuantum;
   if (n_splits > max_splits) n_splits = max_splits;
   if (n_splits > kMaxSplits) n_splits = kMaxSplits;
-  split_len = split_len_for(d, n_splits, geo.tile_rows);
+  split_len = split_len_for(d, n_splits);
   used = (d->capacity + split_len - 1) / split_len;
   return TTS_OK;
 }
@@ -101,7 +102,6 @@ tts_status prepare_attn(const tts_kv_desc* d, const void* k_cache, const void* v
   if (st != TTS_OK) return st;
   if (k_cache == nullptr || v_cache == nullptr) return TTS_ERR_NULL;
   if (!aligned16(k_cache) || !aligned16(v_cache)) return TTS_ERR_ALIGN;
-  const AttnGeometry geo = attn_geometry(d->kv_dtype == TTS_BF16, d->head_dim);
   int split_len = 0, used = 0;
   st = resolve_splits(d, n_splits_req, split_len, used);
   if (st != TTS_OK) return st;
@@ -122,9 +122,7 @@ tts_status prepare_attn(const tts_kv_desc* d, const void* k_cache, const void* v
     p.ws_cnt = nullptr;
     p.ws_sched = nullptr;
   }
-  const int tiles_per_split = split_len / geo.tile_rows;
-  p.n_stages = tiles_per_split < geo.max_stages ? tiles_per_split : geo.max_stages;
-  if (p.n_stages < 1) p.n_stages = 1;
+  p.n_stages = 0;  // chosen by the launcher
   p.k_cache = k_cache;
   p.v_cache = v_cache;
   p.B = d->B;

@@ -17,12 +17,20 @@
 //     One bulk copy costs about the same time whatever its size up to tens of KB and
 //     copies issued by one thread run one after another, so tiles are 16 KB per copy
 //     and K and V are issued by two producer warps side by side.
+//   * A grid that fits the GPU at two CTAs per SM sizes each CTA's ring to hold its
+//     whole split (the last, partial tile packed as K rows then V rows), so the split
+//     streams in before the dependency wait ends.  Its producers keep one tile each in
+//     flight: the whole layer's prefetch would otherwise queue in front of the
+//     preceding launch's split merge, which is on the critical path.
 //   * Consumer warps split each tile's rows.  A row is covered by LPR lanes with 16
 //     bytes each (4 f32 or 8 bf16 elements); q.k is reduced across those lanes with
 //     xor shuffles; each warp keeps its own online-softmax state (running max in log2
 //     units, running sum, unnormalised output), merged at the end in shared memory.
 //   * Rows at or past n_valid are never copied or read: the -inf of the padded tail
 //     is realised as "not there", so poison in the tail cannot leak.
+//   * Fused: one warp of the split holding the new position builds the new K/V row in
+//     registers (norm + RoPE, conversion to the cache type), stores it to the cache and
+//     starts its softmax state with it, so the row is never read back.
 //   * Split-KV: every split writes (o, m, l) to the workspace and takes a ticket (one
 //     acquire-release atomic per CTA); the last split of a (stream, kv head) merges all
 //     partials with a log-sum-exp combine whose loads are all issued up front, and
@@ -30,8 +38,8 @@
 //   * Launch configuration depends only on capacity; splits past the window exit early.
 //   * Programmatic dependent launch: each launch lets the next one be scheduled as soon
 //     as its own consumers pass their dependency wait.  With TTS_KV_PREFETCH_BEFORE_WAIT
-//     the producer starts streaming cache tiles (and the consumers load gamma and the
-//     RoPE row) before the preceding kernel has finished.
+//     the producers start streaming cache tiles (and the consumers read cur_len) before
+//     the preceding kernel has finished.
 //   * Every mbarrier wait is bounded (kWaitLimitCycles); on expiry TTS_EFLAG_TIMEOUT is
 //     set, the copies already issued are waited for (bounded), and the CTA finishes.
 #include "common.cuh"
@@ -72,17 +80,30 @@
 #ifndef TTS_BF16_64_NS
 #define TTS_BF16_64_NS 4
 #endif
-// Ring stages actually used (each stage is a 16 KB K tile plus a 16 KB V tile for the
-// 128-wide heads): three in a grid of many CTAs (two CTAs per SM); four in a cluster
-// grid, which has fewer CTAs than SMs, so the next launch's CTAs start on the idle SMs.
-#ifndef TTS_STAGES_WAVES
-#define TTS_STAGES_WAVES 3
+// Ring sizes.  A grid that fits on the GPU at two CTAs per SM gives each CTA as many
+// stages as fit in half an SM's shared memory, so a split of up to that many tiles is
+// streamed in whole before the dependency wait ends.  A persistent grid (more work
+// than fits at once) keeps TTS_RING_KB_STREAM per CTA; a cluster grid, which has
+// fewer CTAs than SMs, TTS_RING_KB_CLUSTER.
+#ifndef TTS_RING_KB_STREAM
+#define TTS_RING_KB_STREAM 96
 #endif
-#ifndef TTS_STAGES_CLUSTER
-#define TTS_STAGES_CLUSTER 4
+#ifndef TTS_RING_KB_CLUSTER
+#define TTS_RING_KB_CLUSTER 128
 #endif
 #ifndef TTS_BF16_64_NC
 #define TTS_BF16_64_NC 4
+#endif
+// Tiles a producer warp keeps in flight (0 = as many as the ring holds).  Once HBM is
+// saturated a deeper queue streams no faster, but every other memory request of the
+// GPU -- the preceding launch's split merge among them -- waits behind it.  A grid of
+// single-item CTAs prefetches whole splits while the preceding launch finishes, so it
+// is paced; a persistent grid streams item after item and is not.
+#ifndef TTS_INFLIGHT_SINGLE
+#define TTS_INFLIGHT_SINGLE 1
+#endif
+#ifndef TTS_INFLIGHT_STREAM
+#define TTS_INFLIGHT_STREAM 0
 #endif
 #ifndef TTS_ATTN_MIN_BLOCKS
 #define TTS_ATTN_MIN_BLOCKS 2
@@ -161,29 +182,49 @@ struct Cfg {
   static_assert(LPR >= 2 && LPR <= 32 && EPL % VE == 0, "row must span 2..32 lanes");
   static_assert(NT % Q4 == 0 || Q4 % NT == 0, "combine layout");
 
-  // Shared memory: the ring of ns stages, mbarriers (full[NS], empty[NS], gather),
-  // the fresh K/V row, the per-warp merge scratch, a flag word, and (cluster mode)
-  // the gather area where the cluster's splits deposit their partials in rank 0.
+  // Shared memory: the ring of ns stages, its mbarriers (full[NS], empty[NS], the
+  // cluster gather barrier, item-ready[4], item-free[4]), then the areas below.
   static constexpr int PART = G * (D + 2);    // floats of one split's partial (o, m, l per head)
-  static constexpr size_t bar_off(int ns) { return static_cast<size_t>(ns) * STAGE_BYTES; }
-  // barriers: full[NS], empty[NS], gather, item-ready[4], item-free[4]
-  static constexpr size_t fresh_off(int ns) { return bar_off(ns) + ((2 * NS + 9) * sizeof(uint64_t) + 15) / 16 * 16; }
-  static constexpr size_t scratch_off(int ns) { return fresh_off(ns) + 2 * ROW_BYTES; }
-  static constexpr size_t flag_off(int ns) {
-    return scratch_off(ns) + static_cast<size_t>(NC) * PART * sizeof(float);
-  }
+  static constexpr size_t BAR_BYTES = ((2 * NS + 9) * sizeof(uint64_t) + 15) / 16 * 16;
+  static constexpr size_t SCRATCH_BYTES = (static_cast<size_t>(NC) * PART * sizeof(float) + 15) / 16 * 16;
+  static constexpr size_t FLAG_BYTES = 32;    // ticket flag, persistent item queue[4]
   // merge of up to kCombSplits partials (workspace path) or 16 (cluster path)
   static constexpr int kCombSplits = 256;
   static constexpr size_t COMB_BYTES =
       ((2 * G * kCombSplits + G) * sizeof(float) + 15) / 16 * 16 + NT * 16;
-  static constexpr size_t comb_off(int ns) { return flag_off(ns) + 32; }  // flag + item queue[4]
-  static constexpr size_t gather_off(int ns) { return comb_off(ns) + COMB_BYTES; }
-  static constexpr size_t list_off(int ns, int cluster) {
-    return gather_off(ns) + static_cast<size_t>(cluster > 1 ? cluster : 0) * PART * sizeof(float);
+  struct Layout {
+    size_t bar, scratch, flag, comb, gather, list, total;
+  };
+  // The merge scratch and the combine area are used only after the CTA's tiles are
+  // consumed.  A CTA with a single item puts them over the ring (idle by then, every
+  // copy it issued having landed) when the ring is large enough; a persistent CTA keeps
+  // streaming its next item into the ring and gives them space of their own.
+  static bool over_ring(size_t ring_bytes, bool persistent) {
+    return !persistent && ring_bytes >= SCRATCH_BYTES + COMB_BYTES;
   }
-  // persistent mode: prefix sums of the work list, B + 1 ints
-  static constexpr size_t smem_bytes(int ns, int cluster, int list_ints = 0) {
-    return list_off(ns, cluster) + static_cast<size_t>(list_ints) * sizeof(int);
+  // ring_bytes: ns full stages, or (a split held whole) its full tiles' stages plus the
+  // last, partial tile packed as K rows then V rows
+  static Layout layout(size_t ring_bytes, int cluster, bool persistent, int list_ints) {
+    Layout L;
+    L.bar = ring_bytes;
+    size_t o = L.bar + BAR_BYTES;
+    L.flag = o;
+    o += FLAG_BYTES;
+    if (over_ring(ring_bytes, persistent)) {
+      L.scratch = 0;
+      L.comb = SCRATCH_BYTES;
+    } else {
+      L.scratch = o;
+      o += SCRATCH_BYTES;
+      L.comb = o;
+      o += COMB_BYTES;
+    }
+    L.gather = o;
+    o += static_cast<size_t>(cluster > 1 ? cluster : 0) * PART * sizeof(float);
+    L.list = o;
+    o += static_cast<size_t>(list_ints) * sizeof(int);
+    L.total = o;
+    return L;
   }
 };
 
@@ -349,18 +390,19 @@ __device__ __forceinline__ void combine_splits(const AttnParams& p, int b, int g
   const int h = qi / (D / 4);
   const int d4 = qi - h * (D / 4);
   const float4* op = reinterpret_cast<const float4*>(p.ws_o) + (head0 + h) * p.n_splits * (D / 4) + d4;
-  float4 v[BATCH];
-#pragma unroll
-  for (int k = 0; k < BATCH; ++k) {
-    const int s = r + k * R;
-    v[k] = (s < n_act) ? __ldcg(op + static_cast<int64_t>(s) * (D / 4)) : make_float4(0.f, 0.f, 0.f, 0.f);
-  }
+  // the (m, l) pairs gate the weights: requested first
   for (int i = tid; i < G * n_act; i += NT) {
     const int hh = i / n_act;
     const int s = i - hh * n_act;
     const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.ws_ml) + (head0 + hh) * p.n_splits + s);
     sm_w[i] = ml.x;
     sm_l[i] = ml.y;
+  }
+  float4 v[BATCH];
+#pragma unroll
+  for (int k = 0; k < BATCH; ++k) {
+    const int s = r + k * R;
+    v[k] = (s < n_act) ? __ldcg(op + static_cast<int64_t>(s) * (D / 4)) : make_float4(0.f, 0.f, 0.f, 0.f);
   }
   named_barrier(1, NT);
   // warp hh < G: M = max m, w_s = 2^(m_s - M), L = sum l_s w_s
@@ -483,19 +525,17 @@ decode_attn_kernel(const AttnParams p) {
   const int Hq = p.n_q_heads, Hkv = p.n_kv_heads;
 
   unsigned char* ring = smem;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::bar_off(ns));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + p.sm_bar);
   uint64_t* empty = full + C::NS;
   uint64_t* gbar = empty + C::NS;
   uint64_t* ibar = gbar + 1;   // persistent: item published in queue slot j
   uint64_t* ifree = ibar + 4;  // persistent: queue slot j read by every reader
-  unsigned char* fresh_k = smem + C::fresh_off(ns);
-  unsigned char* fresh_v = fresh_k + C::ROW_BYTES;
-  float* scratch = reinterpret_cast<float*>(smem + C::scratch_off(ns));
-  int* s_last = reinterpret_cast<int*>(smem + C::flag_off(ns));
-  volatile int* s_item = reinterpret_cast<volatile int*>(smem + C::flag_off(ns) + 16);
-  unsigned char* comb = smem + C::comb_off(ns);
-  int* s_pre = reinterpret_cast<int*>(smem + C::list_off(ns, p.cluster));  // persistent: [B+1]
-  float* gather = reinterpret_cast<float*>(smem + C::gather_off(ns));
+  float* scratch = reinterpret_cast<float*>(smem + p.sm_scratch);
+  int* s_last = reinterpret_cast<int*>(smem + p.sm_flag);
+  volatile int* s_item = reinterpret_cast<volatile int*>(smem + p.sm_flag + 16);
+  unsigned char* comb = smem + p.sm_comb;
+  int* s_pre = reinterpret_cast<int*>(smem + p.sm_list);  // persistent: [B+1]
+  float* gather = reinterpret_cast<float*>(smem + p.sm_gather);
   // Cluster mode: the n_splits CTAs of one (stream, kv head) form a cluster and merge
   // their partials in rank 0's shared memory (rank == split).
   const bool clustered = p.cluster > 1;
@@ -593,6 +633,7 @@ decode_attn_kernel(const AttnParams p) {
     // runs on across items, so the next item's tiles stream in while this one drains.
     const int pw = warp - NC;
     const uint64_t pol = l2_evict_first_policy();
+    const int inflight = (p.inflight > 0 && p.inflight < ns) ? p.inflight : 0;
     const unsigned char* src = static_cast<const unsigned char*>(pw == 0 ? p.k_cache : p.v_cache);
     int issued = 0;
     int stage = 0;
@@ -627,18 +668,25 @@ decode_attn_kernel(const AttnParams p) {
       if (!persistent && it.split >= it.n_act) break;  // outside the window
       const int32_t* bt = p.paged ? p.block_table + static_cast<int64_t>(it.b) * p.bt_stride : nullptr;
       for (int t = 0; t < it.ntiles; ++t) {
-        if (issued >= ns) {
-          int w = 1;
-          if (lane == 0) w = mbar_wait(&empty[stage], (round & 1u) ^ 1u) ? 1 : 0;
-          if (__shfl_sync(kFull, w, 0) == 0) {
-            if (lane == 0) set_err(p.err, TTS_EFLAG_TIMEOUT);
-            ok = false;
-            break;
+        int w = 1;
+        if (lane == 0) {
+          // pace: the tile issued `inflight` tiles ago has landed (its stage is not
+          // reused before this one is issued, since inflight <= ns)
+          if (inflight > 0 && issued >= inflight) {
+            const int k = issued - inflight;
+            w = mbar_wait(&full[k % ns], static_cast<uint32_t>(k / ns) & 1u) ? 1 : 0;
           }
+          if (w && issued >= ns) w = mbar_wait(&empty[stage], (round & 1u) ^ 1u) ? 1 : 0;
+        }
+        if (__shfl_sync(kFull, w, 0) == 0) {
+          if (lane == 0) set_err(p.err, TTS_EFLAG_TIMEOUT);
+          ok = false;
+          break;
         }
         const int row0 = it.r0 + t * T;
         const int rows = min(T, it.r0 + it.n_rows - row0);
-        unsigned char* dst = ring + stage * C::STAGE_BYTES + pw * C::TILE_BYTES;
+        // a stage holds the tile's K rows, then its V rows
+        unsigned char* dst = ring + stage * C::STAGE_BYTES + pw * rows * C::ROW_BYTES;
         if (lane == 0) mbar_arrive_expect_tx(&full[stage], static_cast<uint32_t>(rows) * C::ROW_BYTES);
         __syncwarp();
         if (!p.paged) {
@@ -696,6 +744,21 @@ decode_attn_kernel(const AttnParams p) {
   const int tid = threadIdx.x;  // < NT
   const int lr = lane % LPR;
   const int half = D / 2;
+  // The new K/V row of the window (fused) is folded in by one warp, from registers.
+  constexpr int kFreshWarp = 0;
+  float gq[EPL], gk[EPL];
+  float2 csr[EPL];
+  auto load_consts = [&](const Item& it) {
+    const int rope_pos = min(max(it.cur, 0), p.max_pos - 1);
+    const float2* cs_row = p.cs + static_cast<int64_t>(rope_pos) * half;
+    load_norm_consts<VE, VEC, LPR>(p.gamma_q, cs_row, lr, D, gq, csr);
+    if (it.has_fresh && warp == kFreshWarp) load_norm_consts<VE, VEC, LPR>(p.gamma_k, cs_row, lr, D, gk, csr);
+  };
+  // A single-item CTA knows its item up front.  With the prefetch flag cur_len is not
+  // written by the preceding launch, so the item is worked out before the dependency
+  // wait, while that launch finishes.
+  Item it0 = {};
+  if (!persistent && early) it0 = item_at(0);
   if (early) grid_wait();
   grid_launch_dependents();
   if (tid == 0) TTS_STAMP(1);
@@ -715,7 +778,7 @@ decode_attn_kernel(const AttnParams p) {
     } else if (round_item > 0) {
       break;
     }
-    const Item it = item_at(i);
+    const Item it = (!persistent && early) ? it0 : item_at(i);
     const bool active = it.split < it.n_act;
     if (!persistent && !active) {
       // Outside the window: nothing to stream.  A cluster peer still reports in when
@@ -740,41 +803,46 @@ decode_attn_kernel(const AttnParams p) {
       }
     }
 
-    float gq[EPL], gk[EPL];
-    float2 csr[EPL];
-    if (FUSED) {
-      const int rope_pos = min(max(it.cur, 0), p.max_pos - 1);
-      const float2* cs_row = p.cs + static_cast<int64_t>(rope_pos) * half;
-      load_norm_consts<VE, VEC, LPR>(p.gamma_q, cs_row, lr, D, gq, csr);
-      if (it.has_fresh) load_norm_consts<VE, VEC, LPR>(p.gamma_k, cs_row, lr, D, gk, csr);
-    }
+    if (FUSED) load_consts(it);
+    const bool fresh_here = FUSED && it.has_fresh && warp == kFreshWarp;
     float q[G][EPL];
 #pragma unroll
-    for (int h = 0; h < G; ++h) {
+    for (int h = 0; h < G; ++h)
       load_row_f32<VE, VEC, LPR>(
           p.q + static_cast<int64_t>(b) * p.q_stride + static_cast<int64_t>(g * G + h) * D, lr, q[h]);
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
       if (FUSED) norm_rope_regs<VE, VEC, LPR>(q[h], gq, csr, p.eps, lr, D);
 #pragma unroll
       for (int k = 0; k < EPL; ++k) q[h][k] *= p.scale_log2;
     }
 
+    float m_run[G], l_run[G], o[G][EPL];
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      m_run[h] = -INFINITY;
+      l_run[h] = 0.f;
+#pragma unroll
+      for (int k = 0; k < EPL; ++k) o[h][k] = 0.f;
+    }
+
     // Fused: build the new K/V row (norm + RoPE on k, v as is), convert it to the cache
-    // type, store it to the cache and keep a copy in shared memory for this CTA.
-    if (FUSED && it.has_fresh && warp == 0) {
+    // type and store it to the cache; then start this warp's softmax state with it.
+    // Every row group of the warp holds the row, so the score and the running maximum
+    // are warp-uniform; its weight 2^0 = 1 and its V row are counted by row group 0.
+    if (fresh_here) {
       float kr[EPL], vr[EPL];
       const int64_t roff = static_cast<int64_t>(b) * p.kv_new_stride + static_cast<int64_t>(g) * D;
       load_row_f32<VE, VEC, LPR>(p.k_new + roff, lr, kr);
       load_row_f32<VE, VEC, LPR>(p.v_new + roff, lr, vr);
       norm_rope_regs<VE, VEC, LPR>(kr, gk, csr, p.eps, lr, D);
-      if (lane < LPR) {
-        uint4 kp[VEC], vp[VEC];
+      uint4 kp[VEC], vp[VEC];
 #pragma unroll
-        for (int j = 0; j < VEC; ++j) {
-          kp[j] = pack_vec(kr + j * VE, static_cast<KvT*>(nullptr));
-          vp[j] = pack_vec(vr + j * VE, static_cast<KvT*>(nullptr));
-          *reinterpret_cast<uint4*>(fresh_k + (j * LPR + lr) * 16) = kp[j];
-          *reinterpret_cast<uint4*>(fresh_v + (j * LPR + lr) * 16) = vp[j];
-        }
+      for (int j = 0; j < VEC; ++j) {
+        kp[j] = pack_vec(kr + j * VE, static_cast<KvT*>(nullptr));
+        vp[j] = pack_vec(vr + j * VE, static_cast<KvT*>(nullptr));
+      }
+      if (lane < LPR) {
         size_t off;
         bool write = true;
         if (!p.paged) {
@@ -795,16 +863,34 @@ decode_attn_kernel(const AttnParams p) {
           }
         }
       }
-      __syncwarp();
-    }
-
-    float m_run[G], l_run[G], o[G][EPL];
+      // the row as the cache holds it (rounded to the cache type)
 #pragma unroll
-    for (int h = 0; h < G; ++h) {
-      m_run[h] = -INFINITY;
-      l_run[h] = 0.f;
+      for (int j = 0; j < VEC; ++j) {
+        float kx[VE], vx[VE];
+        KvVec<KvT>::unpack(kp[j], kx);
+        KvVec<KvT>::unpack(vp[j], vx);
 #pragma unroll
-      for (int k = 0; k < EPL; ++k) o[h][k] = 0.f;
+        for (int e = 0; e < VE; ++e) {
+          kr[j * VE + e] = kx[e];
+          vr[j * VE + e] = vx[e];
+        }
+      }
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+        for (int k = 0; k < EPL; k += 2) {
+          a0 = fmaf(q[h][k], kr[k], a0);
+          a1 = fmaf(q[h][k + 1], kr[k + 1], a1);
+        }
+        float sc = a0 + a1;
+#pragma unroll
+        for (int off = LPR / 2; off >= 1; off >>= 1) sc += __shfl_xor_sync(kFull, sc, off);
+        m_run[h] = sc;
+        l_run[h] = lane < LPR ? 1.f : 0.f;
+#pragma unroll
+        for (int k = 0; k < EPL; ++k) o[h][k] = lane < LPR ? vr[k] : 0.f;
+      }
     }
 
     if (tid == 0) { if (persistent) TTS_STAMP_ITEM(2, i); else TTS_STAMP(2); }
@@ -856,7 +942,7 @@ decode_attn_kernel(const AttnParams p) {
       if (mbar_wait(&full[sc], pc)) {
         if (n_full == 0 && tid == 0) { if (persistent) TTS_STAMP_ITEM(3, i); else TTS_STAMP(3); }
         tile_scores<C, KvT, true>(ring + sc * C::STAGE_BYTES, tail, warp, lane, q, s_cur);
-        tile_softmax_pv<C, KvT, true>(ring + sc * C::STAGE_BYTES + C::TILE_BYTES, tail, warp,
+        tile_softmax_pv<C, KvT, true>(ring + sc * C::STAGE_BYTES + tail * C::ROW_BYTES, tail, warp,
                                       lane, s_cur, m_run, l_run, o);
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[sc]);
@@ -869,10 +955,6 @@ decode_attn_kernel(const AttnParams p) {
       }
     }
     if (!ok) set_err(p.err, TTS_EFLAG_TIMEOUT);
-    if (FUSED && it.has_fresh && ok) {
-      tile_scores<C, KvT, true>(fresh_k, 1, warp, lane, q, s_cur);
-      tile_softmax_pv<C, KvT, true>(fresh_v, 1, warp, lane, s_cur, m_run, l_run, o);
-    }
     if (tid == 0) { if (persistent) TTS_STAMP_ITEM(4, i); else TTS_STAMP(4); }
 
     // Merge the row groups of this warp, then the warps of this CTA.
@@ -885,6 +967,8 @@ decode_attn_kernel(const AttnParams p) {
         for (int k = 0; k < EPL; ++k) o[h][k] += __shfl_xor_sync(kFull, o[h][k], off);
       }
     }
+    // the scratch may lie over the ring, whose last tiles other warps may still read
+    if (p.sm_scratch < p.sm_bar) named_barrier(1, NT);
     if (lane < LPR) {
 #pragma unroll
       for (int h = 0; h < G; ++h) {
@@ -1024,17 +1108,25 @@ cudaError_t launch_one(const AttnParams& p_in, cudaStream_t s) {
   using C = Cfg<KvT, D, G>;
   auto kern = decode_attn_kernel<KvT, D, G, FUSED>;
   // Per device: the kernel attributes, the largest cluster of this kernel the GPU can
-  // co-schedule (cluster mode is used only up to that size), the SM count and how many
-  // CTAs of the persistent configuration fit on one SM.
+  // co-schedule (cluster mode is used only up to that size), the SM count, how many CTAs
+  // of the persistent configuration fit on one SM, and the deepest ring that still lets
+  // two single-item CTAs share an SM.
   static int configured_for = -1;
   static int max_cluster = 1;
   static int n_sm = 1;
   static int per_sm = 1;
+  static size_t single_budget = 0;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
+  auto ring_stages = [](int kb) {
+    const int n = static_cast<int>((static_cast<size_t>(kb) << 10) / C::STAGE_BYTES);
+    return n < 1 ? 1 : (n > C::NS ? C::NS : n);
+  };
   if (configured_for != dev) {
-    const size_t max_smem = C::smem_bytes(C::NS, kMaxCluster, kMaxListStreams + 1);
+    size_t max_smem = C::layout(static_cast<size_t>(C::NS) * C::STAGE_BYTES, kMaxCluster, true, kMaxListStreams + 1).total;
+    const size_t single = C::layout(static_cast<size_t>(C::NS) * C::STAGE_BYTES, 0, false, 0).total;
+    if (single > max_smem) max_smem = single;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(max_smem));
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
@@ -1042,7 +1134,8 @@ cudaError_t launch_one(const AttnParams& p_in, cudaStream_t s) {
     cudaLaunchConfig_t q = {};
     q.gridDim = dim3(kMaxCluster, 1, 1);
     q.blockDim = dim3(C::THREADS);
-    q.dynamicSmemBytes = C::smem_bytes(C::NS, kMaxCluster);
+    q.dynamicSmemBytes =
+        C::layout(static_cast<size_t>(ring_stages(TTS_RING_KB_CLUSTER)) * C::STAGE_BYTES, kMaxCluster, false, 0).total;
     cudaLaunchAttribute qa[1];
     qa[0].id = cudaLaunchAttributeClusterDimension;
     qa[0].val.clusterDim.x = kMaxCluster;
@@ -1061,12 +1154,20 @@ cudaError_t launch_one(const AttnParams& p_in, cudaStream_t s) {
       n_sm = 1;
     }
     int occ = 0;
-    const size_t wave_smem = C::smem_bytes(TTS_STAGES_WAVES < C::NS ? TTS_STAGES_WAVES : C::NS, 0, 64);
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, C::THREADS, wave_smem) != cudaSuccess || occ < 1) {
+    const size_t stream_smem =
+        C::layout(static_cast<size_t>(ring_stages(TTS_RING_KB_STREAM)) * C::STAGE_BYTES, 0, true, 64).total;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, C::THREADS, stream_smem) != cudaSuccess || occ < 1) {
       cudaGetLastError();
       occ = 1;
     }
     per_sm = occ;
+    int sm_bytes = 0, reserved = 0;
+    if (cudaDeviceGetAttribute(&sm_bytes, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess) {
+      cudaGetLastError();
+      sm_bytes = 0;
+    }
+    single_budget = static_cast<size_t>(sm_bytes) / 2 - static_cast<size_t>(reserved);
     configured_for = dev;
   }
   AttnParams p = p_in;
@@ -1078,16 +1179,39 @@ cudaError_t launch_one(const AttnParams& p_in, cudaStream_t s) {
   p.cluster = (p.n_splits > 1 && p.n_splits <= max_cluster && p.ws_o != nullptr && one_wave) ? p.n_splits : 0;
   const long long resident = static_cast<long long>(n_sm) * per_sm;
   p.persistent = (p.cluster == 0 && ctas > resident && p.B <= kMaxListStreams) ? 1 : 0;
-  const int want = p.cluster > 1 ? TTS_STAGES_CLUSTER : TTS_STAGES_WAVES;
-  if (p.n_stages > want) p.n_stages = want;
-  cudaLaunchConfig_t cfg = {};
-  if (p.persistent) {
-    cfg.gridDim = dim3(static_cast<unsigned>(resident), 1, 1);
-    cfg.dynamicSmemBytes = C::smem_bytes(p.n_stages, 0, p.B + 1);
+  // Ring: a split held whole when it fits two CTAs to an SM, else as many full stages as
+  // the mode allows (at most the split's tiles).
+  const int ntiles = (p.split_len + C::T - 1) / C::T;
+  size_t ring_bytes;
+  if (p.persistent || p.cluster > 1) {
+    int ns = ring_stages(p.persistent ? TTS_RING_KB_STREAM : TTS_RING_KB_CLUSTER);
+    if (ns > ntiles) ns = ntiles;
+    p.n_stages = ns;
+    ring_bytes = static_cast<size_t>(ns) * C::STAGE_BYTES;
   } else {
-    cfg.gridDim = dim3(p.n_splits, p.n_kv_heads, p.B);
-    cfg.dynamicSmemBytes = C::smem_bytes(p.n_stages, p.cluster);
+    const int last = p.split_len - (ntiles - 1) * C::T;
+    const size_t whole = static_cast<size_t>(ntiles - 1) * C::STAGE_BYTES + 2 * static_cast<size_t>(last) * C::ROW_BYTES;
+    if (ntiles <= C::NS && C::layout(whole, 0, false, 0).total <= single_budget) {
+      p.n_stages = ntiles;
+      ring_bytes = whole;
+    } else {
+      int ns = ntiles < C::NS ? ntiles : C::NS;
+      while (ns > 1 && C::layout(static_cast<size_t>(ns) * C::STAGE_BYTES, 0, false, 0).total > single_budget) --ns;
+      p.n_stages = ns;
+      ring_bytes = static_cast<size_t>(ns) * C::STAGE_BYTES;
+    }
   }
+  const typename C::Layout L = C::layout(ring_bytes, p.cluster, p.persistent != 0, p.persistent ? p.B + 1 : 0);
+  p.inflight = p.persistent ? TTS_INFLIGHT_STREAM : TTS_INFLIGHT_SINGLE;
+  p.sm_bar = static_cast<uint32_t>(L.bar);
+  p.sm_scratch = static_cast<uint32_t>(L.scratch);
+  p.sm_flag = static_cast<uint32_t>(L.flag);
+  p.sm_comb = static_cast<uint32_t>(L.comb);
+  p.sm_gather = static_cast<uint32_t>(L.gather);
+  p.sm_list = static_cast<uint32_t>(L.list);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = p.persistent ? dim3(static_cast<unsigned>(resident), 1, 1) : dim3(p.n_splits, p.n_kv_heads, p.B);
+  cfg.dynamicSmemBytes = L.total;
   cfg.blockDim = dim3(C::THREADS);
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
@@ -1118,28 +1242,11 @@ AttnGeometry geometry_of() {
   return AttnGeometry{C::T, C::NS, C::STAGE_BYTES, C::THREADS};
 }
 
-template <typename KvT, int D>
-size_t smem_of(int group, int ns) {
-  switch (group) {
-    case 1: return Cfg<KvT, D, 1>::smem_bytes(ns, kMaxCluster, kMaxListStreams + 1);
-    case 2: return Cfg<KvT, D, 2>::smem_bytes(ns, kMaxCluster, kMaxListStreams + 1);
-    case 4: return Cfg<KvT, D, 4>::smem_bytes(ns, kMaxCluster, kMaxListStreams + 1);
-    default: return 0;
-  }
-}
-
 }  // namespace
 
 AttnGeometry attn_geometry(int kv_bf16, int head_dim) {
   if (kv_bf16) return head_dim == 64 ? geometry_of<__nv_bfloat16, 64>() : geometry_of<__nv_bfloat16, 128>();
   return head_dim == 64 ? geometry_of<float, 64>() : geometry_of<float, 128>();
-}
-
-size_t attn_smem_bytes(int kv_bf16, int head_dim, int group, int n_stages) {
-  if (kv_bf16)
-    return head_dim == 64 ? smem_of<__nv_bfloat16, 64>(group, n_stages)
-                          : smem_of<__nv_bfloat16, 128>(group, n_stages);
-  return head_dim == 64 ? smem_of<float, 64>(group, n_stages) : smem_of<float, 128>(group, n_stages);
 }
 
 cudaError_t launch_decode_attn(const AttnParams& p, int kv_bf16, int head_dim, int group,

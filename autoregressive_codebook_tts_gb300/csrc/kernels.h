@@ -78,9 +78,14 @@ struct AttnParams {
   int* ws_sched;        // [2] persistent mode: work counter, finished-CTA counter
   int n_splits;         // grid.x
   int split_len;        // positions per split, a multiple of the tile
-  int n_stages;         // pipeline depth actually used (<= the kernel's maximum)
+  int n_stages;         // ring stages actually used (set by the launcher)
   int cluster;          // set by the launcher: splits per cluster (>1 = cluster merge)
   int persistent;       // set by the launcher: 1 = fixed grid walking the active items
+  int inflight;         // set by the launcher: tiles a producer keeps in flight (0 = ring)
+  // set by the launcher: byte offsets in dynamic shared memory of the ring's mbarriers
+  // (the ring starts at 0), the per-warp merge scratch, the flag word and item queue,
+  // the combine area, the cluster gather area and the persistent work list
+  uint32_t sm_bar, sm_scratch, sm_flag, sm_comb, sm_gather, sm_list;
   uint32_t flags;
   int32_t* err;
 };
@@ -100,7 +105,6 @@ struct AttnGeometry {
   int threads;       // consumer warps + one producer warp
 };
 AttnGeometry attn_geometry(int kv_bf16, int head_dim);
-size_t attn_smem_bytes(int kv_bf16, int head_dim, int group, int n_stages);
 cudaError_t launch_decode_attn(const AttnParams& p, int kv_bf16, int head_dim, int group,
                                bool fused, cudaStream_t s);
 

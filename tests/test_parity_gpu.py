@@ -210,8 +210,10 @@ def test_decode_attn_poison_padding_and_quantum_invariance(tts):
         ws = tts.workspace(desc, 0)
         out = torch.empty(1, 16, 128, device="cuda")
         nv = torch.tensor([38], dtype=torch.int32, device="cuda")
-        tts.tts_decode_attn(L.d_q, L.d_K, L.d_V, desc, nv, scale_of(w), out, ws)
+        ef = err_flag()
+        tts.tts_decode_attn(L.d_q, L.d_K, L.d_V, desc, nv, scale_of(w), out, ws, 0, ef)
         outs.append(out.cpu())
+        assert ef.item() == 0
     torch.cuda.synchronize()
     assert all(torch.isfinite(o).all() for o in outs)
     assert all(torch.equal(outs[0], o) for o in outs[1:])
@@ -223,11 +225,14 @@ def test_decode_attn_split_counts_agree(tts):
     desc = L.desc(tts)
     nv = (L.d_cur + 1).to(torch.int32)
     res = []
+    # one split; a few; a cluster; a persistent grid with 2-tile and 1-tile splits
     for ns in [1, 2, 16, 64, 128]:
         ws = tts.workspace(desc, ns)
         out = torch.empty(1, 16, 128, device="cuda")
-        tts.tts_decode_attn(L.d_q, L.d_K, L.d_V, desc, nv, scale_of(w), out, ws, ns)
+        ef = err_flag()
+        tts.tts_decode_attn(L.d_q, L.d_K, L.d_V, desc, nv, scale_of(w), out, ws, ns, ef)
         res.append(out.cpu().numpy())
+        assert ef.item() == 0, ns
     torch.cuda.synchronize()
     ref, _, _ = oracle.decode_attn(L.q_np(), cache_np(L.K), cache_np(L.V), L.layout(),
                                    np.array([3001], np.int32), scale_of(w))
@@ -254,8 +259,10 @@ def test_decode_attn_paged_equals_contiguous(tts):
         desc = L.desc(tts)
         ws = tts.workspace(desc, 8)
         out = torch.empty(4, 16, 128, device="cuda")
-        tts.tts_decode_attn(Lc.d_q, L.d_K, L.d_V, desc, nv, scale_of(wc), out, ws, 8)
+        ef = err_flag()
+        tts.tts_decode_attn(Lc.d_q, L.d_K, L.d_V, desc, nv, scale_of(wc), out, ws, 8, ef)
         outs.append(out.cpu())
+        assert ef.item() == 0
     torch.cuda.synchronize()
     assert torch.equal(outs[0], outs[1])
 
@@ -271,15 +278,17 @@ def test_decode_attn_batched_equals_per_stream(tts):
     nv = (L.d_cur + 1).to(torch.int32)
     ws = tts.workspace(desc, 8)
     out = torch.empty(5, 16, 128, device="cuda")
-    tts.tts_decode_attn(L.d_q, L.d_K, L.d_V, desc, nv, scale_of(w), out, ws, 8)
+    ef = err_flag()
+    tts.tts_decode_attn(L.d_q, L.d_K, L.d_V, desc, nv, scale_of(w), out, ws, 8, ef)
     w1 = W.workload("batched", B=1, layers=1)
     for b in range(5):
         d1 = tts.kv_desc(1, 16, 8, 128, 4096, "bf16")
         ws1 = tts.workspace(d1, 8)
         o1 = torch.empty(1, 16, 128, device="cuda")
         tts.tts_decode_attn(L.d_q[b:b + 1], L.d_K[b:b + 1], L.d_V[b:b + 1], d1, nv[b:b + 1],
-                            scale_of(w1), o1, ws1, 8)
+                            scale_of(w1), o1, ws1, 8, ef)
         torch.cuda.synchronize()
+        assert ef.item() == 0
         assert row_rel_err(o1[0].cpu().numpy(), out[b].cpu().numpy()) <= 1e-6
 
 
