@@ -989,14 +989,19 @@ decode_attn_kernel(const AttnParams p) {
     for (int idx = tid; idx < G * D; idx += NT) {
       const int h = idx / D;
       const int d = idx - h * D;
+      float mw[NC];
       float M = -INFINITY;
 #pragma unroll
-      for (int w = 0; w < NC; ++w) M = fmaxf(M, scratch[(w * G + h) * (D + 2) + D]);
+      for (int w = 0; w < NC; ++w) {
+        mw[w] = scratch[(w * G + h) * (D + 2) + D];
+        M = fmaxf(M, mw[w]);
+      }
       float L = 0.f, O = 0.f;
 #pragma unroll
       for (int w = 0; w < NC; ++w) {
         const float* srcp = scratch + (w * G + h) * (D + 2);
-        const float f = (srcp[D] == -INFINITY) ? 0.f : exp2f(srcp[D] - M);
+        // a warp without rows has m = -inf and l = o = 0; some warp always has rows
+        const float f = (mw[w] == -INFINITY) ? 0.f : fast_exp2(mw[w] - M);
         L = fmaf(srcp[D + 1], f, L);
         O = fmaf(srcp[d], f, O);
       }

@@ -111,8 +111,12 @@ __device__ __forceinline__ void named_barrier(int id, int threads) {
 // ---------------------------------------------------------------------------
 // Vector loads and bf16 unpacking
 // ---------------------------------------------------------------------------
+// 16 bytes from shared memory (an explicit shared-window load, never a generic one).
 __device__ __forceinline__ uint4 lds128(const void* p) {
-  return *reinterpret_cast<const uint4*>(p);
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(smem_u32(p)));
+  return v;
 }
 
 // Eight bf16 packed in a uint4 (element 0 in the low half of .x) -> eight floats.
