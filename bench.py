@@ -293,6 +293,25 @@ def cpu_oracle_sample(state, w, cur_len, seconds):
                                    f"of the {w.name} workload at {lens}, {dt:.1f} s")
 
 
+def max_over_ranks(values, world, device=None):
+    """This rank's timings (seconds) -> their maxima over all ranks, on every rank.  The
+    ranks are independent replicas (own streams, own caches); this reduction of the
+    timings is the only collective of a multi-GPU run."""
+    if world == 1:
+        return [float(v) for v in values]
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
+
+
+def whole_job_gbs(world, bytes_per_step, steps, seconds):
+    """Whole-job throughput: every rank moved bytes_per_step per step; the slowest rank's
+    time counts."""
+    return world * bytes_per_step * steps / seconds / 1e9
+
+
 def run_native(args, rank, world):
     import torch
     from autoregressive_codebook_tts_gb300 import build as b
@@ -374,10 +393,7 @@ def run_native(args, rank, world):
     if int(h_ef.item()) != 0:
         raise RuntimeError(f"device error flag {int(h_ef.item())}")
 
-    if world > 1:
-        tt = torch.tensor([t_frame, t_layers, t_e2e], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        t_frame, t_layers, t_e2e = [float(x) for x in tt.tolist()]
+    t_frame, t_layers, t_e2e = max_over_ranks([t_frame, t_layers, t_e2e], world, dev)
 
     sweep = None
     if args.sweep and args.workload == "talker" and rank == 0:
@@ -400,7 +416,7 @@ def run_native(args, rank, world):
             del fr, ly, st, gf, flush
 
     peak, peak_kind = hbm_peak()
-    value = world * frame_bytes * args.steps / t_frame / 1e9
+    value = whole_job_gbs(world, frame_bytes, args.steps, t_frame)
     dom_bytes = per_layer
     dom_time = t_layers / (args.steps * w.layers)
     achieved = dom_bytes / dom_time / 1e9
@@ -436,7 +452,7 @@ def run_native(args, rank, world):
                      "kernel": "decode_attn_kernel<fused> (tts_decode_step)",
                      "peak_source": f"{peak_kind} HBM copy bandwidth",
                      "bytes_per_launch": dom_bytes, "us_per_launch": round(dom_time * 1e6, 3)},
-        "e2e": {"value": round(world * frame_bytes * e2e_steps / t_e2e / 1e9, 2), "unit": "GB/s",
+        "e2e": {"value": round(whole_job_gbs(world, frame_bytes, e2e_steps, t_e2e), 2), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(t_e2e / e2e_steps * 1e3, 5)},
         "gpu_launches": args.steps * (1 + w.layers),
