@@ -21,6 +21,9 @@ Steps and the passages they follow (page titles as printed on the pages):
 * ``decode_step`` / ``predictor_frame`` -- compositions of the above in the order the
   KV cache section gives (norm+RoPE, write the new row, attend; the predictor resets
   its 16-slot cache, prefills T=2 and then decodes 14 single tokens).
+* ``prefill_step`` -- the same section's prefill: T new positions per stream written
+  into the cache, each of their queries attending causally over [0, its position],
+  i.e. T decode queries whose windows end at their own rows.
 """
 from __future__ import annotations
 
@@ -223,6 +226,32 @@ def decode_step(q, k, v, gamma_q, gamma_k, eps, base, k_cache, v_cache, layout: 
     kn = rms_norm_rope(k, gamma_k, eps, cur_len, base)
     kv_set_rows(kn, v, k_cache, v_cache, layout, cur_len)
     out, _, _ = decode_attn(qn, k_cache, v_cache, layout, cur_len + 1, scale)
+    return out
+
+
+def prefill_step(q, k, v, gamma_q, gamma_k, eps, base, k_cache, v_cache, layout: KvLayout,
+                 start, scale):
+    """T new positions per stream ("qwentts.cpp", KV cache section: the prefill writes
+    the prompt's rows from the reset position, causally).  Stream b's rows t < T sit at
+    position start[b] + t.  Every q and k row is RMS-normed and rotated at its own
+    position, every k/v row is written into the cache at it, and query t attends over
+    the window [0, start[b] + t + 1): the rows before the prompt and the prompt's rows
+    up to its own.  Mutates the caches; returns out [B][T][Hq][D] f32.
+
+    q: [B][T][Hq][D], k, v: [B][T][Hkv][D] (f32); start: [B] int32."""
+    q = _c(q, np.float32)
+    k = _c(k, np.float32)
+    v = _c(v, np.float32)
+    start = _c(start, np.int32)
+    B, T, Hq, D = q.shape
+    pos = start[:, None] + np.arange(T, dtype=np.int32)[None, :]
+    for t in range(T):  # all of the prompt's rows are in the cache before any query
+        kn = rms_norm_rope(k[:, t], gamma_k, eps, pos[:, t], base)
+        kv_set_rows(kn, v[:, t], k_cache, v_cache, layout, pos[:, t])
+    out = np.empty((B, T, Hq, D), np.float32)
+    for t in range(T):
+        qn = rms_norm_rope(q[:, t], gamma_q, eps, pos[:, t], base)
+        out[:, t], _, _ = decode_attn(qn, k_cache, v_cache, layout, pos[:, t] + 1, scale)
     return out
 
 

@@ -445,3 +445,92 @@ def test_predictor_frame_reset_masks_the_previous_frame():
             assert np.array_equal(o2[t][l], o3[t][l])
     for j in range(15):
         assert np.array_equal(e2[j], tabs[j][c2[:, j]])
+
+
+# ---------------------------------------------------------------------------
+# Prefill: T new positions per stream, causal
+# ---------------------------------------------------------------------------
+def _prefill_case(rng, B, T, Hq, Hkv, D, cap):
+    q = rng.standard_normal((B, T, Hq, D)).astype(np.float32)
+    k = rng.standard_normal((B, T, Hkv, D)).astype(np.float32)
+    v = rng.standard_normal((B, T, Hkv, D)).astype(np.float32)
+    gq = rng.uniform(0.5, 1.5, D).astype(np.float32)
+    gk = rng.uniform(0.5, 1.5, D).astype(np.float32)
+    kc = rng.standard_normal((B, Hkv, cap, D)).astype(np.float32)
+    vc = rng.standard_normal((B, Hkv, cap, D)).astype(np.float32)
+    return q, k, v, gq, gk, kc, vc
+
+
+@pytest.mark.parametrize("start", [0, 9])
+def test_prefill_matches_torch_causal_sdpa(start):
+    """torch scaled_dot_product_attention in float64 over [rows before the prompt | the
+    prompt's rows] with a mask that lets prompt query t see every earlier row and the
+    prompt's rows 0..t; q and k rows rotated at positions start + t, computed here."""
+    rng = np.random.default_rng(21)
+    B, T, Hq, Hkv, D, cap = 2, 6, 4, 2, 16, 32
+    q, k, v, gq, gk, kc, vc = _prefill_case(rng, B, T, Hq, Hkv, D, cap)
+    eps = np.float32(1e-6)
+    kc0, vc0 = kc.copy(), vc.copy()
+    out = oracle.prefill_step(q, k, v, gq, gk, eps, 1e6, kc, vc, oracle.KvLayout(B, Hkv, D, cap),
+                              np.array([start] * B, np.int32), 1.0 / math.sqrt(D))
+    n = start + T
+    mask = np.zeros((T, n), bool)
+    for t in range(T):
+        mask[t, :start + t + 1] = True
+    for b in range(B):
+        qn = np.stack([oracle.rms_norm_rope(q[b, t][None], gq, eps, np.array([start + t], np.int32), 1e6)[0]
+                       for t in range(T)])            # [T][Hq][D]
+        kn = np.stack([oracle.rms_norm_rope(k[b, t][None], gk, eps, np.array([start + t], np.int32), 1e6)[0]
+                       for t in range(T)])            # [T][Hkv][D]
+        K = np.concatenate([kc0[b, :, :start], kn.transpose(1, 0, 2)], axis=1).astype(np.float64)
+        V = np.concatenate([vc0[b, :, :start], v[b].transpose(1, 0, 2)], axis=1).astype(np.float64)
+        ref = F.scaled_dot_product_attention(
+            torch.from_numpy(qn.transpose(1, 0, 2).astype(np.float64))[None],
+            torch.from_numpy(K)[None], torch.from_numpy(V)[None],
+            attn_mask=torch.from_numpy(mask), enable_gqa=True)[0].numpy()   # [Hq][T][D]
+        np.testing.assert_allclose(out[b], ref.transpose(1, 0, 2), rtol=1e-6, atol=1e-7)
+        # the prompt's rows are in the cache at their positions; the rest is untouched
+        assert np.array_equal(kc[b, :, start:n], kn.transpose(1, 0, 2))
+        assert np.array_equal(vc[b, :, start:n], v[b].transpose(1, 0, 2))
+        assert np.array_equal(kc[b, :, :start], kc0[b, :, :start])
+        assert np.array_equal(kc[b, :, n:], kc0[b, :, n:])
+
+
+@pytest.mark.parametrize("kv_dtype", ["f32", "bf16"])
+def test_prefill_equals_decode_steps_one_by_one(kv_dtype):
+    """A prompt of T rows in one prefill = T decode steps at start, start + 1, ...: every
+    query's window ends at its own row, so writing the later rows first changes nothing.
+    Also T = 1 is exactly one decode step."""
+    rng = np.random.default_rng(22)
+    B, T, Hq, Hkv, D, cap = 3, 5, 4, 2, 16, 24
+    q, k, v, gq, gk, kc, vc = _prefill_case(rng, B, T, Hq, Hkv, D, cap)
+    if kv_dtype == "bf16":
+        kc, vc = oracle.bf16_rne_array(kc), oracle.bf16_rne_array(vc)
+    start = np.array([0, 7, 19], np.int32)
+    lay = oracle.KvLayout(B, Hkv, D, cap, kv_dtype)
+    kp, vp = kc.copy(), vc.copy()
+    out = oracle.prefill_step(q, k, v, gq, gk, np.float32(1e-6), 1e6, kp, vp, lay, start, 0.3)
+    ks, vs = kc.copy(), vc.copy()
+    for t in range(T):
+        o = oracle.decode_step(q[:, t], k[:, t], v[:, t], gq, gk, np.float32(1e-6), 1e6, ks, vs,
+                               lay, start + t, 0.3)
+        assert np.array_equal(o, out[:, t]), t
+    assert np.array_equal(kp, ks) and np.array_equal(vp, vs)
+    k1, v1 = kc.copy(), vc.copy()
+    o1 = oracle.prefill_step(q[:, :1], k[:, :1], v[:, :1], gq, gk, np.float32(1e-6), 1e6, k1, v1,
+                             lay, start, 0.3)
+    assert np.array_equal(o1[:, 0], out[:, 0])
+
+
+def test_prefill_first_query_of_an_empty_cache_is_its_own_value_row():
+    """start = 0 on a NaN-filled cache: query 0 sees only row 0 (o = v_0 exactly), and no
+    query reads past its own row (the NaN rows after the prompt never leak)."""
+    rng = np.random.default_rng(23)
+    B, T, Hq, Hkv, D, cap = 1, 4, 4, 2, 8, 16
+    q, k, v, gq, gk, _, _ = _prefill_case(rng, B, T, Hq, Hkv, D, cap)
+    kc = np.full((B, Hkv, cap, D), np.nan, np.float32)
+    vc = kc.copy()
+    out = oracle.prefill_step(q, k, v, gq, gk, np.float32(1e-6), 1e6, kc, vc,
+                              oracle.KvLayout(B, Hkv, D, cap), np.zeros(B, np.int32), 0.5)
+    assert np.array_equal(out[0, 0], np.repeat(v[0, 0], Hq // Hkv, axis=0))
+    assert np.isfinite(out).all()
