@@ -123,6 +123,8 @@ tts_status prepare_attn(const tts_kv_desc* d, const void* k_cache, const void* v
     p.ws_sched = nullptr;
   }
   p.n_stages = 0;  // chosen by the launcher
+  p.q_per_stream = 1;
+  p.lens_add = 0;
   p.k_cache = k_cache;
   p.v_cache = v_cache;
   p.B = d->B;
@@ -346,6 +348,79 @@ tts_status tts_decode_step(const float* q, const float* k, const float* v, int64
   p.err = err_flag;
   return from_cuda(launch_decode_attn(p, d->kv_dtype == TTS_BF16, d->head_dim,
                                       d->n_q_heads / d->n_kv_heads, true, as_stream(stream)));
+}
+
+size_t tts_prefill_workspace_size(const tts_kv_desc* d, int32_t T, int32_t n_splits) {
+  if (check_desc(d) != TTS_OK || T < 1 || static_cast<int64_t>(d->B) * T > 65535) return 0;
+  tts_kv_desc dq = *d;  // the B*T queries take the place of the streams
+  dq.B = d->B * T;
+  return tts_decode_attn_workspace_size(&dq, n_splits);
+}
+
+tts_status tts_prefill_step(float* q, const float* k, const float* v, int64_t row_stride,
+                            const float* gamma_q, const float* gamma_k, float eps,
+                            const float* rope_cs, int32_t rope_max_pos, void* k_cache,
+                            void* v_cache, const tts_kv_desc* d, const int32_t* start_pos,
+                            int32_t T, float scale, float* out, void* workspace, size_t ws_bytes,
+                            int32_t n_splits, int32_t* err_flag, void* stream) {
+  if (q == nullptr || k == nullptr || v == nullptr || gamma_q == nullptr || gamma_k == nullptr ||
+      rope_cs == nullptr || start_pos == nullptr || out == nullptr || d == nullptr)
+    return TTS_ERR_NULL;
+  tts_status st = check_desc(d);
+  if (st != TTS_OK) return st;
+  if (T < 1 || static_cast<int64_t>(d->B) * T > 65535) return TTS_ERR_SHAPE;
+  tts_kv_desc dq = *d;
+  dq.B = d->B * T;
+  AttnParams p = {};
+  int used = 0;
+  st = prepare_attn(&dq, k_cache, v_cache, workspace, ws_bytes, n_splits, p, used);
+  if (st != TTS_OK) return st;
+  if (row_stride < static_cast<int64_t>(d->n_q_heads) * d->head_dim || rope_max_pos < 1 || !(eps >= 0.f))
+    return TTS_ERR_SHAPE;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(gamma_q) ||
+      !aligned16(gamma_k) || !aligned16(rope_cs) || row_stride % 4 != 0)
+    return TTS_ERR_ALIGN;
+  if (!std::isfinite(scale)) return TTS_ERR_SHAPE;
+  cudaStream_t s = as_stream(stream);
+  PrefillRowsParams rp = {};
+  rp.q = q;
+  rp.k = k;
+  rp.v = v;
+  rp.row_stride = row_stride;
+  rp.gamma_q = gamma_q;
+  rp.gamma_k = gamma_k;
+  rp.eps = eps;
+  rp.cs = reinterpret_cast<const float2*>(rope_cs);
+  rp.max_pos = rope_max_pos;
+  rp.k_cache = k_cache;
+  rp.v_cache = v_cache;
+  rp.B = d->B;
+  rp.T = T;
+  rp.n_q_heads = d->n_q_heads;
+  rp.n_kv_heads = d->n_kv_heads;
+  rp.head_dim = d->head_dim;
+  rp.capacity = d->capacity;
+  rp.kv_bf16 = d->kv_dtype == TTS_BF16;
+  rp.paged = d->paged;
+  rp.page_size = d->paged ? d->page_size : 1;
+  rp.n_pages = d->paged ? d->n_pages : 0;
+  rp.bt_stride = d->paged ? d->bt_stride : 0;
+  rp.block_table = d->paged ? d->block_table : nullptr;
+  rp.start = start_pos;
+  rp.err = err_flag;
+  st = from_cuda(launch_prefill_rows(rp, s));
+  if (st != TTS_OK) return st;
+  p.q = q;
+  p.q_stride = row_stride;
+  p.lens = start_pos;
+  p.q_per_stream = T;
+  p.lens_add = 1;  // query t's window is [0, start + t + 1)
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.out = out;
+  p.err = err_flag;
+  p.flags &= ~TTS_KV_PREFETCH_BEFORE_WAIT;  // the rows launch writes the cache
+  return from_cuda(launch_decode_attn(p, d->kv_dtype == TTS_BF16, d->head_dim,
+                                      d->n_q_heads / d->n_kv_heads, false, s));
 }
 
 }  // extern "C"

@@ -469,9 +469,12 @@ __device__ __forceinline__ void combine_splits(const AttnParams& p, int b, int g
   }
 }
 
-// One unit of work: the rows [r0, r0 + split_len) of one (stream, kv head).
+// One unit of work: the rows [r0, r0 + split_len) of one (query stream, kv head).
+// Query stream b reads the cache of stream cb = b / q_per_stream (a prefill's
+// q_per_stream queries share their stream's cache).
 struct Item {
   int b, g, split;
+  int cb;         // cache stream
   int nv;         // window length (clamped)
   int cur;        // fused: position of the new row
   bool fresh_ok;  // fused: cur is a valid position
@@ -484,6 +487,7 @@ template <bool FUSED>
 __device__ __forceinline__ Item make_item(const AttnParams& p, int T, int b, int g, int split, int raw) {
   Item it;
   it.b = b;
+  it.cb = b / p.q_per_stream;
   it.g = g;
   it.split = split;
   int cache_end;
@@ -504,6 +508,13 @@ __device__ __forceinline__ Item make_item(const AttnParams& p, int T, int b, int
   it.ntiles = (it.n_rows + T - 1) / T;
   it.n_act = min(p.n_splits, (it.nv + p.split_len - 1) / p.split_len);
   return it;
+}
+
+// The window input of query stream b: cur_len (fused) or n_valid, read from its cache
+// stream's entry plus the query's offset within that stream (prefill queries).
+__device__ __forceinline__ int raw_len(const AttnParams& p, int b) {
+  const int cb = b / p.q_per_stream;
+  return __ldcg(p.lens + cb) + (b - cb * p.q_per_stream) + p.lens_add;
 }
 
 __device__ __forceinline__ int n_active(const AttnParams& p, int raw, bool fused) {
@@ -577,7 +588,7 @@ decode_attn_kernel(const AttnParams p) {
       int carry = 0;
       for (int b0 = 0; b0 < p.B; b0 += 32) {
         const int bb = b0 + lane;
-        int v = bb < p.B ? Hkv * n_active(p, __ldcg(p.lens + bb), FUSED) : 0;
+        int v = bb < p.B ? Hkv * n_active(p, raw_len(p, bb), FUSED) : 0;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
           const int u = __shfl_up_sync(kFull, v, off);
@@ -610,7 +621,7 @@ decode_attn_kernel(const AttnParams p) {
       g = blockIdx.y;
       split = blockIdx.x;
     }
-    return make_item<FUSED>(p, T, b, g, split, __ldcg(p.lens + b));
+    return make_item<FUSED>(p, T, b, g, split, raw_len(p, b));
   };
   // Persistent mode: queue slot j = k % 4 carries this CTA's k-th item from the
   // scheduler (the K producer's lane 0) to the V producer and the consumer warps;
@@ -666,7 +677,7 @@ decode_attn_kernel(const AttnParams p) {
       }
       const Item it = item_at(i);
       if (!persistent && it.split >= it.n_act) break;  // outside the window
-      const int32_t* bt = p.paged ? p.block_table + static_cast<int64_t>(it.b) * p.bt_stride : nullptr;
+      const int32_t* bt = p.paged ? p.block_table + static_cast<int64_t>(it.cb) * p.bt_stride : nullptr;
       for (int t = 0; t < it.ntiles; ++t) {
         int w = 1;
         if (lane == 0) {
@@ -692,7 +703,7 @@ decode_attn_kernel(const AttnParams p) {
         if (!p.paged) {
           if (lane == 0) {
             const size_t off =
-                ((static_cast<size_t>(it.b) * Hkv + it.g) * p.capacity + row0) * C::ROW_BYTES;
+                ((static_cast<size_t>(it.cb) * Hkv + it.g) * p.capacity + row0) * C::ROW_BYTES;
             bulk_g2s(dst, src + off, static_cast<uint32_t>(rows) * C::ROW_BYTES, &full[stage], pol);
           }
         } else {
@@ -798,7 +809,7 @@ decode_attn_kernel(const AttnParams p) {
         if (!it.fresh_ok) set_err(p.err, TTS_EFLAG_POS_RANGE);
         if (it.cur < 0 || it.cur >= p.max_pos) set_err(p.err, TTS_EFLAG_POS_RANGE);
       } else {
-        const int raw = __ldcg(p.lens + b);
+        const int raw = raw_len(p, b);
         if (raw < 1 || raw > p.capacity) set_err(p.err, TTS_EFLAG_NVALID);
       }
     }
@@ -1183,7 +1194,9 @@ cudaError_t launch_one(const AttnParams& p_in, cudaStream_t s) {
   const bool one_wave = ctas <= n_sm;
   p.cluster = (p.n_splits > 1 && p.n_splits <= max_cluster && p.ws_o != nullptr && one_wave) ? p.n_splits : 0;
   const long long resident = static_cast<long long>(n_sm) * per_sm;
-  p.persistent = (p.cluster == 0 && ctas > resident && p.B <= kMaxListStreams) ? 1 : 0;
+  // (the work counters live in the workspace, which a one-split launch does not have;
+  // such a grid runs as several plain waves)
+  p.persistent = (p.cluster == 0 && ctas > resident && p.B <= kMaxListStreams && p.ws_sched != nullptr) ? 1 : 0;
   // Ring: a split held whole when it fits two CTAs to an SM, else as many full stages as
   // the mode allows (at most the split's tiles).
   const int ntiles = (p.split_len + C::T - 1) / C::T;

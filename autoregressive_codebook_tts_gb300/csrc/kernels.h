@@ -69,7 +69,10 @@ struct AttnParams {
   int B, n_q_heads, n_kv_heads, capacity;
   int paged, page_size, page_shift, n_pages, bt_stride;
   const int32_t* block_table;
-  const int32_t* lens;  // standalone: n_valid; fused: cur_len
+  const int32_t* lens;  // standalone: n_valid; fused: cur_len; prefill: start position
+  // Query streams per cache stream (1, or a prefill's T queries) and the constant added
+  // to lens[cache stream] + query offset to form the window input (prefill: 1).
+  int q_per_stream, lens_add;
   float scale_log2;     // softmax scale * log2(e)
   float* out;
   float* ws_o;          // [B][Hq][n_splits][D]
@@ -90,12 +93,34 @@ struct AttnParams {
   int32_t* err;
 };
 
+// Prefill rows: for query row r = b * T + t (position start[b] + t), q RMS-normed and
+// rotated in place, k normed and rotated into the cache, v copied into the cache.
+struct PrefillRowsParams {
+  float* q;
+  const float* k;
+  const float* v;
+  int64_t row_stride;   // floats between consecutive rows r of q, k and v
+  const float* gamma_q;
+  const float* gamma_k;
+  float eps;
+  const float2* cs;
+  int max_pos;
+  void* k_cache;
+  void* v_cache;
+  int B, T, n_q_heads, n_kv_heads, head_dim, capacity, kv_bf16;
+  int paged, page_size, n_pages, bt_stride;
+  const int32_t* block_table;
+  const int32_t* start;
+  int32_t* err;
+};
+
 // Launch helpers (return a cudaError_t from the launch).
 cudaError_t launch_frame_embed(const EmbedParams& p, cudaStream_t s);
 cudaError_t launch_rope_table(float* cs, int max_pos, int head_dim, double base, cudaStream_t s);
 cudaError_t launch_qk_norm_rope(const NormRopeParams& p, cudaStream_t s);
 cudaError_t launch_set_rows(const SetRowsParams& p, cudaStream_t s);
 cudaError_t launch_zero(void* ptr, size_t bytes, cudaStream_t s);
+cudaError_t launch_prefill_rows(const PrefillRowsParams& p, cudaStream_t s);
 
 // Tile geometry of the attention kernel for a (dtype, head_dim) pair.
 struct AttnGeometry {

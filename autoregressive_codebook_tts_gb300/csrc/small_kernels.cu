@@ -178,6 +178,78 @@ __global__ void __launch_bounds__(kSetRowsThreads) set_rows_kernel(const SetRows
   store4(static_cast<KvT*>(p.v_cache) + row * D + d, vv);
 }
 
+// ---------------------------------------------------------------------------
+// Prefill rows ("qwentts.cpp ... src/pipeline-tts.h", KV cache section: the prefill
+// writes the prompt's positions into the cache).  Row r = b * T + t sits at position
+// start[b] + t: its q heads are RMS-normed and rotated in place (the attention reads
+// them), its k heads normed, rotated and written into the cache, its v heads written
+// as they are.  One group of D/4 lanes per head row, as in the standalone norm.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void store4(float* dst, const float (&x)[4]) {
+  *reinterpret_cast<float4*>(dst) = make_float4(x[0], x[1], x[2], x[3]);
+}
+__device__ __forceinline__ void store4(__nv_bfloat16* dst, const float (&x)[4]) {
+  store4(dst, make_float4(x[0], x[1], x[2], x[3]));
+}
+
+template <int D, typename KvT>
+__global__ void __launch_bounds__(kNormWarps * 32) prefill_rows_kernel(const PrefillRowsParams p) {
+  constexpr int EPL = 4, LPR = D / EPL, RPW = 32 / LPR;
+  grid_wait();
+  grid_launch_dependents();
+  const int r = blockIdx.y;  // b * T + t
+  const int b = r / p.T;
+  const int t = r - b * p.T;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int Hq = p.n_q_heads, Hkv = p.n_kv_heads;
+  const int row = (blockIdx.x * kNormWarps + warp) * RPW + lane / LPR;  // head row
+  const bool live = row < Hq + 2 * Hkv;  // whole row groups are live or not
+  const int pos = __ldcg(p.start + b) + t;
+  const bool pos_ok = pos >= 0 && pos < p.capacity && pos < p.max_pos;
+  if (!pos_ok && row == 0 && (lane % LPR) == 0) set_err(p.err, TTS_EFLAG_POS_RANGE);
+  const int rpos = min(max(pos, 0), p.max_pos - 1);
+  const int kind = row < Hq ? 0 : (row < Hq + Hkv ? 1 : 2);  // q, k, v
+  const int e0 = (lane % LPR) * EPL;
+  const int64_t base = static_cast<int64_t>(r) * p.row_stride;
+  const float* src = kind == 0 ? p.q + base + static_cast<int64_t>(row) * D
+                   : kind == 1 ? p.k + base + static_cast<int64_t>(row - Hq) * D
+                               : p.v + base + static_cast<int64_t>(row - Hq - Hkv) * D;
+  float x[EPL] = {0.f, 0.f, 0.f, 0.f};
+  if (live) {
+    const float4 v = __ldcg(reinterpret_cast<const float4*>(src + e0));
+    x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
+  }
+  // Every group runs the norm's shuffles (v and dead rows on their own values or zeros,
+  // results discarded), so the full-warp shuffles stay convergent.
+  float y[EPL] = {x[0], x[1], x[2], x[3]};
+  float gam[EPL];
+  float2 cs[EPL];
+  load_norm_consts<EPL, 1, LPR>(kind == 1 ? p.gamma_k : p.gamma_q, p.cs + static_cast<int64_t>(rpos) * (D / 2),
+                                lane % LPR, D, gam, cs);
+  norm_rope_regs<EPL, 1, LPR>(y, gam, cs, p.eps, lane % LPR, D);
+  if (!live) return;
+  if (kind == 0) {
+    *reinterpret_cast<float4*>(p.q + base + static_cast<int64_t>(row) * D + e0) = make_float4(y[0], y[1], y[2], y[3]);
+    return;
+  }
+  if (!pos_ok) return;
+  const int g = kind == 1 ? row - Hq : row - Hq - Hkv;
+  size_t crow;
+  if (!p.paged) {
+    crow = (static_cast<size_t>(b) * Hkv + g) * p.capacity + pos;
+  } else {
+    const int page = __ldcg(p.block_table + static_cast<int64_t>(b) * p.bt_stride + pos / p.page_size);
+    if (page < 0 || page >= p.n_pages) {
+      if ((lane % LPR) == 0) set_err(p.err, TTS_EFLAG_PAGE);
+      return;
+    }
+    crow = (static_cast<size_t>(page) * Hkv + g) * p.page_size + pos % p.page_size;
+  }
+  KvT* dst = static_cast<KvT*>(kind == 1 ? p.k_cache : p.v_cache) + crow * D + e0;
+  if (kind == 1) store4(dst, y);
+  else store4(dst, x);
+}
+
 __global__ void zero_kernel(uint4* p, size_t n16) {
   grid_wait();
   grid_launch_dependents();
@@ -216,6 +288,19 @@ cudaError_t launch_set_rows(const SetRowsParams& p, cudaStream_t s) {
   dim3 grid((n4 + kSetRowsThreads - 1) / kSetRowsThreads, p.B);
   if (p.kv_bf16) return launch_pdl(set_rows_kernel<__nv_bfloat16>, grid, dim3(kSetRowsThreads), 0, s, p);
   return launch_pdl(set_rows_kernel<float>, grid, dim3(kSetRowsThreads), 0, s, p);
+}
+
+cudaError_t launch_prefill_rows(const PrefillRowsParams& p, cudaStream_t s) {
+  const int rows = p.n_q_heads + 2 * p.n_kv_heads;
+  const int rows_per_block = kNormWarps * (32 / (p.head_dim / 4));
+  dim3 grid((rows + rows_per_block - 1) / rows_per_block, p.B * p.T);
+  if (p.head_dim == 64)
+    return p.kv_bf16 ? launch_pdl(prefill_rows_kernel<64, __nv_bfloat16>, grid, dim3(kNormWarps * 32), 0, s, p)
+                     : launch_pdl(prefill_rows_kernel<64, float>, grid, dim3(kNormWarps * 32), 0, s, p);
+  if (p.head_dim == 128)
+    return p.kv_bf16 ? launch_pdl(prefill_rows_kernel<128, __nv_bfloat16>, grid, dim3(kNormWarps * 32), 0, s, p)
+                     : launch_pdl(prefill_rows_kernel<128, float>, grid, dim3(kNormWarps * 32), 0, s, p);
+  return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_zero(void* ptr, size_t bytes, cudaStream_t s) {

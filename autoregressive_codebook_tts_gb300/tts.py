@@ -38,6 +38,8 @@ EXPORTED = [
     "tts_rope_table", "tts_qk_norm_rope", "tts_kv_set_rows", "tts_decode_attn_workspace_size",
     "tts_decode_attn_default_splits", "tts_workspace_init", "tts_decode_attn", "tts_decode_step",
     "tts_decode_step_noalloc",
+    "tts_prefill_workspace_size",
+    "tts_prefill_step",
 ]
 
 
@@ -76,6 +78,9 @@ _sigs = {
                          ctypes.POINTER(TtsKvDesc), _P, _F, _P, _P, _SZ, _I32, _P, _P], _I32),
     "tts_decode_step_noalloc": ([_P, _P, _P, _I64, _P, _P, _F, _P, _I32, _P, _P,
                                  ctypes.POINTER(TtsKvDesc), _P, _F, _P, _I32, _P, _P], _I32),
+    "tts_prefill_workspace_size": ([ctypes.POINTER(TtsKvDesc), _I32, _I32], _SZ),
+    "tts_prefill_step": ([_P, _P, _P, _I64, _P, _P, _F, _P, _I32, _P, _P,
+                          ctypes.POINTER(TtsKvDesc), _P, _I32, _F, _P, _P, _SZ, _I32, _P, _P], _I32),
 }
 for _name, (_args, _ret) in _sigs.items():
     _fn = getattr(_lib, _name)
@@ -232,6 +237,32 @@ def tts_decode_step_noalloc(q, k, v, gamma_q, gamma_k, eps, cs, max_pos, k_cache
                                         _ptr(k_cache), _ptr(v_cache), ctypes.byref(desc),
                                         _ptr(cur_len), float(scale), _ptr(out), n_splits,
                                         _ptr(err_flag), _stream(stream)), "tts_decode_step_noalloc")
+
+
+def tts_prefill_workspace_size(desc: TtsKvDesc, T: int, n_splits=0) -> int:
+    return int(_lib.tts_prefill_workspace_size(ctypes.byref(desc), T, n_splits))
+
+
+def prefill_workspace(desc: TtsKvDesc, T: int, n_splits=0, device="cuda", stream=None):
+    """Allocate (through torch) and clear a workspace for a prefill of T positions."""
+    n = max(tts_prefill_workspace_size(desc, T, n_splits), 256)
+    ws = torch.empty(n, dtype=torch.uint8, device=device)
+    tts_workspace_init(ws, stream)
+    return ws
+
+
+def tts_prefill_step(q, k, v, gamma_q, gamma_k, eps, cs, max_pos, k_cache, v_cache,
+                     desc: TtsKvDesc, start_pos, T, scale, out, ws, n_splits=0, err_flag=None,
+                     stream=None):
+    """q, k, v: [B*T, ...] row views (row r = b*T + t); q is normed in place."""
+    stride = _row_stride(q)
+    assert k.stride(0) == stride and v.stride(0) == stride, "q, k, v rows must share one stride"
+    _check(_lib.tts_prefill_step(_ptr(q), _ptr(k), _ptr(v), stride, _ptr(gamma_q), _ptr(gamma_k),
+                                 float(eps), _ptr(cs), max_pos, _ptr(k_cache), _ptr(v_cache),
+                                 ctypes.byref(desc), _ptr(start_pos), int(T), float(scale),
+                                 _ptr(out), _ptr(ws),
+                                 0 if ws is None else ws.numel() * ws.element_size(),
+                                 n_splits, _ptr(err_flag), _stream(stream)), "tts_prefill_step")
 
 
 def default_scale(head_dim: int) -> float:

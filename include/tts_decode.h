@@ -261,6 +261,35 @@ tts_status tts_decode_step_noalloc(const float* q, const float* k, const float* 
                                    const tts_kv_desc* desc, const int32_t* cur_len, float scale,
                                    float* out, int32_t n_splits, int32_t* err_flag, void* stream);
 
+/* ---------------------------------------------------------------------------
+ * Prefill: T new positions per stream in one call ([P-pipeline], KV-cache section:
+ * the prefill writes the prompt's rows from the reset position, causally).  Row t of
+ * stream b sits at position p = start_pos[b] + t, t < T:
+ *   q'[b][t] = norm_rope(q[b][t], gamma_q, p), written back into q (in place)
+ *   K[b][.][p] = cvt(norm_rope(k[b][t], gamma_k, p)),  V[b][.][p] = cvt(v[b][t])
+ *   out[b][t] = attention of q'[b][t] over [0, p + 1)
+ * so every query sees the rows before the prompt and the prompt's rows up to its own.
+ * With start_pos = 0 it is the prefill after a cache reset.
+ *   q, k, v: device f32 rows, row r = b*T + t at ptr + r*row_stride (heads contiguous;
+ *        they may be strided views of one projection row).  k and v are read only.
+ *   out: device f32 [B][T][Hq][D], dense.
+ *   start_pos: device int32 [B].  A position outside [0, capacity) or [0, rope_max_pos)
+ *        is not written and sets TTS_EFLAG_POS_RANGE; a window past capacity is clamped
+ *        and sets TTS_EFLAG_NVALID.  Paged: a page id outside [0, n_pages) skips that
+ *        row's write and sets TTS_EFLAG_PAGE.
+ *   workspace: at least tts_prefill_workspace_size(desc, T, n_splits) bytes, otherwise
+ *        as for tts_decode_attn (its B x T queries take the place of its B streams).
+ * Two launches on `stream`: the rows, then the attention.  B*T must not exceed 65535.
+ * ------------------------------------------------------------------------- */
+size_t tts_prefill_workspace_size(const tts_kv_desc* desc, int32_t T, int32_t n_splits);
+
+tts_status tts_prefill_step(float* q, const float* k, const float* v, int64_t row_stride,
+                            const float* gamma_q, const float* gamma_k, float eps,
+                            const float* rope_cs, int32_t rope_max_pos, void* k_cache,
+                            void* v_cache, const tts_kv_desc* desc, const int32_t* start_pos,
+                            int32_t T, float scale, float* out, void* workspace, size_t ws_bytes,
+                            int32_t n_splits, int32_t* err_flag, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -240,6 +240,23 @@ def test_decode_attn_split_counts_agree(tts):
         assert row_rel_err(r, ref) <= ATTN_TOL["f32"]
 
 
+def test_decode_attn_one_split_over_more_ctas_than_fit(tts):
+    """One split per kv head and more (stream, kv head) pairs than the GPU holds at
+    once: no workspace, so the grid runs as plain waves (no work counter)."""
+    w = W.workload("batched", B=40, layers=1)
+    L = Layer(w, seed=45, poison=False)
+    desc = L.desc(tts)
+    nv = (L.d_cur + 1).to(torch.int32)
+    out = torch.empty(w.B, 16, 128, device="cuda")
+    ef = err_flag()
+    tts.tts_decode_attn(L.d_q, L.d_K, L.d_V, desc, nv, scale_of(w), out, None, 1, ef)
+    torch.cuda.synchronize()
+    assert ef.item() == 0
+    ref, _, _ = oracle.decode_attn(L.q_np(), cache_np(L.K), cache_np(L.V), L.layout(),
+                                   nv.cpu().numpy(), scale_of(w))
+    assert row_rel_err(out.cpu().numpy(), ref) <= ATTN_TOL["bf16"]
+
+
 def test_decode_attn_paged_equals_contiguous(tts):
     """The same logical rows through a shuffled block table give bit-identical output
     (same tiles, same arithmetic)."""

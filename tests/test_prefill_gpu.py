@@ -1,0 +1,160 @@
+"""Prefill of T positions per stream (tts_prefill_step) against the oracle: the cache
+bytes bit-exact, the q rows normed in place, every query's output within the attention
+tolerance of the causal definition.  Contiguous and paged, f32 and bf16, a prompt after
+a reset (start 0) and after earlier rows, and the error flags of positions past the
+cache."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from autoregressive_codebook_tts_gb300 import workloads as W
+from gpu_helpers import ATTN_TOL, NORM_TOL, Layer, bits, cache_np, rope_table, row_rel_err, scale_of
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def tts(cuda_dev):
+    from autoregressive_codebook_tts_gb300 import build
+    build.build()
+    from autoregressive_codebook_tts_gb300 import tts as mod
+    return mod
+
+
+def _run(tts, w, start, T, seed, n_splits=0, poison=True):
+    """Prefill T rows per stream at `start`; returns (layer, rows, out, ef, ref_out, kc, vc, qn)."""
+    L = Layer(w, seed=seed, cur_len=start, poison=poison)
+    B, Hq, Hkv, D = w.B, w.n_q_heads, w.n_kv_heads, w.head_dim
+    rows, _, _, _ = W.qkv(B * T, Hq, Hkv, D, seed + 10)
+    qd, kd = Hq * D, Hkv * D
+    d_rows = rows.cuda()
+    q, k, v = d_rows[:, :qd], d_rows[:, qd:qd + kd], d_rows[:, qd + kd:]
+    cs = rope_table(tts, w.capacity, D, w.rope_base)
+    desc = L.desc(tts)
+    ws = tts.prefill_workspace(desc, T, n_splits)
+    out = torch.full((B, T, Hq, D), float("nan"), device="cuda")
+    ef = torch.zeros(1, dtype=torch.int32, device="cuda")
+    start_d = torch.as_tensor(start, dtype=torch.int32).cuda()
+    tts.tts_prefill_step(q, k, v, L.d_gq, L.d_gk, w.eps, cs, w.capacity, L.d_K, L.d_V, desc,
+                         start_d, T, scale_of(w), out, ws, n_splits, ef)
+    torch.cuda.synchronize()
+    # oracle on the host copies of the same inputs
+    hr = rows.numpy()
+    qh = hr[:, :qd].reshape(B, T, Hq, D)
+    kh = hr[:, qd:qd + kd].reshape(B, T, Hkv, D)
+    vh = hr[:, qd + kd:].reshape(B, T, Hkv, D)
+    kc, vc = cache_np(L.K), cache_np(L.V)
+    st = np.asarray(start, np.int32)
+    ref = oracle.prefill_step(qh, kh, vh, L.gq.numpy(), L.gk.numpy(), np.float32(w.eps), w.rope_base,
+                              kc, vc, L.layout(), st, scale_of(w))
+    pos = st[:, None] + np.arange(T, dtype=np.int32)[None, :]
+    qn = np.stack([oracle.rms_norm_rope(qh[:, t], L.gq.numpy(), np.float32(w.eps), pos[:, t], w.rope_base)
+                   for t in range(T)], axis=1)
+    return L, q, out, ef, ref, kc, vc, qn
+
+
+def _check_caches(L, w, start, T, kc, vc):
+    """V: every byte equal.  K: every byte outside the prompt's rows equal; the prompt's
+    rows (normed and rotated in f32 on the device, in double by the oracle) within
+    2e-6 (f32) or one bf16 ulp."""
+    gk, gv = cache_np(L.d_K), cache_np(L.d_V)
+    assert np.array_equal(bits(gv), bits(vc))
+    mask = np.zeros(kc.shape, bool)
+    for b in range(w.B):
+        for t in range(T):
+            p = int(start[b]) + t
+            if p >= w.capacity:
+                continue
+            for g in range(w.n_kv_heads):
+                if w.paged:
+                    mask[int(L.bt[b, p // w.page_size]), g, p % w.page_size] = True
+                else:
+                    mask[b, g, p] = True
+    assert not ((bits(gk) != bits(kc)) & ~mask).any()
+    if w.kv_dtype == "f32":
+        np.testing.assert_allclose(gk[mask], kc[mask], rtol=2e-6, atol=2e-6)
+    else:
+        assert np.abs(gk[mask].astype(np.int32) - kc[mask].astype(np.int32)).max() <= 1
+
+
+CASES = [
+    ("tiny", dict(), [0], 1),
+    ("tiny", dict(), [0], 2),
+    ("tiny", dict(), [37], 7),
+    ("tiny", dict(), [0], 40),
+    ("batched", dict(B=2, layers=1), [100, 3000], 33),
+    ("paged", dict(B=2, layers=1, n_pages=600), [50, 1000], 20),
+    ("talker", dict(layers=1), [4000], 64),
+]
+
+
+@pytest.mark.parametrize("name,over,start,T", CASES)
+def test_prefill_matches_oracle(tts, name, over, start, T):
+    w = W.workload(name, **over)
+    L, q, out, ef, ref, kc, vc, qn = _run(tts, w, start, T, seed=60)
+    assert ef.item() == 0
+    _check_caches(L, w, start, T, kc, vc)
+    # q normed and rotated in place
+    qg = q.cpu().numpy().reshape(qn.shape)
+    assert row_rel_err(qg.reshape(-1, w.head_dim)[None], qn.reshape(-1, w.head_dim)[None]) <= NORM_TOL
+    # every query within the attention tolerance of the causal definition
+    o = out.cpu().numpy()
+    assert np.isfinite(o).all()
+    assert row_rel_err(o.reshape(-1, w.n_q_heads, w.head_dim),
+                       ref.reshape(-1, w.n_q_heads, w.head_dim)) <= ATTN_TOL[w.kv_dtype]
+
+
+@pytest.mark.parametrize("n_splits", [1, 3, 16])
+def test_prefill_split_counts_agree(tts, n_splits):
+    w = W.workload("talker", layers=1)
+    _, _, out, ef, ref, _, _, _ = _run(tts, w, [1500], 24, seed=61, n_splits=n_splits)
+    assert ef.item() == 0
+    assert row_rel_err(out.cpu().numpy().reshape(-1, 16, 128), ref.reshape(-1, 16, 128)) <= ATTN_TOL["f32"]
+
+
+def test_prefill_of_one_row_equals_the_decode_step(tts):
+    """T = 1 at start c is the decode step at cur_len c: the same cache bytes, outputs
+    within rounding of each other (different kernels: the decode step folds the new row
+    in from registers, the prefill reads it back from the cache)."""
+    w = W.workload("batched", B=3, layers=1)
+    cur = [5, 700, 2047]
+    L, _, out, ef, _, _, _, _ = _run(tts, w, cur, 1, seed=62, poison=False)
+    assert ef.item() == 0
+    D2 = Layer(w, seed=62, cur_len=cur, poison=False)
+    rows, _, _, _ = W.qkv(w.B, 16, 8, 128, 72)
+    d_rows = rows.cuda()
+    cs = rope_table(tts, w.capacity, 128, w.rope_base)
+    desc = D2.desc(tts)
+    o2 = torch.empty(w.B, 16, 128, device="cuda")
+    tts.tts_decode_step(d_rows[:, :2048], d_rows[:, 2048:3072], d_rows[:, 3072:], D2.d_gq, D2.d_gk,
+                        w.eps, cs, w.capacity, D2.d_K, D2.d_V, desc, D2.d_cur, scale_of(w), o2,
+                        tts.workspace(desc, 0), 0, ef)
+    torch.cuda.synchronize()
+    assert ef.item() == 0
+    assert torch.equal(D2.d_K.view(torch.int16), L.d_K.view(torch.int16))
+    assert torch.equal(D2.d_V.view(torch.int16), L.d_V.view(torch.int16))
+    assert row_rel_err(o2.cpu().numpy(), out[:, 0].cpu().numpy()) <= 1e-3  # bf16 KV, two paths
+
+
+def test_predictor_two_row_prefill_after_reset(tts):
+    """The code predictor's T = 2 prefill at position 0 (16-slot f32 cache, D = 64)."""
+    w = W.workload("predictor", layers=1)
+    L, _, out, ef, ref, kc, vc, _ = _run(tts, w, [0] * w.B, 2, seed=63)
+    assert ef.item() == 0
+    _check_caches(L, w, [0] * w.B, 2, kc, vc)
+    assert row_rel_err(out.cpu().numpy().reshape(-1, 16, 64), ref.reshape(-1, 16, 64)) <= ATTN_TOL["f32"]
+
+
+def test_prefill_flags_positions_past_the_cache(tts):
+    """A prompt running past capacity: the rows inside are written, the rest skipped
+    with TTS_EFLAG_POS_RANGE, and the windows past capacity clamped with
+    TTS_EFLAG_NVALID; the queries inside the cache are still exact."""
+    w = W.workload("tiny")
+    T, start = 6, w.capacity - 3
+    L, _, out, ef, ref, kc, vc, _ = _run(tts, w, [start], T, seed=64)
+    assert ef.item() & tts.EFLAG_POS_RANGE and ef.item() & tts.EFLAG_NVALID
+    _check_caches(L, w, [start], T, kc, vc)
+    inside = 3
+    assert row_rel_err(out[:, :inside].cpu().numpy().reshape(-1, 16, 128),
+                       ref[:, :inside].reshape(-1, 16, 128)) <= ATTN_TOL["f32"]
