@@ -40,7 +40,9 @@ def parse():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
-    ap.add_argument("--workload", default="talker", choices=["talker", "batched", "paged"])
+    ap.add_argument("--workload", default="talker", choices=["talker", "batched", "paged", "prefill"])
+    ap.add_argument("--prefill-t", type=int, default=128, help="prefill: prompt positions per stream")
+    ap.add_argument("--prefill-start", type=int, default=0, help="prefill: first prompt position")
     ap.add_argument("--cur-len", type=int, default=4095)
     ap.add_argument("--n-splits", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -467,6 +469,150 @@ def run_native(args, rank, world):
     return res
 
 
+def run_prefill(args, rank, world):
+    """Prompt prefill on the talker shapes: T positions per stream from --prefill-start,
+    one tts_prefill_step per layer for all 28 layers, captured into a CUDA graph."""
+    import torch
+    from autoregressive_codebook_tts_gb300 import build as b
+    b.build()
+    from autoregressive_codebook_tts_gb300 import tts
+    from autoregressive_codebook_tts_gb300 import workloads as W
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    w = W.workload("talker")
+    T, start = args.prefill_t, args.prefill_start
+    B, L, Hq, Hkv, D = w.B, w.layers, w.n_q_heads, w.n_kv_heads, w.head_dim
+    if start < 0 or start + T > w.capacity:
+        raise SystemExit("prefill window outside the cache")
+    g = torch.Generator(device=dev)
+    g.manual_seed(rank)
+    qd, kd = Hq * D, Hkv * D
+    qkv = torch.randn(L, B * T, qd + 2 * kd, generator=g, device=dev)
+    gq = torch.rand(L, D, generator=g, device=dev) + 0.5
+    gk = torch.rand(L, D, generator=g, device=dev) + 0.5
+    caches = []
+    for _ in range(L):
+        K = torch.empty(B, Hkv, w.capacity, D, device=dev)
+        V = torch.empty_like(K)
+        K.normal_(generator=g)
+        V.normal_(generator=g)
+        caches.append((K, V))
+    cs = torch.empty(w.capacity, D // 2, 2, device=dev)
+    tts.tts_rope_table(cs, w.capacity, D, w.rope_base)
+    desc = tts.kv_desc(B, Hq, Hkv, D, w.capacity, w.kv_dtype, window_quantum=w.window_quantum)
+    ws = tts.prefill_workspace(desc, T, args.n_splits, device=dev)
+    outs = torch.empty(L, B, T, Hq, D, device=dev)
+    ef = torch.zeros(1, dtype=torch.int32, device=dev)
+    start_t = torch.full((B,), start, dtype=torch.int32, device=dev)
+    scale = 1.0 / math.sqrt(D)
+
+    def layers():
+        for l in range(L):
+            K, V = caches[l]
+            rows = qkv[l]
+            tts.tts_prefill_step(rows[:, :qd], rows[:, qd:qd + kd], rows[:, qd + kd:], gq[l], gk[l],
+                                 w.eps, cs, w.capacity, K, V, desc, start_t, T, scale, outs[l], ws,
+                                 args.n_splits, ef)
+
+    gl = capture(layers, torch)
+    for _ in range(args.warmup):
+        gl.replay()
+    torch.cuda.synchronize()
+    if ef.item() != 0:
+        raise RuntimeError(f"device error flag {ef.item()}")
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t = timed_replays(gl, args.steps, torch)
+    clk = clocks.stop()
+    (t,) = max_over_ranks([t], world, dev)
+    # bytes a layer must move through HBM at least: the prompt's q/k/v rows read, q
+    # written back, its k/v rows written to the cache, the earlier cache rows read once,
+    # the output written
+    hbm = B * (T * (qd + 2 * kd) * 4 + T * qd * 4 + T * 2 * kd * 4 + start * 2 * kd * 4 + T * qd * 4)
+    # K/V rows the queries read (the prompt's own rows come back from L2)
+    attn_rows = B * sum(start + i + 1 for i in range(T))
+    attn_bytes = attn_rows * 2 * kd * 4
+    peak, peak_kind = hbm_peak()
+    t_layer = t / (args.steps * L)
+    achieved = hbm / t_layer / 1e9
+    value = world * B * T * args.steps / t
+    return {
+        "metric": "prefill: prompt positions per second (B streams, all 28 layers)",
+        "value": round(value, 1), "unit": "positions/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(t / args.steps * 1e3, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded, device-generated; random-init, no weights)",
+        "config": {"workload": f"prefill: talker shapes, B={B}, {T} prompt positions from {start}, "
+                               f"28 layers, f32 KV, capacity {w.capacity}",
+                   "frame_step": "graph replay of 28 x tts_prefill_step",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "us_per_layer": round(t_layer * 1e6, 3),
+        "attn_kv_gb_s": round(attn_bytes / t_layer / 1e9, 1),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": None,
+                     "kernel": "tts_prefill_step (rows + attention launches)",
+                     "peak_source": "measured HBM copy bandwidth" if peak_kind == "measured"
+                     else "fallback HBM copy bandwidth", "bytes_per_launch": hbm},
+        "gpu_launches": 2 * L * args.steps,
+        "clocks": clk,
+    }
+
+
+def run_reference_prefill(args, world):
+    """The oracle's prefill of one layer (talker shapes) as the reference arm's step."""
+    import numpy as np
+    from autoregressive_codebook_tts_gb300 import workloads as W
+    import oracle
+    w = W.workload("talker")
+    T, start = args.prefill_t, args.prefill_start
+    B, Hq, Hkv, D = w.B, w.n_q_heads, w.n_kv_heads, w.head_dim
+    rows, _, _, _ = W.qkv(B * T, Hq, Hkv, D, seed=3)
+    r = rows.numpy()
+    qd, kd = Hq * D, Hkv * D
+    q = r[:, :qd].reshape(B, T, Hq, D)
+    k = r[:, qd:qd + kd].reshape(B, T, Hkv, D)
+    v = r[:, qd + kd:].reshape(B, T, Hkv, D)
+    gq, gk = W.gamma(D, 4).numpy(), W.gamma(D, 5).numpy()
+    K, V = W.cache(w, [start] * B, seed=7, poison=False)
+    kc, vc = K.numpy().copy(), V.numpy().copy()
+    lay = oracle.KvLayout(B, Hkv, D, w.capacity, w.kv_dtype)
+    st = np.full(B, start, np.int32)
+
+    def step():
+        oracle.prefill_step(q, k, v, gq, gk, np.float32(w.eps), w.rope_base, kc, vc, lay, st,
+                            1.0 / math.sqrt(D))
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = time.perf_counter() - t0
+    # one step is one layer of the 28: positions per second of the whole prompt
+    value = B * T * args.steps / (dt * w.layers)
+    sample = f"each step: one layer's prefill of {T} positions from {start} (1 of {w.layers} layers)"
+    return {
+        "impl": "reference",
+        "metric": "prefill: prompt positions per second (B streams, all 28 layers)",
+        "value": round(value, 3), "unit": "positions/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)",
+        "data": "synthetic (seeded)",
+        "config": {"workload": f"prefill: talker shapes, B={B}, {T} prompt positions from {start}",
+                   "parallelism": "single host thread"},
+        "cpu_baseline": {"value": round(value, 3), "unit": "positions/s", "cores": 1,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 3), "unit": "positions/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
 def run_reference(args, rank, world):
     """The CPU oracle timed as the reference arm, on the same workload and metric."""
     import numpy as np
@@ -474,6 +620,8 @@ def run_reference(args, rank, world):
     from autoregressive_codebook_tts_gb300 import workloads as W
     import oracle
     oracle.build()
+    if args.workload == "prefill":
+        return run_reference_prefill(args, world)
     w = W.workload(args.workload)
     cur_list = [args.cur_len] * w.B if args.workload == "talker" else [int(c) for c in W.cur_lens(w, 0)]
     cur = np.array(cur_list, np.int32)
@@ -543,7 +691,7 @@ def main():
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl")
-    res = run_native(args, rank, world)
+    res = run_prefill(args, rank, world) if args.workload == "prefill" else run_native(args, rank, world)
     if rank == 0:
         print(json.dumps(res))
     if world > 1:
