@@ -10,7 +10,8 @@
 namespace tts {
 
 struct EmbedParams {
-  const float* tab[TTS_MAX_TABLES];
+  const void* tab[TTS_MAX_TABLES];  // f32 or bf16 rows (tab_bf16)
+  int tab_bf16;
   int n_tables, vocab, hidden;
   const int32_t* ids;
   int64_t ids_stride;

@@ -31,6 +31,18 @@ cudaError_t launch_pdl(Kernel kern, dim3 grid, dim3 block, size_t smem, cudaStre
 // ---------------------------------------------------------------------------
 constexpr int kEmbedThreads = 128;
 
+// Four consecutive table entries as f32: a 16-byte load of f32, or an 8-byte load of
+// bf16 widened exactly (the bf16 bits are the high half of the f32).
+__device__ __forceinline__ float4 load_row4(const float* row, int c4) {
+  return __ldg(reinterpret_cast<const float4*>(row) + c4);
+}
+__device__ __forceinline__ float4 load_row4(const __nv_bfloat16* row, int c4) {
+  const uint2 w = __ldg(reinterpret_cast<const uint2*>(row) + c4);
+  return make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xffff0000u),
+                     __uint_as_float(w.y << 16), __uint_as_float(w.y & 0xffff0000u));
+}
+
+template <typename TabT>
 __global__ void __launch_bounds__(kEmbedThreads) frame_embed_kernel(const EmbedParams p) {
   grid_wait();
   grid_launch_dependents();
@@ -48,7 +60,7 @@ __global__ void __launch_bounds__(kEmbedThreads) frame_embed_kernel(const EmbedP
         bad = true;
         id = min(max(id, 0), p.vocab - 1);
       }
-      rows[t] = __ldg(reinterpret_cast<const float4*>(p.tab[t] + static_cast<int64_t>(id) * p.hidden) + c4);
+      rows[t] = load_row4(static_cast<const TabT*>(p.tab[t]) + static_cast<int64_t>(id) * p.hidden, c4);
     }
   }
   float4 acc = rows[0];
@@ -263,7 +275,8 @@ __global__ void zero_kernel(uint4* p, size_t n16) {
 cudaError_t launch_frame_embed(const EmbedParams& p, cudaStream_t s) {
   const int cols4 = p.hidden / 4;
   dim3 grid((cols4 + kEmbedThreads - 1) / kEmbedThreads, p.B);
-  return launch_pdl(frame_embed_kernel, grid, dim3(kEmbedThreads), 0, s, p);
+  if (p.tab_bf16) return launch_pdl(frame_embed_kernel<__nv_bfloat16>, grid, dim3(kEmbedThreads), 0, s, p);
+  return launch_pdl(frame_embed_kernel<float>, grid, dim3(kEmbedThreads), 0, s, p);
 }
 
 cudaError_t launch_rope_table(float* cs, int max_pos, int head_dim, double base, cudaStream_t s) {

@@ -45,7 +45,7 @@ EXPORTED = [
 
 class TtsTables(ctypes.Structure):
     _fields_ = [("tab", ctypes.c_void_p * TTS_MAX_TABLES), ("n_tables", ctypes.c_int32),
-                ("vocab", ctypes.c_int32), ("hidden", ctypes.c_int32)]
+                ("vocab", ctypes.c_int32), ("hidden", ctypes.c_int32), ("dtype", ctypes.c_int32)]
 
 
 class TtsKvDesc(ctypes.Structure):
@@ -145,11 +145,16 @@ def kv_desc(B, n_q_heads, n_kv_heads, head_dim, capacity, kv_dtype="f32", window
 
 
 def tables(tabs) -> TtsTables:
+    """Table descriptor for f32 or bf16 tables (all of one dtype)."""
     t = TtsTables()
+    dts = {x.dtype for x in tabs}
+    if len(dts) != 1 or not dts <= {torch.float32, torch.bfloat16}:
+        raise ValueError("codebook tables must all be float32 or all bfloat16")
     for i, x in enumerate(tabs):
         t.tab[i] = x.data_ptr()
     t.n_tables = len(tabs)
     t.vocab, t.hidden = tabs[0].shape
+    t.dtype = TTS_BF16 if tabs[0].dtype == torch.bfloat16 else TTS_F32
     return t
 
 

@@ -30,6 +30,7 @@ sys.path.insert(0, ROOT)
 METRIC = "decode-attn KV GB/s (% of HBM peak); frame steps/sec at B streams, 1 GB300"
 FALLBACK_HBM_GBS = 6800.0
 NOMINAL_HBM_GBS = 7900.0
+L2_BYTES = 129 * 2 ** 20  # GB300 L2
 ATTN_SRC = os.path.join(ROOT, "autoregressive_codebook_tts_gb300", "csrc", "attn.cu")
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "decode_step_talker_f32_cur4095.txt")
 
@@ -41,6 +42,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--workload", default="talker", choices=["talker", "batched", "paged", "prefill"])
+    ap.add_argument("--layers", type=int, default=0,
+                    help="layers per frame (0 = the workload's own; fewer only for small profiling cases)")
     ap.add_argument("--prefill-t", type=int, default=128, help="prefill: prompt positions per stream")
     ap.add_argument("--prefill-start", type=int, default=0, help="prefill: first prompt position")
     ap.add_argument("--cur-len", type=int, default=4095)
@@ -324,7 +327,7 @@ def run_native(args, rank, world):
     local = int(os.environ.get("LOCAL_RANK", "0"))
     dev = torch.device(f"cuda:{local}")
     torch.cuda.set_device(dev)
-    w = W.workload(args.workload)
+    w = W.workload(args.workload, **({"layers": args.layers} if args.layers > 0 else {}))
     if args.workload == "talker":
         cur_arg = args.cur_len
         cur_list = [args.cur_len] * w.B
@@ -443,7 +446,9 @@ def run_native(args, rank, world):
                                 + (f", paged {w.page_size}-token pages" if w.paged else "")
                                 + (f", cur_len {args.cur_len}" if args.workload == 'talker' else ", ragged cur_len")),
                    "B": w.B, "layers": w.layers, "window_rows_per_layer": sum(c + 1 for c in cur_list),
-                   "l2": "inputs larger than L2 (KV working set per frame %.0f MiB)" % (w.layers * kv_layer / 2 ** 20),
+                   "l2": ("inputs larger than L2 (KV working set per frame %.0f MiB)" if w.layers * kv_layer > 2 * L2_BYTES
+                          else "KV working set per frame %.0f MiB, below twice L2: a profiling case, not a bench value")
+                         % (w.layers * kv_layer / 2 ** 20),
                    "frame_step": "graph replay of tts_frame_embed + %d x tts_decode_step" % w.layers,
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "pct_of_hbm_peak": round(100 * value / world / peak, 2),

@@ -60,8 +60,8 @@ extern "C" {
 
 /* ABI version range ([P-pipeline]-style ABI probe): a caller built against version V
  * may use this library iff tts_abi_min_version() <= V <= tts_abi_version(). */
-#define TTS_ABI_VERSION 1
-#define TTS_ABI_MIN_VERSION 1
+#define TTS_ABI_VERSION 2
+#define TTS_ABI_MIN_VERSION 2
 int32_t tts_abi_version(void);
 int32_t tts_abi_min_version(void);
 
@@ -92,12 +92,15 @@ typedef enum { TTS_F32 = 0, TTS_BF16 = 1 } tts_dtype;
 #define TTS_MAX_TABLES 16
 
 /* Codebook tables for the frame-input composition.  tab[g] points to a dense row-major
- * [vocab][hidden] f32 table; only the first n_tables entries are read. */
+ * [vocab][hidden] table of element type `dtype` (f32, or bf16 -- [P-pipeline] TTFA
+ * section: the gather works on any table type); only the first n_tables entries are
+ * read.  (ABI 2 added `dtype`.) */
 typedef struct {
-  const float* tab[TTS_MAX_TABLES];
+  const void* tab[TTS_MAX_TABLES];
   int32_t n_tables; /* 1..16 */
   int32_t vocab;    /* rows per table */
-  int32_t hidden;   /* row length in floats, a multiple of 4 */
+  int32_t hidden;   /* row length in elements, a multiple of 4 */
+  int32_t dtype;    /* tts_dtype of every table */
 } tts_tables;
 
 /* Flags of tts_kv_desc.flags */
@@ -139,7 +142,8 @@ typedef struct {
  * Step 1: frame-input composition.  [P-pipeline], on-device AR input assembly.
  *   out[b] = ((tab[0][ids[b][0]] + tab[1][ids[b][1]]) + ... ) + overlay[b]
  * in f32, codebooks in ascending order, the overlay added last; the result is
- * bit-identical to that sequence of single f32 additions.  For a code-predictor
+ * bit-identical to that sequence of single f32 additions.  bf16 table entries are
+ * widened to f32 exactly before they are added.  For a code-predictor
  * sub-step pass one group table (n_tables = 1) and overlay = NULL.
  *   ids:     device int32 [B][ids_stride], first n_tables entries per row read.
  *   overlay: device f32 rows of `hidden`, row stride overlay_stride; or NULL.

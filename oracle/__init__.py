@@ -116,10 +116,13 @@ def bf16_bits_to_f32(h) -> np.ndarray:
 def frame_embed(tables, ids, overlay=None):
     """out[b] = ((E_0[c_b0] + E_1[c_b1]) + ... ) + overlay[b], f32, fixed order.
 
-    tables: list of [vocab][hidden] f32 arrays; ids: [B][n_tables] int32;
+    tables: list of [vocab][hidden] arrays, f32, or uint16 holding bf16 bit patterns
+    (the "TTFA / prompt build" section's gather of any table type: a bf16 entry is
+    widened to f32 exactly, then added like an f32 one); ids: [B][n_tables] int32;
     overlay: [B][hidden] f32 or None.  Returns (out [B][hidden] f32, clamped flag).
     """
-    tabs = [_c(t, np.float32) for t in tables]
+    tabs = [bf16_bits_to_f32(t) if np.asarray(t).dtype == np.uint16 else _c(t, np.float32)
+            for t in tables]
     ids = _c(ids, np.int32)
     B, n = ids.shape
     vocab, hidden = tabs[0].shape

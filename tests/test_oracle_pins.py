@@ -534,3 +534,23 @@ def test_prefill_first_query_of_an_empty_cache_is_its_own_value_row():
                               oracle.KvLayout(B, Hkv, D, cap), np.zeros(B, np.int32), 0.5)
     assert np.array_equal(out[0, 0], np.repeat(v[0, 0], Hq // Hkv, axis=0))
     assert np.isfinite(out).all()
+
+
+def test_embed_bf16_tables_closed_form():
+    """bf16 tables (bit patterns): entries (g + 1) + c/8 are exact in bf16 and every
+    partial sum is exact in f32, so out = sum_g ((g + 1) + c_g / 8) + overlay exactly."""
+    n, vocab, hidden, B = 16, 16, 8, 3
+    tabs = []
+    for g in range(n):
+        vals = np.array([[(g + 1) + c / 8.0] * hidden for c in range(vocab)], np.float32)
+        u = vals.view(np.uint32)
+        assert (u & 0xFFFF).max() == 0  # exactly representable in bf16
+        tabs.append((u >> 16).astype(np.uint16))
+    rng = np.random.default_rng(30)
+    ids = rng.integers(0, vocab, (B, n)).astype(np.int32)
+    ov = np.full((B, hidden), 0.5, np.float32)
+    out, flag = oracle.frame_embed(tabs, ids, ov)
+    assert flag == 0
+    for b in range(B):
+        want = sum((g + 1) + ids[b, g] / 8.0 for g in range(n)) + 0.5
+        assert np.all(out[b] == np.float32(want))
