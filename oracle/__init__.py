@@ -24,10 +24,16 @@ Steps and the passages they follow (page titles as printed on the pages):
 * ``prefill_step`` -- the same section's prefill: T new positions per stream written
   into the cache, each of their queries attending causally over [0, its position],
   i.e. T decode queries whose windows end at their own rows.
+* ``sample`` -- the in-graph sampler with a counter RNG ("qwentts.cpp" pages: the
+  predictor frame unroll and the in-graph sampler; the optimisations table's
+  "one-kernel counter RNG"): greedy, or temperature/top-k sampling driven by the
+  published Philox4x64-10 counter generator, every decision taken in f32 in a fixed
+  order (``exp2_f32`` is this oracle's own exponential, see its docstring).
 """
 from __future__ import annotations
 
 import ctypes
+import math
 import os
 import subprocess
 import threading
@@ -292,3 +298,94 @@ def predictor_frame(group_tables, codes, bridge, qkv_per_substep, gammas, eps, b
             per_layer.append(decode_step(q, k, v, gq, gk, eps, base, kc, vc, layout, cur, scale))
         outs.append(per_layer)
     return embeds, outs
+
+
+# ---------------------------------------------------------------------------
+# In-graph sampler with a counter RNG
+# ---------------------------------------------------------------------------
+_M64 = (1 << 64) - 1
+
+
+def philox4x64_10(counter, key):
+    """Philox4x64 with 10 rounds (Salmon, Moraes, Dror, Shaw, "Parallel random numbers:
+    as easy as 1, 2, 3", SC 2011): four 64-bit counter words, two 64-bit key words ->
+    four 64-bit outputs.  Each round multiplies words 0 and 2 by the two round
+    multipliers (high and low halves of the 128-bit products), mixes the high halves
+    with words 1 and 3 and the key, and the key is bumped by the two Weyl constants
+    between rounds."""
+    c = [int(x) & _M64 for x in counter]
+    k = [int(x) & _M64 for x in key]
+    for r in range(10):
+        if r > 0:
+            k[0] = (k[0] + 0x9E3779B97F4A7C15) & _M64
+            k[1] = (k[1] + 0xBB67AE8584CAA73B) & _M64
+        p0 = 0xD2E7470EE14C6C93 * c[0]
+        p1 = 0xCA5A826395121157 * c[2]
+        c = [(p1 >> 64) ^ c[1] ^ k[0], p1 & _M64, (p0 >> 64) ^ c[3] ^ k[1], p0 & _M64]
+    return c
+
+
+def uniform_f32(seed, counter, b):
+    """The sampler's uniform for stream b at `counter`: the top 24 bits of the first
+    Philox4x64-10 output for counter words (counter, b, 0, 0) and key (seed, 0), times
+    2^-24 (exact in f32, in [0, 1))."""
+    x = philox4x64_10([counter, b, 0, 0], [seed, 0])[0]
+    return np.float32((x >> 40) * (1.0 / (1 << 24)))
+
+
+# 2^f on [0, 1): Taylor coefficients (ln 2)^j / j!, j = 0..9, rounded to f32.
+_EXP2_C = [np.float32(math.log(2.0) ** j / math.factorial(j)) for j in range(10)]
+
+
+def exp2_f32(x):
+    """2^x for an f32 x <= 0, in f32 operations in a fixed order: 0 below -126; else
+    n = floor(x), f = x - n (exact), p = Horner over the degree-9 Taylor polynomial of
+    2^f (each product and sum rounded to f32, no fused multiply-add), times 2^n
+    (exact)."""
+    x = np.float32(x)
+    if x < np.float32(-126.0):
+        return np.float32(0.0)
+    n = math.floor(float(x))
+    f = np.float32(x - np.float32(n))
+    p = _EXP2_C[9]
+    for j in range(8, -1, -1):
+        p = np.float32(np.float32(p * f) + _EXP2_C[j])
+    return np.float32(p * np.float32(2.0 ** n))
+
+
+def sample(logits, top_k, temperature, seed, counter):
+    """Token ids [B] int32 from logits [B][V] f32.
+
+    top_k = 0 or 1: greedy, the index of the largest logit (the lowest such index on a
+    tie).  top_k = k > 1: the k largest logits (larger first, lower index first on a
+    tie) l_0 >= ... >= l_{k-1}; c = f32(log2(e) / temperature) (rounded once from
+    double); w_i = exp2_f32(f32(f32(l_i - l_0) * c)); S = w_0 + ... + w_{k-1} summed in
+    that order in f32; r = f32(u * S) with u = uniform_f32(seed, counter, b); the result
+    is the candidate i of the first running sum (in f32, same order) above r, or the
+    last candidate if none is.  NaN logits count as -inf."""
+    lg = np.array(logits, dtype=np.float32, copy=True)
+    lg[np.isnan(lg)] = -np.inf
+    B, V = lg.shape
+    out = np.empty(B, np.int32)
+    c = np.float32(1.4426950408889634 / float(temperature)) if top_k > 1 else np.float32(0)
+    for b in range(B):
+        row = lg[b]
+        if top_k <= 1:
+            out[b] = int(np.argmax(row))  # first maximum
+            continue
+        order = sorted(range(V), key=lambda i: (-float(row[i]), i))[:top_k]
+        m = row[order[0]]
+        w = [exp2_f32(np.float32(np.float32(row[i] - m) * c)) for i in order]
+        S = np.float32(0.0)
+        for wi in w:
+            S = np.float32(S + wi)
+        r = np.float32(uniform_f32(seed, counter, b) * S)
+        acc = np.float32(0.0)
+        pick = len(order) - 1
+        for j, wi in enumerate(w):
+            acc = np.float32(acc + wi)
+            if acc > r:
+                pick = j
+                break
+        out[b] = order[pick]
+    return out

@@ -554,3 +554,61 @@ def test_embed_bf16_tables_closed_form():
     for b in range(B):
         want = sum((g + 1) + ids[b, g] / 8.0 for g in range(n)) + 0.5
         assert np.all(out[b] == np.float32(want))
+
+
+# ---------------------------------------------------------------------------
+# In-graph sampler: counter RNG, own exponential, greedy / top-k
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("key", [(0, 0), (1, 2), (0xDEADBEEF12345678, 0x0123456789ABCDEF)])
+def test_philox_matches_numpy_philox(key):
+    """numpy's Philox bit generator (Philox4x64-10) steps its counter before each
+    block: its outputs 4(n-1)..4n-1 are the block at counter n."""
+    bg = np.random.Philox(key=np.array(key, dtype=np.uint64),
+                          counter=np.zeros(4, dtype=np.uint64))
+    raw = bg.random_raw(12)
+    for n in range(1, 4):
+        assert [int(x) for x in raw[4 * (n - 1):4 * n]] == oracle.philox4x64_10([n, 0, 0, 0], key)
+
+
+def test_exp2_f32_accuracy_and_exact_powers():
+    xs = np.concatenate([-np.linspace(0, 126, 20001), -np.random.default_rng(31).uniform(0, 126, 2000)])
+    got = np.array([oracle.exp2_f32(x) for x in xs.astype(np.float32)], np.float64)
+    ref = np.exp2(xs.astype(np.float32).astype(np.float64))
+    assert np.max(np.abs(got - ref) / ref) < 3e-7
+    for n in range(0, 127):
+        assert oracle.exp2_f32(np.float32(-n)) == np.float32(2.0 ** -n)
+    assert oracle.exp2_f32(np.float32(-126.5)) == 0.0
+
+
+def test_uniform_is_the_top_24_bits():
+    x = oracle.philox4x64_10([5, 3, 0, 0], [11, 0])[0]
+    assert oracle.uniform_f32(11, 5, 3) == np.float32((x >> 40) / 2.0 ** 24)
+
+
+def test_greedy_is_the_first_maximum():
+    rng = np.random.default_rng(32)
+    lg = rng.standard_normal((6, 300)).astype(np.float32)
+    lg[1, [7, 200]] = 9.0   # a tie: the lower index wins
+    lg[2, 5] = np.nan       # NaN counts as -inf
+    ids = oracle.sample(lg, 0, 1.0, 1, 0)
+    ref = np.argmax(np.where(np.isnan(lg), -np.inf, lg), axis=1)
+    assert np.array_equal(ids, ref) and ids[1] == 7
+    assert np.array_equal(oracle.sample(lg, 1, 0.5, 1, 3), ids)
+
+
+def test_top_k_draws_follow_the_tempered_softmax():
+    """Over many counters the draws of one stream match the softmax of the top-k
+    logits at the given temperature (chi-square, fixed seeds), and never leave the
+    top k."""
+    logits = np.array([[2.0, 1.5, 1.4, 0.3, -1.0, 1.45, -5.0, 0.0]], np.float32)
+    k, T, n = 4, 0.7, 3000
+    top = sorted(range(8), key=lambda i: (-logits[0, i], i))[:k]
+    p = np.exp(logits[0, top].astype(np.float64) / T)
+    p /= p.sum()
+    counts = {i: 0 for i in range(8)}
+    for c in range(n):
+        counts[int(oracle.sample(logits, k, T, 99, c)[0])] += 1
+    assert all(counts[i] == 0 for i in range(8) if i not in top)
+    obs = np.array([counts[i] for i in top], np.float64)
+    chi2 = float(((obs - n * p) ** 2 / (n * p)).sum())
+    assert chi2 < 16.3  # 3 degrees of freedom, p = 0.001
