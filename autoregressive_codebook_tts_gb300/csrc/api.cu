@@ -425,4 +425,35 @@ tts_status tts_prefill_step(float* q, const float* k, const float* v, int64_t ro
                                       d->n_q_heads / d->n_kv_heads, false, s));
 }
 
+tts_status tts_sample(const float* logits, int64_t logits_stride, int32_t B, int32_t vocab,
+                      int32_t top_k, float temperature, uint64_t seed, const uint64_t* counter,
+                      int32_t* out_ids, int64_t out_stride, void* stream) {
+  if (logits == nullptr || out_ids == nullptr || (top_k > 1 && counter == nullptr)) return TTS_ERR_NULL;
+  if (B < 1 || B > 65535 || vocab < 1 || vocab > TTS_MAX_SAMPLE_VOCAB || logits_stride < vocab ||
+      out_stride < 1 || top_k < 0 || top_k > TTS_MAX_TOP_K || top_k > vocab)
+    return TTS_ERR_SHAPE;
+  if (top_k > 1 && !(temperature > 0.f && std::isfinite(temperature))) return TTS_ERR_SHAPE;
+  if ((reinterpret_cast<uintptr_t>(logits) & 3u) != 0 || (reinterpret_cast<uintptr_t>(out_ids) & 3u) != 0 ||
+      (counter != nullptr && (reinterpret_cast<uintptr_t>(counter) & 7u) != 0))
+    return TTS_ERR_ALIGN;
+  SampleParams p = {};
+  p.logits = logits;
+  p.stride = logits_stride;
+  p.B = B;
+  p.V = vocab;
+  p.top_k = top_k;
+  p.c = top_k > 1 ? static_cast<float>(1.4426950408889634 / static_cast<double>(temperature)) : 0.f;
+  p.seed = seed;
+  p.counter = counter;
+  p.out = out_ids;
+  p.out_stride = out_stride;
+  return from_cuda(launch_sample(p, as_stream(stream)));
+}
+
+tts_status tts_counter_advance(uint64_t* counter, uint64_t by, void* stream) {
+  if (counter == nullptr) return TTS_ERR_NULL;
+  if ((reinterpret_cast<uintptr_t>(counter) & 7u) != 0) return TTS_ERR_ALIGN;
+  return from_cuda(launch_counter_advance(counter, by, as_stream(stream)));
+}
+
 }  // extern "C"

@@ -115,6 +115,18 @@ struct PrefillRowsParams {
   int32_t* err;
 };
 
+// Sampler: one stream per CTA (see sample.cu).
+struct SampleParams {
+  const float* logits;
+  int64_t stride;       // floats between consecutive streams' logits
+  int B, V, top_k;      // top_k 0 or 1: greedy
+  float c;              // log2(e) / temperature, rounded once to f32
+  uint64_t seed;
+  const uint64_t* counter;
+  int32_t* out;
+  int64_t out_stride;   // int32 elements between consecutive streams' ids
+};
+
 // Launch helpers (return a cudaError_t from the launch).
 cudaError_t launch_frame_embed(const EmbedParams& p, cudaStream_t s);
 cudaError_t launch_rope_table(float* cs, int max_pos, int head_dim, double base, cudaStream_t s);
@@ -122,6 +134,8 @@ cudaError_t launch_qk_norm_rope(const NormRopeParams& p, cudaStream_t s);
 cudaError_t launch_set_rows(const SetRowsParams& p, cudaStream_t s);
 cudaError_t launch_zero(void* ptr, size_t bytes, cudaStream_t s);
 cudaError_t launch_prefill_rows(const PrefillRowsParams& p, cudaStream_t s);
+cudaError_t launch_sample(const SampleParams& p, cudaStream_t s);
+cudaError_t launch_counter_advance(uint64_t* counter, uint64_t by, cudaStream_t s);
 
 // Tile geometry of the attention kernel for a (dtype, head_dim) pair.
 struct AttnGeometry {

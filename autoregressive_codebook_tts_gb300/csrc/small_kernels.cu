@@ -6,22 +6,6 @@
 namespace tts {
 namespace {
 
-template <typename Kernel, typename... Args>
-cudaError_t launch_pdl(Kernel kern, dim3 grid, dim3 block, size_t smem, cudaStream_t s,
-                       Args... args) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = grid;
-  cfg.blockDim = block;
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, args...);
-}
-
 // ---------------------------------------------------------------------------
 // Frame-input composition ("qwentts.cpp ... src/pipeline-tts.h", on-device AR input
 // assembly): out[b] = ((E_0[c0] + E_1[c1]) + ...) + overlay[b].  One thread per four

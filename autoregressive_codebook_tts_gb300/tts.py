@@ -40,6 +40,8 @@ EXPORTED = [
     "tts_decode_step_noalloc",
     "tts_prefill_workspace_size",
     "tts_prefill_step",
+    "tts_sample",
+    "tts_counter_advance",
 ]
 
 
@@ -79,6 +81,8 @@ _sigs = {
     "tts_decode_step_noalloc": ([_P, _P, _P, _I64, _P, _P, _F, _P, _I32, _P, _P,
                                  ctypes.POINTER(TtsKvDesc), _P, _F, _P, _I32, _P, _P], _I32),
     "tts_prefill_workspace_size": ([ctypes.POINTER(TtsKvDesc), _I32, _I32], _SZ),
+    "tts_sample": ([_P, _I64, _I32, _I32, _I32, _F, ctypes.c_uint64, _P, _P, _I64, _P], _I32),
+    "tts_counter_advance": ([_P, ctypes.c_uint64, _P], _I32),
     "tts_prefill_step": ([_P, _P, _P, _I64, _P, _P, _F, _P, _I32, _P, _P,
                           ctypes.POINTER(TtsKvDesc), _P, _I32, _F, _P, _P, _SZ, _I32, _P, _P], _I32),
 }
@@ -268,6 +272,20 @@ def tts_prefill_step(q, k, v, gamma_q, gamma_k, eps, cs, max_pos, k_cache, v_cac
                                  _ptr(out), _ptr(ws),
                                  0 if ws is None else ws.numel() * ws.element_size(),
                                  n_splits, _ptr(err_flag), _stream(stream)), "tts_prefill_step")
+
+
+def tts_sample(logits, top_k, temperature, seed, counter, out_ids, stream=None):
+    """logits [B, V] f32 (rows may be strided); out_ids: int32 tensor whose first dim
+    indexes streams (a column view of an ids buffer is fine)."""
+    B, V = logits.shape
+    _check(_lib.tts_sample(_ptr(logits), logits.stride(0), B, V, int(top_k), float(temperature),
+                           ctypes.c_uint64(int(seed) & ((1 << 64) - 1)), _ptr(counter),
+                           _ptr(out_ids), out_ids.stride(0), _stream(stream)), "tts_sample")
+
+
+def tts_counter_advance(counter, by=1, stream=None):
+    _check(_lib.tts_counter_advance(_ptr(counter), ctypes.c_uint64(int(by)), _stream(stream)),
+           "tts_counter_advance")
 
 
 def default_scale(head_dim: int) -> float:

@@ -294,6 +294,37 @@ tts_status tts_prefill_step(float* q, const float* k, const float* v, int64_t ro
                             int32_t T, float scale, float* out, void* workspace, size_t ws_bytes,
                             int32_t n_splits, int32_t* err_flag, void* stream);
 
+/* ---------------------------------------------------------------------------
+ * In-graph sampler with a counter RNG ([P-pipeline]: the predictor frame unroll and
+ * the in-graph sampler; [engine] options table, "Lean Talker frame": one-kernel
+ * counter RNG).  For stream b, from its logits row l (vocab entries; NaN counts as
+ * -inf):
+ *   top_k 0 or 1: the index of the largest logit (the lowest such index on a tie);
+ *   top_k = k in [2, TTS_MAX_TOP_K]: candidates are the k largest logits, larger first
+ *   and lower index first on a tie, l_0 >= ... >= l_{k-1}; with c = log2(e)/temperature
+ *   rounded once to f32, w_i = 2^(f32(f32(l_i - l_0) * c)) in f32 (an exponential of
+ *   this library's own: degree-9 Taylor polynomial of 2^f on [0, 1) in Horner form,
+ *   times 2^floor, 0 below 2^-126); S = w_0 + ... + w_{k-1} in that order; u = top 24
+ *   bits of the first output of Philox4x64-10 at counter words (*counter, b, 0, 0) and
+ *   key (seed, 0), times 2^-24; the token is candidate i of the first running sum
+ *   (same order) above f32(u * S), else the last candidate.  Every operation is a
+ *   single f32 rounding in that order, so the result is exactly reproducible.
+ *   logits: device f32, stream b at logits + b*logits_stride.
+ *   counter: device uint64 (read only here); advance it between draws with
+ *        tts_counter_advance so that a replayed graph draws fresh numbers.
+ *   out_ids: device int32, stream b's token at out_ids + b*out_stride (for example
+ *        the column of the next frame's code ids).
+ * vocab must not exceed TTS_MAX_SAMPLE_VOCAB.
+ * ------------------------------------------------------------------------- */
+#define TTS_MAX_TOP_K 64
+#define TTS_MAX_SAMPLE_VOCAB 8192
+tts_status tts_sample(const float* logits, int64_t logits_stride, int32_t B, int32_t vocab,
+                      int32_t top_k, float temperature, uint64_t seed, const uint64_t* counter,
+                      int32_t* out_ids, int64_t out_stride, void* stream);
+
+/* *counter += by, as one kernel on `stream` (graph-capturable). */
+tts_status tts_counter_advance(uint64_t* counter, uint64_t by, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -343,7 +343,7 @@ def exp2_f32(x):
     2^f (each product and sum rounded to f32, no fused multiply-add), times 2^n
     (exact)."""
     x = np.float32(x)
-    if x < np.float32(-126.0):
+    if not x >= np.float32(-126.0):  # also NaN
         return np.float32(0.0)
     n = math.floor(float(x))
     f = np.float32(x - np.float32(n))
@@ -362,7 +362,8 @@ def sample(logits, top_k, temperature, seed, counter):
     double); w_i = exp2_f32(f32(f32(l_i - l_0) * c)); S = w_0 + ... + w_{k-1} summed in
     that order in f32; r = f32(u * S) with u = uniform_f32(seed, counter, b); the result
     is the candidate i of the first running sum (in f32, same order) above r, or the
-    last candidate if none is.  NaN logits count as -inf."""
+    last candidate if none is.  NaN logits count as -inf; when the top candidate is not
+    finite the result is that candidate."""
     lg = np.array(logits, dtype=np.float32, copy=True)
     lg[np.isnan(lg)] = -np.inf
     B, V = lg.shape
@@ -375,6 +376,9 @@ def sample(logits, top_k, temperature, seed, counter):
             continue
         order = sorted(range(V), key=lambda i: (-float(row[i]), i))[:top_k]
         m = row[order[0]]
+        if not np.isfinite(m):  # no finite logit on top: the first candidate
+            out[b] = order[0]
+            continue
         w = [exp2_f32(np.float32(np.float32(row[i] - m) * c)) for i in order]
         S = np.float32(0.0)
         for wi in w:
