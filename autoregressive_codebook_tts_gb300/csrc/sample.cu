@@ -2,11 +2,13 @@
 // frame unroll keeps its in-graph sampler; "minicpm-o-4.5 ... optimizations.md",
 // options table, "Lean Talker frame": one-kernel counter RNG).
 //
-// One CTA per stream.  The logits row is staged in shared memory; the top_k candidates
-// (larger logit first, lower index first on a tie) are taken by top_k rounds of a
-// block-wide arg-max that skips the candidates already taken.  Thread 0 then turns them
-// into weights 2^((l_i - l_0) * log2(e) / T) and walks the running sum against
-// u * sum, u from Philox4x64-10 at counter words (counter, stream) and key (seed, 0).
+// One CTA per stream.  The logits row is staged in shared memory as order-preserving
+// integer keys; the k-th largest is found by a radix selection (four 8-bit passes of
+// a shared-memory histogram), the top_k candidates gathered (ties at the threshold by
+// lowest index) and ordered by rank (larger logit first, lower index first).  Each
+// candidate's weight 2^((l_i - l_0) * log2(e) / T) is computed by its own thread;
+// thread 0 walks the running sum against u * sum, u from Philox4x64-10 at counter words
+// (counter, stream) and key (seed, 0).
 // Every value that decides the token is computed in f32 in a fixed order with explicit
 // round-to-nearest operations (no contraction into fused multiply-adds); the
 // exponential is this file's own (a degree-9 Taylor polynomial of 2^f, f in [0, 1),
@@ -60,89 +62,178 @@ __device__ __forceinline__ float exp2_f32(float x) {
   return __fmul_rn(p, __int_as_float((n + 127) << 23));
 }
 
-// Is (va, ia) ahead of (vb, ib): larger value first, lower index first on a tie.
-__device__ __forceinline__ bool ahead(float va, int ia, float vb, int ib) {
-  return ib < 0 || (ia >= 0 && (va > vb || (va == vb && ia < ib)));
+// Order-preserving 32-bit key of a float (a larger float has a larger key); the
+// caller maps NaN to -inf and -0 to +0 first, so equal floats have equal keys.
+__device__ __forceinline__ uint32_t float_key(float v) {
+  const uint32_t u = __float_as_uint(v);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key_float(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
 }
 
+// Is (ka, ia) ahead of (kb, ib): larger key first, lower index first on a tie.
+__device__ __forceinline__ bool key_ahead(uint32_t ka, int ia, uint32_t kb, int ib) {
+  return ka > kb || (ka == kb && ia < ib);
+}
+
+constexpr int kChunk = TTS_MAX_SAMPLE_VOCAB / kSampleThreads;  // indices per thread, at most
+
 __global__ void __launch_bounds__(kSampleThreads) sample_kernel(const SampleParams p) {
-  extern __shared__ float s_val[];  // the row; NaN marks a taken candidate
-  __shared__ float s_wv[kSampleWarps];
-  __shared__ int s_wi[kSampleWarps];
-  __shared__ float s_cv[TTS_MAX_TOP_K];
+  extern __shared__ uint32_t s_key[];  // the row as keys
+  __shared__ int s_hist[256];
+  __shared__ int s_sel[2];             // chosen digit, keys still to take at the threshold
+  __shared__ int s_scan[kSampleThreads];
+  __shared__ int s_n;
+  __shared__ uint32_t s_ck[TTS_MAX_TOP_K];
   __shared__ int s_ci[TTS_MAX_TOP_K];
+  __shared__ uint32_t s_sk[TTS_MAX_TOP_K];
+  __shared__ int s_si[TTS_MAX_TOP_K];
+  __shared__ float s_w[TTS_MAX_TOP_K];
+  __shared__ uint32_t s_wk[kSampleWarps];
+  __shared__ int s_wi[kSampleWarps];
   grid_wait();
   grid_launch_dependents();
   const int b = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int V = p.V;
   const float* row = p.logits + static_cast<int64_t>(b) * p.stride;
-  for (int i = tid; i < p.V; i += kSampleThreads) {
-    const float v = __ldcg(row + i);
-    s_val[i] = (v != v) ? -INFINITY : v;  // a NaN logit counts as -inf
+  for (int i = tid; i < V; i += kSampleThreads) {
+    float v = __ldcg(row + i);
+    if (v != v) v = -INFINITY;  // a NaN logit counts as -inf
+    if (v == 0.0f) v = 0.0f;    // -0 and +0 are the same logit
+    s_key[i] = float_key(v);
   }
   __syncthreads();
-  const int rounds = p.top_k > 1 ? p.top_k : 1;
-  for (int j = 0; j < rounds; ++j) {
-    float bv = -INFINITY;
+
+  if (p.top_k <= 1) {
+    // greedy: the largest logit, the lowest index on a tie
+    uint32_t bk = 0;
     int bi = -1;
-    for (int i = tid; i < p.V; i += kSampleThreads) {
-      const float v = s_val[i];
-      if (v == v && ahead(v, i, bv, bi)) {
-        bv = v;
+    for (int i = tid; i < V; i += kSampleThreads) {
+      const uint32_t k = s_key[i];
+      if (bi < 0 || key_ahead(k, i, bk, bi)) {
+        bk = k;
         bi = i;
       }
     }
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) {
-      const float ov = __shfl_xor_sync(kFull, bv, off);
+      const uint32_t ok = __shfl_xor_sync(kFull, bk, off);
       const int oi = __shfl_xor_sync(kFull, bi, off);
-      if (ahead(ov, oi, bv, bi)) {
-        bv = ov;
+      if (oi >= 0 && (bi < 0 || key_ahead(ok, oi, bk, bi))) {
+        bk = ok;
         bi = oi;
       }
     }
     if (lane == 0) {
-      s_wv[warp] = bv;
+      s_wk[warp] = bk;
       s_wi[warp] = bi;
     }
     __syncthreads();
     if (tid == 0) {
       for (int w = 1; w < kSampleWarps; ++w)
-        if (ahead(s_wv[w], s_wi[w], bv, bi)) {
-          bv = s_wv[w];
+        if (s_wi[w] >= 0 && (bi < 0 || key_ahead(s_wk[w], s_wi[w], bk, bi))) {
+          bk = s_wk[w];
           bi = s_wi[w];
         }
-      s_cv[j] = bv;
-      s_ci[j] = bi;
-      s_val[bi] = __int_as_float(0x7fc00000);  // taken
+      p.out[static_cast<int64_t>(b) * p.out_stride] = bi;
+    }
+    return;
+  }
+
+  // The k-th largest key by radix selection, 8 bits a pass from the top: `prefix`
+  // holds the digits fixed so far, `need` how many keys with that prefix are still to
+  // take.  After the last pass, `prefix` is the threshold key and `need` how many of
+  // the keys equal to it belong to the top k (the lowest-index ones).
+  const int k = p.top_k;
+  uint32_t prefix = 0, mask = 0;
+  int need = k;
+  for (int shift = 24; shift >= 0; shift -= 8) {
+    s_hist[tid] = 0;  // 256 threads, 256 bins
+    __syncthreads();
+    for (int i = tid; i < V; i += kSampleThreads) {
+      const uint32_t key = s_key[i];
+      if ((key & mask) == prefix) atomicAdd(&s_hist[(key >> shift) & 255u], 1);
     }
     __syncthreads();
+    if (tid == 0) {
+      int above = 0, d = 255;
+      for (; d > 0; --d) {
+        if (above + s_hist[d] >= need) break;
+        above += s_hist[d];
+      }
+      s_sel[0] = d;
+      s_sel[1] = need - above;
+    }
+    __syncthreads();
+    prefix |= static_cast<uint32_t>(s_sel[0]) << shift;
+    mask |= 255u << shift;
+    need = s_sel[1];
+    __syncthreads();
   }
+  // Gather the k candidates: every key above the threshold, and the `need` lowest
+  // indices of those equal to it (each thread owns a contiguous index range, so an
+  // exclusive scan of the per-thread counts ranks the equal keys by index).
+  const int i0 = tid * kChunk;
+  const int i1 = min(i0 + kChunk, V);
+  int eq = 0;
+  for (int i = i0; i < i1; ++i) eq += s_key[i] == prefix;
+  s_scan[tid] = eq;
+  if (tid == 0) s_n = 0;
+  __syncthreads();
+  for (int off = 1; off < kSampleThreads; off <<= 1) {  // inclusive scan
+    const int v = tid >= off ? s_scan[tid - off] : 0;
+    __syncthreads();
+    s_scan[tid] += v;
+    __syncthreads();
+  }
+  int rank = s_scan[tid] - eq;  // equal keys at lower indices
+  for (int i = i0; i < i1; ++i) {
+    const uint32_t key = s_key[i];
+    bool take = key > prefix;
+    if (key == prefix) take = rank++ < need;
+    if (take) {
+      const int slot = atomicAdd(&s_n, 1);
+      s_ck[slot] = key;
+      s_ci[slot] = i;
+    }
+  }
+  __syncthreads();
+  // Order them (larger key first, lower index first) by rank, and weigh them.
+  if (tid < k) {
+    const uint32_t mk = s_ck[tid];
+    const int mi = s_ci[tid];
+    int r = 0;
+    for (int j = 0; j < k; ++j) r += key_ahead(s_ck[j], s_ci[j], mk, mi);
+    s_sk[r] = mk;
+    s_si[r] = mi;
+  }
+  __syncthreads();
+  const float m = key_float(s_sk[0]);
+  const bool finite_top = m > -INFINITY && m < INFINITY;
+  if (tid < k && finite_top) s_w[tid] = exp2_f32(__fmul_rn(__fsub_rn(key_float(s_sk[tid]), m), p.c));
+  __syncthreads();
   if (tid != 0) return;
   int pick = 0;
-  const float m = s_cv[0];
-  if (p.top_k > 1 && m > -INFINITY && m < INFINITY) {
-    float w[TTS_MAX_TOP_K];
+  if (finite_top) {
     float S = 0.0f;
-    for (int j = 0; j < p.top_k; ++j) {
-      w[j] = exp2_f32(__fmul_rn(__fsub_rn(s_cv[j], m), p.c));
-      S = __fadd_rn(S, w[j]);
-    }
+    for (int j = 0; j < k; ++j) S = __fadd_rn(S, s_w[j]);
     uint64_t ctr[4] = {__ldcg(p.counter), static_cast<uint64_t>(b), 0ull, 0ull};
     philox4x64_10(ctr, p.seed, 0ull);
     const float u = static_cast<float>(ctr[0] >> 40) * 0x1.0p-24f;  // exact
     const float r = __fmul_rn(u, S);
     float acc = 0.0f;
-    pick = p.top_k - 1;
-    for (int j = 0; j < p.top_k; ++j) {
-      acc = __fadd_rn(acc, w[j]);
+    pick = k - 1;
+    for (int j = 0; j < k; ++j) {
+      acc = __fadd_rn(acc, s_w[j]);
       if (acc > r) {
         pick = j;
         break;
       }
     }
   }
-  p.out[static_cast<int64_t>(b) * p.out_stride] = s_ci[pick];
+  p.out[static_cast<int64_t>(b) * p.out_stride] = s_si[pick];
 }
 
 __global__ void counter_advance_kernel(uint64_t* counter, uint64_t by) {

@@ -41,7 +41,10 @@ def parse():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
-    ap.add_argument("--workload", default="talker", choices=["talker", "batched", "paged", "prefill"])
+    ap.add_argument("--workload", default="talker",
+                    choices=["talker", "batched", "paged", "prefill", "predictor"])
+    ap.add_argument("--frames-per-replay", type=int, default=4,
+                    help="predictor: frames unrolled into one graph replay")
     ap.add_argument("--layers", type=int, default=0,
                     help="layers per frame (0 = the workload's own; fewer only for small profiling cases)")
     ap.add_argument("--prefill-t", type=int, default=128, help="prefill: prompt positions per stream")
@@ -569,6 +572,174 @@ def run_prefill(args, rank, world):
     }
 
 
+def run_predictor(args, rank, world):
+    """Code-predictor frames, K per graph replay: per frame the T=2 prefill (rows 0, 1)
+    of all layers, then 14 single-token decode steps; before every step after the
+    prefill the in-graph sampler draws the next code from that step's logits and the
+    frame-input composition gathers it from its group table.  The logits (the output
+    heads are outside this path) are fixed synthetic rows, one per sub-step."""
+    import torch
+    from autoregressive_codebook_tts_gb300 import build as b
+    b.build()
+    from autoregressive_codebook_tts_gb300 import tts
+    from autoregressive_codebook_tts_gb300 import workloads as W
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    w = W.workload("predictor")
+    B, L, Hq, Hkv, D, V = w.B, w.layers, w.n_q_heads, w.n_kv_heads, w.head_dim, w.vocab
+    K = max(1, args.frames_per_replay)
+    g = torch.Generator(device=dev)
+    g.manual_seed(rank)
+    qd, kd = Hq * D, Hkv * D
+    tables = [torch.randn(V, w.hidden, generator=g, device=dev) * w.table_std for _ in range(15)]
+    tabs = [tts.tables([t]) for t in tables]
+    qkv = torch.randn(16, L, B, qd + 2 * kd, generator=g, device=dev)   # per position, layer
+    pre = torch.randn(L, 2 * B, qd + 2 * kd, generator=g, device=dev)    # prefill rows b*2+t
+    logits = torch.randn(15, B, V, generator=g, device=dev) * 2.0
+    gq = torch.rand(L, D, generator=g, device=dev) + 0.5
+    gk = torch.rand(L, D, generator=g, device=dev) + 0.5
+    caches = [(torch.zeros(B, Hkv, w.capacity, D, device=dev), torch.zeros(B, Hkv, w.capacity, D, device=dev))
+              for _ in range(L)]
+    cs = torch.empty(w.capacity, D // 2, 2, device=dev)
+    tts.tts_rope_table(cs, w.capacity, D, w.rope_base)
+    desc = tts.kv_desc(B, Hq, Hkv, D, w.capacity, "f32", window_quantum=w.window_quantum)
+    ws = tts.workspace(desc, 0, device=dev)
+    pws = tts.prefill_workspace(desc, 2, 0, device=dev)
+    codes = torch.zeros(B, 16, dtype=torch.int32, device=dev)
+    emb = torch.empty(B, w.hidden, device=dev)
+    out = torch.empty(B, Hq, D, device=dev)
+    pout = torch.empty(B, 2, Hq, D, device=dev)
+    zeros = torch.zeros(B, dtype=torch.int32, device=dev)
+    curs = [torch.full((B,), t, dtype=torch.int32, device=dev) for t in range(16)]
+    counter = torch.zeros(1, dtype=torch.int64, device=dev)
+    ef = torch.zeros(1, dtype=torch.int32, device=dev)
+    scale = 1.0 / math.sqrt(D)
+    top_k, temp, seed = 50, 0.9, 1234 + rank
+
+    def frame():
+        # the reset is the position: the prefill writes rows 0 and 1 from position 0
+        tts.tts_frame_embed(tabs[0], codes[:, 0:1], None, emb, ef)
+        for l in range(L):
+            rows = pre[l]
+            tts.tts_prefill_step(rows[:, :qd], rows[:, qd:qd + kd], rows[:, qd + kd:], gq[l], gk[l],
+                                 w.eps, cs, w.capacity, caches[l][0], caches[l][1], desc, zeros, 2,
+                                 scale, pout, pws, 0, ef)
+        for t in range(2, 16):
+            j = t - 1  # code j, drawn from the previous step's logits, then gathered
+            tts.tts_sample(logits[j - 1], top_k, temp, seed, counter, codes[:, j])
+            tts.tts_frame_embed(tabs[j], codes[:, j:j + 1], None, emb, ef)
+            for l in range(L):
+                rows = qkv[t, l]
+                tts.tts_decode_step(rows[:, :qd], rows[:, qd:qd + kd], rows[:, qd + kd:], gq[l], gk[l],
+                                    w.eps, cs, w.capacity, caches[l][0], caches[l][1], desc, curs[t],
+                                    scale, out, ws, 0, ef)
+        tts.tts_sample(logits[14], top_k, temp, seed, counter, codes[:, 15])
+        tts.tts_counter_advance(counter, 1)
+
+    def frames():
+        for _ in range(K):
+            frame()
+
+    gr = capture(frames, torch)
+    for _ in range(args.warmup):
+        gr.replay()
+    torch.cuda.synchronize()
+    if ef.item() != 0:
+        raise RuntimeError(f"device error flag {ef.item()}")
+    replays = max(1, args.steps // K)
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t = timed_replays(gr, replays, torch)
+    clk = clocks.stop()
+    (t,) = max_over_ranks([t], world, dev)
+    n_frames = replays * K
+    # algorithmic bytes per frame: every step's window (rows 0..t) for every layer and
+    # stream, the new rows, q/k/v and outputs, the gathered table rows, the logits
+    kv = sum(t + 1 for t in range(16)) * L * B * 2 * kd * 4
+    act = 16 * L * B * ((qd + 2 * kd) * 4 + qd * 4) + 15 * B * (w.hidden * 4 * 2 + V * 4)
+    frame_bytes = kv + act
+    peak, peak_kind = hbm_peak()
+    launches = 1 + 2 * L + 14 * (2 + L) + 2
+    value = world * B * n_frames / t
+    return {
+        "metric": "code-predictor frame steps per second (B streams)",
+        "value": round(value, 1), "unit": "frame steps/s", "n_gpus": world, "steps": n_frames,
+        "warmup": args.warmup, "ms_per_step": round(t / n_frames * 1e3, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded, device-generated; random-init, no weights; fixed logits)",
+        "config": {"workload": f"predictor: B={B} streams, {L} layers, hidden {w.hidden}, 16/8 heads, "
+                               f"head_dim {D}, f32 KV, 16-slot cache reset per frame, T=2 prefill + 14 decodes, "
+                               f"top-{top_k} sampling at T={temp}",
+                   "frames_per_replay": K, "launches_per_frame": launches,
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "us_per_frame": round(t / n_frames * 1e6, 2),
+        "roofline": {"bound": "hbm", "achieved": round(frame_bytes / (t / n_frames) / 1e9, 1), "peak": peak,
+                     "unit": "GB/s", "frac": round(frame_bytes / (t / n_frames) / 1e9 / peak, 4),
+                     "traffic": None, "kernel": "whole predictor frame (launch-bound; the roofline "
+                     "fraction is not meaningful at 0.4 MB per launch)",
+                     "peak_source": "measured HBM copy bandwidth" if peak_kind == "measured"
+                     else "fallback HBM copy bandwidth", "bytes_per_frame": frame_bytes},
+        "gpu_launches": launches * n_frames,
+        "clocks": clk,
+    }
+
+
+def run_reference_predictor(args, world):
+    """The oracle's code-predictor frame (same shapes, fixed codes) as the reference
+    arm's step: one step = one frame of all streams."""
+    import numpy as np
+    from autoregressive_codebook_tts_gb300 import workloads as W
+    import oracle
+    w = W.workload("predictor")
+    B, L, Hq, Hkv, D = w.B, w.layers, w.n_q_heads, w.n_kv_heads, w.head_dim
+    tabs = [t.numpy() for t in W.tables(15, w.vocab, w.hidden, seed=50)]
+    codes = W.code_ids(B, 15, w.vocab, seed=70).numpy()
+    qkv = []
+    for t in range(16):
+        per_l = []
+        for l in range(L):
+            _, q, k, v = W.qkv(B, Hq, Hkv, D, seed=16 * l + t)
+            per_l.append((q.numpy().reshape(B, Hq, D), k.numpy().reshape(B, Hkv, D),
+                          v.numpy().reshape(B, Hkv, D)))
+        qkv.append(per_l)
+    gam = [(W.gamma(D, 4 + l).numpy(), W.gamma(D, 40 + l).numpy()) for l in range(L)]
+    caches = [(np.zeros((B, Hkv, w.capacity, D), np.float32), np.zeros((B, Hkv, w.capacity, D), np.float32))
+              for _ in range(L)]
+    lay = oracle.KvLayout(B, Hkv, D, w.capacity)
+
+    def step():
+        oracle.predictor_frame(tabs, codes, None, qkv, gam, np.float32(w.eps), w.rope_base, caches, lay,
+                               1.0 / math.sqrt(D))
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = time.perf_counter() - t0
+    value = B * args.steps / dt
+    return {
+        "impl": "reference",
+        "metric": "code-predictor frame steps per second (B streams)",
+        "value": round(value, 3), "unit": "frame steps/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)",
+        "data": "synthetic (seeded)",
+        "config": {"workload": f"predictor: B={B} streams, {L} layers (same shapes as the native arm)",
+                   "parallelism": "single host thread"},
+        "cpu_baseline": {"value": round(value, 3), "unit": "frame steps/s", "cores": 1, "kind": "oracle",
+                         "sample": "each step: one whole predictor frame of all streams (fixed codes)"},
+        "e2e": {"value": round(value, 3), "unit": "frame steps/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
 def run_reference_prefill(args, world):
     """The oracle's prefill of one layer (talker shapes) as the reference arm's step."""
     import numpy as np
@@ -627,6 +798,8 @@ def run_reference(args, rank, world):
     oracle.build()
     if args.workload == "prefill":
         return run_reference_prefill(args, world)
+    if args.workload == "predictor":
+        return run_reference_predictor(args, world)
     w = W.workload(args.workload)
     cur_list = [args.cur_len] * w.B if args.workload == "talker" else [int(c) for c in W.cur_lens(w, 0)]
     cur = np.array(cur_list, np.int32)
@@ -696,7 +869,12 @@ def main():
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl")
-    res = run_prefill(args, rank, world) if args.workload == "prefill" else run_native(args, rank, world)
+    if args.workload == "prefill":
+        res = run_prefill(args, rank, world)
+    elif args.workload == "predictor":
+        res = run_predictor(args, rank, world)
+    else:
+        res = run_native(args, rank, world)
     if rank == 0:
         print(json.dumps(res))
     if world > 1:
