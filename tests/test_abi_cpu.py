@@ -119,3 +119,44 @@ def test_other_entry_points_validate(tts):
                                      1e-6, P(16), 4096, None, None) == 1
     assert tts._lib.tts_qk_norm_rope(P(16), 1000, P(16), 1024, P(16), P(16), P(16), 1, 16, 8, 128,
                                      1e-6, P(16), 4096, None, None) == 2
+
+
+@no_gpu
+def test_prefill_sampler_and_table_dtype_validate(tts):
+    P = ctypes.c_void_p
+    t = tts.TtsTables()
+    t.n_tables, t.vocab, t.hidden, t.dtype = 1, 2048, 1024, 5
+    assert tts._lib.tts_frame_embed(ctypes.byref(t), P(16), 16, None, 0, P(16), 1, None, None) == 3
+
+    d = tts.kv_desc(2, 16, 8, 128, 4096)
+
+    def prefill(q=16, T=4, stride=4096, ws=256, ws_bytes=1 << 20, start=16):
+        return tts._lib.tts_prefill_step(P(q) if q else None, P(16), P(16), stride, P(16), P(16),
+                                         1e-6, P(16), 4096, P(16), P(16), ctypes.byref(d),
+                                         P(start) if start else None, T, 0.1, P(16),
+                                         P(ws) if ws else None, ws_bytes, 8, None, None)
+    assert prefill(q=0) == 1
+    assert prefill(start=0) == 1
+    assert prefill(T=0) == 2
+    assert prefill(T=40000) == 2                 # B*T above 65535 queries
+    assert prefill(stride=1000) == 2             # row shorter than the q heads
+    assert prefill(q=24) == 5                    # misaligned q
+    assert prefill(ws_bytes=16) == 6             # workspace too small for 8 splits
+    assert tts.tts_prefill_workspace_size(d, 4, 8) > tts.tts_decode_attn_workspace_size(d, 8)
+    assert tts.tts_prefill_workspace_size(d, 0, 8) == 0
+
+    def sample(lg=16, V=2048, k=50, T=1.0, ctr=64, out=16, stride=2048):
+        return tts._lib.tts_sample(P(lg) if lg else None, stride, 4, V, k, T, 1,
+                                   P(ctr) if ctr else None, P(out) if out else None, 1, None)
+    assert sample(lg=0) == 1
+    assert sample(out=0) == 1
+    assert sample(ctr=0) == 1                    # sampling needs the counter
+    assert sample(V=9000, stride=9000) == 2      # above TTS_MAX_SAMPLE_VOCAB
+    assert sample(k=65) == 2                     # above TTS_MAX_TOP_K
+    assert sample(V=32, k=40, stride=32) == 2    # k above the vocabulary
+    assert sample(T=0.0) == 2
+    assert sample(stride=100) == 2               # rows overlap
+    assert sample(lg=18) == 5                    # misaligned logits
+    assert sample(ctr=68) == 5                   # misaligned counter
+    assert tts._lib.tts_counter_advance(None, 1, None) == 1
+    assert tts._lib.tts_counter_advance(P(12), 1, None) == 5
