@@ -105,6 +105,11 @@
 #ifndef TTS_INFLIGHT_STREAM
 #define TTS_INFLIGHT_STREAM 0
 #endif
+// Persistent grids: the fixed cost of a work item (q load, merge, ticket), in cache
+// rows' worth of streaming time, used to choose the split length of a launch.
+#ifndef TTS_ITEM_COST_ROWS
+#define TTS_ITEM_COST_ROWS 128
+#endif
 #ifndef TTS_ATTN_MIN_BLOCKS
 #define TTS_ATTN_MIN_BLOCKS 2
 #endif
@@ -484,7 +489,8 @@ struct Item {
 };
 
 template <bool FUSED>
-__device__ __forceinline__ Item make_item(const AttnParams& p, int T, int b, int g, int split, int raw) {
+__device__ __forceinline__ Item make_item(const AttnParams& p, int T, int b, int g, int split, int raw,
+                                          int split_len) {
   Item it;
   it.b = b;
   it.cb = b / p.q_per_stream;
@@ -502,11 +508,11 @@ __device__ __forceinline__ Item make_item(const AttnParams& p, int T, int b, int
     it.nv = min(max(raw, 1), p.capacity);
     cache_end = it.nv;
   }
-  it.r0 = split * p.split_len;
-  it.n_rows = max(0, min(it.r0 + p.split_len, cache_end) - it.r0);
-  it.has_fresh = FUSED && it.fresh_ok && it.cur >= it.r0 && it.cur < it.r0 + p.split_len;
+  it.r0 = split * split_len;
+  it.n_rows = max(0, min(it.r0 + split_len, cache_end) - it.r0);
+  it.has_fresh = FUSED && it.fresh_ok && it.cur >= it.r0 && it.cur < it.r0 + split_len;
   it.ntiles = (it.n_rows + T - 1) / T;
-  it.n_act = min(p.n_splits, (it.nv + p.split_len - 1) / p.split_len);
+  it.n_act = min(p.n_splits, (it.nv + split_len - 1) / split_len);
   return it;
 }
 
@@ -517,9 +523,12 @@ __device__ __forceinline__ int raw_len(const AttnParams& p, int b) {
   return __ldcg(p.lens + cb) + (b - cb * p.q_per_stream) + p.lens_add;
 }
 
-__device__ __forceinline__ int n_active(const AttnParams& p, int raw, bool fused) {
-  const int nv = fused ? min(max(raw + 1, 1), p.capacity) : min(max(raw, 1), p.capacity);
-  return min(p.n_splits, (nv + p.split_len - 1) / p.split_len);
+__device__ __forceinline__ int window_len(const AttnParams& p, int raw, bool fused) {
+  return fused ? min(max(raw + 1, 1), p.capacity) : min(max(raw, 1), p.capacity);
+}
+
+__device__ __forceinline__ int n_active(const AttnParams& p, int nv, int split_len) {
+  return min(p.n_splits, (nv + split_len - 1) / split_len);
 }
 
 template <typename KvT, int D, int G, bool FUSED>
@@ -583,24 +592,72 @@ decode_attn_kernel(const AttnParams p) {
   // splits only, prefix sums of Hkv * n_act[b] in shared memory.  Otherwise one item,
   // the CTA's own (split, g, b).
   int n_items;
+  int split_len = p.split_len;
+  volatile int* s_split = reinterpret_cast<volatile int*>(smem + p.sm_flag + 8);
   if (persistent) {
+    // The split length of this launch, chosen from the actual windows: for r = 1, 2, 3
+    // rounds of items over the grid, L_r is the smallest multiple of the tile (at least
+    // the launcher's split) that cuts the windows into at most r * grid items; a CTA
+    // then finishes within about r * (L_r + the fixed cost of an item), and the r with
+    // the smallest such bound wins.  Few large items instead of a long queue of small
+    // ones: each item pays a q load, a merge and a ticket.  Every CTA computes the same
+    // value from the same windows.
     if (warp == 0) {
+      for (int b0 = 0; b0 < p.B; b0 += 32) {  // s_pre[b + 1] = window length, for now
+        const int bb = b0 + lane;
+        if (bb < p.B) s_pre[bb + 1] = window_len(p, raw_len(p, bb), FUSED);
+      }
+      __syncwarp();
+      auto items_at = [&](int L) -> long long {
+        long long n = 0;
+        for (int b0 = 0; b0 < p.B; b0 += 32) {
+          const int bb = b0 + lane;
+          int v = bb < p.B ? Hkv * n_active(p, s_pre[bb + 1], L) : 0;
+#pragma unroll
+          for (int off = 16; off >= 1; off >>= 1) v += __shfl_xor_sync(kFull, v, off);
+          n += v;
+        }
+        return n;
+      };
+      const int lo0 = (p.split_len + T - 1) / T, hi0 = (p.capacity + T - 1) / T;  // in tiles
+      long long best = -1;
+      for (int r = 1; r <= 3; ++r) {
+        const long long target = static_cast<long long>(r) * gridDim.x;
+        int lo = lo0, hi = hi0;
+        if (items_at(lo * T) > target) {
+          while (hi - lo > 1) {  // items_at(hi * T) <= target unless even whole windows exceed it
+            const int mid = (lo + hi) >> 1;
+            if (items_at(mid * T) <= target) hi = mid; else lo = mid;
+          }
+          lo = hi;
+        }
+        const long long est = static_cast<long long>(r) * (lo * T + TTS_ITEM_COST_ROWS);
+        if (best < 0 || est < best) {
+          best = est;
+          split_len = lo * T;
+        }
+      }
       int carry = 0;
       for (int b0 = 0; b0 < p.B; b0 += 32) {
         const int bb = b0 + lane;
-        int v = bb < p.B ? Hkv * n_active(p, raw_len(p, bb), FUSED) : 0;
+        int v = bb < p.B ? Hkv * n_active(p, s_pre[bb + 1], split_len) : 0;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
           const int u = __shfl_up_sync(kFull, v, off);
           if (lane >= off) v += u;
         }
+        __syncwarp();
         if (bb < p.B) s_pre[bb + 1] = carry + v;
         carry += __shfl_sync(kFull, v, 31);
       }
-      if (lane == 0) s_pre[0] = 0;
+      if (lane == 0) {
+        s_pre[0] = 0;
+        *s_split = split_len;
+      }
     }
     __syncthreads();
     n_items = s_pre[p.B];
+    split_len = *s_split;
   } else {
     n_items = 1;
   }
@@ -621,7 +678,7 @@ decode_attn_kernel(const AttnParams p) {
       g = blockIdx.y;
       split = blockIdx.x;
     }
-    return make_item<FUSED>(p, T, b, g, split, raw_len(p, b));
+    return make_item<FUSED>(p, T, b, g, split, raw_len(p, b), split_len);
   };
   // Persistent mode: queue slot j = k % 4 carries this CTA's k-th item from the
   // scheduler (the K producer's lane 0) to the V producer and the consumer warps;
@@ -1203,7 +1260,11 @@ cudaError_t launch_one(const AttnParams& p_in, cudaStream_t s) {
   size_t ring_bytes;
   if (p.persistent || p.cluster > 1) {
     int ns = ring_stages(p.persistent ? TTS_RING_KB_STREAM : TTS_RING_KB_CLUSTER);
-    if (ns > ntiles) ns = ntiles;
+    // a persistent launch picks its split length on the device (up to the capacity);
+    // the consumers' two-deep pipeline needs two stages once an item has two tiles
+    const int item_tiles = p.persistent ? (p.capacity + C::T - 1) / C::T : ntiles;
+    if (ns > item_tiles) ns = item_tiles;
+    if (ns < 2 && item_tiles >= 2) ns = 2;
     p.n_stages = ns;
     ring_bytes = static_cast<size_t>(ns) * C::STAGE_BYTES;
   } else {
