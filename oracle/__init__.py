@@ -24,6 +24,11 @@ Steps and the passages they follow (page titles as printed on the pages):
 * ``prefill_step`` -- the same section's prefill: T new positions per stream written
   into the cache, each of their queries attending causally over [0, its position],
   i.e. T decode queries whose windows end at their own rows.
+* ``rmsnorm_bf16`` / ``gemv_bf16`` / ``decode_layer`` -- one whole talker decode layer
+  with bf16 weights (the optimisations table's fused Thinker kernels: residual add +
+  RMSNorm, q/k norm + RoPE, SiLU-multiply, "each reproducing the reference rounding with
+  integer round-to-nearest-even"): activations rounded to bf16 by RNE where a bf16 model
+  would hold them (GEMV inputs), products summed exactly (float64), outputs in f32.
 * ``sample`` -- the in-graph sampler with a counter RNG ("qwentts.cpp" pages: the
   predictor frame unroll and the in-graph sampler; the optimisations table's
   "one-kernel counter RNG"): greedy, or temperature/top-k sampling driven by the
@@ -393,3 +398,65 @@ def sample(logits, top_k, temperature, seed, counter):
                 break
         out[b] = order[pick]
     return out
+
+
+# ---------------------------------------------------------------------------
+# A whole decode layer with bf16 weights
+# ---------------------------------------------------------------------------
+def bf16_round(x) -> np.ndarray:
+    """f32 values rounded to bf16 by round-to-nearest-even, returned as f32."""
+    return bf16_bits_to_f32(bf16_rne_array(np.asarray(x, np.float32)))
+
+
+def rmsnorm_bf16(h, gamma, eps):
+    """x = h * (mean(h^2) + eps)^-1/2 * gamma per row, in double, rounded once to bf16
+    (returned as f32 holding bf16 values).  h: [B][H] f32, gamma: [H] f32."""
+    h64 = np.asarray(h, np.float64)
+    r = 1.0 / np.sqrt((h64 * h64).mean(axis=1, keepdims=True) + float(eps))
+    y = (h64 * r * np.asarray(gamma, np.float64)).astype(np.float32)
+    return bf16_round(y)
+
+
+def gemv_bf16(x, w_bits):
+    """y[b][n] = sum_k x[b][k] * W[n][k] with x holding bf16 values (f32 arrays) and W
+    bf16 bit patterns [N][K]; the products and their sum are exact in float64, rounded
+    once to f32."""
+    W = bf16_bits_to_f32(w_bits).astype(np.float64)
+    return (np.asarray(x, np.float64) @ W.T).astype(np.float32)
+
+
+def silu_mul_bf16(gate, up):
+    """a = silu(gate) * up = gate / (1 + e^-gate) * up in double, rounded once to bf16."""
+    g = np.asarray(gate, np.float64)
+    a = g / (1.0 + np.exp(-g)) * np.asarray(up, np.float64)
+    return bf16_round(a.astype(np.float32))
+
+
+def decode_layer(h, wts, k_cache, v_cache, layout: KvLayout, cur_len, eps, base, scale):
+    """One talker decode layer for B streams, in place on the residual stream h ([B][H]
+    f32):  x = rmsnorm(h)_bf16;  qkv = x W_qkv^T;  attn = decode_step(q, k, v);
+    h = h + bf16(attn) W_o^T;  x2 = rmsnorm(h)_bf16;  gate, up = x2 W_gu^T (rows
+    [0, I) and [I, 2I));  h = h + silu_mul(gate, up)_bf16 W_down^T.  The residual adds
+    are single f32 additions.  wts: dict with gamma_attn, gamma_mlp (f32 [H]), gamma_q,
+    gamma_k (f32 [D]), w_qkv [(Hq + 2 Hkv) D][H], w_o [H][Hq D], w_gu [2I][H],
+    w_down [H][I] (bf16 bit patterns).  Mutates h and the caches; returns h."""
+    B, H = h.shape
+    D = layout.head_dim
+    Hkv = layout.n_kv_heads
+    Hq = wts["w_o"].shape[1] // D
+    x = rmsnorm_bf16(h, wts["gamma_attn"], eps)
+    qkv = gemv_bf16(x, wts["w_qkv"])
+    q = qkv[:, :Hq * D].reshape(B, Hq, D)
+    k = qkv[:, Hq * D:(Hq + Hkv) * D].reshape(B, Hkv, D)
+    v = qkv[:, (Hq + Hkv) * D:].reshape(B, Hkv, D)
+    attn = decode_step(q, k, v, wts["gamma_q"], wts["gamma_k"], eps, base, k_cache, v_cache,
+                       layout, cur_len, scale)
+    o = gemv_bf16(bf16_round(attn.reshape(B, Hq * D)), wts["w_o"])
+    h[...] = (h + o).astype(np.float32)
+    x2 = rmsnorm_bf16(h, wts["gamma_mlp"], eps)
+    gu = gemv_bf16(x2, wts["w_gu"])
+    I = gu.shape[1] // 2
+    a = silu_mul_bf16(gu[:, :I], gu[:, I:])
+    d = gemv_bf16(a, wts["w_down"])
+    h[...] = (h + d).astype(np.float32)
+    return h

@@ -612,3 +612,111 @@ def test_top_k_draws_follow_the_tempered_softmax():
     obs = np.array([counts[i] for i in top], np.float64)
     chi2 = float(((obs - n * p) ** 2 / (n * p)).sum())
     assert chi2 < 16.3  # 3 degrees of freedom, p = 0.001
+
+
+# ---------------------------------------------------------------------------
+# Whole decode layer with bf16 weights (NEXT-2)
+# ---------------------------------------------------------------------------
+def _bf16_bits(t):
+    return t.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def _torch_bf16(x64):
+    """float64 tensor -> f32 -> bf16 (round to nearest even) -> back to float64."""
+    return x64.float().to(torch.bfloat16).double()
+
+
+def test_rmsnorm_bf16_matches_torch_rms_norm():
+    rng = np.random.default_rng(40)
+    h = (rng.standard_normal((3, 64)) * 3).astype(np.float32)
+    g = rng.uniform(0.5, 1.5, 64).astype(np.float32)
+    got = oracle.rmsnorm_bf16(h, g, 1e-6)
+    ref = _torch_bf16(F.rms_norm(torch.from_numpy(h).double(), (64,), torch.from_numpy(g).double(), eps=1e-6))
+    assert np.array_equal(got, ref.float().numpy())
+
+
+def test_gemv_bf16_matches_torch_matmul():
+    rng = np.random.default_rng(41)
+    x = oracle.bf16_round(rng.standard_normal((4, 96)).astype(np.float32))
+    W = torch.from_numpy(rng.standard_normal((40, 96)).astype(np.float32))
+    got = oracle.gemv_bf16(x, _bf16_bits(W))
+    ref = (torch.from_numpy(x).double() @ W.to(torch.bfloat16).double().T).float().numpy()
+    np.testing.assert_array_max_ulp(got, ref, maxulp=1)
+
+
+def test_silu_mul_matches_torch_silu():
+    rng = np.random.default_rng(42)
+    g = (rng.standard_normal((2, 500)) * 4).astype(np.float32)
+    u = rng.standard_normal((2, 500)).astype(np.float32)
+    got = oracle.silu_mul_bf16(g, u)
+    ref = _torch_bf16(F.silu(torch.from_numpy(g).double()) * torch.from_numpy(u).double()).float().numpy()
+    # one bf16 step where float64 silu formulas round to f32 on either side of a tie
+    diff = np.abs(got.view(np.uint32).astype(np.int64) - ref.view(np.uint32).astype(np.int64)) >> 16
+    assert diff.max() <= 1 and (diff == 0).mean() > 0.99
+
+
+def _layer_case(rng, B=2, H=64, Hq=4, Hkv=2, D=16, I=96, cap=32):
+    t = lambda *s: torch.from_numpy((rng.standard_normal(s) * 0.2).astype(np.float32))
+    wts = dict(gamma_attn=rng.uniform(0.5, 1.5, H).astype(np.float32),
+               gamma_mlp=rng.uniform(0.5, 1.5, H).astype(np.float32),
+               gamma_q=rng.uniform(0.5, 1.5, D).astype(np.float32),
+               gamma_k=rng.uniform(0.5, 1.5, D).astype(np.float32),
+               w_qkv=_bf16_bits(t((Hq + 2 * Hkv) * D, H)), w_o=_bf16_bits(t(H, Hq * D)),
+               w_gu=_bf16_bits(t(2 * I, H)), w_down=_bf16_bits(t(H, I)))
+    h = (rng.standard_normal((B, H)) * 2).astype(np.float32)
+    kc = rng.standard_normal((B, Hkv, cap, D)).astype(np.float32)
+    vc = rng.standard_normal((B, Hkv, cap, D)).astype(np.float32)
+    return wts, h, kc, vc, oracle.KvLayout(B, Hkv, D, cap)
+
+
+def test_decode_layer_mlp_half_matches_torch():
+    """With W_o = 0 the attention half adds exactly nothing, so the layer is the MLP
+    half alone: torch rms_norm, matmuls in float64, silu, bf16 roundings by torch."""
+    rng = np.random.default_rng(43)
+    wts, h, kc, vc, lay = _layer_case(rng)
+    wts["w_o"][:] = 0
+    h0 = h.copy()
+    oracle.decode_layer(h, wts, kc, vc, lay, np.array([5, 30], np.int32), np.float32(1e-6), 1e6, 0.25)
+    T = torch.from_numpy
+    x2 = _torch_bf16(F.rms_norm(T(h0).double(), (64,), T(wts["gamma_mlp"]).double(), eps=1e-6))
+    Wgu = T(oracle.bf16_bits_to_f32(wts["w_gu"])).double()
+    gu = (x2 @ Wgu.T).float().double()
+    a = _torch_bf16(F.silu(gu[:, :96]) * gu[:, 96:])
+    d = (a @ T(oracle.bf16_bits_to_f32(wts["w_down"])).double().T).float()
+    ref = (T(h0) + d).numpy()
+    np.testing.assert_array_max_ulp(h, ref, maxulp=2)
+
+
+def test_decode_layer_attention_half_matches_torch():
+    """With the up rows of W_gu zero the MLP half adds exactly nothing: h gains
+    bf16(attention) W_o^T, where the attention is the pinned decode step of the
+    normed-and-projected row."""
+    rng = np.random.default_rng(44)
+    wts, h, kc, vc, lay = _layer_case(rng)
+    wts["w_gu"][96:] = 0
+    h0 = h.copy()
+    kc0, vc0 = kc.copy(), vc.copy()
+    cur = np.array([0, 17], np.int32)
+    oracle.decode_layer(h, wts, kc, vc, lay, cur, np.float32(1e-6), 1e6, 0.25)
+    T = torch.from_numpy
+    x = _torch_bf16(F.rms_norm(T(h0).double(), (64,), T(wts["gamma_attn"]).double(), eps=1e-6))
+    qkv = (x @ T(oracle.bf16_bits_to_f32(wts["w_qkv"])).double().T).float().numpy()
+    q, k, v = qkv[:, :64].reshape(2, 4, 16), qkv[:, 64:96].reshape(2, 2, 16), qkv[:, 96:].reshape(2, 2, 16)
+    attn = oracle.decode_step(q, k, v, wts["gamma_q"], wts["gamma_k"], np.float32(1e-6), 1e6,
+                              kc0, vc0, lay, cur, 0.25)
+    o = (_torch_bf16(T(attn.reshape(2, 64)).double()) @ T(oracle.bf16_bits_to_f32(wts["w_o"])).double().T).float()
+    np.testing.assert_array_max_ulp(h, (T(h0) + o).numpy(), maxulp=2)
+    assert np.array_equal(kc, kc0) and np.array_equal(vc, vc0)  # the step wrote the same rows
+
+
+def test_decode_layer_batched_equals_per_stream():
+    rng = np.random.default_rng(45)
+    wts, h, kc, vc, lay = _layer_case(rng, B=3)
+    cur = np.array([0, 9, 31], np.int32)
+    hb, kb, vb = h.copy(), kc.copy(), vc.copy()
+    oracle.decode_layer(hb, wts, kb, vb, lay, cur, np.float32(1e-6), 1e6, 0.25)
+    for b in range(3):
+        h1, k1, v1 = h[b:b + 1].copy(), kc[b:b + 1].copy(), vc[b:b + 1].copy()
+        oracle.decode_layer(h1, wts, k1, v1, oracle.KvLayout(1, 2, 16, 32), cur[b:b + 1],
+                            np.float32(1e-6), 1e6, 0.25)
+        assert np.array_equal(h1[0], hb[b]) and np.array_equal(k1[0], kb[b])
