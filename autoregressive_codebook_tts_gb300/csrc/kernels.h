@@ -127,6 +127,20 @@ struct SampleParams {
   int64_t out_stride;   // int32 elements between consecutive streams' ids
 };
 
+// bf16-weight GEMV of the decode layer (see layer.cu): y[b][n] = sum_k x[b][k] W[n][k].
+constexpr int kGemvMaxB = 8;      // streams per launch
+constexpr int kGemvMaxK = 8192;   // row length (a multiple of 256)
+struct GemvParams {
+  const void* x;        // f32 or bf16 [B][K], rows x_stride elements apart
+  int64_t x_stride;
+  const void* w;        // bf16 [rows][K]
+  int n_out;            // output rows (SiLU-multiply: gate/up pairs)
+  int K, B;
+  int inter;            // SiLU-multiply: offset of the up rows
+  void* y;              // f32 [B][..] (store, residual) or bf16 [B][inter] (SiLU-multiply)
+  int64_t y_stride;
+};
+
 // Launch helpers (return a cudaError_t from the launch).
 cudaError_t launch_frame_embed(const EmbedParams& p, cudaStream_t s);
 cudaError_t launch_rope_table(float* cs, int max_pos, int head_dim, double base, cudaStream_t s);
@@ -136,6 +150,10 @@ cudaError_t launch_zero(void* ptr, size_t bytes, cudaStream_t s);
 cudaError_t launch_prefill_rows(const PrefillRowsParams& p, cudaStream_t s);
 cudaError_t launch_sample(const SampleParams& p, cudaStream_t s);
 cudaError_t launch_counter_advance(uint64_t* counter, uint64_t by, cudaStream_t s);
+cudaError_t launch_rmsnorm_bf16(const float* h, const float* gamma, float eps, int B, int H, void* x,
+                                cudaStream_t s);
+// epilogue 0: store f32, 1: add into f32 (residual), 2: SiLU-multiply to bf16
+cudaError_t launch_gemv_bf16(const GemvParams& p, int x_f32, int epilogue, cudaStream_t s);
 
 // Tile geometry of the attention kernel for a (dtype, head_dim) pair.
 struct AttnGeometry {

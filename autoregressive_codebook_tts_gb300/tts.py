@@ -42,6 +42,8 @@ EXPORTED = [
     "tts_prefill_step",
     "tts_sample",
     "tts_counter_advance",
+    "tts_decode_layer_scratch_size",
+    "tts_decode_layer",
 ]
 
 
@@ -58,6 +60,13 @@ class TtsKvDesc(ctypes.Structure):
                 ("page_size", ctypes.c_int32), ("n_pages", ctypes.c_int32),
                 ("bt_stride", ctypes.c_int32), ("flags", ctypes.c_uint32),
                 ("block_table", ctypes.c_void_p)]
+
+
+class TtsLayerWeights(ctypes.Structure):
+    _fields_ = [("w_qkv", ctypes.c_void_p), ("w_o", ctypes.c_void_p), ("w_gu", ctypes.c_void_p),
+                ("w_down", ctypes.c_void_p), ("gamma_attn", ctypes.c_void_p),
+                ("gamma_mlp", ctypes.c_void_p), ("gamma_q", ctypes.c_void_p),
+                ("gamma_k", ctypes.c_void_p), ("hidden", ctypes.c_int32), ("inter", ctypes.c_int32)]
 
 
 _P, _I32, _I64, _F, _D, _SZ = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float,
@@ -83,6 +92,9 @@ _sigs = {
     "tts_prefill_workspace_size": ([ctypes.POINTER(TtsKvDesc), _I32, _I32], _SZ),
     "tts_sample": ([_P, _I64, _I32, _I32, _I32, _F, ctypes.c_uint64, _P, _P, _I64, _P], _I32),
     "tts_counter_advance": ([_P, ctypes.c_uint64, _P], _I32),
+    "tts_decode_layer_scratch_size": ([ctypes.POINTER(TtsKvDesc), _I32, _I32, _I32], _SZ),
+    "tts_decode_layer": ([_P, ctypes.POINTER(TtsLayerWeights), _F, _P, _I32, _P, _P,
+                          ctypes.POINTER(TtsKvDesc), _P, _F, _P, _SZ, _I32, _P, _P], _I32),
     "tts_prefill_step": ([_P, _P, _P, _I64, _P, _P, _F, _P, _I32, _P, _P,
                           ctypes.POINTER(TtsKvDesc), _P, _I32, _F, _P, _P, _SZ, _I32, _P, _P], _I32),
 }
@@ -286,6 +298,42 @@ def tts_sample(logits, top_k, temperature, seed, counter, out_ids, stream=None):
 def tts_counter_advance(counter, by=1, stream=None):
     _check(_lib.tts_counter_advance(_ptr(counter), ctypes.c_uint64(int(by)), _stream(stream)),
            "tts_counter_advance")
+
+
+def layer_weights(w_qkv, w_o, w_gu, w_down, gamma_attn, gamma_mlp, gamma_q, gamma_k) -> TtsLayerWeights:
+    """Descriptor of one layer's weights: bf16 matrices, f32 norm weights (device tensors;
+    the caller keeps them alive)."""
+    for m in (w_qkv, w_o, w_gu, w_down):
+        if m.dtype != torch.bfloat16 or not m.is_contiguous():
+            raise ValueError("layer weight matrices must be contiguous bfloat16")
+    t = TtsLayerWeights()
+    t.w_qkv, t.w_o, t.w_gu, t.w_down = (m.data_ptr() for m in (w_qkv, w_o, w_gu, w_down))
+    t.gamma_attn, t.gamma_mlp, t.gamma_q, t.gamma_k = (
+        g.data_ptr() for g in (gamma_attn, gamma_mlp, gamma_q, gamma_k))
+    t.hidden = w_qkv.shape[1]
+    t.inter = w_down.shape[1]
+    return t
+
+
+def tts_decode_layer_scratch_size(desc: TtsKvDesc, hidden, inter, n_splits=0) -> int:
+    return int(_lib.tts_decode_layer_scratch_size(ctypes.byref(desc), hidden, inter, n_splits))
+
+
+def layer_scratch(desc: TtsKvDesc, hidden, inter, n_splits=0, device="cuda", stream=None):
+    """Allocate (through torch) and clear the scratch of a decode layer."""
+    n = max(tts_decode_layer_scratch_size(desc, hidden, inter, n_splits), 256)
+    ws = torch.empty(n, dtype=torch.uint8, device=device)
+    tts_workspace_init(ws, stream)
+    return ws
+
+
+def tts_decode_layer(h, weights: TtsLayerWeights, eps, cs, max_pos, k_cache, v_cache,
+                     desc: TtsKvDesc, cur_len, scale, scratch, n_splits=0, err_flag=None,
+                     stream=None):
+    _check(_lib.tts_decode_layer(_ptr(h), ctypes.byref(weights), float(eps), _ptr(cs), max_pos,
+                                 _ptr(k_cache), _ptr(v_cache), ctypes.byref(desc), _ptr(cur_len),
+                                 float(scale), _ptr(scratch), scratch.numel() * scratch.element_size(),
+                                 n_splits, _ptr(err_flag), _stream(stream)), "tts_decode_layer")
 
 
 def default_scale(head_dim: int) -> float:

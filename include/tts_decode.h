@@ -325,6 +325,48 @@ tts_status tts_sample(const float* logits, int64_t logits_stride, int32_t B, int
 /* *counter += by, as one kernel on `stream` (graph-capturable). */
 tts_status tts_counter_advance(uint64_t* counter, uint64_t by, void* stream);
 
+/* ---------------------------------------------------------------------------
+ * One whole talker decode layer with bf16 weights, for B <= 8 streams ([engine] core
+ * table: fused residual add + RMSNorm, q/k norm + RoPE, SiLU-multiply, reproducing the
+ * reference rounding with integer round-to-nearest-even; [pipeline] KV-cache section
+ * for the step).  In place on the residual stream h [B][hidden] (f32):
+ *   x = bf16(rmsnorm(h) * gamma_attn)          (statistics in double, RNE to bf16)
+ *   qkv = x W_qkv^T                             (f32; q, k, v as in tts_decode_step)
+ *   attn = tts_decode_step(q, k, v, ...)        (norm + RoPE, new row, attention)
+ *   h = h + bf16(attn) W_o^T
+ *   x = bf16(rmsnorm(h) * gamma_mlp)
+ *   a = bf16(silu(x W_gate^T) * x W_up^T)       (silu in double)
+ *   h = h + a W_down^T
+ * Products accumulate in f32; every residual add is one f32 addition.  Seven launches
+ * on `stream`.  Weights are bf16, row-major, rows of `hidden` (or `inter`) elements:
+ *   w_qkv [(Hq + 2 Hkv) D][hidden], w_o [hidden][Hq D], w_gu [2 inter][hidden] (the
+ *   gate rows, then the up rows), w_down [hidden][inter].
+ * hidden, inter and Hq*D must be multiples of 256 and at most 8192.
+ *   scratch: device memory of tts_decode_layer_scratch_size() bytes, 256-byte aligned,
+ *        zeroed once before its first use (it holds the attention workspace).
+ * ------------------------------------------------------------------------- */
+typedef struct {
+  const void* w_qkv;
+  const void* w_o;
+  const void* w_gu;
+  const void* w_down;
+  const float* gamma_attn; /* [hidden] */
+  const float* gamma_mlp;  /* [hidden] */
+  const float* gamma_q;    /* [head_dim] */
+  const float* gamma_k;    /* [head_dim] */
+  int32_t hidden;
+  int32_t inter;
+} tts_layer_weights;
+
+size_t tts_decode_layer_scratch_size(const tts_kv_desc* desc, int32_t hidden, int32_t inter,
+                                     int32_t n_splits);
+
+tts_status tts_decode_layer(float* h, const tts_layer_weights* weights, float eps,
+                            const float* rope_cs, int32_t rope_max_pos, void* k_cache,
+                            void* v_cache, const tts_kv_desc* desc, const int32_t* cur_len,
+                            float scale, void* scratch, size_t scratch_bytes, int32_t n_splits,
+                            int32_t* err_flag, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -1,0 +1,91 @@
+"""A whole talker decode layer with bf16 weights (tts_decode_layer) against the
+oracle's decode_layer: the residual stream after the layer within 1e-3 per stream row
+(max |diff| / max |ref|), the cache rows as for the decode step.  The GPU sums the
+products in f32 where the oracle sums them exactly, so a bf16 rounding of an
+intermediate (the norm output, the attention output, the SiLU product) can land one
+bf16 step apart; such a step moves the layer's output by about 2^-8 of one product
+term, far inside the bound."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from autoregressive_codebook_tts_gb300 import workloads as W
+from gpu_helpers import Layer, bits, cache_np, rope_table, scale_of
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def tts(cuda_dev):
+    from autoregressive_codebook_tts_gb300 import build
+    build.build()
+    from autoregressive_codebook_tts_gb300 import tts as mod
+    return mod
+
+
+def _weights(H, I, Hq, Hkv, D, seed):
+    g = torch.Generator().manual_seed(seed)
+    m = lambda r, c: (torch.randn(r, c, generator=g) * 0.02).to(torch.bfloat16)
+    return dict(w_qkv=m((Hq + 2 * Hkv) * D, H), w_o=m(H, Hq * D), w_gu=m(2 * I, H), w_down=m(H, I),
+                gamma_attn=torch.rand(H, generator=g) + 0.5, gamma_mlp=torch.rand(H, generator=g) + 0.5,
+                gamma_q=torch.rand(D, generator=g) + 0.5, gamma_k=torch.rand(D, generator=g) + 0.5)
+
+
+def _bits16(t):
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+@pytest.mark.parametrize("B,cur", [(1, [4095]), (1, [100]), (4, [7, 1000, 2047, 3000]), (8, [300] * 8)])
+def test_decode_layer_matches_oracle(tts, B, cur):
+    w = W.workload("talker", B=B, layers=1)
+    H, I, Hq, Hkv, D = w.hidden, 3 * w.hidden, w.n_q_heads, w.n_kv_heads, w.head_dim
+    L = Layer(w, seed=80, cur_len=cur, poison=True)
+    wt = _weights(H, I, Hq, Hkv, D, 81)
+    d = {k: v.cuda() for k, v in wt.items()}
+    lw = tts.layer_weights(d["w_qkv"], d["w_o"], d["w_gu"], d["w_down"], d["gamma_attn"],
+                           d["gamma_mlp"], d["gamma_q"], d["gamma_k"])
+    g = torch.Generator().manual_seed(82)
+    h0 = torch.randn(B, H, generator=g)
+    h = h0.cuda()
+    cs = rope_table(tts, w.capacity, D, w.rope_base)
+    desc = L.desc(tts)
+    scratch = tts.layer_scratch(desc, H, I, 0)
+    ef = torch.zeros(1, dtype=torch.int32, device="cuda")
+    tts.tts_decode_layer(h, lw, w.eps, cs, w.capacity, L.d_K, L.d_V, desc, L.d_cur, scale_of(w),
+                         scratch, 0, ef)
+    torch.cuda.synchronize()
+    assert ef.item() == 0
+    hk, hv = cache_np(L.K), cache_np(L.V)
+    ref = h0.numpy().copy()
+    ow = {k: (_bits16(v) if v.dtype == torch.bfloat16 else v.numpy()) for k, v in wt.items()}
+    oracle.decode_layer(ref, ow, hk, hv, L.layout(), L.cur.numpy(), np.float32(w.eps), w.rope_base,
+                        scale_of(w))
+    got = h.cpu().numpy()
+    err = (np.abs(got - ref).max(axis=1) / np.abs(ref).max(axis=1)).max()
+    assert err <= 1e-3, err
+    # the cache: only the new rows changed; V rows exact, K rows within rounding
+    gk, gv = cache_np(L.d_K), cache_np(L.d_V)
+    mask = np.zeros(hk.shape, bool)
+    for b in range(B):
+        mask[b, :, cur[b]] = True
+    assert not ((bits(gk) != bits(hk)) & ~mask).any() and not ((bits(gv) != bits(hv)) & ~mask).any()
+    np.testing.assert_allclose(gk[mask], hk[mask], rtol=1e-4, atol=1e-4)
+    np.testing.assert_allclose(gv[mask], hv[mask], rtol=1e-4, atol=1e-4)
+
+
+def test_decode_layer_rejects_more_than_eight_streams(tts):
+    w = W.workload("talker", B=9, layers=1)
+    desc = tts.kv_desc(9, 16, 8, 128, 4096)
+    assert tts.tts_decode_layer_scratch_size(desc, 2048, 6144) > 0
+    wt = {k: v.cuda() for k, v in _weights(2048, 6144, 16, 8, 128, 83).items()}
+    lw = tts.layer_weights(wt["w_qkv"], wt["w_o"], wt["w_gu"], wt["w_down"], wt["gamma_attn"],
+                           wt["gamma_mlp"], wt["gamma_q"], wt["gamma_k"])
+    h = torch.zeros(9, 2048, device="cuda")
+    K = torch.zeros(9, 8, 4096, 128, device="cuda")
+    cur = torch.zeros(9, dtype=torch.int32, device="cuda")
+    cs = rope_table(tts, 4096, 128, w.rope_base)
+    with pytest.raises(tts.TtsError) as e:
+        tts.tts_decode_layer(h, lw, 1e-6, cs, 4096, K, K, desc, cur, 0.1,
+                             tts.layer_scratch(desc, 2048, 6144), 0)
+    assert e.value.status == 2
