@@ -460,19 +460,19 @@ tts_status tts_counter_advance(uint64_t* counter, uint64_t by, void* stream) {
 
 namespace {
 
-// Scratch of a decode layer, 256-byte regions: x (bf16 [B][hidden], the norm output),
-// a (bf16 [B][inter], the SiLU-multiply output), the qkv rows (f32), the attention
-// output (f32 [B][Hq D]), then the attention workspace.
+// Scratch of a decode layer, 256-byte regions: a (bf16 [B][inter], the SiLU-multiply
+// output), the qkv rows (f32), the attention output (f32 [B][Hq D]), then the
+// attention workspace.
 struct LayerScratch {
-  size_t x_off, a_off, qkv_off, attn_off, ws_off, total;
+  size_t a_off, qkv_off, attn_off, ws_off, total;
 };
 LayerScratch layer_scratch(const tts_kv_desc* d, int hidden, int inter, int n_splits) {
   LayerScratch L;
   const size_t B = static_cast<size_t>(d->B);
   const size_t width = static_cast<size_t>(d->n_q_heads + 2 * d->n_kv_heads) * d->head_dim;
-  L.x_off = 0;
-  L.a_off = round256(B * hidden * 2);
-  L.qkv_off = L.a_off + round256(B * inter * 2);
+  (void)hidden;
+  L.a_off = 0;
+  L.qkv_off = round256(B * inter * 2);
   L.attn_off = L.qkv_off + round256(B * width * 4);
   L.ws_off = L.attn_off + round256(B * d->n_q_heads * d->head_dim * 4);
   L.total = L.ws_off + round256(tts_decode_attn_workspace_size(d, n_splits));
@@ -513,33 +513,32 @@ tts_status tts_decode_layer(float* h, const tts_layer_weights* w, float eps, con
   const LayerScratch L = layer_scratch(d, H, I, n_splits);
   if (scratch_bytes < L.total) return TTS_ERR_WORKSPACE;
   unsigned char* sc = static_cast<unsigned char*>(scratch);
-  void* x = sc + L.x_off;
   void* a = sc + L.a_off;
   float* qkv = reinterpret_cast<float*>(sc + L.qkv_off);
   float* attn = reinterpret_cast<float*>(sc + L.attn_off);
   cudaStream_t s = as_stream(stream);
-  cudaError_t e = launch_rmsnorm_bf16(h, w->gamma_attn, eps, B, H, x, s);
-  if (e != cudaSuccess) return from_cuda(e);
+  // qkv = bf16(rmsnorm(h)) W_qkv^T
   GemvParams g = {};
-  g.x = x; g.x_stride = H; g.w = w->w_qkv; g.n_out = width; g.K = H; g.B = B;
-  g.y = qkv; g.y_stride = width;
-  if ((e = launch_gemv_bf16(g, 0, 0, s)) != cudaSuccess) return from_cuda(e);
+  g.x = h; g.x_stride = H; g.gamma = w->gamma_attn; g.eps = eps;
+  g.w = w->w_qkv; g.n_out = width; g.K = H; g.B = B; g.y = qkv; g.y_stride = width;
+  cudaError_t e = launch_gemv_bf16(g, 2, 0, s);
+  if (e != cudaSuccess) return from_cuda(e);
   st = tts_decode_step(qkv, qkv + qd, qkv + qd + kd, width, w->gamma_q, w->gamma_k, eps, rope_cs,
                        rope_max_pos, k_cache, v_cache, d, cur_len, scale, attn, sc + L.ws_off,
                        L.total - L.ws_off, n_splits, err_flag, stream);
   if (st != TTS_OK) return st;
+  // h += bf16(attn) W_o^T
   g = {};
-  g.x = attn; g.x_stride = qd; g.w = w->w_o; g.n_out = H; g.K = qd; g.B = B;
-  g.y = h; g.y_stride = H;
+  g.x = attn; g.x_stride = qd; g.w = w->w_o; g.n_out = H; g.K = qd; g.B = B; g.y = h; g.y_stride = H;
   if ((e = launch_gemv_bf16(g, 1, 1, s)) != cudaSuccess) return from_cuda(e);
-  if ((e = launch_rmsnorm_bf16(h, w->gamma_mlp, eps, B, H, x, s)) != cudaSuccess) return from_cuda(e);
+  // a = bf16(silu(x W_gate^T) * x W_up^T), x = bf16(rmsnorm(h))
   g = {};
-  g.x = x; g.x_stride = H; g.w = w->w_gu; g.n_out = I; g.K = H; g.B = B; g.inter = I;
-  g.y = a; g.y_stride = I;
-  if ((e = launch_gemv_bf16(g, 0, 2, s)) != cudaSuccess) return from_cuda(e);
+  g.x = h; g.x_stride = H; g.gamma = w->gamma_mlp; g.eps = eps;
+  g.w = w->w_gu; g.n_out = I; g.K = H; g.B = B; g.inter = I; g.y = a; g.y_stride = I;
+  if ((e = launch_gemv_bf16(g, 2, 2, s)) != cudaSuccess) return from_cuda(e);
+  // h += a W_down^T
   g = {};
-  g.x = a; g.x_stride = I; g.w = w->w_down; g.n_out = H; g.K = I; g.B = B;
-  g.y = h; g.y_stride = H;
+  g.x = a; g.x_stride = I; g.w = w->w_down; g.n_out = H; g.K = I; g.B = B; g.y = h; g.y_stride = H;
   return from_cuda(launch_gemv_bf16(g, 0, 1, s));
 }
 

@@ -133,6 +133,8 @@ constexpr int kGemvMaxK = 8192;   // row length (a multiple of 256)
 struct GemvParams {
   const void* x;        // f32 or bf16 [B][K], rows x_stride elements apart
   int64_t x_stride;
+  const float* gamma;   // RMS-norm input mode: gamma [K], and eps
+  float eps;
   const void* w;        // bf16 [rows][K]
   int n_out;            // output rows (SiLU-multiply: gate/up pairs)
   int K, B;
@@ -150,10 +152,9 @@ cudaError_t launch_zero(void* ptr, size_t bytes, cudaStream_t s);
 cudaError_t launch_prefill_rows(const PrefillRowsParams& p, cudaStream_t s);
 cudaError_t launch_sample(const SampleParams& p, cudaStream_t s);
 cudaError_t launch_counter_advance(uint64_t* counter, uint64_t by, cudaStream_t s);
-cudaError_t launch_rmsnorm_bf16(const float* h, const float* gamma, float eps, int B, int H, void* x,
-                                cudaStream_t s);
-// epilogue 0: store f32, 1: add into f32 (residual), 2: SiLU-multiply to bf16
-cudaError_t launch_gemv_bf16(const GemvParams& p, int x_f32, int epilogue, cudaStream_t s);
+// x_mode 0: bf16 input, 1: f32 input rounded to bf16, 2: bf16 of the RMS norm of an
+// f32 input; epilogue 0: store f32, 1: add into f32 (residual), 2: SiLU-multiply to bf16
+cudaError_t launch_gemv_bf16(const GemvParams& p, int x_mode, int epilogue, cudaStream_t s);
 
 // Tile geometry of the attention kernel for a (dtype, head_dim) pair.
 struct AttnGeometry {

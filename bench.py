@@ -42,7 +42,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--workload", default="talker",
-                    choices=["talker", "batched", "paged", "prefill", "predictor"])
+                    choices=["talker", "batched", "paged", "prefill", "predictor", "layer"])
+    ap.add_argument("--layer-streams", type=int, default=1, help="layer: streams (1..8)")
     ap.add_argument("--frames-per-replay", type=int, default=4,
                     help="predictor: frames unrolled into one graph replay")
     ap.add_argument("--layers", type=int, default=0,
@@ -740,6 +741,106 @@ def run_reference_predictor(args, world):
     }
 
 
+def run_layer(args, rank, world):
+    """Whole talker frames: the frame-input composition, then 28 tts_decode_layer calls
+    (norms, bf16-weight GEMVs, the fused decode step, residuals) on random-init bf16
+    weights, captured into one CUDA graph."""
+    import torch
+    from autoregressive_codebook_tts_gb300 import build as b
+    b.build()
+    from autoregressive_codebook_tts_gb300 import tts
+    from autoregressive_codebook_tts_gb300 import workloads as W
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    B = args.layer_streams
+    w = W.workload("talker", B=B)
+    L, H, Hq, Hkv, D = w.layers, w.hidden, w.n_q_heads, w.n_kv_heads, w.head_dim
+    I = 3 * H
+    g = torch.Generator(device=dev)
+    g.manual_seed(rank)
+    mat = lambda r, c: (torch.randn(r, c, generator=g, device=dev) * 0.02).to(torch.bfloat16)
+    layers_w = []
+    keep = []
+    for _ in range(L):
+        t = dict(w_qkv=mat((Hq + 2 * Hkv) * D, H), w_o=mat(H, Hq * D), w_gu=mat(2 * I, H), w_down=mat(H, I),
+                 ga=torch.rand(H, generator=g, device=dev) + 0.5, gm=torch.rand(H, generator=g, device=dev) + 0.5,
+                 gq=torch.rand(D, generator=g, device=dev) + 0.5, gk=torch.rand(D, generator=g, device=dev) + 0.5)
+        keep.append(t)
+        layers_w.append(tts.layer_weights(t["w_qkv"], t["w_o"], t["w_gu"], t["w_down"], t["ga"], t["gm"],
+                                          t["gq"], t["gk"]))
+    caches = []
+    for _ in range(L):
+        K = torch.empty(B, Hkv, w.capacity, D, device=dev)
+        V = torch.empty_like(K)
+        K.normal_(generator=g)
+        V.normal_(generator=g)
+        caches.append((K, V))
+    cs = torch.empty(w.capacity, D // 2, 2, device=dev)
+    tts.tts_rope_table(cs, w.capacity, D, w.rope_base)
+    desc = tts.kv_desc(B, Hq, Hkv, D, w.capacity, "f32", window_quantum=w.window_quantum,
+                       flags=tts.TTS_KV_PREFETCH_BEFORE_WAIT)
+    scratch = tts.layer_scratch(desc, H, I, args.n_splits, device=dev)
+    tabs = [torch.randn(w.vocab, H, generator=g, device=dev) * w.table_std for _ in range(w.n_tables)]
+    tabs_struct = tts.tables(tabs)
+    ids = torch.randint(0, w.vocab, (B, w.n_tables), generator=g, device=dev, dtype=torch.int32)
+    overlay = torch.randn(B, H, generator=g, device=dev) * w.table_std
+    hbuf = torch.empty(B, H, device=dev)
+    cur = torch.full((B,), args.cur_len, dtype=torch.int32, device=dev)
+    ef = torch.zeros(1, dtype=torch.int32, device=dev)
+    scale = 1.0 / math.sqrt(D)
+
+    def frame():
+        tts.tts_frame_embed(tabs_struct, ids, overlay, hbuf, ef)
+        for l in range(L):
+            tts.tts_decode_layer(hbuf, layers_w[l], w.eps, cs, w.capacity, caches[l][0], caches[l][1], desc,
+                                 cur, scale, scratch, args.n_splits, ef)
+
+    gr = capture(frame, torch)
+    for _ in range(args.warmup):
+        gr.replay()
+    torch.cuda.synchronize()
+    if ef.item() != 0:
+        raise RuntimeError(f"device error flag {ef.item()}")
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t = timed_replays(gr, args.steps, torch)
+    clk = clocks.stop()
+    (t,) = max_over_ranks([t], world, dev)
+    weights = 2 * ((Hq + 2 * Hkv) * D * H + H * Hq * D + 2 * I * H + H * I)
+    per_layer, kv_layer, embed = step_bytes(w, [args.cur_len] * B)
+    acts = B * (2 * H * 4 * 4 + H * 2 * 2 + I * 2 * 2)   # h reads/writes, x, a (approximate, small)
+    frame_bytes = embed + L * (weights + per_layer + acts)
+    peak, peak_kind = hbm_peak()
+    value = whole_job_gbs(world, frame_bytes, args.steps, t)
+    return {
+        "metric": "talker frame GB/s (weights + KV, % of HBM peak); frame steps/sec",
+        "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(t / args.steps * 1e3, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16-weights/f32",
+        "data": "synthetic (seeded, device-generated; random-init bf16 weights)",
+        "config": {"workload": f"talker layers: B={B} streams, {L} layers, hidden {H}, intermediate {I}, "
+                               f"16/8 heads, head_dim {D}, f32 KV, capacity {w.capacity}, cur_len {args.cur_len}",
+                   "frame_step": f"graph replay of tts_frame_embed + {L} x tts_decode_layer",
+                   "weights_per_layer_bytes": weights,
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "frame_steps_per_s": round(world * B * args.steps / t, 1),
+        "pct_of_hbm_peak": round(100 * value / world / peak, 2),
+        "roofline": {"bound": "hbm", "achieved": round(value / world, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(value / world / peak, 4), "traffic": None,
+                     "kernel": "whole frame (GEMVs and the decode step)",
+                     "peak_source": "measured HBM copy bandwidth" if peak_kind == "measured"
+                     else "fallback HBM copy bandwidth", "bytes_per_frame": frame_bytes},
+        "gpu_launches": args.steps * (1 + 7 * L),
+        "clocks": clk,
+    }
+
+
 def run_reference_prefill(args, world):
     """The oracle's prefill of one layer (talker shapes) as the reference arm's step."""
     import numpy as np
@@ -873,6 +974,8 @@ def main():
         res = run_prefill(args, rank, world)
     elif args.workload == "predictor":
         res = run_predictor(args, rank, world)
+    elif args.workload == "layer":
+        res = run_layer(args, rank, world)
     else:
         res = run_native(args, rank, world)
     if rank == 0:
