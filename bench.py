@@ -755,7 +755,7 @@ def run_layer(args, rank, world):
     dev = torch.device(f"cuda:{local}")
     torch.cuda.set_device(dev)
     B = args.layer_streams
-    w = W.workload("talker", B=B)
+    w = W.workload("talker", B=B, **({"layers": args.layers} if args.layers > 0 else {}))
     L, H, Hq, Hkv, D = w.layers, w.hidden, w.n_q_heads, w.n_kv_heads, w.head_dim
     I = 3 * H
     g = torch.Generator(device=dev)
