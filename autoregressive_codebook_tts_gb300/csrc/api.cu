@@ -520,7 +520,7 @@ tts_status tts_decode_layer(float* h, const tts_layer_weights* w, float eps, con
   // qkv = bf16(rmsnorm(h)) W_qkv^T
   GemvParams g = {};
   g.x = h; g.x_stride = H; g.gamma = w->gamma_attn; g.eps = eps;
-  g.w = w->w_qkv; g.n_out = width; g.K = H; g.B = B; g.y = qkv; g.y_stride = width;
+  g.w = w->w_qkv; g.n_out = width; g.K = H; g.B = B; g.y = qkv; g.y_stride = width; g.err = err_flag;
   cudaError_t e = launch_gemv_bf16(g, 2, 0, s);
   if (e != cudaSuccess) return from_cuda(e);
   st = tts_decode_step(qkv, qkv + qd, qkv + qd + kd, width, w->gamma_q, w->gamma_k, eps, rope_cs,
@@ -530,15 +530,17 @@ tts_status tts_decode_layer(float* h, const tts_layer_weights* w, float eps, con
   // h += bf16(attn) W_o^T
   g = {};
   g.x = attn; g.x_stride = qd; g.w = w->w_o; g.n_out = H; g.K = qd; g.B = B; g.y = h; g.y_stride = H;
+  g.err = err_flag;
   if ((e = launch_gemv_bf16(g, 1, 1, s)) != cudaSuccess) return from_cuda(e);
   // a = bf16(silu(x W_gate^T) * x W_up^T), x = bf16(rmsnorm(h))
   g = {};
   g.x = h; g.x_stride = H; g.gamma = w->gamma_mlp; g.eps = eps;
-  g.w = w->w_gu; g.n_out = I; g.K = H; g.B = B; g.inter = I; g.y = a; g.y_stride = I;
+  g.w = w->w_gu; g.n_out = I; g.K = H; g.B = B; g.inter = I; g.y = a; g.y_stride = I; g.err = err_flag;
   if ((e = launch_gemv_bf16(g, 2, 2, s)) != cudaSuccess) return from_cuda(e);
   // h += a W_down^T
   g = {};
   g.x = a; g.x_stride = I; g.w = w->w_down; g.n_out = H; g.K = I; g.B = B; g.y = h; g.y_stride = H;
+  g.err = err_flag;
   return from_cuda(launch_gemv_bf16(g, 0, 1, s));
 }
 

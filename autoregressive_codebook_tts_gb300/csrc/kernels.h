@@ -141,6 +141,9 @@ struct GemvParams {
   int inter;            // SiLU-multiply: offset of the up rows
   void* y;              // f32 [B][..] (store, residual) or bf16 [B][inter] (SiLU-multiply)
   int64_t y_stride;
+  int32_t* err;         // TTS_EFLAG_TIMEOUT when a bounded wait runs out (may be null)
+  int seg, stages;      // set by the launcher: row segment length, ring depth,
+  uint32_t x_off;       // and the shared-memory offset of the staged activations
 };
 
 // Launch helpers (return a cudaError_t from the launch).
@@ -153,7 +156,8 @@ cudaError_t launch_prefill_rows(const PrefillRowsParams& p, cudaStream_t s);
 cudaError_t launch_sample(const SampleParams& p, cudaStream_t s);
 cudaError_t launch_counter_advance(uint64_t* counter, uint64_t by, cudaStream_t s);
 // x_mode 0: bf16 input, 1: f32 input rounded to bf16, 2: bf16 of the RMS norm of an
-// f32 input; epilogue 0: store f32, 1: add into f32 (residual), 2: SiLU-multiply to bf16
+// f32 input; epilogue 0: store f32, 1: add into f32 (residual), 2: SiLU-multiply to bf16.
+// The pairs built are (2, 0), (1, 1), (2, 2) and (0, 1); B is 1..8.
 cudaError_t launch_gemv_bf16(const GemvParams& p, int x_mode, int epilogue, cudaStream_t s);
 
 // Tile geometry of the attention kernel for a (dtype, head_dim) pair.

@@ -11,13 +11,13 @@
 //   h += a W_down^T                           gemv_bf16_kernel<X_BF16, EPI_RESIDUAL>
 //
 // At the batch sizes of a decode step (B <= 8 here) every product is a GEMV bound by
-// streaming the weights from HBM: one warp per output row (a gate/up pair for the MLP),
-// 16-byte coalesced weight loads four chunks deep, started before the dependency wait,
-// the activations staged once per CTA in shared memory as bf16 (the RMS norm computed
-// there, so it needs no launch of its own), f32 accumulation, a warp reduction and a
-// fused epilogue.  The norm is computed in f32 by every CTA (double arithmetic there
-// cost more than the weight stream); the SiLU, one value per output, in double.  A bf16
-// rounding of an intermediate can therefore land one step from the exact value's.
+// streaming the weights from HBM.  The weights are streamed into a shared-memory ring by
+// bulk copies that start before the dependency wait (they are constants), the activations
+// are staged once per CTA as bf16 (the RMS norm computed there, so it needs no launch of
+// its own), each warp accumulates one row in f32 and a fused epilogue stores, adds into
+// the residual stream or applies the SiLU-multiply.  The norm is computed in f32 by every
+// CTA, and so is the SiLU.  A bf16 rounding of an intermediate can therefore land one
+// step from the exact value's.
 #include <cstdint>
 
 #include <cuda_bf16.h>
@@ -37,217 +37,394 @@ __device__ __forceinline__ uint16_t bf16_bits_rne(float x) {
 enum Epilogue { EPI_STORE = 0, EPI_RESIDUAL = 1, EPI_SILU_MUL = 2 };
 enum XMode { X_BF16 = 0, X_F32 = 1, X_RMSNORM = 2 };
 
-constexpr int kGemvWarps = 8;
-#ifndef TTS_GEMV_DEPTH
-#define TTS_GEMV_DEPTH 8
+constexpr int kRowWarps = 8;                         // consumer warps: one weight row each
+constexpr int kGemvThreads = (kRowWarps + 1) * 32;   // + one producer warp
+constexpr int kSegMax = 2048;                        // elements of a row segment (4 KB)
+constexpr int kGemvRingStages = 4;                   // deepest reused ring
+constexpr int kGemvMaxStages = 8;                    // stages of a whole-fit ring
+#ifndef TTS_GEMV_WHOLE_FIT
+#define TTS_GEMV_WHOLE_FIT 1
 #endif
+constexpr size_t kCoResidentSmem = 110 * 1024;       // two CTAs of this size share an SM
+constexpr size_t kGemvMaxSmem = 220 * 1024;
 
-__device__ __forceinline__ void bf16x8_to_f32(const uint4 v, float (&f)[8]) {
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    f[2 * i] = __uint_as_float(w[i] << 16);
-    f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
-  }
-}
-
-// y[b][n] = sum_k x[b][k] W[n][k] over a grid of at most two CTAs per SM: warp w of
-// CTA c takes output rows w + 8c, w + 8c + 8 * gridDim.x, ... (gate/up row pairs for
-// the SiLU-multiply), streaming each row in 256-element chunks, kGemvDepth chunks in
-// flight.  The weights are constants of the model, so the first loads are issued before
-// the dependency wait and overlap the preceding kernel.  The activations are staged
-// once per CTA as bf16: a bf16 input as is, an f32 input rounded, or (X_RMSNORM) the
-// RMS norm of the f32 residual stream times gamma, in f32.
-#ifndef TTS_GEMV_MIN_BLOCKS
-#define TTS_GEMV_MIN_BLOCKS 1
-#endif
-
+// y[b][n] = sum_k x[b][k] W[n][k], one CTA per SM, CTA c owning the output rows (gate/up
+// pairs for the SiLU-multiply) [c n_out / grid, (c+1) n_out / grid).  Rows are split into
+// segments of `seg` elements (<= 2048, 4 KB of bf16); a stage of the shared-memory ring
+// holds one segment of each of eight weight rows (a group: eight output rows, or four
+// gate rows and their four up rows), and consumer warp w always takes slot w, so a warp
+// keeps its row across the segments of a group.  A producer warp streams the stages with
+// 1-D bulk copies (complete_tx on a per-stage "full" mbarrier; the consumers release a
+// stage on its "empty" mbarrier).  The weights are constants of the model, so the
+// producer never waits for the preceding kernel: the ring fills while that kernel runs,
+// and with at most ~110 KB of shared memory and 112 registers a thread, the CTA fits on
+// an SM beside a CTA of the neighbouring GEMV, so consecutive launches overlap their weight
+// streams.  The consumers wait for the preceding kernel, stage the activations once as
+// bf16 (a bf16 input as is, an f32 input rounded, or the RMS norm of the f32 residual
+// stream times gamma, in f32), and accumulate in f32.
 template <int XM, int EPI, int MAXB>
-__global__ void __launch_bounds__(kGemvWarps * 32, TTS_GEMV_MIN_BLOCKS) gemv_bf16_kernel(const GemvParams p) {
-  extern __shared__ __align__(16) uint16_t s_x[];  // [B][K] bf16
-  __shared__ float s_red[kGemvWarps][MAXB];
-  __shared__ float s_scale[MAXB];
-  constexpr int RPW = EPI == EPI_SILU_MUL ? 2 : 1;
-  // 256-element chunks of each row in flight per warp (about 4 KB a warp)
-  constexpr int kGemvDepth = TTS_GEMV_DEPTH / RPW;
-  const int B = p.B, K = p.K;
+__global__ void __maxnreg__(96) gemv_bf16_kernel(const GemvParams p) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  __shared__ float s_red[kRowWarps][MAXB];
+  __shared__ float s_pair[2][kRowWarps][MAXB];
+  __shared__ __align__(8) uint64_t s_full[kGemvMaxStages];
+  __shared__ __align__(8) uint64_t s_empty[kGemvMaxStages];
+  constexpr int RPI = EPI == EPI_SILU_MUL ? 2 : 1;  // weight rows per output item
+  constexpr int IPG = kRowWarps / RPI;             // output items per group
+  const int B = p.B, K = p.K, seg = p.seg, NS = p.stages;
+  const int S = K / seg;  // segments per row (stages per group)
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int chunks = K / 256;  // K is a multiple of 256
-  const int stride_rows = kGemvWarps * gridDim.x;
-  int n = blockIdx.x * kGemvWarps + warp;  // this warp's first output row (or pair)
-  const uint16_t* W = static_cast<const uint16_t*>(p.w);
-  auto row_ptr = [&](int row, int r) {
-    return W + (static_cast<int64_t>(row) + (r ? p.inter : 0)) * K;
-  };
-  // first weight chunks, before the wait
-  uint4 wv[kGemvDepth][RPW];
-  if (n < p.n_out) {
+  const int i0 = static_cast<int>(static_cast<int64_t>(blockIdx.x) * p.n_out / gridDim.x);
+  const int i1 = static_cast<int>(static_cast<int64_t>(blockIdx.x + 1) * p.n_out / gridDim.x);
+  const int T = (i1 - i0 + IPG - 1) / IPG * S;  // stages of this CTA
+  const uint32_t seg_bytes = static_cast<uint32_t>(seg) * 2u;
+  unsigned char* ring = smem;
+  uint16_t* s_x = reinterpret_cast<uint16_t*>(smem + p.x_off);  // after the ring
+  if (tid == kRowWarps * 32) {
+    for (int i = 0; i < NS; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&s_empty[i], kRowWarps);
+    }
+    mbar_init_fence();
+  }
+  __syncthreads();
+  grid_launch_dependents();
+
+  if (warp == kRowWarps) {  // producer
+    const uint64_t pol = l2_evict_first_policy();
+    const uint16_t* W = static_cast<const uint16_t*>(p.w);
+    bool ok = true;
+    int issued = 0;
+    for (; issued < T; ++issued) {
+      const int t = issued, slot = t % NS;
+      if (t >= NS) {
+        if (lane == 0) ok = mbar_wait(&s_empty[slot], ((t / NS) - 1) & 1);
+        ok = __shfl_sync(kFull, ok, 0);
+        if (!ok) break;
+      }
+      const int g = t / S, sgi = t - g * S;
+      const int first = i0 + g * IPG;
+      const int nval = min(IPG, i1 - first);
+      if (lane == 0) mbar_arrive_expect_tx(&s_full[slot], static_cast<uint32_t>(nval * RPI) * seg_bytes);
+      __syncwarp();
+      if (lane < kRowWarps && lane % IPG < nval) {
+        const int64_t row = first + lane % IPG + (lane / IPG ? p.inter : 0);
+        bulk_g2s(ring + (static_cast<size_t>(slot) * kRowWarps + lane) * seg_bytes,
+                 W + row * K + static_cast<int64_t>(sgi) * seg, seg_bytes, &s_full[slot], pol);
+      }
+    }
+    if (!ok) set_err(p.err, TTS_EFLAG_TIMEOUT);
+    // leave no copy in flight: wait (bounded) for the last stages issued
+    if (lane == 0)
+      for (int t = max(0, issued - NS); t < issued; ++t)
+        if (!mbar_wait(&s_full[t % NS], (t / NS) & 1)) set_err(p.err, TTS_EFLAG_TIMEOUT);
+    return;
+  }
+
+  // ---- consumers (warps 0..7, 256 threads) ----
+  constexpr int kCT = kRowWarps * 32;
+  // residual elements a thread keeps in registers per stream (the rest are read twice)
+  constexpr int kNormRegs = MAXB <= 2 ? 8 : 16 / MAXB;
+  float gam[kNormRegs];
+  if (XM == X_RMSNORM) {
 #pragma unroll
-    for (int d = 0; d < kGemvDepth; ++d)
-#pragma unroll
-      for (int r = 0; r < RPW; ++r)
-        if (d < chunks) wv[d][r] = __ldcs(reinterpret_cast<const uint4*>(row_ptr(n, r) + d * 256) + lane);
+    for (int j = 0; j < kNormRegs; ++j) {
+      const int k = tid + kCT * j;
+      gam[j] = k < K ? __ldg(p.gamma + k) : 0.f;
+    }
   }
   grid_wait();
-  grid_launch_dependents();
-  // stage the activations
+  // residual epilogue: lane b's h[b][n] of this warp's rows, two groups ahead
+  auto resid = [&](int g) -> float {
+    const int it = i0 + g * IPG + warp % IPG;
+    return (it < i1 && lane < B) ? __ldcg(static_cast<const float*>(p.y) + static_cast<int64_t>(lane) * p.y_stride + it)
+                                 : 0.f;
+  };
+  float old0 = 0.f, old1 = 0.f;
+  if (EPI == EPI_RESIDUAL) {
+    old0 = resid(0);
+    old1 = resid(1);
+  }
   if (XM == X_RMSNORM) {
+    const float* h = static_cast<const float*>(p.x);
+    float hv[MAXB][kNormRegs];
     float ss[MAXB];
 #pragma unroll
-    for (int b = 0; b < MAXB; ++b) ss[b] = 0.f;
-    const float* h = static_cast<const float*>(p.x);
-    for (int k = tid; k < K; k += kGemvWarps * 32)
+    for (int b = 0; b < MAXB; ++b) {
+      ss[b] = 0.f;
 #pragma unroll
-      for (int b = 0; b < MAXB; ++b)
-        if (b < B) {
+      for (int j = 0; j < kNormRegs; ++j) {
+        const int k = tid + kCT * j;
+        hv[b][j] = (b < B && k < K) ? __ldcg(h + static_cast<int64_t>(b) * p.x_stride + k) : 0.f;
+      }
+    }
+#pragma unroll
+    for (int b = 0; b < MAXB; ++b) {
+#pragma unroll
+      for (int j = 0; j < kNormRegs; ++j) ss[b] = fmaf(hv[b][j], hv[b][j], ss[b]);
+      if (b < B)
+        for (int k = tid + kCT * kNormRegs; k < K; k += kCT) {
           const float v = __ldcg(h + static_cast<int64_t>(b) * p.x_stride + k);
           ss[b] = fmaf(v, v, ss[b]);
         }
 #pragma unroll
-    for (int b = 0; b < MAXB; ++b) {
-#pragma unroll
       for (int off = 16; off >= 1; off >>= 1) ss[b] += __shfl_xor_sync(kFull, ss[b], off);
       if (lane == 0) s_red[warp][b] = ss[b];
     }
-    __syncthreads();
-    if (tid < MAXB) {
+    named_barrier(1, kCT);
+#pragma unroll
+    for (int b = 0; b < MAXB; ++b) {
+      if (b >= B) break;
       float t = 0.f;
-      for (int w = 0; w < kGemvWarps; ++w) t += s_red[w][tid];
-      s_scale[tid] = 1.0f / sqrtf(t / static_cast<float>(K) + p.eps);
+#pragma unroll
+      for (int w = 0; w < kRowWarps; ++w) t += s_red[w][b];
+      const float scale = 1.0f / sqrtf(t / static_cast<float>(K) + p.eps);
+#pragma unroll
+      for (int j = 0; j < kNormRegs; ++j) {
+        const int k = tid + kCT * j;
+        if (k < K) s_x[b * K + k] = bf16_bits_rne(hv[b][j] * scale * gam[j]);
+      }
+      for (int k = tid + kCT * kNormRegs; k < K; k += kCT)
+        s_x[b * K + k] = bf16_bits_rne(__ldcg(h + static_cast<int64_t>(b) * p.x_stride + k) * scale *
+                                       __ldg(p.gamma + k));
     }
-    __syncthreads();
-    for (int i = tid; i < B * K; i += kGemvWarps * 32) {
-      const int b = i / K, k = i - b * K;
-      const float v = __ldcg(h + static_cast<int64_t>(b) * p.x_stride + k);
-      s_x[i] = bf16_bits_rne(v * s_scale[b] * __ldg(p.gamma + k));
-    }
-  } else {
-    for (int i = tid; i < B * K; i += kGemvWarps * 32) {
-      const int b = i / K, k = i - b * K;
-      if (XM == X_F32)
-        s_x[i] = bf16_bits_rne(__ldcg(static_cast<const float*>(p.x) + static_cast<int64_t>(b) * p.x_stride + k));
-      else
-        s_x[i] = __ldcg(static_cast<const uint16_t*>(p.x) + static_cast<int64_t>(b) * p.x_stride + k);
-    }
-  }
-  __syncthreads();
-  for (; n < p.n_out; n += stride_rows) {
-    float acc[RPW][MAXB];
+  } else if (XM == X_F32) {
+    const int per = K / 4;  // float4 units a stream
+    for (int u0 = tid; u0 < B * per; u0 += 4 * kCT) {
+      float4 v[4];
 #pragma unroll
-    for (int r = 0; r < RPW; ++r)
-#pragma unroll
-      for (int b = 0; b < MAXB; ++b) acc[r][b] = 0.f;
-    for (int c0 = 0; c0 < chunks; c0 += kGemvDepth) {
-      uint4 cur[kGemvDepth][RPW];
-#pragma unroll
-      for (int d = 0; d < kGemvDepth; ++d)
-#pragma unroll
-        for (int r = 0; r < RPW; ++r) cur[d][r] = wv[d][r];
-      // the next group: later chunks of this row, or the first of the next row
-      const int c1 = c0 + kGemvDepth;
-      const int nn = c1 < chunks ? n : n + stride_rows;
-      const int cc = c1 < chunks ? c1 : 0;
-      if (nn < p.n_out) {
-#pragma unroll
-        for (int d = 0; d < kGemvDepth; ++d)
-#pragma unroll
-          for (int r = 0; r < RPW; ++r)
-            if (cc + d < chunks) wv[d][r] = __ldcs(reinterpret_cast<const uint4*>(row_ptr(nn, r) + (cc + d) * 256) + lane);
+      for (int j = 0; j < 4; ++j) {
+        const int u = u0 + j * kCT;
+        if (u < B * per) {
+          const int b = u / per, k4 = u - b * per;
+          v[j] = __ldcg(reinterpret_cast<const float4*>(static_cast<const float*>(p.x) +
+                                                        static_cast<int64_t>(b) * p.x_stride) + k4);
+        }
       }
 #pragma unroll
-      for (int d = 0; d < kGemvDepth; ++d) {
-        if (c0 + d >= chunks) break;
-        float wf[RPW][8];
-#pragma unroll
-        for (int r = 0; r < RPW; ++r) bf16x8_to_f32(cur[d][r], wf[r]);
-        const int k0 = (c0 + d) * 256 + lane * 8;
-#pragma unroll
-        for (int b = 0; b < MAXB; ++b) {
-          if (b >= B) break;
-          float xf[8];
-          bf16x8_to_f32(*reinterpret_cast<const uint4*>(s_x + b * K + k0), xf);
-#pragma unroll
-          for (int r = 0; r < RPW; ++r)
-#pragma unroll
-            for (int e = 0; e < 8; ++e) acc[r][b] = fmaf(wf[r][e], xf[e], acc[r][b]);
+      for (int j = 0; j < 4; ++j) {
+        const int u = u0 + j * kCT;
+        if (u < B * per) {
+          const uint32_t lo = bf16_bits_rne(v[j].x) | (static_cast<uint32_t>(bf16_bits_rne(v[j].y)) << 16);
+          const uint32_t hi = bf16_bits_rne(v[j].z) | (static_cast<uint32_t>(bf16_bits_rne(v[j].w)) << 16);
+          reinterpret_cast<uint2*>(s_x)[u] = make_uint2(lo, hi);  // u = b * per + k4
         }
       }
     }
+  } else {
+    const int per = K / 8;  // 16-byte units a stream
+    for (int u0 = tid; u0 < B * per; u0 += 4 * kCT) {
+      uint4 v[4];
 #pragma unroll
-    for (int r = 0; r < RPW; ++r)
-#pragma unroll
-      for (int b = 0; b < MAXB; ++b)
-#pragma unroll
-        for (int off = 16; off >= 1; off >>= 1) acc[r][b] += __shfl_xor_sync(kFull, acc[r][b], off);
-    if (lane < B) {
-      // lane b writes stream b's result (every lane holds every sum after the reduction)
-      float mine[RPW];
-#pragma unroll
-      for (int r = 0; r < RPW; ++r) {
-        mine[r] = acc[r][0];
-#pragma unroll
-        for (int b = 1; b < MAXB; ++b)
-          if (lane == b) mine[r] = acc[r][b];
+      for (int j = 0; j < 4; ++j) {
+        const int u = u0 + j * kCT;
+        if (u < B * per) {
+          const int b = u / per, k8 = u - b * per;
+          v[j] = __ldcg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.x) +
+                                                       static_cast<int64_t>(b) * p.x_stride) + k8);
+        }
       }
-      const int b = lane;
-      if (EPI == EPI_STORE) {
-        static_cast<float*>(p.y)[static_cast<int64_t>(b) * p.y_stride + n] = mine[0];
-      } else if (EPI == EPI_RESIDUAL) {
-        float* hp = static_cast<float*>(p.y) + static_cast<int64_t>(b) * p.y_stride + n;
-        *hp = __fadd_rn(*hp, mine[0]);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int u = u0 + j * kCT;
+        if (u < B * per) reinterpret_cast<uint4*>(s_x)[u] = v[j];
+      }
+    }
+  }
+  named_barrier(1, kCT);
+
+  float acc[MAXB];
+#pragma unroll
+  for (int b = 0; b < MAXB; ++b) acc[b] = 0.f;
+  bool failed = false;
+  const int chunks = seg / 256;  // at most kSegMax / 256
+  for (int t = 0; t < T; ++t) {
+    const int slot = t % NS;
+    const int g = t / S, sgi = t - g * S;
+    const int item = i0 + g * IPG + warp % IPG;
+    const bool valid = item < i1;
+    if (!failed) {
+      const bool ok = __all_sync(kFull, mbar_wait(&s_full[slot], (t / NS) & 1));
+      if (!ok) {
+        failed = true;
+        if (lane == 0) set_err(p.err, TTS_EFLAG_TIMEOUT);
+      }
+    }
+    if (valid && !failed) {
+      // lane l owns elements 8l..8l+7 of each 256-element chunk; its weight vectors of
+      // the segment are loaded first, so the shared-memory latencies overlap
+      const unsigned char* wrow = ring + (static_cast<size_t>(slot) * kRowWarps + warp) * seg_bytes + lane * 16;
+      const uint16_t* xs = s_x + sgi * seg + lane * 8;
+      constexpr int CM = kSegMax / 256;
+      uint4 wv[CM];
+#pragma unroll
+      for (int c = 0; c < CM; ++c)
+        if (c < chunks) wv[c] = lds128(wrow + c * 512);
+      if constexpr (MAXB <= 2) {
+        // few streams: four independent partial sums per stream
+#pragma unroll
+        for (int b = 0; b < MAXB; ++b) {
+          if (b >= B) break;
+          uint4 xv[CM];
+#pragma unroll
+          for (int c = 0; c < CM; ++c)
+            if (c < chunks) xv[c] = lds128(xs + b * K + c * 256);
+          float part[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int c = 0; c < CM; ++c) {
+            if (c < chunks) {
+              float wf[8], xf[8];
+              unpack_bf16x8(wv[c], wf);
+              unpack_bf16x8(xv[c], xf);
+#pragma unroll
+              for (int e = 0; e < 8; ++e) part[e & 3] = fmaf(wf[e], xf[e], part[e & 3]);
+            }
+          }
+          acc[b] += (part[0] + part[1]) + (part[2] + part[3]);
+        }
       } else {
-        const double g = mine[0], u = mine[RPW - 1];
-        const float a = static_cast<float>(g / (1.0 + exp(-g)) * u);
-        static_cast<uint16_t*>(p.y)[static_cast<int64_t>(b) * p.y_stride + n] = bf16_bits_rne(a);
+        // several streams: their sums are independent chains already
+#pragma unroll
+        for (int c = 0; c < CM; ++c) {
+          if (c < chunks) {
+            float wf[8];
+            unpack_bf16x8(wv[c], wf);
+#pragma unroll
+            for (int b = 0; b < MAXB; ++b) {
+              if (b >= B) break;
+              float xf[8];
+              unpack_bf16x8(lds128(xs + b * K + c * 256), xf);
+#pragma unroll
+              for (int e = 0; e < 8; ++e) acc[b] = fmaf(wf[e], xf[e], acc[b]);
+            }
+          }
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&s_empty[slot]);
+    if (sgi != S - 1) continue;
+    // the group's rows are complete: reduce, epilogue
+#pragma unroll
+    for (int b = 0; b < MAXB; ++b)
+#pragma unroll
+      for (int off = 16; off >= 1; off >>= 1) acc[b] += __shfl_xor_sync(kFull, acc[b], off);
+    float mine = acc[0];  // lane b keeps stream b's sum
+#pragma unroll
+    for (int b = 1; b < MAXB; ++b)
+      if (lane == b) mine = acc[b];
+#pragma unroll
+    for (int b = 0; b < MAXB; ++b) acc[b] = 0.f;
+    if (EPI == EPI_STORE) {
+      if (valid && lane < B && !failed)
+        static_cast<float*>(p.y)[static_cast<int64_t>(lane) * p.y_stride + item] = mine;
+    } else if (EPI == EPI_RESIDUAL) {
+      if (valid && lane < B && !failed)
+        static_cast<float*>(p.y)[static_cast<int64_t>(lane) * p.y_stride + item] = __fadd_rn(old0, mine);
+      old0 = old1;
+      old1 = resid(g + 2);
+    } else {
+      // warp w < IPG holds gate row of item w, warp w + IPG its up row
+      if (lane < MAXB) s_pair[g & 1][warp][lane] = mine;
+      named_barrier(1, kCT);
+      if (warp < IPG && valid && lane < B && !failed) {
+        const float gt = s_pair[g & 1][warp][lane], up = s_pair[g & 1][warp + IPG][lane];
+        const float a = gt / (1.0f + expf(-gt)) * up;
+        static_cast<uint16_t*>(p.y)[static_cast<int64_t>(lane) * p.y_stride + item] = bf16_bits_rne(a);
       }
     }
   }
 }
 
-template <int XM, int EPI>
-cudaError_t launch_gemv_t(const GemvParams& p, cudaStream_t s) {
-  auto kern = gemv_bf16_kernel<XM, EPI, kGemvMaxB>;
-  const size_t smem = static_cast<size_t>(p.B) * p.K * sizeof(uint16_t);
+template <int XM, int EPI, int MAXB>
+cudaError_t launch_gemv_t(const GemvParams& p0, cudaStream_t s) {
+  auto kern = gemv_bf16_kernel<XM, EPI, MAXB>;
+  GemvParams p = p0;
+  // segment: the longest multiple of 256 elements that divides K and is at most 2048
+  int nseg = (p.K + kSegMax - 1) / kSegMax;
+  while (p.K % nseg != 0 || (p.K / nseg) % 256 != 0) ++nseg;
+  p.seg = p.K / nseg;
   static int configured_for = -1;
   static int n_sm = 1;
-  static int per_sm = 1;
+  static size_t co_budget = kCoResidentSmem;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (configured_for != dev) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(kGemvMaxB * kGemvMaxK * sizeof(uint16_t)));
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kGemvMaxSmem));
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
     if (cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n_sm < 1) {
       cudaGetLastError();
       n_sm = 1;
     }
-    // CTAs that fit on an SM with the largest activation block (8 streams x 8192)
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kGemvWarps * 32,
-                                                      kGemvMaxB * 2048 * sizeof(uint16_t)) != cudaSuccess ||
-        per_sm < 1) {
+    // dynamic shared memory that still lets two CTAs (of this or a neighbouring GEMV)
+    // share an SM: half the SM's shared memory less the per-CTA reservation and the
+    // kernel's static shared memory
+    int per_sm = 0, reserved = 0;
+    cudaFuncAttributes fa = {};
+    if (cudaDeviceGetAttribute(&per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) == cudaSuccess &&
+        cudaFuncGetAttributes(&fa, kern) == cudaSuccess && per_sm > 0) {
+      const long long b = per_sm / 2 - reserved - static_cast<long long>(fa.sharedSizeBytes);
+      co_budget = b > 0 ? static_cast<size_t>(b) & ~static_cast<size_t>(127) : kCoResidentSmem;
+    } else {
       cudaGetLastError();
-      per_sm = 1;
     }
     configured_for = dev;
   }
-  int ctas = (p.n_out + kGemvWarps - 1) / kGemvWarps;
-  if (ctas > per_sm * n_sm) ctas = per_sm * n_sm;
-  return launch_pdl(kern, dim3(ctas), dim3(kGemvWarps * 32), smem, s, p);
+  const int ctas = p.n_out < n_sm ? p.n_out : n_sm;
+  constexpr int RPI = EPI == EPI_SILU_MUL ? 2 : 1;
+  constexpr int IPG = kRowWarps / RPI;
+  const size_t seg_bytes = static_cast<size_t>(p.seg) * 2;
+  const size_t stage = kRowWarps * seg_bytes;
+  const size_t x_bytes = static_cast<size_t>(p.B) * p.K * 2;
+  // Whole fit: when a CTA's whole share of the weights fits beside the activations
+  // (stage t in slot t, the last stage holding only its rows), every copy is issued at
+  // once and no slot is reused.
+  const int items_max = (p.n_out + ctas - 1) / ctas;
+  const int groups_max = (items_max + IPG - 1) / IPG;
+  const int t_max = groups_max * nseg;
+  const size_t whole = (static_cast<size_t>(t_max - 1) * kRowWarps + (items_max - (groups_max - 1) * IPG)) * seg_bytes;
+  size_t smem;
+  if (TTS_GEMV_WHOLE_FIT && RPI == 1 && t_max <= kGemvMaxStages && whole + x_bytes <= co_budget) {
+    p.stages = t_max;
+    p.x_off = static_cast<uint32_t>(whole);
+    smem = whole + x_bytes;
+  } else {
+    // the deepest ring that leaves room for a neighbouring GEMV CTA on the SM, else the
+    // deepest that fits at all
+    int ns = kGemvRingStages;
+    while (ns > 2 && ns * stage + x_bytes > co_budget) --ns;
+    if (ns * stage + x_bytes > co_budget) {
+      ns = kGemvRingStages;
+      while (ns > 2 && ns * stage + x_bytes > kGemvMaxSmem) --ns;
+    }
+    p.stages = ns;
+    p.x_off = static_cast<uint32_t>(ns * stage);
+    smem = ns * stage + x_bytes;
+  }
+  if (smem > kGemvMaxSmem) return cudaErrorInvalidValue;
+  return launch_pdl(kern, dim3(ctas), dim3(kGemvThreads), smem, s, p);
 }
 
 }  // namespace
 
 cudaError_t launch_gemv_bf16(const GemvParams& p, int x_mode, int epilogue, cudaStream_t s) {
-#define TTS_GEMV_CASE(XM)                                                                      \
-  if (x_mode == XM) {                                                                          \
-    if (epilogue == EPI_STORE) return launch_gemv_t<XM, EPI_STORE>(p, s);                      \
-    if (epilogue == EPI_RESIDUAL) return launch_gemv_t<XM, EPI_RESIDUAL>(p, s);                \
-    if (epilogue == EPI_SILU_MUL) return launch_gemv_t<XM, EPI_SILU_MUL>(p, s);                \
+  if (p.B < 1 || p.B > kGemvMaxB) return cudaErrorInvalidValue;
+  // streams rounded up to 1, 2, 4 or 8: the kernel's per-stream arrays are that long
+#define TTS_GEMV_CASE(XM, EPI)                                                                 \
+  if (x_mode == XM && epilogue == EPI) {                                                       \
+    if (p.B == 1) return launch_gemv_t<XM, EPI, 1>(p, s);                                      \
+    if (p.B == 2) return launch_gemv_t<XM, EPI, 2>(p, s);                                      \
+    if (p.B <= 4) return launch_gemv_t<XM, EPI, 4>(p, s);                                      \
+    return launch_gemv_t<XM, EPI, 8>(p, s);                                                    \
   }
-  TTS_GEMV_CASE(X_BF16)
-  TTS_GEMV_CASE(X_F32)
-  TTS_GEMV_CASE(X_RMSNORM)
+  TTS_GEMV_CASE(X_RMSNORM, EPI_STORE)     // qkv
+  TTS_GEMV_CASE(X_F32, EPI_RESIDUAL)      // o
+  TTS_GEMV_CASE(X_RMSNORM, EPI_SILU_MUL)  // gate/up
+  TTS_GEMV_CASE(X_BF16, EPI_RESIDUAL)     // down
 #undef TTS_GEMV_CASE
   return cudaErrorInvalidValue;
 }

@@ -330,15 +330,18 @@ tts_status tts_counter_advance(uint64_t* counter, uint64_t by, void* stream);
  * table: fused residual add + RMSNorm, q/k norm + RoPE, SiLU-multiply, reproducing the
  * reference rounding with integer round-to-nearest-even; [pipeline] KV-cache section
  * for the step).  In place on the residual stream h [B][hidden] (f32):
- *   x = bf16(rmsnorm(h) * gamma_attn)          (statistics in double, RNE to bf16)
+ *   x = bf16(rmsnorm(h) * gamma_attn)          (statistics in f32, RNE to bf16)
  *   qkv = x W_qkv^T                             (f32; q, k, v as in tts_decode_step)
  *   attn = tts_decode_step(q, k, v, ...)        (norm + RoPE, new row, attention)
  *   h = h + bf16(attn) W_o^T
  *   x = bf16(rmsnorm(h) * gamma_mlp)
- *   a = bf16(silu(x W_gate^T) * x W_up^T)       (silu in double)
+ *   a = bf16(silu(x W_gate^T) * x W_up^T)       (silu in f32)
  *   h = h + a W_down^T
- * Products accumulate in f32; every residual add is one f32 addition.  Seven launches
- * on `stream`.  Weights are bf16, row-major, rows of `hidden` (or `inter`) elements:
+ * Products accumulate in f32; every residual add is one f32 addition.  Five launches
+ * on `stream` (four GEMVs and the decode step).  The weights and the gammas are treated
+ * as constants: each launch starts reading them before the preceding kernel on `stream`
+ * has finished, so they must not be written by the kernel launched just before this
+ * call on the same stream (write them with a copy, or synchronise first).  Weights are bf16, row-major, rows of `hidden` (or `inter`) elements:
  *   w_qkv [(Hq + 2 Hkv) D][hidden], w_o [hidden][Hq D], w_gu [2 inter][hidden] (the
  *   gate rows, then the up rows), w_down [hidden][inter].
  * hidden, inter and Hq*D must be multiples of 256 and at most 8192.

@@ -36,9 +36,18 @@ def _bits16(t):
     return t.view(torch.int16).numpy().view(np.uint16)
 
 
-@pytest.mark.parametrize("B,cur", [(1, [4095]), (1, [100]), (4, [7, 1000, 2047, 3000]), (8, [300] * 8)])
-def test_decode_layer_matches_oracle(tts, B, cur):
-    w = W.workload("talker", B=B, layers=1)
+# The talker shapes, and two smaller layers whose row lengths split into several
+# segments of 768 / 1280 elements (hidden 768 / 1280, intermediate 3 x hidden) with
+# partial row groups at the ends of the CTAs' ranges.
+SMALL_768 = dict(hidden=768, n_q_heads=4, n_kv_heads=2, capacity=512)
+SMALL_1280 = dict(hidden=1280, n_q_heads=8, n_kv_heads=2, capacity=512)
+
+
+@pytest.mark.parametrize("B,cur,shape", [(1, [4095], {}), (1, [100], {}), (4, [7, 1000, 2047, 3000], {}),
+                                         (8, [300] * 8, {}), (3, [5, 200, 511], SMALL_768),
+                                         (5, [0, 1, 64, 300, 511], SMALL_1280)])
+def test_decode_layer_matches_oracle(tts, B, cur, shape):
+    w = W.workload("talker", B=B, layers=1, **shape)
     H, I, Hq, Hkv, D = w.hidden, 3 * w.hidden, w.n_q_heads, w.n_kv_heads, w.head_dim
     L = Layer(w, seed=80, cur_len=cur, poison=True)
     wt = _weights(H, I, Hq, Hkv, D, 81)
