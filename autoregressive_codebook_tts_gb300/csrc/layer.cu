@@ -3,19 +3,20 @@
 // reference rounding reproduced by integer round-to-nearest-even; "Lean Talker frame":
 // q/k/v as strided views of one projection).
 //
-//   qkv = bf16(rmsnorm(h)) W_qkv^T (f32)      gemv_bf16_kernel<X_RMSNORM, EPI_STORE>
+//   qkv = bf16(rmsnorm(h)) W_qkv^T (f32)      GEMV <X_RMSNORM, EPI_STORE>
 //   attn = decode step (q, k, v)              decode_attn_kernel (fused), unchanged
-//   h += bf16(attn) W_o^T                     gemv_bf16_kernel<X_F32, EPI_RESIDUAL>
+//   h += bf16(attn) W_o^T                     GEMV <X_F32, EPI_RESIDUAL>
 //   a = bf16(silu(x W_g^T) * x W_u^T), x = bf16(rmsnorm(h))
-//                                             gemv_bf16_kernel<X_RMSNORM, EPI_SILU_MUL>
-//   h += a W_down^T                           gemv_bf16_kernel<X_BF16, EPI_RESIDUAL>
+//                                             GEMV <X_RMSNORM, EPI_SILU_MUL>
+//   h += a W_down^T                           GEMV <X_BF16, EPI_RESIDUAL>
 //
 // At the batch sizes of a decode step (B <= 8 here) every product is a GEMV bound by
-// streaming the weights from HBM.  The weights are streamed into a shared-memory ring by
-// bulk copies that start before the dependency wait (they are constants), the activations
-// are staged once per CTA as bf16 (the RMS norm computed there, so it needs no launch of
-// its own), each warp accumulates one row in f32 and a fused epilogue stores, adds into
-// the residual stream or applies the SiLU-multiply.  The norm is computed in f32 by every
+// streaming the weights from HBM.  For up to four streams the weights are streamed into a
+// shared-memory ring by bulk copies (gemv_bf16_kernel), for five to eight through
+// registers (gemv_regs_kernel); both start loading before the dependency wait (the weights
+// are constants), stage the activations once per CTA as bf16 (the RMS norm computed there,
+// so it needs no launch of its own), accumulate each row in f32 and apply a fused
+// epilogue: store, add into the residual stream, or SiLU-multiply.  The norm is computed in f32 by every
 // CTA, and so is the SiLU.  A bf16 rounding of an intermediate can therefore land one
 // step from the exact value's.
 #include <cstdint>
@@ -40,11 +41,7 @@ enum XMode { X_BF16 = 0, X_F32 = 1, X_RMSNORM = 2 };
 constexpr int kRowWarps = 8;                         // consumer warps: one weight row each
 constexpr int kGemvThreads = (kRowWarps + 1) * 32;   // + one producer warp
 constexpr int kSegMax = 2048;                        // elements of a row segment (4 KB)
-constexpr int kGemvRingStages = 4;                   // deepest reused ring
-constexpr int kGemvMaxStages = 8;                    // stages of a whole-fit ring
-#ifndef TTS_GEMV_WHOLE_FIT
-#define TTS_GEMV_WHOLE_FIT 1
-#endif
+constexpr int kGemvMaxStages = 4;
 constexpr size_t kCoResidentSmem = 110 * 1024;       // two CTAs of this size share an SM
 constexpr size_t kGemvMaxSmem = 220 * 1024;
 
@@ -57,13 +54,13 @@ constexpr size_t kGemvMaxSmem = 220 * 1024;
 // 1-D bulk copies (complete_tx on a per-stage "full" mbarrier; the consumers release a
 // stage on its "empty" mbarrier).  The weights are constants of the model, so the
 // producer never waits for the preceding kernel: the ring fills while that kernel runs,
-// and with at most ~110 KB of shared memory and 112 registers a thread, the CTA fits on
-// an SM beside a CTA of the neighbouring GEMV, so consecutive launches overlap their weight
-// streams.  The consumers wait for the preceding kernel, stage the activations once as
+// and with at most ~110 KB of shared memory and few registers (56 a thread for one or two
+// streams) the CTA fits on an SM beside a CTA of the neighbouring kernel, so consecutive
+// launches overlap their weight streams.  The consumers wait for the preceding kernel, stage the activations once as
 // bf16 (a bf16 input as is, an f32 input rounded, or the RMS norm of the f32 residual
 // stream times gamma, in f32), and accumulate in f32.
 template <int XM, int EPI, int MAXB>
-__global__ void __maxnreg__(96) gemv_bf16_kernel(const GemvParams p) {
+__global__ void __maxnreg__(MAXB <= 2 ? 56 : 96) gemv_bf16_kernel(const GemvParams p) {
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ float s_red[kRowWarps][MAXB];
   __shared__ float s_pair[2][kRowWarps][MAXB];
@@ -251,53 +248,18 @@ __global__ void __maxnreg__(96) gemv_bf16_kernel(const GemvParams p) {
       }
     }
     if (valid && !failed) {
-      // lane l owns elements 8l..8l+7 of each 256-element chunk; its weight vectors of
-      // the segment are loaded first, so the shared-memory latencies overlap
-      const unsigned char* wrow = ring + (static_cast<size_t>(slot) * kRowWarps + warp) * seg_bytes + lane * 16;
+      const unsigned char* wrow = ring + (static_cast<size_t>(slot) * kRowWarps + warp) * seg_bytes;
       const uint16_t* xs = s_x + sgi * seg + lane * 8;
-      constexpr int CM = kSegMax / 256;
-      uint4 wv[CM];
-#pragma unroll
-      for (int c = 0; c < CM; ++c)
-        if (c < chunks) wv[c] = lds128(wrow + c * 512);
-      if constexpr (MAXB <= 2) {
-        // few streams: four independent partial sums per stream
+      for (int c = 0; c < chunks; ++c) {
+        float wf[8];
+        unpack_bf16x8(lds128(wrow + (c * 256 + lane * 8) * 2), wf);
 #pragma unroll
         for (int b = 0; b < MAXB; ++b) {
           if (b >= B) break;
-          uint4 xv[CM];
+          float xf[8];
+          unpack_bf16x8(lds128(xs + b * K + c * 256), xf);
 #pragma unroll
-          for (int c = 0; c < CM; ++c)
-            if (c < chunks) xv[c] = lds128(xs + b * K + c * 256);
-          float part[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-          for (int c = 0; c < CM; ++c) {
-            if (c < chunks) {
-              float wf[8], xf[8];
-              unpack_bf16x8(wv[c], wf);
-              unpack_bf16x8(xv[c], xf);
-#pragma unroll
-              for (int e = 0; e < 8; ++e) part[e & 3] = fmaf(wf[e], xf[e], part[e & 3]);
-            }
-          }
-          acc[b] += (part[0] + part[1]) + (part[2] + part[3]);
-        }
-      } else {
-        // several streams: their sums are independent chains already
-#pragma unroll
-        for (int c = 0; c < CM; ++c) {
-          if (c < chunks) {
-            float wf[8];
-            unpack_bf16x8(wv[c], wf);
-#pragma unroll
-            for (int b = 0; b < MAXB; ++b) {
-              if (b >= B) break;
-              float xf[8];
-              unpack_bf16x8(lds128(xs + b * K + c * 256), xf);
-#pragma unroll
-              for (int e = 0; e < 8; ++e) acc[b] = fmaf(wf[e], xf[e], acc[b]);
-            }
-          }
+          for (int e = 0; e < 8; ++e) acc[b] = fmaf(wf[e], xf[e], acc[b]);
         }
       }
     }
@@ -334,6 +296,191 @@ __global__ void __maxnreg__(96) gemv_bf16_kernel(const GemvParams p) {
       }
     }
   }
+}
+
+// Five to eight streams: eight FMAs per weight element make the ring's eight consumer
+// warps the bottleneck, so this kernel streams the weights through registers instead,
+// over up to two CTAs of eight warps per SM: warp w of CTA c takes output rows w + 8c,
+// w + 8c + 8 * gridDim.x, ... (gate/up row pairs for the SiLU-multiply), each row in
+// 256-element chunks, kDepth chunks in flight (about 4 KB a warp), the first issued
+// before the dependency wait.  Activations are staged and epilogues applied as in the
+// ring kernel.
+constexpr int kRegWarps = 8;
+constexpr int kRegDepth = 8;
+
+template <int XM, int EPI>
+__global__ void __launch_bounds__(kRegWarps * 32) gemv_regs_kernel(const GemvParams p) {
+  constexpr int MAXB = kGemvMaxB;
+  extern __shared__ __align__(16) uint16_t s_x[];  // [B][K] bf16
+  __shared__ float s_red[kRegWarps][MAXB];
+  __shared__ float s_scale[MAXB];
+  constexpr int RPW = EPI == EPI_SILU_MUL ? 2 : 1;
+  // 256-element chunks of each row in flight per warp (about 4 KB a warp)
+  constexpr int kDepth = kRegDepth / RPW;
+  const int B = p.B, K = p.K;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int chunks = K / 256;  // K is a multiple of 256
+  const int stride_rows = kRegWarps * gridDim.x;
+  int n = blockIdx.x * kRegWarps + warp;  // this warp's first output row (or pair)
+  const uint16_t* W = static_cast<const uint16_t*>(p.w);
+  auto row_ptr = [&](int row, int r) {
+    return W + (static_cast<int64_t>(row) + (r ? p.inter : 0)) * K;
+  };
+  // first weight chunks, before the wait
+  uint4 wv[kDepth][RPW];
+  if (n < p.n_out) {
+#pragma unroll
+    for (int d = 0; d < kDepth; ++d)
+#pragma unroll
+      for (int r = 0; r < RPW; ++r)
+        if (d < chunks) wv[d][r] = __ldcs(reinterpret_cast<const uint4*>(row_ptr(n, r) + d * 256) + lane);
+  }
+  grid_wait();
+  grid_launch_dependents();
+  // stage the activations
+  if (XM == X_RMSNORM) {
+    float ss[MAXB];
+#pragma unroll
+    for (int b = 0; b < MAXB; ++b) ss[b] = 0.f;
+    const float* h = static_cast<const float*>(p.x);
+    for (int k = tid; k < K; k += kRegWarps * 32)
+#pragma unroll
+      for (int b = 0; b < MAXB; ++b)
+        if (b < B) {
+          const float v = __ldcg(h + static_cast<int64_t>(b) * p.x_stride + k);
+          ss[b] = fmaf(v, v, ss[b]);
+        }
+#pragma unroll
+    for (int b = 0; b < MAXB; ++b) {
+#pragma unroll
+      for (int off = 16; off >= 1; off >>= 1) ss[b] += __shfl_xor_sync(kFull, ss[b], off);
+      if (lane == 0) s_red[warp][b] = ss[b];
+    }
+    __syncthreads();
+    if (tid < MAXB) {
+      float t = 0.f;
+      for (int w = 0; w < kRegWarps; ++w) t += s_red[w][tid];
+      s_scale[tid] = 1.0f / sqrtf(t / static_cast<float>(K) + p.eps);
+    }
+    __syncthreads();
+    for (int i = tid; i < B * K; i += kRegWarps * 32) {
+      const int b = i / K, k = i - b * K;
+      const float v = __ldcg(h + static_cast<int64_t>(b) * p.x_stride + k);
+      s_x[i] = bf16_bits_rne(v * s_scale[b] * __ldg(p.gamma + k));
+    }
+  } else {
+    for (int i = tid; i < B * K; i += kRegWarps * 32) {
+      const int b = i / K, k = i - b * K;
+      if (XM == X_F32)
+        s_x[i] = bf16_bits_rne(__ldcg(static_cast<const float*>(p.x) + static_cast<int64_t>(b) * p.x_stride + k));
+      else
+        s_x[i] = __ldcg(static_cast<const uint16_t*>(p.x) + static_cast<int64_t>(b) * p.x_stride + k);
+    }
+  }
+  __syncthreads();
+  for (; n < p.n_out; n += stride_rows) {
+    float acc[RPW][MAXB];
+#pragma unroll
+    for (int r = 0; r < RPW; ++r)
+#pragma unroll
+      for (int b = 0; b < MAXB; ++b) acc[r][b] = 0.f;
+    for (int c0 = 0; c0 < chunks; c0 += kDepth) {
+      uint4 cur[kDepth][RPW];
+#pragma unroll
+      for (int d = 0; d < kDepth; ++d)
+#pragma unroll
+        for (int r = 0; r < RPW; ++r) cur[d][r] = wv[d][r];
+      // the next group: later chunks of this row, or the first of the next row
+      const int c1 = c0 + kDepth;
+      const int nn = c1 < chunks ? n : n + stride_rows;
+      const int cc = c1 < chunks ? c1 : 0;
+      if (nn < p.n_out) {
+#pragma unroll
+        for (int d = 0; d < kDepth; ++d)
+#pragma unroll
+          for (int r = 0; r < RPW; ++r)
+            if (cc + d < chunks) wv[d][r] = __ldcs(reinterpret_cast<const uint4*>(row_ptr(nn, r) + (cc + d) * 256) + lane);
+      }
+#pragma unroll
+      for (int d = 0; d < kDepth; ++d) {
+        if (c0 + d >= chunks) break;
+        float wf[RPW][8];
+#pragma unroll
+        for (int r = 0; r < RPW; ++r) unpack_bf16x8(cur[d][r], wf[r]);
+        const int k0 = (c0 + d) * 256 + lane * 8;
+#pragma unroll
+        for (int b = 0; b < MAXB; ++b) {
+          if (b >= B) break;
+          float xf[8];
+          unpack_bf16x8(*reinterpret_cast<const uint4*>(s_x + b * K + k0), xf);
+#pragma unroll
+          for (int r = 0; r < RPW; ++r)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[r][b] = fmaf(wf[r][e], xf[e], acc[r][b]);
+        }
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < RPW; ++r)
+#pragma unroll
+      for (int b = 0; b < MAXB; ++b)
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) acc[r][b] += __shfl_xor_sync(kFull, acc[r][b], off);
+    if (lane < B) {
+      // lane b writes stream b's result (every lane holds every sum after the reduction)
+      float mine[RPW];
+#pragma unroll
+      for (int r = 0; r < RPW; ++r) {
+        mine[r] = acc[r][0];
+#pragma unroll
+        for (int b = 1; b < MAXB; ++b)
+          if (lane == b) mine[r] = acc[r][b];
+      }
+      const int b = lane;
+      if (EPI == EPI_STORE) {
+        static_cast<float*>(p.y)[static_cast<int64_t>(b) * p.y_stride + n] = mine[0];
+      } else if (EPI == EPI_RESIDUAL) {
+        float* hp = static_cast<float*>(p.y) + static_cast<int64_t>(b) * p.y_stride + n;
+        *hp = __fadd_rn(*hp, mine[0]);
+      } else {
+        const float g = mine[0], u = mine[RPW - 1];
+        const float a = g / (1.0f + expf(-g)) * u;
+        static_cast<uint16_t*>(p.y)[static_cast<int64_t>(b) * p.y_stride + n] = bf16_bits_rne(a);
+      }
+    }
+  }
+}
+
+template <int XM, int EPI>
+cudaError_t launch_gemv_regs(const GemvParams& p, cudaStream_t s) {
+  auto kern = gemv_regs_kernel<XM, EPI>;
+  const size_t smem = static_cast<size_t>(p.B) * p.K * sizeof(uint16_t);
+  static int configured_for = -1;
+  static int n_sm = 1;
+  static int per_sm = 1;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (configured_for != dev) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kGemvMaxB * kGemvMaxK * sizeof(uint16_t)));
+    if (e != cudaSuccess) return e;
+    if (cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n_sm < 1) {
+      cudaGetLastError();
+      n_sm = 1;
+    }
+    // CTAs that fit on an SM with the activation block of 8 streams x 2048
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kRegWarps * 32,
+                                                      kGemvMaxB * 2048 * sizeof(uint16_t)) != cudaSuccess ||
+        per_sm < 1) {
+      cudaGetLastError();
+      per_sm = 1;
+    }
+    configured_for = dev;
+  }
+  int ctas = (p.n_out + kRegWarps - 1) / kRegWarps;
+  if (ctas > per_sm * n_sm) ctas = per_sm * n_sm;
+  return launch_pdl(kern, dim3(ctas), dim3(kRegWarps * 32), smem, s, p);
 }
 
 template <int XM, int EPI, int MAXB>
@@ -375,36 +522,19 @@ cudaError_t launch_gemv_t(const GemvParams& p0, cudaStream_t s) {
     configured_for = dev;
   }
   const int ctas = p.n_out < n_sm ? p.n_out : n_sm;
-  constexpr int RPI = EPI == EPI_SILU_MUL ? 2 : 1;
-  constexpr int IPG = kRowWarps / RPI;
-  const size_t seg_bytes = static_cast<size_t>(p.seg) * 2;
-  const size_t stage = kRowWarps * seg_bytes;
+  const size_t stage = static_cast<size_t>(kRowWarps) * p.seg * 2;
   const size_t x_bytes = static_cast<size_t>(p.B) * p.K * 2;
-  // Whole fit: when a CTA's whole share of the weights fits beside the activations
-  // (stage t in slot t, the last stage holding only its rows), every copy is issued at
-  // once and no slot is reused.
-  const int items_max = (p.n_out + ctas - 1) / ctas;
-  const int groups_max = (items_max + IPG - 1) / IPG;
-  const int t_max = groups_max * nseg;
-  const size_t whole = (static_cast<size_t>(t_max - 1) * kRowWarps + (items_max - (groups_max - 1) * IPG)) * seg_bytes;
-  size_t smem;
-  if (TTS_GEMV_WHOLE_FIT && RPI == 1 && t_max <= kGemvMaxStages && whole + x_bytes <= co_budget) {
-    p.stages = t_max;
-    p.x_off = static_cast<uint32_t>(whole);
-    smem = whole + x_bytes;
-  } else {
-    // the deepest ring that leaves room for a neighbouring GEMV CTA on the SM, else the
-    // deepest that fits at all
-    int ns = kGemvRingStages;
-    while (ns > 2 && ns * stage + x_bytes > co_budget) --ns;
-    if (ns * stage + x_bytes > co_budget) {
-      ns = kGemvRingStages;
-      while (ns > 2 && ns * stage + x_bytes > kGemvMaxSmem) --ns;
-    }
-    p.stages = ns;
-    p.x_off = static_cast<uint32_t>(ns * stage);
-    smem = ns * stage + x_bytes;
+  // the deepest ring that leaves room for a neighbouring GEMV CTA on the SM, else the
+  // deepest that fits at all
+  int ns = kGemvMaxStages;
+  while (ns > 2 && ns * stage + x_bytes > co_budget) --ns;
+  if (ns * stage + x_bytes > co_budget) {
+    ns = kGemvMaxStages;
+    while (ns > 2 && ns * stage + x_bytes > kGemvMaxSmem) --ns;
   }
+  p.stages = ns;
+  p.x_off = static_cast<uint32_t>(ns * stage);
+  const size_t smem = ns * stage + x_bytes;
   if (smem > kGemvMaxSmem) return cudaErrorInvalidValue;
   return launch_pdl(kern, dim3(ctas), dim3(kGemvThreads), smem, s, p);
 }
@@ -413,13 +543,13 @@ cudaError_t launch_gemv_t(const GemvParams& p0, cudaStream_t s) {
 
 cudaError_t launch_gemv_bf16(const GemvParams& p, int x_mode, int epilogue, cudaStream_t s) {
   if (p.B < 1 || p.B > kGemvMaxB) return cudaErrorInvalidValue;
-  // streams rounded up to 1, 2, 4 or 8: the kernel's per-stream arrays are that long
+  // 1..4 streams: the ring kernel, its per-stream arrays 1, 2 or 4 long; 5..8: registers
 #define TTS_GEMV_CASE(XM, EPI)                                                                 \
   if (x_mode == XM && epilogue == EPI) {                                                       \
     if (p.B == 1) return launch_gemv_t<XM, EPI, 1>(p, s);                                      \
     if (p.B == 2) return launch_gemv_t<XM, EPI, 2>(p, s);                                      \
     if (p.B <= 4) return launch_gemv_t<XM, EPI, 4>(p, s);                                      \
-    return launch_gemv_t<XM, EPI, 8>(p, s);                                                    \
+    return launch_gemv_regs<XM, EPI>(p, s);                                                    \
   }
   TTS_GEMV_CASE(X_RMSNORM, EPI_STORE)     // qkv
   TTS_GEMV_CASE(X_F32, EPI_RESIDUAL)      // o

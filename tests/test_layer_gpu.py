@@ -43,7 +43,7 @@ SMALL_768 = dict(hidden=768, n_q_heads=4, n_kv_heads=2, capacity=512)
 SMALL_1280 = dict(hidden=1280, n_q_heads=8, n_kv_heads=2, capacity=512)
 
 
-@pytest.mark.parametrize("B,cur,shape", [(1, [4095], {}), (1, [100], {}), (4, [7, 1000, 2047, 3000], {}),
+@pytest.mark.parametrize("B,cur,shape", [(1, [4095], {}), (1, [100], {}), (2, [10, 4000], {}), (4, [7, 1000, 2047, 3000], {}),
                                          (8, [300] * 8, {}), (3, [5, 200, 511], SMALL_768),
                                          (5, [0, 1, 64, 300, 511], SMALL_1280)])
 def test_decode_layer_matches_oracle(tts, B, cur, shape):
