@@ -11,8 +11,8 @@
 //   h += a W_down^T                           GEMV <X_BF16, EPI_RESIDUAL>
 //
 // At the batch sizes of a decode step (B <= 8 here) every product is a GEMV bound by
-// streaming the weights from HBM.  For up to four streams the weights are streamed into a
-// shared-memory ring by bulk copies (gemv_bf16_kernel), for five to eight through
+// streaming the weights from HBM.  For one stream the weights are streamed into a
+// shared-memory ring by bulk copies (gemv_bf16_kernel), for two to eight through
 // registers (gemv_regs_kernel); both start loading before the dependency wait (the weights
 // are constants), stage the activations once per CTA as bf16 (the RMS norm computed there,
 // so it needs no launch of its own), accumulate each row in f32 and apply a fused
@@ -54,9 +54,10 @@ constexpr size_t kGemvMaxSmem = 220 * 1024;
 // 1-D bulk copies (complete_tx on a per-stage "full" mbarrier; the consumers release a
 // stage on its "empty" mbarrier).  The weights are constants of the model, so the
 // producer never waits for the preceding kernel: the ring fills while that kernel runs,
-// and with at most ~110 KB of shared memory and few registers (56 a thread for one or two
-// streams) the CTA fits on an SM beside a CTA of the neighbouring kernel, so consecutive
-// launches overlap their weight streams.  The consumers wait for the preceding kernel, stage the activations once as
+// and with at most ~110 KB of shared memory and few registers (56 a thread for one
+// stream) the CTA fits on an SM beside a CTA of the neighbouring kernel, so consecutive
+// launches overlap their weight streams.  The code handles up to MAXB streams; the
+// launcher uses it for one.  The consumers wait for the preceding kernel, stage the activations once as
 // bf16 (a bf16 input as is, an f32 input rounded, or the RMS norm of the f32 residual
 // stream times gamma, in f32), and accumulate in f32.
 template <int XM, int EPI, int MAXB>
@@ -298,8 +299,8 @@ __global__ void __maxnreg__(MAXB <= 2 ? 56 : 96) gemv_bf16_kernel(const GemvPara
   }
 }
 
-// Five to eight streams: eight FMAs per weight element make the ring's eight consumer
-// warps the bottleneck, so this kernel streams the weights through registers instead,
+// Two to eight streams: B FMAs per weight element make the ring's eight consumer warps
+// the bottleneck, so this kernel streams the weights through registers instead,
 // over up to two CTAs of eight warps per SM: warp w of CTA c takes output rows w + 8c,
 // w + 8c + 8 * gridDim.x, ... (gate/up row pairs for the SiLU-multiply), each row in
 // 256-element chunks, kDepth chunks in flight (about 4 KB a warp), the first issued
@@ -543,12 +544,11 @@ cudaError_t launch_gemv_t(const GemvParams& p0, cudaStream_t s) {
 
 cudaError_t launch_gemv_bf16(const GemvParams& p, int x_mode, int epilogue, cudaStream_t s) {
   if (p.B < 1 || p.B > kGemvMaxB) return cudaErrorInvalidValue;
-  // 1..4 streams: the ring kernel, its per-stream arrays 1, 2 or 4 long; 5..8: registers
+  // one stream: the ring kernel; two to eight: the register kernel (faster from two
+  // streams on, where B FMAs per weight element keep the ring's consumers busy)
 #define TTS_GEMV_CASE(XM, EPI)                                                                 \
   if (x_mode == XM && epilogue == EPI) {                                                       \
     if (p.B == 1) return launch_gemv_t<XM, EPI, 1>(p, s);                                      \
-    if (p.B == 2) return launch_gemv_t<XM, EPI, 2>(p, s);                                      \
-    if (p.B <= 4) return launch_gemv_t<XM, EPI, 4>(p, s);                                      \
     return launch_gemv_regs<XM, EPI>(p, s);                                                    \
   }
   TTS_GEMV_CASE(X_RMSNORM, EPI_STORE)     // qkv

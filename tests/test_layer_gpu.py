@@ -38,14 +38,16 @@ def _bits16(t):
 
 # The talker shapes, and two smaller layers whose row lengths split into several
 # segments of 768 / 1280 elements (hidden 768 / 1280, intermediate 3 x hidden) with
-# partial row groups at the ends of the CTAs' ranges.
+# partial row groups at the ends of the CTAs' ranges; one stream runs the ring kernel,
+# two or more the register kernel.
 SMALL_768 = dict(hidden=768, n_q_heads=4, n_kv_heads=2, capacity=512)
 SMALL_1280 = dict(hidden=1280, n_q_heads=8, n_kv_heads=2, capacity=512)
 
 
 @pytest.mark.parametrize("B,cur,shape", [(1, [4095], {}), (1, [100], {}), (2, [10, 4000], {}), (4, [7, 1000, 2047, 3000], {}),
                                          (8, [300] * 8, {}), (3, [5, 200, 511], SMALL_768),
-                                         (5, [0, 1, 64, 300, 511], SMALL_1280)])
+                                         (5, [0, 1, 64, 300, 511], SMALL_1280), (1, [300], SMALL_768),
+                                         (1, [511], SMALL_1280)])
 def test_decode_layer_matches_oracle(tts, B, cur, shape):
     w = W.workload("talker", B=B, layers=1, **shape)
     H, I, Hq, Hkv, D = w.hidden, 3 * w.hidden, w.n_q_heads, w.n_kv_heads, w.head_dim
