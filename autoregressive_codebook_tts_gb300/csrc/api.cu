@@ -523,9 +523,19 @@ tts_status tts_decode_layer(float* h, const tts_layer_weights* w, float eps, con
   g.w = w->w_qkv; g.n_out = width; g.K = H; g.B = B; g.y = qkv; g.y_stride = width; g.err = err_flag;
   cudaError_t e = launch_gemv_bf16(g, 2, 0, s);
   if (e != cudaSuccess) return from_cuda(e);
+  // One stream: the qkv GEMV's CTAs hold one slot of every SM while the attention's
+  // first CTAs start, so about 1.4 attention CTAs per SM (fewer, longer splits than the
+  // standalone default of about two) finish the layer sooner.
+  int32_t splits = n_splits;
+  if (splits == 0 && B == 1) {
+    const int pairs = d->n_kv_heads;
+    splits = (7 * sm_count() + 5 * pairs - 1) / (5 * pairs);
+    const int standalone = tts_decode_attn_default_splits(d);
+    if (splits > standalone) splits = standalone;
+  }
   st = tts_decode_step(qkv, qkv + qd, qkv + qd + kd, width, w->gamma_q, w->gamma_k, eps, rope_cs,
                        rope_max_pos, k_cache, v_cache, d, cur_len, scale, attn, sc + L.ws_off,
-                       L.total - L.ws_off, n_splits, err_flag, stream);
+                       L.total - L.ws_off, splits, err_flag, stream);
   if (st != TTS_OK) return st;
   // h += bf16(attn) W_o^T
   g = {};
