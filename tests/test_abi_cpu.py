@@ -160,3 +160,38 @@ def test_prefill_sampler_and_table_dtype_validate(tts):
     assert sample(ctr=68) == 5                   # misaligned counter
     assert tts._lib.tts_counter_advance(None, 1, None) == 1
     assert tts._lib.tts_counter_advance(P(12), 1, None) == 5
+
+
+@no_gpu
+def test_decode_layer_validates(tts):
+    P = ctypes.c_void_p
+    d = tts.kv_desc(1, 16, 8, 128, 4096)
+    size = tts.tts_decode_layer_scratch_size(d, 2048, 6144, 0)
+    assert size > tts.tts_decode_attn_workspace_size(d, 0)
+    assert tts.tts_decode_layer_scratch_size(d, 2000, 6144, 0) == 0    # hidden not a multiple of 256
+    assert tts.tts_decode_layer_scratch_size(d, 2048, 9216, 0) == 0    # intermediate above 8192
+
+    def weights(hidden=2048, inter=6144, w_qkv=16, gamma_attn=16):
+        w = tts.TtsLayerWeights()
+        w.w_qkv, w.w_o, w.w_gu, w.w_down = w_qkv, 16, 16, 16
+        w.gamma_attn, w.gamma_mlp, w.gamma_q, w.gamma_k = gamma_attn, 16, 16, 16
+        w.hidden, w.inter = hidden, inter
+        return w
+
+    def layer(h=16, w=None, desc=d, eps=1e-6, sc=256, sc_bytes=None):
+        w = weights() if w is None else w
+        return tts._lib.tts_decode_layer(P(h) if h else None, ctypes.byref(w), eps, P(16), 4096, P(16),
+                                         P(16), ctypes.byref(desc), P(16), 0.1, P(sc) if sc else None,
+                                         size if sc_bytes is None else sc_bytes, 0, None, None)
+    assert layer(h=0) == 1
+    assert layer(w=weights(w_qkv=0)) == 1
+    assert layer(w=weights(gamma_attn=0)) == 1
+    assert layer(sc=0) == 1
+    assert layer(desc=tts.kv_desc(9, 16, 8, 128, 4096)) == 2    # more than eight streams
+    assert layer(w=weights(hidden=2000)) == 2
+    assert layer(w=weights(inter=9216)) == 2
+    assert layer(eps=-1.0) == 2
+    assert layer(h=20) == 5                                        # misaligned residual stream
+    assert layer(w=weights(w_qkv=24)) == 5                         # misaligned weights
+    assert layer(sc=272) == 5                                      # scratch not 256-byte aligned
+    assert layer(sc_bytes=1024) == 6                               # scratch too small
