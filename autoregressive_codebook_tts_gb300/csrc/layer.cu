@@ -20,6 +20,7 @@
 // CTA, and so is the SiLU.  A bf16 rounding of an intermediate can therefore land one
 // step from the exact value's.
 #include <cstdint>
+#include <mutex>
 
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -456,28 +457,36 @@ template <int XM, int EPI>
 cudaError_t launch_gemv_regs(const GemvParams& p, cudaStream_t s) {
   auto kern = gemv_regs_kernel<XM, EPI>;
   const size_t smem = static_cast<size_t>(p.B) * p.K * sizeof(uint16_t);
+  // computed once per device under a lock, copied out before use
+  static std::mutex cfg_mutex;
   static int configured_for = -1;
-  static int n_sm = 1;
-  static int per_sm = 1;
+  static int cfg_n_sm = 1;
+  static int cfg_per_sm = 1;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (configured_for != dev) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(kGemvMaxB * kGemvMaxK * sizeof(uint16_t)));
-    if (e != cudaSuccess) return e;
-    if (cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n_sm < 1) {
-      cudaGetLastError();
-      n_sm = 1;
+  int n_sm, per_sm;
+  {
+    std::lock_guard<std::mutex> cfg_lock(cfg_mutex);
+    if (configured_for != dev) {
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(kGemvMaxB * kGemvMaxK * sizeof(uint16_t)));
+      if (e != cudaSuccess) return e;
+      if (cudaDeviceGetAttribute(&cfg_n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || cfg_n_sm < 1) {
+        cudaGetLastError();
+        cfg_n_sm = 1;
+      }
+      // CTAs that fit on an SM with the activation block of 8 streams x 2048
+      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&cfg_per_sm, kern, kRegWarps * 32,
+                                                        kGemvMaxB * 2048 * sizeof(uint16_t)) != cudaSuccess ||
+          cfg_per_sm < 1) {
+        cudaGetLastError();
+        cfg_per_sm = 1;
+      }
+      configured_for = dev;
     }
-    // CTAs that fit on an SM with the activation block of 8 streams x 2048
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kRegWarps * 32,
-                                                      kGemvMaxB * 2048 * sizeof(uint16_t)) != cudaSuccess ||
-        per_sm < 1) {
-      cudaGetLastError();
-      per_sm = 1;
-    }
-    configured_for = dev;
+    n_sm = cfg_n_sm;
+    per_sm = cfg_per_sm;
   }
   int ctas = (p.n_out + kRegWarps - 1) / kRegWarps;
   if (ctas > per_sm * n_sm) ctas = per_sm * n_sm;
@@ -492,20 +501,26 @@ cudaError_t launch_gemv_t(const GemvParams& p0, cudaStream_t s) {
   int nseg = (p.K + kSegMax - 1) / kSegMax;
   while (p.K % nseg != 0 || (p.K / nseg) % 256 != 0) ++nseg;
   p.seg = p.K / nseg;
+  // computed once per device under a lock, copied out before use
+  static std::mutex cfg_mutex;
   static int configured_for = -1;
-  static int n_sm = 1;
-  static size_t co_budget = kCoResidentSmem;
+  static int cfg_n_sm = 1;
+  static size_t cfg_co_budget = kCoResidentSmem;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
+  int n_sm;
+  size_t co_budget;
+  {
+  std::lock_guard<std::mutex> cfg_lock(cfg_mutex);
   if (configured_for != dev) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kGemvMaxSmem));
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
-    if (cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n_sm < 1) {
+    if (cudaDeviceGetAttribute(&cfg_n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || cfg_n_sm < 1) {
       cudaGetLastError();
-      n_sm = 1;
+      cfg_n_sm = 1;
     }
     // dynamic shared memory that still lets two CTAs (of this or a neighbouring GEMV)
     // share an SM: half the SM's shared memory less the per-CTA reservation and the
@@ -516,11 +531,14 @@ cudaError_t launch_gemv_t(const GemvParams& p0, cudaStream_t s) {
         cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) == cudaSuccess &&
         cudaFuncGetAttributes(&fa, kern) == cudaSuccess && per_sm > 0) {
       const long long b = per_sm / 2 - reserved - static_cast<long long>(fa.sharedSizeBytes);
-      co_budget = b > 0 ? static_cast<size_t>(b) & ~static_cast<size_t>(127) : kCoResidentSmem;
+      cfg_co_budget = b > 0 ? static_cast<size_t>(b) & ~static_cast<size_t>(127) : kCoResidentSmem;
     } else {
       cudaGetLastError();
     }
     configured_for = dev;
+  }
+  n_sm = cfg_n_sm;
+  co_budget = cfg_co_budget;
   }
   const int ctas = p.n_out < n_sm ? p.n_out : n_sm;
   const size_t stage = static_cast<size_t>(kRowWarps) * p.seg * 2;

@@ -14,6 +14,7 @@
 // exponential is this file's own (a degree-9 Taylor polynomial of 2^f, f in [0, 1),
 // scaled by 2^floor(x)), not the math library's.
 #include <cstdint>
+#include <mutex>
 
 #include <cuda_runtime.h>
 
@@ -246,15 +247,19 @@ __global__ void counter_advance_kernel(uint64_t* counter, uint64_t by) {
 
 cudaError_t launch_sample(const SampleParams& p, cudaStream_t s) {
   const size_t smem = static_cast<size_t>(p.V) * sizeof(float);
+  static std::mutex cfg_mutex;  // launches may come from several host threads
   static int configured_for = -1;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (configured_for != dev) {
-    e = cudaFuncSetAttribute(sample_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(TTS_MAX_SAMPLE_VOCAB * sizeof(float)));
-    if (e != cudaSuccess) return e;
-    configured_for = dev;
+  {
+    std::lock_guard<std::mutex> cfg_lock(cfg_mutex);
+    if (configured_for != dev) {
+      e = cudaFuncSetAttribute(sample_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(TTS_MAX_SAMPLE_VOCAB * sizeof(float)));
+      if (e != cudaSuccess) return e;
+      configured_for = dev;
+    }
   }
   return launch_pdl(sample_kernel, dim3(p.B), dim3(kSampleThreads), smem, s, p);
 }
