@@ -255,6 +255,25 @@ def timed_replays(g, steps, torch, stream=None):
     return e0.elapsed_time(e1) / 1e3
 
 
+class CpuClock:
+    """Wall time and the process's CPU time over a timed region of the oracle.  `cores` is
+    CPU time / wall time rounded (at least 1): the host threads the oracle actually kept
+    busy, e.g. numpy's BLAS threads in its matrix products."""
+
+    def __enter__(self):
+        self.w0, self.c0 = time.perf_counter(), time.process_time()
+        return self
+
+    def __exit__(self, *exc):
+        self.wall = time.perf_counter() - self.w0
+        self.cpu = time.process_time() - self.c0
+        return False
+
+    @property
+    def cores(self):
+        return max(1, round(self.cpu / self.wall)) if self.wall > 0 else 1
+
+
 def cpu_oracle_sample(state, w, cur_len, seconds):
     """The oracle as it stands, single-threaded, on a bounded sample of the workload:
     the frame-input composition and the fused decode step of layer 0 (same bytes as on
@@ -287,19 +306,19 @@ def cpu_oracle_sample(state, w, cur_len, seconds):
     per_layer, _, embed = step_bytes(w, [int(c) for c in cur])
     done_bytes = 0
     reps = 0
-    t0 = time.perf_counter()
-    while True:
-        oracle.frame_embed(tabs, ids, ov)
-        oracle.decode_step(q, k, v, gq, gk, np.float32(w.eps), w.rope_base, hk, hv, lay, cur,
-                           1.0 / math.sqrt(w.head_dim))
-        done_bytes += embed + per_layer
-        reps += 1
-        if time.perf_counter() - t0 >= seconds:
-            break
-    dt = time.perf_counter() - t0
+    with CpuClock() as clk:
+        while True:
+            oracle.frame_embed(tabs, ids, ov)
+            oracle.decode_step(q, k, v, gq, gk, np.float32(w.eps), w.rope_base, hk, hv, lay, cur,
+                               1.0 / math.sqrt(w.head_dim))
+            done_bytes += embed + per_layer
+            reps += 1
+            if time.perf_counter() - clk.w0 >= seconds:
+                break
+    dt = clk.wall
     lens = f"cur_len {cur_len}" if w.B == 1 else f"its cur_len mix ({int(cur.min())}..{int(cur.max())})"
     return done_bytes / dt / 1e9, (f"{reps} x (frame-input composition + layer-0 fused decode step) "
-                                   f"of the {w.name} workload at {lens}, {dt:.1f} s")
+                                   f"of the {w.name} workload at {lens}, {dt:.1f} s"), clk.cores
 
 
 def max_over_ranks(values, world, device=None):
@@ -472,8 +491,8 @@ def run_native(args, rank, world):
     if sweep is not None:
         res["sweep_cur_len"] = sweep
     if rank == 0 and not args.no_cpu_baseline:
-        gbs, sample = cpu_oracle_sample(state, w, args.cur_len, args.cpu_seconds)
-        res["cpu_baseline"] = {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+        gbs, sample, cores = cpu_oracle_sample(state, w, args.cur_len, args.cpu_seconds)
+        res["cpu_baseline"] = {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
                                "sample": sample}
     return res
 
@@ -720,10 +739,10 @@ def run_reference_predictor(args, world):
 
     for _ in range(args.warmup):
         step()
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        step()
-    dt = time.perf_counter() - t0
+    with CpuClock() as clk:
+        for _ in range(args.steps):
+            step()
+    dt = clk.wall
     value = B * args.steps / dt
     return {
         "impl": "reference",
@@ -733,8 +752,8 @@ def run_reference_predictor(args, world):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)",
         "data": "synthetic (seeded)",
         "config": {"workload": f"predictor: B={B} streams, {L} layers (same shapes as the native arm)",
-                   "parallelism": "single host thread"},
-        "cpu_baseline": {"value": round(value, 3), "unit": "frame steps/s", "cores": 1, "kind": "oracle",
+                   "parallelism": "host threads of the oracle (see cpu_baseline.cores)"},
+        "cpu_baseline": {"value": round(value, 3), "unit": "frame steps/s", "cores": clk.cores, "kind": "oracle",
                          "sample": "each step: one whole predictor frame of all streams (fixed codes)"},
         "e2e": {"value": round(value, 3), "unit": "frame steps/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
@@ -867,10 +886,10 @@ def run_reference_prefill(args, world):
 
     for _ in range(args.warmup):
         step()
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        step()
-    dt = time.perf_counter() - t0
+    with CpuClock() as clk:
+        for _ in range(args.steps):
+            step()
+    dt = clk.wall
     # one step is one layer of the 28: positions per second of the whole prompt
     value = B * T * args.steps / (dt * w.layers)
     sample = f"each step: one layer's prefill of {T} positions from {start} (1 of {w.layers} layers)"
@@ -882,10 +901,68 @@ def run_reference_prefill(args, world):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)",
         "data": "synthetic (seeded)",
         "config": {"workload": f"prefill: talker shapes, B={B}, {T} prompt positions from {start}",
-                   "parallelism": "single host thread"},
-        "cpu_baseline": {"value": round(value, 3), "unit": "positions/s", "cores": 1,
+                   "parallelism": "host threads of the oracle (see cpu_baseline.cores)"},
+        "cpu_baseline": {"value": round(value, 3), "unit": "positions/s", "cores": clk.cores,
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 3), "unit": "positions/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def run_reference_layer(args, world):
+    """The oracle's whole talker decode layer (bf16 weights, same shapes and cur_len as
+    the native layer arm) as the reference arm's step: one layer of the frame."""
+    import numpy as np
+    import torch
+    from autoregressive_codebook_tts_gb300 import workloads as W
+    import oracle
+    B = args.layer_streams
+    w = W.workload("talker", B=B)
+    H, Hq, Hkv, D = w.hidden, w.n_q_heads, w.n_kv_heads, w.head_dim
+    I = 3 * H
+    g = torch.Generator().manual_seed(0)
+    bits = lambda r, c: ((torch.randn(r, c, generator=g) * 0.02).to(torch.bfloat16)
+                         .view(torch.int16).numpy().view(np.uint16))
+    wts = dict(w_qkv=bits((Hq + 2 * Hkv) * D, H), w_o=bits(H, Hq * D), w_gu=bits(2 * I, H),
+               w_down=bits(H, I), gamma_attn=(torch.rand(H, generator=g) + 0.5).numpy(),
+               gamma_mlp=(torch.rand(H, generator=g) + 0.5).numpy(),
+               gamma_q=(torch.rand(D, generator=g) + 0.5).numpy(),
+               gamma_k=(torch.rand(D, generator=g) + 0.5).numpy())
+    cur_list = [args.cur_len] * B
+    K, V = W.cache(w, cur_list, seed=7, poison=False)
+    kc, vc = K.numpy().copy(), V.numpy().copy()
+    lay = oracle.KvLayout(B, Hkv, D, w.capacity, w.kv_dtype)
+    cur = np.array(cur_list, np.int32)
+    h0 = torch.randn(B, H, generator=g).numpy()
+
+    def step():
+        oracle.decode_layer(h0.copy(), wts, kc, vc, lay, cur, np.float32(w.eps), w.rope_base,
+                            1.0 / math.sqrt(D))
+
+    for _ in range(args.warmup):
+        step()
+    with CpuClock() as clk:
+        for _ in range(args.steps):
+            step()
+    dt = clk.wall
+    weights = 2 * ((Hq + 2 * Hkv) * D * H + H * Hq * D + 2 * I * H + H * I)
+    per_layer, _, _ = step_bytes(w, cur_list)
+    value = (weights + per_layer) * args.steps / dt / 1e9
+    sample = (f"each step: one whole decode layer of the talker frame (1 of {w.layers} layers), "
+              f"B={B}, cur_len {args.cur_len}")
+    return {
+        "impl": "reference",
+        "metric": "talker frame GB/s (weights + KV, % of HBM peak); frame steps/sec",
+        "value": round(value, 5), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)",
+        "data": "synthetic (seeded; random-init bf16 weights)",
+        "config": {"workload": f"talker layers: B={B} streams, hidden {H}, intermediate {I}, "
+                               f"16/8 heads, head_dim {D}, f32 KV, capacity {w.capacity}, "
+                               f"cur_len {args.cur_len}", "parallelism": "host threads of the oracle (see cpu_baseline.cores)"},
+        "cpu_baseline": {"value": round(value, 5), "unit": "GB/s", "cores": clk.cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 5), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
 
@@ -901,6 +978,8 @@ def run_reference(args, rank, world):
         return run_reference_prefill(args, world)
     if args.workload == "predictor":
         return run_reference_predictor(args, world)
+    if args.workload == "layer":
+        return run_reference_layer(args, world)
     w = W.workload(args.workload)
     cur_list = [args.cur_len] * w.B if args.workload == "talker" else [int(c) for c in W.cur_lens(w, 0)]
     cur = np.array(cur_list, np.int32)
@@ -936,10 +1015,10 @@ def run_reference(args, rank, world):
 
     for _ in range(args.warmup):
         step()
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        step()
-    dt = time.perf_counter() - t0
+    with CpuClock() as clk:
+        for _ in range(args.steps):
+            step()
+    dt = clk.wall
     value = sample_bytes * args.steps / dt / 1e9
     sample = (f"each step: frame-input composition + one layer's fused decode step of the "
               f"{w.name} workload (1 of {w.layers} layers)")
@@ -950,8 +1029,8 @@ def run_reference(args, rank, world):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)",
         "data": "synthetic (seeded)",
         "config": {"workload": f"{w.name} (same shapes as the native arm)", "B": w.B,
-                   "layers": w.layers, "parallelism": "single host thread"},
-        "cpu_baseline": {"value": round(value, 5), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                   "layers": w.layers, "parallelism": "host threads of the oracle (see cpu_baseline.cores)"},
+        "cpu_baseline": {"value": round(value, 5), "unit": "GB/s", "cores": clk.cores, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": round(value, 5), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
