@@ -275,9 +275,10 @@ class CpuClock:
 
 
 def cpu_oracle_sample(state, w, cur_len, seconds):
-    """The oracle as it stands, single-threaded, on a bounded sample of the workload:
+    """The oracle as it stands, on a bounded sample of the workload:
     the frame-input composition and the fused decode step of layer 0 (same bytes as on
-    the device), repeated for about `seconds`.  Returns (GB/s, sample description)."""
+    the device), repeated for about `seconds`.  Returns (GB/s, sample description, host
+    threads kept busy)."""
     import numpy as np
     import oracle
     import torch
