@@ -614,6 +614,33 @@ def test_top_k_draws_follow_the_tempered_softmax():
     assert chi2 < 16.3  # 3 degrees of freedom, p = 0.001
 
 
+def test_top_k_ties_at_the_threshold_take_the_lowest_indices():
+    """Equal logits at the k-th place: the candidates are the lowest-index ones, equal
+    logits are drawn equally often, and an all-equal row is uniform over indices 0..k-1
+    (chi-square, fixed seeds)."""
+    logits = np.array([[1.0, 5.0, 3.0, 3.0, 3.0, 3.0, 0.0],
+                       [2.0, 2.0, 2.0, 2.0, 2.0, 2.0, 2.0]], np.float32)
+    k, T, n = 3, 2.0, 4000
+    counts = np.zeros((2, 7))
+    for c in range(n):
+        ids = oracle.sample(logits, k, T, 5, c)
+        counts[0, ids[0]] += 1
+        counts[1, ids[1]] += 1
+    assert counts[0, [0, 4, 5, 6]].sum() == 0 and counts[1, 3:].sum() == 0
+    w = np.exp(np.array([5.0, 3.0, 3.0]) / T)
+    for row, p in ((0, w / w.sum()), (1, np.full(3, 1.0 / 3.0))):
+        obs = counts[row, [1, 2, 3]] if row == 0 else counts[row, :3]
+        chi2 = float(((obs - n * p) ** 2 / (n * p)).sum())
+        assert chi2 < 13.8  # 2 degrees of freedom, p = 0.001
+
+
+def test_sample_of_a_row_without_a_finite_logit_is_index_zero():
+    lg = np.full((2, 16), -np.inf, np.float32)
+    lg[1, :] = np.nan
+    assert list(oracle.sample(lg, 0, 1.0, 1, 0)) == [0, 0]
+    assert list(oracle.sample(lg, 4, 0.8, 1, 0)) == [0, 0]
+
+
 # ---------------------------------------------------------------------------
 # Whole decode layer with bf16 weights (NEXT-2)
 # ---------------------------------------------------------------------------
