@@ -100,12 +100,15 @@ def _c(a, dtype):
 # bf16 helpers
 # ---------------------------------------------------------------------------
 def bf16_rne(x: float) -> int:
-    """bf16 bit pattern of one f32 value, integer round-to-nearest-even."""
+    """bf16 bit pattern of one f32 value, integer round-to-nearest-even ("minicpm-o-4.5
+    ... docs/optimizations.md", core table: the fused kernels reproduce the reference
+    rounding with integer round-to-nearest-even)."""
     return int(_load().oracle_bf16_rne(ctypes.c_float(float(np.float32(x)))))
 
 
 def bf16_rne_array(x) -> np.ndarray:
-    """Elementwise bf16 RNE of an f32 array, as uint16 (one oracle call per element)."""
+    """Elementwise bf16 RNE of an f32 array, as uint16 (one oracle call per element;
+    the rounding of ``bf16_rne``)."""
     x = _c(x, np.float32)
     lib = _load()
     out = np.empty(x.shape, np.uint16)
@@ -116,7 +119,10 @@ def bf16_rne_array(x) -> np.ndarray:
 
 
 def bf16_bits_to_f32(h) -> np.ndarray:
-    """Exact widening of bf16 bit patterns (uint16) to f32."""
+    """Exact widening of bf16 bit patterns (uint16) to f32: the bf16 bits become the high
+    half of the f32 (how a bf16 table entry or cache row enters f32 arithmetic; "qwentts.cpp
+    ... src/pipeline-tts.h", on-device AR input assembly: tables of any type read through
+    get_rows)."""
     h = np.asarray(h, dtype=np.uint16)
     return (h.astype(np.uint32) << 16).view(np.float32)
 
@@ -149,7 +155,10 @@ def frame_embed(tables, ids, overlay=None):
 # a2: per-head RMSNorm + RoPE
 # ---------------------------------------------------------------------------
 def rms_norm_rope(x, gamma, eps, pos, base):
-    """x: [B][H][D] f32 -> normed and rotated copy (f32), per the a2 definition."""
+    """x: [B][H][D] f32 -> normed and rotated copy (f32): per-head RMSNorm, then
+    rotate-half RoPE at pos[b] ("minicpm-o-4.5 ... docs/optimizations.md", core table,
+    fused "q/k norm + RoPE"; the formulas are the readings stated in ``oracle.cpp``),
+    in double, rounded to f32 once."""
     x = _c(x, np.float32)
     B, H, D = x.shape
     gamma = _c(gamma, np.float32)
@@ -161,6 +170,8 @@ def rms_norm_rope(x, gamma, eps, pos, base):
 
 
 def rope_angle(pos: int, i: int, head_dim: int, base: float):
+    """(cos, sin) of theta = pos * base^(-2i/head_dim) in double: the RoPE angle of
+    frequency i (the rotation of ``rms_norm_rope``)."""
     cs = np.empty(2, np.float64)
     _load().oracle_rope_angle(int(pos), int(i), int(head_dim), float(base), _ptr(cs))
     return float(cs[0]), float(cs[1])
@@ -191,7 +202,9 @@ class KvLayout:
 
 
 def kv_set_rows(k, v, k_cache, v_cache, layout: KvLayout, dst_pos):
-    """Write k[b], v[b] ([B][Hkv][D] f32) into the caches at dst_pos[b], in place.
+    """Write k[b], v[b] ([B][Hkv][D] f32) into the caches at dst_pos[b], in place
+    ("qwentts.cpp ... src/pipeline-tts.h", fixed topology + set_rows section: KV writes
+    carry their destination rows as data; bf16 caches round by RNE).
 
     Caches are numpy arrays (f32, or uint16 holding bf16 bits).  Returns the
     skipped-write flag.
@@ -210,7 +223,10 @@ def kv_set_rows(k, v, k_cache, v_cache, layout: KvLayout, dst_pos):
 
 
 def decode_attn(q, k_cache, v_cache, layout: KvLayout, n_valid, scale, want_weights=False):
-    """Single-query GQA attention over [0, n_valid[b]) per stream, double precision.
+    """Single-query GQA attention over [0, n_valid[b]) per stream, double precision
+    ("qwentts.cpp ... src/pipeline-tts.h", persistent arenas and KV cache sections: the
+    decode reads the [0, cur_len+1) window, the padded tail masked by -inf, so positions
+    past n_valid carry no weight).
 
     q: [B][Hq][D] f32.  Returns (out [B][Hq][D] f32, weights or None, clamped flag).
     """
@@ -232,9 +248,10 @@ def decode_attn(q, k_cache, v_cache, layout: KvLayout, n_valid, scale, want_weig
 # ---------------------------------------------------------------------------
 def decode_step(q, k, v, gamma_q, gamma_k, eps, base, k_cache, v_cache, layout: KvLayout,
                 cur_len, scale):
-    """One layer of one decode step for B streams, in the order the pages give:
-    q/k RMSNorm + RoPE at position cur_len, write the new K/V row at cur_len, attend
-    over [0, cur_len + 1).  Mutates the caches; returns the attention output."""
+    """One layer of one decode step for B streams, in the order the pages give
+    ("qwentts.cpp ... src/pipeline-tts.h", KV cache section): q/k RMSNorm + RoPE at
+    position cur_len, write the new K/V row at cur_len, attend over [0, cur_len + 1).
+    Mutates the caches; returns the attention output."""
     cur_len = _c(cur_len, np.int32)
     qn = rms_norm_rope(q, gamma_q, eps, cur_len, base)
     kn = rms_norm_rope(k, gamma_k, eps, cur_len, base)
@@ -333,7 +350,8 @@ def philox4x64_10(counter, key):
 def uniform_f32(seed, counter, b):
     """The sampler's uniform for stream b at `counter`: the top 24 bits of the first
     Philox4x64-10 output for counter words (counter, b, 0, 0) and key (seed, 0), times
-    2^-24 (exact in f32, in [0, 1))."""
+    2^-24 (exact in f32, in [0, 1)).  The counter RNG is the "one-kernel counter RNG" of
+    "minicpm-o-4.5 ... docs/optimizations.md" (options table, "Lean Talker frame")."""
     x = philox4x64_10([counter, b, 0, 0], [seed, 0])[0]
     return np.float32((x >> 40) * (1.0 / (1 << 24)))
 
@@ -346,7 +364,9 @@ def exp2_f32(x):
     """2^x for an f32 x <= 0, in f32 operations in a fixed order: 0 below -126; else
     n = floor(x), f = x - n (exact), p = Horner over the degree-9 Taylor polynomial of
     2^f (each product and sum rounded to f32, no fused multiply-add), times 2^n
-    (exact)."""
+    (exact).  The sampler's weights use it ("qwentts.cpp" pages, in-graph sampler), so
+    that both sides of the parity tests take every token decision in the same f32
+    arithmetic."""
     x = np.float32(x)
     if not x >= np.float32(-126.0):  # also NaN
         return np.float32(0.0)
@@ -368,7 +388,10 @@ def sample(logits, top_k, temperature, seed, counter):
     that order in f32; r = f32(u * S) with u = uniform_f32(seed, counter, b); the result
     is the candidate i of the first running sum (in f32, same order) above r, or the
     last candidate if none is.  NaN logits count as -inf; when the top candidate is not
-    finite the result is that candidate."""
+    finite the result is that candidate.  This is the in-graph sampler of the "qwentts.cpp"
+    pages (the code-predictor frame unroll keeps its sampler on the device) on the counter
+    RNG of "minicpm-o-4.5 ... docs/optimizations.md" (options table, "Lean Talker
+    frame"); the tie and rounding rules are this library's readings."""
     lg = np.array(logits, dtype=np.float32, copy=True)
     lg[np.isnan(lg)] = -np.inf
     B, V = lg.shape
@@ -404,13 +427,16 @@ def sample(logits, top_k, temperature, seed, counter):
 # A whole decode layer with bf16 weights
 # ---------------------------------------------------------------------------
 def bf16_round(x) -> np.ndarray:
-    """f32 values rounded to bf16 by round-to-nearest-even, returned as f32."""
+    """f32 values rounded to bf16 by round-to-nearest-even, returned as f32 (the
+    integer RNE of "minicpm-o-4.5 ... docs/optimizations.md", core table)."""
     return bf16_bits_to_f32(bf16_rne_array(np.asarray(x, np.float32)))
 
 
 def rmsnorm_bf16(h, gamma, eps):
     """x = h * (mean(h^2) + eps)^-1/2 * gamma per row, in double, rounded once to bf16
-    (returned as f32 holding bf16 values).  h: [B][H] f32, gamma: [H] f32."""
+    (returned as f32 holding bf16 values).  h: [B][H] f32, gamma: [H] f32.
+    ("minicpm-o-4.5 ... docs/optimizations.md", core table: residual add + RMSNorm
+    fused, integer RNE; the RMSNorm form is this library's reading.)"""
     h64 = np.asarray(h, np.float64)
     r = 1.0 / np.sqrt((h64 * h64).mean(axis=1, keepdims=True) + float(eps))
     y = (h64 * r * np.asarray(gamma, np.float64)).astype(np.float32)
@@ -419,14 +445,17 @@ def rmsnorm_bf16(h, gamma, eps):
 
 def gemv_bf16(x, w_bits):
     """y[b][n] = sum_k x[b][k] * W[n][k] with x holding bf16 values (f32 arrays) and W
-    bf16 bit patterns [N][K]; the products and their sum are exact in float64, rounded
-    once to f32."""
+    bf16 bit patterns [N][K]: every product is exact in float64 (two 8-bit significands),
+    the sum carries double precision (a library matrix product, ~1e-16 relative), and the
+    result is rounded once to f32.  (The QKV / O / gate-up / down projections of a bf16
+    decode layer, "minicpm-o-4.5 ... docs/optimizations.md", core table.)"""
     W = bf16_bits_to_f32(w_bits).astype(np.float64)
     return (np.asarray(x, np.float64) @ W.T).astype(np.float32)
 
 
 def silu_mul_bf16(gate, up):
-    """a = silu(gate) * up = gate / (1 + e^-gate) * up in double, rounded once to bf16."""
+    """a = silu(gate) * up = gate / (1 + e^-gate) * up in double, rounded once to bf16
+    ("minicpm-o-4.5 ... docs/optimizations.md", core table: SiLU-multiply fused)."""
     g = np.asarray(gate, np.float64)
     a = g / (1.0 + np.exp(-g)) * np.asarray(up, np.float64)
     return bf16_round(a.astype(np.float32))
@@ -439,7 +468,12 @@ def decode_layer(h, wts, k_cache, v_cache, layout: KvLayout, cur_len, eps, base,
     [0, I) and [I, 2I));  h = h + silu_mul(gate, up)_bf16 W_down^T.  The residual adds
     are single f32 additions.  wts: dict with gamma_attn, gamma_mlp (f32 [H]), gamma_q,
     gamma_k (f32 [D]), w_qkv [(Hq + 2 Hkv) D][H], w_o [H][Hq D], w_gu [2I][H],
-    w_down [H][I] (bf16 bit patterns).  Mutates h and the caches; returns h."""
+    w_down [H][I] (bf16 bit patterns).  Mutates h and the caches; returns h.
+    ("minicpm-o-4.5 ... docs/optimizations.md", core table: fused residual add +
+    RMSNorm, q/k norm + RoPE and SiLU-multiply with integer RNE; "qwentts.cpp ...
+    src/pipeline-tts.h", KV cache section, for the decode step.  The layer's structure
+    and rounding points are this library's plainest reading of a bf16 transformer
+    layer.)"""
     B, H = h.shape
     D = layout.head_dim
     Hkv = layout.n_kv_heads
