@@ -256,7 +256,8 @@ tts_status tts_decode_step(const float* q, const float* k, const float* v, int64
  * kernel on `stream`) and then runs the step.  All calls share the one array: calls
  * that can overlap on the GPU (different streams, or different threads) race on it and
  * must be serialised by the caller.  Arguments and results are otherwise those of
- * tts_decode_step.
+ * tts_decode_step, and so is the operation (the "qwentts.cpp ... src/pipeline-tts.h"
+ * KV cache section's decode step, cited there).
  * ------------------------------------------------------------------------- */
 tts_status tts_decode_step_noalloc(const float* q, const float* k, const float* v,
                                    int64_t row_stride, const float* gamma_q,
