@@ -195,3 +195,20 @@ def test_decode_layer_validates(tts):
     assert layer(w=weights(w_qkv=24)) == 5                         # misaligned weights
     assert layer(sc=272) == 5                                      # scratch not 256-byte aligned
     assert layer(sc_bytes=1024) == 6                               # scratch too small
+
+
+def test_binding_constants_match_the_header(tts):
+    """The binding re-declares the header's flag bits, dtype codes and limits; they must
+    be the header's values, and the library's status names must match the enum."""
+    src = open(os.path.join(ROOT, "include", "tts_decode.h")).read()
+    defines = {m.group(1): int(m.group(2)) for m in re.finditer(r"#define (TTS_[A-Z0-9_]+) (\d+)u?\b", src)}
+    assert tts.TTS_MAX_TABLES == defines["TTS_MAX_TABLES"]
+    assert tts.TTS_KV_PREFETCH_BEFORE_WAIT == defines["TTS_KV_PREFETCH_BEFORE_WAIT"]
+    for name in ("ID_RANGE", "POS_RANGE", "PAGE", "NVALID", "TIMEOUT"):
+        assert getattr(tts, "EFLAG_" + name) == defines["TTS_EFLAG_" + name]
+    assert tts._lib.tts_abi_version() == defines["TTS_ABI_VERSION"]
+    assert tts._lib.tts_abi_min_version() == defines["TTS_ABI_MIN_VERSION"]
+    dt = dict(re.findall(r"(TTS_F32|TTS_BF16) = (\d+)", src))
+    assert (tts.TTS_F32, tts.TTS_BF16) == (int(dt["TTS_F32"]), int(dt["TTS_BF16"]))
+    for name, code in re.findall(r"\b(TTS_(?:OK|ERR_[A-Z]+)) = (\d+)", src):
+        assert tts._lib.tts_status_str(int(code)).decode() == name
