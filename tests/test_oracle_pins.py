@@ -375,6 +375,85 @@ def test_attn_clamps_invalid_n_valid():
     assert flag == 1 and flag2 == 0 and np.array_equal(out, ref)
 
 
+# Brute-force pins: the oracle's attention against a per-element loop written
+# independently in oracle/brute.py (its own addressing, softmax without max
+# subtraction, Python doubles).  The oracle rounds its double result to f32 once, so
+# the two agree to about one f32 rounding.
+BRUTE_RTOL = 2e-7
+
+
+def _assert_brute(out, ref):
+    ref = np.asarray(ref, np.float64)
+    err = np.abs(out.astype(np.float64) - ref) / np.maximum(np.abs(ref).max(-1, keepdims=True), 1e-30)
+    assert err.max() <= BRUTE_RTOL, err.max()
+
+
+def test_attn_matches_brute_force_on_the_tiny_workload():
+    """The tiny workload's own shapes: 1 stream, 16 q / 8 kv heads, head_dim 128, f32
+    cache of 256 slots, window [0, 38) (cur_len 37 after its row is written), the
+    rest of the cache poisoned with NaN."""
+    from autoregressive_codebook_tts_gb300 import workloads as W
+    from oracle.brute import attn_brute
+    w = W.workload("tiny")
+    n_valid = np.array([38], np.int32)
+    K, V = W.cache(w, n_valid.tolist(), seed=21)
+    kc, vc = K.numpy(), V.numpy()
+    q = W.qkv(w.B, w.n_q_heads, w.n_kv_heads, w.head_dim, seed=22)[1].numpy().reshape(
+        w.B, w.n_q_heads, w.head_dim).copy()
+    scale = 1.0 / math.sqrt(w.head_dim)
+    lay = oracle.KvLayout(w.B, w.n_kv_heads, w.head_dim, w.capacity, "f32")
+    out, _, flag = oracle.decode_attn(q, kc, vc, lay, n_valid, scale)
+    assert flag == 0
+    _assert_brute(out, attn_brute(q, kc, vc, n_valid, scale))
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(4, 4), (4, 2), (8, 2)])
+def test_attn_matches_brute_force_gqa_groups(Hq, Hkv):
+    """head_dim 4, windows of 1..64 rows, GQA groups 1, 2 and 4."""
+    from oracle.brute import attn_brute
+    rng = np.random.default_rng(31 + Hq + Hkv)
+    B, D, cap = 4, 4, 64
+    q, kc, vc = _rand_case(rng, B, Hq, Hkv, D, cap)
+    n_valid = np.array([1, 2, 33, 64], np.int32)
+    out, _, flag = oracle.decode_attn(q, kc, vc, oracle.KvLayout(B, Hkv, D, cap), n_valid, 0.5)
+    assert flag == 0
+    _assert_brute(out, attn_brute(q, kc, vc, n_valid, 0.5))
+
+
+def test_attn_matches_brute_force_paged_bf16_with_unused_entries_minus_one():
+    """A paged bf16 pool of shuffled 16-slot pages; block-table entries past each
+    stream's window hold -1 (they are never read, so neither side may touch them)."""
+    from oracle.brute import attn_brute
+    rng = np.random.default_rng(41)
+    B, Hq, Hkv, D, ps, n_pages = 2, 4, 2, 4, 16, 9
+    cap = 4 * ps
+    bt = np.array([[6, 1, 8, -1], [2, 7, 0, 4]], np.int32)
+    n_valid = np.array([37, 64], np.int32)
+    q = rng.standard_normal((B, Hq, D)).astype(np.float32)
+    pool = [torch.from_numpy(rng.standard_normal((n_pages, Hkv, ps, D)).astype(np.float32))
+            .to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16) for _ in range(2)]
+    lay = oracle.KvLayout(B, Hkv, D, cap, "bf16", paged=True, page_size=ps, n_pages=n_pages,
+                          block_table=bt)
+    out, _, flag = oracle.decode_attn(q, pool[0], pool[1], lay, n_valid, 0.5)
+    assert flag == 0
+    _assert_brute(out, attn_brute(q, pool[0], pool[1], n_valid, 0.5, kv_dtype="bf16", paged=True,
+                                  page_size=ps, block_table=bt))
+
+
+def test_brute_force_pin_catches_a_swapped_gqa_map():
+    """The brute-force comparison is sharp enough to see a plausible mistake: feeding
+    the oracle the kv heads in the opposite order (a wrong GQA map) fails it."""
+    from oracle.brute import attn_brute
+    rng = np.random.default_rng(43)
+    B, Hq, Hkv, D, cap = 1, 4, 2, 4, 16
+    q, kc, vc = _rand_case(rng, B, Hq, Hkv, D, cap)
+    n_valid = np.array([16], np.int32)
+    out, _, _ = oracle.decode_attn(q, kc[:, ::-1].copy(), vc[:, ::-1].copy(),
+                                   oracle.KvLayout(B, Hkv, D, cap), n_valid, 0.5)
+    with pytest.raises(AssertionError):
+        _assert_brute(out, attn_brute(q, kc, vc, n_valid, 0.5))
+
+
 # ---------------------------------------------------------------------------
 # Compositions
 # ---------------------------------------------------------------------------
