@@ -150,6 +150,10 @@ extern "C" {
 
 int32_t tts_abi_version(void) { return TTS_ABI_VERSION; }
 int32_t tts_abi_min_version(void) { return TTS_ABI_MIN_VERSION; }
+tts_status tts_abi_check(int32_t caller_version) {
+  return (caller_version >= TTS_ABI_MIN_VERSION && caller_version <= TTS_ABI_VERSION) ? TTS_OK
+                                                                                      : TTS_ERR_ABI;
+}
 
 const char* tts_status_str(int32_t s) {
   switch (s) {
@@ -427,7 +431,7 @@ tts_status tts_prefill_step(float* q, const float* k, const float* v, int64_t ro
 
 tts_status tts_sample(const float* logits, int64_t logits_stride, int32_t B, int32_t vocab,
                       int32_t top_k, float temperature, uint64_t seed, const uint64_t* counter,
-                      int32_t* out_ids, int64_t out_stride, void* stream) {
+                      uint32_t draw, int32_t* out_ids, int64_t out_stride, void* stream) {
   if (logits == nullptr || out_ids == nullptr || (top_k > 1 && counter == nullptr)) return TTS_ERR_NULL;
   if (B < 1 || B > 65535 || vocab < 1 || vocab > TTS_MAX_SAMPLE_VOCAB || logits_stride < vocab ||
       out_stride < 1 || top_k < 0 || top_k > TTS_MAX_TOP_K || top_k > vocab)
@@ -445,6 +449,7 @@ tts_status tts_sample(const float* logits, int64_t logits_stride, int32_t B, int
   p.c = top_k > 1 ? static_cast<float>(1.4426950408889634 / static_cast<double>(temperature)) : 0.f;
   p.seed = seed;
   p.counter = counter;
+  p.draw = draw;
   p.out = out_ids;
   p.out_stride = out_stride;
   return from_cuda(launch_sample(p, as_stream(stream)));

@@ -42,6 +42,8 @@
 //     the preceding kernel has finished.
 //   * Every mbarrier wait is bounded (kWaitLimitCycles); on expiry TTS_EFLAG_TIMEOUT is
 //     set, the copies already issued are waited for (bounded), and the CTA finishes.
+#include <mutex>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -1175,74 +1177,88 @@ decode_attn_kernel(const AttnParams p) {
 constexpr int kMaxCluster = 16;
 
 constexpr int kMaxListStreams = 2048;  // persistent mode keeps B + 1 prefix sums in smem
+constexpr int kMaxDevices = 64;
 
 template <typename KvT, int D, int G, bool FUSED>
 cudaError_t launch_one(const AttnParams& p_in, cudaStream_t s) {
   using C = Cfg<KvT, D, G>;
   auto kern = decode_attn_kernel<KvT, D, G, FUSED>;
-  // Per device: the kernel attributes, the largest cluster of this kernel the GPU can
-  // co-schedule (cluster mode is used only up to that size), the SM count, how many CTAs
-  // of the persistent configuration fit on one SM, and the deepest ring that still lets
-  // two single-item CTAs share an SM.
-  static int configured_for = -1;
-  static int max_cluster = 1;
-  static int n_sm = 1;
-  static int per_sm = 1;
-  static size_t single_budget = 0;
+  // Per device, computed once under a mutex and copied out (several host threads may
+  // launch on several devices): the kernel attributes, the largest cluster of this
+  // kernel the GPU can co-schedule (cluster mode is used only up to that size), the SM
+  // count, how many CTAs of the persistent configuration fit on one SM, and the deepest
+  // ring that still lets two single-item CTAs share an SM.
+  struct DeviceInfo {
+    bool ready;
+    int max_cluster, n_sm, per_sm;
+    size_t single_budget;
+  };
+  static std::mutex info_mutex;
+  static DeviceInfo info[kMaxDevices] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   auto ring_stages = [](int kb) {
     const int n = static_cast<int>((static_cast<size_t>(kb) << 10) / C::STAGE_BYTES);
     return n < 1 ? 1 : (n > C::NS ? C::NS : n);
   };
-  if (configured_for != dev) {
-    size_t max_smem = C::layout(static_cast<size_t>(C::NS) * C::STAGE_BYTES, kMaxCluster, true, kMaxListStreams + 1).total;
-    const size_t single = C::layout(static_cast<size_t>(C::NS) * C::STAGE_BYTES, 0, false, 0).total;
-    if (single > max_smem) max_smem = single;
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(max_smem));
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    if (e != cudaSuccess) return e;
-    cudaLaunchConfig_t q = {};
-    q.gridDim = dim3(kMaxCluster, 1, 1);
-    q.blockDim = dim3(C::THREADS);
-    q.dynamicSmemBytes =
-        C::layout(static_cast<size_t>(ring_stages(TTS_RING_KB_CLUSTER)) * C::STAGE_BYTES, kMaxCluster, false, 0).total;
-    cudaLaunchAttribute qa[1];
-    qa[0].id = cudaLaunchAttributeClusterDimension;
-    qa[0].val.clusterDim.x = kMaxCluster;
-    qa[0].val.clusterDim.y = 1;
-    qa[0].val.clusterDim.z = 1;
-    q.attrs = qa;
-    q.numAttrs = 1;
-    int mc = 1;
-    if (cudaOccupancyMaxPotentialClusterSize(&mc, kern, &q) != cudaSuccess) {
-      cudaGetLastError();
-      mc = 8;  // portable cluster size
+  DeviceInfo di;
+  {
+    std::lock_guard<std::mutex> lock(info_mutex);
+    if (!info[dev].ready) {
+      DeviceInfo nd = {};
+      size_t max_smem = C::layout(static_cast<size_t>(C::NS) * C::STAGE_BYTES, kMaxCluster, true, kMaxListStreams + 1).total;
+      const size_t single = C::layout(static_cast<size_t>(C::NS) * C::STAGE_BYTES, 0, false, 0).total;
+      if (single > max_smem) max_smem = single;
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(max_smem));
+      if (e != cudaSuccess) return e;
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+      if (e != cudaSuccess) return e;
+      cudaLaunchConfig_t q = {};
+      q.gridDim = dim3(kMaxCluster, 1, 1);
+      q.blockDim = dim3(C::THREADS);
+      q.dynamicSmemBytes =
+          C::layout(static_cast<size_t>(ring_stages(TTS_RING_KB_CLUSTER)) * C::STAGE_BYTES, kMaxCluster, false, 0).total;
+      cudaLaunchAttribute qa[1];
+      qa[0].id = cudaLaunchAttributeClusterDimension;
+      qa[0].val.clusterDim.x = kMaxCluster;
+      qa[0].val.clusterDim.y = 1;
+      qa[0].val.clusterDim.z = 1;
+      q.attrs = qa;
+      q.numAttrs = 1;
+      int mc = 1;
+      if (cudaOccupancyMaxPotentialClusterSize(&mc, kern, &q) != cudaSuccess) {
+        cudaGetLastError();
+        mc = 8;  // portable cluster size
+      }
+      nd.max_cluster = mc < 1 ? 1 : (mc > kMaxCluster ? kMaxCluster : mc);
+      if (cudaDeviceGetAttribute(&nd.n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || nd.n_sm < 1) {
+        cudaGetLastError();
+        nd.n_sm = 1;
+      }
+      int occ = 0;
+      const size_t stream_smem =
+          C::layout(static_cast<size_t>(ring_stages(TTS_RING_KB_STREAM)) * C::STAGE_BYTES, 0, true, 64).total;
+      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, C::THREADS, stream_smem) != cudaSuccess || occ < 1) {
+        cudaGetLastError();
+        occ = 1;
+      }
+      nd.per_sm = occ;
+      int sm_bytes = 0, reserved = 0;
+      if (cudaDeviceGetAttribute(&sm_bytes, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
+          cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess) {
+        cudaGetLastError();
+        sm_bytes = 0;
+      }
+      nd.single_budget = static_cast<size_t>(sm_bytes) / 2 - static_cast<size_t>(reserved);
+      nd.ready = true;
+      info[dev] = nd;
     }
-    max_cluster = mc < 1 ? 1 : (mc > kMaxCluster ? kMaxCluster : mc);
-    if (cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n_sm < 1) {
-      cudaGetLastError();
-      n_sm = 1;
-    }
-    int occ = 0;
-    const size_t stream_smem =
-        C::layout(static_cast<size_t>(ring_stages(TTS_RING_KB_STREAM)) * C::STAGE_BYTES, 0, true, 64).total;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, C::THREADS, stream_smem) != cudaSuccess || occ < 1) {
-      cudaGetLastError();
-      occ = 1;
-    }
-    per_sm = occ;
-    int sm_bytes = 0, reserved = 0;
-    if (cudaDeviceGetAttribute(&sm_bytes, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess) {
-      cudaGetLastError();
-      sm_bytes = 0;
-    }
-    single_budget = static_cast<size_t>(sm_bytes) / 2 - static_cast<size_t>(reserved);
-    configured_for = dev;
+    di = info[dev];
   }
+  const int max_cluster = di.max_cluster, n_sm = di.n_sm, per_sm = di.per_sm;
+  const size_t single_budget = di.single_budget;
   AttnParams p = p_in;
   // Clusters pay off when the whole grid is one wave of one CTA per SM (few streams).
   // A grid larger than what fits at once becomes persistent: as many CTAs as fit, each

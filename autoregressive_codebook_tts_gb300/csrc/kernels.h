@@ -123,6 +123,7 @@ struct SampleParams {
   float c;              // log2(e) / temperature, rounded once to f32
   uint64_t seed;
   const uint64_t* counter;
+  uint32_t draw;        // third counter word: the draw's index within one counter value
   int32_t* out;
   int64_t out_stride;   // int32 elements between consecutive streams' ids
 };

@@ -8,7 +8,7 @@
 // lowest index) and ordered by rank (larger logit first, lower index first).  Each
 // candidate's weight 2^((l_i - l_0) * log2(e) / T) is computed by its own thread;
 // thread 0 walks the running sum against u * sum, u from Philox4x64-10 at counter words
-// (counter, stream) and key (seed, 0).
+// (counter, stream, draw, 0) and key (seed, 0).
 // Every value that decides the token is computed in f32 in a fixed order with explicit
 // round-to-nearest operations (no contraction into fused multiply-adds); the
 // exponential is this file's own (a degree-9 Taylor polynomial of 2^f, f in [0, 1),
@@ -220,7 +220,7 @@ __global__ void __launch_bounds__(kSampleThreads) sample_kernel(const SamplePara
   if (finite_top) {
     float S = 0.0f;
     for (int j = 0; j < k; ++j) S = __fadd_rn(S, s_w[j]);
-    uint64_t ctr[4] = {__ldcg(p.counter), static_cast<uint64_t>(b), 0ull, 0ull};
+    uint64_t ctr[4] = {__ldcg(p.counter), static_cast<uint64_t>(b), static_cast<uint64_t>(p.draw), 0ull};
     philox4x64_10(ctr, p.seed, 0ull);
     const float u = static_cast<float>(ctr[0] >> 40) * 0x1.0p-24f;  // exact
     const float r = __fmul_rn(u, S);

@@ -34,7 +34,7 @@ EFLAG_NVALID = 8
 EFLAG_TIMEOUT = 16
 
 EXPORTED = [
-    "tts_abi_version", "tts_abi_min_version", "tts_status_str", "tts_frame_embed",
+    "tts_abi_version", "tts_abi_min_version", "tts_abi_check", "tts_status_str", "tts_frame_embed",
     "tts_rope_table", "tts_qk_norm_rope", "tts_kv_set_rows", "tts_decode_attn_workspace_size",
     "tts_decode_attn_default_splits", "tts_workspace_init", "tts_decode_attn", "tts_decode_step",
     "tts_decode_step_noalloc",
@@ -74,6 +74,7 @@ _P, _I32, _I64, _F, _D, _SZ = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, 
 _sigs = {
     "tts_abi_version": ([], _I32),
     "tts_abi_min_version": ([], _I32),
+    "tts_abi_check": ([_I32], _I32),
     "tts_status_str": ([_I32], ctypes.c_char_p),
     "tts_frame_embed": ([ctypes.POINTER(TtsTables), _P, _I64, _P, _I64, _P, _I32, _P, _P], _I32),
     "tts_rope_table": ([_P, _I32, _I32, _D, _P], _I32),
@@ -90,7 +91,8 @@ _sigs = {
     "tts_decode_step_noalloc": ([_P, _P, _P, _I64, _P, _P, _F, _P, _I32, _P, _P,
                                  ctypes.POINTER(TtsKvDesc), _P, _F, _P, _I32, _P, _P], _I32),
     "tts_prefill_workspace_size": ([ctypes.POINTER(TtsKvDesc), _I32, _I32], _SZ),
-    "tts_sample": ([_P, _I64, _I32, _I32, _I32, _F, ctypes.c_uint64, _P, _P, _I64, _P], _I32),
+    "tts_sample": ([_P, _I64, _I32, _I32, _I32, _F, ctypes.c_uint64, _P, ctypes.c_uint32, _P, _I64, _P],
+                   _I32),
     "tts_counter_advance": ([_P, ctypes.c_uint64, _P], _I32),
     "tts_decode_layer_scratch_size": ([ctypes.POINTER(TtsKvDesc), _I32, _I32, _I32], _SZ),
     "tts_decode_layer": ([_P, ctypes.POINTER(TtsLayerWeights), _F, _P, _I32, _P, _P,
@@ -136,6 +138,11 @@ def abi_version() -> int:
 
 def abi_min_version() -> int:
     return _lib.tts_abi_min_version()
+
+
+def abi_check(caller_version: int) -> int:
+    """The library's own range test of a caller's ABI version: 0 (TTS_OK) or TTS_ERR_ABI."""
+    return int(_lib.tts_abi_check(int(caller_version)))
 
 
 def status_str(status: int) -> str:
@@ -286,13 +293,15 @@ def tts_prefill_step(q, k, v, gamma_q, gamma_k, eps, cs, max_pos, k_cache, v_cac
                                  n_splits, _ptr(err_flag), _stream(stream)), "tts_prefill_step")
 
 
-def tts_sample(logits, top_k, temperature, seed, counter, out_ids, stream=None):
+def tts_sample(logits, top_k, temperature, seed, counter, out_ids, draw=0, stream=None):
     """logits [B, V] f32 (rows may be strided); out_ids: int32 tensor whose first dim
-    indexes streams (a column view of an ids buffer is fine)."""
+    indexes streams (a column view of an ids buffer is fine); draw: the third Philox
+    counter word (e.g. the sub-step within a frame)."""
     B, V = logits.shape
     _check(_lib.tts_sample(_ptr(logits), logits.stride(0), B, V, int(top_k), float(temperature),
                            ctypes.c_uint64(int(seed) & ((1 << 64) - 1)), _ptr(counter),
-                           _ptr(out_ids), out_ids.stride(0), _stream(stream)), "tts_sample")
+                           ctypes.c_uint32(int(draw)), _ptr(out_ids), out_ids.stride(0),
+                           _stream(stream)), "tts_sample")
 
 
 def tts_counter_advance(counter, by=1, stream=None):

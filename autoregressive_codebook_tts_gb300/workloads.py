@@ -129,6 +129,12 @@ def gamma(head_dim: int, seed: int, lo: float = 0.5, hi: float = 1.5) -> torch.T
     return torch.rand(head_dim, generator=_gen(seed), dtype=torch.float32) * (hi - lo) + lo
 
 
+def logits(n: int, B: int, vocab: int, seed: int, scale: float = 2.0) -> torch.Tensor:
+    """Synthetic sampler inputs ~N(0, scale^2), f32 [n][B][vocab] (the output heads that
+    would produce them are outside this path)."""
+    return torch.randn(n, B, vocab, generator=_gen(seed), dtype=torch.float32) * scale
+
+
 def cur_lens(w: Workload, seed: int) -> torch.Tensor:
     """Positions of the token decoded this step, int32 [B] (rows [0, cur_len) are
     already in the cache)."""

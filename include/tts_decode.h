@@ -58,10 +58,15 @@
 extern "C" {
 #endif
 
-/* ABI version range ([P-pipeline]-style ABI probe): a caller built against version V
- * may use this library iff tts_abi_min_version() <= V <= tts_abi_version(). */
-#define TTS_ABI_VERSION 2
-#define TTS_ABI_MIN_VERSION 2
+/* ABI version range (the ABI-bump section of the "qwentts.cpp ... commits/branch/
+ * master/tests" page: a version range checked by a probe whose two bounds both
+ * reject).  A caller built against version V may use this library iff
+ * tts_abi_min_version() <= V <= tts_abi_version(); tts_abi_check(V) makes that test
+ * inside the library and returns TTS_OK, or TTS_ERR_ABI for a V below the minimum or
+ * above the current version.  (ABI 2 added tts_tables.dtype; ABI 3 added the `draw`
+ * argument of tts_sample and tts_abi_check.) */
+#define TTS_ABI_VERSION 3
+#define TTS_ABI_MIN_VERSION 3
 int32_t tts_abi_version(void);
 int32_t tts_abi_min_version(void);
 
@@ -74,18 +79,23 @@ typedef enum {
   TTS_ERR_ALIGN = 5,      /* a pointer or stride breaks the 16-byte rule */
   TTS_ERR_WORKSPACE = 6,  /* workspace NULL or smaller than required */
   TTS_ERR_CUDA = 7,       /* the CUDA runtime refused the launch */
-  TTS_ERR_ABI = 8         /* reserved for version mismatches */
+  TTS_ERR_ABI = 8         /* a caller ABI version outside the supported range */
 } tts_status;
 
 /* Human-readable name of a status code (static string). */
 const char* tts_status_str(int32_t status);
+
+/* TTS_OK iff tts_abi_min_version() <= caller_version <= tts_abi_version(), else
+ * TTS_ERR_ABI.  Pass the TTS_ABI_VERSION of the header the caller was built with. */
+tts_status tts_abi_check(int32_t caller_version);
 
 /* Device-side error bits OR-ed into *err_flag. */
 #define TTS_EFLAG_ID_RANGE 1    /* code id outside [0, vocab): clamped into range   */
 #define TTS_EFLAG_POS_RANGE 2   /* position outside the cache/RoPE table: see call  */
 #define TTS_EFLAG_PAGE 4        /* block-table entry outside [0, n_pages): see call */
 #define TTS_EFLAG_NVALID 8      /* n_valid outside [1, capacity]: clamped into it   */
-#define TTS_EFLAG_TIMEOUT 16    /* a bounded in-kernel wait ran out; output invalid */
+#define TTS_EFLAG_TIMEOUT 16    /* a bounded in-kernel wait ran out; output invalid;
+                                   re-zero the call's workspace before its next use */
 
 typedef enum { TTS_F32 = 0, TTS_BF16 = 1 } tts_dtype;
 
@@ -210,8 +220,11 @@ tts_status tts_kv_set_rows(const float* k, const float* v, int64_t kv_row_stride
  *        TTS_EFLAG_PAGE.
  *   workspace: device scratch of at least tts_decode_attn_workspace_size() bytes,
  *        256-byte aligned, zeroed once before its first use (tts_workspace_init or a
- *        memset); every call leaves it ready for the next.  Calls that overlap in time
- *        on the GPU must not share a workspace.
+ *        memset); every call that completes without TTS_EFLAG_TIMEOUT leaves it ready
+ *        for the next.  After a call that set TTS_EFLAG_TIMEOUT its split tickets and
+ *        work counters may hold stale counts: zero it again (tts_workspace_init) before
+ *        the next call that uses it.  Calls that overlap in time on the GPU must not
+ *        share a workspace.
  *   n_splits: ranges per kv head, >= 1; 0 picks tts_decode_attn_default_splits().
  * ------------------------------------------------------------------------- */
 size_t tts_decode_attn_workspace_size(const tts_kv_desc* desc, int32_t n_splits);
@@ -243,7 +256,7 @@ tts_status tts_decode_step(const float* q, const float* k, const float* v, int64
                            int32_t n_splits, int32_t* err_flag, void* stream);
 
 /* ---------------------------------------------------------------------------
- * tts_decode_step without a workspace argument.  The pages have no counterpart: this
+ * tts_decode_step without a workspace argument.  The paper has no counterpart: this
  * is a convenience of this library for callers that cannot allocate device memory when
  * they run a step -- e.g. a real-time audio callback that must not enter an allocator,
  * or a host framework that only lends out the tensors it owns.  The caller still passes
@@ -256,8 +269,7 @@ tts_status tts_decode_step(const float* q, const float* k, const float* v, int64
  * kernel on `stream`) and then runs the step.  All calls share the one array: calls
  * that can overlap on the GPU (different streams, or different threads) race on it and
  * must be serialised by the caller.  Arguments and results are otherwise those of
- * tts_decode_step, and so is the operation (the "qwentts.cpp ... src/pipeline-tts.h"
- * KV cache section's decode step, cited there).
+ * tts_decode_step.
  * ------------------------------------------------------------------------- */
 tts_status tts_decode_step_noalloc(const float* q, const float* k, const float* v,
                                    int64_t row_stride, const float* gamma_q,
@@ -306,13 +318,16 @@ tts_status tts_prefill_step(float* q, const float* k, const float* v, int64_t ro
  *   rounded once to f32, w_i = 2^(f32(f32(l_i - l_0) * c)) in f32 (an exponential of
  *   this library's own: degree-9 Taylor polynomial of 2^f on [0, 1) in Horner form,
  *   times 2^floor, 0 below 2^-126); S = w_0 + ... + w_{k-1} in that order; u = top 24
- *   bits of the first output of Philox4x64-10 at counter words (*counter, b, 0, 0) and
- *   key (seed, 0), times 2^-24; the token is candidate i of the first running sum
+ *   bits of the first output of Philox4x64-10 at counter words (*counter, b, draw, 0)
+ *   and key (seed, 0), times 2^-24; the token is candidate i of the first running sum
  *   (same order) above f32(u * S), else the last candidate.  Every operation is a
  *   single f32 rounding in that order, so the result is exactly reproducible.
  *   logits: device f32, stream b at logits + b*logits_stride.
- *   counter: device uint64 (read only here); advance it between draws with
+ *   counter: device uint64 (read only here); advance it between replays with
  *        tts_counter_advance so that a replayed graph draws fresh numbers.
+ *   draw: a host constant told apart inside one counter value, e.g. the sub-step of a
+ *        code-predictor frame, so that the frame's draws are independent while the
+ *        counter moves once per frame.
  *   out_ids: device int32, stream b's token at out_ids + b*out_stride (for example
  *        the column of the next frame's code ids).
  * vocab must not exceed TTS_MAX_SAMPLE_VOCAB.
@@ -321,7 +336,7 @@ tts_status tts_prefill_step(float* q, const float* k, const float* v, int64_t ro
 #define TTS_MAX_SAMPLE_VOCAB 8192
 tts_status tts_sample(const float* logits, int64_t logits_stride, int32_t B, int32_t vocab,
                       int32_t top_k, float temperature, uint64_t seed, const uint64_t* counter,
-                      int32_t* out_ids, int64_t out_stride, void* stream);
+                      uint32_t draw, int32_t* out_ids, int64_t out_stride, void* stream);
 
 /* *counter += by, as one kernel on `stream` (graph-capturable). */
 tts_status tts_counter_advance(uint64_t* counter, uint64_t by, void* stream);

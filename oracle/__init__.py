@@ -347,12 +347,14 @@ def philox4x64_10(counter, key):
     return c
 
 
-def uniform_f32(seed, counter, b):
+def uniform_f32(seed, counter, b, draw=0):
     """The sampler's uniform for stream b at `counter`: the top 24 bits of the first
-    Philox4x64-10 output for counter words (counter, b, 0, 0) and key (seed, 0), times
+    Philox4x64-10 output for counter words (counter, b, draw, 0) and key (seed, 0), times
     2^-24 (exact in f32, in [0, 1)).  The counter RNG is the "one-kernel counter RNG" of
-    "minicpm-o-4.5 ... docs/optimizations.md" (options table, "Lean Talker frame")."""
-    x = philox4x64_10([counter, b, 0, 0], [seed, 0])[0]
+    "minicpm-o-4.5 ... docs/optimizations.md" (options table, "Lean Talker frame");
+    `draw` tells apart the draws made at one counter value (the sub-steps of a
+    code-predictor frame, each of which samples its own sub-code)."""
+    x = philox4x64_10([counter, b, draw, 0], [seed, 0])[0]
     return np.float32((x >> 40) * (1.0 / (1 << 24)))
 
 
@@ -378,14 +380,14 @@ def exp2_f32(x):
     return np.float32(p * np.float32(2.0 ** n))
 
 
-def sample(logits, top_k, temperature, seed, counter):
+def sample(logits, top_k, temperature, seed, counter, draw=0):
     """Token ids [B] int32 from logits [B][V] f32.
 
     top_k = 0 or 1: greedy, the index of the largest logit (the lowest such index on a
     tie).  top_k = k > 1: the k largest logits (larger first, lower index first on a
     tie) l_0 >= ... >= l_{k-1}; c = f32(log2(e) / temperature) (rounded once from
     double); w_i = exp2_f32(f32(f32(l_i - l_0) * c)); S = w_0 + ... + w_{k-1} summed in
-    that order in f32; r = f32(u * S) with u = uniform_f32(seed, counter, b); the result
+    that order in f32; r = f32(u * S) with u = uniform_f32(seed, counter, b, draw); the result
     is the candidate i of the first running sum (in f32, same order) above r, or the
     last candidate if none is.  NaN logits count as -inf; when the top candidate is not
     finite the result is that candidate.  This is the in-graph sampler of the "qwentts.cpp"
@@ -411,7 +413,7 @@ def sample(logits, top_k, temperature, seed, counter):
         S = np.float32(0.0)
         for wi in w:
             S = np.float32(S + wi)
-        r = np.float32(uniform_f32(seed, counter, b) * S)
+        r = np.float32(uniform_f32(seed, counter, b, draw) * S)
         acc = np.float32(0.0)
         pick = len(order) - 1
         for j, wi in enumerate(w):

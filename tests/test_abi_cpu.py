@@ -43,13 +43,18 @@ def test_library_exports_every_declared_function(tts):
 
 
 def test_abi_version_probe(tts):
+    """The probe of the "qwentts.cpp" tests page (ABI bump section): both bounds of the
+    supported range accept, and the library itself rejects a caller version one below
+    the minimum and one above the current version (tts_abi_check, called through the C
+    boundary)."""
     lo, hi = tts.abi_min_version(), tts.abi_version()
     assert 1 <= lo <= hi
-
-    def compatible(v):
-        return lo <= v <= hi
-    assert compatible(hi) and compatible(lo)
-    assert not compatible(lo - 1) and not compatible(hi + 1)
+    ok, err_abi = 0, 8
+    assert tts.abi_check(lo) == ok and tts.abi_check(hi) == ok
+    assert tts.abi_check(lo - 1) == err_abi
+    assert tts.abi_check(hi + 1) == err_abi
+    assert tts.abi_check(-(2 ** 31)) == err_abi and tts.abi_check(2 ** 31 - 1) == err_abi
+    assert tts.status_str(tts.abi_check(hi + 1)) == "TTS_ERR_ABI"
 
 
 def test_status_strings(tts):
@@ -147,7 +152,7 @@ def test_prefill_sampler_and_table_dtype_validate(tts):
 
     def sample(lg=16, V=2048, k=50, T=1.0, ctr=64, out=16, stride=2048):
         return tts._lib.tts_sample(P(lg) if lg else None, stride, 4, V, k, T, 1,
-                                   P(ctr) if ctr else None, P(out) if out else None, 1, None)
+                                   P(ctr) if ctr else None, 0, P(out) if out else None, 1, None)
     assert sample(lg=0) == 1
     assert sample(out=0) == 1
     assert sample(ctr=0) == 1                    # sampling needs the counter

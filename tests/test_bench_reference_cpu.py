@@ -12,18 +12,23 @@ import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
+ATTN_METRIC = "decode-attn KV GB/s (% of HBM peak); frame steps/sec at B streams, 1 GB300"
 NATIVE_METRIC = {
-    "talker": "decode-attn KV GB/s (% of HBM peak); frame steps/sec at B streams, 1 GB300",
+    None: ATTN_METRIC,
+    "talker": ATTN_METRIC,
+    "paged": ATTN_METRIC,
     "layer": "talker frame GB/s (weights + KV, % of HBM peak); frame steps/sec",
     "prefill": "prefill: prompt positions per second (B streams, all 28 layers)",
 }
 
 
-@pytest.mark.parametrize("workload", ["talker", "layer", "prefill"])
+@pytest.mark.parametrize("workload", [None, "talker", "paged", "layer", "prefill"])
 def test_reference_arm_prints_one_contract_line(workload):
-    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--workload", workload,
-                        "--steps", "1", "--warmup", "3"], cwd=ROOT, capture_output=True, text=True,
-                       timeout=600)
+    """None: the default workload (32 batched streams, bf16 KV), as the driver runs it."""
+    cmd = [sys.executable, "bench.py", "--impl", "reference", "--steps", "1", "--warmup", "3"]
+    if workload is not None:
+        cmd += ["--workload", workload]
+    r = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=600)
     assert r.returncode == 0, r.stderr[-2000:]
     lines = [l for l in r.stdout.splitlines() if l.strip()]
     assert len(lines) == 1

@@ -659,9 +659,23 @@ def test_exp2_f32_accuracy_and_exact_powers():
     assert oracle.exp2_f32(np.float32(-126.5)) == 0.0
 
 
+def test_philox_all_counter_words_match_numpy_philox():
+    """Every counter word enters the generator as numpy's Philox has it: started at
+    (c - 1, b, d, 0), numpy's first block is the block at counter (c, b, d, 0) -- the
+    words the sampler uses for stream b's draw d at counter value c."""
+    key = (0x1234, 0)
+    for c, b, d in [(1, 0, 0), (7, 3, 0), (7, 3, 1), (7, 3, 14), (2 ** 40, 31, 9)]:
+        bg = np.random.Philox(key=np.array(key, dtype=np.uint64),
+                              counter=np.array([c - 1, b, d, 0], dtype=np.uint64))
+        assert [int(x) for x in bg.random_raw(4)] == oracle.philox4x64_10([c, b, d, 0], key)
+
+
 def test_uniform_is_the_top_24_bits():
     x = oracle.philox4x64_10([5, 3, 0, 0], [11, 0])[0]
     assert oracle.uniform_f32(11, 5, 3) == np.float32((x >> 40) / 2.0 ** 24)
+    y = oracle.philox4x64_10([5, 3, 7, 0], [11, 0])[0]
+    assert oracle.uniform_f32(11, 5, 3, draw=7) == np.float32((y >> 40) / 2.0 ** 24)
+    assert x != y
 
 
 def test_greedy_is_the_first_maximum():

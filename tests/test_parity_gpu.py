@@ -344,6 +344,43 @@ def test_decode_attn_flags_bad_n_valid_and_pages(tts):
     assert ef.item() & tts.EFLAG_NVALID and ef.item() & tts.EFLAG_PAGE
 
 
+@pytest.mark.parametrize("n_splits", [0, 4])
+def test_paged_entries_past_the_window_are_never_read(tts, n_splits):
+    """Block-table entries past each stream's window (from ceil(n_valid / 16) on) hold
+    -1: the paged pool is per layer and only a stream's used pages are assigned.  They
+    must never be read nor flagged, so the fused step and the standalone attention give
+    the same bytes as with a fully assigned table, with err_flag 0.  Default splits run
+    the 8-stream workload as a persistent grid whose split length is chosen on the
+    device; 4 splits run one item per CTA."""
+    w = W.workload("paged", layers=1)
+    L = Layer(w, seed=46)
+    cs = rope_table(tts, w.capacity, w.head_dim, w.rope_base)
+    trimmed = L.d_bt.clone()
+    for b in range(w.B):
+        used = (int(L.cur[b]) + 1 + w.page_size - 1) // w.page_size
+        trimmed[b, used:] = -1
+    assert (trimmed == -1).any()
+    results = []
+    for bt in (L.d_bt, trimmed):
+        K, V = L.d_K.clone(), L.d_V.clone()
+        desc = tts.kv_desc(w.B, w.n_q_heads, w.n_kv_heads, w.head_dim, w.capacity, w.kv_dtype,
+                           paged=True, page_size=w.page_size, n_pages=w.n_pages, block_table=bt)
+        ws = tts.workspace(desc, n_splits)
+        ef = err_flag()
+        step = torch.full((w.B, w.n_q_heads, w.head_dim), float("nan"), device="cuda")
+        tts.tts_decode_step(L.d_q, L.d_k, L.d_v, L.d_gq, L.d_gk, w.eps, cs, w.capacity, K, V,
+                            desc, L.d_cur, scale_of(w), step, ws, n_splits, ef)
+        attn = torch.full_like(step, float("nan"))
+        nv = (L.d_cur + 1).to(torch.int32)
+        tts.tts_decode_attn(step, K, V, desc, nv, scale_of(w), attn, ws, n_splits, ef)
+        torch.cuda.synchronize()
+        assert ef.item() == 0
+        results.append((step.cpu(), attn.cpu(), K.cpu(), V.cpu()))
+    for a, b in zip(*results):
+        assert torch.equal(a.view(torch.int16) if a.dtype == torch.bfloat16 else a.view(torch.int32),
+                           b.view(torch.int16) if b.dtype == torch.bfloat16 else b.view(torch.int32))
+
+
 # ---------------------------------------------------------------------------
 # Steps 2+3+4 fused: tts_decode_step
 # ---------------------------------------------------------------------------
