@@ -144,7 +144,12 @@ __device__ __forceinline__ unsigned long long gtime() {
   do {                                                                                     \
     if ((item) < kTraceCtas) g_trace[(item)][slot] = gtime();                              \
   } while (0)
+#define TTS_TRACE_SET(slot, item, value)                                                   \
+  do {                                                                                     \
+    if ((item) < kTraceCtas) g_trace[(item)][slot] = (value);                              \
+  } while (0)
 #else
+#define TTS_TRACE_SET(slot, item, value) do {} while (0)
 #define TTS_STAMP(slot) do {} while (0)
 #define TTS_STAMP_ITEM(slot, item) do {} while (0)
 #endif
@@ -190,17 +195,26 @@ struct Cfg {
   static_assert(NT % Q4 == 0 || Q4 % NT == 0, "combine layout");
 
   // Shared memory: the ring of ns stages, its mbarriers (full[NS], empty[NS], the
-  // cluster gather barrier, item-ready[4], item-free[4]), then the areas below.
+  // cluster gather barrier, item-ready[4], item-free[4], q-ready[4]), then the areas
+  // below.
   static constexpr int PART = G * (D + 2);    // floats of one split's partial (o, m, l per head)
-  static constexpr size_t BAR_BYTES = ((2 * NS + 9) * sizeof(uint64_t) + 15) / 16 * 16;
+  static constexpr size_t BAR_BYTES = ((2 * NS + 13) * sizeof(uint64_t) + 15) / 16 * 16;
   static constexpr size_t SCRATCH_BYTES = (static_cast<size_t>(NC) * PART * sizeof(float) + 15) / 16 * 16;
-  static constexpr size_t FLAG_BYTES = 32;    // ticket flag, persistent item queue[4]
+  static constexpr size_t FLAG_BYTES = 96;    // ticket flag, range length, item queue[4][4]
   // merge of up to kCombSplits partials (workspace path) or 16 (cluster path)
   static constexpr int kCombSplits = 256;
-  static constexpr size_t COMB_BYTES =
-      ((2 * G * kCombSplits + G) * sizeof(float) + 15) / 16 * 16 + NT * 16;
+  static constexpr size_t comb_bytes(int n_splits) {
+    return ((2 * G * static_cast<size_t>(n_splits) + G) * sizeof(float) + 15) / 16 * 16 + NT * 16;
+  }
+  static constexpr size_t COMB_BYTES = comb_bytes(kCombSplits);
+  // Persistent mode: per item-queue slot the item's raw q rows (G heads) and its RoPE
+  // row, copied in by the scheduler; and gamma_q, gamma_k staged once per CTA.
+  static constexpr size_t QROW_BYTES = static_cast<size_t>(G) * D * sizeof(float);
+  static constexpr size_t CSROW_BYTES = static_cast<size_t>(D / 2) * sizeof(float2);
+  static constexpr size_t QSLOT_BYTES = QROW_BYTES + CSROW_BYTES;
+  static constexpr size_t QBUF_BYTES = 4 * QSLOT_BYTES + 2 * D * sizeof(float);
   struct Layout {
-    size_t bar, scratch, flag, comb, gather, list, total;
+    size_t bar, scratch, flag, comb, gather, list, qbuf, total;
   };
   // The merge scratch and the combine area are used only after the CTA's tiles are
   // consumed.  A CTA with a single item puts them over the ring (idle by then, every
@@ -211,7 +225,9 @@ struct Cfg {
   }
   // ring_bytes: ns full stages, or (a split held whole) its full tiles' stages plus the
   // last, partial tile packed as K rows then V rows
-  static Layout layout(size_t ring_bytes, int cluster, bool persistent, int list_ints) {
+  // n_splits: splits of the launch (a persistent CTA's combine area holds that many).
+  static Layout layout(size_t ring_bytes, int cluster, bool persistent, int list_ints,
+                       int n_splits = kCombSplits) {
     Layout L;
     L.bar = ring_bytes;
     size_t o = L.bar + BAR_BYTES;
@@ -224,10 +240,12 @@ struct Cfg {
       L.scratch = o;
       o += SCRATCH_BYTES;
       L.comb = o;
-      o += COMB_BYTES;
+      o += persistent ? comb_bytes(n_splits < kCombSplits ? n_splits : kCombSplits) : COMB_BYTES;
     }
     L.gather = o;
     o += static_cast<size_t>(cluster > 1 ? cluster : 0) * PART * sizeof(float);
+    L.qbuf = o;
+    o += persistent ? QBUF_BYTES : 0;
     L.list = o;
     o += static_cast<size_t>(list_ints) * sizeof(int);
     L.total = o;
@@ -268,49 +286,55 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
-// The lane's elements of one staged K or V row (zeros for rows at or past nrows).
+// The lane's elements of one staged K or V row as pairs of consecutive elements (zeros
+// for rows at or past nrows).  A bf16 pair is one 32-bit word: the low half is the
+// first element; widening to f32 puts the bf16 bits in the high half of each float.
+__device__ __forceinline__ void unpack_pairs(const uint4 v, float2* f, float*) {
+  f[0] = make_float2(__uint_as_float(v.x), __uint_as_float(v.y));
+  f[1] = make_float2(__uint_as_float(v.z), __uint_as_float(v.w));
+}
+__device__ __forceinline__ void unpack_pairs(const uint4 v, float2* f, __nv_bfloat16*) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) f[i] = make_float2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xffff0000u));
+}
+
 template <class C, typename KvT, bool PARTIAL>
 __device__ __forceinline__ void load_smem_row(const unsigned char* __restrict__ tile, int row,
-                                              int nrows, int lr, float (&f)[C::EPL]) {
-  constexpr int VE = C::VE;
+                                              int nrows, int lr, float2 (&f)[C::EPL / 2]) {
+  constexpr int PV = C::VE / 2;  // pairs per 16-byte vector
   if (!PARTIAL || row < nrows) {
 #pragma unroll
-    for (int j = 0; j < C::VEC; ++j) {
-      float part[VE];
-      KvVec<KvT>::unpack(lds128(tile + row * C::ROW_BYTES + (j * C::LPR + lr) * 16), part);
-#pragma unroll
-      for (int e = 0; e < VE; ++e) f[j * VE + e] = part[e];
-    }
+    for (int j = 0; j < C::VEC; ++j)
+      unpack_pairs(lds128(tile + row * C::ROW_BYTES + (j * C::LPR + lr) * 16), f + j * PV,
+                   static_cast<KvT*>(nullptr));
   } else {
 #pragma unroll
-    for (int i = 0; i < C::EPL; ++i) f[i] = 0.f;
+    for (int i = 0; i < C::EPL / 2; ++i) f[i] = make_float2(0.f, 0.f);
   }
 }
 
 // Phase 1 of a tile for this warp: q.K scores of its rows (log2 units), reduced over
-// the LPR lanes of each row; rows at or past nrows get -inf.
+// the LPR lanes of each row; rows at or past nrows get -inf.  The lane's partial dot
+// products run on pairs of elements (packed f32x2 multiply-adds).
 template <class C, typename KvT, bool PARTIAL>
 __device__ __forceinline__ void tile_scores(const unsigned char* __restrict__ kt, int nrows,
-                                            int warp, int lane, const float (&q)[C::G][C::EPL],
+                                            int warp, int lane, const float2 (&q)[C::G][C::EPL / 2],
                                             float (&s)[C::STEPS][C::G]) {
-  constexpr int G = C::G, EPL = C::EPL, LPR = C::LPR, STEPS = C::STEPS;
+  constexpr int G = C::G, NP = C::EPL / 2, LPR = C::LPR, STEPS = C::STEPS;
   const int lr = lane % LPR;
   const int row_base = warp * C::RPW + lane / LPR;
 #pragma unroll
   for (int st = 0; st < STEPS; ++st) {
     const int row = row_base + st * C::RPI;
-    float kf[EPL];
+    float2 kf[NP];
     load_smem_row<C, KvT, PARTIAL>(kt, row, nrows, lr, kf);
 #pragma unroll
     for (int h = 0; h < G; ++h) {
-      // two partial sums halve the FMA dependency chain
-      float a0 = 0.f, a1 = 0.f;
+      float2 a = __fmul2_rn(q[h][0], kf[0]);
 #pragma unroll
-      for (int i = 0; i < EPL; i += 2) {
-        a0 = fmaf(q[h][i], kf[i], a0);
-        a1 = fmaf(q[h][i + 1], kf[i + 1], a1);
-      }
-      s[st][h] = a0 + a1;
+      for (int i = 1; i < NP; ++i) a = __ffma2_rn(q[h][i], kf[i], a);
+      s[st][h] = a.x + a.y;
     }
   }
 #pragma unroll
@@ -328,13 +352,13 @@ __device__ __forceinline__ void tile_scores(const unsigned char* __restrict__ kt
   }
 }
 
-// Phase 2 of a tile: online-softmax update with the tile's scores, then P.V.
+// Phase 2 of a tile: online-softmax update with the tile's scores, then P.V on pairs.
 template <class C, typename KvT, bool PARTIAL>
 __device__ __forceinline__ void tile_softmax_pv(const unsigned char* __restrict__ vt, int nrows,
                                                 int warp, int lane, float (&s)[C::STEPS][C::G],
                                                 float (&m_run)[C::G], float (&l_run)[C::G],
-                                                float (&o)[C::G][C::EPL]) {
-  constexpr int G = C::G, EPL = C::EPL, LPR = C::LPR, STEPS = C::STEPS;
+                                                float2 (&o)[C::G][C::EPL / 2]) {
+  constexpr int G = C::G, NP = C::EPL / 2, LPR = C::LPR, STEPS = C::STEPS;
   const int lr = lane % LPR;
   const int row_base = warp * C::RPW + lane / LPR;
 #pragma unroll
@@ -352,8 +376,9 @@ __device__ __forceinline__ void tile_softmax_pv(const unsigned char* __restrict_
       const float alpha = fast_exp2(m_run[h] - mx);  // 0 on the first tile (m_run = -inf)
       m_run[h] = mx;
       l_run[h] *= alpha;
+      const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll
-      for (int i = 0; i < EPL; ++i) o[h][i] *= alpha;
+      for (int i = 0; i < NP; ++i) o[h][i] = __fmul2_rn(o[h][i], a2);
     }
     const float m_use = (m_run[h] == -INFINITY) ? 0.f : m_run[h];
 #pragma unroll
@@ -365,12 +390,14 @@ __device__ __forceinline__ void tile_softmax_pv(const unsigned char* __restrict_
 #pragma unroll
   for (int st = 0; st < STEPS; ++st) {
     const int row = row_base + st * C::RPI;
-    float vf[EPL];
+    float2 vf[NP];
     load_smem_row<C, KvT, PARTIAL>(vt, row, nrows, lr, vf);
 #pragma unroll
-    for (int h = 0; h < G; ++h)
+    for (int h = 0; h < G; ++h) {
+      const float2 w2 = make_float2(s[st][h], s[st][h]);
 #pragma unroll
-      for (int i = 0; i < EPL; ++i) o[h][i] = fmaf(s[st][h], vf[i], o[h][i]);
+      for (int i = 0; i < NP; ++i) o[h][i] = __ffma2_rn(w2, vf[i], o[h][i]);
+    }
   }
 }
 
@@ -518,6 +545,36 @@ __device__ __forceinline__ Item make_item(const AttnParams& p, int T, int b, int
   return it;
 }
 
+// A persistent item: rows [r0, r1) of the window of (query stream b, kv head g), the
+// split-th of the n_act pieces the window is cut into.
+template <bool FUSED>
+__device__ __forceinline__ Item make_item_rows(const AttnParams& p, int T, int b, int g, int split,
+                                               int raw, int r0, int r1, int n_act) {
+  Item it;
+  it.b = b;
+  it.cb = b / p.q_per_stream;
+  it.g = g;
+  it.split = split;
+  int cache_end;
+  if (FUSED) {
+    it.cur = raw;
+    it.fresh_ok = raw >= 0 && raw < p.capacity;
+    it.nv = min(max(raw + 1, 1), p.capacity);
+    cache_end = it.fresh_ok ? raw : it.nv;
+  } else {
+    it.cur = 0;
+    it.fresh_ok = false;
+    it.nv = min(max(raw, 1), p.capacity);
+    cache_end = it.nv;
+  }
+  it.r0 = r0;
+  it.n_rows = max(0, min(r1, cache_end) - r0);
+  it.has_fresh = FUSED && it.fresh_ok && it.cur >= r0 && it.cur < r1;
+  it.ntiles = (it.n_rows + T - 1) / T;
+  it.n_act = n_act;
+  return it;
+}
+
 // The window input of query stream b: cur_len (fused) or n_valid, read from its cache
 // stream's entry plus the query's offset within that stream (prefill queries).
 __device__ __forceinline__ int raw_len(const AttnParams& p, int b) {
@@ -552,11 +609,14 @@ decode_attn_kernel(const AttnParams p) {
   uint64_t* gbar = empty + C::NS;
   uint64_t* ibar = gbar + 1;   // persistent: item published in queue slot j
   uint64_t* ifree = ibar + 4;  // persistent: queue slot j read by every reader
+  uint64_t* qbar = ifree + 4;  // persistent: the q (and RoPE) rows of queue slot j landed
+  // persistent: per queue slot the item's raw q rows then its RoPE row; then gamma_q,
+  // gamma_k
+  unsigned char* qbuf = smem + p.sm_qbuf;
+  float* s_gamma = reinterpret_cast<float*>(qbuf + 4 * C::QSLOT_BYTES);
   float* scratch = reinterpret_cast<float*>(smem + p.sm_scratch);
   int* s_last = reinterpret_cast<int*>(smem + p.sm_flag);
-  volatile int* s_item = reinterpret_cast<volatile int*>(smem + p.sm_flag + 16);
   unsigned char* comb = smem + p.sm_comb;
-  int* s_pre = reinterpret_cast<int*>(smem + p.sm_list);  // persistent: [B+1]
   float* gather = reinterpret_cast<float*>(smem + p.sm_gather);
   // Cluster mode: the n_splits CTAs of one (stream, kv head) form a cluster and merge
   // their partials in rank 0's shared memory (rank == split).
@@ -576,6 +636,7 @@ decode_attn_kernel(const AttnParams p) {
       for (int j = 0; j < 4; ++j) {
         mbar_init(&ibar[j], 1);        // the scheduler publishes
         mbar_init(&ifree[j], NC + 1);  // the V producer and every consumer warp read
+        mbar_init(&qbar[j], 1);        // the scheduler's arrival (plus the q bytes)
       }
     }
     mbar_init_fence();
@@ -590,111 +651,128 @@ decode_attn_kernel(const AttnParams p) {
   const bool early = FUSED && (p.flags & TTS_KV_PREFETCH_BEFORE_WAIT);
   if (!early) grid_wait();
 
-  // Work list.  Persistent: item i -> (stream b, kv head g, split) over the active
-  // splits only, prefix sums of Hkv * n_act[b] in shared memory.  Otherwise one item,
-  // the CTA's own (split, g, b).
-  int n_items;
-  int split_len = p.split_len;
-  volatile int* s_split = reinterpret_cast<volatile int*>(smem + p.sm_flag + 8);
+  // Work list.  Persistent: a static partition of the launch's work into equal shares.
+  // Every (stream b, kv head g) pair costs kItemCost + n_valid[b] units (a fixed cost
+  // per piece, in cache rows' worth of streaming time, then one unit per window row);
+  // the pairs are laid end to end in (b, g) order and CTA r takes the units
+  // [r K, (r + 1) K), i.e. the window rows of the pairs that range covers, cut on
+  // multiples of 16 rows.  K is the total over the grid, but at least enough that no
+  // window is cut into more pieces than the workspace has split slots.  No CTA takes
+  // work from another at run time, and every CTA computes the same partition from the
+  // same windows.  Otherwise one item, the CTA's own (split, g, b).
+  constexpr int kItemCost = TTS_ITEM_COST_ROWS;
+  constexpr int kMinRangeRows = 64;
+  const int split_len = p.split_len;
+  long long* s_cost = reinterpret_cast<long long*>(smem + p.sm_list);  // [B + 1] prefix of Hkv (kItemCost + nv)
+  int* s_nv = reinterpret_cast<int*>(smem + p.sm_list + (static_cast<size_t>(p.B) + 1) * sizeof(long long));
+  volatile long long* s_K = reinterpret_cast<volatile long long*>(smem + p.sm_flag + 8);
+  long long K = 0, c_total = 0;
   if (persistent) {
-    // The split length of this launch, chosen from the actual windows: for r = 1, 2, 3
-    // rounds of items over the grid, L_r is the smallest multiple of the tile (at least
-    // the launcher's split) that cuts the windows into at most r * grid items; a CTA
-    // then finishes within about r * (L_r + the fixed cost of an item), and the r with
-    // the smallest such bound wins.  Few large items instead of a long queue of small
-    // ones: each item pays a q load, a merge and a ticket.  Every CTA computes the same
-    // value from the same windows.
     if (warp == 0) {
-      for (int b0 = 0; b0 < p.B; b0 += 32) {  // s_pre[b + 1] = window length, for now
-        const int bb = b0 + lane;
-        if (bb < p.B) s_pre[bb + 1] = window_len(p, raw_len(p, bb), FUSED);
-      }
-      __syncwarp();
-      auto items_at = [&](int L) -> long long {
-        long long n = 0;
-        for (int b0 = 0; b0 < p.B; b0 += 32) {
-          const int bb = b0 + lane;
-          int v = bb < p.B ? Hkv * n_active(p, s_pre[bb + 1], L) : 0;
-#pragma unroll
-          for (int off = 16; off >= 1; off >>= 1) v += __shfl_xor_sync(kFull, v, off);
-          n += v;
-        }
-        return n;
-      };
-      const int lo0 = (p.split_len + T - 1) / T, hi0 = (p.capacity + T - 1) / T;  // in tiles
-      long long best = -1;
-      for (int r = 1; r <= 3; ++r) {
-        const long long target = static_cast<long long>(r) * gridDim.x;
-        int lo = lo0, hi = hi0;
-        if (items_at(lo * T) > target) {
-          while (hi - lo > 1) {  // items_at(hi * T) <= target unless even whole windows exceed it
-            const int mid = (lo + hi) >> 1;
-            if (items_at(mid * T) <= target) hi = mid; else lo = mid;
-          }
-          lo = hi;
-        }
-        const long long est = static_cast<long long>(r) * (lo * T + TTS_ITEM_COST_ROWS);
-        if (best < 0 || est < best) {
-          best = est;
-          split_len = lo * T;
-        }
-      }
-      int carry = 0;
+      long long carry = 0;
+      int max_cost = 0;
       for (int b0 = 0; b0 < p.B; b0 += 32) {
         const int bb = b0 + lane;
-        int v = bb < p.B ? Hkv * n_active(p, s_pre[bb + 1], split_len) : 0;
+        const int nv = bb < p.B ? window_len(p, raw_len(p, bb), FUSED) : 0;
+        if (bb < p.B) s_nv[bb] = nv;
+        long long v = bb < p.B ? static_cast<long long>(Hkv) * (kItemCost + nv) : 0;
+        max_cost = max(max_cost, bb < p.B ? kItemCost + nv : 0);
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
-          const int u = __shfl_up_sync(kFull, v, off);
+          const long long u = __shfl_up_sync(kFull, v, off);
           if (lane >= off) v += u;
         }
-        __syncwarp();
-        if (bb < p.B) s_pre[bb + 1] = carry + v;
+        if (bb < p.B) s_cost[bb + 1] = carry + v;
         carry += __shfl_sync(kFull, v, 31);
       }
+#pragma unroll
+      for (int off = 16; off >= 1; off >>= 1) max_cost = max(max_cost, __shfl_xor_sync(kFull, max_cost, off));
       if (lane == 0) {
-        s_pre[0] = 0;
-        *s_split = split_len;
+        s_cost[0] = 0;
+        const long long R = gridDim.x;
+        const long long even = (carry + R - 1) / R;
+        // a window of n rows meets at most n / K + 2 ranges after the 16-row rounding
+        // (boundaries move by at most 8 rows): K >= (max cost + 32) / (splits - 1)
+        // keeps that within the workspace's n_splits slots
+        const long long bound = (static_cast<long long>(max_cost) + 32 + p.n_splits - 2) / (p.n_splits - 1);
+        *s_K = max(max(even, bound), static_cast<long long>(kMinRangeRows));
       }
     }
     __syncthreads();
-    n_items = s_pre[p.B];
-    split_len = *s_split;
-  } else {
-    n_items = 1;
+    K = *s_K;
+    c_total = s_cost[p.B];
   }
-  auto item_at = [&](int i) -> Item {
-    int b, g, split;
-    if (persistent) {
-      int lo = 0, hi = p.B;  // largest b with s_pre[b] <= i
-      while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (s_pre[mid] <= i) lo = mid; else hi = mid;
-      }
-      b = lo;
-      const int r = i - s_pre[b];
-      g = r % Hkv;
-      split = r / Hkv;
-    } else {
-      b = blockIdx.z;
-      g = blockIdx.y;
-      split = blockIdx.x;
+  // Window rows of pair (b, g) below the cost boundary min(r K, total), rounded to a
+  // multiple of 16 and clamped to [0, nv]: non-decreasing in r, 0 at r = 0 and nv at
+  // r = gridDim.x.  CTA r's piece of the pair is [row_at(r), row_at(r + 1)).
+  auto row_at = [&](int b, int g, long long r) -> int {
+    const int nv = s_nv[b];
+    const long long start = s_cost[b] + static_cast<long long>(g) * (kItemCost + nv) + kItemCost;
+    const long long x = min(r * K, c_total) - start;
+    if (x <= 0) return 0;
+    if (x >= nv) return nv;
+    return min((static_cast<int>(x) + 8) & ~15, nv);
+  };
+  // Persistent: the queue entry of pair `pair` for this CTA: {pair, r0, r1, split | n_act << 16}
+  // where the pieces of the pair belong to CTAs r_a..r_b (those with non-empty rows).
+  auto piece_of = [&](int pair, int4& e) {
+    const int b = pair / Hkv, g = pair - (pair / Hkv) * Hkv;
+    const int R = gridDim.x;
+    const int r = blockIdx.x;
+    const int nv = s_nv[b];
+    int lo = 0, hi = R;  // smallest r' with row_at(r') > 0
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (row_at(b, g, mid) > 0) hi = mid; else lo = mid;
     }
-    return make_item<FUSED>(p, T, b, g, split, raw_len(p, b), split_len);
+    const int ra = hi - 1;
+    lo = 0;
+    hi = R;              // smallest r' with row_at(r') >= nv
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (row_at(b, g, mid) >= nv) hi = mid; else lo = mid;
+    }
+    const int rb = hi - 1;
+    e = make_int4(pair, row_at(b, g, r), row_at(b, g, r + 1), (r - ra) | ((rb - ra + 1) << 16));
   };
-  // Persistent mode: queue slot j = k % 4 carries this CTA's k-th item from the
-  // scheduler (the K producer's lane 0) to the V producer and the consumer warps;
-  // -1 ends the list.  Returns false if a bounded wait ran out.
-  auto next_item = [&](int& k, int& item) -> bool {
-    const int j = k & 3;
-    if (!mbar_wait(&ibar[j], static_cast<uint32_t>(k >> 2) & 1u)) return false;
-    item = s_item[j];
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&ifree[j]);
-    ++k;
-    return true;
+  // Persistent: the first pair at or after `from` in which this CTA has rows, or -1.
+  auto next_pair = [&](int from) -> int {
+    const long long hi_cost = min((static_cast<long long>(blockIdx.x) + 1) * K, c_total);
+    for (int pr = from; pr < p.B * Hkv; ++pr) {
+      const int b = pr / Hkv, g = pr - (pr / Hkv) * Hkv;
+      if (s_cost[b] + static_cast<long long>(g) * (kItemCost + s_nv[b]) >= hi_cost) return -1;
+      if (row_at(b, g, blockIdx.x) < row_at(b, g, static_cast<long long>(blockIdx.x) + 1)) return pr;
+    }
+    return -1;
   };
-
+  // Persistent: the pair that holds the cost unit min(r K, total), where this CTA's
+  // range starts.
+  auto first_pair = [&]() -> int {
+    const long long c0 = min(static_cast<long long>(blockIdx.x) * K, c_total);
+    int lo = 0, hi = p.B;  // largest b with s_cost[b] <= c0
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (s_cost[mid] <= c0) lo = mid; else hi = mid;
+    }
+    const long long g = (c0 - s_cost[lo]) / (kItemCost + s_nv[lo]);
+    return lo * Hkv + static_cast<int>(min(g, static_cast<long long>(Hkv - 1)));
+  };
+  volatile int4* s_item = reinterpret_cast<volatile int4*>(smem + p.sm_flag + 32);
+  auto item_of = [&](const int4 e) -> Item {
+    if (persistent) {
+      const int b = e.x / Hkv;
+      return make_item_rows<FUSED>(p, T, b, e.x - b * Hkv, e.w & 0xffff, raw_len(p, b), e.y, e.z,
+                                   e.w >> 16);
+    }
+    return make_item<FUSED>(p, T, blockIdx.z, blockIdx.y, blockIdx.x, raw_len(p, blockIdx.z), split_len);
+  };
+  auto read_entry = [&](int j) -> int4 {
+    const int4 e = make_int4(s_item[j].x, s_item[j].y, s_item[j].z, s_item[j].w);
+    return e;
+  };
+  // Persistent mode: queue slot j = k % 4 carries this CTA's k-th entry (pair, rows,
+  // split and piece count) from the scheduler (the K producer's lane 0) to the V
+  // producer and the consumer warps; a negative pair ends the list.
   if (warp >= NC) {
     // ----------------------------------------------------------------- producers
     // Warp NC streams the K tiles, warp NC+1 the V tiles: bulk copies issued by
@@ -710,7 +788,8 @@ decode_attn_kernel(const AttnParams p) {
     uint32_t round = 0;
     bool ok = true;
     int k = 0;  // items taken so far
-    int i = persistent ? (static_cast<int>(blockIdx.x) < n_items ? static_cast<int>(blockIdx.x) : -1) : 0;
+    int pair = (persistent && pw == 0) ? next_pair(first_pair()) : 0;
+    int4 e = make_int4(-1, 0, 0, 0);
     for (;;) {
       if (persistent) {
         if (pw == 0) {
@@ -722,19 +801,49 @@ decode_attn_kernel(const AttnParams p) {
             if (lane == 0) set_err(p.err, TTS_EFLAG_TIMEOUT);
             break;
           }
+          if (pair >= 0) piece_of(pair, e); else e = make_int4(-1, 0, 0, 0);
           if (lane == 0) {
-            s_item[j] = i;
+            s_item[j].x = e.x;
+            s_item[j].y = e.y;
+            s_item[j].z = e.z;
+            s_item[j].w = e.w;
             mbar_arrive(&ibar[j]);
+            // From the second item on (the dependency wait is behind us: q is written by
+            // the preceding kernel) the item's q rows, and in the fused form its RoPE
+            // row, are copied into the slot, so the consumers find them in shared memory.
+            if (k >= 1 && e.x >= 0) {
+              const Item qi = item_of(e);
+              const uint32_t bytes = static_cast<uint32_t>(C::QROW_BYTES + (FUSED ? C::CSROW_BYTES : 0));
+              mbar_arrive_expect_tx(&qbar[j], bytes);
+              bulk_g2s_plain(qbuf + j * C::QSLOT_BYTES,
+                             p.q + static_cast<int64_t>(qi.b) * p.q_stride + static_cast<int64_t>(qi.g) * G * D,
+                             static_cast<uint32_t>(C::QROW_BYTES), &qbar[j]);
+              if (FUSED) {
+                const int rope_pos = min(max(qi.cur, 0), p.max_pos - 1);
+                bulk_g2s_plain(qbuf + j * C::QSLOT_BYTES + C::QROW_BYTES,
+                               p.cs + static_cast<int64_t>(rope_pos) * (D / 2),
+                               static_cast<uint32_t>(C::CSROW_BYTES), &qbar[j]);
+              }
+            } else {
+              mbar_arrive(&qbar[j]);
+            }
           }
           __syncwarp();
           ++k;
-        } else if (!next_item(k, i)) {
-          if (lane == 0) set_err(p.err, TTS_EFLAG_TIMEOUT);
-          break;
+        } else {
+          const int j = k & 3;
+          if (!mbar_wait(&ibar[j], static_cast<uint32_t>(k >> 2) & 1u)) {
+            if (lane == 0) set_err(p.err, TTS_EFLAG_TIMEOUT);
+            break;
+          }
+          e = read_entry(j);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&ifree[j]);
+          ++k;
         }
-        if (i < 0) break;
+        if (e.x < 0) break;
       }
-      const Item it = item_at(i);
+      const Item it = item_of(e);
       if (!persistent && it.split >= it.n_act) break;  // outside the window
       const int32_t* bt = p.paged ? p.block_table + static_cast<int64_t>(it.cb) * p.bt_stride : nullptr;
       for (int t = 0; t < it.ntiles; ++t) {
@@ -792,21 +901,18 @@ decode_attn_kernel(const AttnParams p) {
       }
       if (!ok || !persistent) break;
       if (pw == 0) {
-        // next item from the work counter (after the dependency wait: the counter is
-        // reset by the preceding launch on this workspace when it finishes)
+        // the next item's q rows are copied after the dependency wait
         if (k == 1 && early) grid_wait();
-        int nxt = -1;
-        if (lane == 0) {
-          const int v = static_cast<int>(gridDim.x) + atomicAdd(p.ws_sched, 1);
-          nxt = v < n_items ? v : -1;
-        }
-        i = __shfl_sync(kFull, nxt, 0);
+        pair = next_pair(pair + 1);
       }
     }
     // Do not leave while copies into this CTA's shared memory may be in flight.
-    if (lane == 0)
+    if (lane == 0) {
       for (int t = max(0, issued - ns); t < issued; ++t)
         mbar_wait(&full[t % ns], static_cast<uint32_t>(t / ns) & 1u);
+      if (persistent && pw == 0)
+        for (int t = max(0, k - 4); t < k; ++t) mbar_wait(&qbar[t & 3], static_cast<uint32_t>(t >> 2) & 1u);
+    }
     return;
   }
 
@@ -828,7 +934,12 @@ decode_attn_kernel(const AttnParams p) {
   // written by the preceding launch, so the item is worked out before the dependency
   // wait, while that launch finishes.
   Item it0 = {};
-  if (!persistent && early) it0 = item_at(0);
+  if (!persistent && early) it0 = item_of(make_int4(0, 0, 0, 0));
+  if (persistent && FUSED) {
+    // gamma_q and gamma_k, read once per CTA (constants of the layer)
+    for (int e = tid; e < 2 * D; e += NT) s_gamma[e] = __ldcg((e < D ? p.gamma_q : p.gamma_k) + (e % D));
+    named_barrier(1, NT);
+  }
   if (early) grid_wait();
   grid_launch_dependents();
   if (tid == 0) TTS_STAMP(1);
@@ -837,18 +948,41 @@ decode_attn_kernel(const AttnParams p) {
   uint32_t pc = 0u;    // parity of its phase
   bool ok = true;
   int kq = 0;  // items taken from the queue so far (persistent)
+  int jq = 0;  // queue slot of the current item (persistent)
+  // persistent: the ticket of the previous item, issued at its end and resolved at the
+  // end of the next one (thread 0 holds the atomic's result)
+  int pend_b = -1, pend_g = 0, pend_nact = 0, pend_prev = 0;
+  auto resolve_pending = [&]() {
+    if (tid == 0) *s_last = (pend_prev == pend_nact - 1) ? 1 : 0;
+    named_barrier(1, NT);
+    if (*s_last != 0) {
+      combine_splits<C>(p, pend_b, pend_g, pend_nact, tid, comb);
+      if (tid == 0) p.ws_cnt[pend_b * Hkv + pend_g] = 0;
+    }
+    named_barrier(1, NT);
+    pend_b = -1;
+  };
+  int4 ecur = make_int4(0, 0, 0, 0);
   for (int round_item = 0;; ++round_item) {
     int i = 0;
     if (persistent) {
-      if (!next_item(kq, i)) {
+      jq = kq & 3;
+      if (!mbar_wait(&ibar[jq], static_cast<uint32_t>(kq >> 2) & 1u)) {
         set_err(p.err, TTS_EFLAG_TIMEOUT);
         break;
       }
-      if (i < 0) break;
+      ecur = read_entry(jq);
+      ++kq;
+      i = static_cast<int>(blockIdx.x) * 8 + min(kq - 1, 7);  // trace slot of this item
+      if (ecur.x < 0) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ifree[jq]);
+        break;
+      }
     } else if (round_item > 0) {
       break;
     }
-    const Item it = (!persistent && early) ? it0 : item_at(i);
+    const Item it = (!persistent && early) ? it0 : item_of(ecur);
     const bool active = it.split < it.n_act;
     if (!persistent && !active) {
       // Outside the window: nothing to stream.  A cluster peer still reports in when
@@ -861,7 +995,11 @@ decode_attn_kernel(const AttnParams p) {
       return;
     }
     const int b = it.b, g = it.g, split = it.split;
-    if (persistent && tid == 0) { TTS_STAMP_ITEM(0, i); TTS_STAMP_ITEM(1, blockIdx.x * 0 + i); }
+    if (persistent && tid == 0) {
+      TTS_STAMP_ITEM(0, i);
+      TTS_TRACE_SET(1, i, blockIdx.x | (static_cast<unsigned long long>(it.n_rows) << 16) |
+                              (static_cast<unsigned long long>(kq) << 32));
+    }
     const bool reporter = (split == 0 && g == 0 && tid == 0);
     if (reporter) {
       if (FUSED) {
@@ -873,27 +1011,57 @@ decode_attn_kernel(const AttnParams p) {
       }
     }
 
-    if (FUSED) load_consts(it);
+    // From a persistent CTA's second item on, the scheduler has copied the raw q rows
+    // (and the RoPE row) into the item's queue slot; otherwise they come from global
+    // memory.
+    const bool q_in_smem = persistent && kq >= 2;
     const bool fresh_here = FUSED && it.has_fresh && warp == kFreshWarp;
     float q[G][EPL];
+    if (q_in_smem) {
+      if (!mbar_wait(&qbar[jq], static_cast<uint32_t>((kq - 1) >> 2) & 1u)) {
+        set_err(p.err, TTS_EFLAG_TIMEOUT);
+        ok = false;
+      }
+      const float* qs = reinterpret_cast<const float*>(qbuf + jq * C::QSLOT_BYTES);
+      if (FUSED) {
+        const float2* cs_row = reinterpret_cast<const float2*>(qbuf + jq * C::QSLOT_BYTES + C::QROW_BYTES);
+        load_norm_consts_smem<VE, VEC, LPR>(s_gamma, cs_row, lr, D, gq, csr);
+        if (fresh_here) load_norm_consts_smem<VE, VEC, LPR>(s_gamma + D, cs_row, lr, D, gk, csr);
+      }
 #pragma unroll
-    for (int h = 0; h < G; ++h)
-      load_row_f32<VE, VEC, LPR>(
-          p.q + static_cast<int64_t>(b) * p.q_stride + static_cast<int64_t>(g * G + h) * D, lr, q[h]);
+      for (int h = 0; h < G; ++h) load_row_smem<VE, VEC, LPR>(qs + h * D, lr, q[h]);
+    } else {
+      if (FUSED) load_consts(it);
+#pragma unroll
+      for (int h = 0; h < G; ++h)
+        load_row_f32<VE, VEC, LPR>(
+            p.q + static_cast<int64_t>(b) * p.q_stride + static_cast<int64_t>(g * G + h) * D, lr, q[h]);
+    }
+    if (persistent) {
+      // every value of the slot this warp needs is in registers: release the slot
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ifree[jq]);
+    }
 #pragma unroll
     for (int h = 0; h < G; ++h) {
       if (FUSED) norm_rope_regs<VE, VEC, LPR>(q[h], gq, csr, p.eps, lr, D);
 #pragma unroll
       for (int k = 0; k < EPL; ++k) q[h][k] *= p.scale_log2;
     }
+    float2 q2[G][EPL / 2];
+#pragma unroll
+    for (int h = 0; h < G; ++h)
+#pragma unroll
+      for (int i = 0; i < EPL / 2; ++i) q2[h][i] = make_float2(q[h][2 * i], q[h][2 * i + 1]);
 
-    float m_run[G], l_run[G], o[G][EPL];
+    float m_run[G], l_run[G];
+    float2 o[G][EPL / 2];
 #pragma unroll
     for (int h = 0; h < G; ++h) {
       m_run[h] = -INFINITY;
       l_run[h] = 0.f;
 #pragma unroll
-      for (int k = 0; k < EPL; ++k) o[h][k] = 0.f;
+      for (int k = 0; k < EPL / 2; ++k) o[h][k] = make_float2(0.f, 0.f);
     }
 
     // Fused: build the new K/V row (norm + RoPE on k, v as is), convert it to the cache
@@ -959,7 +1127,8 @@ decode_attn_kernel(const AttnParams p) {
         m_run[h] = sc;
         l_run[h] = lane < LPR ? 1.f : 0.f;
 #pragma unroll
-        for (int k = 0; k < EPL; ++k) o[h][k] = lane < LPR ? vr[k] : 0.f;
+        for (int k = 0; k < EPL / 2; ++k)
+          o[h][k] = lane < LPR ? make_float2(vr[2 * k], vr[2 * k + 1]) : make_float2(0.f, 0.f);
       }
     }
 
@@ -973,7 +1142,7 @@ decode_attn_kernel(const AttnParams p) {
     if (ok && n_full > 0) {
       ok = mbar_wait(&full[sc], pc);
       if (tid == 0) { if (persistent) TTS_STAMP_ITEM(3, i); else TTS_STAMP(3); }
-      if (ok) tile_scores<C, KvT, false>(ring + sc * C::STAGE_BYTES, T, warp, lane, q, s_cur);
+      if (ok) tile_scores<C, KvT, false>(ring + sc * C::STAGE_BYTES, T, warp, lane, q2, s_cur);
     }
     for (int t = 0; ok && t + 1 < n_full; ++t) {
       int sn = sc + 1;
@@ -986,7 +1155,7 @@ decode_attn_kernel(const AttnParams p) {
         ok = false;
         break;
       }
-      tile_scores<C, KvT, false>(ring + sn * C::STAGE_BYTES, T, warp, lane, q, s_nxt);
+      tile_scores<C, KvT, false>(ring + sn * C::STAGE_BYTES, T, warp, lane, q2, s_nxt);
       tile_softmax_pv<C, KvT, false>(ring + sc * C::STAGE_BYTES + C::TILE_BYTES, T, warp, lane,
                                      s_cur, m_run, l_run, o);
       __syncwarp();
@@ -1011,7 +1180,7 @@ decode_attn_kernel(const AttnParams p) {
     if (ok && tail > 0) {
       if (mbar_wait(&full[sc], pc)) {
         if (n_full == 0 && tid == 0) { if (persistent) TTS_STAMP_ITEM(3, i); else TTS_STAMP(3); }
-        tile_scores<C, KvT, true>(ring + sc * C::STAGE_BYTES, tail, warp, lane, q, s_cur);
+        tile_scores<C, KvT, true>(ring + sc * C::STAGE_BYTES, tail, warp, lane, q2, s_cur);
         tile_softmax_pv<C, KvT, true>(ring + sc * C::STAGE_BYTES + tail * C::ROW_BYTES, tail, warp,
                                       lane, s_cur, m_run, l_run, o);
         __syncwarp();
@@ -1034,7 +1203,10 @@ decode_attn_kernel(const AttnParams p) {
       for (int off = LPR; off < 32; off <<= 1) {
         l_run[h] += __shfl_xor_sync(kFull, l_run[h], off);
 #pragma unroll
-        for (int k = 0; k < EPL; ++k) o[h][k] += __shfl_xor_sync(kFull, o[h][k], off);
+        for (int k = 0; k < EPL / 2; ++k) {
+          o[h][k].x += __shfl_xor_sync(kFull, o[h][k].x, off);
+          o[h][k].y += __shfl_xor_sync(kFull, o[h][k].y, off);
+        }
       }
     }
     // the scratch may lie over the ring, whose last tiles other warps may still read
@@ -1046,7 +1218,10 @@ decode_attn_kernel(const AttnParams p) {
 #pragma unroll
         for (int j = 0; j < VEC; ++j)
 #pragma unroll
-          for (int e = 0; e < VE; ++e) dst[(j * LPR + lr) * VE + e] = o[h][j * VE + e];
+          for (int e = 0; e < VE; e += 2) {
+            dst[(j * LPR + lr) * VE + e] = o[h][(j * VE + e) / 2].x;
+            dst[(j * LPR + lr) * VE + e + 1] = o[h][(j * VE + e) / 2].y;
+          }
         if (lane == 0) {
           dst[D] = m_run[h];
           dst[D + 1] = l_run[h];
@@ -1144,7 +1319,20 @@ decode_attn_kernel(const AttnParams p) {
       return;
     }
 
-    if (!direct) {
+    if (persistent) {
+      // The previous item's ticket has long returned: if it was the last of its
+      // (stream, kv head), merge that pair's partials now.  Then take this item's
+      // ticket without waiting for the atomic's result (resolved after the next item).
+      if (pend_b >= 0) resolve_pending();
+      if (!direct) {
+        named_barrier(1, NT);  // every partial store of this item precedes the ticket
+        if (tid == 0) pend_prev = atomic_add_acq_rel_gpu(p.ws_cnt + b * Hkv + g, 1);
+        pend_b = b;
+        pend_g = g;
+        pend_nact = it.n_act;
+        if (tid == 0) TTS_STAMP_ITEM(6, i);
+      }
+    } else if (!direct) {
       // Ticket: the last of this (stream, kv head)'s active splits merges all partials.
       named_barrier(1, NT);
       if (tid == 0) {
@@ -1152,31 +1340,27 @@ decode_attn_kernel(const AttnParams p) {
         *s_last = (prev == it.n_act - 1) ? 1 : 0;
       }
       named_barrier(1, NT);
-      if (tid == 0) { if (persistent) TTS_STAMP_ITEM(6, i); else TTS_STAMP(6); }
+      if (tid == 0) TTS_STAMP(6);
       if (*s_last != 0) {
         combine_splits<C>(p, b, g, it.n_act, tid, comb);
         if (tid == 0) {
           p.ws_cnt[b * Hkv + g] = 0;
-          { if (persistent) TTS_STAMP_ITEM(7, i); else TTS_STAMP(7); }
+          TTS_STAMP(7);
         }
       }
     }
     // the merge scratch and flag are reused by the next item
     named_barrier(1, NT);
+    if (persistent && tid == 0) TTS_STAMP_ITEM(7, i);
   }
-  if (persistent && tid == 0) {
-    // the last CTA to finish resets the work counter for the next launch
-    const int prev = atomic_add_acq_rel_gpu(p.ws_sched + 1, 1);
-    if (prev == static_cast<int>(gridDim.x) - 1) {
-      p.ws_sched[0] = 0;
-      p.ws_sched[1] = 0;
-    }
-  }
+  if (persistent && pend_b >= 0) resolve_pending();
 }
 
 constexpr int kMaxCluster = 16;
 
-constexpr int kMaxListStreams = 2048;  // persistent mode keeps B + 1 prefix sums in smem
+constexpr int kMaxListStreams = 2048;  // persistent mode keeps per-stream costs in smem
+// 32-bit words of the persistent work list: B + 1 64-bit cost prefix sums, B window lengths
+constexpr int list_ints(int B) { return 2 * (B + 1) + B; }
 constexpr int kMaxDevices = 64;
 
 template <typename KvT, int D, int G, bool FUSED>
@@ -1208,7 +1392,7 @@ cudaError_t launch_one(const AttnParams& p_in, cudaStream_t s) {
     std::lock_guard<std::mutex> lock(info_mutex);
     if (!info[dev].ready) {
       DeviceInfo nd = {};
-      size_t max_smem = C::layout(static_cast<size_t>(C::NS) * C::STAGE_BYTES, kMaxCluster, true, kMaxListStreams + 1).total;
+      size_t max_smem = C::layout(static_cast<size_t>(C::NS) * C::STAGE_BYTES, kMaxCluster, true, list_ints(kMaxListStreams)).total;
       const size_t single = C::layout(static_cast<size_t>(C::NS) * C::STAGE_BYTES, 0, false, 0).total;
       if (single > max_smem) max_smem = single;
       e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(max_smem));
@@ -1239,7 +1423,7 @@ cudaError_t launch_one(const AttnParams& p_in, cudaStream_t s) {
       }
       int occ = 0;
       const size_t stream_smem =
-          C::layout(static_cast<size_t>(ring_stages(TTS_RING_KB_STREAM)) * C::STAGE_BYTES, 0, true, 64).total;
+          C::layout(static_cast<size_t>(ring_stages(TTS_RING_KB_STREAM)) * C::STAGE_BYTES, 0, true, list_ints(64), 16).total;
       if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, C::THREADS, stream_smem) != cudaSuccess || occ < 1) {
         cudaGetLastError();
         occ = 1;
@@ -1296,7 +1480,8 @@ cudaError_t launch_one(const AttnParams& p_in, cudaStream_t s) {
       ring_bytes = static_cast<size_t>(ns) * C::STAGE_BYTES;
     }
   }
-  const typename C::Layout L = C::layout(ring_bytes, p.cluster, p.persistent != 0, p.persistent ? p.B + 1 : 0);
+  const typename C::Layout L =
+      C::layout(ring_bytes, p.cluster, p.persistent != 0, p.persistent ? list_ints(p.B) : 0, p.n_splits);
   p.inflight = p.persistent ? TTS_INFLIGHT_STREAM : TTS_INFLIGHT_SINGLE;
   p.sm_bar = static_cast<uint32_t>(L.bar);
   p.sm_scratch = static_cast<uint32_t>(L.scratch);
@@ -1304,6 +1489,7 @@ cudaError_t launch_one(const AttnParams& p_in, cudaStream_t s) {
   p.sm_comb = static_cast<uint32_t>(L.comb);
   p.sm_gather = static_cast<uint32_t>(L.gather);
   p.sm_list = static_cast<uint32_t>(L.list);
+  p.sm_qbuf = static_cast<uint32_t>(L.qbuf);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = p.persistent ? dim3(static_cast<unsigned>(resident), 1, 1) : dim3(p.n_splits, p.n_kv_heads, p.B);
   cfg.dynamicSmemBytes = L.total;

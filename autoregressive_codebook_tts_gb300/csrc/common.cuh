@@ -103,6 +103,15 @@ __device__ __forceinline__ void bulk_g2s(void* smem_dst, const void* gmem_src, u
       : "memory");
 }
 
+// The same copy with the default L2 policy (for small rows read again soon).
+__device__ __forceinline__ void bulk_g2s_plain(void* smem_dst, const void* gmem_src, uint32_t bytes,
+                                               uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      ::"r"(smem_u32(smem_dst)), "l"(gmem_src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
 // Named barrier over a subset of the CTA's warps (id 0 is __syncthreads).
 __device__ __forceinline__ void named_barrier(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
@@ -183,6 +192,45 @@ __device__ __forceinline__ void load_norm_consts(const float* gamma, const float
       cs[j * VE + e + 2] = make_float2(c1.x, c1.y); cs[j * VE + e + 3] = make_float2(c1.z, c1.w);
     }
   }
+}
+
+// load_norm_consts from shared-memory copies of gamma and of the RoPE row.
+template <int VE, int VEC, int LPR>
+__device__ __forceinline__ void load_norm_consts_smem(const float* gamma, const float2* cs_row, int lr,
+                                                      int D, float (&gam)[VE * VEC],
+                                                      float2 (&cs)[VE * VEC]) {
+  const int half = D / 2;
+#pragma unroll
+  for (int j = 0; j < VEC; ++j) {
+    const int idx = (j * LPR + lr) * VE;
+    const int f = idx < half ? idx : idx - half;
+#pragma unroll
+    for (int e = 0; e < VE; e += 4) {
+      const uint4 gv = lds128(gamma + idx + e);
+      gam[j * VE + e] = __uint_as_float(gv.x); gam[j * VE + e + 1] = __uint_as_float(gv.y);
+      gam[j * VE + e + 2] = __uint_as_float(gv.z); gam[j * VE + e + 3] = __uint_as_float(gv.w);
+      const uint4 c0 = lds128(cs_row + f + e);
+      const uint4 c1 = lds128(cs_row + f + e + 2);
+      cs[j * VE + e] = make_float2(__uint_as_float(c0.x), __uint_as_float(c0.y));
+      cs[j * VE + e + 1] = make_float2(__uint_as_float(c0.z), __uint_as_float(c0.w));
+      cs[j * VE + e + 2] = make_float2(__uint_as_float(c1.x), __uint_as_float(c1.y));
+      cs[j * VE + e + 3] = make_float2(__uint_as_float(c1.z), __uint_as_float(c1.w));
+    }
+  }
+}
+
+// The lane's elements of an f32 row held in shared memory, in the lane layout of the
+// cache rows: element e of vector j is row element (j * LPR + lr) * VE + e.
+template <int VE, int VEC, int LPR>
+__device__ __forceinline__ void load_row_smem(const float* row, int lr, float (&x)[VE * VEC]) {
+#pragma unroll
+  for (int j = 0; j < VEC; ++j)
+#pragma unroll
+    for (int e = 0; e < VE; e += 4) {
+      const uint4 v = lds128(row + (j * LPR + lr) * VE + e);
+      x[j * VE + e] = __uint_as_float(v.x); x[j * VE + e + 1] = __uint_as_float(v.y);
+      x[j * VE + e + 2] = __uint_as_float(v.z); x[j * VE + e + 3] = __uint_as_float(v.w);
+    }
 }
 
 template <int VE, int VEC, int LPR>

@@ -88,8 +88,9 @@ struct AttnParams {
   int inflight;         // set by the launcher: tiles a producer keeps in flight (0 = ring)
   // set by the launcher: byte offsets in dynamic shared memory of the ring's mbarriers
   // (the ring starts at 0), the per-warp merge scratch, the flag word and item queue,
-  // the combine area, the cluster gather area and the persistent work list
-  uint32_t sm_bar, sm_scratch, sm_flag, sm_comb, sm_gather, sm_list;
+  // the combine area, the cluster gather area, the persistent work list and the
+  // persistent q slots
+  uint32_t sm_bar, sm_scratch, sm_flag, sm_comb, sm_gather, sm_list, sm_qbuf;
   uint32_t flags;
   int32_t* err;
 };
