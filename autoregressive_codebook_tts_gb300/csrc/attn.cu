@@ -110,7 +110,7 @@
 // Persistent grids: the fixed cost of a work item (q load, merge, ticket), in cache
 // rows' worth of streaming time, used to choose the split length of a launch.
 #ifndef TTS_ITEM_COST_ROWS
-#define TTS_ITEM_COST_ROWS 128
+#define TTS_ITEM_COST_ROWS 256
 #endif
 #ifndef TTS_ATTN_MIN_BLOCKS
 #define TTS_ATTN_MIN_BLOCKS 2
@@ -626,7 +626,7 @@ decode_attn_kernel(const AttnParams p) {
   const bool persistent = p.persistent != 0;
 
   if (threadIdx.x == 0) {
-    TTS_STAMP(0);
+    if (p.persistent == 0) TTS_STAMP(0);
     for (int s = 0; s < ns; ++s) {
       mbar_init(&full[s], 2);  // one arrival from each producer warp, plus the bytes
       mbar_init(&empty[s], NC);
@@ -942,7 +942,7 @@ decode_attn_kernel(const AttnParams p) {
   }
   if (early) grid_wait();
   grid_launch_dependents();
-  if (tid == 0) TTS_STAMP(1);
+  if (tid == 0 && !persistent) TTS_STAMP(1);
 
   int sc = 0;          // ring stage of the next tile
   uint32_t pc = 0u;    // parity of its phase
@@ -997,8 +997,11 @@ decode_attn_kernel(const AttnParams p) {
     const int b = it.b, g = it.g, split = it.split;
     if (persistent && tid == 0) {
       TTS_STAMP_ITEM(0, i);
+      unsigned smid;
+      asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
       TTS_TRACE_SET(1, i, blockIdx.x | (static_cast<unsigned long long>(it.n_rows) << 16) |
-                              (static_cast<unsigned long long>(kq) << 32));
+                              (static_cast<unsigned long long>(kq) << 32) |
+                              (static_cast<unsigned long long>(smid) << 40));
     }
     const bool reporter = (split == 0 && g == 0 && tid == 0);
     if (reporter) {
@@ -1395,6 +1398,12 @@ cudaError_t launch_one(const AttnParams& p_in, cudaStream_t s) {
       size_t max_smem = C::layout(static_cast<size_t>(C::NS) * C::STAGE_BYTES, kMaxCluster, true, list_ints(kMaxListStreams)).total;
       const size_t single = C::layout(static_cast<size_t>(C::NS) * C::STAGE_BYTES, 0, false, 0).total;
       if (single > max_smem) max_smem = single;
+      // no launch can use more than a block may opt into; a layout above it fails to launch
+      int optin = 0;
+      if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) == cudaSuccess && optin > 0 &&
+          max_smem > static_cast<size_t>(optin))
+        max_smem = static_cast<size_t>(optin);
+      cudaGetLastError();
       e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(max_smem));
       if (e != cudaSuccess) return e;
       e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
