@@ -665,6 +665,7 @@ decode_attn_kernel(const AttnParams p) {
   const int split_len = p.split_len;
   long long* s_cost = reinterpret_cast<long long*>(smem + p.sm_list);  // [B + 1] prefix of Hkv (kItemCost + nv)
   int* s_nv = reinterpret_cast<int*>(smem + p.sm_list + (static_cast<size_t>(p.B) + 1) * sizeof(long long));
+  int* s_raw = s_nv + p.B;  // persistent: the window input of every query stream (cur_len or n_valid)
   volatile long long* s_K = reinterpret_cast<volatile long long*>(smem + p.sm_flag + 8);
   long long K = 0, c_total = 0;
   if (persistent) {
@@ -673,8 +674,12 @@ decode_attn_kernel(const AttnParams p) {
       int max_cost = 0;
       for (int b0 = 0; b0 < p.B; b0 += 32) {
         const int bb = b0 + lane;
-        const int nv = bb < p.B ? window_len(p, raw_len(p, bb), FUSED) : 0;
-        if (bb < p.B) s_nv[bb] = nv;
+        const int raw = bb < p.B ? raw_len(p, bb) : 0;
+        const int nv = bb < p.B ? window_len(p, raw, FUSED) : 0;
+        if (bb < p.B) {
+          s_nv[bb] = nv;
+          s_raw[bb] = raw;
+        }
         long long v = bb < p.B ? static_cast<long long>(Hkv) * (kItemCost + nv) : 0;
         max_cost = max(max_cost, bb < p.B ? kItemCost + nv : 0);
 #pragma unroll
@@ -761,7 +766,7 @@ decode_attn_kernel(const AttnParams p) {
   auto item_of = [&](const int4 e) -> Item {
     if (persistent) {
       const int b = e.x / Hkv;
-      return make_item_rows<FUSED>(p, T, b, e.x - b * Hkv, e.w & 0xffff, raw_len(p, b), e.y, e.z,
+      return make_item_rows<FUSED>(p, T, b, e.x - b * Hkv, e.w & 0xffff, s_raw[b], e.y, e.z,
                                    e.w >> 16);
     }
     return make_item<FUSED>(p, T, blockIdx.z, blockIdx.y, blockIdx.x, raw_len(p, blockIdx.z), split_len);
@@ -846,7 +851,27 @@ decode_attn_kernel(const AttnParams p) {
       const Item it = item_of(e);
       if (!persistent && it.split >= it.n_act) break;  // outside the window
       const int32_t* bt = p.paged ? p.block_table + static_cast<int64_t>(it.cb) * p.bt_stride : nullptr;
+      // Paged: lane k issues piece k of a tile (the piece that starts the tile, then one
+      // per page).  When every piece of a tile has its own lane, each lane's block-table
+      // entry is loaded one tile ahead, so the load's latency overlaps the wait for a
+      // free stage instead of delaying the copies.
+      const bool ahead = p.paged && (T / p.page_size + 1 <= 32);
+      auto piece_start = [&](int t) -> int {
+        const int row0 = it.r0 + t * T;
+        return lane == 0 ? row0 : (row0 & ~(p.page_size - 1)) + lane * p.page_size;
+      };
+      auto tile_end = [&](int t) -> int { return min(it.r0 + (t + 1) * T, it.r0 + it.n_rows); };
+      int pg_next = -1;
+      if (ahead && it.ntiles > 0) {
+        const int st = piece_start(0);
+        if (st < tile_end(0)) pg_next = __ldcg(bt + (st >> p.page_shift));
+      }
       for (int t = 0; t < it.ntiles; ++t) {
+        const int pg_cur = pg_next;
+        if (ahead && t + 1 < it.ntiles) {
+          const int st = piece_start(t + 1);
+          pg_next = st < tile_end(t + 1) ? __ldcg(bt + (st >> p.page_shift)) : -1;
+        }
         int w = 1;
         if (lane == 0) {
           // pace: the tile issued `inflight` tiles ago has landed (its stage is not
@@ -873,6 +898,21 @@ decode_attn_kernel(const AttnParams p) {
             const size_t off =
                 ((static_cast<size_t>(it.cb) * Hkv + it.g) * p.capacity + row0) * C::ROW_BYTES;
             bulk_g2s(dst, src + off, static_cast<uint32_t>(rows) * C::ROW_BYTES, &full[stage], pol);
+          }
+        } else if (ahead) {
+          const int start = piece_start(t);
+          if (start < row0 + rows) {
+            int page = pg_cur;
+            if (page < 0 || page >= p.n_pages) {
+              set_err(p.err, TTS_EFLAG_PAGE);
+              page = 0;
+            }
+            const int slot = start & (p.page_size - 1);
+            const int n = min(p.page_size - slot, row0 + rows - start);
+            const size_t off =
+                ((static_cast<size_t>(page) * Hkv + it.g) * p.page_size + slot) * C::ROW_BYTES;
+            bulk_g2s(dst + (start - row0) * C::ROW_BYTES, src + off,
+                     static_cast<uint32_t>(n) * C::ROW_BYTES, &full[stage], pol);
           }
         } else {
           const int re = row0 + rows;
@@ -1362,8 +1402,9 @@ decode_attn_kernel(const AttnParams p) {
 constexpr int kMaxCluster = 16;
 
 constexpr int kMaxListStreams = 2048;  // persistent mode keeps per-stream costs in smem
-// 32-bit words of the persistent work list: B + 1 64-bit cost prefix sums, B window lengths
-constexpr int list_ints(int B) { return 2 * (B + 1) + B; }
+// 32-bit words of the persistent work list: B + 1 64-bit cost prefix sums, B window
+// lengths and B window inputs
+constexpr int list_ints(int B) { return 2 * (B + 1) + 2 * B; }
 constexpr int kMaxDevices = 64;
 
 template <typename KvT, int D, int G, bool FUSED>
