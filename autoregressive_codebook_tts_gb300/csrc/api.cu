@@ -177,9 +177,10 @@ tts_status tts_frame_embed(const tts_tables* t, const int32_t* ids, int64_t ids_
   if (t->n_tables < 1 || t->n_tables > TTS_MAX_TABLES || t->vocab < 1 || t->hidden < 4 ||
       t->hidden % 4 != 0 || B < 1 || B > 65535 || ids_stride < t->n_tables)
     return TTS_ERR_SHAPE;
-  if (t->dtype != TTS_F32 && t->dtype != TTS_BF16) return TTS_ERR_DTYPE;
+  if (t->dtype != TTS_F32 && t->dtype != TTS_BF16 && t->dtype != TTS_Q8_0) return TTS_ERR_DTYPE;
+  if (t->dtype == TTS_Q8_0 && t->hidden % 32 != 0) return TTS_ERR_SHAPE;
   EmbedParams p = {};
-  p.tab_bf16 = t->dtype == TTS_BF16;
+  p.tab_dtype = t->dtype;
   for (int i = 0; i < t->n_tables; ++i) {
     if (t->tab[i] == nullptr) return TTS_ERR_NULL;
     if (!aligned16(t->tab[i])) return TTS_ERR_ALIGN;

@@ -10,8 +10,8 @@
 namespace tts {
 
 struct EmbedParams {
-  const void* tab[TTS_MAX_TABLES];  // f32 or bf16 rows (tab_bf16)
-  int tab_bf16;
+  const void* tab[TTS_MAX_TABLES];  // f32, bf16 or Q8_0 rows (tab_dtype)
+  int tab_dtype;                    // tts_dtype
   int n_tables, vocab, hidden;
   const int32_t* ids;
   int64_t ids_stride;

@@ -23,7 +23,8 @@ if not os.path.exists(LIB_PATH):
 
 _lib = ctypes.CDLL(LIB_PATH)
 
-TTS_F32, TTS_BF16 = 0, 1
+TTS_F32, TTS_BF16, TTS_Q8_0 = 0, 1, 2
+Q8_0_BLOCK, Q8_0_BYTES = 32, 34  # entries and bytes of a Q8_0 block
 TTS_MAX_TABLES = 16
 TTS_KV_PREFETCH_BEFORE_WAIT = 1
 
@@ -168,16 +169,24 @@ def kv_desc(B, n_q_heads, n_kv_heads, head_dim, capacity, kv_dtype="f32", window
 
 
 def tables(tabs) -> TtsTables:
-    """Table descriptor for f32 or bf16 tables (all of one dtype)."""
+    """Table descriptor for f32, bf16 or Q8_0 tables (all of one dtype).  A Q8_0 table is
+    a uint8 tensor [vocab][hidden / 32 * 34] of 34-byte blocks (binary16 scale, then 32
+    int8 quants)."""
     t = TtsTables()
     dts = {x.dtype for x in tabs}
-    if len(dts) != 1 or not dts <= {torch.float32, torch.bfloat16}:
-        raise ValueError("codebook tables must all be float32 or all bfloat16")
+    if len(dts) != 1 or not dts <= {torch.float32, torch.bfloat16, torch.uint8}:
+        raise ValueError("codebook tables must all be float32, all bfloat16 or all uint8 (Q8_0)")
     for i, x in enumerate(tabs):
         t.tab[i] = x.data_ptr()
     t.n_tables = len(tabs)
-    t.vocab, t.hidden = tabs[0].shape
-    t.dtype = TTS_BF16 if tabs[0].dtype == torch.bfloat16 else TTS_F32
+    if tabs[0].dtype == torch.uint8:
+        if tabs[0].shape[1] % Q8_0_BYTES:
+            raise ValueError("a Q8_0 row is a whole number of 34-byte blocks")
+        t.vocab, t.hidden = tabs[0].shape[0], tabs[0].shape[1] // Q8_0_BYTES * Q8_0_BLOCK
+        t.dtype = TTS_Q8_0
+    else:
+        t.vocab, t.hidden = tabs[0].shape
+        t.dtype = TTS_BF16 if tabs[0].dtype == torch.bfloat16 else TTS_F32
     return t
 
 

@@ -100,6 +100,23 @@ def tables(n_tables: int, vocab: int, hidden: int, seed: int, std: float = 0.02,
             for _ in range(n_tables)]
 
 
+def q8_0_tables(n_tables: int, vocab: int, hidden: int, seed: int, device="cpu"):
+    """n_tables Q8_0 codebook tables as uint8 [vocab][hidden / 32 * 34]: per 34-byte block
+    a binary16 scale (random magnitude in [1e-4, 4e-4], random sign) then 32 int8 quants
+    uniform in [-127, 127], so entries span about +-0.05 like the f32 tables.  Only random
+    bytes laid out in the block format; no quantisation is done here."""
+    g = _gen(seed)
+    nb = hidden // 32
+    out = []
+    for _ in range(n_tables):
+        mag = torch.rand(vocab, nb, 1, generator=g) * 3e-4 + 1e-4
+        sign = torch.randint(0, 2, (vocab, nb, 1), generator=g) * 2 - 1
+        d = (mag * sign).to(torch.float16).view(torch.uint8).reshape(vocab, nb, 2)
+        q = torch.randint(-127, 128, (vocab, nb, 32), generator=g, dtype=torch.int8).view(torch.uint8)
+        out.append(torch.cat([d, q], dim=2).reshape(vocab, nb * 34).contiguous().to(device))
+    return out
+
+
 def code_ids(B: int, n_tables: int, vocab: int, seed: int) -> torch.Tensor:
     """Code ids uniform in [0, vocab), int32 [B][n_tables]."""
     return torch.randint(0, vocab, (B, n_tables), generator=_gen(seed), dtype=torch.int32)

@@ -64,7 +64,7 @@ extern "C" {
  * tts_abi_min_version() <= V <= tts_abi_version(); tts_abi_check(V) makes that test
  * inside the library and returns TTS_OK, or TTS_ERR_ABI for a V below the minimum or
  * above the current version.  (ABI 2 added tts_tables.dtype; ABI 3 added the `draw`
- * argument of tts_sample and tts_abi_check.) */
+ * argument of tts_sample, tts_abi_check and Q8_0 codebook tables.) */
 #define TTS_ABI_VERSION 3
 #define TTS_ABI_MIN_VERSION 3
 int32_t tts_abi_version(void);
@@ -97,20 +97,29 @@ tts_status tts_abi_check(int32_t caller_version);
 #define TTS_EFLAG_TIMEOUT 16    /* a bounded in-kernel wait ran out; output invalid;
                                    re-zero the call's workspace before its next use */
 
-typedef enum { TTS_F32 = 0, TTS_BF16 = 1 } tts_dtype;
+/* Element types.  KV caches: f32 or bf16.  Codebook tables: f32, bf16 or Q8_0. */
+typedef enum { TTS_F32 = 0, TTS_BF16 = 1, TTS_Q8_0 = 2 } tts_dtype;
 
 #define TTS_MAX_TABLES 16
 
 /* Codebook tables for the frame-input composition.  tab[g] points to a dense row-major
- * [vocab][hidden] table of element type `dtype` (f32, or bf16 -- [P-pipeline] TTFA
- * section: the gather works on any table type); only the first n_tables entries are
- * read.  (ABI 2 added `dtype`.) */
+ * table of `vocab` rows of `hidden` entries of element type `dtype` ([P-pipeline] TTFA /
+ * prompt-build section: the tables are gathered whatever their type, "any quant via
+ * get_rows"; its TTFA measurements use Q8_0 tables); only the first n_tables entries
+ * are read.
+ *   TTS_F32:  4 bytes an entry.
+ *   TTS_BF16: 2 bytes an entry; an entry enters the sum widened to f32 exactly.
+ *   TTS_Q8_0: blocks of 32 consecutive entries of a row, 34 bytes a block (a binary16
+ *             scale d, then 32 signed 8-bit quants q); a row is hidden/32 blocks,
+ *             hidden a multiple of 32.  An entry is the f32 product d * q, which is
+ *             exact (a GGUF Q8_0 tensor has this layout).
+ * (ABI 2 added `dtype`; ABI 3 added TTS_Q8_0.) */
 typedef struct {
   const void* tab[TTS_MAX_TABLES];
   int32_t n_tables; /* 1..16 */
   int32_t vocab;    /* rows per table */
-  int32_t hidden;   /* row length in elements, a multiple of 4 */
-  int32_t dtype;    /* tts_dtype of every table */
+  int32_t hidden;   /* row length in elements, a multiple of 4 (of 32 for Q8_0) */
+  int32_t dtype;    /* tts_dtype of every table: TTS_F32, TTS_BF16 or TTS_Q8_0 */
 } tts_tables;
 
 /* Flags of tts_kv_desc.flags */
@@ -153,7 +162,8 @@ typedef struct {
  *   out[b] = ((tab[0][ids[b][0]] + tab[1][ids[b][1]]) + ... ) + overlay[b]
  * in f32, codebooks in ascending order, the overlay added last; the result is
  * bit-identical to that sequence of single f32 additions.  bf16 table entries are
- * widened to f32 exactly before they are added.  For a code-predictor
+ * widened to f32 exactly, Q8_0 entries are the exact f32 product d * q, before they
+ * are added.  For a code-predictor
  * sub-step pass one group table (n_tables = 1) and overlay = NULL.
  *   ids:     device int32 [B][ids_stride], first n_tables entries per row read.
  *   overlay: device f32 rows of `hidden`, row stride overlay_stride; or NULL.

@@ -118,6 +118,23 @@ def bf16_rne_array(x) -> np.ndarray:
     return out
 
 
+def q8_0_dequant(t) -> np.ndarray:
+    """Entries of a Q8_0 table as f32.  t: uint8 [vocab][n_blocks * 34]; each 34-byte block
+    holds 32 consecutive entries of a row: a little-endian IEEE binary16 scale d, then 32
+    two's-complement int8 quants q; an entry is d * q.  d widens to f32 exactly and the
+    product of an 11-bit and an 8-bit significand is exact in f32 ("qwentts.cpp ...
+    src/pipeline-tts.h", TTFA / prompt-build section: the tables are gathered whatever
+    their quantisation; its TTFA measurements use Q8_0 tables)."""
+    t = np.ascontiguousarray(np.asarray(t, dtype=np.uint8))
+    vocab, nbytes = t.shape
+    if nbytes % 34:
+        raise ValueError("a Q8_0 row is a whole number of 34-byte blocks")
+    blocks = t.reshape(vocab, nbytes // 34, 34)
+    d = np.ascontiguousarray(blocks[:, :, :2]).view("<f2").astype(np.float32)    # [vocab][nb][1]
+    q = np.ascontiguousarray(blocks[:, :, 2:]).view(np.int8).astype(np.float32)  # [vocab][nb][32]
+    return (d * q).reshape(vocab, -1)
+
+
 def bf16_bits_to_f32(h) -> np.ndarray:
     """Exact widening of bf16 bit patterns (uint16) to f32: the bf16 bits become the high
     half of the f32 (how a bf16 table entry or cache row enters f32 arithmetic; "qwentts.cpp
@@ -133,13 +150,20 @@ def bf16_bits_to_f32(h) -> np.ndarray:
 def frame_embed(tables, ids, overlay=None):
     """out[b] = ((E_0[c_b0] + E_1[c_b1]) + ... ) + overlay[b], f32, fixed order.
 
-    tables: list of [vocab][hidden] arrays, f32, or uint16 holding bf16 bit patterns
-    (the "TTFA / prompt build" section's gather of any table type: a bf16 entry is
-    widened to f32 exactly, then added like an f32 one); ids: [B][n_tables] int32;
-    overlay: [B][hidden] f32 or None.  Returns (out [B][hidden] f32, clamped flag).
+    tables: list of [vocab][hidden] arrays, f32, or uint16 holding bf16 bit patterns, or
+    uint8 Q8_0 rows [vocab][hidden / 32 * 34] (the "TTFA / prompt build" section's gather of
+    any table type: a bf16 entry is widened to f32 exactly, a Q8_0 entry is its exact f32
+    product d * q, then added like an f32 one); ids: [B][n_tables] int32; overlay:
+    [B][hidden] f32 or None.  Returns (out [B][hidden] f32, clamped flag).
     """
-    tabs = [bf16_bits_to_f32(t) if np.asarray(t).dtype == np.uint16 else _c(t, np.float32)
-            for t in tables]
+    def as_f32(t):
+        dt = np.asarray(t).dtype
+        if dt == np.uint16:
+            return bf16_bits_to_f32(t)
+        if dt == np.uint8:
+            return q8_0_dequant(t)
+        return _c(t, np.float32)
+    tabs = [as_f32(t) for t in tables]
     ids = _c(ids, np.int32)
     B, n = ids.shape
     vocab, hidden = tabs[0].shape

@@ -132,6 +132,9 @@ def test_prefill_sampler_and_table_dtype_validate(tts):
     t = tts.TtsTables()
     t.n_tables, t.vocab, t.hidden, t.dtype = 1, 2048, 1024, 5
     assert tts._lib.tts_frame_embed(ctypes.byref(t), P(16), 16, None, 0, P(16), 1, None, None) == 3
+    t.tab[0] = 16
+    t.dtype, t.hidden = tts.TTS_Q8_0, 1000                     # Q8_0 rows are whole 32-entry blocks
+    assert tts._lib.tts_frame_embed(ctypes.byref(t), P(16), 16, None, 0, P(16), 1, None, None) == 2
 
     d = tts.kv_desc(2, 16, 8, 128, 4096)
 
@@ -213,7 +216,8 @@ def test_binding_constants_match_the_header(tts):
         assert getattr(tts, "EFLAG_" + name) == defines["TTS_EFLAG_" + name]
     assert tts._lib.tts_abi_version() == defines["TTS_ABI_VERSION"]
     assert tts._lib.tts_abi_min_version() == defines["TTS_ABI_MIN_VERSION"]
-    dt = dict(re.findall(r"(TTS_F32|TTS_BF16) = (\d+)", src))
-    assert (tts.TTS_F32, tts.TTS_BF16) == (int(dt["TTS_F32"]), int(dt["TTS_BF16"]))
+    dt = dict(re.findall(r"(TTS_F32|TTS_BF16|TTS_Q8_0) = (\d+)", src))
+    assert (tts.TTS_F32, tts.TTS_BF16, tts.TTS_Q8_0) == (int(dt["TTS_F32"]), int(dt["TTS_BF16"]),
+                                                          int(dt["TTS_Q8_0"]))
     for name, code in re.findall(r"\b(TTS_(?:OK|ERR_[A-Z]+)) = (\d+)", src):
         assert tts._lib.tts_status_str(int(code)).decode() == name

@@ -615,6 +615,70 @@ def test_prefill_first_query_of_an_empty_cache_is_its_own_value_row():
     assert np.isfinite(out).all()
 
 
+def _q8_block(d_bits, qs):
+    """One 34-byte Q8_0 block from a binary16 bit pattern and up to 32 quants (rest 0)."""
+    q = list(qs) + [0] * (32 - len(qs))
+    return bytes([d_bits & 0xFF, d_bits >> 8]) + bytes([v & 0xFF for v in q])
+
+
+def test_q8_0_entries_hand_derived():
+    """Every golden row is its own block in a one-row table; the gathered row holds d * q
+    at the block's first entry and 0 at the rest (entry = scale times quant)."""
+    rows = read_golden("q8_0_blocks.txt")
+    blob = b"".join(_q8_block(int(d, 16), [int(q)]) for d, q, _ in rows)
+    tab = np.frombuffer(blob, np.uint8).reshape(1, -1)
+    out, flag = oracle.frame_embed([tab], np.zeros((1, 1), np.int32), None)
+    assert flag == 0
+    got = out.reshape(len(rows), 32)
+    for k, (_, _, expect) in enumerate(rows):
+        assert got[k, 0] == np.float32(float(expect)), (k, got[k, 0], expect)
+        assert np.all(got[k, 1:] == 0.0)
+
+
+def test_q8_0_block_layout_and_row_addressing():
+    """Entry i of a row comes from block i // 32, quant i % 32; row r starts r * 34 *
+    hidden / 32 bytes in; scales of 2^k times quants equal to the column index give an
+    exact closed form for every entry of every row."""
+    vocab, hidden = 5, 96
+    nb = hidden // 32
+    blob = b""
+    for r in range(vocab):
+        for k in range(nb):
+            # d = 2^(r - k) as binary16: exponent field 15 + r - k, zero mantissa
+            d_bits = (15 + r - k) << 10
+            blob += _q8_block(d_bits, [(j + 32 * k) % 100 - 50 for j in range(32)])
+    tab = np.frombuffer(blob, np.uint8).reshape(vocab, -1)
+    ids = np.array([[4], [0], [2]], np.int32)
+    out, _ = oracle.frame_embed([tab], ids, None)
+    for b, r in enumerate([4, 0, 2]):
+        for i in range(hidden):
+            k, j = divmod(i, 32)
+            assert out[b, i] == np.float32((i % 100 - 50) * 2.0 ** (r - k))
+
+
+def test_q8_0_sum_of_sixteen_tables_closed_form():
+    """Sixteen Q8_0 tables with power-of-two scales and small quants: every partial sum
+    is exact in f32, so the gather-sum equals the exact rational sum."""
+    vocab, hidden, B = 8, 64, 3
+    rng = np.random.default_rng(71)
+    tabs, vals = [], []
+    for g in range(16):
+        blob, v = b"", np.zeros((vocab, hidden))
+        for r in range(vocab):
+            for k in range(hidden // 32):
+                e = int(rng.integers(-6, 3))
+                qs = [int(x) for x in rng.integers(-20, 21, 32)]
+                blob += _q8_block((15 + e) << 10, qs)
+                v[r, 32 * k:32 * k + 32] = np.array(qs) * 2.0 ** e
+        tabs.append(np.frombuffer(blob, np.uint8).reshape(vocab, -1))
+        vals.append(v)
+    ids = rng.integers(0, vocab, (B, 16)).astype(np.int32)
+    ov = (rng.integers(-8, 9, (B, hidden)) * 2.0 ** -4).astype(np.float32)
+    out, _ = oracle.frame_embed(tabs, ids, ov)
+    exact = sum(vals[g][ids[:, g]] for g in range(16)) + ov
+    assert np.array_equal(out.astype(np.float64), exact)
+
+
 def test_embed_bf16_tables_closed_form():
     """bf16 tables (bit patterns): entries (g + 1) + c/8 are exact in bf16 and every
     partial sum is exact in f32, so out = sum_g ((g + 1) + c_g / 8) + overlay exactly."""

@@ -77,6 +77,27 @@ def test_frame_embed_bf16_tables_bit_exact(tts, n_tables, hidden, B, overlay):
     assert np.array_equal(bits(out.cpu().numpy()), bits(ref))
 
 
+@pytest.mark.parametrize("n_tables,hidden,B,overlay", [
+    (16, 2048, 32, True),    # batched talker frame from Q8_0 tables
+    (1, 1024, 32, False),    # predictor sub-step
+    (3, 32, 5, True),        # one block per row
+])
+def test_frame_embed_q8_0_tables_bit_exact(tts, n_tables, hidden, B, overlay):
+    """Q8_0 codebook tables (34-byte blocks: binary16 scale, 32 int8 quants): every entry
+    is the exact f32 product scale * quant, then the same f32 sum as for f32 tables."""
+    tabs = W.q8_0_tables(n_tables, 2048, hidden, seed=6)
+    ids = W.code_ids(B, n_tables, 2048, seed=7)
+    ov = W.overlay(B, hidden, seed=8) if overlay else None
+    ref, flag = oracle.frame_embed([t.numpy() for t in tabs], ids.numpy(),
+                                   None if ov is None else ov.numpy())
+    out = torch.full((B, hidden), float("nan"), device="cuda")
+    ef = err_flag()
+    tts.tts_frame_embed([t.cuda() for t in tabs], ids.cuda(), None if ov is None else ov.cuda(), out, ef)
+    torch.cuda.synchronize()
+    assert flag == 0 and ef.item() == 0
+    assert np.array_equal(bits(out.cpu().numpy()), bits(ref))
+
+
 def test_frame_embed_clamps_and_flags_bad_ids(tts):
     tabs = W.tables(3, 64, 16, seed=3)
     ids = torch.tensor([[0, 70, 5], [-3, 1, 63]], dtype=torch.int32)
