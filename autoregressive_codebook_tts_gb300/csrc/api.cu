@@ -466,22 +466,38 @@ tts_status tts_counter_advance(uint64_t* counter, uint64_t by, void* stream) {
 
 namespace {
 
+// From this many streams on the layer's projections run on the tensor cores.
+#ifndef TTS_MMA_MIN_STREAMS
+#define TTS_MMA_MIN_STREAMS 4
+#endif
+constexpr int kMmaMinStreams = TTS_MMA_MIN_STREAMS;
+
 // Scratch of a decode layer, 256-byte regions: a (bf16 [B][inter], the SiLU-multiply
-// output), the qkv rows (f32), the attention output (f32 [B][Hq D]), then the
-// attention workspace.
+// output), the qkv rows (f32), the attention output (f32 [B][Hq D]), the attention
+// workspace, then (from kMmaMinStreams streams on) the tensor-core GEMVs' tickets and
+// partial sums, sized for the largest of the four projections.
 struct LayerScratch {
-  size_t a_off, qkv_off, attn_off, ws_off, total;
+  size_t a_off, qkv_off, attn_off, ws_off, mma_off, mma_bytes, total;
 };
 LayerScratch layer_scratch(const tts_kv_desc* d, int hidden, int inter, int n_splits) {
   LayerScratch L;
   const size_t B = static_cast<size_t>(d->B);
-  const size_t width = static_cast<size_t>(d->n_q_heads + 2 * d->n_kv_heads) * d->head_dim;
-  (void)hidden;
+  const int qd = d->n_q_heads * d->head_dim;
+  const int width = (d->n_q_heads + 2 * d->n_kv_heads) * d->head_dim;
   L.a_off = 0;
   L.qkv_off = round256(B * inter * 2);
   L.attn_off = L.qkv_off + round256(B * width * 4);
-  L.ws_off = L.attn_off + round256(B * d->n_q_heads * d->head_dim * 4);
-  L.total = L.ws_off + round256(tts_decode_attn_workspace_size(d, n_splits));
+  L.ws_off = L.attn_off + round256(B * qd * 4);
+  L.mma_off = L.ws_off + round256(tts_decode_attn_workspace_size(d, n_splits));
+  L.mma_bytes = 0;
+  if (d->B >= kMmaMinStreams) {
+    const int sms = sm_count();
+    const int nb = d->B <= 16 ? 16 : 32;
+    const size_t w[4] = {gemv_mma_workspace(hidden, width, 0, 2, sms, nb), gemv_mma_workspace(qd, hidden, 1, 1, sms, nb),
+                         gemv_mma_workspace(hidden, inter, 2, 2, sms, nb), gemv_mma_workspace(inter, hidden, 1, 0, sms, nb)};
+    for (size_t x : w) L.mma_bytes = x > L.mma_bytes ? x : L.mma_bytes;
+  }
+  L.total = L.mma_off + round256(L.mma_bytes);
   return L;
 }
 
@@ -511,10 +527,11 @@ tts_status tts_decode_layer(float* h, const tts_layer_weights* w, float eps, con
   const int qd = d->n_q_heads * d->head_dim;
   const int kd = d->n_kv_heads * d->head_dim;
   const int width = qd + 2 * kd;
-  if (B > kGemvMaxB || !layer_dim_ok(H) || !layer_dim_ok(I) || !layer_dim_ok(qd) || !(eps >= 0.f))
+  if (B > kGemvMmaMaxB || !layer_dim_ok(H) || !layer_dim_ok(I) || !layer_dim_ok(qd) || !(eps >= 0.f))
     return TTS_ERR_SHAPE;
   if (!aligned16(h) || !aligned16(w->w_qkv) || !aligned16(w->w_o) || !aligned16(w->w_gu) ||
-      !aligned16(w->w_down) || (reinterpret_cast<uintptr_t>(scratch) & 255u) != 0)
+      !aligned16(w->w_down) || !aligned16(w->gamma_attn) || !aligned16(w->gamma_mlp) ||
+      (reinterpret_cast<uintptr_t>(scratch) & 255u) != 0)
     return TTS_ERR_ALIGN;
   const LayerScratch L = layer_scratch(d, H, I, n_splits);
   if (scratch_bytes < L.total) return TTS_ERR_WORKSPACE;
@@ -523,11 +540,19 @@ tts_status tts_decode_layer(float* h, const tts_layer_weights* w, float eps, con
   float* qkv = reinterpret_cast<float*>(sc + L.qkv_off);
   float* attn = reinterpret_cast<float*>(sc + L.attn_off);
   cudaStream_t s = as_stream(stream);
+  const int sms = sm_count();
+  // one stream: the ring GEMV; 2..kMmaMinStreams-1: the register GEMV; from
+  // kMmaMinStreams on: the tensor-core GEMV
+  auto gemv = [&](const GemvParams& g, int x_mode, int epilogue) -> cudaError_t {
+    if (B >= kMmaMinStreams)
+      return launch_gemv_mma(g, x_mode, epilogue, sc + L.mma_off, L.mma_bytes, sms, s);
+    return launch_gemv_bf16(g, x_mode, epilogue, s);
+  };
   // qkv = bf16(rmsnorm(h)) W_qkv^T
   GemvParams g = {};
   g.x = h; g.x_stride = H; g.gamma = w->gamma_attn; g.eps = eps;
   g.w = w->w_qkv; g.n_out = width; g.K = H; g.B = B; g.y = qkv; g.y_stride = width; g.err = err_flag;
-  cudaError_t e = launch_gemv_bf16(g, 2, 0, s);
+  cudaError_t e = gemv(g, 2, 0);
   if (e != cudaSuccess) return from_cuda(e);
   // One stream: the qkv GEMV's CTAs hold one slot of every SM while the attention's
   // first CTAs start, so about 1.4 attention CTAs per SM (fewer, longer splits than the
@@ -547,17 +572,17 @@ tts_status tts_decode_layer(float* h, const tts_layer_weights* w, float eps, con
   g = {};
   g.x = attn; g.x_stride = qd; g.w = w->w_o; g.n_out = H; g.K = qd; g.B = B; g.y = h; g.y_stride = H;
   g.err = err_flag;
-  if ((e = launch_gemv_bf16(g, 1, 1, s)) != cudaSuccess) return from_cuda(e);
+  if ((e = gemv(g, 1, 1)) != cudaSuccess) return from_cuda(e);
   // a = bf16(silu(x W_gate^T) * x W_up^T), x = bf16(rmsnorm(h))
   g = {};
   g.x = h; g.x_stride = H; g.gamma = w->gamma_mlp; g.eps = eps;
   g.w = w->w_gu; g.n_out = I; g.K = H; g.B = B; g.inter = I; g.y = a; g.y_stride = I; g.err = err_flag;
-  if ((e = launch_gemv_bf16(g, 2, 2, s)) != cudaSuccess) return from_cuda(e);
+  if ((e = gemv(g, 2, 2)) != cudaSuccess) return from_cuda(e);
   // h += a W_down^T
   g = {};
   g.x = a; g.x_stride = I; g.w = w->w_down; g.n_out = H; g.K = I; g.B = B; g.y = h; g.y_stride = H;
   g.err = err_flag;
-  return from_cuda(launch_gemv_bf16(g, 0, 1, s));
+  return from_cuda(gemv(g, 0, 1));
 }
 
 }  // extern "C"

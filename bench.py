@@ -41,7 +41,7 @@ def parse():
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--workload", default="batched",
                     choices=["talker", "batched", "paged", "prefill", "predictor", "layer"])
-    ap.add_argument("--layer-streams", type=int, default=1, help="layer: streams (1..8)")
+    ap.add_argument("--layer-streams", type=int, default=1, help="layer: streams (1..32)")
     ap.add_argument("--frames-per-replay", type=int, default=4,
                     help="predictor: frames unrolled into one graph replay")
     ap.add_argument("--layers", type=int, default=0,

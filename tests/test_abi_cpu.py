@@ -195,7 +195,7 @@ def test_decode_layer_validates(tts):
     assert layer(w=weights(w_qkv=0)) == 1
     assert layer(w=weights(gamma_attn=0)) == 1
     assert layer(sc=0) == 1
-    assert layer(desc=tts.kv_desc(9, 16, 8, 128, 4096)) == 2    # more than eight streams
+    assert layer(desc=tts.kv_desc(33, 16, 8, 128, 4096)) == 2   # more than 32 streams
     assert layer(w=weights(hidden=2000)) == 2
     assert layer(w=weights(inter=9216)) == 2
     assert layer(eps=-1.0) == 2

@@ -4,7 +4,8 @@ oracle's decode_layer: the residual stream after the layer within 1e-3 per strea
 products in f32 where the oracle sums them exactly, so a bf16 rounding of an
 intermediate (the norm output, the attention output, the SiLU product) can land one
 bf16 step apart; such a step moves the layer's output by about 2^-8 of one product
-term, far inside the bound."""
+term, far inside the bound.  From four streams on the projections run on the tensor
+cores, whose f32 accumulation order differs again; the bound covers it the same way."""
 import numpy as np
 import pytest
 import torch
@@ -44,10 +45,19 @@ SMALL_768 = dict(hidden=768, n_q_heads=4, n_kv_heads=2, capacity=512)
 SMALL_1280 = dict(hidden=1280, n_q_heads=8, n_kv_heads=2, capacity=512)
 
 
+# From four streams on the projections run on the tensor cores (tcgen05): 16 and 32
+# streams use the MMA's N of 16 and 32, the small layers odd tile counts and column
+# ranges (hidden 768: six 128-row tiles of the output projections, 2304 SiLU items).
+STREAMS_16 = [3, 40, 97, 130, 200, 255, 256, 300, 311, 350, 400, 401, 450, 480, 500, 511]
+STREAMS_32 = [(b * 37) % 512 for b in range(32)]
+
+
 @pytest.mark.parametrize("B,cur,shape", [(1, [4095], {}), (1, [100], {}), (2, [10, 4000], {}), (4, [7, 1000, 2047, 3000], {}),
                                          (8, [300] * 8, {}), (3, [5, 200, 511], SMALL_768),
                                          (5, [0, 1, 64, 300, 511], SMALL_1280), (1, [300], SMALL_768),
-                                         (1, [511], SMALL_1280)])
+                                         (1, [511], SMALL_1280), (16, STREAMS_16, dict(capacity=512)),
+                                         (32, STREAMS_32, dict(capacity=512)),
+                                         (7, [1, 2, 3, 4, 5, 6, 7], SMALL_768)])
 def test_decode_layer_matches_oracle(tts, B, cur, shape):
     w = W.workload("talker", B=B, layers=1, **shape)
     H, I, Hq, Hkv, D = w.hidden, 3 * w.hidden, w.n_q_heads, w.n_kv_heads, w.head_dim
@@ -85,16 +95,16 @@ def test_decode_layer_matches_oracle(tts, B, cur, shape):
     np.testing.assert_allclose(gv[mask], hv[mask], rtol=1e-4, atol=1e-4)
 
 
-def test_decode_layer_rejects_more_than_eight_streams(tts):
-    w = W.workload("talker", B=9, layers=1)
-    desc = tts.kv_desc(9, 16, 8, 128, 4096)
+def test_decode_layer_rejects_more_than_32_streams(tts):
+    w = W.workload("talker", B=33, layers=1)
+    desc = tts.kv_desc(33, 16, 8, 128, 4096)
     assert tts.tts_decode_layer_scratch_size(desc, 2048, 6144) > 0
     wt = {k: v.cuda() for k, v in _weights(2048, 6144, 16, 8, 128, 83).items()}
     lw = tts.layer_weights(wt["w_qkv"], wt["w_o"], wt["w_gu"], wt["w_down"], wt["gamma_attn"],
                            wt["gamma_mlp"], wt["gamma_q"], wt["gamma_k"])
-    h = torch.zeros(9, 2048, device="cuda")
-    K = torch.zeros(9, 8, 4096, 128, device="cuda")
-    cur = torch.zeros(9, dtype=torch.int32, device="cuda")
+    h = torch.zeros(33, 2048, device="cuda")
+    K = torch.zeros(33, 8, 16, 128, device="cuda")  # never read: the call is refused first
+    cur = torch.zeros(33, dtype=torch.int32, device="cuda")
     cs = rope_table(tts, 4096, 128, w.rope_base)
     with pytest.raises(tts.TtsError) as e:
         tts.tts_decode_layer(h, lw, 1e-6, cs, 4096, K, K, desc, cur, 0.1,
