@@ -472,32 +472,28 @@ namespace {
 #endif
 constexpr int kMmaMinStreams = TTS_MMA_MIN_STREAMS;
 
-// Scratch of a decode layer, 256-byte regions: a (bf16 [B][inter], the SiLU-multiply
-// output), the qkv rows (f32), the attention output (f32 [B][Hq D]), the attention
-// workspace, then (from kMmaMinStreams streams on) the tensor-core GEMVs' tickets and
-// partial sums, sized for the largest of the four projections.
+// Scratch of a decode layer, 256-byte regions: a (the SiLU-multiply output, bf16: [B][inter]
+// rows below kMmaMinStreams streams, else packed for the tensor-core down projection,
+// [inter / 8][slots][8]), the qkv rows (f32), the attention output (f32 [B][Hq D]), the
+// attention workspace, then (from kMmaMinStreams streams on) the packed activations of
+// the other three projections (bf16, max(hidden, Hq D) x slots).
 struct LayerScratch {
-  size_t a_off, qkv_off, attn_off, ws_off, mma_off, mma_bytes, total;
+  size_t a_off, qkv_off, attn_off, ws_off, xp_off, total;
 };
 LayerScratch layer_scratch(const tts_kv_desc* d, int hidden, int inter, int n_splits) {
   LayerScratch L;
+  const bool mma = d->B >= kMmaMinStreams;
   const size_t B = static_cast<size_t>(d->B);
+  const size_t rows = mma ? static_cast<size_t>(gemv_mma_slots(d->B)) : B;
   const int qd = d->n_q_heads * d->head_dim;
   const int width = (d->n_q_heads + 2 * d->n_kv_heads) * d->head_dim;
   L.a_off = 0;
-  L.qkv_off = round256(B * inter * 2);
+  L.qkv_off = round256(rows * inter * 2);
   L.attn_off = L.qkv_off + round256(B * width * 4);
   L.ws_off = L.attn_off + round256(B * qd * 4);
-  L.mma_off = L.ws_off + round256(tts_decode_attn_workspace_size(d, n_splits));
-  L.mma_bytes = 0;
-  if (d->B >= kMmaMinStreams) {
-    const int sms = sm_count();
-    const int nb = d->B <= 16 ? 16 : 32;
-    const size_t w[4] = {gemv_mma_workspace(hidden, width, 0, 2, sms, nb), gemv_mma_workspace(qd, hidden, 1, 1, sms, nb),
-                         gemv_mma_workspace(hidden, inter, 2, 2, sms, nb), gemv_mma_workspace(inter, hidden, 1, 0, sms, nb)};
-    for (size_t x : w) L.mma_bytes = x > L.mma_bytes ? x : L.mma_bytes;
-  }
-  L.total = L.mma_off + round256(L.mma_bytes);
+  L.xp_off = L.ws_off + round256(tts_decode_attn_workspace_size(d, n_splits));
+  const size_t kx = static_cast<size_t>(hidden > qd ? hidden : qd);
+  L.total = L.xp_off + (mma ? round256(rows * kx * 2) : 0);
   return L;
 }
 
@@ -544,8 +540,7 @@ tts_status tts_decode_layer(float* h, const tts_layer_weights* w, float eps, con
   // one stream: the ring GEMV; 2..kMmaMinStreams-1: the register GEMV; from
   // kMmaMinStreams on: the tensor-core GEMV
   auto gemv = [&](const GemvParams& g, int x_mode, int epilogue) -> cudaError_t {
-    if (B >= kMmaMinStreams)
-      return launch_gemv_mma(g, x_mode, epilogue, sc + L.mma_off, L.mma_bytes, sms, s);
+    if (B >= kMmaMinStreams) return launch_gemv_mma(g, x_mode, epilogue, sc + L.xp_off, sms, s);
     return launch_gemv_bf16(g, x_mode, epilogue, s);
   };
   // qkv = bf16(rmsnorm(h)) W_qkv^T

@@ -161,13 +161,15 @@ cudaError_t launch_counter_advance(uint64_t* counter, uint64_t by, cudaStream_t 
 // f32 input; epilogue 0: store f32, 1: add into f32 (residual), 2: SiLU-multiply to bf16.
 // The pairs built are (2, 0), (1, 1), (2, 2) and (0, 1); B is 1..8.
 cudaError_t launch_gemv_bf16(const GemvParams& p, int x_mode, int epilogue, cudaStream_t s);
-// The same GEMVs on the tensor cores (gemv_mma.cu) for 1..kGemvMmaMaxB streams; K a
-// multiple of 64; `workspace` (zeroed once, left zeroed by every launch) of at least
-// gemv_mma_workspace() bytes holds split tickets and partial sums.
+// The same GEMVs on the tensor cores (gemv_mma.cu) for 1..kGemvMmaMaxB streams, K a
+// multiple of 64.  The activations go in packed for the MMA, P[k / 8][slot][k % 8] bf16
+// for gemv_mma_slots(B) stream slots: x_mode 0 takes p.x in that layout (what the
+// SiLU-multiply epilogue writes, into p.y, y_stride unused); x_mode 1 (f32 rows) and 2
+// (RMS norm of f32 rows times gamma) pack p.x into `xpack` (K x slots bf16, 16-byte
+// aligned) with a small kernel launched first.
 constexpr int kGemvMmaMaxB = 32;
-size_t gemv_mma_workspace(int K, int n_out, int epilogue, int x_mode, int n_sm, int nb);
-cudaError_t launch_gemv_mma(const GemvParams& p, int x_mode, int epilogue, void* workspace, size_t ws_bytes,
-                            int n_sm, cudaStream_t s);
+int gemv_mma_slots(int B);
+cudaError_t launch_gemv_mma(const GemvParams& p, int x_mode, int epilogue, void* xpack, int n_sm, cudaStream_t s);
 
 // Tile geometry of the attention kernel for a (dtype, head_dim) pair.
 struct AttnGeometry {
