@@ -536,11 +536,10 @@ tts_status tts_decode_layer(float* h, const tts_layer_weights* w, float eps, con
   float* qkv = reinterpret_cast<float*>(sc + L.qkv_off);
   float* attn = reinterpret_cast<float*>(sc + L.attn_off);
   cudaStream_t s = as_stream(stream);
-  const int sms = sm_count();
   // one stream: the ring GEMV; 2..kMmaMinStreams-1: the register GEMV; from
   // kMmaMinStreams on: the tensor-core GEMV
   auto gemv = [&](const GemvParams& g, int x_mode, int epilogue) -> cudaError_t {
-    if (B >= kMmaMinStreams) return launch_gemv_mma(g, x_mode, epilogue, sc + L.xp_off, sms, s);
+    if (B >= kMmaMinStreams) return launch_gemv_mma(g, x_mode, epilogue, sc + L.xp_off, s);
     return launch_gemv_bf16(g, x_mode, epilogue, s);
   };
   // qkv = bf16(rmsnorm(h)) W_qkv^T

@@ -13,18 +13,21 @@
 //     K-major core-matrix layout the MMA reads, P[k / 8][slot][k % 8] for NB = 16 or 32
 //     stream slots (slots >= B zero); the SiLU-multiply epilogue writes its output in
 //     that layout directly, ready for the down projection;
-//   * one CTA per (tile of 128 weight rows, range of kc columns); for the SiLU-multiply
+//   * one CTA per (tile of 128 weight rows, range of columns); for the SiLU-multiply
 //     a tile is 64 gate rows and their 64 up rows.  The tile is the MMA's M = 128
 //     operand, the streams its N and K steps of 16.  The column ranges of a tile form
 //     one thread-block cluster;
-//   * warp 4 streams stages of 64 columns through a shared-memory ring: the weight tile
-//     (16 KB) by a 2-D TMA tensor load in the 128-byte swizzled K-major layout, and the
-//     matching NB x 64 activation chunk (contiguous in the packed layout) by a 1-D bulk
-//     copy, both on the stage's mbarrier.  Weights are constants, so the first stages'
-//     weight loads start before the dependency wait;
+//   * warp 4 streams stages of 256 columns through a shared-memory ring: the weights
+//     (64 KB: four 128-row x 64-column sub-tiles in the 128-byte swizzled K-major layout)
+//     by ONE 3-D (SiLU-multiply: 4-D) TMA tensor load, and the matching NB x 256
+//     activation chunk (contiguous in the packed layout) by one 1-D bulk copy, both on
+//     the stage's mbarrier.  An SM keeps only a few bulk copies in flight, so its
+//     streaming rate grows with the bytes per copy: 16 KB copies stop near 50 GB/s an SM,
+//     far below HBM's share.  Weights are constants, so the first stages' weight loads
+//     start before the dependency wait;
 //   * lane 0 of warp 5 issues tcgen05.mma (f32 accumulator in tensor memory, 32 columns
-//     allocated by warp 5), four per stage, and commits each stage back to the producer,
-//     then the whole tile to the epilogue;
+//     allocated by warp 5), sixteen per stage, and commits each stage back to the
+//     producer, then the whole tile to the epilogue;
 //   * warps 0..3 read the accumulator back (tcgen05.ld, one row a thread, one column a
 //     stream) into shared memory; after a cluster barrier CTA r of the cluster sums the
 //     ranges' partials of its 128 / S rows from every CTA's shared memory, in rank order
@@ -33,7 +36,9 @@
 // Every mbarrier wait is bounded; on expiry TTS_EFLAG_TIMEOUT is set and the CTA winds
 // down (it still reaches both cluster barriers, so its peers never wait on it).
 #include <cstdint>
+#include <map>
 #include <mutex>
+#include <tuple>
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -44,15 +49,61 @@
 #include "kernels.h"
 
 namespace tts {
+
+#ifdef TTS_TRACE
+// Optional timeline of the projections (build with -DTTS_TRACE): one row per CTA of
+// every launch, appended in start order: a tag (kind, grid, block, SM) and %globaltimer
+// stamps at entry, after the dependency wait, when the accumulator is complete and at
+// exit; read with tts_gtrace_read().
+constexpr int kGTraceRows = 65536;
+__device__ unsigned long long g_gtrace[kGTraceRows][8];
+__device__ unsigned int g_gtrace_n;
+__device__ __forceinline__ unsigned long long gtrace_time() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ unsigned int gtrace_smid() {
+  unsigned int r;
+  asm volatile("mov.u32 %0, %%smid;" : "=r"(r));
+  return r;
+}
+#define TTS_GTRACE_BEGIN(kind, row_var)                                                             \
+  __shared__ unsigned int row_var;                                                                 \
+  if (threadIdx.x == 0) {                                                                          \
+    const unsigned long long t_ = gtrace_time();                                                   \
+    row_var = atomicAdd(&g_gtrace_n, 1u);                                                          \
+    if (row_var < kGTraceRows) {                                                                   \
+      g_gtrace[row_var][0] = (static_cast<unsigned long long>(kind)) |                             \
+                             (static_cast<unsigned long long>(gridDim.x) << 8) |                   \
+                             (static_cast<unsigned long long>(gridDim.y) << 20) |                  \
+                             (static_cast<unsigned long long>(blockIdx.x) << 28) |                 \
+                             (static_cast<unsigned long long>(blockIdx.y) << 40) |                 \
+                             (static_cast<unsigned long long>(gtrace_smid()) << 48);               \
+      g_gtrace[row_var][1] = t_;                                                                   \
+    }                                                                                              \
+  }
+#define TTS_GTRACE(row_var, slot)                                                                   \
+  do {                                                                                             \
+    if ((row_var) < kGTraceRows) g_gtrace[(row_var)][slot] = gtrace_time();                        \
+  } while (0)
+#else
+#define TTS_GTRACE_BEGIN(kind, row_var)
+#define TTS_GTRACE(row_var, slot) do {} while (0)
+#endif
+
 namespace {
 
 enum Epilogue { EPI_STORE = 0, EPI_RESIDUAL = 1, EPI_SILU_MUL = 2 };
 enum XMode { X_PACKED = 0, X_F32 = 1, X_RMSNORM = 2 };
 
 constexpr int kMmaM = 128;            // weight rows a tile
-constexpr int kStageCols = 64;        // columns a stage (128 bytes of bf16: one swizzle row)
-constexpr int kWBytes = kMmaM * kStageCols * 2;
-constexpr int kMaxStages = 8;
+constexpr int kChunkCols = 64;        // columns of one swizzled sub-tile (128 bytes of bf16)
+constexpr int kChunks = 4;            // sub-tiles a stage
+constexpr int kStageCols = kChunkCols * kChunks;
+constexpr int kChunkBytes = kMmaM * kChunkCols * 2;
+constexpr int kWBytes = kChunkBytes * kChunks;
+constexpr int kMaxStages = 4;
 constexpr int kMaxCluster = 8;        // column ranges of a tile (portable cluster size)
 constexpr int kThreads = 192;         // warps 0-3 epilogue, 4 producer, 5 MMA
 constexpr int kTmemCols = 32;
@@ -60,7 +111,7 @@ constexpr int kRedLd = kMmaM + 16;    // floats between the streams' rows of the
 
 struct MmaGemvParams {
   GemvParams g;         // x: the packed activations
-  int kc, stages;
+  int stages;           // ring depth
 };
 
 constexpr int stage_bytes(int nb) { return kWBytes + nb * kStageCols * 2; }
@@ -83,12 +134,26 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint3
          (static_cast<uint64_t>(swizzle & 7) << 61);
 }
 
-__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int c0, int c1, uint64_t* bar,
+// One tensor-map load of the stage's weights: every sub-tile of 64 columns x 128 rows in
+// the 128-byte swizzled layout, one after the other (3-D box {64, 128, chunks}; for the
+// SiLU-multiply a 4-D box {64, 64, gate/up, chunks}, so each sub-tile holds its 64 gate
+// rows then their 64 up rows).
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int c0, int c1, int c2, uint64_t* bar,
                                             uint64_t policy) {
   asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
-      " [%0], [%1, {%2, %3}], [%4], %5;"
-      ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar)), "l"(policy)
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3, %4}], [%5], %6;"
+      ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar)),
+        "l"(policy)
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, int c0, int c1, int c2, int c3,
+                                            uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6], %7;"
+      ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3),
+        "r"(smem_u32(bar)), "l"(policy)
       : "memory");
 }
 
@@ -152,12 +217,20 @@ template <int XM>
 __global__ void __launch_bounds__(kPackThreads) pack_x_kernel(const float* x, int64_t stride, const float* gamma,
                                                               float eps, int K, int B, int NB, uint4* xp) {
   __shared__ float red[kPackThreads / 32];
+  TTS_GTRACE_BEGIN(0x10 | XM, trow);
   grid_wait();
   grid_launch_dependents();
   const int b = blockIdx.x, tid = threadIdx.x;
+#ifdef TTS_TRACE
+  __syncthreads();
+  if (tid == 0) TTS_GTRACE(trow, 2);
+#endif
   const int groups = K / 8;
   if (b >= B) {
     for (int c = tid; c < groups; c += kPackThreads) xp[static_cast<int64_t>(c) * NB + b] = make_uint4(0, 0, 0, 0);
+#ifdef TTS_TRACE
+    if (tid == 0) TTS_GTRACE(trow, 4);
+#endif
     return;
   }
   const float4* row = reinterpret_cast<const float4*>(x + static_cast<int64_t>(b) * stride);
@@ -209,6 +282,9 @@ __global__ void __launch_bounds__(kPackThreads) pack_x_kernel(const float* x, in
           make_uint4(pack2_bf16(f[0], f[1]), pack2_bf16(f[2], f[3]), pack2_bf16(f[4], f[5]), pack2_bf16(f[6], f[7]));
     }
   }
+#ifdef TTS_TRACE
+  if (tid == 0) TTS_GTRACE(trow, 4);
+#endif
 }
 
 template <int EPI, int NB>
@@ -221,7 +297,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_mma_kernel(const __grid_cons
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   // the 128-byte swizzle repeats every 1024 bytes: the stages start on such a boundary
   unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  const int NS = mp.stages, kc = mp.kc;
+  const int NS = mp.stages;
   unsigned char* ring = smem;                                          // NS stages: weights | x
   // the partial sums, [NB][kRedLd] f32, over the ring once every MMA has read it
   float* red = reinterpret_cast<float*>(ring);
@@ -229,12 +305,22 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_mma_kernel(const __grid_cons
   uint64_t* empty = full + kMaxStages;                                 // [NS]
   uint64_t* done = empty + kMaxStages;
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(done + 1);
+  TTS_GTRACE_BEGIN(EPI | (NB == 32 ? 4 : 0), trow);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int tile = blockIdx.x;
-  const int S = gridDim.y, rank = blockIdx.y;   // the tile's column ranges = the cluster
-  const int k0 = rank * kc;
-  const int nst = kc / kStageCols;
+  // epilogue of a store / residual tile: rows in groups of 4, rank r of the cluster
+  // taking groups [32 r / S, 32 (r + 1) / S) of every stream, unit u = (stream, group)
+  // handled by thread u % 128 (at most kUnits each)
+  constexpr int kUnits = NB / 4;
+  float4 old[kUnits];
+  // the tile's column ranges = the cluster; range r holds stages [r n / S, (r + 1) n / S)
+  // of the n = K / 64 stages of a row
+  const int S = gridDim.y, rank = blockIdx.y;
+  const int n_all = p.K / kStageCols;
+  const int st0 = rank * n_all / S, nst = (rank + 1) * n_all / S - st0;
+  const int k0 = st0 * kStageCols;
+  const int q0 = 32 * rank / S, qpr = 32 * (rank + 1) / S - q0;
 
   if (tid == 0) {
     for (int i = 0; i < NS; ++i) {
@@ -262,14 +348,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_mma_kernel(const __grid_cons
       const unsigned char* xsrc = static_cast<const unsigned char*>(p.x) + static_cast<int64_t>(k0) * NB * 2;
       auto load_w = [&](int i) {
         const int s = i % NS;
-        const int col = k0 + i * kStageCols;
+        const int chunk = (k0 + i * kStageCols) / kChunkCols;
         mbar_arrive_expect_tx(&full[s], kStage);
-        if (EPI == EPI_SILU_MUL) {
-          tma_load_2d(ring + s * kStage, &wmap, col, tile * 64, &full[s], pol);
-          tma_load_2d(ring + s * kStage + kWBytes / 2, &wmap, col, p.inter + tile * 64, &full[s], pol);
-        } else {
-          tma_load_2d(ring + s * kStage, &wmap, col, tile * kMmaM, &full[s], pol);
-        }
+        if (EPI == EPI_SILU_MUL) tma_load_4d(ring + s * kStage, &wmap, 0, tile * 64, 0, chunk, &full[s], pol);
+        else tma_load_3d(ring + s * kStage, &wmap, 0, tile * kMmaM, chunk, &full[s], pol);
       };
       auto load_x = [&](int i) {
         const int s = i % NS;
@@ -279,6 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_mma_kernel(const __grid_cons
       const int pre = nst < NS ? nst : NS;
       for (int i = 0; i < pre; ++i) load_w(i);
       grid_wait();
+      TTS_GTRACE(trow, 2);
       for (int i = 0; i < pre; ++i) load_x(i);
       int issued = pre;
       bool ok = true;
@@ -313,10 +396,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_mma_kernel(const __grid_cons
         const uint32_t base = smem_u32(ring + s * kStage);
 #pragma unroll
         for (int j = 0; j < kStageCols / 16; ++j) {
-          // A: the weight tile, 128-byte swizzled rows of 64 columns, 8-row groups 1024
-          // bytes apart, advanced 32 bytes a K step; B: the activation chunk, core
-          // matrices of 8 streams x 8 columns, 8-column groups NB * 16 bytes apart
-          const uint64_t ad = smem_desc(base + j * 32, 16, 1024, 2);
+          // A: sub-tile j / 4 of the weights, 128-byte swizzled rows of 64 columns, 8-row
+          // groups 1024 bytes apart, advanced 32 bytes a K step; B: the activation chunk,
+          // core matrices of 8 streams x 8 columns, 8-column groups NB * 16 bytes apart
+          const uint64_t ad = smem_desc(base + (j >> 2) * kChunkBytes + (j & 3) * 32, 16, 1024, 2);
           const uint64_t bd = smem_desc(base + kWBytes + 2 * j * (NB * 16), NB * 16, 128, 0);
           const uint32_t acc = (i > 0 || j > 0) ? 1u : 0u;
           asm volatile(
@@ -335,9 +418,25 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_mma_kernel(const __grid_cons
     }
   } else {
     // ---------------------------------------- the partial of this column range
+    grid_wait();   // the residual stream and the outputs belong to earlier kernels too
+    if (EPI == EPI_RESIDUAL) {
+      // this thread's old residual values, loaded while the weights stream
+#pragma unroll
+      for (int k = 0; k < kUnits; ++k) {
+        const int u = tid + 128 * k;
+        old[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (u < qpr * NB) {
+          const int b = u / qpr, row = tile * kMmaM + (q0 + u - b * qpr) * 4;
+          if (b < p.B && row < p.n_out)
+            old[k] = __ldcg(reinterpret_cast<const float4*>(static_cast<const float*>(p.y) +
+                                                            static_cast<int64_t>(b) * p.y_stride + row));
+        }
+      }
+    }
     const int m = warp * 32 + lane;
     float v[NB];
     const bool got = mbar_wait(done, 0);
+    if (tid == 0) TTS_GTRACE(trow, 3);
     if (!got && lane == 0) set_err(p.err, TTS_EFLAG_TIMEOUT);
     tc_fence_after();
     if (got) tmem_row<NB>(tmem + (static_cast<uint32_t>(warp * 32) << 16), v);
@@ -349,20 +448,22 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_mma_kernel(const __grid_cons
     for (int b = 0; b < NB; ++b) red[b * kRedLd + m] = v[b];
   }
   __syncwarp();   // the producer and MMA lanes rejoin their warps before the aligned barrier
+  if (tid == 0) TTS_GTRACE(trow, 5);
   tc_fence_before();
   cluster_sync_all();   // every range's partial is in its CTA's shared memory
+  if (tid == 0) TTS_GTRACE(trow, 6);
   if (warp < 4) {
-    grid_wait();   // the residual stream and the outputs belong to earlier kernels too
     uint32_t peer[kMaxCluster];
 #pragma unroll
     for (int r = 0; r < kMaxCluster; ++r) peer[r] = r < S ? map_shared_rank(red, r) : 0u;
     if (EPI == EPI_SILU_MUL) {
-      // items (gate row i, up row 64 + i) of this rank: 64 / S, in groups of 8 per stream
-      const int per = 64 / S, gpr = per / 8;
+      // items (gate row i, up row 64 + i) in groups of 8: rank r takes groups
+      // [8 r / S, 8 (r + 1) / S) of every stream
+      const int g0 = 8 * rank / S, gpr = 8 * (rank + 1) / S - g0;
       for (int u = tid; u < gpr * NB; u += 128) {
-        const int b = u / gpr, il = rank * per + (u - b * gpr) * 8;
+        const int b = u / gpr, il = (g0 + u - b * gpr) * 8;
         const int item = tile * 64 + il;
-        float4 g0 = make_float4(0.f, 0.f, 0.f, 0.f), g1 = g0, u0 = g0, u1 = g0;
+        float4 ga = make_float4(0.f, 0.f, 0.f, 0.f), gb = ga, ua = ga, ub = ga;
         const uint32_t off = static_cast<uint32_t>((b * kRedLd + il) * 4);
         // two ranks' loads in flight at a time, summed in rank order
 #pragma unroll
@@ -383,16 +484,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_mma_kernel(const __grid_cons
 #pragma unroll
             for (int h = 0; h < 2; ++h)
               if (r + h < S) {
-                add4(g0, q[h][0]);
-                add4(g1, q[h][1]);
-                add4(u0, q[h][2]);
-                add4(u1, q[h][3]);
+                add4(ga, q[h][0]);
+                add4(gb, q[h][1]);
+                add4(ua, q[h][2]);
+                add4(ub, q[h][3]);
               }
           }
         }
         if (item < p.n_out) {
-          const float gt[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
-          const float up[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+          const float gt[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
+          const float up[8] = {ua.x, ua.y, ua.z, ua.w, ub.x, ub.y, ub.z, ub.w};
           float o[8];
 #pragma unroll
           for (int e = 0; e < 8; ++e) o[e] = b < p.B ? gt[e] / (1.0f + expf(-gt[e])) * up[e] : 0.f;
@@ -401,10 +502,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_mma_kernel(const __grid_cons
         }
       }
     } else {
-      // rows of this rank: 128 / S, in groups of 4 per stream
-      const int per = kMmaM / S, qpr = per / 4;
-      for (int u = tid; u < qpr * NB; u += 128) {
-        const int b = u / qpr, rl = rank * per + (u - b * qpr) * 4;
+#pragma unroll
+      for (int k = 0; k < kUnits; ++k) {
+        const int u = tid + 128 * k;
+        if (u >= qpr * NB) break;
+        const int b = u / qpr, rl = (q0 + u - b * qpr) * 4;
         const int row = tile * kMmaM + rl;
         if (b >= p.B) continue;
         const uint32_t off = static_cast<uint32_t>((b * kRedLd + rl) * 4);
@@ -417,17 +519,19 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_mma_kernel(const __grid_cons
           if (r < S) add4(acc, q[r]);
         if (row < p.n_out) {
           float4* yp = reinterpret_cast<float4*>(static_cast<float*>(p.y) + static_cast<int64_t>(b) * p.y_stride + row);
-          if (EPI == EPI_RESIDUAL) {
-            const float4 old = __ldcg(yp);
-            acc = make_float4(__fadd_rn(old.x, acc.x), __fadd_rn(old.y, acc.y), __fadd_rn(old.z, acc.z),
-                              __fadd_rn(old.w, acc.w));
-          }
+          if (EPI == EPI_RESIDUAL)
+            acc = make_float4(__fadd_rn(old[k].x, acc.x), __fadd_rn(old[k].y, acc.y), __fadd_rn(old[k].z, acc.z),
+                              __fadd_rn(old[k].w, acc.w));
           *yp = acc;
         }
       }
     }
   }
-  cluster_sync_all();   // no CTA leaves while a peer still reads its partial
+  if (tid == 0) TTS_GTRACE(trow, 7);
+  // no CTA leaves while a peer still reads its partial (the reads are complete once
+  // their sums are stored, so the arrival needs no release)
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;\n\tbarrier.cluster.wait.aligned;" ::: "memory");
+  if (tid == 0) TTS_GTRACE(trow, 4);
   if (warp == 5) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(kTmemCols) : "memory");
@@ -455,70 +559,140 @@ size_t smem_bytes(int NB, int stages) {
   return 1024 + static_cast<size_t>(stages) * stage_bytes(NB) + (2 * kMaxStages + 1) * sizeof(uint64_t) + 16;
 }
 
-// Launch plan: tiles, column ranges per tile (the cluster size) and ring depth.  Ranges
-// are a power-of-two share of K (a multiple of 64 columns), as many as keep the grid
-// within one wave at two CTAs per SM (at most kMaxCluster); the ring as deep as lets two
-// CTAs share an SM when the grid needs that, else as deep as one CTA may be.
-constexpr size_t kTwoPerSmBytes = 113 * 1024;
-constexpr size_t kOnePerSmBytes = 227 * 1024;
-void gemv_mma_plan(int K, int n_out, int epilogue, int n_sm, int nb, int& tiles, int& splits, int& kc,
-                   int& stages) {
-  tiles = epilogue == EPI_SILU_MUL ? (n_out + 63) / 64 : (n_out + kMmaM - 1) / kMmaM;
-  int s = 1;
-  while (s < kMaxCluster && tiles * s * 2 <= 2 * n_sm && K % (2 * s * kStageCols) == 0) s *= 2;
-  splits = s;
-  kc = K / s;
-  const int nst = kc / kStageCols;
-  const size_t budget = tiles * s <= n_sm ? kOnePerSmBytes : kTwoPerSmBytes;
-  int ns = nst < kMaxStages ? nst : kMaxStages;
-  while (ns > 2 && smem_bytes(nb, ns) > budget) --ns;
-  stages = ns;
+// One CTA per SM: a kernel that allocates tensor memory is given at most one block per
+// SM, so a launch is planned as a single wave.  Tiles of 128 rows, split into S column
+// ranges (the cluster size), S as large as keeps every tile's cluster resident at once
+// (the largest S with tiles <= the device's maximum of active S-CTA clusters); the ring
+// as deep as one CTA's shared memory allows.
+
+struct OccKey {
+  int dev, epi, nb, s, stages;
+  bool operator<(const OccKey& o) const {
+    return std::tie(dev, epi, nb, s, stages) < std::tie(o.dev, o.epi, o.nb, o.s, o.stages);
+  }
+};
+
+// The dynamic shared memory one CTA of the kernel may take on device `dev` (the opt-in
+// maximum less the kernel's static shared memory), set as the kernel's limit once per
+// device; 0 on failure.
+template <int EPI, int NB>
+size_t configure(int dev) {
+  static std::mutex mtx;
+  static size_t budget[64] = {};
+  std::lock_guard<std::mutex> lock(mtx);
+  if (budget[dev] != 0) return budget[dev];
+  int optin = 0;
+  cudaFuncAttributes fa;
+  if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
+      cudaFuncGetAttributes(&fa, gemv_mma_kernel<EPI, NB>) != cudaSuccess ||
+      static_cast<size_t>(optin) <= fa.sharedSizeBytes)
+    return 0;
+  const size_t b = static_cast<size_t>(optin) - fa.sharedSizeBytes;
+  if (cudaFuncSetAttribute(gemv_mma_kernel<EPI, NB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(b)) != cudaSuccess)
+    return 0;
+  budget[dev] = b;
+  return b;
+}
+
+// Clusters of S CTAs of this kernel the device keeps resident at once (cached).
+template <int EPI, int NB>
+int max_active_clusters(int dev, int S, int stages) {
+  static std::mutex mtx;
+  static std::map<OccKey, int> cache;
+  const OccKey key = {dev, EPI, NB, S, stages};
+  {
+    std::lock_guard<std::mutex> lock(mtx);
+    const auto it = cache.find(key);
+    if (it != cache.end()) return it->second;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1, S);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem_bytes(NB, stages);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = static_cast<unsigned>(S);
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, gemv_mma_kernel<EPI, NB>, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    n = 0;
+  }
+  std::lock_guard<std::mutex> lock(mtx);
+  cache[key] = n;
+  return n;
 }
 
 template <int EPI, int NB>
-cudaError_t launch_mma_t(const MmaGemvParams& mp, int splits, int tiles, cudaStream_t s) {
+cudaError_t launch_mma_t(const GemvParams& p, cudaStream_t s) {
   auto kern = gemv_mma_kernel<EPI, NB>;
-  const GemvParams& p = mp.g;
-  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
-  if (enc == nullptr) return cudaErrorNotSupported;
-  // the weight matrix: rows of K bf16, a box of 64 columns x 128 rows (64 for the gate
-  // and up halves of a SiLU-multiply tile), 128-byte swizzle
-  const int rows = EPI == EPI_SILU_MUL ? 2 * p.inter : p.n_out;
-  CUtensorMap map;
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(p.K), static_cast<cuuint64_t>(rows)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(p.K) * 2};
-  cuuint32_t box[2] = {kStageCols, EPI == EPI_SILU_MUL ? 64u : static_cast<cuuint32_t>(kMmaM)};
-  cuuint32_t estr[2] = {1, 1};
-  if (enc(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(p.w), dims, strides, box, estr,
-          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-    return cudaErrorInvalidValue;
-  const size_t smem = smem_bytes(NB, mp.stages);
-  static std::mutex mtx;
-  static bool configured[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  {
-    std::lock_guard<std::mutex> lock(mtx);
-    if (!configured[dev]) {
-      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kOnePerSmBytes));
-      if (e != cudaSuccess) return e;
-      configured[dev] = true;
+  const size_t budget = configure<EPI, NB>(dev);
+  if (budget == 0) {
+    const cudaError_t le = cudaGetLastError();
+    return le != cudaSuccess ? le : cudaErrorInvalidValue;
+  }
+  // the plan
+  const int n_all = p.K / kStageCols;
+  const int tiles = EPI == EPI_SILU_MUL ? (p.n_out + 63) / 64 : (p.n_out + kMmaM - 1) / kMmaM;
+  int S = 0, stages = 0;
+  for (int c = n_all < kMaxCluster ? n_all : kMaxCluster; c >= 1 && S == 0; --c) {
+    const int longest = (n_all + c - 1) / c;
+    int ns = longest < kMaxStages ? longest : kMaxStages;
+    while (ns > 1 && smem_bytes(NB, ns) > budget) --ns;
+    if (c == 1 || tiles <= max_active_clusters<EPI, NB>(dev, c, ns)) {
+      S = c;
+      stages = ns;
     }
   }
+  MmaGemvParams mp = {};
+  mp.g = p;
+  mp.stages = stages;
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (enc == nullptr) return cudaErrorNotSupported;
+  // the weight matrix, rows of K bf16, seen as [K / 64 sub-tile columns][rows][64]
+  // (strides: a row K * 2 bytes, a sub-tile column 128 bytes); a box of 4 sub-tile
+  // columns x 128 rows x 64, 128-byte swizzle.  SiLU-multiply: [K / 64][gate / up][inter
+  // rows][64], a box of 4 x 2 x 64 x 64 (the up half inter * K * 2 bytes on).
+  const cuuint64_t K = static_cast<cuuint64_t>(p.K);
+  CUtensorMap map;
+  CUresult r;
+  if (EPI == EPI_SILU_MUL) {
+    cuuint64_t dims[4] = {kChunkCols, static_cast<cuuint64_t>(p.inter), 2, K / kChunkCols};
+    cuuint64_t strides[3] = {K * 2, static_cast<cuuint64_t>(p.inter) * K * 2, kChunkCols * 2};
+    cuuint32_t box[4] = {kChunkCols, 64, 2, kChunks};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    r = enc(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(p.w), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  } else {
+    cuuint64_t dims[3] = {kChunkCols, static_cast<cuuint64_t>(p.n_out), K / kChunkCols};
+    cuuint64_t strides[2] = {K * 2, kChunkCols * 2};
+    cuuint32_t box[3] = {kChunkCols, static_cast<cuuint32_t>(kMmaM), kChunks};
+    cuuint32_t estr[3] = {1, 1, 1};
+    r = enc(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(p.w), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  }
+  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(tiles, splits);
+  cfg.gridDim = dim3(tiles, S);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = smem;
+  cfg.dynamicSmemBytes = smem_bytes(NB, stages);
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   attr[1].id = cudaLaunchAttributeClusterDimension;
   attr[1].val.clusterDim.x = 1;
-  attr[1].val.clusterDim.y = static_cast<unsigned>(splits);
+  attr[1].val.clusterDim.y = static_cast<unsigned>(S);
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
@@ -527,20 +701,30 @@ cudaError_t launch_mma_t(const MmaGemvParams& mp, int splits, int tiles, cudaStr
 
 }  // namespace
 
+#ifdef TTS_TRACE
+extern "C" int tts_gtrace_read(unsigned long long* host, int n_rows) {
+  return static_cast<int>(cudaMemcpyFromSymbol(host, g_gtrace, static_cast<size_t>(n_rows) * 8 * sizeof(unsigned long long)));
+}
+extern "C" int tts_gtrace_clear(void) {
+  static unsigned long long zeros[1024][8];
+  unsigned int z = 0;
+  for (int r = 0; r < kGTraceRows; r += 1024)
+    if (cudaMemcpyToSymbol(g_gtrace, zeros, sizeof(zeros), static_cast<size_t>(r) * 8 * sizeof(unsigned long long)) != cudaSuccess)
+      return 1;
+  return static_cast<int>(cudaMemcpyToSymbol(g_gtrace_n, &z, sizeof(z)));
+}
+#endif
+
 int gemv_mma_slots(int B) { return B <= 16 ? 16 : 32; }
 
-cudaError_t launch_gemv_mma(const GemvParams& p, int x_mode, int epilogue, void* xpack, int n_sm, cudaStream_t s) {
+cudaError_t launch_gemv_mma(const GemvParams& p, int x_mode, int epilogue, void* xpack, cudaStream_t s) {
   if (p.B < 1 || p.B > kGemvMmaMaxB || p.K % kStageCols != 0 || p.K > kGemvMaxK || p.n_out % 8 != 0)
     return cudaErrorInvalidValue;
   const int nb = gemv_mma_slots(p.B);
   const uintptr_t align = reinterpret_cast<uintptr_t>(p.y) | reinterpret_cast<uintptr_t>(xpack) |
                           reinterpret_cast<uintptr_t>(p.x);
   if ((align & 15u) != 0 || (epilogue != EPI_SILU_MUL && p.y_stride % 4 != 0)) return cudaErrorInvalidValue;
-  MmaGemvParams mp = {};
-  mp.g = p;
-  int tiles, splits;
-  gemv_mma_plan(p.K, p.n_out, epilogue, n_sm, nb, tiles, splits, mp.kc, mp.stages);
-  if (smem_bytes(nb, mp.stages) > kOnePerSmBytes) return cudaErrorInvalidValue;
+  GemvParams g = p;
   if (x_mode != X_PACKED) {
     if (xpack == nullptr || (x_mode == X_RMSNORM && p.gamma == nullptr) || p.x_stride % 4 != 0)
       return cudaErrorInvalidValue;
@@ -552,14 +736,13 @@ cudaError_t launch_gemv_mma(const GemvParams& p, int x_mode, int epilogue, void*
             : launch_pdl(pack_x_kernel<X_F32>, dim3(nb), dim3(kPackThreads), 0, s, x, p.x_stride, p.gamma, p.eps,
                          p.K, p.B, nb, static_cast<uint4*>(xpack));
     if (e != cudaSuccess) return e;
-    mp.g.x = xpack;
+    g.x = xpack;
   }
-  if (epilogue == EPI_STORE) return nb == 16 ? launch_mma_t<EPI_STORE, 16>(mp, splits, tiles, s)
-                                             : launch_mma_t<EPI_STORE, 32>(mp, splits, tiles, s);
-  if (epilogue == EPI_RESIDUAL) return nb == 16 ? launch_mma_t<EPI_RESIDUAL, 16>(mp, splits, tiles, s)
-                                                : launch_mma_t<EPI_RESIDUAL, 32>(mp, splits, tiles, s);
-  if (epilogue == EPI_SILU_MUL) return nb == 16 ? launch_mma_t<EPI_SILU_MUL, 16>(mp, splits, tiles, s)
-                                                : launch_mma_t<EPI_SILU_MUL, 32>(mp, splits, tiles, s);
+  if (epilogue == EPI_STORE) return nb == 16 ? launch_mma_t<EPI_STORE, 16>(g, s) : launch_mma_t<EPI_STORE, 32>(g, s);
+  if (epilogue == EPI_RESIDUAL)
+    return nb == 16 ? launch_mma_t<EPI_RESIDUAL, 16>(g, s) : launch_mma_t<EPI_RESIDUAL, 32>(g, s);
+  if (epilogue == EPI_SILU_MUL)
+    return nb == 16 ? launch_mma_t<EPI_SILU_MUL, 16>(g, s) : launch_mma_t<EPI_SILU_MUL, 32>(g, s);
   return cudaErrorInvalidValue;
 }
 

@@ -169,7 +169,7 @@ cudaError_t launch_gemv_bf16(const GemvParams& p, int x_mode, int epilogue, cuda
 // aligned) with a small kernel launched first.
 constexpr int kGemvMmaMaxB = 32;
 int gemv_mma_slots(int B);
-cudaError_t launch_gemv_mma(const GemvParams& p, int x_mode, int epilogue, void* xpack, int n_sm, cudaStream_t s);
+cudaError_t launch_gemv_mma(const GemvParams& p, int x_mode, int epilogue, void* xpack, cudaStream_t s);
 
 // Tile geometry of the attention kernel for a (dtype, head_dim) pair.
 struct AttnGeometry {
