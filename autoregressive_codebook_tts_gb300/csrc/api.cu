@@ -144,6 +144,15 @@ tts_status prepare_attn(const tts_kv_desc* d, const void* k_cache, const void* v
   return TTS_OK;
 }
 
+// Prompts of kPrefillMinT rows or more take the multi-query kernel (query blocks share
+// every K/V tile); shorter ones run as B x T decode queries.
+bool multi_query_prefill(const tts_kv_desc* d, int T) {
+  const int64_t rows = d->paged ? static_cast<int64_t>(d->n_pages) * d->n_kv_heads * d->page_size
+                                : static_cast<int64_t>(d->B) * d->n_kv_heads * d->capacity;
+  return prefill_attn_supported(d->head_dim, d->n_q_heads / d->n_kv_heads, d->paged, d->paged ? d->page_size : 1, T) &&
+         rows < (int64_t{1} << 31);
+}
+
 }  // namespace
 
 extern "C" {
@@ -359,6 +368,12 @@ tts_status tts_decode_step(const float* q, const float* k, const float* v, int64
 
 size_t tts_prefill_workspace_size(const tts_kv_desc* d, int32_t T, int32_t n_splits) {
   if (check_desc(d) != TTS_OK || T < 1 || static_cast<int64_t>(d->B) * T > 65535) return 0;
+  if (multi_query_prefill(d, T)) {
+    // the chunk results of the multi-query kernel (none with one chunk per item)
+    const size_t w = prefill_attn_workspace(d->B, T, d->n_kv_heads, d->n_q_heads / d->n_kv_heads, d->head_dim,
+                                            d->capacity, n_splits, sm_count());
+    return w > 256 ? w : 256;
+  }
   tts_kv_desc dq = *d;  // the B*T queries take the place of the streams
   dq.B = d->B * T;
   return tts_decode_attn_workspace_size(&dq, n_splits);
@@ -376,12 +391,32 @@ tts_status tts_prefill_step(float* q, const float* k, const float* v, int64_t ro
   tts_status st = check_desc(d);
   if (st != TTS_OK) return st;
   if (T < 1 || static_cast<int64_t>(d->B) * T > 65535) return TTS_ERR_SHAPE;
+  const bool mq = multi_query_prefill(d, T);
   tts_kv_desc dq = *d;
   dq.B = d->B * T;
   AttnParams p = {};
   int used = 0;
-  st = prepare_attn(&dq, k_cache, v_cache, workspace, ws_bytes, n_splits, p, used);
-  if (st != TTS_OK) return st;
+  PrefillAttnParams pp = {};
+  if (mq) {
+    if (k_cache == nullptr || v_cache == nullptr) return TTS_ERR_NULL;
+    if (!aligned16(k_cache) || !aligned16(v_cache)) return TTS_ERR_ALIGN;
+    prefill_attn_plan(d->B, T, d->n_kv_heads, d->n_q_heads / d->n_kv_heads, d->capacity, n_splits, sm_count(),
+                      pp.n_qb, pp.n_ch, pp.ch_len);
+    if (pp.n_ch > 65535) return TTS_ERR_SHAPE;
+    if (pp.n_ch > 1) {
+      const size_t need = prefill_attn_workspace(d->B, T, d->n_kv_heads, d->n_q_heads / d->n_kv_heads, d->head_dim,
+                                                 d->capacity, n_splits, sm_count());
+      if (workspace == nullptr) return TTS_ERR_WORKSPACE;
+      if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return TTS_ERR_ALIGN;
+      if (ws_bytes < need) return TTS_ERR_WORKSPACE;
+      const size_t rows = static_cast<size_t>(d->B) * d->n_kv_heads * pp.n_qb * pp.n_ch * 64;
+      pp.part = static_cast<float*>(workspace);
+      pp.ml = pp.part + rows * d->head_dim;
+    }
+  } else {
+    st = prepare_attn(&dq, k_cache, v_cache, workspace, ws_bytes, n_splits, p, used);
+    if (st != TTS_OK) return st;
+  }
   if (row_stride < static_cast<int64_t>(d->n_q_heads) * d->head_dim || rope_max_pos < 1 || !(eps >= 0.f))
     return TTS_ERR_SHAPE;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(gamma_q) ||
@@ -417,6 +452,26 @@ tts_status tts_prefill_step(float* q, const float* k, const float* v, int64_t ro
   rp.err = err_flag;
   st = from_cuda(launch_prefill_rows(rp, s));
   if (st != TTS_OK) return st;
+  if (mq) {
+    pp.q = q;
+    pp.q_stride = row_stride;
+    pp.start = start_pos;
+    pp.B = d->B;
+    pp.T = T;
+    pp.n_q_heads = d->n_q_heads;
+    pp.n_kv_heads = d->n_kv_heads;
+    pp.capacity = d->capacity;
+    pp.paged = d->paged;
+    pp.page_size = d->paged ? d->page_size : 1;
+    pp.n_pages = d->paged ? d->n_pages : 0;
+    pp.bt_stride = d->paged ? d->bt_stride : 0;
+    pp.block_table = d->paged ? d->block_table : nullptr;
+    pp.scale_log2 = scale * 1.4426950408889634f;
+    pp.out = out;
+    pp.err = err_flag;
+    return from_cuda(launch_prefill_attn(pp, k_cache, v_cache, d->kv_dtype == TTS_BF16, d->head_dim,
+                                         d->n_q_heads / d->n_kv_heads, s));
+  }
   p.q = q;
   p.q_stride = row_stride;
   p.lens = start_pos;

@@ -99,11 +99,15 @@ enum XMode { X_PACKED = 0, X_F32 = 1, X_RMSNORM = 2 };
 
 constexpr int kMmaM = 128;            // weight rows a tile
 constexpr int kChunkCols = 64;        // columns of one swizzled sub-tile (128 bytes of bf16)
-constexpr int kChunks = 4;            // sub-tiles a stage
+#ifndef TTS_GEMV_CHUNKS
+#define TTS_GEMV_CHUNKS 4
+#endif
+constexpr int kChunks = TTS_GEMV_CHUNKS;  // sub-tiles a stage (K is a multiple of 256)
+static_assert(kChunks == 1 || kChunks == 2 || kChunks == 4, "sub-tiles a stage");
 constexpr int kStageCols = kChunkCols * kChunks;
 constexpr int kChunkBytes = kMmaM * kChunkCols * 2;
 constexpr int kWBytes = kChunkBytes * kChunks;
-constexpr int kMaxStages = 4;
+constexpr int kMaxStages = 8;
 constexpr int kMaxCluster = 8;        // column ranges of a tile (portable cluster size)
 constexpr int kThreads = 192;         // warps 0-3 epilogue, 4 producer, 5 MMA
 constexpr int kTmemCols = 32;

@@ -171,6 +171,33 @@ constexpr int kGemvMmaMaxB = 32;
 int gemv_mma_slots(int B);
 cudaError_t launch_gemv_mma(const GemvParams& p, int x_mode, int epilogue, void* xpack, cudaStream_t s);
 
+// Multi-query prefill attention (prefill_attn.cu): blocks of 64 query rows (64 / G
+// queries x the G q heads of a kv head) share every K/V tile of their causal window.
+// Query row (b, t, h) reads q at q + (b * T + t) * q_stride + h * D (already normed and
+// rotated) and sees cache rows [0, min(max(start[b] + t + 1, 1), capacity)).
+constexpr int kPrefillMinT = 8;   // shorter prompts take the per-query decode path
+struct PrefillAttnParams {
+  const float* q;
+  int64_t q_stride;
+  const int32_t* start;         // [B]
+  int B, T, n_q_heads, n_kv_heads, capacity;
+  int paged, page_size, n_pages, bt_stride;
+  const int32_t* block_table;
+  float scale_log2;             // scale * log2(e)
+  float* out;                   // [B][T][Hq][D]
+  float* part;                  // chunk rows [items][n_ch][64][D] (n_ch > 1)
+  float* ml;                    // their (max, sum) [items][n_ch][64][2]
+  int n_qb, n_ch, ch_len;       // query blocks per (stream, kv head), chunks per item, rows per chunk
+  int32_t* err;
+};
+bool prefill_attn_supported(int head_dim, int group, int paged, int page_size, int T);
+void prefill_attn_plan(int B, int T, int n_kv_heads, int group, int capacity, int n_splits, int n_sm, int& n_qb,
+                       int& n_ch, int& ch_len);
+size_t prefill_attn_workspace(int B, int T, int n_kv_heads, int group, int head_dim, int capacity, int n_splits,
+                              int n_sm);
+cudaError_t launch_prefill_attn(const PrefillAttnParams& p, const void* k_cache, const void* v_cache, bool kv_bf16,
+                                int head_dim, int group, cudaStream_t s);
+
 // Tile geometry of the attention kernel for a (dtype, head_dim) pair.
 struct AttnGeometry {
   int tile_rows;     // positions per pipeline stage

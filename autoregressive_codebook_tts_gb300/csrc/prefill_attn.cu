@@ -1,0 +1,529 @@
+// Multi-query prefill attention: the T new positions of a stream attend to the cache
+// causally ("qwentts.cpp -- src/pipeline-tts.h" commit page, KV-cache section: the
+// prefill writes the prompt's rows from the reset position; query t of stream b sees
+// positions [0, start[b] + t + 1)).  The decode-step kernel would stream each query's
+// whole window once per query; here a block of query rows shares every K/V tile:
+//
+//   * work item = (stream b, kv head g, block of QB = 64 / G queries), i.e. 64 query
+//     rows (query t_local, q head h of the group, row t_local * G + h); its window
+//     [0, start + t_last + 1) is cut into chunks of ch_len rows, one CTA per (chunk,
+//     item);
+//   * warp 8 (one lane) streams the chunk's 64-row K and V tiles into a 2-stage ring
+//     with 3-D tensor-map loads in the 128-byte swizzled layout (f32: boxes of 32
+//     floats x rows x D/32; bf16: 64 x rows x D/64), one load per tile and operand
+//     (paged: one per page of the tile);
+//   * warps 0..7 own 8 query rows each.  Scores S = Q K^T (f32, q rows broadcast from
+//     shared memory, lane l takes key rows l and l + 32); an online softmax per row in
+//     base 2 (scale folded into log2 e) with the causal mask as each row's window end;
+//     the probabilities go to a warp-private patch of shared memory and O += P V with
+//     lane l owning D/32 consecutive columns of its 8 rows;
+//   * a chunk's result is written unnormalised with its row max and sum, and a second
+//     kernel merges the chunks of every row in chunk order (max, rescale, sum, divide);
+//     with one chunk per item the first kernel writes the normalised rows itself.
+// Every wait is bounded; on expiry TTS_EFLAG_TIMEOUT is set and the CTA winds down.
+#include <cstdint>
+#include <mutex>
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace tts {
+namespace {
+
+constexpr int kRows = 64;          // query rows of an item
+constexpr int kTile = 64;          // cache rows of a tile
+constexpr int kWarps = 8;          // compute warps, 8 query rows each
+constexpr int kThreads = (kWarps + 1) * 32;
+constexpr int kStages = 2;
+
+template <typename KvT> struct KvTraits;
+template <> struct KvTraits<float> {
+  static constexpr int kPerUnit = 4;       // elements of a 16-byte unit
+  static constexpr int kPerChunk = 32;     // elements of a 128-byte swizzle row
+};
+template <> struct KvTraits<__nv_bfloat16> {
+  static constexpr int kPerUnit = 8;
+  static constexpr int kPerChunk = 64;
+};
+
+// Default L2 policy: the items of the other query blocks of a (stream, kv head) read the
+// same tiles soon after.
+__device__ __forceinline__ void tma_load_3d_pf(void* dst, const CUtensorMap* map, int c0, int c1, int c2,
+                                               uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];"
+      ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Byte offset of 16-byte unit `u` (of the D row) of tile row j in a tile written as
+// boxes of `br` rows (br a power of two >= 8): box j / br, then the row's 128-byte
+// chunk, then the row; the 128-byte swizzle permutes units within a chunk by row % 8.
+template <typename KvT, int D>
+__device__ __forceinline__ uint32_t tile_off(int j, int u, int br_shift) {
+  using Tr = KvTraits<KvT>;
+  constexpr int kChunks = D / Tr::kPerChunk;
+  const int br = 1 << br_shift;
+  const int box = j >> br_shift, jr = j & (br - 1);
+  const int c = u >> 3, uc = u & 7;
+  return static_cast<uint32_t>(((box * kChunks + c) * br + jr) * 128 + ((uc ^ (j & 7)) << 4));
+}
+
+__device__ __forceinline__ float4 lds_f4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ uint2 lds_u2(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ float2 lds_f2(uint32_t addr) {
+  float2 v;
+  asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ uint4 lds128_addr(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+
+// Scores of the warp's 8 query rows against tile rows `lane` and `lane + 32`.
+template <typename KvT, int D>
+__device__ __forceinline__ void tile_scores(uint32_t kb, uint32_t qw, int lane, int br_shift, float (&sc)[8][2]) {
+  using Tr = KvTraits<KvT>;
+  constexpr int kUnits = D / Tr::kPerUnit;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) sc[i][0] = sc[i][1] = 0.f;
+#pragma unroll 2
+  for (int u = 0; u < kUnits; ++u) {
+    const uint32_t a0 = kb + tile_off<KvT, D>(lane, u, br_shift);
+    const uint32_t a1 = kb + tile_off<KvT, D>(lane + 32, u, br_shift);
+    if constexpr (Tr::kPerUnit == 4) {
+      const float4 k0 = lds_f4(a0), k1 = lds_f4(a1);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float4 q = lds_f4(qw + (i * D + u * 4) * 4);
+        sc[i][0] = fmaf(q.x, k0.x, sc[i][0]);
+        sc[i][1] = fmaf(q.x, k1.x, sc[i][1]);
+        sc[i][0] = fmaf(q.y, k0.y, sc[i][0]);
+        sc[i][1] = fmaf(q.y, k1.y, sc[i][1]);
+        sc[i][0] = fmaf(q.z, k0.z, sc[i][0]);
+        sc[i][1] = fmaf(q.z, k1.z, sc[i][1]);
+        sc[i][0] = fmaf(q.w, k0.w, sc[i][0]);
+        sc[i][1] = fmaf(q.w, k1.w, sc[i][1]);
+      }
+    } else {
+      const uint4 w0 = lds128_addr(a0), w1 = lds128_addr(a1);
+      const float k0[8] = {bf16_lo(w0.x), bf16_hi(w0.x), bf16_lo(w0.y), bf16_hi(w0.y),
+                           bf16_lo(w0.z), bf16_hi(w0.z), bf16_lo(w0.w), bf16_hi(w0.w)};
+      const float k1[8] = {bf16_lo(w1.x), bf16_hi(w1.x), bf16_lo(w1.y), bf16_hi(w1.y),
+                           bf16_lo(w1.z), bf16_hi(w1.z), bf16_lo(w1.w), bf16_hi(w1.w)};
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float4 qa = lds_f4(qw + (i * D + u * 8) * 4);
+        const float4 qc = lds_f4(qw + (i * D + u * 8 + 4) * 4);
+        const float q[8] = {qa.x, qa.y, qa.z, qa.w, qc.x, qc.y, qc.z, qc.w};
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          sc[i][0] = fmaf(q[e], k0[e], sc[i][0]);
+          sc[i][1] = fmaf(q[e], k1[e], sc[i][1]);
+        }
+      }
+    }
+  }
+}
+
+// Columns [lane * DPL, lane * DPL + DPL) of V tile row j, widened to f32.
+template <typename KvT, int D>
+__device__ __forceinline__ void v_cols(uint32_t vb, int j, int lane, int br_shift, float (&v)[D / 32]) {
+  using Tr = KvTraits<KvT>;
+  constexpr int DPL = D / 32;
+  constexpr int kLanesPerUnit = Tr::kPerUnit / DPL;
+  const int u = lane / kLanesPerUnit, part = lane % kLanesPerUnit;
+  const uint32_t a = vb + tile_off<KvT, D>(j, u, br_shift) + part * DPL * static_cast<int>(sizeof(KvT));
+  if constexpr (sizeof(KvT) == 4 && DPL == 4) {
+    const float4 x = lds_f4(a);
+    v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
+  } else if constexpr (sizeof(KvT) == 4 && DPL == 2) {
+    const float2 x = lds_f2(a);
+    v[0] = x.x; v[1] = x.y;
+  } else if constexpr (DPL == 4) {
+    const uint2 w = lds_u2(a);
+    v[0] = bf16_lo(w.x); v[1] = bf16_hi(w.x); v[2] = bf16_lo(w.y); v[3] = bf16_hi(w.y);
+  } else {
+    uint32_t w;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(w) : "r"(a));
+    v[0] = bf16_lo(w); v[1] = bf16_hi(w);
+  }
+}
+
+__device__ __forceinline__ float warp_max(float x) {
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) x = fmaxf(x, __shfl_xor_sync(kFull, x, o));
+  return x;
+}
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) x += __shfl_xor_sync(kFull, x, o);
+  return x;
+}
+
+template <typename KvT, int D, int G>
+__global__ void __launch_bounds__(kThreads, 1) prefill_attn_kernel(const __grid_constant__ CUtensorMap kmap,
+                                                                    const __grid_constant__ CUtensorMap vmap,
+                                                                    const PrefillAttnParams p) {
+  constexpr int kTileBytes = kTile * D * static_cast<int>(sizeof(KvT));
+  constexpr int QB = kRows / G;   // queries of an item
+  constexpr int DPL = D / 32;     // output columns of a lane
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  unsigned char* ring = smem;                                                     // kStages x (K | V)
+  float* sq = reinterpret_cast<float*>(ring + kStages * 2 * kTileBytes);          // [64][D]
+  float* sp = sq + kRows * D;                                                     // [8][64][8]
+  uint64_t* full = reinterpret_cast<uint64_t*>(sp + kWarps * kTile * 8);
+  uint64_t* empty = full + kStages;
+
+  const int item = blockIdx.x, ch = blockIdx.y;
+  const int qb = item % p.n_qb, bg = item / p.n_qb;
+  const int g = bg % p.n_kv_heads, b = bg / p.n_kv_heads;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int t0 = qb * QB;
+  const int nq = min(QB, p.T - t0);
+
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kWarps);
+    }
+    mbar_init_fence();
+  }
+  __syncthreads();
+  grid_wait();   // the rows launch wrote the prompt's cache rows and rotated q rows
+  grid_launch_dependents();
+  const int st = __ldcg(p.start + b);
+  // the item's window ends with its last query's: [0, start + t0 + nq)
+  const int nv_max = min(max(st + t0 + nq, 1), p.capacity);
+  const int c0 = ch * p.ch_len;
+  if (c0 >= nv_max) return;   // the chunk holds no row of any window of the item
+  const int c1 = min(c0 + p.ch_len, nv_max);
+  const int ntiles = (c1 - c0 + kTile - 1) / kTile;
+  const int br = p.paged ? min(kTile, p.page_size) : kTile;
+  const int br_shift = 31 - __clz(br);
+
+  if (warp == kWarps) {
+    // ---------------------------------------------------------------- producer
+    if (lane == 0) {
+      int issued = 0;
+      bool ok = true;
+      const int box_bytes = br * D * static_cast<int>(sizeof(KvT));
+      for (; issued < ntiles; ++issued) {
+        const int s = issued % kStages;
+        if (issued >= kStages && !mbar_wait(&empty[s], static_cast<uint32_t>((issued / kStages) - 1) & 1u)) {
+          ok = false;
+          break;
+        }
+        unsigned char* kd = ring + s * 2 * kTileBytes;
+        unsigned char* vd = kd + kTileBytes;
+        const int r0 = c0 + issued * kTile;
+        if (!p.paged) {
+          mbar_arrive_expect_tx(&full[s], 2 * kTileBytes);
+          const int row = (b * p.n_kv_heads + g) * p.capacity + r0;
+          tma_load_3d_pf(kd, &kmap, 0, row, 0, &full[s]);
+          tma_load_3d_pf(vd, &vmap, 0, row, 0, &full[s]);
+        } else {
+          // the boxes (pages, or 64-row parts of a page) that hold rows of the chunk
+          const int rend = min(r0 + kTile, c1);
+          const int nbox = (rend - r0 + br - 1) / br;
+          mbar_arrive_expect_tx(&full[s], 2 * nbox * box_bytes);
+          for (int k = 0; k < nbox; ++k) {
+            const int pos = r0 + k * br;
+            int page = __ldcg(p.block_table + static_cast<int64_t>(b) * p.bt_stride + pos / p.page_size);
+            if (page < 0 || page >= p.n_pages) {
+              set_err(p.err, TTS_EFLAG_PAGE);
+              page = 0;
+            }
+            const int row = (page * p.n_kv_heads + g) * p.page_size + (pos & (p.page_size - 1));
+            tma_load_3d_pf(kd + k * box_bytes, &kmap, 0, row, 0, &full[s]);
+            tma_load_3d_pf(vd + k * box_bytes, &vmap, 0, row, 0, &full[s]);
+          }
+        }
+      }
+      if (!ok) set_err(p.err, TTS_EFLAG_TIMEOUT);
+      // no copy may still be landing when the CTA leaves
+      for (int t = max(0, issued - kStages); t < issued; ++t)
+        mbar_wait(&full[t % kStages], static_cast<uint32_t>(t / kStages) & 1u);
+    }
+    return;
+  }
+
+  // ------------------------------------------------------------------ consumers
+  // the warp's 8 query rows (row r = t_local * G + h), zero past the prompt
+  float* sqw = sq + warp * 8 * D;
+  for (int e = lane; e < 8 * D / 4; e += 32) {
+    const int i = e / (D / 4), d4 = e - i * (D / 4);
+    const int r = warp * 8 + i, tl = r / G, h = r - tl * G;
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (tl < nq)
+      v = __ldcg(reinterpret_cast<const float4*>(p.q + static_cast<int64_t>(b * p.T + t0 + tl) * p.q_stride +
+                                                 (g * G + h) * D) + d4);
+    reinterpret_cast<float4*>(sqw)[e] = v;
+  }
+  __syncwarp();
+  int nv[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int r = warp * 8 + i, tl = r / G;
+    const int raw = st + t0 + tl + 1;
+    nv[i] = tl < nq ? min(max(raw, 1), p.capacity) : 0;
+    if (ch == 0 && lane == 0 && tl < nq && (r - tl * G) == 0 && g == 0 && (raw < 1 || raw > p.capacity))
+      set_err(p.err, TTS_EFLAG_NVALID);
+  }
+  float m[8], l[8], o[8][DPL];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    m[i] = -INFINITY;
+    l[i] = 0.f;
+#pragma unroll
+    for (int c = 0; c < DPL; ++c) o[i][c] = 0.f;
+  }
+  const uint32_t qw = smem_u32(sqw);
+  float* spw = sp + warp * kTile * 8;
+  const uint32_t pw = smem_u32(spw);
+  bool ok = true;
+  for (int it = 0; it < ntiles; ++it) {
+    const int s = it % kStages;
+    if (!mbar_wait(&full[s], static_cast<uint32_t>(it / kStages) & 1u)) {
+      ok = false;
+      break;
+    }
+    const uint32_t kb = smem_u32(ring + s * 2 * kTileBytes), vb = kb + kTileBytes;
+    const int r0 = c0 + it * kTile, nrow = min(kTile, c1 - r0);
+    float sc[8][2];
+    tile_scores<KvT, D>(kb, qw, lane, br_shift, sc);
+    // online softmax in base 2; a row past a query's window (or past the chunk) gets -inf
+    float p0[8], p1[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float a0 = (lane < nrow && r0 + lane < nv[i]) ? sc[i][0] * p.scale_log2 : -INFINITY;
+      const float a1 = (lane + 32 < nrow && r0 + lane + 32 < nv[i]) ? sc[i][1] * p.scale_log2 : -INFINITY;
+      const float mn = fmaxf(m[i], warp_max(fmaxf(a0, a1)));
+      float alpha = 1.f;
+      if (mn == -INFINITY) {
+        p0[i] = p1[i] = 0.f;
+      } else {
+        alpha = exp2f(m[i] - mn);
+        p0[i] = exp2f(a0 - mn);
+        p1[i] = exp2f(a1 - mn);
+      }
+      l[i] = fmaf(l[i], alpha, warp_sum(p0[i] + p1[i]));
+      m[i] = mn;
+#pragma unroll
+      for (int c = 0; c < DPL; ++c) o[i][c] *= alpha;
+    }
+    // the warp's probabilities: [tile row][8 query rows]
+    reinterpret_cast<float4*>(spw + lane * 8)[0] = make_float4(p0[0], p0[1], p0[2], p0[3]);
+    reinterpret_cast<float4*>(spw + lane * 8)[1] = make_float4(p0[4], p0[5], p0[6], p0[7]);
+    reinterpret_cast<float4*>(spw + (lane + 32) * 8)[0] = make_float4(p1[0], p1[1], p1[2], p1[3]);
+    reinterpret_cast<float4*>(spw + (lane + 32) * 8)[1] = make_float4(p1[4], p1[5], p1[6], p1[7]);
+    __syncwarp();
+    for (int j = 0; j < nrow; ++j) {
+      const float4 pa = lds_f4(pw + j * 32), pb = lds_f4(pw + j * 32 + 16);
+      const float pr[8] = {pa.x, pa.y, pa.z, pa.w, pb.x, pb.y, pb.z, pb.w};
+      float v[DPL];
+      v_cols<KvT, D>(vb, j, lane, br_shift, v);
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int c = 0; c < DPL; ++c) o[i][c] = fmaf(pr[i], v[c], o[i][c]);
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
+  }
+  if (!ok && lane == 0) set_err(p.err, TTS_EFLAG_TIMEOUT);
+
+  // the chunk's rows: normalised when it is the only chunk, else with their max and sum
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int r = warp * 8 + i, tl = r / G, h = r - tl * G;
+    if (tl >= nq) continue;
+    if (p.n_ch == 1) {
+      const float inv = l[i] > 0.f ? 1.f / l[i] : 0.f;
+      float* dst = p.out + (static_cast<int64_t>(b * p.T + t0 + tl) * p.n_q_heads + g * G + h) * D + lane * DPL;
+#pragma unroll
+      for (int c = 0; c < DPL; ++c) dst[c] = o[i][c] * inv;
+    } else {
+      const int64_t row = (static_cast<int64_t>(item) * p.n_ch + ch) * kRows + r;
+      float* dst = p.part + row * D + lane * DPL;
+#pragma unroll
+      for (int c = 0; c < DPL; ++c) dst[c] = o[i][c];
+      if (lane == 0) reinterpret_cast<float2*>(p.ml)[row] = make_float2(m[i], l[i]);
+    }
+  }
+}
+
+
+// The chunks of every query row merged in chunk order: M = max m_c, L = sum l_c 2^(m_c - M),
+// out = sum O_c 2^(m_c - M) / L.  One CTA per item; chunk 0 holds a row of every window.
+__global__ void __launch_bounds__(256) prefill_combine_kernel(const PrefillAttnParams p, int G, int D) {
+  grid_wait();
+  grid_launch_dependents();
+  const int item = blockIdx.x;
+  const int QB = kRows / G;
+  const int qb = item % p.n_qb, bg = item / p.n_qb;
+  const int g = bg % p.n_kv_heads, b = bg / p.n_kv_heads;
+  const int t0 = qb * QB, nq = min(QB, p.T - t0);
+  const int st = __ldcg(p.start + b);
+  const int nv_max = min(max(st + t0 + nq, 1), p.capacity);
+  const int n_act = min(p.n_ch, (nv_max + p.ch_len - 1) / p.ch_len);
+  const int D4 = D / 4;
+  for (int e = threadIdx.x; e < kRows * D4; e += 256) {
+    const int r = e / D4, d4 = e - r * D4, tl = r / G, h = r - tl * G;
+    if (tl >= nq) continue;
+    const int64_t row0 = static_cast<int64_t>(item) * p.n_ch * kRows + r;
+    float M = -INFINITY;
+    for (int c = 0; c < n_act; ++c) M = fmaxf(M, __ldcg(reinterpret_cast<const float2*>(p.ml) + row0 + c * kRows).x);
+    float L = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int c = 0; c < n_act; ++c) {
+      const int64_t row = row0 + c * kRows;
+      const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.ml) + row);
+      const float w = exp2f(ml.x - M);
+      const float4 x = __ldcg(reinterpret_cast<const float4*>(p.part + row * D) + d4);
+      L = fmaf(ml.y, w, L);
+      acc.x = fmaf(x.x, w, acc.x);
+      acc.y = fmaf(x.y, w, acc.y);
+      acc.z = fmaf(x.z, w, acc.z);
+      acc.w = fmaf(x.w, w, acc.w);
+    }
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    reinterpret_cast<float4*>(p.out + (static_cast<int64_t>(b * p.T + t0 + tl) * p.n_q_heads + g * G + h) * D)[d4] =
+        make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+  static std::mutex mtx;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::lock_guard<std::mutex> lock(mtx);
+  if (fn == nullptr) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    else
+      cudaGetLastError();
+  }
+  return fn;
+}
+
+template <typename KvT, int D>
+size_t prefill_smem() {
+  return 1024 + static_cast<size_t>(kStages) * 2 * kTile * D * sizeof(KvT) + static_cast<size_t>(kRows) * D * 4 +
+         static_cast<size_t>(kWarps) * kTile * 8 * 4 + 2 * kStages * sizeof(uint64_t);
+}
+
+template <typename KvT, int D, int G>
+cudaError_t launch_t(const PrefillAttnParams& p, const void* kc, const void* vc, cudaStream_t s) {
+  using Tr = KvTraits<KvT>;
+  auto kern = prefill_attn_kernel<KvT, D, G>;
+  PFN_cuTensorMapEncodeTiled_v12000 enc = encoder();
+  if (enc == nullptr) return cudaErrorNotSupported;
+  // the cache as [D / chunk][rows][chunk elements]: rows of D elements (stride D x size),
+  // 128-byte chunks of a row 128 bytes apart; boxes of br rows
+  const uint64_t rows = p.paged ? static_cast<uint64_t>(p.n_pages) * p.n_kv_heads * p.page_size
+                                : static_cast<uint64_t>(p.B) * p.n_kv_heads * p.capacity;
+  const int br = p.paged ? (p.page_size < kTile ? p.page_size : kTile) : kTile;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(Tr::kPerChunk), rows, static_cast<cuuint64_t>(D / Tr::kPerChunk)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * sizeof(KvT), 128};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(Tr::kPerChunk), static_cast<cuuint32_t>(br),
+                       static_cast<cuuint32_t>(D / Tr::kPerChunk)};
+  cuuint32_t estr[3] = {1, 1, 1};
+  const CUtensorMapDataType dt = sizeof(KvT) == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  CUtensorMap kmap, vmap;
+  if (enc(&kmap, dt, 3, const_cast<void*>(kc), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) !=
+          CUDA_SUCCESS ||
+      enc(&vmap, dt, 3, const_cast<void*>(vc), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) !=
+          CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+  const size_t smem = prefill_smem<KvT, D>();
+  static std::mutex mtx;
+  static bool configured[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  {
+    std::lock_guard<std::mutex> lock(mtx);
+    if (!configured[dev]) {
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+      if (e != cudaSuccess) return e;
+      configured[dev] = true;
+    }
+  }
+  const int items = p.B * p.n_kv_heads * p.n_qb;
+  e = launch_pdl(kern, dim3(items, p.n_ch), dim3(kThreads), smem, s, kmap, vmap, p);
+  if (e != cudaSuccess || p.n_ch == 1) return e;
+  return launch_pdl(prefill_combine_kernel, dim3(items), dim3(256), 0, s, p, G, D);
+}
+
+}  // namespace
+
+bool prefill_attn_supported(int head_dim, int group, int paged, int page_size, int T) {
+  return (head_dim == 64 || head_dim == 128) && (group == 1 || group == 2 || group == 4) &&
+         (!paged || page_size >= 8) && T >= kPrefillMinT;
+}
+
+void prefill_attn_plan(int B, int T, int n_kv_heads, int group, int capacity, int n_splits, int n_sm, int& n_qb,
+                       int& n_ch, int& ch_len) {
+  const int QB = kRows / group;
+  n_qb = (T + QB - 1) / QB;
+  const int items = B * n_kv_heads * n_qb;
+  const int max_ch = (capacity + kTile - 1) / kTile;
+  int c = n_splits > 0 ? n_splits : (4 * n_sm + items - 1) / items;
+  if (n_splits <= 0 && c > (capacity + 4 * kTile - 1) / (4 * kTile)) c = (capacity + 4 * kTile - 1) / (4 * kTile);
+  if (c > max_ch) c = max_ch;
+  if (c < 1) c = 1;
+  ch_len = ((capacity + c - 1) / c + kTile - 1) / kTile * kTile;
+  n_ch = (capacity + ch_len - 1) / ch_len;
+}
+
+size_t prefill_attn_workspace(int B, int T, int n_kv_heads, int group, int head_dim, int capacity, int n_splits,
+                              int n_sm) {
+  int n_qb, n_ch, ch_len;
+  prefill_attn_plan(B, T, n_kv_heads, group, capacity, n_splits, n_sm, n_qb, n_ch, ch_len);
+  if (n_ch == 1) return 0;
+  const size_t rows = static_cast<size_t>(B) * n_kv_heads * n_qb * n_ch * kRows;
+  return rows * (static_cast<size_t>(head_dim) + 2) * sizeof(float);
+}
+
+cudaError_t launch_prefill_attn(const PrefillAttnParams& p, const void* k_cache, const void* v_cache, bool kv_bf16,
+                                int head_dim, int group, cudaStream_t s) {
+#define TTS_PF_CASE(KT, DD, GG) \
+  if (head_dim == DD && group == GG) return launch_t<KT, DD, GG>(p, k_cache, v_cache, s);
+  if (kv_bf16) {
+    TTS_PF_CASE(__nv_bfloat16, 128, 1) TTS_PF_CASE(__nv_bfloat16, 128, 2) TTS_PF_CASE(__nv_bfloat16, 128, 4)
+    TTS_PF_CASE(__nv_bfloat16, 64, 1) TTS_PF_CASE(__nv_bfloat16, 64, 2) TTS_PF_CASE(__nv_bfloat16, 64, 4)
+  } else {
+    TTS_PF_CASE(float, 128, 1) TTS_PF_CASE(float, 128, 2) TTS_PF_CASE(float, 128, 4)
+    TTS_PF_CASE(float, 64, 1) TTS_PF_CASE(float, 64, 2) TTS_PF_CASE(float, 64, 4)
+  }
+#undef TTS_PF_CASE
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace tts
