@@ -62,19 +62,6 @@ __device__ __forceinline__ void tma_load_3d_pf(void* dst, const CUtensorMap* map
       : "memory");
 }
 
-// Byte offset of 16-byte unit `u` (of the D row) of tile row j in a tile written as
-// boxes of `br` rows (br a power of two >= 8): box j / br, then the row's 128-byte
-// chunk, then the row; the 128-byte swizzle permutes units within a chunk by row % 8.
-template <typename KvT, int D>
-__device__ __forceinline__ uint32_t tile_off(int j, int u, int br_shift) {
-  using Tr = KvTraits<KvT>;
-  constexpr int kChunks = D / Tr::kPerChunk;
-  const int br = 1 << br_shift;
-  const int box = j >> br_shift, jr = j & (br - 1);
-  const int c = u >> 3, uc = u & 7;
-  return static_cast<uint32_t>(((box * kChunks + c) * br + jr) * 128 + ((uc ^ (j & 7)) << 4));
-}
-
 __device__ __forceinline__ float4 lds_f4(uint32_t addr) {
   float4 v;
   asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
@@ -99,46 +86,66 @@ __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w 
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
 
-// Scores of the warp's 8 query rows against tile rows `lane` and `lane + 32`.
+// Placement of a tile in shared memory: boxes of br = 2^br_shift rows, each box
+// [128-byte chunk c][row][128 bytes], so row j's chunk c starts at
+//   row_base(j) + c * br * 128,  row_base(j) = ((j >> br_shift) * chunks * br + (j & (br - 1))) * 128,
+// and its 16-byte unit uc sits at ((uc ^ (j & 7)) << 4) within the chunk.
 template <typename KvT, int D>
-__device__ __forceinline__ void tile_scores(uint32_t kb, uint32_t qw, int lane, int br_shift, float (&sc)[8][2]) {
+__device__ __forceinline__ uint32_t row_base(int j, int br_shift) {
+  constexpr int kChunks = D / KvTraits<KvT>::kPerChunk;
+  return static_cast<uint32_t>((((j >> br_shift) * kChunks << br_shift) + (j & ((1 << br_shift) - 1))) * 128);
+}
+
+// Scores of the warp's 8 query rows against tile rows `lane` and `lane + 32` (the same
+// row % 8, so one swizzle serves both), as pairs of partial sums over the even and odd
+// columns of D (packed f32 multiply-adds on adjacent elements); the caller adds the
+// halves.
+template <typename KvT, int D>
+__device__ __forceinline__ void tile_scores(uint32_t kb, uint32_t qw, int lane, int br_shift, float2 (&sc)[8][2]) {
   using Tr = KvTraits<KvT>;
-  constexpr int kUnits = D / Tr::kPerUnit;
+  constexpr int kChunks = D / Tr::kPerChunk;
+  const uint32_t b0 = kb + row_base<KvT, D>(lane, br_shift);
+  const uint32_t b1 = kb + row_base<KvT, D>(lane + 32, br_shift);
+  const uint32_t cstride = 128u << br_shift;
+  const int j7 = lane & 7;
 #pragma unroll
-  for (int i = 0; i < 8; ++i) sc[i][0] = sc[i][1] = 0.f;
-#pragma unroll 2
-  for (int u = 0; u < kUnits; ++u) {
-    const uint32_t a0 = kb + tile_off<KvT, D>(lane, u, br_shift);
-    const uint32_t a1 = kb + tile_off<KvT, D>(lane + 32, u, br_shift);
-    if constexpr (Tr::kPerUnit == 4) {
-      const float4 k0 = lds_f4(a0), k1 = lds_f4(a1);
+  for (int i = 0; i < 8; ++i) sc[i][0] = sc[i][1] = make_float2(0.f, 0.f);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float4 q = lds_f4(qw + (i * D + u * 4) * 4);
-        sc[i][0] = fmaf(q.x, k0.x, sc[i][0]);
-        sc[i][1] = fmaf(q.x, k1.x, sc[i][1]);
-        sc[i][0] = fmaf(q.y, k0.y, sc[i][0]);
-        sc[i][1] = fmaf(q.y, k1.y, sc[i][1]);
-        sc[i][0] = fmaf(q.z, k0.z, sc[i][0]);
-        sc[i][1] = fmaf(q.z, k1.z, sc[i][1]);
-        sc[i][0] = fmaf(q.w, k0.w, sc[i][0]);
-        sc[i][1] = fmaf(q.w, k1.w, sc[i][1]);
-      }
-    } else {
-      const uint4 w0 = lds128_addr(a0), w1 = lds128_addr(a1);
-      const float k0[8] = {bf16_lo(w0.x), bf16_hi(w0.x), bf16_lo(w0.y), bf16_hi(w0.y),
-                           bf16_lo(w0.z), bf16_hi(w0.z), bf16_lo(w0.w), bf16_hi(w0.w)};
-      const float k1[8] = {bf16_lo(w1.x), bf16_hi(w1.x), bf16_lo(w1.y), bf16_hi(w1.y),
-                           bf16_lo(w1.z), bf16_hi(w1.z), bf16_lo(w1.w), bf16_hi(w1.w)};
+  for (int c = 0; c < kChunks; ++c) {
+#pragma unroll 4
+    for (int uc = 0; uc < 8; ++uc) {
+      const uint32_t off = c * cstride + ((uc ^ j7) << 4);
+      const int u = c * 8 + uc;
+      if constexpr (Tr::kPerUnit == 4) {
+        const float4 k0 = lds_f4(b0 + off), k1 = lds_f4(b1 + off);
+        const float2 k0a = make_float2(k0.x, k0.y), k0b = make_float2(k0.z, k0.w);
+        const float2 k1a = make_float2(k1.x, k1.y), k1b = make_float2(k1.z, k1.w);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float4 qa = lds_f4(qw + (i * D + u * 8) * 4);
-        const float4 qc = lds_f4(qw + (i * D + u * 8 + 4) * 4);
-        const float q[8] = {qa.x, qa.y, qa.z, qa.w, qc.x, qc.y, qc.z, qc.w};
+        for (int i = 0; i < 8; ++i) {
+          const float4 q = lds_f4(qw + (i * D + u * 4) * 4);
+          const float2 qa = make_float2(q.x, q.y), qb = make_float2(q.z, q.w);
+          sc[i][0] = __ffma2_rn(qa, k0a, sc[i][0]);
+          sc[i][1] = __ffma2_rn(qa, k1a, sc[i][1]);
+          sc[i][0] = __ffma2_rn(qb, k0b, sc[i][0]);
+          sc[i][1] = __ffma2_rn(qb, k1b, sc[i][1]);
+        }
+      } else {
+        const uint4 w0 = lds128_addr(b0 + off), w1 = lds128_addr(b1 + off);
+        const float2 k0[4] = {make_float2(bf16_lo(w0.x), bf16_hi(w0.x)), make_float2(bf16_lo(w0.y), bf16_hi(w0.y)),
+                              make_float2(bf16_lo(w0.z), bf16_hi(w0.z)), make_float2(bf16_lo(w0.w), bf16_hi(w0.w))};
+        const float2 k1[4] = {make_float2(bf16_lo(w1.x), bf16_hi(w1.x)), make_float2(bf16_lo(w1.y), bf16_hi(w1.y)),
+                              make_float2(bf16_lo(w1.z), bf16_hi(w1.z)), make_float2(bf16_lo(w1.w), bf16_hi(w1.w))};
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          sc[i][0] = fmaf(q[e], k0[e], sc[i][0]);
-          sc[i][1] = fmaf(q[e], k1[e], sc[i][1]);
+        for (int i = 0; i < 8; ++i) {
+          const float4 qa = lds_f4(qw + (i * D + u * 8) * 4);
+          const float4 qc = lds_f4(qw + (i * D + u * 8 + 4) * 4);
+          const float2 q[4] = {make_float2(qa.x, qa.y), make_float2(qa.z, qa.w), make_float2(qc.x, qc.y),
+                               make_float2(qc.z, qc.w)};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            sc[i][0] = __ffma2_rn(q[e], k0[e], sc[i][0]);
+            sc[i][1] = __ffma2_rn(q[e], k1[e], sc[i][1]);
+          }
         }
       }
     }
@@ -152,7 +159,8 @@ __device__ __forceinline__ void v_cols(uint32_t vb, int j, int lane, int br_shif
   constexpr int DPL = D / 32;
   constexpr int kLanesPerUnit = Tr::kPerUnit / DPL;
   const int u = lane / kLanesPerUnit, part = lane % kLanesPerUnit;
-  const uint32_t a = vb + tile_off<KvT, D>(j, u, br_shift) + part * DPL * static_cast<int>(sizeof(KvT));
+  const uint32_t a = vb + row_base<KvT, D>(j, br_shift) + (u >> 3) * (128u << br_shift) + (((u & 7) ^ (j & 7)) << 4) +
+                     part * DPL * static_cast<int>(sizeof(KvT));
   if constexpr (sizeof(KvT) == 4 && DPL == 4) {
     const float4 x = lds_f4(a);
     v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
@@ -290,14 +298,18 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_attn_kernel(const __grid_
     if (ch == 0 && lane == 0 && tl < nq && (r - tl * G) == 0 && g == 0 && (raw < 1 || raw > p.capacity))
       set_err(p.err, TTS_EFLAG_NVALID);
   }
-  float m[8], l[8], o[8][DPL];
+  // o2[ip][c]: columns lane * DPL + c of rows 2 ip and 2 ip + 1 (packed multiply-adds)
+  float m[8], l[8];
+  float2 o2[4][DPL];
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     m[i] = -INFINITY;
     l[i] = 0.f;
-#pragma unroll
-    for (int c = 0; c < DPL; ++c) o[i][c] = 0.f;
   }
+#pragma unroll
+  for (int ip = 0; ip < 4; ++ip)
+#pragma unroll
+    for (int c = 0; c < DPL; ++c) o2[ip][c] = make_float2(0.f, 0.f);
   const uint32_t qw = smem_u32(sqw);
   float* spw = sp + warp * kTile * 8;
   const uint32_t pw = smem_u32(spw);
@@ -310,14 +322,15 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_attn_kernel(const __grid_
     }
     const uint32_t kb = smem_u32(ring + s * 2 * kTileBytes), vb = kb + kTileBytes;
     const int r0 = c0 + it * kTile, nrow = min(kTile, c1 - r0);
-    float sc[8][2];
-    tile_scores<KvT, D>(kb, qw, lane, br_shift, sc);
+    float2 sc2[8][2];
+    tile_scores<KvT, D>(kb, qw, lane, br_shift, sc2);
     // online softmax in base 2; a row past a query's window (or past the chunk) gets -inf
-    float p0[8], p1[8];
+    float p0[8], p1[8], al[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      const float a0 = (lane < nrow && r0 + lane < nv[i]) ? sc[i][0] * p.scale_log2 : -INFINITY;
-      const float a1 = (lane + 32 < nrow && r0 + lane + 32 < nv[i]) ? sc[i][1] * p.scale_log2 : -INFINITY;
+      const float s0 = sc2[i][0].x + sc2[i][0].y, s1 = sc2[i][1].x + sc2[i][1].y;
+      const float a0 = (lane < nrow && r0 + lane < nv[i]) ? s0 * p.scale_log2 : -INFINITY;
+      const float a1 = (lane + 32 < nrow && r0 + lane + 32 < nv[i]) ? s1 * p.scale_log2 : -INFINITY;
       const float mn = fmaxf(m[i], warp_max(fmaxf(a0, a1)));
       float alpha = 1.f;
       if (mn == -INFINITY) {
@@ -329,8 +342,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_attn_kernel(const __grid_
       }
       l[i] = fmaf(l[i], alpha, warp_sum(p0[i] + p1[i]));
       m[i] = mn;
+      al[i] = alpha;
+    }
 #pragma unroll
-      for (int c = 0; c < DPL; ++c) o[i][c] *= alpha;
+    for (int ip = 0; ip < 4; ++ip) {
+      const float2 a2 = make_float2(al[2 * ip], al[2 * ip + 1]);
+#pragma unroll
+      for (int c = 0; c < DPL; ++c) o2[ip][c] = __fmul2_rn(o2[ip][c], a2);
     }
     // the warp's probabilities: [tile row][8 query rows]
     reinterpret_cast<float4*>(spw + lane * 8)[0] = make_float4(p0[0], p0[1], p0[2], p0[3]);
@@ -338,15 +356,19 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_attn_kernel(const __grid_
     reinterpret_cast<float4*>(spw + (lane + 32) * 8)[0] = make_float4(p1[0], p1[1], p1[2], p1[3]);
     reinterpret_cast<float4*>(spw + (lane + 32) * 8)[1] = make_float4(p1[4], p1[5], p1[6], p1[7]);
     __syncwarp();
+#pragma unroll 4
     for (int j = 0; j < nrow; ++j) {
       const float4 pa = lds_f4(pw + j * 32), pb = lds_f4(pw + j * 32 + 16);
-      const float pr[8] = {pa.x, pa.y, pa.z, pa.w, pb.x, pb.y, pb.z, pb.w};
+      const float2 pr[4] = {make_float2(pa.x, pa.y), make_float2(pa.z, pa.w), make_float2(pb.x, pb.y),
+                            make_float2(pb.z, pb.w)};
       float v[DPL];
       v_cols<KvT, D>(vb, j, lane, br_shift, v);
 #pragma unroll
-      for (int i = 0; i < 8; ++i)
+      for (int c = 0; c < DPL; ++c) {
+        const float2 v2 = make_float2(v[c], v[c]);
 #pragma unroll
-        for (int c = 0; c < DPL; ++c) o[i][c] = fmaf(pr[i], v[c], o[i][c]);
+        for (int ip = 0; ip < 4; ++ip) o2[ip][c] = __ffma2_rn(pr[ip], v2, o2[ip][c]);
+      }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);
@@ -358,16 +380,19 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_attn_kernel(const __grid_
   for (int i = 0; i < 8; ++i) {
     const int r = warp * 8 + i, tl = r / G, h = r - tl * G;
     if (tl >= nq) continue;
+    float o[DPL];
+#pragma unroll
+    for (int c = 0; c < DPL; ++c) o[c] = (i & 1) ? o2[i >> 1][c].y : o2[i >> 1][c].x;
     if (p.n_ch == 1) {
       const float inv = l[i] > 0.f ? 1.f / l[i] : 0.f;
       float* dst = p.out + (static_cast<int64_t>(b * p.T + t0 + tl) * p.n_q_heads + g * G + h) * D + lane * DPL;
 #pragma unroll
-      for (int c = 0; c < DPL; ++c) dst[c] = o[i][c] * inv;
+      for (int c = 0; c < DPL; ++c) dst[c] = o[c] * inv;
     } else {
       const int64_t row = (static_cast<int64_t>(item) * p.n_ch + ch) * kRows + r;
       float* dst = p.part + row * D + lane * DPL;
 #pragma unroll
-      for (int c = 0; c < DPL; ++c) dst[c] = o[i][c];
+      for (int c = 0; c < DPL; ++c) dst[c] = o[c];
       if (lane == 0) reinterpret_cast<float2*>(p.ml)[row] = make_float2(m[i], l[i]);
     }
   }
@@ -375,7 +400,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_attn_kernel(const __grid_
 
 
 // The chunks of every query row merged in chunk order: M = max m_c, L = sum l_c 2^(m_c - M),
-// out = sum O_c 2^(m_c - M) / L.  One CTA per item; chunk 0 holds a row of every window.
+// out = sum O_c 2^(m_c - M) / L.  One CTA per (item, 8 query rows), a thread per (row,
+// 4 columns); chunk 0 holds a row of every window, so M is finite.
+constexpr int kCombineRows = 8;
+constexpr int kMaxCombineChunks = 64;
 __global__ void __launch_bounds__(256) prefill_combine_kernel(const PrefillAttnParams p, int G, int D) {
   grid_wait();
   grid_launch_dependents();
@@ -386,31 +414,34 @@ __global__ void __launch_bounds__(256) prefill_combine_kernel(const PrefillAttnP
   const int t0 = qb * QB, nq = min(QB, p.T - t0);
   const int st = __ldcg(p.start + b);
   const int nv_max = min(max(st + t0 + nq, 1), p.capacity);
-  const int n_act = min(p.n_ch, (nv_max + p.ch_len - 1) / p.ch_len);
+  const int n_act = min(min(p.n_ch, kMaxCombineChunks), (nv_max + p.ch_len - 1) / p.ch_len);
   const int D4 = D / 4;
-  for (int e = threadIdx.x; e < kRows * D4; e += 256) {
-    const int r = e / D4, d4 = e - r * D4, tl = r / G, h = r - tl * G;
-    if (tl >= nq) continue;
-    const int64_t row0 = static_cast<int64_t>(item) * p.n_ch * kRows + r;
-    float M = -INFINITY;
-    for (int c = 0; c < n_act; ++c) M = fmaxf(M, __ldcg(reinterpret_cast<const float2*>(p.ml) + row0 + c * kRows).x);
-    float L = 0.f;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int c = 0; c < n_act; ++c) {
-      const int64_t row = row0 + c * kRows;
-      const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.ml) + row);
-      const float w = exp2f(ml.x - M);
-      const float4 x = __ldcg(reinterpret_cast<const float4*>(p.part + row * D) + d4);
-      L = fmaf(ml.y, w, L);
-      acc.x = fmaf(x.x, w, acc.x);
-      acc.y = fmaf(x.y, w, acc.y);
-      acc.z = fmaf(x.z, w, acc.z);
-      acc.w = fmaf(x.w, w, acc.w);
-    }
-    const float inv = L > 0.f ? 1.f / L : 0.f;
-    reinterpret_cast<float4*>(p.out + (static_cast<int64_t>(b * p.T + t0 + tl) * p.n_q_heads + g * G + h) * D)[d4] =
-        make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+  const int e = threadIdx.x;
+  if (e >= kCombineRows * D4) return;
+  const int r = blockIdx.y * kCombineRows + e / D4, d4 = e % D4, tl = r / G, h = r - tl * G;
+  if (tl >= nq) return;
+  const int64_t row0 = static_cast<int64_t>(item) * p.n_ch * kRows + r;
+  const float2* ml = reinterpret_cast<const float2*>(p.ml) + row0;
+  float M = -INFINITY;
+#pragma unroll 8
+  for (int c = 0; c < n_act; ++c) M = fmaxf(M, __ldcg(ml + c * kRows).x);
+  float L = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+  for (int c = 0; c < n_act; ++c) {
+    const int64_t row = row0 + c * kRows;
+    const float2 mlc = __ldcg(ml + c * kRows);
+    const float4 x = __ldcg(reinterpret_cast<const float4*>(p.part + row * D) + d4);
+    const float w = exp2f(mlc.x - M);
+    L = fmaf(mlc.y, w, L);
+    acc.x = fmaf(x.x, w, acc.x);
+    acc.y = fmaf(x.y, w, acc.y);
+    acc.z = fmaf(x.z, w, acc.z);
+    acc.w = fmaf(x.w, w, acc.w);
   }
+  const float inv = L > 0.f ? 1.f / L : 0.f;
+  reinterpret_cast<float4*>(p.out + (static_cast<int64_t>(b * p.T + t0 + tl) * p.n_q_heads + g * G + h) * D)[d4] =
+      make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encoder() {
@@ -478,7 +509,7 @@ cudaError_t launch_t(const PrefillAttnParams& p, const void* kc, const void* vc,
   const int items = p.B * p.n_kv_heads * p.n_qb;
   e = launch_pdl(kern, dim3(items, p.n_ch), dim3(kThreads), smem, s, kmap, vmap, p);
   if (e != cudaSuccess || p.n_ch == 1) return e;
-  return launch_pdl(prefill_combine_kernel, dim3(items), dim3(256), 0, s, p, G, D);
+  return launch_pdl(prefill_combine_kernel, dim3(items, kRows / kCombineRows), dim3(256), 0, s, p, G, D);
 }
 
 }  // namespace
@@ -497,6 +528,7 @@ void prefill_attn_plan(int B, int T, int n_kv_heads, int group, int capacity, in
   int c = n_splits > 0 ? n_splits : (4 * n_sm + items - 1) / items;
   if (n_splits <= 0 && c > (capacity + 4 * kTile - 1) / (4 * kTile)) c = (capacity + 4 * kTile - 1) / (4 * kTile);
   if (c > max_ch) c = max_ch;
+  if (c > kMaxCombineChunks) c = kMaxCombineChunks;
   if (c < 1) c = 1;
   ch_len = ((capacity + c - 1) / c + kTile - 1) / kTile * kTile;
   n_ch = (capacity + ch_len - 1) / ch_len;
