@@ -306,7 +306,12 @@ tts_status tts_decode_step_noalloc(const float* q, const float* k, const float* 
  *        row's write and sets TTS_EFLAG_PAGE.
  *   workspace: at least tts_prefill_workspace_size(desc, T, n_splits) bytes, otherwise
  *        as for tts_decode_attn (its B x T queries take the place of its B streams).
- * Two launches on `stream`: the rows, then the attention.  B*T must not exceed 65535.
+ * Launches on `stream`: the rows, then the attention.  T < 8: the attention runs the
+ * B*T queries one by one (as tts_decode_attn).  T >= 8 (and, paged, pages of 8 rows or
+ * more): blocks of 64 / (Hq / Hkv) queries of a stream share every K/V tile of their
+ * window, the windows cut into chunks; with more than one chunk a third launch merges
+ * them in chunk order (that path's workspace needs no zeroing).  B*T must not exceed
+ * 65535.
  * ------------------------------------------------------------------------- */
 size_t tts_prefill_workspace_size(const tts_kv_desc* desc, int32_t T, int32_t n_splits);
 
@@ -352,7 +357,7 @@ tts_status tts_sample(const float* logits, int64_t logits_stride, int32_t B, int
 tts_status tts_counter_advance(uint64_t* counter, uint64_t by, void* stream);
 
 /* ---------------------------------------------------------------------------
- * One whole talker decode layer with bf16 weights, for B <= 8 streams ([engine] core
+ * One whole talker decode layer with bf16 weights, for B <= 32 streams ([engine] core
  * table: fused residual add + RMSNorm, q/k norm + RoPE, SiLU-multiply, reproducing the
  * reference rounding with integer round-to-nearest-even; [pipeline] KV-cache section
  * for the step).  In place on the residual stream h [B][hidden] (f32):
@@ -363,8 +368,13 @@ tts_status tts_counter_advance(uint64_t* counter, uint64_t by, void* stream);
  *   x = bf16(rmsnorm(h) * gamma_mlp)
  *   a = bf16(silu(x W_gate^T) * x W_up^T)       (silu in f32)
  *   h = h + a W_down^T
- * Products accumulate in f32; every residual add is one f32 addition.  Five launches
- * on `stream` (four GEMVs and the decode step).  The weights and the gammas are treated
+ * Products accumulate in f32; every residual add is one f32 addition.  One to three
+ * streams: five launches on `stream` (four GEMVs on the CUDA cores and the decode
+ * step).  Four or more: the projections run on the tensor cores (bf16 x bf16, f32
+ * accumulator) and each norm or f32 input is first rounded and packed for them by a
+ * small kernel, eight launches (three packs, four projections, the decode step); the
+ * sums of a projection's column ranges are added in a fixed order, so results do not
+ * depend on timing.  The weights and the gammas are treated
  * as constants: each launch starts reading them before the preceding kernel on `stream`
  * has finished, so they must not be written by the kernel launched just before this
  * call on the same stream (write them with a copy, or synchronise first).  Weights are bf16, row-major, rows of `hidden` (or `inter`) elements:
