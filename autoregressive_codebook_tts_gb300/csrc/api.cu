@@ -517,6 +517,12 @@ tts_status tts_counter_advance(uint64_t* counter, uint64_t by, void* stream) {
   return from_cuda(launch_counter_advance(counter, by, as_stream(stream)));
 }
 
+tts_status tts_check_wait_timeout(int32_t* err_flag, void* stream) {
+  if (err_flag == nullptr) return TTS_ERR_NULL;
+  if ((reinterpret_cast<uintptr_t>(err_flag) & 3u) != 0) return TTS_ERR_ALIGN;
+  return from_cuda(launch_wait_timeout_probe(err_flag, as_stream(stream)));
+}
+
 }  // extern "C"
 
 namespace {

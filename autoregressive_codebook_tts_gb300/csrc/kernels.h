@@ -154,6 +154,7 @@ cudaError_t launch_rope_table(float* cs, int max_pos, int head_dim, double base,
 cudaError_t launch_qk_norm_rope(const NormRopeParams& p, cudaStream_t s);
 cudaError_t launch_set_rows(const SetRowsParams& p, cudaStream_t s);
 cudaError_t launch_zero(void* ptr, size_t bytes, cudaStream_t s);
+cudaError_t launch_wait_timeout_probe(int32_t* err, cudaStream_t s);
 cudaError_t launch_prefill_rows(const PrefillRowsParams& p, cudaStream_t s);
 cudaError_t launch_sample(const SampleParams& p, cudaStream_t s);
 cudaError_t launch_counter_advance(uint64_t* counter, uint64_t by, cudaStream_t s);

@@ -333,6 +333,21 @@ cudaError_t launch_prefill_rows(const PrefillRowsParams& p, cudaStream_t s) {
   return cudaErrorInvalidValue;
 }
 
+// Self-test of the bounded wait: one thread waits for phase 0 of an mbarrier that nothing
+// arrives on, through the same mbar_wait every kernel uses; when the wait limit runs out it
+// sets TTS_EFLAG_TIMEOUT and returns.
+__global__ void wait_timeout_probe_kernel(int32_t* err) {
+  __shared__ uint64_t bar;
+  mbar_init(&bar, 1);
+  mbar_init_fence();
+  if (!mbar_wait(&bar, 0u)) set_err(err, TTS_EFLAG_TIMEOUT);
+}
+
+cudaError_t launch_wait_timeout_probe(int32_t* err, cudaStream_t s) {
+  wait_timeout_probe_kernel<<<1, 1, 0, s>>>(err);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_zero(void* ptr, size_t bytes, cudaStream_t s) {
   const size_t n16 = bytes / 16;
   if (n16 == 0) return cudaSuccess;

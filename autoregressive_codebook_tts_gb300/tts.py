@@ -43,6 +43,7 @@ EXPORTED = [
     "tts_prefill_step",
     "tts_sample",
     "tts_counter_advance",
+    "tts_check_wait_timeout",
     "tts_decode_layer_scratch_size",
     "tts_decode_layer",
 ]
@@ -95,6 +96,7 @@ _sigs = {
     "tts_sample": ([_P, _I64, _I32, _I32, _I32, _F, ctypes.c_uint64, _P, ctypes.c_uint32, _P, _I64, _P],
                    _I32),
     "tts_counter_advance": ([_P, ctypes.c_uint64, _P], _I32),
+    "tts_check_wait_timeout": ([_P, _P], _I32),
     "tts_decode_layer_scratch_size": ([ctypes.POINTER(TtsKvDesc), _I32, _I32, _I32], _SZ),
     "tts_decode_layer": ([_P, ctypes.POINTER(TtsLayerWeights), _F, _P, _I32, _P, _P,
                           ctypes.POINTER(TtsKvDesc), _P, _F, _P, _SZ, _I32, _P, _P], _I32),
@@ -316,6 +318,12 @@ def tts_sample(logits, top_k, temperature, seed, counter, out_ids, draw=0, strea
 def tts_counter_advance(counter, by=1, stream=None):
     _check(_lib.tts_counter_advance(_ptr(counter), ctypes.c_uint64(int(by)), _stream(stream)),
            "tts_counter_advance")
+
+
+def tts_check_wait_timeout(err_flag, stream=None):
+    """One bounded wait that nothing ends: sets TTS_EFLAG_TIMEOUT in err_flag after about
+    a second."""
+    _check(_lib.tts_check_wait_timeout(_ptr(err_flag), _stream(stream)), "tts_check_wait_timeout")
 
 
 def layer_weights(w_qkv, w_o, w_gu, w_down, gamma_attn, gamma_mlp, gamma_q, gamma_k) -> TtsLayerWeights:

@@ -357,6 +357,18 @@ tts_status tts_sample(const float* logits, int64_t logits_stride, int32_t B, int
 tts_status tts_counter_advance(uint64_t* counter, uint64_t by, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * Self-test of the error path of the bounded waits.  Every wait inside this library's
+ * kernels (on an mbarrier, a cluster peer or a counter) gives up after a fixed number
+ * of SM clock cycles (about a second at the GB300's clocks), sets TTS_EFLAG_TIMEOUT in
+ * err_flag and winds its kernel down, so the context stays usable (the workspace of
+ * the call must then be re-zeroed before its next use).  This call launches one thread
+ * that waits, with that same wait, for an mbarrier phase that nothing completes: after
+ * the limit it sets TTS_EFLAG_TIMEOUT in *err_flag (device int32) and returns.  It
+ * faults nothing and holds the GPU for about a second; for tests of error handling.
+ * ------------------------------------------------------------------------- */
+tts_status tts_check_wait_timeout(int32_t* err_flag, void* stream);
+
+/* ---------------------------------------------------------------------------
  * One whole talker decode layer with bf16 weights, for B <= 32 streams ([engine] core
  * table: fused residual add + RMSNorm, q/k norm + RoPE, SiLU-multiply, reproducing the
  * reference rounding with integer round-to-nearest-even; [pipeline] KV-cache section
