@@ -527,9 +527,12 @@ tts_status tts_check_wait_timeout(int32_t* err_flag, void* stream) {
 
 namespace {
 
-// From this many streams on the layer's projections run on the tensor cores.
+// From this many streams on the layer's projections run on the tensor cores (default:
+// always; their 64 KB tensor-map stages stream the weights faster than the CUDA-core
+// GEMVs of layer.cu even at one stream, where 15 of the MMA's 16 columns are padding).
+// A build with a larger value keeps the CUDA-core GEMVs below it.
 #ifndef TTS_MMA_MIN_STREAMS
-#define TTS_MMA_MIN_STREAMS 4
+#define TTS_MMA_MIN_STREAMS 1
 #endif
 constexpr int kMmaMinStreams = TTS_MMA_MIN_STREAMS;
 
@@ -597,8 +600,8 @@ tts_status tts_decode_layer(float* h, const tts_layer_weights* w, float eps, con
   float* qkv = reinterpret_cast<float*>(sc + L.qkv_off);
   float* attn = reinterpret_cast<float*>(sc + L.attn_off);
   cudaStream_t s = as_stream(stream);
-  // one stream: the ring GEMV; 2..kMmaMinStreams-1: the register GEMV; from
-  // kMmaMinStreams on: the tensor-core GEMV
+  // from kMmaMinStreams streams on the tensor-core GEMV; below it (a build option) the
+  // ring GEMV for one stream and the register GEMV for more
   auto gemv = [&](const GemvParams& g, int x_mode, int epilogue) -> cudaError_t {
     if (B >= kMmaMinStreams) return launch_gemv_mma(g, x_mode, epilogue, sc + L.xp_off, s);
     return launch_gemv_bf16(g, x_mode, epilogue, s);

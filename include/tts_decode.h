@@ -380,13 +380,12 @@ tts_status tts_check_wait_timeout(int32_t* err_flag, void* stream);
  *   x = bf16(rmsnorm(h) * gamma_mlp)
  *   a = bf16(silu(x W_gate^T) * x W_up^T)       (silu in f32)
  *   h = h + a W_down^T
- * Products accumulate in f32; every residual add is one f32 addition.  One to three
- * streams: five launches on `stream` (four GEMVs on the CUDA cores and the decode
- * step).  Four or more: the projections run on the tensor cores (bf16 x bf16, f32
- * accumulator) and each norm or f32 input is first rounded and packed for them by a
- * small kernel, eight launches (three packs, four projections, the decode step); the
- * sums of a projection's column ranges are added in a fixed order, so results do not
- * depend on timing.  The weights and the gammas are treated
+ * Products accumulate in f32; every residual add is one f32 addition.  The projections
+ * run on the tensor cores (bf16 x bf16, f32 accumulator) and each norm or f32 input is
+ * first rounded and packed for them by a small kernel: eight launches on `stream`
+ * (three packs, four projections, the decode step); the sums of a projection's column
+ * ranges are added in a fixed order, so results do not depend on timing.  The weights
+ * and the gammas are treated
  * as constants: each launch starts reading them before the preceding kernel on `stream`
  * has finished, so they must not be written by the kernel launched just before this
  * call on the same stream (write them with a copy, or synchronise first).  Weights are bf16, row-major, rows of `hidden` (or `inter`) elements:

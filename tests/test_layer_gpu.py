@@ -4,8 +4,8 @@ oracle's decode_layer: the residual stream after the layer within 1e-3 per strea
 products in f32 where the oracle sums them exactly, so a bf16 rounding of an
 intermediate (the norm output, the attention output, the SiLU product) can land one
 bf16 step apart; such a step moves the layer's output by about 2^-8 of one product
-term, far inside the bound.  From four streams on the projections run on the tensor
-cores, whose f32 accumulation order differs again; the bound covers it the same way."""
+term, far inside the bound.  The projections run on the tensor cores, whose f32
+accumulation order differs again; the bound covers it the same way."""
 import numpy as np
 import pytest
 import torch
@@ -39,15 +39,14 @@ def _bits16(t):
 
 # The talker shapes, and two smaller layers whose row lengths split into several
 # segments of 768 / 1280 elements (hidden 768 / 1280, intermediate 3 x hidden) with
-# partial row groups at the ends of the CTAs' ranges; one stream runs the ring kernel,
-# two or more the register kernel.
+# partial ranges at the ends of the clusters' column splits (1 to 8 streams use the
+# MMA's N of 16 with padding slots).
 SMALL_768 = dict(hidden=768, n_q_heads=4, n_kv_heads=2, capacity=512)
 SMALL_1280 = dict(hidden=1280, n_q_heads=8, n_kv_heads=2, capacity=512)
 
 
-# From four streams on the projections run on the tensor cores (tcgen05): 16 and 32
-# streams use the MMA's N of 16 and 32, the small layers odd tile counts and column
-# ranges (hidden 768: six 128-row tiles of the output projections, 2304 SiLU items).
+# 16 and 32 streams use the MMA's N of 16 and 32, the small layers odd tile counts and
+# column ranges (hidden 768: six 128-row tiles of the output projections, 2304 SiLU items).
 STREAMS_16 = [3, 40, 97, 130, 200, 255, 256, 300, 311, 350, 400, 401, 450, 480, 500, 511]
 STREAMS_32 = [(b * 37) % 512 for b in range(32)]
 
