@@ -501,43 +501,76 @@ def measure_frames(args, tts, W, w, cur_arg, cur_list, dev, rank, world, full):
 
     t_e2e, e2e_steps, h2d, d2h = None, 0, 0, 0
     if full:
-        # end to end through the public calls with host buffers: upload this frame's
-        # inputs from pinned memory, run the frame, read back every layer's output
+        # End to end through the public calls with host buffers, pipelined as a serving
+        # loop would run it: two frame states (each its own inputs, caches, outputs and
+        # graph) alternate; step k+1's inputs are uploaded from pinned memory on a copy
+        # stream while frame k runs, and frame k's outputs (every layer's attention rows,
+        # the composed inputs, the error flag) are read back on the copy stream once it
+        # ends.  Every step's uploads and read-backs lie inside the timed region.
+        frame2, _, state2 = build_frame(tts, W, w, cur_arg, args.n_splits, dev, seed=rank)
+        g_frame2 = capture(frame2, torch)
+        sets = [(state, g_frame), (state2, g_frame2)]
         h_ids = state["ids"].cpu().pin_memory()
         h_ov = state["overlay"].cpu().pin_memory()
         h_qkv = state["qkv"].cpu().pin_memory()
         h_cur = state["cur"].cpu().pin_memory()
         h_out = torch.empty_like(state["outs"], device="cpu").pin_memory()
         h_emb = torch.empty_like(state["emb"], device="cpu").pin_memory()
-        h_ef = torch.empty(1, dtype=torch.int32).pin_memory()
+        h_ef = [torch.zeros(1, dtype=torch.int32).pin_memory() for _ in range(2)]
         s = torch.cuda.current_stream()
+        cp = torch.cuda.Stream(device=dev)
+        up = [torch.cuda.Event() for _ in range(2)]
+        done = [torch.cuda.Event() for _ in range(2)]
 
-        def e2e_step():
-            state["ids"].copy_(h_ids, non_blocking=True)
-            state["overlay"].copy_(h_ov, non_blocking=True)
-            state["qkv"].copy_(h_qkv, non_blocking=True)
-            state["cur"].copy_(h_cur, non_blocking=True)
-            g_frame.replay()
-            h_out.copy_(state["outs"], non_blocking=True)
-            h_emb.copy_(state["emb"], non_blocking=True)
-            h_ef.copy_(state["ef"], non_blocking=True)
+        def upload(j):
+            st = sets[j][0]
+            st["ids"].copy_(h_ids, non_blocking=True)
+            st["overlay"].copy_(h_ov, non_blocking=True)
+            st["qkv"].copy_(h_qkv, non_blocking=True)
+            st["cur"].copy_(h_cur, non_blocking=True)
 
-        for _ in range(3):
-            e2e_step()
+        def readback(j):
+            st = sets[j][0]
+            h_out.copy_(st["outs"], non_blocking=True)
+            h_emb.copy_(st["emb"], non_blocking=True)
+            h_ef[j].copy_(st["ef"], non_blocking=True)
+
+        def run(n):
+            # step k uses set k % 2; its upload waits for frame k - 2 (same set) to end
+            with torch.cuda.stream(cp):
+                cp.wait_stream(s)
+                upload(0)
+                up[0].record(cp)
+            for k in range(n):
+                j = k % 2
+                s.wait_event(up[j])
+                sets[j][1].replay()
+                done[j].record(s)
+                with torch.cuda.stream(cp):
+                    if k + 1 < n:
+                        if k >= 1:
+                            cp.wait_event(done[1 - j])
+                        upload(1 - j)
+                        up[1 - j].record(cp)
+                    cp.wait_event(done[j])
+                    readback(j)
+            s.wait_stream(cp)
+
+        run(4)
         torch.cuda.synchronize()
         e2e_steps = max(10, args.steps)
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(s)
-        for _ in range(e2e_steps):
-            e2e_step()
+        run(e2e_steps)
         e1.record(s)
         torch.cuda.synchronize()
         t_e2e = e0.elapsed_time(e1) / 1e3
         h2d = sum(t.numel() * t.element_size() for t in (h_ids, h_ov, h_qkv, h_cur))
-        d2h = sum(t.numel() * t.element_size() for t in (h_out, h_emb, h_ef))
-        if int(h_ef.item()) != 0:
-            raise RuntimeError(f"device error flag {int(h_ef.item())}")
+        d2h = sum(t.numel() * t.element_size() for t in (h_out, h_emb, h_ef[0]))
+        if int(h_ef[0].item()) != 0 or int(h_ef[1].item()) != 0:
+            raise RuntimeError(f"device error flag {int(h_ef[0].item())} / {int(h_ef[1].item())}")
+        del state2, sets, g_frame2
         t_frame, t_layers, t_e2e = max_over_ranks([t_frame, t_layers, t_e2e], world, dev)
     else:
         t_frame, t_layers = max_over_ranks([t_frame, t_layers], world, dev)
