@@ -255,6 +255,24 @@ def timed_replays(g, steps, torch, stream=None):
     return e0.elapsed_time(e1) / 1e3
 
 
+def replay_percentiles(g, steps, torch, flush=None):
+    """Per-replay device times (CUDA events around each replay, after the timed region),
+    as {"p10", "p50", "p90"} in ms; the L2 flush, when given, runs before each replay."""
+    st = torch.cuda.current_stream()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    torch.cuda.synchronize()
+    for a, b in ev:
+        if flush is not None:
+            flush.fill_(1)
+        a.record(st)
+        g.replay()
+        b.record(st)
+    torch.cuda.synchronize()
+    ts = sorted(a.elapsed_time(b) for a, b in ev)
+    pick = lambda q: ts[min(len(ts) - 1, int(round(q * (len(ts) - 1))))]
+    return {"p10": round(pick(0.1), 5), "p50": round(pick(0.5), 5), "p90": round(pick(0.9), 5)}
+
+
 class CpuClock:
     """Wall time and the process's CPU time over a timed region of the oracle.  `cores` is
     CPU time / wall time rounded (at least 1): the host threads the oracle actually kept
@@ -468,7 +486,7 @@ def measure_frames(args, tts, W, w, cur_arg, cur_list, dev, rank, world, full):
     frame_bytes = embed + w.layers * per_layer
     L2 = l2_bytes(dev)
     flush = None
-    if w.layers * kv_layer < 2 * L2:  # working set would sit in L2: flush it per frame
+    if w.layers * kv_layer < 4 * L2:  # working set within reach of L2: flush it per frame
         flush = torch.empty(2 * L2, dtype=torch.uint8, device=dev)
 
     g_frame = capture(frame, torch)
@@ -498,6 +516,8 @@ def measure_frames(args, tts, W, w, cur_arg, cur_list, dev, rank, world, full):
     # the dominant kernel alone: the L fused decode-step launches of the same frame
     t_layers = timed_replays(g_layers, args.steps, torch)
     clk = clocks.stop()
+    # the spread of single frames (outside the timed region above)
+    spread = replay_percentiles(g_frame, max(args.steps, 10), torch, flush)
 
     t_e2e, e2e_steps, h2d, d2h = None, 0, 0, 0
     if full:
@@ -601,6 +621,7 @@ def measure_frames(args, tts, W, w, cur_arg, cur_list, dev, rank, world, full):
         "pct_of_hbm_peak": round(100 * value / world / peak, 2),
         "pct_of_nominal_hbm": round(100 * value / world / NOMINAL_HBM_GBS, 2),
         "frame_steps_per_s": round(world * w.B * args.steps / t_frame, 1),
+        "ms_per_frame_spread": spread,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
                      "kernel": "decode_attn_kernel<fused> (tts_decode_step)",
