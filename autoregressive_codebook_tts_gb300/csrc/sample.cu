@@ -80,11 +80,29 @@ __device__ __forceinline__ bool key_ahead(uint32_t ka, int ia, uint32_t kb, int 
 
 constexpr int kChunk = TTS_MAX_SAMPLE_VOCAB / kSampleThreads;  // indices per thread, at most
 
+// Inclusive sum of v over threads 0..tid of the block (kSampleThreads threads, all of
+// them calling); s_part holds kSampleWarps ints of scratch.
+__device__ __forceinline__ int block_inclusive_sum(int v, int* s_part) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int o = __shfl_up_sync(kFull, v, off);
+    if (lane >= off) v += o;
+  }
+  if (lane == 31) s_part[warp] = v;
+  __syncthreads();
+  int before = 0;
+#pragma unroll
+  for (int w = 0; w < kSampleWarps; ++w) before += w < warp ? s_part[w] : 0;
+  __syncthreads();  // s_part may be reused by the caller's next scan
+  return v + before;
+}
+
 __global__ void __launch_bounds__(kSampleThreads) sample_kernel(const SampleParams p) {
   extern __shared__ uint32_t s_key[];  // the row as keys
   __shared__ int s_hist[256];
   __shared__ int s_sel[2];             // chosen digit, keys still to take at the threshold
-  __shared__ int s_scan[kSampleThreads];
+  __shared__ int s_part[kSampleWarps];
   __shared__ int s_n;
   __shared__ uint32_t s_ck[TTS_MAX_TOP_K];
   __shared__ int s_ci[TTS_MAX_TOP_K];
@@ -153,19 +171,25 @@ __global__ void __launch_bounds__(kSampleThreads) sample_kernel(const SamplePara
   for (int shift = 24; shift >= 0; shift -= 8) {
     s_hist[tid] = 0;  // 256 threads, 256 bins
     __syncthreads();
-    for (int i = tid; i < V; i += kSampleThreads) {
-      const uint32_t key = s_key[i];
-      if ((key & mask) == prefix) atomicAdd(&s_hist[(key >> shift) & 255u], 1);
+    // keys that match the digits fixed so far, counted per next digit; lanes with the
+    // same digit add once (their count) instead of each contending for the bin
+    for (int base = 0; base < V; base += kSampleThreads) {
+      const int i = base + tid;
+      const uint32_t key = i < V ? s_key[i] : 0u;
+      const bool in = i < V && (key & mask) == prefix;
+      const uint32_t bin = (key >> shift) & 255u;
+      const unsigned peers = __match_any_sync(kFull, in ? bin : 0xFFFFFFFFu);
+      if (in && lane == __ffs(peers) - 1) atomicAdd(&s_hist[bin], __popc(peers));
     }
     __syncthreads();
-    if (tid == 0) {
-      int above = 0, d = 255;
-      for (; d > 0; --d) {
-        if (above + s_hist[d] >= need) break;
-        above += s_hist[d];
-      }
-      s_sel[0] = d;
-      s_sel[1] = need - above;
+    // the digit d with (keys in bins above d) < need <= (keys in bins from d up):
+    // thread t holds bin 255 - t, so its inclusive sum counts the bins from it upward
+    const int c = s_hist[255 - tid];
+    const int incl = block_inclusive_sum(c, s_part);
+    const int excl = incl - c;
+    if (excl < need && incl >= need) {
+      s_sel[0] = 255 - tid;
+      s_sel[1] = need - excl;
     }
     __syncthreads();
     prefix |= static_cast<uint32_t>(s_sel[0]) << shift;
@@ -180,16 +204,8 @@ __global__ void __launch_bounds__(kSampleThreads) sample_kernel(const SamplePara
   const int i1 = min(i0 + kChunk, V);
   int eq = 0;
   for (int i = i0; i < i1; ++i) eq += s_key[i] == prefix;
-  s_scan[tid] = eq;
   if (tid == 0) s_n = 0;
-  __syncthreads();
-  for (int off = 1; off < kSampleThreads; off <<= 1) {  // inclusive scan
-    const int v = tid >= off ? s_scan[tid - off] : 0;
-    __syncthreads();
-    s_scan[tid] += v;
-    __syncthreads();
-  }
-  int rank = s_scan[tid] - eq;  // equal keys at lower indices
+  int rank = block_inclusive_sum(eq, s_part) - eq;  // equal keys at lower indices
   for (int i = i0; i < i1; ++i) {
     const uint32_t key = s_key[i];
     bool take = key > prefix;
