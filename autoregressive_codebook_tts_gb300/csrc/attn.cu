@@ -1080,6 +1080,15 @@ decode_attn_kernel(const AttnParams p) {
         load_row_f32<VE, VEC, LPR>(
             p.q + static_cast<int64_t>(b) * p.q_stride + static_cast<int64_t>(g * G + h) * D, lr, q[h]);
     }
+    // head_dim 64 (short rows, registers to spare): the new K/V row's loads go out with
+    // q's, one round trip instead of two on a short window's critical path
+    constexpr bool kFreshEarly = (D == 64);
+    float kr[EPL], vr[EPL];
+    if (kFreshEarly && fresh_here) {
+      const int64_t roff = static_cast<int64_t>(b) * p.kv_new_stride + static_cast<int64_t>(g) * D;
+      load_row_f32<VE, VEC, LPR>(p.k_new + roff, lr, kr);
+      load_row_f32<VE, VEC, LPR>(p.v_new + roff, lr, vr);
+    }
     if (persistent) {
       // every value of the slot this warp needs is in registers: release the slot
       __syncwarp();
@@ -1112,10 +1121,11 @@ decode_attn_kernel(const AttnParams p) {
     // Every row group of the warp holds the row, so the score and the running maximum
     // are warp-uniform; its weight 2^0 = 1 and its V row are counted by row group 0.
     if (fresh_here) {
-      float kr[EPL], vr[EPL];
-      const int64_t roff = static_cast<int64_t>(b) * p.kv_new_stride + static_cast<int64_t>(g) * D;
-      load_row_f32<VE, VEC, LPR>(p.k_new + roff, lr, kr);
-      load_row_f32<VE, VEC, LPR>(p.v_new + roff, lr, vr);
+      if (!kFreshEarly) {
+        const int64_t roff = static_cast<int64_t>(b) * p.kv_new_stride + static_cast<int64_t>(g) * D;
+        load_row_f32<VE, VEC, LPR>(p.k_new + roff, lr, kr);
+        load_row_f32<VE, VEC, LPR>(p.v_new + roff, lr, vr);
+      }
       norm_rope_regs<VE, VEC, LPR>(kr, gk, csr, p.eps, lr, D);
       uint4 kp[VEC], vp[VEC];
 #pragma unroll
