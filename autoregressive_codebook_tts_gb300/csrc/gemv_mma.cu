@@ -1,4 +1,4 @@
-// Decode-layer GEMVs for 4 to 32 streams on the 5th-generation tensor cores (tcgen05):
+// Decode-layer GEMVs for 1 to 32 streams on the 5th-generation tensor cores (tcgen05):
 // y[b][n] = sum_k x[b][k] W[n][k] for B streams, bf16 weights and activations, f32
 // accumulation ("minicpm-o-4.5 ... optimizations.md", core table: fused residual add +
 // RMSNorm and SiLU-multiply around the projections, integer round-to-nearest-even).
