@@ -64,8 +64,14 @@ class PredictorFrames:
                         torch.zeros(B, n_kv_heads, capacity, D, device=device)) for _ in range(layers)]
         self.cs = torch.empty(capacity, D // 2, 2, device=device)
         tts.tts_rope_table(self.cs, capacity, D, rope_base)
+        # The enqueue order keeps TTS_KV_PREFETCH_BEFORE_WAIT's promise: the launch just
+        # before a decode step is the gather or another layer's step, neither of which
+        # writes this layer's cache; a layer's rows are written by its own step one
+        # sub-step earlier (or by the frame's prefill), launches that have completed by
+        # then, and the cur_len tensors are constants.  So the steps may start streaming
+        # their cache rows before the preceding launch ends.
         self.desc = tts.kv_desc(B, n_q_heads, n_kv_heads, D, capacity, "f32",
-                                window_quantum=capacity)
+                                window_quantum=capacity, flags=tts.TTS_KV_PREFETCH_BEFORE_WAIT)
         self.ws = tts.workspace(self.desc, 0, device=device)
         self.pws = tts.prefill_workspace(self.desc, 2, 0, device=device)
         self.codes = torch.zeros(slots, B, 16, dtype=torch.int32, device=device)
