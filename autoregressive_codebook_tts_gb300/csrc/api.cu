@@ -511,6 +511,44 @@ tts_status tts_sample(const float* logits, int64_t logits_stride, int32_t B, int
   return from_cuda(launch_sample(p, as_stream(stream)));
 }
 
+tts_status tts_sample_embed(const float* logits, int64_t logits_stride, int32_t B, int32_t vocab,
+                            int32_t top_k, float temperature, uint64_t seed, const uint64_t* counter,
+                            uint32_t draw, int32_t* out_ids, int64_t out_stride, const tts_tables* table,
+                            float* out_rows, void* stream) {
+  if (logits == nullptr || out_ids == nullptr || (top_k > 1 && counter == nullptr) || table == nullptr ||
+      out_rows == nullptr || table->tab[0] == nullptr)
+    return TTS_ERR_NULL;
+  if (B < 1 || B > 65535 || vocab < 1 || vocab > TTS_MAX_SAMPLE_VOCAB || logits_stride < vocab ||
+      out_stride < 1 || top_k < 0 || top_k > TTS_MAX_TOP_K || top_k > vocab)
+    return TTS_ERR_SHAPE;
+  if (top_k > 1 && !(temperature > 0.f && std::isfinite(temperature))) return TTS_ERR_SHAPE;
+  if (table->n_tables != 1 || table->vocab < vocab || table->hidden < 4 || table->hidden % 4 != 0)
+    return TTS_ERR_SHAPE;
+  if (table->dtype != TTS_F32 && table->dtype != TTS_BF16 && table->dtype != TTS_Q8_0) return TTS_ERR_DTYPE;
+  if (table->dtype == TTS_Q8_0 && table->hidden % 32 != 0) return TTS_ERR_SHAPE;
+  if ((reinterpret_cast<uintptr_t>(logits) & 3u) != 0 || (reinterpret_cast<uintptr_t>(out_ids) & 3u) != 0 ||
+      (counter != nullptr && (reinterpret_cast<uintptr_t>(counter) & 7u) != 0) || !aligned16(table->tab[0]) ||
+      !aligned16(out_rows))
+    return TTS_ERR_ALIGN;
+  SampleParams p = {};
+  p.logits = logits;
+  p.stride = logits_stride;
+  p.B = B;
+  p.V = vocab;
+  p.top_k = top_k;
+  p.c = top_k > 1 ? static_cast<float>(1.4426950408889634 / static_cast<double>(temperature)) : 0.f;
+  p.seed = seed;
+  p.counter = counter;
+  p.draw = draw;
+  p.out = out_ids;
+  p.out_stride = out_stride;
+  p.emb_tab = table->tab[0];
+  p.emb_dtype = table->dtype;
+  p.emb_hidden = table->hidden;
+  p.emb_out = out_rows;
+  return from_cuda(launch_sample(p, as_stream(stream)));
+}
+
 tts_status tts_counter_advance(uint64_t* counter, uint64_t by, void* stream) {
   if (counter == nullptr) return TTS_ERR_NULL;
   if ((reinterpret_cast<uintptr_t>(counter) & 7u) != 0) return TTS_ERR_ALIGN;

@@ -127,6 +127,11 @@ struct SampleParams {
   uint32_t draw;        // third counter word: the draw's index within one counter value
   int32_t* out;
   int64_t out_stride;   // int32 elements between consecutive streams' ids
+  // optional gather of the drawn token's table row (emb_out == nullptr: none)
+  const void* emb_tab;  // f32, bf16 or Q8_0 rows of emb_hidden entries
+  int emb_dtype;        // tts_dtype
+  int emb_hidden;
+  float* emb_out;       // f32 [B][emb_hidden]
 };
 
 // bf16-weight GEMV of the decode layer (see layer.cu): y[b][n] = sum_k x[b][k] W[n][k].

@@ -20,6 +20,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "table_rows.cuh"
 
 namespace tts {
 namespace {
@@ -98,6 +99,24 @@ __device__ __forceinline__ int block_inclusive_sum(int v, int* s_part) {
   return v + before;
 }
 
+// The drawn token's table row into emb_out[b] (the frame-input composition of one table
+// without an overlay: the row itself, entries widened or dequantised exactly).  Every
+// thread of the CTA calls this; `pick` is read after a barrier.
+template <typename TabT>
+__device__ __forceinline__ void gather_row_t(const SampleParams& p, int b, int id) {
+  const TabT* row = table_row<TabT>(p.emb_tab, id, p.emb_hidden);
+  float4* dst = reinterpret_cast<float4*>(p.emb_out + static_cast<int64_t>(b) * p.emb_hidden);
+  for (int c4 = threadIdx.x; c4 < p.emb_hidden / 4; c4 += kSampleThreads) dst[c4] = load_row4(row, c4);
+}
+__device__ __forceinline__ void gather_row(const SampleParams& p, int b, volatile int& pick) {
+  if (p.emb_out == nullptr) return;
+  __syncthreads();
+  const int id = pick;
+  if (p.emb_dtype == TTS_BF16) gather_row_t<__nv_bfloat16>(p, b, id);
+  else if (p.emb_dtype == TTS_Q8_0) gather_row_t<Q8Block>(p, b, id);
+  else gather_row_t<float>(p, b, id);
+}
+
 __global__ void __launch_bounds__(kSampleThreads) sample_kernel(const SampleParams p) {
   extern __shared__ uint32_t s_key[];  // the row as keys
   __shared__ int s_hist[256];
@@ -111,6 +130,7 @@ __global__ void __launch_bounds__(kSampleThreads) sample_kernel(const SamplePara
   __shared__ float s_w[TTS_MAX_TOP_K];
   __shared__ uint32_t s_wk[kSampleWarps];
   __shared__ int s_wi[kSampleWarps];
+  __shared__ int s_pick;
   grid_wait();
   grid_launch_dependents();
   const int b = blockIdx.x;
@@ -157,7 +177,9 @@ __global__ void __launch_bounds__(kSampleThreads) sample_kernel(const SamplePara
           bi = s_wi[w];
         }
       p.out[static_cast<int64_t>(b) * p.out_stride] = bi;
+      s_pick = bi;
     }
+    gather_row(p, b, s_pick);
     return;
   }
 
@@ -231,7 +253,7 @@ __global__ void __launch_bounds__(kSampleThreads) sample_kernel(const SamplePara
   const bool finite_top = m > -INFINITY && m < INFINITY;
   if (tid < k && finite_top) s_w[tid] = exp2_f32(__fmul_rn(__fsub_rn(key_float(s_sk[tid]), m), p.c));
   __syncthreads();
-  if (tid != 0) return;
+  if (tid == 0) {
   int pick = 0;
   if (finite_top) {
     float S = 0.0f;
@@ -251,6 +273,9 @@ __global__ void __launch_bounds__(kSampleThreads) sample_kernel(const SamplePara
     }
   }
   p.out[static_cast<int64_t>(b) * p.out_stride] = s_si[pick];
+  s_pick = s_si[pick];
+  }
+  gather_row(p, b, s_pick);
 }
 
 __global__ void counter_advance_kernel(uint64_t* counter, uint64_t by) {

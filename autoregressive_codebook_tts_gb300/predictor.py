@@ -16,8 +16,9 @@ replays several frames per graph launch.  One frame of B streams, in the order o
   * the sampler draws sub-code 15 from the last logits, and the counter advances.
 
 Everything here is argument marshalling: buffers are allocated once, and ``enqueue``
-only issues ``tts_frame_embed``, ``tts_prefill_step``, ``tts_sample``,
-``tts_decode_step`` and ``tts_counter_advance`` calls (plus one device copy of the
+only issues ``tts_frame_embed``, ``tts_prefill_step``, ``tts_sample_embed`` (the sampler
+with the gather of the drawn code), ``tts_sample``, ``tts_decode_step`` and
+``tts_counter_advance`` calls (plus one device copy of the
 prefill rows, which the prefill norms in place).  The QKV projection and the
 output heads sit outside this path, so the q/k/v rows of every (position, layer) and
 the logits of every sub-step are inputs.  Sampler draw j of a frame uses the Philox
@@ -84,7 +85,7 @@ class PredictorFrames:
         self.counter = torch.zeros(1, dtype=torch.int64, device=device)
         self.err = torch.zeros(1, dtype=torch.int32, device=device)
         self.scale = 1.0 / math.sqrt(D)
-        self.launches_per_frame = 1 + 2 * layers + 14 * (2 + layers) + 2
+        self.launches_per_frame = 1 + 2 * layers + 14 * (1 + layers) + 2
 
     def enqueue(self, k=0, stream=None):
         """One frame into slot k % slots, on `stream` (default: the current stream)."""
@@ -108,10 +109,10 @@ class PredictorFrames:
                                  stream=stream)
         for t in range(2, 16):
             j = t - 1
-            tts.tts_sample(self.logits[j - 1], self.top_k, self.temperature, self.seed,
-                           self.counter, codes[:, j], draw=j, stream=stream)
-            tts.tts_frame_embed(self.tabs[j], codes[:, j:j + 1], None, self.emb[s, j], ef,
-                                stream=stream)
+            # the sampler draws sub-code j and gathers its row of group table j (one launch)
+            tts.tts_sample_embed(self.logits[j - 1], self.top_k, self.temperature, self.seed,
+                                 self.counter, codes[:, j], self.tabs[j], self.emb[s, j], draw=j,
+                                 stream=stream)
             for l in range(L):
                 rows = self.qkv[t, l]
                 kc, vc = self.caches[l]

@@ -42,6 +42,7 @@ EXPORTED = [
     "tts_prefill_workspace_size",
     "tts_prefill_step",
     "tts_sample",
+    "tts_sample_embed",
     "tts_counter_advance",
     "tts_check_wait_timeout",
     "tts_decode_layer_scratch_size",
@@ -95,6 +96,8 @@ _sigs = {
     "tts_prefill_workspace_size": ([ctypes.POINTER(TtsKvDesc), _I32, _I32], _SZ),
     "tts_sample": ([_P, _I64, _I32, _I32, _I32, _F, ctypes.c_uint64, _P, ctypes.c_uint32, _P, _I64, _P],
                    _I32),
+    "tts_sample_embed": ([_P, _I64, _I32, _I32, _I32, _F, ctypes.c_uint64, _P, ctypes.c_uint32, _P, _I64,
+                          ctypes.POINTER(TtsTables), _P, _P], _I32),
     "tts_counter_advance": ([_P, ctypes.c_uint64, _P], _I32),
     "tts_check_wait_timeout": ([_P, _P], _I32),
     "tts_decode_layer_scratch_size": ([ctypes.POINTER(TtsKvDesc), _I32, _I32, _I32], _SZ),
@@ -313,6 +316,18 @@ def tts_sample(logits, top_k, temperature, seed, counter, out_ids, draw=0, strea
                            ctypes.c_uint64(int(seed) & ((1 << 64) - 1)), _ptr(counter),
                            ctypes.c_uint32(int(draw)), _ptr(out_ids), out_ids.stride(0),
                            _stream(stream)), "tts_sample")
+
+
+def tts_sample_embed(logits, top_k, temperature, seed, counter, out_ids, table, out_rows, draw=0,
+                     stream=None):
+    """tts_sample, then the drawn tokens' rows of one table into out_rows [B, hidden] f32,
+    in one launch; table: a TtsTables of one table or a list of one tensor."""
+    B, V = logits.shape
+    t = tables(table) if not isinstance(table, TtsTables) else table
+    _check(_lib.tts_sample_embed(_ptr(logits), logits.stride(0), B, V, int(top_k), float(temperature),
+                                 ctypes.c_uint64(int(seed) & ((1 << 64) - 1)), _ptr(counter),
+                                 ctypes.c_uint32(int(draw)), _ptr(out_ids), out_ids.stride(0),
+                                 ctypes.byref(t), _ptr(out_rows), _stream(stream)), "tts_sample_embed")
 
 
 def tts_counter_advance(counter, by=1, stream=None):

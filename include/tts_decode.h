@@ -353,6 +353,18 @@ tts_status tts_sample(const float* logits, int64_t logits_stride, int32_t B, int
                       int32_t top_k, float temperature, uint64_t seed, const uint64_t* counter,
                       uint32_t draw, int32_t* out_ids, int64_t out_stride, void* stream);
 
+/* The sampler and the gather of the drawn codes in one launch: exactly tts_sample(...)
+ * followed by tts_frame_embed(table, out_ids, out_stride, NULL, 0, out_rows, B, ...)
+ * with one table and no overlay, i.e. out_rows[b] (device f32 [B][table->hidden],
+ * dense) is the drawn token's row of table->tab[0], entries widened (bf16) or
+ * dequantised (Q8_0) exactly.  table->n_tables must be 1 and table->vocab >= vocab.
+ * ([P-pipeline]: the code predictor's in-graph sampler feeds the next sub-step's
+ * gather; one launch instead of two per sub-step.) */
+tts_status tts_sample_embed(const float* logits, int64_t logits_stride, int32_t B, int32_t vocab,
+                            int32_t top_k, float temperature, uint64_t seed, const uint64_t* counter,
+                            uint32_t draw, int32_t* out_ids, int64_t out_stride, const tts_tables* table,
+                            float* out_rows, void* stream);
+
 /* *counter += by, as one kernel on `stream` (graph-capturable). */
 tts_status tts_counter_advance(uint64_t* counter, uint64_t by, void* stream);
 

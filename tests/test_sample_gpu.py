@@ -6,6 +6,7 @@ import pytest
 import torch
 
 import oracle
+from autoregressive_codebook_tts_gb300 import workloads as W
 
 pytestmark = pytest.mark.gpu
 
@@ -96,3 +97,32 @@ def test_counter_advances_inside_a_replayed_graph(tts):
     assert int(counter.item()) == 4
     for r in range(4):
         assert np.array_equal(outs[r].cpu().numpy(), oracle.sample(lg.numpy(), 16, 0.8, seed, r)), r
+
+
+@pytest.mark.parametrize("dtype,top_k", [("f32", 50), ("bf16", 0), ("q8_0", 8), ("f32", 1)])
+def test_sample_embed_equals_sample_then_gather(tts, dtype, top_k):
+    """tts_sample_embed is tts_sample followed by the one-table gather of the drawn codes:
+    the same ids (also against the oracle) and the same row bytes."""
+    B, V, hidden, seed = 32, 2048, 1024, 99
+    lg = _logits(B, V, 11)
+    d_lg = lg.cuda()
+    if dtype == "q8_0":
+        tab = W.q8_0_tables(1, V, hidden, seed=12)[0].cuda()
+    else:
+        tab = W.tables(1, V, hidden, seed=12)[0]
+        tab = (tab.to(torch.bfloat16) if dtype == "bf16" else tab).cuda()
+    t = tts.tables([tab])
+    counter = torch.full((1,), 5, dtype=torch.int64, device="cuda")
+    ids_a = torch.full((B, 3), -1, dtype=torch.int32, device="cuda")
+    ids_b = torch.full((B, 3), -1, dtype=torch.int32, device="cuda")
+    rows_a = torch.full((B, hidden), float("nan"), device="cuda")
+    rows_b = torch.full((B, hidden), float("nan"), device="cuda")
+    ef = torch.zeros(1, dtype=torch.int32, device="cuda")
+    tts.tts_sample(d_lg, top_k, 0.9, seed, counter, ids_a[:, 1], draw=4)
+    tts.tts_frame_embed(t, ids_a[:, 1:2], None, rows_a, ef)
+    tts.tts_sample_embed(d_lg, top_k, 0.9, seed, counter, ids_b[:, 1], t, rows_b, draw=4)
+    torch.cuda.synchronize()
+    assert ef.item() == 0
+    assert torch.equal(ids_a, ids_b)
+    assert np.array_equal(ids_b[:, 1].cpu().numpy(), oracle.sample(lg.numpy(), top_k, 0.9, seed, 5, draw=4))
+    assert torch.equal(rows_a.view(torch.int32), rows_b.view(torch.int32))
