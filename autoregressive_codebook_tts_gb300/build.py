@@ -13,7 +13,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libttsdecode.so")
-SOURCES = ["attn.cu", "small_kernels.cu", "api.cu", "noalloc.cu", "sample.cu", "layer.cu", "gemv_mma.cu", "prefill_attn.cu"]
+SOURCES = ["attn.cu", "small_kernels.cu", "api.cu", "noalloc.cu", "sample.cu", "layer.cu", "gemv_mma.cu", "prefill_attn.cu", "prefill_attn_tc.cu"]
 HEADERS = ["common.cuh", "kernels.h", "table_rows.cuh"]
 ROOT = os.path.dirname(HERE)
 PUBLIC_HEADER = os.path.join(ROOT, "include", "tts_decode.h")

@@ -146,6 +146,12 @@ tts_status prepare_attn(const tts_kv_desc* d, const void* k_cache, const void* v
 
 // Prompts of kPrefillMinT rows or more take the multi-query kernel (query blocks share
 // every K/V tile); shorter ones run as B x T decode queries.
+// Query rows of a multi-query prefill item: 128 on the tensor cores (bf16, head_dim 128,
+// contiguous or pages of 64+ rows), else 64.
+int prefill_rows(const tts_kv_desc* d) {
+  return prefill_rows_per_item(d->kv_dtype == TTS_BF16, d->head_dim, d->paged, d->paged ? d->page_size : 1);
+}
+
 bool multi_query_prefill(const tts_kv_desc* d, int T) {
   const int64_t rows = d->paged ? static_cast<int64_t>(d->n_pages) * d->n_kv_heads * d->page_size
                                 : static_cast<int64_t>(d->B) * d->n_kv_heads * d->capacity;
@@ -371,7 +377,7 @@ size_t tts_prefill_workspace_size(const tts_kv_desc* d, int32_t T, int32_t n_spl
   if (multi_query_prefill(d, T)) {
     // the chunk results of the multi-query kernel (none with one chunk per item)
     const size_t w = prefill_attn_workspace(d->B, T, d->n_kv_heads, d->n_q_heads / d->n_kv_heads, d->head_dim,
-                                            d->capacity, n_splits, sm_count());
+                                            d->capacity, n_splits, sm_count(), prefill_rows(d));
     return w > 256 ? w : 256;
   }
   tts_kv_desc dq = *d;  // the B*T queries take the place of the streams
@@ -400,16 +406,17 @@ tts_status tts_prefill_step(float* q, const float* k, const float* v, int64_t ro
   if (mq) {
     if (k_cache == nullptr || v_cache == nullptr) return TTS_ERR_NULL;
     if (!aligned16(k_cache) || !aligned16(v_cache)) return TTS_ERR_ALIGN;
+    pp.rows = prefill_rows(d);
     prefill_attn_plan(d->B, T, d->n_kv_heads, d->n_q_heads / d->n_kv_heads, d->capacity, n_splits, sm_count(),
-                      pp.n_qb, pp.n_ch, pp.ch_len);
+                      pp.rows, pp.n_qb, pp.n_ch, pp.ch_len);
     if (pp.n_ch > 65535) return TTS_ERR_SHAPE;
     if (pp.n_ch > 1) {
       const size_t need = prefill_attn_workspace(d->B, T, d->n_kv_heads, d->n_q_heads / d->n_kv_heads, d->head_dim,
-                                                 d->capacity, n_splits, sm_count());
+                                                 d->capacity, n_splits, sm_count(), pp.rows);
       if (workspace == nullptr) return TTS_ERR_WORKSPACE;
       if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return TTS_ERR_ALIGN;
       if (ws_bytes < need) return TTS_ERR_WORKSPACE;
-      const size_t rows = static_cast<size_t>(d->B) * d->n_kv_heads * pp.n_qb * pp.n_ch * 64;
+      const size_t rows = static_cast<size_t>(d->B) * d->n_kv_heads * pp.n_qb * pp.n_ch * pp.rows;
       pp.part = static_cast<float*>(workspace);
       pp.ml = pp.part + rows * d->head_dim;
     }

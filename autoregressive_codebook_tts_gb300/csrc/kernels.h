@@ -194,13 +194,20 @@ struct PrefillAttnParams {
   float* part;                  // chunk rows [items][n_ch][64][D] (n_ch > 1)
   float* ml;                    // their (max, sum) [items][n_ch][64][2]
   int n_qb, n_ch, ch_len;       // query blocks per (stream, kv head), chunks per item, rows per chunk
+  int rows;                     // query rows of an item: 64 (CUDA cores) or 128 (tensor cores)
   int32_t* err;
 };
 bool prefill_attn_supported(int head_dim, int group, int paged, int page_size, int T);
-void prefill_attn_plan(int B, int T, int n_kv_heads, int group, int capacity, int n_splits, int n_sm, int& n_qb,
-                       int& n_ch, int& ch_len);
+// The tensor-core form (prefill_attn_tc.cu): bf16 caches, head_dim 128, contiguous or
+// pages of 64 rows or more; items of 128 query rows.
+bool prefill_attn_tc_supported(int kv_bf16, int head_dim, int paged, int page_size);
+int prefill_rows_per_item(int kv_bf16, int head_dim, int paged, int page_size);
+void prefill_attn_plan(int B, int T, int n_kv_heads, int group, int capacity, int n_splits, int n_sm, int rows,
+                       int& n_qb, int& n_ch, int& ch_len);
 size_t prefill_attn_workspace(int B, int T, int n_kv_heads, int group, int head_dim, int capacity, int n_splits,
-                              int n_sm);
+                              int n_sm, int rows);
+cudaError_t launch_prefill_attn_tc(const PrefillAttnParams& p, const void* k_cache, const void* v_cache, int group,
+                                   cudaStream_t s);
 cudaError_t launch_prefill_attn(const PrefillAttnParams& p, const void* k_cache, const void* v_cache, bool kv_bf16,
                                 int head_dim, int group, cudaStream_t s);
 

@@ -408,7 +408,7 @@ __global__ void __launch_bounds__(256) prefill_combine_kernel(const PrefillAttnP
   grid_wait();
   grid_launch_dependents();
   const int item = blockIdx.x;
-  const int QB = kRows / G;
+  const int QB = p.rows / G;
   const int qb = item % p.n_qb, bg = item / p.n_qb;
   const int g = bg % p.n_kv_heads, b = bg / p.n_kv_heads;
   const int t0 = qb * QB, nq = min(QB, p.T - t0);
@@ -420,17 +420,17 @@ __global__ void __launch_bounds__(256) prefill_combine_kernel(const PrefillAttnP
   if (e >= kCombineRows * D4) return;
   const int r = blockIdx.y * kCombineRows + e / D4, d4 = e % D4, tl = r / G, h = r - tl * G;
   if (tl >= nq) return;
-  const int64_t row0 = static_cast<int64_t>(item) * p.n_ch * kRows + r;
+  const int64_t row0 = static_cast<int64_t>(item) * p.n_ch * p.rows + r;
   const float2* ml = reinterpret_cast<const float2*>(p.ml) + row0;
   float M = -INFINITY;
 #pragma unroll 8
-  for (int c = 0; c < n_act; ++c) M = fmaxf(M, __ldcg(ml + c * kRows).x);
+  for (int c = 0; c < n_act; ++c) M = fmaxf(M, __ldcg(ml + c * p.rows).x);
   float L = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 4
   for (int c = 0; c < n_act; ++c) {
-    const int64_t row = row0 + c * kRows;
-    const float2 mlc = __ldcg(ml + c * kRows);
+    const int64_t row = row0 + c * p.rows;
+    const float2 mlc = __ldcg(ml + c * p.rows);
     const float4 x = __ldcg(reinterpret_cast<const float4*>(p.part + row * D) + d4);
     const float w = exp2f(mlc.x - M);
     L = fmaf(mlc.y, w, L);
@@ -512,6 +512,11 @@ cudaError_t launch_t(const PrefillAttnParams& p, const void* kc, const void* vc,
   return launch_pdl(prefill_combine_kernel, dim3(items, kRows / kCombineRows), dim3(256), 0, s, p, G, D);
 }
 
+cudaError_t launch_combine(const PrefillAttnParams& p, int G, int D, cudaStream_t s) {
+  const int items = p.B * p.n_kv_heads * p.n_qb;
+  return launch_pdl(prefill_combine_kernel, dim3(items, p.rows / kCombineRows), dim3(256), 0, s, p, G, D);
+}
+
 }  // namespace
 
 bool prefill_attn_supported(int head_dim, int group, int paged, int page_size, int T) {
@@ -519,9 +524,13 @@ bool prefill_attn_supported(int head_dim, int group, int paged, int page_size, i
          (!paged || page_size >= 8) && T >= kPrefillMinT;
 }
 
-void prefill_attn_plan(int B, int T, int n_kv_heads, int group, int capacity, int n_splits, int n_sm, int& n_qb,
-                       int& n_ch, int& ch_len) {
-  const int QB = kRows / group;
+int prefill_rows_per_item(int kv_bf16, int head_dim, int paged, int page_size) {
+  return prefill_attn_tc_supported(kv_bf16, head_dim, paged, page_size) ? 2 * kRows : kRows;
+}
+
+void prefill_attn_plan(int B, int T, int n_kv_heads, int group, int capacity, int n_splits, int n_sm, int rows,
+                       int& n_qb, int& n_ch, int& ch_len) {
+  const int QB = rows / group;
   n_qb = (T + QB - 1) / QB;
   const int items = B * n_kv_heads * n_qb;
   const int max_ch = (capacity + kTile - 1) / kTile;
@@ -535,16 +544,22 @@ void prefill_attn_plan(int B, int T, int n_kv_heads, int group, int capacity, in
 }
 
 size_t prefill_attn_workspace(int B, int T, int n_kv_heads, int group, int head_dim, int capacity, int n_splits,
-                              int n_sm) {
+                              int n_sm, int rows_per_item) {
   int n_qb, n_ch, ch_len;
-  prefill_attn_plan(B, T, n_kv_heads, group, capacity, n_splits, n_sm, n_qb, n_ch, ch_len);
+  prefill_attn_plan(B, T, n_kv_heads, group, capacity, n_splits, n_sm, rows_per_item, n_qb, n_ch, ch_len);
   if (n_ch == 1) return 0;
-  const size_t rows = static_cast<size_t>(B) * n_kv_heads * n_qb * n_ch * kRows;
+  const size_t rows = static_cast<size_t>(B) * n_kv_heads * n_qb * n_ch * rows_per_item;
   return rows * (static_cast<size_t>(head_dim) + 2) * sizeof(float);
 }
 
 cudaError_t launch_prefill_attn(const PrefillAttnParams& p, const void* k_cache, const void* v_cache, bool kv_bf16,
                                 int head_dim, int group, cudaStream_t s) {
+  if (p.rows == 2 * kRows) {
+    const cudaError_t e = launch_prefill_attn_tc(p, k_cache, v_cache, group, s);
+    if (e != cudaSuccess || p.n_ch == 1) return e;
+    return launch_combine(p, group, head_dim, s);
+  }
+  if (p.rows != kRows) return cudaErrorInvalidValue;
 #define TTS_PF_CASE(KT, DD, GG) \
   if (head_dim == DD && group == GG) return launch_t<KT, DD, GG>(p, k_cache, v_cache, s);
   if (kv_bf16) {

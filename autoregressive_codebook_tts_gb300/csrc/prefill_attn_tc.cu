@@ -1,0 +1,512 @@
+// Multi-query prefill attention on the 5th-generation tensor cores, for bf16 caches with
+// head_dim 128 ("qwentts.cpp -- src/pipeline-tts.h" commit page, KV-cache section: the
+// prefill writes the prompt's rows, query t of stream b sees positions
+// [0, start[b] + t + 1)).  A work item is 128 query rows (128 / G queries of a stream
+// times the G q heads of one kv head), the MMA's M; its window is cut into chunks, one
+// CTA per (item, chunk), merged by prefill_combine_kernel as for the CUDA-core kernel.
+//
+// Per 64-row tile of the chunk (N = 64 cache rows):
+//   S = Q_hi K^T + Q_lo K^T          two K-major bf16 products (K = D = 128), the query
+//                                    rows split once into a bf16 value and its bf16
+//                                    remainder, so S carries about 16 bits of q; K is
+//                                    exact in bf16;
+//   online softmax, one thread per query row reading its S row from tensor memory, in
+//   base 2 with the causal mask (the row's window end) and the chunk end; the running
+//   maximum is moved only when a row's maximum grows by more than 2^8, and then the
+//   row's O accumulator is rescaled in tensor memory (the result is the same: O and the
+//   row sum are both relative to the maximum in use);
+//   O += P_hi V + P_lo V             P split like q; V is the MN-major operand (stored
+//                                    [row][d]); K = 64 rows.
+// S has two tensor-memory buffers (the product of tile t+1 runs while tile t's softmax
+// does), O one (128 columns).  Warps 0-3 are the softmax warps (query row = TMEM lane),
+// warp 4 streams K and V tiles with 3-D tensor-map loads (one per tile and operand),
+// warp 5 allocates tensor memory and issues the products.  In the last tile, V rows past
+// the chunk are zeroed before their product (a cache tail may hold anything).
+// Every wait is bounded; on expiry TTS_EFLAG_TIMEOUT is set and the CTA winds down.
+#include <cstdint>
+#include <mutex>
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace tts {
+namespace {
+
+constexpr int kD = 128;
+constexpr int kM = 128;                   // query rows of an item
+constexpr int kN = 64;                    // cache rows of a tile
+constexpr int kNS = 3;                    // K/V ring stages
+constexpr int kThreads = 192;
+constexpr int kQBytes = kM * kD * 2;      // 32 KB: two 64-column swizzled chunks
+constexpr int kTileBytes = kN * kD * 2;   // 16 KB
+constexpr int kPBytes = kM * kN * 2;      // 16 KB: one 64-column swizzled chunk
+constexpr int kTmemCols = 256;            // S[2] (2 x 64) + O (128)
+
+// smem: Q_hi | Q_lo | ring (K | V) x kNS | P_hi | P_lo | barriers
+constexpr int kOffQh = 0, kOffQl = kQBytes, kOffRing = 2 * kQBytes;
+constexpr int kOffPh = kOffRing + kNS * 2 * kTileBytes, kOffPl = kOffPh + kPBytes;
+constexpr int kOffBar = kOffPl + kPBytes;
+constexpr size_t kSmem = 1024 + kOffBar + 32 * sizeof(uint64_t);
+
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  return static_cast<uint64_t>((addr & 0x3FFFF) >> 4) | (static_cast<uint64_t>((lbo >> 4) & 0x3FFF) << 16) |
+         (static_cast<uint64_t>((sbo >> 4) & 0x3FFF) << 32) | (static_cast<uint64_t>(1) << 46) |
+         (static_cast<uint64_t>(2) << 61);   // 128-byte swizzle
+}
+
+// Byte offset of bf16 element (r, col) of a tile of R rows stored as 64-column chunks of
+// 128-byte rows with the 128-byte swizzle (16-byte unit u of row r at (u ^ r % 8)).
+__device__ __forceinline__ uint32_t sw_off(int r, int col, int R) {
+  const int c = col >> 6, o = (col & 63) * 2;
+  return static_cast<uint32_t>(c * (R * 128) + r * 128 + ((((o >> 4) ^ (r & 7)) << 4) | (o & 15)));
+}
+
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int c1, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];"
+      ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(c1), "r"(0), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void mma_f16(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+      ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(acc) : "memory");
+}
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+               ::"r"(smem_u32(bar)) : "memory");
+}
+
+// 32 consecutive columns of this thread's TMEM lane (a row of its warp's 32 lanes).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};"
+      ::"r"(taddr), "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+        "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+        "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+        "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+        "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+        "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])),
+        "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])),
+        "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
+        "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
+        "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
+        "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+      : "memory");
+}
+
+__device__ __forceinline__ uint32_t bf16_bits(float x) {
+  const __nv_bfloat16 h = __float2bfloat16_rn(x);
+  return *reinterpret_cast<const uint16_t*>(&h);
+}
+// A row of 64 values as two bf16 rows: hi = bf16(x), lo = bf16(x - hi) (x - hi is exact).
+__device__ __forceinline__ void split_row64(const float* x, unsigned char* hi_row, unsigned char* lo_row, int r) {
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    uint32_t h[4], l[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float a = x[u * 8 + 2 * e], b = x[u * 8 + 2 * e + 1];
+      const uint32_t ha = bf16_bits(a), hb = bf16_bits(b);
+      h[e] = ha | (hb << 16);
+      const float ra = a - __uint_as_float(ha << 16), rb = b - __uint_as_float(hb << 16);
+      l[e] = bf16_bits(ra) | (bf16_bits(rb) << 16);
+    }
+    const uint32_t off = static_cast<uint32_t>(((u ^ (r & 7)) << 4));
+    *reinterpret_cast<uint4*>(hi_row + off) = make_uint4(h[0], h[1], h[2], h[3]);
+    *reinterpret_cast<uint4*>(lo_row + off) = make_uint4(l[0], l[1], l[2], l[3]);
+  }
+}
+
+
+template <int G>
+__global__ void __launch_bounds__(kThreads, 1) prefill_attn_tc_kernel(const __grid_constant__ CUtensorMap kmap,
+                                                                       const __grid_constant__ CUtensorMap vmap,
+                                                                       const PrefillAttnParams p) {
+  constexpr int QB = kM / G;   // queries of an item
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  unsigned char* sQh = smem + kOffQh;
+  unsigned char* sQl = smem + kOffQl;
+  unsigned char* ring = smem + kOffRing;
+  unsigned char* sPh = smem + kOffPh;
+  unsigned char* sPl = smem + kOffPl;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kOffBar);  // [kNS] K and V landed
+  uint64_t* empty = full + kNS;                                  // [kNS] the tile's products done
+  uint64_t* qready = empty + kNS;                                // the split query rows written
+  uint64_t* sready = qready + 1;                                 // [2] S(t) in tensor memory
+  uint64_t* sfree = sready + 2;                                  // [2] S(t) read by every row
+  uint64_t* pready = sfree + 2;                                  // P(t) written (and O rescaled)
+  uint64_t* pvdone = pready + 1;                                 // O += P(t) V(t) done
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(pvdone + 1);
+
+  const int item = blockIdx.x, ch = blockIdx.y;
+  const int qb = item % p.n_qb, bg = item / p.n_qb;
+  const int g = bg % p.n_kv_heads, b = bg / p.n_kv_heads;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int t0 = qb * QB;
+  const int nq = min(QB, p.T - t0);
+
+  if (tid == 0) {
+    for (int s = 0; s < kNS; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(qready, 128);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sready[i], 1);
+      mbar_init(&sfree[i], 128);
+    }
+    mbar_init(pready, 128);
+    mbar_init(pvdone, 1);
+    mbar_init_fence();
+  }
+  if (warp == 5) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                 ::"r"(smem_u32(s_tmem)), "n"(kTmemCols) : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *s_tmem;
+  const uint32_t tS[2] = {tmem, tmem + kN};
+  const uint32_t tO = tmem + 2 * kN;
+  grid_wait();   // the rows launch wrote the prompt's cache rows and rotated q rows
+  grid_launch_dependents();
+  const int st = __ldcg(p.start + b);
+  const int nv_max = min(max(st + t0 + nq, 1), p.capacity);
+  const int c0 = ch * p.ch_len;
+  const int c1 = min(c0 + p.ch_len, nv_max);
+  const int ntiles = c0 < nv_max ? (c1 - c0 + kN - 1) / kN : 0;
+
+  if (warp == 4) {
+    // ---------------------------------------------------------------- producer
+    if (lane == 0 && ntiles > 0) {
+      int issued = 0;
+      bool ok = true;
+      for (; issued < ntiles; ++issued) {
+        const int s = issued % kNS;
+        if (issued >= kNS && !mbar_wait(&empty[s], static_cast<uint32_t>((issued / kNS) - 1) & 1u)) {
+          ok = false;
+          break;
+        }
+        const int r0 = c0 + issued * kN;
+        int row;
+        if (!p.paged) {
+          row = (b * p.n_kv_heads + g) * p.capacity + r0;
+        } else {
+          // pages of 64 rows or more: the tile lies in one page
+          int page = __ldcg(p.block_table + static_cast<int64_t>(b) * p.bt_stride + r0 / p.page_size);
+          if (page < 0 || page >= p.n_pages) {
+            set_err(p.err, TTS_EFLAG_PAGE);
+            page = 0;
+          }
+          row = (page * p.n_kv_heads + g) * p.page_size + (r0 & (p.page_size - 1));
+        }
+        unsigned char* kd = ring + s * 2 * kTileBytes;
+        mbar_arrive_expect_tx(&full[s], 2 * kTileBytes);
+        tma_load_3d(kd, &kmap, row, &full[s]);
+        tma_load_3d(kd + kTileBytes, &vmap, row, &full[s]);
+      }
+      if (!ok) set_err(p.err, TTS_EFLAG_TIMEOUT);
+      for (int t = max(0, issued - kNS); t < issued; ++t)
+        mbar_wait(&full[t % kNS], static_cast<uint32_t>(t / kNS) & 1u);
+    }
+  } else if (warp == 5) {
+    // -------------------------------------------------------------- MMA issuer
+    if (lane == 0 && ntiles > 0) {
+      // kind::f16, f32 accumulator, bf16 A and B; S: N = 64, both K-major; O: N = 128,
+      // B (V) MN-major (bit 16)
+      const uint32_t idS = (1u << 4) | (1u << 7) | (1u << 10) | ((kN >> 3) << 17) | ((kM >> 4) << 24);
+      const uint32_t idO =
+          (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) | ((kD >> 3) << 17) | ((kM >> 4) << 24);
+      const uint32_t qh = smem_u32(sQh), ql = smem_u32(sQl), ph = smem_u32(sPh), pl = smem_u32(sPl);
+      auto issue_s = [&](int t) {
+        const uint32_t kb = smem_u32(ring + (t % kNS) * 2 * kTileBytes);
+        const uint32_t d = tS[t & 1];
+        // K = 128 in steps of 16: 64-column chunk j / 4, 32 bytes a step within it
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const uint32_t qo = (j >> 2) * (kM * 128) + (j & 3) * 32, ko = (j >> 2) * (kN * 128) + (j & 3) * 32;
+          mma_f16(d, smem_desc(qh + qo, 16, 1024), smem_desc(kb + ko, 16, 1024), idS, j > 0 ? 1u : 0u);
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const uint32_t qo = (j >> 2) * (kM * 128) + (j & 3) * 32, ko = (j >> 2) * (kN * 128) + (j & 3) * 32;
+          mma_f16(d, smem_desc(ql + qo, 16, 1024), smem_desc(kb + ko, 16, 1024), idS, 1u);
+        }
+        mma_commit(&sready[t & 1]);
+      };
+      auto issue_pv = [&](int t) {
+        const uint32_t vb = smem_u32(ring + (t % kNS) * 2 * kTileBytes + kTileBytes);
+        // K = 64 cache rows in steps of 16: P 32 bytes a step; V (MN-major) 16 rows =
+        // 2048 bytes a step, its 64-column chunks 8192 bytes apart
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          mma_f16(tO, smem_desc(ph + j * 32, 16, 1024), smem_desc(vb + j * 2048, 8192, 1024), idO,
+                  (t > 0 || j > 0) ? 1u : 0u);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          mma_f16(tO, smem_desc(pl + j * 32, 16, 1024), smem_desc(vb + j * 2048, 8192, 1024), idO, 1u);
+        mma_commit(&empty[t % kNS]);
+        mma_commit(pvdone);
+      };
+      bool ok = mbar_wait(qready, 0);
+      int t = 0;
+      for (; ok && t < ntiles; ++t) {
+        if (!mbar_wait(&full[t % kNS], static_cast<uint32_t>(t / kNS) & 1u)) ok = false;
+        if (ok && t >= 2 && !mbar_wait(&sfree[t & 1], static_cast<uint32_t>((t - 2) >> 1) & 1u)) ok = false;
+        if (!ok) break;
+        tc_fence_after();
+        issue_s(t);
+        if (t >= 1) {
+          if (!mbar_wait(pready, static_cast<uint32_t>(t - 1) & 1u)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          issue_pv(t - 1);
+        }
+      }
+      if (ok) {
+        if (mbar_wait(pready, static_cast<uint32_t>(ntiles - 1) & 1u)) {
+          tc_fence_after();
+          issue_pv(ntiles - 1);
+        } else {
+          ok = false;
+        }
+      }
+      if (!ok) set_err(p.err, TTS_EFLAG_TIMEOUT);
+    }
+  } else {
+    // ---------------------------------------------------------- softmax warps
+    const int r = tid, tl = r / G, h = r - tl * G;
+    const int raw = st + t0 + tl + 1;
+    const int nv = tl < nq ? min(max(raw, 1), p.capacity) : 0;
+    if (ch == 0 && g == 0 && h == 0 && tl < nq && (raw < 1 || raw > p.capacity)) set_err(p.err, TTS_EFLAG_NVALID);
+    // the query row, split into bf16 value and remainder, in the swizzled A layout
+    {
+      float x[kD];
+      const float4* src = reinterpret_cast<const float4*>(p.q + static_cast<int64_t>(b * p.T + t0 + tl) * p.q_stride +
+                                                          (g * G + h) * kD);
+#pragma unroll
+      for (int c = 0; c < kD / 4; ++c) {
+        const float4 v = tl < nq ? __ldcg(src + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+        x[4 * c] = v.x;
+        x[4 * c + 1] = v.y;
+        x[4 * c + 2] = v.z;
+        x[4 * c + 3] = v.w;
+      }
+      split_row64(x, sQh + r * 128, sQl + r * 128, r);
+      split_row64(x + 64, sQh + kM * 128 + r * 128, sQl + kM * 128 + r * 128, r);
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    mbar_arrive(qready);
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    float m_used = -INFINITY, l = 0.f;
+    bool ok = ntiles > 0;
+    for (int t = 0; ok && t < ntiles; ++t) {
+      // wait results are made warp-uniform: the tensor-memory loads below are
+      // warp-wide (.sync.aligned) and must be reached by all 32 lanes together
+      if (!__all_sync(kFull, mbar_wait(&sready[t & 1], static_cast<uint32_t>(t >> 1) & 1u))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      float sv[kN];
+      {
+        float a32[32];
+        tmem_ld32(tS[t & 1] + lane_base, a32);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) sv[j] = a32[j];
+        tmem_ld32(tS[t & 1] + lane_base + 32, a32);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) sv[32 + j] = a32[j];
+      }
+      tc_fence_before();
+      mbar_arrive(&sfree[t & 1]);
+      const int r0 = c0 + t * kN, nrow = min(kN, c1 - r0);
+      float mx = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < kN; ++j) {
+        sv[j] = (j < nrow && r0 + j < nv) ? sv[j] * p.scale_log2 : -INFINITY;
+        mx = fmaxf(mx, sv[j]);
+      }
+      // O and the P buffer are the product's until O += P(t-1) V(t-1) is done
+      if (t >= 1) {
+        if (!__all_sync(kFull, mbar_wait(pvdone, static_cast<uint32_t>(t - 1) & 1u))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+      }
+      // a row moves its maximum in use only when it grew by more than 2^8; rows whose
+      // O holds earlier tiles rescale it (every lane of the warp takes part in the
+      // tensor-memory round trip, a row that keeps its maximum with factor 1)
+      const bool move = mx > m_used + 8.0f;
+      const float alpha = (move && m_used > -INFINITY) ? exp2f(m_used - mx) : 1.0f;
+      if (__any_sync(kFull, move && m_used > -INFINITY)) {
+#pragma unroll
+        for (int c = 0; c < kD / 32; ++c) {
+          float o[32];
+          tmem_ld32(tO + lane_base + 32 * c, o);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] *= alpha;
+          tmem_st32(tO + lane_base + 32 * c, o);
+        }
+        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+      }
+      if (move) {
+        l *= alpha;
+        m_used = mx;
+      }
+      float sum = 0.f;
+#pragma unroll
+      for (int j = 0; j < kN; ++j) {
+        sv[j] = m_used == -INFINITY ? 0.f : exp2f(sv[j] - m_used);
+        sum += sv[j];
+      }
+      l += sum;
+      if (t == ntiles - 1 && nrow < kN) {
+        // V rows past the chunk take part in the product with weight 0: make them 0
+        unsigned char* vt = ring + (t % kNS) * 2 * kTileBytes + kTileBytes;
+        for (int idx = tid; idx < (kN - nrow) * 16; idx += 128) {
+          const int row = nrow + idx / 16, u = idx % 16;
+          *reinterpret_cast<uint4*>(vt + sw_off(row, u * 8, kN)) = make_uint4(0, 0, 0, 0);
+        }
+      }
+      split_row64(sv, sPh + r * 128, sPl + r * 128, r);
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      tc_fence_before();
+      mbar_arrive(pready);
+    }
+    if (!ok) {
+      if (ntiles > 0 && lane == 0) set_err(p.err, TTS_EFLAG_TIMEOUT);
+    } else if (__all_sync(kFull, mbar_wait(pvdone, static_cast<uint32_t>(ntiles - 1) & 1u))) {
+      tc_fence_after();
+      const int64_t orow = p.n_ch == 1 ? static_cast<int64_t>(b * p.T + t0 + tl) * p.n_q_heads + g * G + h
+                                       : (static_cast<int64_t>(item) * p.n_ch + ch) * kM + r;
+      float* dst = (p.n_ch == 1 ? p.out : p.part) + orow * kD;
+      const float inv = p.n_ch == 1 ? (l > 0.f ? 1.f / l : 0.f) : 1.f;
+      // every lane reads (warp-wide loads); rows past the prompt store nothing
+#pragma unroll
+      for (int c = 0; c < kD / 32; ++c) {
+        float o[32];
+        tmem_ld32(tO + lane_base + 32 * c, o);
+        if (tl < nq)
+#pragma unroll
+          for (int e = 0; e < 32; e += 4)
+            *reinterpret_cast<float4*>(dst + 32 * c + e) =
+                make_float4(o[e] * inv, o[e + 1] * inv, o[e + 2] * inv, o[e + 3] * inv);
+      }
+      if (tl < nq && p.n_ch > 1) reinterpret_cast<float2*>(p.ml)[orow] = make_float2(m_used, l);
+    } else if (lane == 0) {
+      set_err(p.err, TTS_EFLAG_TIMEOUT);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(kTmemCols) : "memory");
+  }
+}
+
+
+PFN_cuTensorMapEncodeTiled_v12000 tc_encoder() {
+  static std::mutex mtx;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::lock_guard<std::mutex> lock(mtx);
+  if (fn == nullptr) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    else
+      cudaGetLastError();
+  }
+  return fn;
+}
+
+template <int G>
+cudaError_t launch_tc_t(const PrefillAttnParams& p, const void* kc, const void* vc, cudaStream_t s) {
+  auto kern = prefill_attn_tc_kernel<G>;
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tc_encoder();
+  if (enc == nullptr) return cudaErrorNotSupported;
+  // the cache as [2 chunks of 64 columns][rows][64 bf16], a box of 64 rows (a whole tile)
+  const uint64_t rows = p.paged ? static_cast<uint64_t>(p.n_pages) * p.n_kv_heads * p.page_size
+                                : static_cast<uint64_t>(p.B) * p.n_kv_heads * p.capacity;
+  cuuint64_t dims[3] = {64, rows, kD / 64};
+  cuuint64_t strides[2] = {kD * 2, 128};
+  cuuint32_t box[3] = {64, kN, kD / 64};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUtensorMap kmap, vmap;
+  if (enc(&kmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(kc), dims, strides, box, estr,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS ||
+      enc(&vmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(vc), dims, strides, box, estr,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+  static std::mutex mtx;
+  static bool configured[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  {
+    std::lock_guard<std::mutex> lock(mtx);
+    if (!configured[dev]) {
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmem));
+      if (e != cudaSuccess) return e;
+      configured[dev] = true;
+    }
+  }
+  const int items = p.B * p.n_kv_heads * p.n_qb;
+  return launch_pdl(kern, dim3(items, p.n_ch), dim3(kThreads), kSmem, s, kmap, vmap, p);
+}
+
+}  // namespace
+
+bool prefill_attn_tc_supported(int kv_bf16, int head_dim, int paged, int page_size) {
+  return kv_bf16 && head_dim == kD && (!paged || page_size >= kN);
+}
+
+cudaError_t launch_prefill_attn_tc(const PrefillAttnParams& p, const void* k_cache, const void* v_cache, int group,
+                                   cudaStream_t s) {
+  if (p.rows != kM) return cudaErrorInvalidValue;
+  if (group == 1) return launch_tc_t<1>(p, k_cache, v_cache, s);
+  if (group == 2) return launch_tc_t<2>(p, k_cache, v_cache, s);
+  if (group == 4) return launch_tc_t<4>(p, k_cache, v_cache, s);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace tts

@@ -48,6 +48,7 @@ def parse():
                     help="layers per frame (0 = the workload's own; fewer only for small profiling cases)")
     ap.add_argument("--prefill-t", type=int, default=128, help="prefill: prompt positions per stream")
     ap.add_argument("--prefill-start", type=int, default=0, help="prefill: first prompt position")
+    ap.add_argument("--prefill-kv", default="f32", choices=["f32", "bf16"], help="prefill: cache element type")
     ap.add_argument("--cur-len", type=int, default=4095)
     ap.add_argument("--n-splits", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -702,7 +703,7 @@ def run_prefill(args, rank, world):
     local = int(os.environ.get("LOCAL_RANK", "0"))
     dev = torch.device(f"cuda:{local}")
     torch.cuda.set_device(dev)
-    w = W.workload("talker")
+    w = W.workload("talker", kv_dtype=args.prefill_kv)
     T, start = args.prefill_t, args.prefill_start
     B, L, Hq, Hkv, D = w.B, w.layers, w.n_q_heads, w.n_kv_heads, w.head_dim
     if start < 0 or start + T > w.capacity:
@@ -714,8 +715,9 @@ def run_prefill(args, rank, world):
     gq = torch.rand(L, D, generator=g, device=dev) + 0.5
     gk = torch.rand(L, D, generator=g, device=dev) + 0.5
     caches = []
+    kv_t = torch.float32 if w.kv_dtype == "f32" else torch.bfloat16
     for _ in range(L):
-        K = torch.empty(B, Hkv, w.capacity, D, device=dev)
+        K = torch.empty(B, Hkv, w.capacity, D, device=dev, dtype=kv_t)
         V = torch.empty_like(K)
         K.normal_(generator=g)
         V.normal_(generator=g)
@@ -755,10 +757,11 @@ def run_prefill(args, rank, world):
     # bytes a layer must move through HBM at least: the prompt's q/k/v rows read, q
     # written back, its k/v rows written to the cache, the earlier cache rows read once,
     # the output written
-    hbm = B * (T * (qd + 2 * kd) * 4 + T * qd * 4 + T * 2 * kd * 4 + start * 2 * kd * 4 + T * qd * 4)
+    e = w.elem_bytes
+    hbm = B * (T * (qd + 2 * kd) * 4 + T * qd * 4 + T * 2 * kd * e + start * 2 * kd * e + T * qd * 4)
     # K/V rows the queries read (the prompt's own rows come back from L2)
     attn_rows = B * sum(start + i + 1 for i in range(T))
-    attn_bytes = attn_rows * 2 * kd * 4
+    attn_bytes = attn_rows * 2 * kd * e
     peak, peak_kind = hbm_peak()
     t_layer = t / (args.steps * L)
     achieved = hbm / t_layer / 1e9
@@ -767,10 +770,11 @@ def run_prefill(args, rank, world):
         "metric": "prefill: prompt positions per second (B streams, all 28 layers)",
         "value": round(value, 1), "unit": "positions/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(t / args.steps * 1e3, 5),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32" if w.kv_dtype == "f32" else "bf16-kv/f32",
         "data": "synthetic (seeded, device-generated; random-init, no weights)",
         "config": {"workload": f"prefill: talker shapes, B={B}, {T} prompt positions from {start}, "
-                               f"28 layers, f32 KV, capacity {w.capacity}",
+                               f"28 layers, {w.kv_dtype} KV, capacity {w.capacity}",
                    "frame_step": "graph replay of 28 x tts_prefill_step",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "us_per_layer": round(t_layer * 1e6, 3),
