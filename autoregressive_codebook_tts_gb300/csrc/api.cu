@@ -408,7 +408,7 @@ tts_status tts_prefill_step(float* q, const float* k, const float* v, int64_t ro
     if (!aligned16(k_cache) || !aligned16(v_cache)) return TTS_ERR_ALIGN;
     pp.rows = prefill_rows(d);
     prefill_attn_plan(d->B, T, d->n_kv_heads, d->n_q_heads / d->n_kv_heads, d->capacity, n_splits, sm_count(),
-                      pp.rows, pp.n_qb, pp.n_ch, pp.ch_len);
+                      pp.rows, pp.n_qb, pp.n_ch);
     if (pp.n_ch > 65535) return TTS_ERR_SHAPE;
     if (pp.n_ch > 1) {
       const size_t need = prefill_attn_workspace(d->B, T, d->n_kv_heads, d->n_q_heads / d->n_kv_heads, d->head_dim,

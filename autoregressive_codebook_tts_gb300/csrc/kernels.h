@@ -182,6 +182,15 @@ cudaError_t launch_gemv_mma(const GemvParams& p, int x_mode, int epilogue, void*
 // Query row (b, t, h) reads q at q + (b * T + t) * q_stride + h * D (already normed and
 // rotated) and sees cache rows [0, min(max(start[b] + t + 1, 1), capacity)).
 constexpr int kPrefillMinT = 8;   // shorter prompts take the per-query decode path
+constexpr int kPrefillTile = 64;  // cache rows of a K/V tile (both prefill kernels)
+// Rows of each of an item's n_ch chunks: its window [0, nv_max) cut into n_ch parts of
+// whole tiles (the last ones may be short or empty).  The window is known only on the
+// device (start[] is a device array), so the attention and combine kernels both derive
+// the cut from it, the same way.
+__host__ __device__ inline int prefill_chunk_len(int nv_max, int n_ch) {
+  const int per = (nv_max + n_ch - 1) / n_ch;
+  return (per + kPrefillTile - 1) / kPrefillTile * kPrefillTile;
+}
 struct PrefillAttnParams {
   const float* q;
   int64_t q_stride;
@@ -191,9 +200,9 @@ struct PrefillAttnParams {
   const int32_t* block_table;
   float scale_log2;             // scale * log2(e)
   float* out;                   // [B][T][Hq][D]
-  float* part;                  // chunk rows [items][n_ch][64][D] (n_ch > 1)
-  float* ml;                    // their (max, sum) [items][n_ch][64][2]
-  int n_qb, n_ch, ch_len;       // query blocks per (stream, kv head), chunks per item, rows per chunk
+  float* part;                  // chunk rows [items][n_ch][rows][D] (n_ch > 1)
+  float* ml;                    // their (max, sum) [items][n_ch][rows][2]
+  int n_qb, n_ch;               // query blocks per (stream, kv head), chunks per item
   int rows;                     // query rows of an item: 64 (CUDA cores) or 128 (tensor cores)
   int32_t* err;
 };
@@ -203,7 +212,7 @@ bool prefill_attn_supported(int head_dim, int group, int paged, int page_size, i
 bool prefill_attn_tc_supported(int kv_bf16, int head_dim, int paged, int page_size);
 int prefill_rows_per_item(int kv_bf16, int head_dim, int paged, int page_size);
 void prefill_attn_plan(int B, int T, int n_kv_heads, int group, int capacity, int n_splits, int n_sm, int rows,
-                       int& n_qb, int& n_ch, int& ch_len);
+                       int& n_qb, int& n_ch);
 size_t prefill_attn_workspace(int B, int T, int n_kv_heads, int group, int head_dim, int capacity, int n_splits,
                               int n_sm, int rows);
 cudaError_t launch_prefill_attn_tc(const PrefillAttnParams& p, const void* k_cache, const void* v_cache, int group,

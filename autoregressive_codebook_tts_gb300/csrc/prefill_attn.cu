@@ -6,8 +6,8 @@
 //
 //   * work item = (stream b, kv head g, block of QB = 64 / G queries), i.e. 64 query
 //     rows (query t_local, q head h of the group, row t_local * G + h); its window
-//     [0, start + t_last + 1) is cut into chunks of ch_len rows, one CTA per (chunk,
-//     item);
+//     [0, start + t_last + 1) is cut on the device into n_ch chunks of whole tiles
+//     (prefill_chunk_len), one CTA per (chunk, item);
 //   * warp 8 (one lane) streams the chunk's 64-row K and V tiles into a 2-stage ring
 //     with 3-D tensor-map loads in the 128-byte swizzled layout (f32: boxes of 32
 //     floats x rows x D/32; bf16: 64 x rows x D/64), one load per tile and operand
@@ -223,9 +223,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_attn_kernel(const __grid_
   const int st = __ldcg(p.start + b);
   // the item's window ends with its last query's: [0, start + t0 + nq)
   const int nv_max = min(max(st + t0 + nq, 1), p.capacity);
-  const int c0 = ch * p.ch_len;
+  const int ch_len = prefill_chunk_len(nv_max, p.n_ch);
+  const int c0 = ch * ch_len;
   if (c0 >= nv_max) return;   // the chunk holds no row of any window of the item
-  const int c1 = min(c0 + p.ch_len, nv_max);
+  const int c1 = min(c0 + ch_len, nv_max);
   const int ntiles = (c1 - c0 + kTile - 1) / kTile;
   const int br = p.paged ? min(kTile, p.page_size) : kTile;
   const int br_shift = 31 - __clz(br);
@@ -414,7 +415,8 @@ __global__ void __launch_bounds__(256) prefill_combine_kernel(const PrefillAttnP
   const int t0 = qb * QB, nq = min(QB, p.T - t0);
   const int st = __ldcg(p.start + b);
   const int nv_max = min(max(st + t0 + nq, 1), p.capacity);
-  const int n_act = min(min(p.n_ch, kMaxCombineChunks), (nv_max + p.ch_len - 1) / p.ch_len);
+  const int ch_len = prefill_chunk_len(nv_max, p.n_ch);
+  const int n_act = min(min(p.n_ch, kMaxCombineChunks), (nv_max + ch_len - 1) / ch_len);
   const int D4 = D / 4;
   const int e = threadIdx.x;
   if (e >= kCombineRows * D4) return;
@@ -529,24 +531,24 @@ int prefill_rows_per_item(int kv_bf16, int head_dim, int paged, int page_size) {
 }
 
 void prefill_attn_plan(int B, int T, int n_kv_heads, int group, int capacity, int n_splits, int n_sm, int rows,
-                       int& n_qb, int& n_ch, int& ch_len) {
+                       int& n_qb, int& n_ch) {
   const int QB = rows / group;
   n_qb = (T + QB - 1) / QB;
   const int items = B * n_kv_heads * n_qb;
+  // Both kernels hold one CTA per SM: by default as many chunks as fill one wave.  Each
+  // item's window is cut into that many parts on the device (prefill_chunk_len).
+  int c = n_splits > 0 ? n_splits : n_sm / items;
   const int max_ch = (capacity + kTile - 1) / kTile;
-  int c = n_splits > 0 ? n_splits : (4 * n_sm + items - 1) / items;
-  if (n_splits <= 0 && c > (capacity + 4 * kTile - 1) / (4 * kTile)) c = (capacity + 4 * kTile - 1) / (4 * kTile);
   if (c > max_ch) c = max_ch;
   if (c > kMaxCombineChunks) c = kMaxCombineChunks;
   if (c < 1) c = 1;
-  ch_len = ((capacity + c - 1) / c + kTile - 1) / kTile * kTile;
-  n_ch = (capacity + ch_len - 1) / ch_len;
+  n_ch = c;
 }
 
 size_t prefill_attn_workspace(int B, int T, int n_kv_heads, int group, int head_dim, int capacity, int n_splits,
                               int n_sm, int rows_per_item) {
-  int n_qb, n_ch, ch_len;
-  prefill_attn_plan(B, T, n_kv_heads, group, capacity, n_splits, n_sm, rows_per_item, n_qb, n_ch, ch_len);
+  int n_qb, n_ch;
+  prefill_attn_plan(B, T, n_kv_heads, group, capacity, n_splits, n_sm, rows_per_item, n_qb, n_ch);
   if (n_ch == 1) return 0;
   const size_t rows = static_cast<size_t>(B) * n_kv_heads * n_qb * n_ch * rows_per_item;
   return rows * (static_cast<size_t>(head_dim) + 2) * sizeof(float);

@@ -2,26 +2,30 @@
 // head_dim 128 ("qwentts.cpp -- src/pipeline-tts.h" commit page, KV-cache section: the
 // prefill writes the prompt's rows, query t of stream b sees positions
 // [0, start[b] + t + 1)).  A work item is 128 query rows (128 / G queries of a stream
-// times the G q heads of one kv head), the MMA's M; its window is cut into chunks, one
-// CTA per (item, chunk), merged by prefill_combine_kernel as for the CUDA-core kernel.
+// times the G q heads of one kv head), the MMA's M; its window is cut on the device into
+// n_ch chunks of whole tiles, one CTA per (item, chunk), merged by
+// prefill_combine_kernel as for the CUDA-core kernel.
 //
 // Per 64-row tile of the chunk (N = 64 cache rows):
 //   S = Q_hi K^T + Q_lo K^T          two K-major bf16 products (K = D = 128), the query
 //                                    rows split once into a bf16 value and its bf16
 //                                    remainder, so S carries about 16 bits of q; K is
 //                                    exact in bf16;
-//   online softmax, one thread per query row reading its S row from tensor memory, in
-//   base 2 with the causal mask (the row's window end) and the chunk end; the running
-//   maximum is moved only when a row's maximum grows by more than 2^8, and then the
-//   row's O accumulator is rescaled in tensor memory (the result is the same: O and the
-//   row sum are both relative to the maximum in use);
+//   online softmax in base 2 with the causal mask (the row's window end) and the chunk
+//   end.  Two warpgroups share the work: query row r is TMEM lane r for both, the first
+//   takes score columns 0-31 (and O columns 0-63), the second 32-63 (O 64-127); they
+//   agree on the row maximum through shared memory at one named barrier a tile, whose
+//   AND-reduction also makes every bounded wait's outcome common to both.  The running
+//   maximum moves only when a row's maximum grows by more than 2^8, and then O is
+//   rescaled in tensor memory (the result is the same: O and the row sum are both
+//   relative to the maximum in use);
 //   O += P_hi V + P_lo V             P split like q; V is the MN-major operand (stored
 //                                    [row][d]); K = 64 rows.
 // S has two tensor-memory buffers (the product of tile t+1 runs while tile t's softmax
-// does), O one (128 columns).  Warps 0-3 are the softmax warps (query row = TMEM lane),
-// warp 4 streams K and V tiles with 3-D tensor-map loads (one per tile and operand),
-// warp 5 allocates tensor memory and issues the products.  In the last tile, V rows past
-// the chunk are zeroed before their product (a cache tail may hold anything).
+// does), O one (128 columns).  Warps 0-7 are the softmax warps, warp 8 streams K and V
+// tiles with 3-D tensor-map loads (one per tile and operand), warp 9 allocates tensor
+// memory and issues the products.  In the last tile, V rows past the chunk are zeroed
+// before their product (a cache tail may hold anything).
 // Every wait is bounded; on expiry TTS_EFLAG_TIMEOUT is set and the CTA winds down.
 #include <cstdint>
 #include <mutex>
@@ -39,18 +43,22 @@ namespace {
 
 constexpr int kD = 128;
 constexpr int kM = 128;                   // query rows of an item
-constexpr int kN = 64;                    // cache rows of a tile
+constexpr int kN = kPrefillTile;          // cache rows of a tile (64)
 constexpr int kNS = 3;                    // K/V ring stages
-constexpr int kThreads = 192;
+constexpr int kSmxWarps = 8;              // two softmax warpgroups
+constexpr int kProducerWarp = 8, kMmaWarp = 9;
+constexpr int kThreads = 320;
 constexpr int kQBytes = kM * kD * 2;      // 32 KB: two 64-column swizzled chunks
 constexpr int kTileBytes = kN * kD * 2;   // 16 KB
 constexpr int kPBytes = kM * kN * 2;      // 16 KB: one 64-column swizzled chunk
 constexpr int kTmemCols = 256;            // S[2] (2 x 64) + O (128)
 
-// smem: Q_hi | Q_lo | ring (K | V) x kNS | P_hi | P_lo | barriers
+// smem: Q_hi | Q_lo | ring (K | V) x kNS | P_hi | P_lo | row maxima [2][2][128] |
+// row sums [2][128] | barriers
 constexpr int kOffQh = 0, kOffQl = kQBytes, kOffRing = 2 * kQBytes;
 constexpr int kOffPh = kOffRing + kNS * 2 * kTileBytes, kOffPl = kOffPh + kPBytes;
-constexpr int kOffBar = kOffPl + kPBytes;
+constexpr int kOffMax = kOffPl + kPBytes, kOffSum = kOffMax + 2 * 2 * kM * 4;
+constexpr int kOffBar = kOffSum + 2 * kM * 4;
 constexpr size_t kSmem = 1024 + kOffBar + 32 * sizeof(uint64_t);
 
 __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
@@ -121,29 +129,44 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) 
       : "memory");
 }
 
-__device__ __forceinline__ uint32_t bf16_bits(float x) {
-  const __nv_bfloat16 h = __float2bfloat16_rn(x);
-  return *reinterpret_cast<const uint16_t*>(&h);
-}
-// A row of 64 values as two bf16 rows: hi = bf16(x), lo = bf16(x - hi) (x - hi is exact).
-__device__ __forceinline__ void split_row64(const float* x, unsigned char* hi_row, unsigned char* lo_row, int r) {
+// Eight values (x[0..7]) as one 16-byte unit of bf16 values (hi = bf16(x)) and one of
+// their bf16 remainders (lo = bf16(x - hi); x - hi is exact, so the fused negate-add
+// computes it without rounding), stored at the swizzled unit position of row r.
+__device__ __forceinline__ void split_unit(const float* x, unsigned char* hi_row, unsigned char* lo_row, int u,
+                                           int r) {
+  uint32_t h[4], l[4];
 #pragma unroll
-  for (int u = 0; u < 8; ++u) {
-    uint32_t h[4], l[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const float a = x[u * 8 + 2 * e], b = x[u * 8 + 2 * e + 1];
-      const uint32_t ha = bf16_bits(a), hb = bf16_bits(b);
-      h[e] = ha | (hb << 16);
-      const float ra = a - __uint_as_float(ha << 16), rb = b - __uint_as_float(hb << 16);
-      l[e] = bf16_bits(ra) | (bf16_bits(rb) << 16);
-    }
-    const uint32_t off = static_cast<uint32_t>(((u ^ (r & 7)) << 4));
-    *reinterpret_cast<uint4*>(hi_row + off) = make_uint4(h[0], h[1], h[2], h[3]);
-    *reinterpret_cast<uint4*>(lo_row + off) = make_uint4(l[0], l[1], l[2], l[3]);
+  for (int e = 0; e < 4; ++e) {
+    const __nv_bfloat162 hb = __floats2bfloat162_rn(x[2 * e], x[2 * e + 1]);
+    h[e] = *reinterpret_cast<const uint32_t*>(&hb);
+    const float2 hf = make_float2(__uint_as_float(h[e] << 16), __uint_as_float(h[e] & 0xFFFF0000u));
+    const float2 rem = __ffma2_rn(hf, make_float2(-1.f, -1.f), make_float2(x[2 * e], x[2 * e + 1]));
+    const __nv_bfloat162 lb = __floats2bfloat162_rn(rem.x, rem.y);
+    l[e] = *reinterpret_cast<const uint32_t*>(&lb);
   }
+  const uint32_t off = static_cast<uint32_t>((u ^ (r & 7)) << 4);
+  *reinterpret_cast<uint4*>(hi_row + off) = make_uint4(h[0], h[1], h[2], h[3]);
+  *reinterpret_cast<uint4*>(lo_row + off) = make_uint4(l[0], l[1], l[2], l[3]);
 }
 
+// Named barrier 1 over the 256 softmax threads, returning the AND of every thread's v
+// (warp-convergent: each warp reaches it with all lanes).
+__device__ __forceinline__ bool softmax_sync_and(bool v) {
+  uint32_t out;
+  asm volatile(
+      "{\n\t.reg .pred pi, po;\n\tsetp.ne.u32 pi, %1, 0;\n\t"
+      "bar.red.and.pred po, 1, 256, pi;\n\tselp.u32 %0, 1, 0, po;\n\t}"
+      : "=r"(out) : "r"(static_cast<uint32_t>(v)) : "memory");
+  return out != 0;
+}
+
+// 2^x with the MUFU instruction (relative error about 2^-22; 2^-inf = 0, results below
+// 2^-126 flush to 0, far below what a softmax weight can contribute).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 
 template <int G>
 __global__ void __launch_bounds__(kThreads, 1) prefill_attn_tc_kernel(const __grid_constant__ CUtensorMap kmap,
@@ -157,11 +180,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_attn_tc_kernel(const __gr
   unsigned char* ring = smem + kOffRing;
   unsigned char* sPh = smem + kOffPh;
   unsigned char* sPl = smem + kOffPl;
+  float* s_max = reinterpret_cast<float*>(smem + kOffMax);       // [tile parity][half][row]
+  float* s_sum = reinterpret_cast<float*>(smem + kOffSum);       // [half][row]
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kOffBar);  // [kNS] K and V landed
   uint64_t* empty = full + kNS;                                  // [kNS] the tile's products done
   uint64_t* qready = empty + kNS;                                // the split query rows written
   uint64_t* sready = qready + 1;                                 // [2] S(t) in tensor memory
-  uint64_t* sfree = sready + 2;                                  // [2] S(t) read by every row
+  uint64_t* sfree = sready + 2;                                  // [2] S(t) read by every thread
   uint64_t* pready = sfree + 2;                                  // P(t) written (and O rescaled)
   uint64_t* pvdone = pready + 1;                                 // O += P(t) V(t) done
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(pvdone + 1);
@@ -172,22 +197,23 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_attn_tc_kernel(const __gr
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int t0 = qb * QB;
   const int nq = min(QB, p.T - t0);
+  constexpr int kSmx = kSmxWarps * 32;
 
   if (tid == 0) {
     for (int s = 0; s < kNS; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    mbar_init(qready, 128);
+    mbar_init(qready, kSmx);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sready[i], 1);
-      mbar_init(&sfree[i], 128);
+      mbar_init(&sfree[i], kSmx);
     }
-    mbar_init(pready, 128);
+    mbar_init(pready, kSmx);
     mbar_init(pvdone, 1);
     mbar_init_fence();
   }
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
                  ::"r"(smem_u32(s_tmem)), "n"(kTmemCols) : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
@@ -196,17 +222,17 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_attn_tc_kernel(const __gr
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *s_tmem;
-  const uint32_t tS[2] = {tmem, tmem + kN};
-  const uint32_t tO = tmem + 2 * kN;
+  const uint32_t tO = tmem + 2 * kN;   // S(t) at tmem + (t & 1) * kN
   grid_wait();   // the rows launch wrote the prompt's cache rows and rotated q rows
   grid_launch_dependents();
   const int st = __ldcg(p.start + b);
   const int nv_max = min(max(st + t0 + nq, 1), p.capacity);
-  const int c0 = ch * p.ch_len;
-  const int c1 = min(c0 + p.ch_len, nv_max);
+  const int ch_len = prefill_chunk_len(nv_max, p.n_ch);
+  const int c0 = ch * ch_len;
+  const int c1 = min(c0 + ch_len, nv_max);
   const int ntiles = c0 < nv_max ? (c1 - c0 + kN - 1) / kN : 0;
 
-  if (warp == 4) {
+  if (warp == kProducerWarp) {
     // ---------------------------------------------------------------- producer
     if (lane == 0 && ntiles > 0) {
       int issued = 0;
@@ -222,7 +248,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_attn_tc_kernel(const __gr
         if (!p.paged) {
           row = (b * p.n_kv_heads + g) * p.capacity + r0;
         } else {
-          // pages of 64 rows or more: the tile lies in one page
+          // pages of 64 rows or more: the tile (64 rows from a multiple of 64) lies in one page
           int page = __ldcg(p.block_table + static_cast<int64_t>(b) * p.bt_stride + r0 / p.page_size);
           if (page < 0 || page >= p.n_pages) {
             set_err(p.err, TTS_EFLAG_PAGE);
@@ -239,7 +265,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_attn_tc_kernel(const __gr
       for (int t = max(0, issued - kNS); t < issued; ++t)
         mbar_wait(&full[t % kNS], static_cast<uint32_t>(t / kNS) & 1u);
     }
-  } else if (warp == 5) {
+  } else if (warp == kMmaWarp) {
     // -------------------------------------------------------------- MMA issuer
     if (lane == 0 && ntiles > 0) {
       // kind::f16, f32 accumulator, bf16 A and B; S: N = 64, both K-major; O: N = 128,
@@ -250,7 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_attn_tc_kernel(const __gr
       const uint32_t qh = smem_u32(sQh), ql = smem_u32(sQl), ph = smem_u32(sPh), pl = smem_u32(sPl);
       auto issue_s = [&](int t) {
         const uint32_t kb = smem_u32(ring + (t % kNS) * 2 * kTileBytes);
-        const uint32_t d = tS[t & 1];
+        const uint32_t d = tmem + (t & 1) * kN;
         // K = 128 in steps of 16: 64-column chunk j / 4, 32 bytes a step within it
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
@@ -307,133 +333,149 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_attn_tc_kernel(const __gr
     }
   } else {
     // ---------------------------------------------------------- softmax warps
-    const int r = tid, tl = r / G, h = r - tl * G;
+    const int w = warp >> 2;                    // column half: S 32 w.., O 64 w..
+    const int r = (warp & 3) * 32 + lane;       // query row = TMEM lane
+    const int tl = r / G, h = r - tl * G;
     const int raw = st + t0 + tl + 1;
-    const int nv = tl < nq ? min(max(raw, 1), p.capacity) : 0;
-    if (ch == 0 && g == 0 && h == 0 && tl < nq && (raw < 1 || raw > p.capacity)) set_err(p.err, TTS_EFLAG_NVALID);
-    // the query row, split into bf16 value and remainder, in the swizzled A layout
+    // the row's window end within the chunk; rows past the prompt run on zero query rows
+    // and store nothing
+    const int lim = tl < nq ? min(min(max(raw, 1), p.capacity), c1) : c1;
+    if (w == 0 && ch == 0 && g == 0 && h == 0 && tl < nq && (raw < 1 || raw > p.capacity))
+      set_err(p.err, TTS_EFLAG_NVALID);
+    // this half of the query row, split into bf16 value and remainder, in the swizzled A
+    // layout (64-column chunk w)
     {
-      float x[kD];
+      float x[64];
       const float4* src = reinterpret_cast<const float4*>(p.q + static_cast<int64_t>(b * p.T + t0 + tl) * p.q_stride +
-                                                          (g * G + h) * kD);
+                                                          (g * G + h) * kD + 64 * w);
 #pragma unroll
-      for (int c = 0; c < kD / 4; ++c) {
+      for (int c = 0; c < 16; ++c) {
         const float4 v = tl < nq ? __ldcg(src + c) : make_float4(0.f, 0.f, 0.f, 0.f);
         x[4 * c] = v.x;
         x[4 * c + 1] = v.y;
         x[4 * c + 2] = v.z;
         x[4 * c + 3] = v.w;
       }
-      split_row64(x, sQh + r * 128, sQl + r * 128, r);
-      split_row64(x + 64, sQh + kM * 128 + r * 128, sQl + kM * 128 + r * 128, r);
+      unsigned char* qh = sQh + w * (kM * 128) + r * 128;
+      unsigned char* ql = sQl + w * (kM * 128) + r * 128;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) split_unit(x + 8 * u, qh, ql, u, r);
     }
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     mbar_arrive(qready);
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const float c = p.scale_log2;
     float m_used = -INFINITY, l = 0.f;
     bool ok = ntiles > 0;
     for (int t = 0; ok && t < ntiles; ++t) {
-      // wait results are made warp-uniform: the tensor-memory loads below are
-      // warp-wide (.sync.aligned) and must be reached by all 32 lanes together
-      if (!__all_sync(kFull, mbar_wait(&sready[t & 1], static_cast<uint32_t>(t >> 1) & 1u))) {
+      const int r0 = c0 + t * kN, base = r0 + 32 * w;   // cache row of this thread's first score
+      float sv[32];
+      float mx = -INFINITY;
+      // wait results are made warp-uniform (the tensor-memory loads are warp-wide) and
+      // then common to both warpgroups at the barrier below
+      bool good = __all_sync(kFull, mbar_wait(&sready[t & 1], static_cast<uint32_t>(t >> 1) & 1u));
+      if (good) {
+        tc_fence_after();
+        tmem_ld32(tmem + (t & 1) * kN + lane_base + 32 * w, sv);
+        tc_fence_before();
+        mbar_arrive(&sfree[t & 1]);
+        if (__all_sync(kFull, base + 32 <= lim)) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) mx = fmaxf(mx, sv[j]);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            sv[j] = base + j < lim ? sv[j] : -INFINITY;
+            mx = fmaxf(mx, sv[j]);
+          }
+        }
+        // O and the P buffer are the product's until O += P(t-1) V(t-1) is done
+        if (t >= 1) good = __all_sync(kFull, mbar_wait(pvdone, static_cast<uint32_t>(t - 1) & 1u));
+      }
+      float* mrow = s_max + (t & 1) * 2 * kM;
+      mrow[w * kM + r] = mx;
+      if (!softmax_sync_and(good)) {
         ok = false;
         break;
       }
-      tc_fence_after();
-      float sv[kN];
-      {
-        float a32[32];
-        tmem_ld32(tS[t & 1] + lane_base, a32);
-#pragma unroll
-        for (int j = 0; j < 32; ++j) sv[j] = a32[j];
-        tmem_ld32(tS[t & 1] + lane_base + 32, a32);
-#pragma unroll
-        for (int j = 0; j < 32; ++j) sv[32 + j] = a32[j];
-      }
-      tc_fence_before();
-      mbar_arrive(&sfree[t & 1]);
-      const int r0 = c0 + t * kN, nrow = min(kN, c1 - r0);
-      float mx = -INFINITY;
-#pragma unroll
-      for (int j = 0; j < kN; ++j) {
-        sv[j] = (j < nrow && r0 + j < nv) ? sv[j] * p.scale_log2 : -INFINITY;
-        mx = fmaxf(mx, sv[j]);
-      }
-      // O and the P buffer are the product's until O += P(t-1) V(t-1) is done
-      if (t >= 1) {
-        if (!__all_sync(kFull, mbar_wait(pvdone, static_cast<uint32_t>(t - 1) & 1u))) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-      }
+      if (t >= 1) tc_fence_after();
+      const float mxs = fmaxf(mx, mrow[(1 - w) * kM + r]) * c;   // the row's maximum, base 2
       // a row moves its maximum in use only when it grew by more than 2^8; rows whose
-      // O holds earlier tiles rescale it (every lane of the warp takes part in the
-      // tensor-memory round trip, a row that keeps its maximum with factor 1)
-      const bool move = mx > m_used + 8.0f;
-      const float alpha = (move && m_used > -INFINITY) ? exp2f(m_used - mx) : 1.0f;
-      if (__any_sync(kFull, move && m_used > -INFINITY)) {
+      // O holds earlier tiles rescale their half of it (every lane of the warp takes part
+      // in the tensor-memory round trip, a row that keeps its maximum with factor 1)
+      const bool move = mxs > m_used + 8.0f;
+      const bool rescale = move && m_used > -INFINITY;
+      const float alpha = rescale ? ex2(m_used - mxs) : 1.0f;
+      if (__any_sync(kFull, rescale)) {
 #pragma unroll
-        for (int c = 0; c < kD / 32; ++c) {
+        for (int cc = 0; cc < 2; ++cc) {
           float o[32];
-          tmem_ld32(tO + lane_base + 32 * c, o);
+          tmem_ld32(tO + lane_base + 64 * w + 32 * cc, o);
 #pragma unroll
           for (int e = 0; e < 32; ++e) o[e] *= alpha;
-          tmem_st32(tO + lane_base + 32 * c, o);
+          tmem_st32(tO + lane_base + 64 * w + 32 * cc, o);
         }
         asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       }
       if (move) {
         l *= alpha;
-        m_used = mx;
+        m_used = mxs;
       }
-      float sum = 0.f;
+      const float msub = m_used == -INFINITY ? 0.f : m_used;
+      float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
-      for (int j = 0; j < kN; ++j) {
-        sv[j] = m_used == -INFINITY ? 0.f : exp2f(sv[j] - m_used);
-        sum += sv[j];
+      for (int i = 0; i < 16; ++i) {
+        const float2 z = __ffma2_rn(make_float2(sv[2 * i], sv[2 * i + 1]), make_float2(c, c), make_float2(-msub, -msub));
+        sv[2 * i] = ex2(z.x);
+        sv[2 * i + 1] = ex2(z.y);
+        acc = __fadd2_rn(acc, make_float2(sv[2 * i], sv[2 * i + 1]));
       }
-      l += sum;
-      if (t == ntiles - 1 && nrow < kN) {
+      l += acc.x + acc.y;
+      if (t == ntiles - 1 && c1 - r0 < kN) {
         // V rows past the chunk take part in the product with weight 0: make them 0
+        const int nrow = c1 - r0;
         unsigned char* vt = ring + (t % kNS) * 2 * kTileBytes + kTileBytes;
-        for (int idx = tid; idx < (kN - nrow) * 16; idx += 128) {
+        for (int idx = tid; idx < (kN - nrow) * 16; idx += kSmx) {
           const int row = nrow + idx / 16, u = idx % 16;
           *reinterpret_cast<uint4*>(vt + sw_off(row, u * 8, kN)) = make_uint4(0, 0, 0, 0);
         }
       }
-      split_row64(sv, sPh + r * 128, sPl + r * 128, r);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) split_unit(sv + 8 * u, sPh + r * 128, sPl + r * 128, 4 * w + u, r);
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       tc_fence_before();
       mbar_arrive(pready);
     }
-    if (!ok) {
-      if (ntiles > 0 && lane == 0) set_err(p.err, TTS_EFLAG_TIMEOUT);
-    } else if (__all_sync(kFull, mbar_wait(pvdone, static_cast<uint32_t>(ntiles - 1) & 1u))) {
-      tc_fence_after();
-      const int64_t orow = p.n_ch == 1 ? static_cast<int64_t>(b * p.T + t0 + tl) * p.n_q_heads + g * G + h
-                                       : (static_cast<int64_t>(item) * p.n_ch + ch) * kM + r;
-      float* dst = (p.n_ch == 1 ? p.out : p.part) + orow * kD;
-      const float inv = p.n_ch == 1 ? (l > 0.f ? 1.f / l : 0.f) : 1.f;
-      // every lane reads (warp-wide loads); rows past the prompt store nothing
+    if (ok) {
+      const bool done = __all_sync(kFull, mbar_wait(pvdone, static_cast<uint32_t>(ntiles - 1) & 1u));
+      s_sum[w * kM + r] = l;
+      ok = softmax_sync_and(done);
+      if (ok) {
+        tc_fence_after();
+        const float lt = l + s_sum[(1 - w) * kM + r];
+        const int64_t orow = p.n_ch == 1 ? static_cast<int64_t>(b * p.T + t0 + tl) * p.n_q_heads + g * G + h
+                                         : (static_cast<int64_t>(item) * p.n_ch + ch) * kM + r;
+        float* dst = (p.n_ch == 1 ? p.out : p.part) + orow * kD + 64 * w;
+        const float inv = p.n_ch == 1 ? (lt > 0.f ? 1.f / lt : 0.f) : 1.f;
+        // every lane reads (warp-wide loads); rows past the prompt store nothing
 #pragma unroll
-      for (int c = 0; c < kD / 32; ++c) {
-        float o[32];
-        tmem_ld32(tO + lane_base + 32 * c, o);
-        if (tl < nq)
+        for (int cc = 0; cc < 2; ++cc) {
+          float o[32];
+          tmem_ld32(tO + lane_base + 64 * w + 32 * cc, o);
+          if (tl < nq)
 #pragma unroll
-          for (int e = 0; e < 32; e += 4)
-            *reinterpret_cast<float4*>(dst + 32 * c + e) =
-                make_float4(o[e] * inv, o[e + 1] * inv, o[e + 2] * inv, o[e + 3] * inv);
+            for (int e = 0; e < 32; e += 4)
+              *reinterpret_cast<float4*>(dst + 32 * cc + e) =
+                  make_float4(o[e] * inv, o[e + 1] * inv, o[e + 2] * inv, o[e + 3] * inv);
+        }
+        if (w == 0 && tl < nq && p.n_ch > 1) reinterpret_cast<float2*>(p.ml)[orow] = make_float2(m_used, lt);
       }
-      if (tl < nq && p.n_ch > 1) reinterpret_cast<float2*>(p.ml)[orow] = make_float2(m_used, l);
-    } else if (lane == 0) {
-      set_err(p.err, TTS_EFLAG_TIMEOUT);
     }
+    if (!ok && ntiles > 0 && lane == 0) set_err(p.err, TTS_EFLAG_TIMEOUT);
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(kTmemCols) : "memory");
   }
