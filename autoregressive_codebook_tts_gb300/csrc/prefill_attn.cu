@@ -402,9 +402,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_attn_kernel(const __grid_
 
 // The chunks of every query row merged in chunk order: M = max m_c, L = sum l_c 2^(m_c - M),
 // out = sum O_c 2^(m_c - M) / L.  One CTA per (item, 8 query rows), a thread per (row,
-// 4 columns); chunk 0 holds a row of every window, so M is finite.
+// 4 columns).  The chunks are taken 8 at a time, all 16 loads of a batch issued before
+// any is used, with the running sums moved to each batch's maximum (the same merge as
+// one pass over all chunks, up to rounding); chunk 0 holds a row of every window, so M
+// is finite from the first batch on.
 constexpr int kCombineRows = 8;
 constexpr int kMaxCombineChunks = 64;
+constexpr int kCombineBatch = 8;
 __global__ void __launch_bounds__(256) prefill_combine_kernel(const PrefillAttnParams p, int G, int D) {
   grid_wait();
   grid_launch_dependents();
@@ -424,22 +428,39 @@ __global__ void __launch_bounds__(256) prefill_combine_kernel(const PrefillAttnP
   if (tl >= nq) return;
   const int64_t row0 = static_cast<int64_t>(item) * p.n_ch * p.rows + r;
   const float2* ml = reinterpret_cast<const float2*>(p.ml) + row0;
-  float M = -INFINITY;
-#pragma unroll 8
-  for (int c = 0; c < n_act; ++c) M = fmaxf(M, __ldcg(ml + c * p.rows).x);
-  float L = 0.f;
+  const float4* part = reinterpret_cast<const float4*>(p.part + row0 * D) + d4;
+  const int64_t cstride4 = static_cast<int64_t>(p.rows) * D4;   // float4s between chunks of a row
+  float M = -INFINITY, L = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-  for (int c = 0; c < n_act; ++c) {
-    const int64_t row = row0 + c * p.rows;
-    const float2 mlc = __ldcg(ml + c * p.rows);
-    const float4 x = __ldcg(reinterpret_cast<const float4*>(p.part + row * D) + d4);
-    const float w = exp2f(mlc.x - M);
-    L = fmaf(mlc.y, w, L);
-    acc.x = fmaf(x.x, w, acc.x);
-    acc.y = fmaf(x.y, w, acc.y);
-    acc.z = fmaf(x.z, w, acc.z);
-    acc.w = fmaf(x.w, w, acc.w);
+  for (int c0 = 0; c0 < n_act; c0 += kCombineBatch) {
+    float2 mlc[kCombineBatch];
+    float4 x[kCombineBatch];
+#pragma unroll
+    for (int i = 0; i < kCombineBatch; ++i) {
+      if (c0 + i < n_act) {
+        mlc[i] = __ldcg(ml + static_cast<int64_t>(c0 + i) * p.rows);
+        x[i] = __ldcg(part + (c0 + i) * cstride4);
+      } else {
+        mlc[i] = make_float2(-INFINITY, 0.f);
+        x[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+    float Mb = M;
+#pragma unroll
+    for (int i = 0; i < kCombineBatch; ++i) Mb = fmaxf(Mb, mlc[i].x);
+    const float s = M == -INFINITY ? 0.f : exp2f(M - Mb);
+    L *= s;
+    acc = make_float4(acc.x * s, acc.y * s, acc.z * s, acc.w * s);
+    M = Mb;
+#pragma unroll
+    for (int i = 0; i < kCombineBatch; ++i) {
+      const float w = mlc[i].x == -INFINITY ? 0.f : exp2f(mlc[i].x - M);
+      L = fmaf(mlc[i].y, w, L);
+      acc.x = fmaf(x[i].x, w, acc.x);
+      acc.y = fmaf(x[i].y, w, acc.y);
+      acc.z = fmaf(x[i].z, w, acc.z);
+      acc.w = fmaf(x[i].w, w, acc.w);
+    }
   }
   const float inv = L > 0.f ? 1.f / L : 0.f;
   reinterpret_cast<float4*>(p.out + (static_cast<int64_t>(b * p.T + t0 + tl) * p.n_q_heads + g * G + h) * D)[d4] =

@@ -22,10 +22,13 @@
 //   O += P_hi V + P_lo V             P split like q; V is the MN-major operand (stored
 //                                    [row][d]); K = 64 rows.
 // S has two tensor-memory buffers (the product of tile t+1 runs while tile t's softmax
-// does), O one (128 columns).  Warps 0-7 are the softmax warps, warp 8 streams K and V
-// tiles with 3-D tensor-map loads (one per tile and operand), warp 9 allocates tensor
-// memory and issues the products.  In the last tile, V rows past the chunk are zeroed
-// before their product (a cache tail may hold anything).
+// does), O one (128 columns); P has two shared-memory buffers, so tile t's softmax waits
+// for O += P(t-2) V(t-2) only, and for O += P(t-1) V(t-1) only when it rescales O.  K
+// and V have rings of their own (3 and 2 stages): a K stage frees when S is done, a V
+// stage when its product with P is.  Warps 0-7 are the softmax warps, warp 8 streams K
+// and V tiles with 3-D tensor-map loads (one per tile and operand), warp 9 allocates
+// tensor memory and issues the products.  In the last tile, V rows past the chunk are
+// zeroed before their product (a cache tail may hold anything).
 // Every wait is bounded; on expiry TTS_EFLAG_TIMEOUT is set and the CTA winds down.
 #include <cstdint>
 #include <mutex>
@@ -44,7 +47,7 @@ namespace {
 constexpr int kD = 128;
 constexpr int kM = 128;                   // query rows of an item
 constexpr int kN = kPrefillTile;          // cache rows of a tile (64)
-constexpr int kNS = 3;                    // K/V ring stages
+constexpr int kNK = 3, kNV = 2;           // K and V ring stages
 constexpr int kSmxWarps = 8;              // two softmax warpgroups
 constexpr int kProducerWarp = 8, kMmaWarp = 9;
 constexpr int kThreads = 320;
@@ -53,11 +56,11 @@ constexpr int kTileBytes = kN * kD * 2;   // 16 KB
 constexpr int kPBytes = kM * kN * 2;      // 16 KB: one 64-column swizzled chunk
 constexpr int kTmemCols = 256;            // S[2] (2 x 64) + O (128)
 
-// smem: Q_hi | Q_lo | ring (K | V) x kNS | P_hi | P_lo | row maxima [2][2][128] |
-// row sums [2][128] | barriers
-constexpr int kOffQh = 0, kOffQl = kQBytes, kOffRing = 2 * kQBytes;
-constexpr int kOffPh = kOffRing + kNS * 2 * kTileBytes, kOffPl = kOffPh + kPBytes;
-constexpr int kOffMax = kOffPl + kPBytes, kOffSum = kOffMax + 2 * 2 * kM * 4;
+// smem: Q_hi | Q_lo | K ring x kNK | V ring x kNV | (P_hi | P_lo) x 2 | row maxima
+// [2][2][128] | row sums [2][128] | barriers
+constexpr int kOffQh = 0, kOffQl = kQBytes, kOffK = 2 * kQBytes, kOffV = kOffK + kNK * kTileBytes;
+constexpr int kOffP = kOffV + kNV * kTileBytes;   // P buffer i: hi at kOffP + 2 i kPBytes, lo after it
+constexpr int kOffMax = kOffP + 4 * kPBytes, kOffSum = kOffMax + 2 * 2 * kM * 4;
 constexpr int kOffBar = kOffSum + 2 * kM * 4;
 constexpr size_t kSmem = 1024 + kOffBar + 32 * sizeof(uint64_t);
 
@@ -129,14 +132,14 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) 
       : "memory");
 }
 
-// Eight values (x[0..7]) as one 16-byte unit of bf16 values (hi = bf16(x)) and one of
-// their bf16 remainders (lo = bf16(x - hi); x - hi is exact, so the fused negate-add
-// computes it without rounding), stored at the swizzled unit position of row r.
-__device__ __forceinline__ void split_unit(const float* x, unsigned char* hi_row, unsigned char* lo_row, int u,
-                                           int r) {
-  uint32_t h[4], l[4];
+// 2 NP values as NP packed pairs of bf16 values (hi = bf16(x)) and of their bf16
+// remainders (lo = bf16(x - hi); x - hi is exact, so the fused negate-add computes it
+// without rounding); split_unit stores eight of them as one 16-byte unit of each at the
+// swizzled unit position of row r.
+template <int NP>
+__device__ __forceinline__ void split_pairs(const float* x, uint32_t (&h)[NP], uint32_t (&l)[NP]) {
 #pragma unroll
-  for (int e = 0; e < 4; ++e) {
+  for (int e = 0; e < NP; ++e) {
     const __nv_bfloat162 hb = __floats2bfloat162_rn(x[2 * e], x[2 * e + 1]);
     h[e] = *reinterpret_cast<const uint32_t*>(&hb);
     const float2 hf = make_float2(__uint_as_float(h[e] << 16), __uint_as_float(h[e] & 0xFFFF0000u));
@@ -144,12 +147,19 @@ __device__ __forceinline__ void split_unit(const float* x, unsigned char* hi_row
     const __nv_bfloat162 lb = __floats2bfloat162_rn(rem.x, rem.y);
     l[e] = *reinterpret_cast<const uint32_t*>(&lb);
   }
+}
+__device__ __forceinline__ void split_unit(const float* x, unsigned char* hi_row, unsigned char* lo_row, int u,
+                                           int r) {
+  uint32_t h[4], l[4];
+  split_pairs(x, h, l);
   const uint32_t off = static_cast<uint32_t>((u ^ (r & 7)) << 4);
   *reinterpret_cast<uint4*>(hi_row + off) = make_uint4(h[0], h[1], h[2], h[3]);
   *reinterpret_cast<uint4*>(lo_row + off) = make_uint4(l[0], l[1], l[2], l[3]);
 }
 
-// Named barrier 1 over the 256 softmax threads, returning the AND of every thread's v
+// Named barrier 1 over the 256 softmax threads.
+__device__ __forceinline__ void softmax_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+// The same barrier, returning the AND of every thread's v
 // (warp-convergent: each warp reaches it with all lanes).
 __device__ __forceinline__ bool softmax_sync_and(bool v) {
   uint32_t out;
@@ -173,23 +183,26 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_attn_tc_kernel(const __gr
                                                                        const __grid_constant__ CUtensorMap vmap,
                                                                        const PrefillAttnParams p) {
   constexpr int QB = kM / G;   // queries of an item
+  constexpr int kSmx = kSmxWarps * 32;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   unsigned char* sQh = smem + kOffQh;
   unsigned char* sQl = smem + kOffQl;
-  unsigned char* ring = smem + kOffRing;
-  unsigned char* sPh = smem + kOffPh;
-  unsigned char* sPl = smem + kOffPl;
+  unsigned char* sK = smem + kOffK;
+  unsigned char* sV = smem + kOffV;
+  unsigned char* sP = smem + kOffP;
   float* s_max = reinterpret_cast<float*>(smem + kOffMax);       // [tile parity][half][row]
   float* s_sum = reinterpret_cast<float*>(smem + kOffSum);       // [half][row]
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kOffBar);  // [kNS] K and V landed
-  uint64_t* empty = full + kNS;                                  // [kNS] the tile's products done
-  uint64_t* qready = empty + kNS;                                // the split query rows written
+  uint64_t* fullK = reinterpret_cast<uint64_t*>(smem + kOffBar); // [kNK] K(t) landed
+  uint64_t* emptyK = fullK + kNK;                                // [kNK] S(t) done
+  uint64_t* fullV = emptyK + kNK;                                // [kNV] V(t) landed
+  uint64_t* emptyV = fullV + kNV;                                // [kNV] O += P(t) V(t) done
+  uint64_t* qready = emptyV + kNV;                               // the split query rows written
   uint64_t* sready = qready + 1;                                 // [2] S(t) in tensor memory
   uint64_t* sfree = sready + 2;                                  // [2] S(t) read by every thread
-  uint64_t* pready = sfree + 2;                                  // P(t) written (and O rescaled)
-  uint64_t* pvdone = pready + 1;                                 // O += P(t) V(t) done
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(pvdone + 1);
+  uint64_t* pready = sfree + 2;                                  // [2] P(t) written (and O rescaled)
+  uint64_t* pvdone = pready + 2;                                 // [2] O += P(t) V(t) done (P buffer t & 1)
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(pvdone + 2);
 
   const int item = blockIdx.x, ch = blockIdx.y;
   const int qb = item % p.n_qb, bg = item / p.n_qb;
@@ -197,20 +210,23 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_attn_tc_kernel(const __gr
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int t0 = qb * QB;
   const int nq = min(QB, p.T - t0);
-  constexpr int kSmx = kSmxWarps * 32;
 
   if (tid == 0) {
-    for (int s = 0; s < kNS; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+    for (int s = 0; s < kNK; ++s) {
+      mbar_init(&fullK[s], 1);
+      mbar_init(&emptyK[s], 1);
+    }
+    for (int s = 0; s < kNV; ++s) {
+      mbar_init(&fullV[s], 1);
+      mbar_init(&emptyV[s], 1);
     }
     mbar_init(qready, kSmx);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sready[i], 1);
       mbar_init(&sfree[i], kSmx);
+      mbar_init(&pready[i], kSmx);
+      mbar_init(&pvdone[i], 1);
     }
-    mbar_init(pready, kSmx);
-    mbar_init(pvdone, 1);
     mbar_init_fence();
   }
   if (warp == kMmaWarp) {
@@ -234,16 +250,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_attn_tc_kernel(const __gr
 
   if (warp == kProducerWarp) {
     // ---------------------------------------------------------------- producer
+    // K(t) goes into its stage once S(t - kNK) is done, V(t) once O += P(t - kNV) V(t - kNV) is
     if (lane == 0 && ntiles > 0) {
-      int issued = 0;
+      int nk = 0, nvv = 0;   // K and V tiles issued
       bool ok = true;
-      for (; issued < ntiles; ++issued) {
-        const int s = issued % kNS;
-        if (issued >= kNS && !mbar_wait(&empty[s], static_cast<uint32_t>((issued / kNS) - 1) & 1u)) {
-          ok = false;
-          break;
-        }
-        const int r0 = c0 + issued * kN;
+      for (int i = 0; i < ntiles; ++i) {
+        const int r0 = c0 + i * kN;
         int row;
         if (!p.paged) {
           row = (b * p.n_kv_heads + g) * p.capacity + r0;
@@ -256,26 +268,41 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_attn_tc_kernel(const __gr
           }
           row = (page * p.n_kv_heads + g) * p.page_size + (r0 & (p.page_size - 1));
         }
-        unsigned char* kd = ring + s * 2 * kTileBytes;
-        mbar_arrive_expect_tx(&full[s], 2 * kTileBytes);
-        tma_load_3d(kd, &kmap, row, &full[s]);
-        tma_load_3d(kd + kTileBytes, &vmap, row, &full[s]);
+        const int ks = i % kNK, vs = i % kNV;
+        if (i >= kNK && !mbar_wait(&emptyK[ks], static_cast<uint32_t>((i / kNK) - 1) & 1u)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(&fullK[ks], kTileBytes);
+        tma_load_3d(sK + ks * kTileBytes, &kmap, row, &fullK[ks]);
+        nk = i + 1;
+        if (i >= kNV && !mbar_wait(&emptyV[vs], static_cast<uint32_t>((i / kNV) - 1) & 1u)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(&fullV[vs], kTileBytes);
+        tma_load_3d(sV + vs * kTileBytes, &vmap, row, &fullV[vs]);
+        nvv = i + 1;
       }
       if (!ok) set_err(p.err, TTS_EFLAG_TIMEOUT);
-      for (int t = max(0, issued - kNS); t < issued; ++t)
-        mbar_wait(&full[t % kNS], static_cast<uint32_t>(t / kNS) & 1u);
+      // every copy still in flight lands before the CTA ends (earlier ones were consumed)
+      for (int t = max(0, nk - kNK); t < nk; ++t) mbar_wait(&fullK[t % kNK], static_cast<uint32_t>(t / kNK) & 1u);
+      for (int t = max(0, nvv - kNV); t < nvv; ++t) mbar_wait(&fullV[t % kNV], static_cast<uint32_t>(t / kNV) & 1u);
     }
   } else if (warp == kMmaWarp) {
     // -------------------------------------------------------------- MMA issuer
+    // Barriers with one phase per tile come in pairs (tile parity) wherever a waiter could
+    // otherwise see a later tile's phase: each wait below is for a phase that cannot be
+    // overtaken before the waiter has passed it.
     if (lane == 0 && ntiles > 0) {
       // kind::f16, f32 accumulator, bf16 A and B; S: N = 64, both K-major; O: N = 128,
       // B (V) MN-major (bit 16)
       const uint32_t idS = (1u << 4) | (1u << 7) | (1u << 10) | ((kN >> 3) << 17) | ((kM >> 4) << 24);
       const uint32_t idO =
           (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) | ((kD >> 3) << 17) | ((kM >> 4) << 24);
-      const uint32_t qh = smem_u32(sQh), ql = smem_u32(sQl), ph = smem_u32(sPh), pl = smem_u32(sPl);
+      const uint32_t qh = smem_u32(sQh), ql = smem_u32(sQl), pb = smem_u32(sP);
       auto issue_s = [&](int t) {
-        const uint32_t kb = smem_u32(ring + (t % kNS) * 2 * kTileBytes);
+        const uint32_t kb = smem_u32(sK + (t % kNK) * kTileBytes);
         const uint32_t d = tmem + (t & 1) * kN;
         // K = 128 in steps of 16: 64-column chunk j / 4, 32 bytes a step within it
 #pragma unroll
@@ -289,9 +316,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_attn_tc_kernel(const __gr
           mma_f16(d, smem_desc(ql + qo, 16, 1024), smem_desc(kb + ko, 16, 1024), idS, 1u);
         }
         mma_commit(&sready[t & 1]);
+        mma_commit(&emptyK[t % kNK]);
       };
       auto issue_pv = [&](int t) {
-        const uint32_t vb = smem_u32(ring + (t % kNS) * 2 * kTileBytes + kTileBytes);
+        const uint32_t vb = smem_u32(sV + (t % kNV) * kTileBytes);
+        const uint32_t ph = pb + (t & 1) * 2 * kPBytes, pl = ph + kPBytes;
         // K = 64 cache rows in steps of 16: P 32 bytes a step; V (MN-major) 16 rows =
         // 2048 bytes a step, its 64-column chunks 8192 bytes apart
 #pragma unroll
@@ -301,19 +330,23 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_attn_tc_kernel(const __gr
 #pragma unroll
         for (int j = 0; j < 4; ++j)
           mma_f16(tO, smem_desc(pl + j * 32, 16, 1024), smem_desc(vb + j * 2048, 8192, 1024), idO, 1u);
-        mma_commit(&empty[t % kNS]);
-        mma_commit(pvdone);
+        mma_commit(&emptyV[t % kNV]);
+        mma_commit(&pvdone[t & 1]);
+      };
+      auto wait_pv_inputs = [&](int t) {
+        return mbar_wait(&pready[t & 1], static_cast<uint32_t>(t >> 1) & 1u) &&
+               mbar_wait(&fullV[t % kNV], static_cast<uint32_t>(t / kNV) & 1u);
       };
       bool ok = mbar_wait(qready, 0);
       int t = 0;
       for (; ok && t < ntiles; ++t) {
-        if (!mbar_wait(&full[t % kNS], static_cast<uint32_t>(t / kNS) & 1u)) ok = false;
+        if (!mbar_wait(&fullK[t % kNK], static_cast<uint32_t>(t / kNK) & 1u)) ok = false;
         if (ok && t >= 2 && !mbar_wait(&sfree[t & 1], static_cast<uint32_t>((t - 2) >> 1) & 1u)) ok = false;
         if (!ok) break;
         tc_fence_after();
         issue_s(t);
         if (t >= 1) {
-          if (!mbar_wait(pready, static_cast<uint32_t>(t - 1) & 1u)) {
+          if (!wait_pv_inputs(t - 1)) {
             ok = false;
             break;
           }
@@ -322,7 +355,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_attn_tc_kernel(const __gr
         }
       }
       if (ok) {
-        if (mbar_wait(pready, static_cast<uint32_t>(ntiles - 1) & 1u)) {
+        if (wait_pv_inputs(ntiles - 1)) {
           tc_fence_after();
           issue_pv(ntiles - 1);
         } else {
@@ -342,31 +375,36 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_attn_tc_kernel(const __gr
     const int lim = tl < nq ? min(min(max(raw, 1), p.capacity), c1) : c1;
     if (w == 0 && ch == 0 && g == 0 && h == 0 && tl < nq && (raw < 1 || raw > p.capacity))
       set_err(p.err, TTS_EFLAG_NVALID);
-    // this half of the query row, split into bf16 value and remainder, in the swizzled A
-    // layout (64-column chunk w)
+    // the query rows, split into bf16 value and remainder, in the swizzled A layout:
+    // warp k takes rows 16k..16k+15, one coalesced 512-byte row per load (lane j holds
+    // columns 4j..4j+3: 64-column chunk j / 16, 16-byte unit (j % 16) / 2, half j % 2)
     {
-      float x[64];
-      const float4* src = reinterpret_cast<const float4*>(p.q + static_cast<int64_t>(b * p.T + t0 + tl) * p.q_stride +
-                                                          (g * G + h) * kD + 64 * w);
+      float4 v[16];
 #pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        const float4 v = tl < nq ? __ldcg(src + c) : make_float4(0.f, 0.f, 0.f, 0.f);
-        x[4 * c] = v.x;
-        x[4 * c + 1] = v.y;
-        x[4 * c + 2] = v.z;
-        x[4 * c + 3] = v.w;
+      for (int i = 0; i < 16; ++i) {
+        const int rr = warp * 16 + i, tr = rr / G, hr = rr - tr * G;
+        v[i] = tr < nq ? __ldcg(reinterpret_cast<const float4*>(p.q + static_cast<int64_t>(b * p.T + t0 + tr) * p.q_stride +
+                                                                (g * G + hr) * kD) + lane)
+                       : make_float4(0.f, 0.f, 0.f, 0.f);
       }
-      unsigned char* qh = sQh + w * (kM * 128) + r * 128;
-      unsigned char* ql = sQl + w * (kM * 128) + r * 128;
 #pragma unroll
-      for (int u = 0; u < 8; ++u) split_unit(x + 8 * u, qh, ql, u, r);
+      for (int i = 0; i < 16; ++i) {
+        const int rr = warp * 16 + i;
+        const uint32_t off = static_cast<uint32_t>((lane >> 4) * (kM * 128) + rr * 128 +
+                                                   ((((lane & 15) >> 1) ^ (rr & 7)) << 4) + ((lane & 1) << 3));
+        const float x[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+        uint32_t hq[2], lq[2];
+        split_pairs(x, hq, lq);
+        *reinterpret_cast<uint2*>(sQh + off) = make_uint2(hq[0], hq[1]);
+        *reinterpret_cast<uint2*>(sQl + off) = make_uint2(lq[0], lq[1]);
+      }
     }
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     mbar_arrive(qready);
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const float c = p.scale_log2;
     float m_used = -INFINITY, l = 0.f;
-    bool ok = ntiles > 0;
+    bool ok = ntiles > 0, bad = false;
     for (int t = 0; ok && t < ntiles; ++t) {
       const int r0 = c0 + t * kN, base = r0 + 32 * w;   // cache row of this thread's first score
       float sv[32];
@@ -379,26 +417,30 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_attn_tc_kernel(const __gr
         tmem_ld32(tmem + (t & 1) * kN + lane_base + 32 * w, sv);
         tc_fence_before();
         mbar_arrive(&sfree[t & 1]);
-        if (__all_sync(kFull, base + 32 <= lim)) {
+        if (!__all_sync(kFull, base + 32 <= lim)) {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) mx = fmaxf(mx, sv[j]);
-        } else {
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            sv[j] = base + j < lim ? sv[j] : -INFINITY;
-            mx = fmaxf(mx, sv[j]);
-          }
+          for (int j = 0; j < 32; ++j) sv[j] = base + j < lim ? sv[j] : -INFINITY;
         }
-        // O and the P buffer are the product's until O += P(t-1) V(t-1) is done
-        if (t >= 1) good = __all_sync(kFull, mbar_wait(pvdone, static_cast<uint32_t>(t - 1) & 1u));
+        float m16[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) m16[j] = fmaxf(sv[j], sv[j + 16]);
+#pragma unroll
+        for (int s = 8; s >= 1; s >>= 1)
+#pragma unroll
+          for (int j = 0; j < s; ++j) m16[j] = fmaxf(m16[j], m16[j + s]);
+        mx = m16[0];
+        // P buffer t & 1 is the product's until O += P(t-2) V(t-2) is done
+        if (t >= 2) good = __all_sync(kFull, mbar_wait(&pvdone[t & 1], static_cast<uint32_t>((t - 2) >> 1) & 1u));
+        // the last tile's V rows past the chunk are zeroed below: the tile must have landed
+        if (good && t == ntiles - 1 && c1 - r0 < kN)
+          good = __all_sync(kFull, mbar_wait(&fullV[t % kNV], static_cast<uint32_t>(t / kNV) & 1u));
       }
       float* mrow = s_max + (t & 1) * 2 * kM;
       mrow[w * kM + r] = mx;
-      if (!softmax_sync_and(good)) {
+      if (!softmax_sync_and(good && !bad)) {
         ok = false;
         break;
       }
-      if (t >= 1) tc_fence_after();
       const float mxs = fmaxf(mx, mrow[(1 - w) * kM + r]) * c;   // the row's maximum, base 2
       // a row moves its maximum in use only when it grew by more than 2^8; rows whose
       // O holds earlier tiles rescale their half of it (every lane of the warp takes part
@@ -407,68 +449,95 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_attn_tc_kernel(const __gr
       const bool rescale = move && m_used > -INFINITY;
       const float alpha = rescale ? ex2(m_used - mxs) : 1.0f;
       if (__any_sync(kFull, rescale)) {
+        // O holds tiles up to t-1 once O += P(t-1) V(t-1) is done (t >= 1 here: the
+        // maximum in use is finite); an expired wait skips the rescale and ends the loop
+        // at the next barrier
+        if (__all_sync(kFull, mbar_wait(&pvdone[(t - 1) & 1], static_cast<uint32_t>((t - 1) >> 1) & 1u))) {
+          tc_fence_after();
 #pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-          float o[32];
-          tmem_ld32(tO + lane_base + 64 * w + 32 * cc, o);
+          for (int cc = 0; cc < 2; ++cc) {
+            float o[32];
+            tmem_ld32(tO + lane_base + 64 * w + 32 * cc, o);
 #pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] *= alpha;
-          tmem_st32(tO + lane_base + 64 * w + 32 * cc, o);
+            for (int e = 0; e < 32; ++e) o[e] *= alpha;
+            tmem_st32(tO + lane_base + 64 * w + 32 * cc, o);
+          }
+          asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+        } else {
+          bad = true;
         }
-        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       }
       if (move) {
         l *= alpha;
         m_used = mxs;
       }
       const float msub = m_used == -INFINITY ? 0.f : m_used;
-      float2 acc = make_float2(0.f, 0.f);
+      float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
         const float2 z = __ffma2_rn(make_float2(sv[2 * i], sv[2 * i + 1]), make_float2(c, c), make_float2(-msub, -msub));
         sv[2 * i] = ex2(z.x);
         sv[2 * i + 1] = ex2(z.y);
-        acc = __fadd2_rn(acc, make_float2(sv[2 * i], sv[2 * i + 1]));
+        acc[i & 3] = __fadd2_rn(acc[i & 3], make_float2(sv[2 * i], sv[2 * i + 1]));
       }
-      l += acc.x + acc.y;
+      const float2 a01 = __fadd2_rn(acc[0], acc[1]), a23 = __fadd2_rn(acc[2], acc[3]);
+      const float2 a = __fadd2_rn(a01, a23);
+      l += a.x + a.y;
       if (t == ntiles - 1 && c1 - r0 < kN) {
         // V rows past the chunk take part in the product with weight 0: make them 0
         const int nrow = c1 - r0;
-        unsigned char* vt = ring + (t % kNS) * 2 * kTileBytes + kTileBytes;
+        unsigned char* vt = sV + (t % kNV) * kTileBytes;
         for (int idx = tid; idx < (kN - nrow) * 16; idx += kSmx) {
           const int row = nrow + idx / 16, u = idx % 16;
           *reinterpret_cast<uint4*>(vt + sw_off(row, u * 8, kN)) = make_uint4(0, 0, 0, 0);
         }
       }
+      unsigned char* ph = sP + (t & 1) * 2 * kPBytes + r * 128;
 #pragma unroll
-      for (int u = 0; u < 4; ++u) split_unit(sv + 8 * u, sPh + r * 128, sPl + r * 128, 4 * w + u, r);
+      for (int u = 0; u < 4; ++u) split_unit(sv + 8 * u, ph, ph + kPBytes, 4 * w + u, r);
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       tc_fence_before();
-      mbar_arrive(pready);
+      mbar_arrive(&pready[t & 1]);
     }
     if (ok) {
-      const bool done = __all_sync(kFull, mbar_wait(pvdone, static_cast<uint32_t>(ntiles - 1) & 1u));
+      const int tlast = ntiles - 1;
+      const bool done = __all_sync(kFull, mbar_wait(&pvdone[tlast & 1], static_cast<uint32_t>(tlast >> 1) & 1u));
       s_sum[w * kM + r] = l;
-      ok = softmax_sync_and(done);
+      ok = softmax_sync_and(done && !bad);
       if (ok) {
         tc_fence_after();
         const float lt = l + s_sum[(1 - w) * kM + r];
-        const int64_t orow = p.n_ch == 1 ? static_cast<int64_t>(b * p.T + t0 + tl) * p.n_q_heads + g * G + h
-                                         : (static_cast<int64_t>(item) * p.n_ch + ch) * kM + r;
-        float* dst = (p.n_ch == 1 ? p.out : p.part) + orow * kD + 64 * w;
         const float inv = p.n_ch == 1 ? (lt > 0.f ? 1.f / lt : 0.f) : 1.f;
-        // every lane reads (warp-wide loads); rows past the prompt store nothing
+        // O staged in the K and V rings (every product is done, every load consumed):
+        // row r's 16-byte unit u at (u ^ r % 32), so that both the row-per-lane writes
+        // here and the unit-per-lane reads below are conflict-free
+        float* so = reinterpret_cast<float*>(smem + kOffK);
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc) {
           float o[32];
           tmem_ld32(tO + lane_base + 64 * w + 32 * cc, o);
-          if (tl < nq)
 #pragma unroll
-            for (int e = 0; e < 32; e += 4)
-              *reinterpret_cast<float4*>(dst + 32 * cc + e) =
-                  make_float4(o[e] * inv, o[e + 1] * inv, o[e + 2] * inv, o[e + 3] * inv);
+          for (int e = 0; e < 8; ++e) {
+            const int u = 16 * w + 8 * cc + e;
+            *reinterpret_cast<float4*>(so + r * kD + ((u ^ (r & 31)) << 2)) =
+                make_float4(o[4 * e] * inv, o[4 * e + 1] * inv, o[4 * e + 2] * inv, o[4 * e + 3] * inv);
+          }
         }
-        if (w == 0 && tl < nq && p.n_ch > 1) reinterpret_cast<float2*>(p.ml)[orow] = make_float2(m_used, lt);
+        if (w == 0 && tl < nq && p.n_ch > 1)
+          reinterpret_cast<float2*>(p.ml)[(static_cast<int64_t>(item) * p.n_ch + ch) * kM + r] = make_float2(m_used, lt);
+        softmax_sync();
+        // coalesced stores: warp k writes rows 16k..16k+15, lane j the row's unit j;
+        // rows past the prompt store nothing
+#pragma unroll 4
+        for (int i = 0; i < 16; ++i) {
+          const int rr = warp * 16 + i, tr = rr / G, hr = rr - tr * G;
+          if (tr < nq) {
+            const int64_t orow = p.n_ch == 1 ? static_cast<int64_t>(b * p.T + t0 + tr) * p.n_q_heads + g * G + hr
+                                             : (static_cast<int64_t>(item) * p.n_ch + ch) * kM + rr;
+            float* dst = (p.n_ch == 1 ? p.out : p.part) + orow * kD;
+            reinterpret_cast<float4*>(dst)[lane] = *reinterpret_cast<const float4*>(so + rr * kD + ((lane ^ (rr & 31)) << 2));
+          }
+        }
       }
     }
     if (!ok && ntiles > 0 && lane == 0) set_err(p.err, TTS_EFLAG_TIMEOUT);
