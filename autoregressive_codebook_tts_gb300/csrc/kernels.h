@@ -204,6 +204,8 @@ struct PrefillAttnParams {
   float* ml;                    // their (max, sum) [items][n_ch][rows][2]
   int n_qb, n_ch;               // query blocks per (stream, kv head), chunks per item
   int rows;                     // query rows of an item: 64 (CUDA cores) or 128 (tensor cores)
+  int merge_in_cluster;         // tensor cores, 1 < n_ch <= 8: an item's chunks form a cluster
+                                // and merge there (set by the launcher)
   int32_t* err;
 };
 bool prefill_attn_supported(int head_dim, int group, int paged, int page_size, int T);
@@ -215,8 +217,12 @@ void prefill_attn_plan(int B, int T, int n_kv_heads, int group, int capacity, in
                        int& n_qb, int& n_ch);
 size_t prefill_attn_workspace(int B, int T, int n_kv_heads, int group, int head_dim, int capacity, int n_splits,
                               int n_sm, int rows);
+// Clusters of S (2..8) CTAs of the tensor-core kernel the current device keeps resident
+// at once (0 if none or S is out of range).
+int prefill_tc_active_clusters(int group, int S);
+// *merged: the chunks were merged inside the launch (no combine launch needed).
 cudaError_t launch_prefill_attn_tc(const PrefillAttnParams& p, const void* k_cache, const void* v_cache, int group,
-                                   cudaStream_t s);
+                                   cudaStream_t s, bool* merged);
 cudaError_t launch_prefill_attn(const PrefillAttnParams& p, const void* k_cache, const void* v_cache, bool kv_bf16,
                                 int head_dim, int group, cudaStream_t s);
 

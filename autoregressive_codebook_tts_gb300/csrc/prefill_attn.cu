@@ -556,9 +556,19 @@ void prefill_attn_plan(int B, int T, int n_kv_heads, int group, int capacity, in
   const int QB = rows / group;
   n_qb = (T + QB - 1) / QB;
   const int items = B * n_kv_heads * n_qb;
-  // Both kernels hold one CTA per SM: by default as many chunks as fill one wave.  Each
-  // item's window is cut into that many parts on the device (prefill_chunk_len).
+  // Both kernels hold one CTA per SM: by default as many chunks as fill one wave.  On
+  // the tensor cores an item's 2..8 chunks can form a cluster and merge there, saving the
+  // combine launch and the partial rows' round trip (worth about two tiles of the loop):
+  // the largest cluster size whose clusters are all resident at once is taken when it
+  // keeps at least half the chunks of the one-wave cut.  Each item's window is cut into
+  // n_ch parts on the device (prefill_chunk_len).
   int c = n_splits > 0 ? n_splits : n_sm / items;
+  if (n_splits <= 0 && rows == 2 * kRows) {
+    int sc = 0;
+    for (int s = 8; s >= 2 && sc == 0; --s)
+      if (items <= prefill_tc_active_clusters(group, s)) sc = s;
+    if (sc >= 2 && 2 * sc >= c) c = sc;
+  }
   const int max_ch = (capacity + kTile - 1) / kTile;
   if (c > max_ch) c = max_ch;
   if (c > kMaxCombineChunks) c = kMaxCombineChunks;
@@ -578,8 +588,9 @@ size_t prefill_attn_workspace(int B, int T, int n_kv_heads, int group, int head_
 cudaError_t launch_prefill_attn(const PrefillAttnParams& p, const void* k_cache, const void* v_cache, bool kv_bf16,
                                 int head_dim, int group, cudaStream_t s) {
   if (p.rows == 2 * kRows) {
-    const cudaError_t e = launch_prefill_attn_tc(p, k_cache, v_cache, group, s);
-    if (e != cudaSuccess || p.n_ch == 1) return e;
+    bool merged = false;
+    const cudaError_t e = launch_prefill_attn_tc(p, k_cache, v_cache, group, s, &merged);
+    if (e != cudaSuccess || p.n_ch == 1 || merged) return e;
     return launch_combine(p, group, head_dim, s);
   }
   if (p.rows != kRows) return cudaErrorInvalidValue;

@@ -55,6 +55,7 @@ constexpr int kQBytes = kM * kD * 2;      // 32 KB: two 64-column swizzled chunk
 constexpr int kTileBytes = kN * kD * 2;   // 16 KB
 constexpr int kPBytes = kM * kN * 2;      // 16 KB: one 64-column swizzled chunk
 constexpr int kTmemCols = 256;            // S[2] (2 x 64) + O (128)
+constexpr int kMaxClusterCh = 8;          // chunks merged in a cluster (portable size)
 
 // smem: Q_hi | Q_lo | K ring x kNK | V ring x kNV | (P_hi | P_lo) x 2 | row maxima
 // [2][2][128] | row sums [2][128] | barriers
@@ -157,6 +158,19 @@ __device__ __forceinline__ void split_unit(const float* x, unsigned char* hi_row
   *reinterpret_cast<uint4*>(lo_row + off) = make_uint4(l[0], l[1], l[2], l[3]);
 }
 
+// 8 and 16 bytes of another CTA's shared memory (cluster-window addresses from mapa).
+__device__ __forceinline__ float2 ld_cluster_f32x2(uint32_t addr) {
+  float2 v;
+  asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ float4 ld_cluster_f32x4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr) : "memory");
+  return v;
+}
+
 // Named barrier 1 over the 256 softmax threads.
 __device__ __forceinline__ void softmax_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 // The same barrier, returning the AND of every thread's v
@@ -193,6 +207,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_attn_tc_kernel(const __gr
   unsigned char* sP = smem + kOffP;
   float* s_max = reinterpret_cast<float*>(smem + kOffMax);       // [tile parity][half][row]
   float* s_sum = reinterpret_cast<float*>(smem + kOffSum);       // [half][row]
+  float* so = reinterpret_cast<float*>(smem + kOffK);            // O staging [row][128] after the loop
+  float2* s_ml = reinterpret_cast<float2*>(smem + kOffMax);      // (max, sum) per row after the loop
   uint64_t* fullK = reinterpret_cast<uint64_t*>(smem + kOffBar); // [kNK] K(t) landed
   uint64_t* emptyK = fullK + kNK;                                // [kNK] S(t) done
   uint64_t* fullV = emptyK + kNK;                                // [kNV] V(t) landed
@@ -499,6 +515,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_attn_tc_kernel(const __gr
       tc_fence_before();
       mbar_arrive(&pready[t & 1]);
     }
+    bool staged = false;
     if (ok) {
       const int tlast = ntiles - 1;
       const bool done = __all_sync(kFull, mbar_wait(&pvdone[tlast & 1], static_cast<uint32_t>(tlast >> 1) & 1u));
@@ -511,7 +528,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_attn_tc_kernel(const __gr
         // O staged in the K and V rings (every product is done, every load consumed):
         // row r's 16-byte unit u at (u ^ r % 32), so that both the row-per-lane writes
         // here and the unit-per-lane reads below are conflict-free
-        float* so = reinterpret_cast<float*>(smem + kOffK);
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc) {
           float o[32];
@@ -523,23 +539,32 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_attn_tc_kernel(const __gr
                 make_float4(o[4 * e] * inv, o[4 * e + 1] * inv, o[4 * e + 2] * inv, o[4 * e + 3] * inv);
           }
         }
-        if (w == 0 && tl < nq && p.n_ch > 1)
-          reinterpret_cast<float2*>(p.ml)[(static_cast<int64_t>(item) * p.n_ch + ch) * kM + r] = make_float2(m_used, lt);
-        softmax_sync();
-        // coalesced stores: warp k writes rows 16k..16k+15, lane j the row's unit j;
-        // rows past the prompt store nothing
+        staged = true;
+        if (p.merge_in_cluster) {
+          if (w == 0) s_ml[r] = make_float2(m_used, lt);   // the loop's maxima are all read
+        } else {
+          if (w == 0 && tl < nq && p.n_ch > 1)
+            reinterpret_cast<float2*>(p.ml)[(static_cast<int64_t>(item) * p.n_ch + ch) * kM + r] =
+                make_float2(m_used, lt);
+          softmax_sync();
+          // coalesced stores: warp k writes rows 16k..16k+15, lane j the row's unit j;
+          // rows past the prompt store nothing
 #pragma unroll 4
-        for (int i = 0; i < 16; ++i) {
-          const int rr = warp * 16 + i, tr = rr / G, hr = rr - tr * G;
-          if (tr < nq) {
-            const int64_t orow = p.n_ch == 1 ? static_cast<int64_t>(b * p.T + t0 + tr) * p.n_q_heads + g * G + hr
-                                             : (static_cast<int64_t>(item) * p.n_ch + ch) * kM + rr;
-            float* dst = (p.n_ch == 1 ? p.out : p.part) + orow * kD;
-            reinterpret_cast<float4*>(dst)[lane] = *reinterpret_cast<const float4*>(so + rr * kD + ((lane ^ (rr & 31)) << 2));
+          for (int i = 0; i < 16; ++i) {
+            const int rr = warp * 16 + i, tr = rr / G, hr = rr - tr * G;
+            if (tr < nq) {
+              const int64_t orow = p.n_ch == 1 ? static_cast<int64_t>(b * p.T + t0 + tr) * p.n_q_heads + g * G + hr
+                                               : (static_cast<int64_t>(item) * p.n_ch + ch) * kM + rr;
+              float* dst = (p.n_ch == 1 ? p.out : p.part) + orow * kD;
+              reinterpret_cast<float4*>(dst)[lane] =
+                  *reinterpret_cast<const float4*>(so + rr * kD + ((lane ^ (rr & 31)) << 2));
+            }
           }
         }
       }
     }
+    // a chunk with no rows (or whose waits ran out) adds nothing to the cluster's merge
+    if (p.merge_in_cluster && !staged && w == 0) s_ml[r] = make_float2(-INFINITY, 0.f);
     if (!ok && ntiles > 0 && lane == 0) set_err(p.err, TTS_EFLAG_TIMEOUT);
   }
   tc_fence_before();
@@ -547,6 +572,59 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_attn_tc_kernel(const __gr
   if (warp == kMmaWarp) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(kTmemCols) : "memory");
+  }
+  if (p.merge_in_cluster) {
+    // Every CTA of the cluster (the item's n_ch chunks, rank = chunk) has staged its rows
+    // and their (max, sum).  Rank k merges rows [128 k / n_ch, 128 (k + 1) / n_ch) in
+    // chunk order, reading the other CTAs' shared memory: M = max m_c,
+    // L = sum l_c 2^(m_c - M), out = sum O_c 2^(m_c - M) / L; warp k of 8 takes rows
+    // k, k + 8, ... of the range, lane j the row's 16-byte unit j.  Every thread of every
+    // CTA reaches both cluster barriers.
+    cluster_sync_all();
+    const int S = p.n_ch, rank = static_cast<int>(cluster_rank());
+    if (warp < kSmxWarps) {
+      uint32_t o_peer[kMaxClusterCh], ml_peer[kMaxClusterCh];
+#pragma unroll
+      for (int c = 0; c < kMaxClusterCh; ++c) {
+        o_peer[c] = c < S ? map_shared_rank(so, static_cast<uint32_t>(c)) : 0u;
+        ml_peer[c] = c < S ? map_shared_rank(s_ml, static_cast<uint32_t>(c)) : 0u;
+      }
+      const int r_hi = (rank + 1) * kM / S;
+      for (int rr = rank * kM / S + warp; rr < r_hi; rr += kSmxWarps) {
+        const int tr = rr / G, hr = rr - tr * G;
+        if (tr >= nq) continue;
+        float2 mlc[kMaxClusterCh];
+        float M = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < kMaxClusterCh; ++c) {
+          mlc[c] = c < S ? ld_cluster_f32x2(ml_peer[c] + rr * 8) : make_float2(-INFINITY, 0.f);
+          M = fmaxf(M, mlc[c].x);
+        }
+        const uint32_t uoff = static_cast<uint32_t>(rr * kD + ((lane ^ (rr & 31)) << 2)) * 4u;
+        float4 x[kMaxClusterCh];
+#pragma unroll
+        for (int c = 0; c < kMaxClusterCh; ++c)
+          x[c] = mlc[c].x > -INFINITY ? ld_cluster_f32x4(o_peer[c] + uoff) : make_float4(0.f, 0.f, 0.f, 0.f);
+        float L = 0.f;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int c = 0; c < kMaxClusterCh; ++c) {
+          const float wc = mlc[c].x > -INFINITY ? exp2f(mlc[c].x - M) : 0.f;
+          L = fmaf(mlc[c].y, wc, L);
+          acc.x = fmaf(x[c].x, wc, acc.x);
+          acc.y = fmaf(x[c].y, wc, acc.y);
+          acc.z = fmaf(x[c].z, wc, acc.z);
+          acc.w = fmaf(x[c].w, wc, acc.w);
+        }
+        const float inv = L > 0.f ? 1.f / L : 0.f;
+        reinterpret_cast<float4*>(p.out + (static_cast<int64_t>(b * p.T + t0 + tr) * p.n_q_heads + g * G + hr) * kD)[lane] =
+            make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+      }
+    }
+    __syncwarp();
+    // no CTA leaves while a peer still reads its rows (the reads are complete once their
+    // sums are stored, so the arrival needs no release)
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;\n\tbarrier.cluster.wait.aligned;" ::: "memory");
   }
 }
 
@@ -567,8 +645,58 @@ PFN_cuTensorMapEncodeTiled_v12000 tc_encoder() {
   return fn;
 }
 
+// Sets the kernel's shared-memory attribute once per device.
 template <int G>
-cudaError_t launch_tc_t(const PrefillAttnParams& p, const void* kc, const void* vc, cudaStream_t s) {
+cudaError_t configure_tc(int dev) {
+  static std::mutex mtx;
+  static bool configured[64] = {};
+  std::lock_guard<std::mutex> lock(mtx);
+  if (!configured[dev]) {
+    const cudaError_t e =
+        cudaFuncSetAttribute(prefill_attn_tc_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmem));
+    if (e != cudaSuccess) return e;
+    configured[dev] = true;
+  }
+  return cudaSuccess;
+}
+
+// Clusters of S CTAs of this kernel the device keeps resident at once (cached per device
+// and S; 0 when they cannot be launched).
+template <int G>
+int active_clusters(int dev, int S) {
+  static std::mutex mtx;
+  static int known[64][kMaxClusterCh + 1];
+  static bool have[64][kMaxClusterCh + 1] = {};
+  if (configure_tc<G>(dev) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  std::lock_guard<std::mutex> lock(mtx);
+  if (!have[dev][S]) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1, S);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = static_cast<unsigned>(S);
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, prefill_attn_tc_kernel<G>, &cfg) != cudaSuccess) {
+      cudaGetLastError();
+      n = 0;
+    }
+    known[dev][S] = n;
+    have[dev][S] = true;
+  }
+  return known[dev][S];
+}
+
+template <int G>
+cudaError_t launch_tc_t(const PrefillAttnParams& p, const void* kc, const void* vc, cudaStream_t s, bool* merged) {
   auto kern = prefill_attn_tc_kernel<G>;
   PFN_cuTensorMapEncodeTiled_v12000 enc = tc_encoder();
   if (enc == nullptr) return cudaErrorNotSupported;
@@ -587,36 +715,62 @@ cudaError_t launch_tc_t(const PrefillAttnParams& p, const void* kc, const void* 
           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
-  static std::mutex mtx;
-  static bool configured[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  {
-    std::lock_guard<std::mutex> lock(mtx);
-    if (!configured[dev]) {
-      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmem));
-      if (e != cudaSuccess) return e;
-      configured[dev] = true;
-    }
-  }
+  e = configure_tc<G>(dev);
+  if (e != cudaSuccess) return e;
   const int items = p.B * p.n_kv_heads * p.n_qb;
-  return launch_pdl(kern, dim3(items, p.n_ch), dim3(kThreads), kSmem, s, kmap, vmap, p);
+  // 2..8 chunks whose clusters (one per item) are all resident at once: merged in the
+  // launch; otherwise one chunk (rows normalised in place) or the combine launch after
+  // this one
+  const bool merge = p.n_ch > 1 && p.n_ch <= kMaxClusterCh && items <= active_clusters<G>(dev, p.n_ch);
+  PrefillAttnParams q = p;
+  q.merge_in_cluster = merge ? 1 : 0;
+  *merged = merge;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(items, p.n_ch);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = 1;
+  attr[1].val.clusterDim.y = static_cast<unsigned>(p.n_ch);
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = merge ? 2 : 1;
+  return cudaLaunchKernelEx(&cfg, kern, kmap, vmap, q);
 }
 
 }  // namespace
+
+int prefill_tc_active_clusters(int group, int S) {
+  int dev = 0;
+  if (S < 2 || S > kMaxClusterCh || cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    cudaGetLastError();
+    return 0;
+  }
+  if (group == 1) return active_clusters<1>(dev, S);
+  if (group == 2) return active_clusters<2>(dev, S);
+  if (group == 4) return active_clusters<4>(dev, S);
+  return 0;
+}
 
 bool prefill_attn_tc_supported(int kv_bf16, int head_dim, int paged, int page_size) {
   return kv_bf16 && head_dim == kD && (!paged || page_size >= kN);
 }
 
 cudaError_t launch_prefill_attn_tc(const PrefillAttnParams& p, const void* k_cache, const void* v_cache, int group,
-                                   cudaStream_t s) {
+                                   cudaStream_t s, bool* merged) {
   if (p.rows != kM) return cudaErrorInvalidValue;
-  if (group == 1) return launch_tc_t<1>(p, k_cache, v_cache, s);
-  if (group == 2) return launch_tc_t<2>(p, k_cache, v_cache, s);
-  if (group == 4) return launch_tc_t<4>(p, k_cache, v_cache, s);
+  *merged = false;
+  if (group == 1) return launch_tc_t<1>(p, k_cache, v_cache, s, merged);
+  if (group == 2) return launch_tc_t<2>(p, k_cache, v_cache, s, merged);
+  if (group == 4) return launch_tc_t<4>(p, k_cache, v_cache, s, merged);
   return cudaErrorInvalidValue;
 }
 

@@ -134,6 +134,19 @@ def test_prefill_split_counts_agree(tts, n_splits):
     assert row_rel_err(out.cpu().numpy().reshape(-1, 16, 128), ref.reshape(-1, 16, 128)) <= ATTN_TOL["f32"]
 
 
+# bf16 caches take the tensor-core kernel: 2..8 chunks whose clusters (one per item) all
+# fit on the device at once merge inside the launch, 1 chunk normalises in place, other
+# counts take the combine launch.  T = 100 gives 16 items of 128 query rows (the second
+# ragged), T = 40 gives 8.
+@pytest.mark.parametrize("T,n_splits", [(100, 1), (100, 2), (100, 5), (100, 8), (100, 9), (100, 16),
+                                        (40, 3), (40, 7), (40, 8)])
+def test_tensor_core_prefill_split_counts(tts, T, n_splits):
+    w = W.workload("talker", layers=1, kv_dtype="bf16")
+    _, _, out, ef, ref, _, _, _ = _run(tts, w, [1500], T, seed=62, n_splits=n_splits)
+    assert ef.item() == 0
+    assert row_rel_err(out.cpu().numpy().reshape(-1, 16, 128), ref.reshape(-1, 16, 128)) <= ATTN_TOL["bf16"]
+
+
 def test_prefill_of_one_row_equals_the_decode_step(tts):
     """T = 1 at start c is the decode step at cur_len c: the same cache bytes, outputs
     within rounding of each other (different kernels: the decode step folds the new row
