@@ -385,6 +385,17 @@ size_t tts_prefill_workspace_size(const tts_kv_desc* d, int32_t T, int32_t n_spl
   return tts_decode_attn_workspace_size(&dq, n_splits);
 }
 
+int32_t tts_prefill_launch_count(const tts_kv_desc* d, int32_t T, int32_t n_splits) {
+  if (check_desc(d) != TTS_OK || T < 1 || static_cast<int64_t>(d->B) * T > 65535) return 0;
+  if (!multi_query_prefill(d, T)) return 2;
+  const int rows = prefill_rows(d), group = d->n_q_heads / d->n_kv_heads;
+  int n_qb = 0, n_ch = 0;
+  prefill_attn_plan(d->B, T, d->n_kv_heads, group, d->capacity, n_splits, sm_count(), rows, n_qb, n_ch);
+  if (n_ch == 1) return 2;
+  const bool merged = rows == 128 && prefill_tc_merges(d->B * d->n_kv_heads * n_qb, group, n_ch);
+  return merged ? 2 : 3;
+}
+
 tts_status tts_prefill_step(float* q, const float* k, const float* v, int64_t row_stride,
                             const float* gamma_q, const float* gamma_k, float eps,
                             const float* rope_cs, int32_t rope_max_pos, void* k_cache,

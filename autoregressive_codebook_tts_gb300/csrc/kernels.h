@@ -220,6 +220,9 @@ size_t prefill_attn_workspace(int B, int T, int n_kv_heads, int group, int head_
 // Clusters of S (2..8) CTAs of the tensor-core kernel the current device keeps resident
 // at once (0 if none or S is out of range).
 int prefill_tc_active_clusters(int group, int S);
+// Whether a tensor-core launch of `items` items in n_ch chunks merges them in clusters
+// (2..8 chunks, every item's cluster resident at once).
+bool prefill_tc_merges(int items, int group, int n_ch);
 // *merged: the chunks were merged inside the launch (no combine launch needed).
 cudaError_t launch_prefill_attn_tc(const PrefillAttnParams& p, const void* k_cache, const void* v_cache, int group,
                                    cudaStream_t s, bool* merged);

@@ -725,7 +725,7 @@ cudaError_t launch_tc_t(const PrefillAttnParams& p, const void* kc, const void* 
   // 2..8 chunks whose clusters (one per item) are all resident at once: merged in the
   // launch; otherwise one chunk (rows normalised in place) or the combine launch after
   // this one
-  const bool merge = p.n_ch > 1 && p.n_ch <= kMaxClusterCh && items <= active_clusters<G>(dev, p.n_ch);
+  const bool merge = prefill_tc_merges(items, G, p.n_ch);
   PrefillAttnParams q = p;
   q.merge_in_cluster = merge ? 1 : 0;
   *merged = merge;
@@ -758,6 +758,10 @@ int prefill_tc_active_clusters(int group, int S) {
   if (group == 2) return active_clusters<2>(dev, S);
   if (group == 4) return active_clusters<4>(dev, S);
   return 0;
+}
+
+bool prefill_tc_merges(int items, int group, int n_ch) {
+  return n_ch > 1 && n_ch <= kMaxClusterCh && items <= prefill_tc_active_clusters(group, n_ch);
 }
 
 bool prefill_attn_tc_supported(int kv_bf16, int head_dim, int paged, int page_size) {

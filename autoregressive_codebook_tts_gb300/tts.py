@@ -40,6 +40,7 @@ EXPORTED = [
     "tts_decode_attn_default_splits", "tts_workspace_init", "tts_decode_attn", "tts_decode_step",
     "tts_decode_step_noalloc",
     "tts_prefill_workspace_size",
+    "tts_prefill_launch_count",
     "tts_prefill_step",
     "tts_sample",
     "tts_sample_embed",
@@ -94,6 +95,7 @@ _sigs = {
     "tts_decode_step_noalloc": ([_P, _P, _P, _I64, _P, _P, _F, _P, _I32, _P, _P,
                                  ctypes.POINTER(TtsKvDesc), _P, _F, _P, _I32, _P, _P], _I32),
     "tts_prefill_workspace_size": ([ctypes.POINTER(TtsKvDesc), _I32, _I32], _SZ),
+    "tts_prefill_launch_count": ([ctypes.POINTER(TtsKvDesc), _I32, _I32], _I32),
     "tts_sample": ([_P, _I64, _I32, _I32, _I32, _F, ctypes.c_uint64, _P, ctypes.c_uint32, _P, _I64, _P],
                    _I32),
     "tts_sample_embed": ([_P, _I64, _I32, _I32, _I32, _F, ctypes.c_uint64, _P, ctypes.c_uint32, _P, _I64,
@@ -283,6 +285,10 @@ def tts_decode_step_noalloc(q, k, v, gamma_q, gamma_k, eps, cs, max_pos, k_cache
 
 def tts_prefill_workspace_size(desc: TtsKvDesc, T: int, n_splits=0) -> int:
     return int(_lib.tts_prefill_workspace_size(ctypes.byref(desc), T, n_splits))
+
+
+def tts_prefill_launch_count(desc: TtsKvDesc, T: int, n_splits=0) -> int:
+    return int(_lib.tts_prefill_launch_count(ctypes.byref(desc), T, n_splits))
 
 
 def prefill_workspace(desc: TtsKvDesc, T: int, n_splits=0, device="cuda", stream=None):

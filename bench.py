@@ -784,7 +784,7 @@ def run_prefill(args, rank, world):
                      "kernel": "tts_prefill_step (rows + attention launches)",
                      "peak_source": "measured HBM copy bandwidth" if peak_kind == "measured"
                      else "fallback HBM copy bandwidth", "bytes_per_launch": hbm},
-        "gpu_launches": 2 * L * args.steps,
+        "gpu_launches": tts.tts_prefill_launch_count(desc, T, args.n_splits) * L * args.steps,
         "clocks": clk,
     }
 

@@ -308,12 +308,19 @@ tts_status tts_decode_step_noalloc(const float* q, const float* k, const float* 
  *        as for tts_decode_attn (its B x T queries take the place of its B streams).
  * Launches on `stream`: the rows, then the attention.  T < 8: the attention runs the
  * B*T queries one by one (as tts_decode_attn).  T >= 8 (and, paged, pages of 8 rows or
- * more): blocks of 64 / (Hq / Hkv) queries of a stream share every K/V tile of their
- * window, the windows cut into chunks; with more than one chunk a third launch merges
- * them in chunk order (that path's workspace needs no zeroing).  B*T must not exceed
- * 65535.
+ * more): blocks of queries of a stream share every K/V tile of their window (bf16
+ * caches with head_dim 128 and contiguous or 64-row-or-larger pages: blocks of
+ * 128 / (Hq / Hkv) queries on the tensor cores; otherwise 64 / (Hq / Hkv) queries on
+ * the CUDA cores), the windows cut into chunks; with more than one chunk a third launch
+ * merges them in chunk order, unless the tensor-core launch merged them itself (2..8
+ * chunks that the device keeps resident as one cluster per block).  That path's
+ * workspace needs no zeroing.  B*T must not exceed 65535.
  * ------------------------------------------------------------------------- */
 size_t tts_prefill_workspace_size(const tts_kv_desc* desc, int32_t T, int32_t n_splits);
+
+/* Kernel launches tts_prefill_step makes for these arguments on the current device (2
+ * or 3); 0 for arguments it would reject as shapes.  For counting a graph's nodes. */
+int32_t tts_prefill_launch_count(const tts_kv_desc* desc, int32_t T, int32_t n_splits);
 
 tts_status tts_prefill_step(float* q, const float* k, const float* v, int64_t row_stride,
                             const float* gamma_q, const float* gamma_k, float eps,

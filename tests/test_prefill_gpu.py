@@ -147,6 +147,19 @@ def test_tensor_core_prefill_split_counts(tts, T, n_splits):
     assert row_rel_err(out.cpu().numpy().reshape(-1, 16, 128), ref.reshape(-1, 16, 128)) <= ATTN_TOL["bf16"]
 
 
+def test_prefill_launch_count(tts):
+    # the rows and the attention, plus the combine when chunks are merged by a third launch
+    w = W.workload("talker", layers=1)
+    d16, d32 = (tts.kv_desc(w.B, w.n_q_heads, w.n_kv_heads, w.head_dim, w.capacity, dt,
+                            window_quantum=w.window_quantum) for dt in ("bf16", "f32"))
+    assert tts.tts_prefill_launch_count(d16, 2) == 2          # per-query decode path
+    assert tts.tts_prefill_launch_count(d32, 24, 1) == 2      # one chunk
+    assert tts.tts_prefill_launch_count(d32, 24, 3) == 3      # CUDA cores: combine launch
+    assert tts.tts_prefill_launch_count(d16, 100, 16) == 3    # more than 8 chunks
+    assert tts.tts_prefill_launch_count(d16, 100, 2) == 2     # 16 clusters of 2 fit at once
+    assert tts.tts_prefill_launch_count(d16, 0) == 0
+
+
 def test_prefill_of_one_row_equals_the_decode_step(tts):
     """T = 1 at start c is the decode step at cur_len c: the same cache bytes, outputs
     within rounding of each other (different kernels: the decode step folds the new row
