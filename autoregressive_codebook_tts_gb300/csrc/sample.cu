@@ -4,11 +4,17 @@
 //
 // One CTA per stream.  The logits row is staged in shared memory as order-preserving
 // integer keys; the k-th largest is found by a radix selection (four 8-bit passes of
-// a shared-memory histogram), the top_k candidates gathered (ties at the threshold by
-// lowest index) and ordered by rank (larger logit first, lower index first).  Each
-// candidate's weight 2^((l_i - l_0) * log2(e) / T) is computed by its own thread;
-// thread 0 walks the running sum against u * sum, u from Philox4x64-10 at counter words
-// (counter, stream, draw, 0) and key (seed, 0).
+// a shared-memory histogram, three barriers a pass).  After the first pass one scan of
+// the row takes every key whose top byte is above the selected digit as a candidate and
+// lists the indices of those with the selected top byte; the other three passes and the
+// rest of the gather run over that list only.  Ties at the threshold go to the lowest
+// indices (the last pass's count of keys equal to the threshold says whether there is a
+// tie to break at all).  The candidates are ordered by rank (larger logit first, lower
+// index first).  Each candidate's weight 2^((l_i - l_0) * log2(e) / T)
+// is computed by its own thread; thread 0 forms the running sums in order while thread
+// 32 draws u from Philox4x64-10 at counter words (counter, stream, draw, 0) and key
+// (seed, 0); the token is the first candidate whose running sum exceeds u * sum (the
+// running sums do not decrease, so every thread can test its own).
 // Every value that decides the token is computed in f32 in a fixed order with explicit
 // round-to-nearest operations (no contraction into fused multiply-adds); the
 // exponential is this file's own (a degree-9 Taylor polynomial of 2^f, f in [0, 1),
@@ -80,6 +86,7 @@ __device__ __forceinline__ bool key_ahead(uint32_t ka, int ia, uint32_t kb, int 
 }
 
 constexpr int kChunk = TTS_MAX_SAMPLE_VOCAB / kSampleThreads;  // indices per thread, at most
+static_assert(TTS_MAX_TOP_K % 16 == 0 && TTS_MAX_TOP_K <= kSampleThreads, "running sums are formed 16 at a time");
 
 // Inclusive sum of v over threads 0..tid of the block (kSampleThreads threads, all of
 // them calling); s_part holds kSampleWarps ints of scratch.
@@ -118,16 +125,18 @@ __device__ __forceinline__ void gather_row(const SampleParams& p, int b, volatil
 }
 
 __global__ void __launch_bounds__(kSampleThreads) sample_kernel(const SampleParams p) {
-  extern __shared__ uint32_t s_key[];  // the row as keys
-  __shared__ int s_hist[256];
-  __shared__ int s_sel[2];             // chosen digit, keys still to take at the threshold
+  extern __shared__ uint32_t s_key[];  // the row as keys, then (top_k >= 2) V ints of index list
+  __shared__ int s_hist[kSampleWarps][256];  // per-warp digit counts of a pass
+  __shared__ int s_sel[2][3];          // per pass parity: digit, keys still to take, bin count
   __shared__ int s_part[kSampleWarps];
-  __shared__ int s_n;
-  __shared__ uint32_t s_ck[TTS_MAX_TOP_K];
-  __shared__ int s_ci[TTS_MAX_TOP_K];
-  __shared__ uint32_t s_sk[TTS_MAX_TOP_K];
-  __shared__ int s_si[TTS_MAX_TOP_K];
-  __shared__ float s_w[TTS_MAX_TOP_K];
+  __shared__ int s_n, s_m;
+  __shared__ uint2 s_cand[TTS_MAX_TOP_K];    // (key, index), in any order
+  __shared__ uint2 s_sorted[TTS_MAX_TOP_K];  // the same, by rank
+  __shared__ __align__(16) float s_w[TTS_MAX_TOP_K];
+  __shared__ __align__(16) float s_acc[TTS_MAX_TOP_K];  // running sums of the weights, in order
+  __shared__ int s_wc[2][kSampleWarps];      // per-warp counts of a two-phase compaction
+  __shared__ float s_u;
+  __shared__ int s_first;
   __shared__ uint32_t s_wk[kSampleWarps];
   __shared__ int s_wi[kSampleWarps];
   __shared__ int s_pick;
@@ -143,6 +152,14 @@ __global__ void __launch_bounds__(kSampleThreads) sample_kernel(const SamplePara
     if (v == 0.0f) v = 0.0f;    // -0 and +0 are the same logit
     s_key[i] = float_key(v);
   }
+#pragma unroll
+  for (int w = 0; w < kSampleWarps; ++w) s_hist[w][255 - tid] = 0;  // thread t owns bin 255 - t
+  if (tid == 0) {
+    s_n = 0;
+    s_m = 0;
+  }
+  // the draw's counter value, read early (its latency hides under the selection)
+  const uint64_t ctr0 = (tid == 32 && p.top_k > 1) ? __ldcg(p.counter) : 0ull;
   __syncthreads();
 
   if (p.top_k <= 1) {
@@ -185,95 +202,200 @@ __global__ void __launch_bounds__(kSampleThreads) sample_kernel(const SamplePara
 
   // The k-th largest key by radix selection, 8 bits a pass from the top: `prefix`
   // holds the digits fixed so far, `need` how many keys with that prefix are still to
-  // take.  After the last pass, `prefix` is the threshold key and `need` how many of
-  // the keys equal to it belong to the top k (the lowest-index ones).
+  // take.  After the last pass, `prefix` is the threshold key, `need` how many of the
+  // keys equal to it belong to the top k (the lowest-index ones) and `n_eq` how many
+  // keys equal it.
   const int k = p.top_k;
+  int* s_list = reinterpret_cast<int*>(s_key + V);  // indices whose keys share the fixed digits
   uint32_t prefix = 0, mask = 0;
-  int need = k;
-  for (int shift = 24; shift >= 0; shift -= 8) {
-    s_hist[tid] = 0;  // 256 threads, 256 bins
-    __syncthreads();
-    // keys that match the digits fixed so far, counted per next digit; lanes with the
-    // same digit add once (their count) instead of each contending for the bin
-    for (int base = 0; base < V; base += kSampleThreads) {
-      const int i = base + tid;
-      const uint32_t key = i < V ? s_key[i] : 0u;
-      const bool in = i < V && (key & mask) == prefix;
-      const uint32_t bin = (key >> shift) & 255u;
-      const unsigned peers = __match_any_sync(kFull, in ? bin : 0xFFFFFFFFu);
-      if (in && lane == __ffs(peers) - 1) atomicAdd(&s_hist[bin], __popc(peers));
+  int need = k, n_eq = 0, n_list = V;
+  for (int pass = 0; pass < 4; ++pass) {
+    const int shift = 24 - 8 * pass;
+    // keys that match the digits fixed so far (pass 0: the whole row; later: the list),
+    // counted per next digit in the warp's own histogram
+    int* hw = s_hist[warp];
+    for (int base = 0; base < n_list; base += kSampleThreads) {
+      const int j = base + tid;
+      if (j < n_list) {
+        const uint32_t key = s_key[pass == 0 ? j : s_list[j]];
+        if ((key & mask) == prefix) atomicAdd(&hw[(key >> shift) & 255u], 1);
+      }
     }
     __syncthreads();
     // the digit d with (keys in bins above d) < need <= (keys in bins from d up):
-    // thread t holds bin 255 - t, so its inclusive sum counts the bins from it upward
-    const int c = s_hist[255 - tid];
-    const int incl = block_inclusive_sum(c, s_part);
+    // thread t holds bin 255 - t (summed over the warps' histograms, which it then
+    // clears for the next pass: no other thread reads them), so its inclusive sum
+    // counts the bins from it upward
+    int c = 0;
+#pragma unroll
+    for (int w = 0; w < kSampleWarps; ++w) {
+      c += s_hist[w][255 - tid];
+      s_hist[w][255 - tid] = 0;
+    }
+    int incl = c;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int o = __shfl_up_sync(kFull, incl, off);
+      if (lane >= off) incl += o;
+    }
+    if (lane == 31) s_part[warp] = incl;
+    __syncthreads();
+#pragma unroll
+    for (int w = 0; w < kSampleWarps; ++w) incl += w < warp ? s_part[w] : 0;
     const int excl = incl - c;
     if (excl < need && incl >= need) {
-      s_sel[0] = 255 - tid;
-      s_sel[1] = need - excl;
+      s_sel[pass & 1][0] = 255 - tid;
+      s_sel[pass & 1][1] = need - excl;
+      s_sel[pass & 1][2] = c;
     }
     __syncthreads();
-    prefix |= static_cast<uint32_t>(s_sel[0]) << shift;
+    prefix |= static_cast<uint32_t>(s_sel[pass & 1][0]) << shift;
     mask |= 255u << shift;
-    need = s_sel[1];
-    __syncthreads();
+    need = s_sel[pass & 1][1];
+    n_eq = s_sel[pass & 1][2];
+    if (pass == 0) {
+      // one scan of the row: keys whose top byte is above the digit are candidates
+      // already; the indices of those with the digit form the list of the next passes.
+      // Two phases without atomics: each warp counts its keys of either kind, then
+      // writes them from its offset (warps in order, lanes in order within a ballot).
+      const uint32_t d0 = prefix >> 24;
+      int na = 0, ns = 0;
+      for (int base = 0; base < V; base += kSampleThreads) {
+        const int i = base + tid;
+        const uint32_t top = i < V ? s_key[i] >> 24 : 0u;
+        na += __popc(__ballot_sync(kFull, i < V && top > d0));
+        ns += __popc(__ballot_sync(kFull, i < V && top == d0));
+      }
+      if (lane == 0) {
+        s_wc[0][warp] = na;
+        s_wc[1][warp] = ns;
+      }
+      __syncthreads();
+      int oa = 0, os = 0;
+#pragma unroll
+      for (int w = 0; w < kSampleWarps; ++w) {
+        oa += w < warp ? s_wc[0][w] : 0;
+        os += w < warp ? s_wc[1][w] : 0;
+      }
+      const unsigned below = (1u << lane) - 1u;
+      for (int base = 0; base < V; base += kSampleThreads) {
+        const int i = base + tid;
+        const uint32_t key = i < V ? s_key[i] : 0u;
+        const uint32_t top = key >> 24;
+        const bool above = i < V && top > d0, same = i < V && top == d0;
+        const unsigned ba = __ballot_sync(kFull, above), bs = __ballot_sync(kFull, same);
+        if (above) s_cand[oa + __popc(ba & below)] = make_uint2(key, static_cast<uint32_t>(i));
+        if (same) s_list[os + __popc(bs & below)] = i;
+        oa += __popc(ba);
+        os += __popc(bs);
+      }
+      if (tid == 0) {
+        int ta = 0, ts = 0;
+        for (int w = 0; w < kSampleWarps; ++w) {
+          ta += s_wc[0][w];
+          ts += s_wc[1][w];
+        }
+        s_n = ta;
+        s_m = ts;
+      }
+      __syncthreads();
+      n_list = s_m;
+    }
   }
-  // Gather the k candidates: every key above the threshold, and the `need` lowest
-  // indices of those equal to it (each thread owns a contiguous index range, so an
-  // exclusive scan of the per-thread counts ranks the equal keys by index).
-  const int i0 = tid * kChunk;
-  const int i1 = min(i0 + kChunk, V);
-  int eq = 0;
-  for (int i = i0; i < i1; ++i) eq += s_key[i] == prefix;
-  if (tid == 0) s_n = 0;
-  int rank = block_inclusive_sum(eq, s_part) - eq;  // equal keys at lower indices
-  for (int i = i0; i < i1; ++i) {
-    const uint32_t key = s_key[i];
-    bool take = key > prefix;
-    if (key == prefix) take = rank++ < need;
-    if (take) {
-      const int slot = atomicAdd(&s_n, 1);
-      s_ck[slot] = key;
-      s_ci[slot] = i;
+  // The rest of the candidates: every listed key above the threshold and the `need`
+  // lowest indices of those equal to it.
+  if (n_eq == need) {
+    // no tie to break: the listed keys at or above the threshold
+    for (int base = 0; base < n_list; base += kSampleThreads) {
+      const int j = base + tid;
+      const int i = j < n_list ? s_list[j] : 0;
+      const uint32_t key = j < n_list ? s_key[i] : 0u;
+      const bool take = j < n_list && key >= prefix;
+      const unsigned bal = __ballot_sync(kFull, take);
+      int slot0 = 0;
+      if (lane == 0 && bal != 0u) slot0 = atomicAdd(&s_n, __popc(bal));
+      slot0 = __shfl_sync(kFull, slot0, 0);
+      if (take) s_cand[slot0 + __popc(bal & ((1u << lane) - 1u))] = make_uint2(key, static_cast<uint32_t>(i));
+    }
+  } else {
+    // ties at the threshold (rare): start over on the whole row; each thread owns a
+    // contiguous index range, so an exclusive scan of the per-thread counts ranks the
+    // equal keys by index
+    __syncthreads();
+    if (tid == 0) s_n = 0;
+    const int i0 = tid * kChunk;
+    const int i1 = min(i0 + kChunk, V);
+    int eq = 0;
+    for (int i = i0; i < i1; ++i) eq += s_key[i] == prefix;
+    int rank = block_inclusive_sum(eq, s_part) - eq;  // equal keys at lower indices (also a barrier)
+    for (int i = i0; i < i1; ++i) {
+      const uint32_t key = s_key[i];
+      bool take = key > prefix;
+      if (key == prefix) take = rank++ < need;
+      if (take) s_cand[atomicAdd(&s_n, 1)] = make_uint2(key, static_cast<uint32_t>(i));
     }
   }
   __syncthreads();
   // Order them (larger key first, lower index first) by rank, and weigh them.
-  if (tid < k) {
-    const uint32_t mk = s_ck[tid];
-    const int mi = s_ci[tid];
+  if (tid < TTS_MAX_TOP_K) {
+    // a candidate's rank: how many others are ahead of it (entries past k are not read
+    // as candidates: their comparisons are masked)
+    const uint2 me = tid < k ? s_cand[tid] : make_uint2(0u, 0u);
     int r = 0;
-    for (int j = 0; j < k; ++j) r += key_ahead(s_ck[j], s_ci[j], mk, mi);
-    s_sk[r] = mk;
-    s_si[r] = mi;
-  }
-  __syncthreads();
-  const float m = key_float(s_sk[0]);
-  const bool finite_top = m > -INFINITY && m < INFINITY;
-  if (tid < k && finite_top) s_w[tid] = exp2_f32(__fmul_rn(__fsub_rn(key_float(s_sk[tid]), m), p.c));
-  __syncthreads();
-  if (tid == 0) {
-  int pick = 0;
-  if (finite_top) {
-    float S = 0.0f;
-    for (int j = 0; j < k; ++j) S = __fadd_rn(S, s_w[j]);
-    uint64_t ctr[4] = {__ldcg(p.counter), static_cast<uint64_t>(b), static_cast<uint64_t>(p.draw), 0ull};
-    philox4x64_10(ctr, p.seed, 0ull);
-    const float u = static_cast<float>(ctr[0] >> 40) * 0x1.0p-24f;  // exact
-    const float r = __fmul_rn(u, S);
-    float acc = 0.0f;
-    pick = k - 1;
-    for (int j = 0; j < k; ++j) {
-      acc = __fadd_rn(acc, s_w[j]);
-      if (acc > r) {
-        pick = j;
-        break;
-      }
+#pragma unroll 16
+    for (int j = 0; j < TTS_MAX_TOP_K; ++j) {
+      const uint2 o = s_cand[j];
+      const bool ahead = (o.x > me.x) | ((o.x == me.x) & (o.y < me.y));
+      r += static_cast<int>((j < k) & ahead);
     }
+    if (tid < k) s_sorted[r] = me;
   }
-  p.out[static_cast<int64_t>(b) * p.out_stride] = s_si[pick];
-  s_pick = s_si[pick];
+  __syncthreads();
+  const float m = key_float(s_sorted[0].x);
+  const bool finite_top = m > -INFINITY && m < INFINITY;
+  if (tid < k && finite_top) s_w[tid] = exp2_f32(__fmul_rn(__fsub_rn(key_float(s_sorted[tid].x), m), p.c));
+  if (tid == 0) s_first = k - 1;
+  __syncthreads();
+  if (finite_top) {
+    if (tid == 0) {
+      // the running sums in candidate order (the weights read into registers first);
+      // the last is the total
+      float acc = 0.0f;
+      for (int j0 = 0; j0 < k; j0 += 16) {
+        float w[16];
+#pragma unroll
+        for (int j = 0; j < 16; j += 4) {
+          const float4 v = *reinterpret_cast<const float4*>(s_w + j0 + j);
+          w[j] = v.x;
+          w[j + 1] = v.y;
+          w[j + 2] = v.z;
+          w[j + 3] = v.w;
+        }
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          if (j0 + j < k) acc = __fadd_rn(acc, w[j]);
+          w[j] = acc;
+        }
+#pragma unroll
+        for (int j = 0; j < 16; j += 4)
+          *reinterpret_cast<float4*>(s_acc + j0 + j) = make_float4(w[j], w[j + 1], w[j + 2], w[j + 3]);
+      }
+    } else if (tid == 32) {
+      uint64_t ctr[4] = {ctr0, static_cast<uint64_t>(b), static_cast<uint64_t>(p.draw), 0ull};
+      philox4x64_10(ctr, p.seed, 0ull);
+      s_u = static_cast<float>(ctr[0] >> 40) * 0x1.0p-24f;  // exact
+    }
+    __syncthreads();
+    // the first candidate whose running sum exceeds u * total (the last if none does)
+    const float r = __fmul_rn(s_u, s_acc[k - 1]);
+    if (tid < k && s_acc[tid] > r && (tid == 0 || !(s_acc[tid - 1] > r))) s_first = tid;
+    __syncthreads();
+  }
+  if (tid == 0) {
+    const int pick = finite_top ? s_first : 0;
+    const int id = static_cast<int>(s_sorted[pick].y);
+    p.out[static_cast<int64_t>(b) * p.out_stride] = id;
+    s_pick = id;
   }
   gather_row(p, b, s_pick);
 }
@@ -287,7 +409,8 @@ __global__ void counter_advance_kernel(uint64_t* counter, uint64_t by) {
 }  // namespace
 
 cudaError_t launch_sample(const SampleParams& p, cudaStream_t s) {
-  const size_t smem = static_cast<size_t>(p.V) * sizeof(float);
+  // the keys, and for top_k >= 2 the index list after them
+  const size_t smem = static_cast<size_t>(p.V) * sizeof(uint32_t) * (p.top_k > 1 ? 2 : 1);
   static std::mutex cfg_mutex;  // launches may come from several host threads
   static int configured_for = -1;
   int dev = 0;
@@ -297,7 +420,7 @@ cudaError_t launch_sample(const SampleParams& p, cudaStream_t s) {
     std::lock_guard<std::mutex> cfg_lock(cfg_mutex);
     if (configured_for != dev) {
       e = cudaFuncSetAttribute(sample_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(TTS_MAX_SAMPLE_VOCAB * sizeof(float)));
+                               static_cast<int>(2 * TTS_MAX_SAMPLE_VOCAB * sizeof(uint32_t)));
       if (e != cudaSuccess) return e;
       configured_for = dev;
     }

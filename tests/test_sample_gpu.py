@@ -58,6 +58,24 @@ def test_sample_ties_nan_and_empty_rows(tts):
     assert ref[1] == 0
 
 
+@pytest.mark.parametrize("top_k", [2, 8, 50, 64])
+def test_sample_ties_at_the_threshold(tts, top_k):
+    # logits on a grid of quarter steps: many keys equal the k-th largest, so the lowest
+    # indices among them must be the ones taken (an odd vocab, not a multiple of 256)
+    B, V = 16, 777
+    lg = torch.round(_logits(B, V, 9) * 2.0) / 4.0
+    lg[0, :] = 1.0                       # every key ties
+    lg[1, :] = 0.0
+    lg[1, 700:] = 2.0                    # 77 equal maxima, more than any top_k
+    for c in range(4):
+        out = torch.full((B,), -1, dtype=torch.int32, device="cuda")
+        counter = torch.full((1,), c, dtype=torch.int64, device="cuda")
+        tts.tts_sample(lg.cuda(), top_k, 0.8, 99, counter, out)
+        torch.cuda.synchronize()
+        ref = oracle.sample(lg.numpy(), top_k, 0.8, 99, c)
+        assert np.array_equal(out.cpu().numpy(), ref), (top_k, c)
+
+
 def test_sample_writes_a_column_of_the_ids_buffer(tts):
     """Strided logits rows (a slice of a wider buffer) in, one column of a [B][16] code
     id buffer out; the other columns untouched."""
