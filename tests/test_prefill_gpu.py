@@ -86,8 +86,10 @@ def _check_caches(L, w, start, T, kc, vc):
         assert (np.abs(got - ref)[mask] <= bound[mask]).all()
 
 
-# Prompts of 8 rows or more take the multi-query kernel (blocks of 64 / G queries
-# sharing every K/V tile), shorter ones the per-query decode path.  The multi-query
+# Prompts of 8 rows or more take a multi-query kernel (blocks of queries sharing every
+# K/V tile: 128 / G on the tensor cores for bf16 caches with head_dim 128 and contiguous
+# or 64-row-or-larger pages, 64 / G on the CUDA cores otherwise), shorter ones the
+# per-query decode path.  The multi-query
 # cases cover f32 and bf16, head_dim 64 and 128, GQA groups 1, 2 and 4, a ragged last
 # query block (T = 130 in blocks of 64, T = 17 in blocks of 16), contiguous caches and
 # pages of 8, 16, 64 and 128 rows (one tile split over pages, one box per page, two
@@ -107,6 +109,11 @@ CASES = [
     ("paged", dict(B=2, layers=1, page_size=64, n_pages=200), [100, 1000], 70),
     ("paged", dict(B=2, layers=1, page_size=128, n_pages=100, kv_dtype="f32"), [0, 2000], 24),
     ("paged", dict(B=2, layers=1, page_size=8, n_pages=300, capacity=1024), [500, 900], 32),
+    # bf16, head_dim 128 on the tensor cores with GQA groups 1 and 4 (blocks of 128 and
+    # 32 queries, the last ragged), contiguous and 64-row pages
+    ("batched", dict(B=2, layers=1, n_kv_heads=16, capacity=2048), [100, 1000], 140),
+    ("batched", dict(B=2, layers=1, n_kv_heads=4, capacity=2048), [50, 1900], 70),
+    ("paged", dict(B=2, layers=1, n_kv_heads=4, page_size=64, n_pages=200), [300, 2000], 45),
 ]
 
 
