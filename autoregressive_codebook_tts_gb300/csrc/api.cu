@@ -333,14 +333,21 @@ tts_status tts_decode_attn(const float* q, int64_t q_row_stride, const void* k_c
                                       d->n_q_heads / d->n_kv_heads, false, as_stream(stream)));
 }
 
-tts_status tts_decode_step(const float* q, const float* k, const float* v, int64_t row_stride,
-                           const float* gamma_q, const float* gamma_k, float eps,
-                           const float* rope_cs, int32_t rope_max_pos, void* k_cache,
-                           void* v_cache, const tts_kv_desc* d, const int32_t* cur_len,
-                           float scale, float* out, void* workspace, size_t ws_bytes,
-                           int32_t n_splits, int32_t* err_flag, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// The fused step; with `packed` non-null the output goes there instead of `out`, rounded to
+// bf16 in the tensor-core projection's input layout [Hq D / 8][slots][8] (the decode layer's
+// o projection then reads it without a packing launch).
+tts_status decode_step_impl(const float* q, const float* k, const float* v, int64_t row_stride,
+                            const float* gamma_q, const float* gamma_k, float eps,
+                            const float* rope_cs, int32_t rope_max_pos, void* k_cache,
+                            void* v_cache, const tts_kv_desc* d, const int32_t* cur_len,
+                            float scale, float* out, __nv_bfloat16* packed, int slots, void* workspace,
+                            size_t ws_bytes, int32_t n_splits, int32_t* err_flag, void* stream) {
   if (q == nullptr || k == nullptr || v == nullptr || gamma_q == nullptr || gamma_k == nullptr ||
-      rope_cs == nullptr || cur_len == nullptr || out == nullptr)
+      rope_cs == nullptr || cur_len == nullptr || (out == nullptr && packed == nullptr))
     return TTS_ERR_NULL;
   AttnParams p = {};
   int used = 0;
@@ -348,8 +355,8 @@ tts_status tts_decode_step(const float* q, const float* k, const float* v, int64
   if (st != TTS_OK) return st;
   if (row_stride < static_cast<int64_t>(d->n_q_heads) * d->head_dim || rope_max_pos < 1 || !(eps >= 0.f))
     return TTS_ERR_SHAPE;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(gamma_q) ||
-      !aligned16(gamma_k) || !aligned16(rope_cs) || row_stride % 4 != 0)
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(packed) ||
+      !aligned16(gamma_q) || !aligned16(gamma_k) || !aligned16(rope_cs) || row_stride % 4 != 0)
     return TTS_ERR_ALIGN;
   if (!std::isfinite(scale)) return TTS_ERR_SHAPE;
   p.q = q;
@@ -367,9 +374,26 @@ tts_status tts_decode_step(const float* q, const float* k, const float* v, int64
   p.lens = cur_len;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.out = out;
+  p.out_packed = packed;
+  p.out_slots = slots;
   p.err = err_flag;
   return from_cuda(launch_decode_attn(p, d->kv_dtype == TTS_BF16, d->head_dim,
                                       d->n_q_heads / d->n_kv_heads, true, as_stream(stream)));
+}
+
+}  // namespace
+
+extern "C" {
+
+tts_status tts_decode_step(const float* q, const float* k, const float* v, int64_t row_stride,
+                           const float* gamma_q, const float* gamma_k, float eps,
+                           const float* rope_cs, int32_t rope_max_pos, void* k_cache,
+                           void* v_cache, const tts_kv_desc* d, const int32_t* cur_len,
+                           float scale, float* out, void* workspace, size_t ws_bytes,
+                           int32_t n_splits, int32_t* err_flag, void* stream) {
+  if (out == nullptr) return TTS_ERR_NULL;
+  return decode_step_impl(q, k, v, row_stride, gamma_q, gamma_k, eps, rope_cs, rope_max_pos, k_cache, v_cache, d,
+                          cur_len, scale, out, nullptr, 0, workspace, ws_bytes, n_splits, err_flag, stream);
 }
 
 size_t tts_prefill_workspace_size(const tts_kv_desc* d, int32_t T, int32_t n_splits) {
@@ -629,6 +653,13 @@ size_t tts_decode_layer_scratch_size(const tts_kv_desc* d, int32_t hidden, int32
   return layer_scratch(d, hidden, inter, n_splits).total;
 }
 
+int32_t tts_decode_layer_launch_count(const tts_kv_desc* d) {
+  if (check_desc(d) != TTS_OK || d->B > kGemvMmaMaxB) return 0;
+  // tensor cores: two norm packs, four projections, the decode step; CUDA cores: the
+  // projections norm their own inputs
+  return d->B >= kMmaMinStreams ? 7 : 5;
+}
+
 tts_status tts_decode_layer(float* h, const tts_layer_weights* w, float eps, const float* rope_cs,
                             int32_t rope_max_pos, void* k_cache, void* v_cache, const tts_kv_desc* d,
                             const int32_t* cur_len, float scale, void* scratch, size_t scratch_bytes,
@@ -678,15 +709,20 @@ tts_status tts_decode_layer(float* h, const tts_layer_weights* w, float eps, con
     const int standalone = tts_decode_attn_default_splits(d);
     if (splits > standalone) splits = standalone;
   }
-  st = tts_decode_step(qkv, qkv + qd, qkv + qd + kd, width, w->gamma_q, w->gamma_k, eps, rope_cs,
-                       rope_max_pos, k_cache, v_cache, d, cur_len, scale, attn, sc + L.ws_off,
-                       L.total - L.ws_off, splits, err_flag, stream);
+  // on the tensor-core path the attention writes its output already packed for the o
+  // projection (bf16, the projection's input layout), so that projection needs no pack
+  const bool packed = B >= kMmaMinStreams;
+  __nv_bfloat16* xp = reinterpret_cast<__nv_bfloat16*>(sc + L.xp_off);
+  st = decode_step_impl(qkv, qkv + qd, qkv + qd + kd, width, w->gamma_q, w->gamma_k, eps, rope_cs,
+                        rope_max_pos, k_cache, v_cache, d, cur_len, scale, packed ? nullptr : attn,
+                        packed ? xp : nullptr, packed ? gemv_mma_slots(B) : 0, sc + L.ws_off,
+                        L.total - L.ws_off, splits, err_flag, stream);
   if (st != TTS_OK) return st;
   // h += bf16(attn) W_o^T
   g = {};
-  g.x = attn; g.x_stride = qd; g.w = w->w_o; g.n_out = H; g.K = qd; g.B = B; g.y = h; g.y_stride = H;
-  g.err = err_flag;
-  if ((e = gemv(g, 1, 1)) != cudaSuccess) return from_cuda(e);
+  g.x = packed ? static_cast<const void*>(xp) : attn; g.x_stride = qd; g.w = w->w_o; g.n_out = H; g.K = qd;
+  g.B = B; g.y = h; g.y_stride = H; g.err = err_flag;
+  if ((e = gemv(g, packed ? 0 : 1, 1)) != cudaSuccess) return from_cuda(e);
   // a = bf16(silu(x W_gate^T) * x W_up^T), x = bf16(rmsnorm(h))
   g = {};
   g.x = h; g.x_stride = H; g.gamma = w->gamma_mlp; g.eps = eps;

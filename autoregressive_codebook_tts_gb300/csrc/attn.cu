@@ -401,6 +401,20 @@ __device__ __forceinline__ void tile_softmax_pv(const unsigned char* __restrict_
   }
 }
 
+// The packed projection input: column k of stream b at element (k / 8, b, k % 8) of
+// [K / 8][slots][8] bf16 (round to nearest even, as the projection's own packing does).
+__device__ __forceinline__ void store_packed1(__nv_bfloat16* xp, int slots, int b, int k, float v) {
+  xp[(static_cast<int64_t>(k >> 3) * slots + b) * 8 + (k & 7)] = __float2bfloat16_rn(v);
+}
+__device__ __forceinline__ void store_packed4(__nv_bfloat16* xp, int slots, int b, int k, float4 v) {
+  // k is a multiple of 4: the four values are half of one 16-byte group
+  const __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
+  uint2 u;
+  u.x = *reinterpret_cast<const uint32_t*>(&lo);
+  u.y = *reinterpret_cast<const uint32_t*>(&hi);
+  *reinterpret_cast<uint2*>(xp + (static_cast<int64_t>(k >> 3) * slots + b) * 8 + (k & 7)) = u;
+}
+
 // Log-sum-exp merge of the n_act split partials of one (stream, kv head), run by the
 // NT consumer threads of the CTA that took the last ticket.  The (m, l) pairs and the
 // first batch of output partials are requested together; per-head maxima and sums use
@@ -498,8 +512,13 @@ __device__ __forceinline__ void combine_splits(const AttnParams& p, int b, int g
       acc.x += a.x; acc.y += a.y; acc.z += a.z; acc.w += a.w;
     }
     const float L = sm_L[h];
-    reinterpret_cast<float4*>(p.out + (head0 + h) * D)[d4] =
-        make_float4(acc.x / L, acc.y / L, acc.z / L, acc.w / L);
+    const float4 o4 = make_float4(acc.x / L, acc.y / L, acc.z / L, acc.w / L);
+    if (p.out_packed == nullptr) {
+      reinterpret_cast<float4*>(p.out + (head0 + h) * D)[d4] = o4;
+    } else {
+      const int k = (g * G + h) * D + d4 * 4;  // column of the stream's output row
+      store_packed4(p.out_packed, p.out_slots, b, k, o4);
+    }
   }
 }
 
@@ -1305,7 +1324,8 @@ decode_attn_kernel(const AttnParams p) {
       }
       const int hq = g * G + h;
       if (direct) {
-        p.out[(static_cast<int64_t>(b) * Hq + hq) * D + d] = O / L;
+        if (p.out_packed == nullptr) p.out[(static_cast<int64_t>(b) * Hq + hq) * D + d] = O / L;
+        else store_packed1(p.out_packed, p.out_slots, b, hq * D + d, O / L);
       } else if (clustered) {
         float* slot = gather + (split * G + h) * (D + 2);
         if (split == 0) {
@@ -1365,7 +1385,8 @@ decode_attn_kernel(const AttnParams p) {
           float O = 0.f;
 #pragma unroll 4
           for (int s2 = 0; s2 < n_act; ++s2) O = fmaf(gather[(s2 * G + h) * (D + 2) + d], sm_w[h * 16 + s2], O);
-          p.out[(static_cast<int64_t>(b) * Hq + g * G + h) * D + d] = O / sm_w[G * 16 + h];
+          if (p.out_packed == nullptr) p.out[(static_cast<int64_t>(b) * Hq + g * G + h) * D + d] = O / sm_w[G * 16 + h];
+          else store_packed1(p.out_packed, p.out_slots, b, (g * G + h) * D + d, O / sm_w[G * 16 + h]);
         }
         if (tid == 0) { if (persistent) TTS_STAMP_ITEM(7, i); else TTS_STAMP(7); }
       }

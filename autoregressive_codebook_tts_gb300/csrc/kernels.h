@@ -3,6 +3,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include "../../include/tts_decode.h"
@@ -76,6 +77,10 @@ struct AttnParams {
   int q_per_stream, lens_add;
   float scale_log2;     // softmax scale * log2(e)
   float* out;
+  // optional: the output rounded to bf16 in the projection input layout
+  // [Hq D / 8][out_slots][8] (the stream's slot b), written instead of `out`
+  __nv_bfloat16* out_packed;
+  int out_slots;
   float* ws_o;          // [B][Hq][n_splits][D]
   float* ws_ml;         // [B][Hq][n_splits][2]
   int* ws_cnt;          // [B][Hkv] split tickets

@@ -47,6 +47,7 @@ EXPORTED = [
     "tts_counter_advance",
     "tts_check_wait_timeout",
     "tts_decode_layer_scratch_size",
+    "tts_decode_layer_launch_count",
     "tts_decode_layer",
 ]
 
@@ -103,6 +104,7 @@ _sigs = {
     "tts_counter_advance": ([_P, ctypes.c_uint64, _P], _I32),
     "tts_check_wait_timeout": ([_P, _P], _I32),
     "tts_decode_layer_scratch_size": ([ctypes.POINTER(TtsKvDesc), _I32, _I32, _I32], _SZ),
+    "tts_decode_layer_launch_count": ([ctypes.POINTER(TtsKvDesc)], _I32),
     "tts_decode_layer": ([_P, ctypes.POINTER(TtsLayerWeights), _F, _P, _I32, _P, _P,
                           ctypes.POINTER(TtsKvDesc), _P, _F, _P, _SZ, _I32, _P, _P], _I32),
     "tts_prefill_step": ([_P, _P, _P, _I64, _P, _P, _F, _P, _I32, _P, _P,
@@ -360,6 +362,10 @@ def layer_weights(w_qkv, w_o, w_gu, w_down, gamma_attn, gamma_mlp, gamma_q, gamm
     t.hidden = w_qkv.shape[1]
     t.inter = w_down.shape[1]
     return t
+
+
+def tts_decode_layer_launch_count(desc: TtsKvDesc) -> int:
+    return int(_lib.tts_decode_layer_launch_count(ctypes.byref(desc)))
 
 
 def tts_decode_layer_scratch_size(desc: TtsKvDesc, hidden, inter, n_splits=0) -> int:

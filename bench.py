@@ -1019,7 +1019,7 @@ def run_layer(args, rank, world):
                      "kernel": "whole frame (GEMVs and the decode step)",
                      "peak_source": "measured HBM copy bandwidth" if peak_kind == "measured"
                      else "fallback HBM copy bandwidth", "bytes_per_frame": frame_bytes},
-        "gpu_launches": args.steps * (1 + 5 * L),
+        "gpu_launches": args.steps * (1 + tts.tts_decode_layer_launch_count(desc) * L),
         "clocks": clk,
     }
 

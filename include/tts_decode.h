@@ -400,14 +400,16 @@ tts_status tts_check_wait_timeout(int32_t* err_flag, void* stream);
  *   a = bf16(silu(x W_gate^T) * x W_up^T)       (silu in f32)
  *   h = h + a W_down^T
  * Products accumulate in f32; every residual add is one f32 addition.  The projections
- * run on the tensor cores (bf16 x bf16, f32 accumulator) and each norm or f32 input is
- * first rounded and packed for them by a small kernel: eight launches on `stream`
- * (three packs, four projections, the decode step); the sums of a projection's column
- * ranges are added in a fixed order, so results do not depend on timing.  The weights
- * and the gammas are treated
- * as constants: each launch starts reading them before the preceding kernel on `stream`
- * has finished, so they must not be written by the kernel launched just before this
- * call on the same stream (write them with a copy, or synchronise first).  Weights are bf16, row-major, rows of `hidden` (or `inter`) elements:
+ * run on the tensor cores (bf16 x bf16, f32 accumulator).  Each norm input is rounded
+ * and packed for them by a small kernel; the decode step writes its output already
+ * rounded and packed, and the SiLU-multiply writes `a` packed.  That makes seven
+ * launches on `stream` (two packs, four projections, the decode step;
+ * tts_decode_layer_launch_count).  The sums of a projection's column ranges are added in
+ * a fixed order, so results do not depend on timing.  The weights and the gammas are
+ * treated as constants: each launch starts reading them before the preceding kernel on
+ * `stream` has finished, so they must not be written by the kernel launched just before
+ * this call on the same stream (write them with a copy, or synchronise first).  Weights
+ * are bf16, row-major, rows of `hidden` (or `inter`) elements:
  *   w_qkv [(Hq + 2 Hkv) D][hidden], w_o [hidden][Hq D], w_gu [2 inter][hidden] (the
  *   gate rows, then the up rows), w_down [hidden][inter].
  * hidden, inter and Hq*D must be multiples of 256 and at most 8192.
@@ -429,6 +431,10 @@ typedef struct {
 
 size_t tts_decode_layer_scratch_size(const tts_kv_desc* desc, int32_t hidden, int32_t inter,
                                      int32_t n_splits);
+
+/* Kernel launches one tts_decode_layer call makes for this descriptor (7; 5 in a build
+ * whose CUDA-core projections serve this stream count); 0 for a descriptor it rejects. */
+int32_t tts_decode_layer_launch_count(const tts_kv_desc* desc);
 
 tts_status tts_decode_layer(float* h, const tts_layer_weights* weights, float eps,
                             const float* rope_cs, int32_t rope_max_pos, void* k_cache,

@@ -63,6 +63,15 @@ def test_status_strings(tts):
     assert tts.status_str(99) == "TTS_ERR_UNKNOWN"
 
 
+def test_decode_layer_launch_count(tts):
+    # two norm packs, four projections and the decode step (its output goes to the o
+    # projection already packed); shapes the layer rejects count 0
+    assert tts.tts_decode_layer_launch_count(tts.kv_desc(32, 16, 8, 128, 4096, "f32")) == 7
+    assert tts.tts_decode_layer_launch_count(tts.kv_desc(1, 16, 8, 128, 4096, "bf16")) == 7
+    assert tts.tts_decode_layer_launch_count(tts.kv_desc(33, 16, 8, 128, 4096, "f32")) == 0
+    assert tts.tts_decode_layer_launch_count(tts.kv_desc(4, 16, 8, 96, 4096, "f32")) == 0
+
+
 def _call_attn(tts, desc, q=16, k=16, v=16, nv=16, out=16, ws=256, ws_bytes=1 << 20, n_splits=0):
     P = ctypes.c_void_p
     return tts._lib.tts_decode_attn(P(q) if q else None, desc.n_q_heads * desc.head_dim,
