@@ -500,7 +500,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_mma_kernel(const __grid_cons
           const float up[8] = {ua.x, ua.y, ua.z, ua.w, ub.x, ub.y, ub.z, ub.w};
           float o[8];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) o[e] = b < p.B ? gt[e] / (1.0f + expf(-gt[e])) * up[e] : 0.f;
+          // silu(g) = g / (1 + e^-g) with the fast exponential and division (a few ulp;
+          // for g below about -88 the denominator is inf and the quotient 0, the limit)
+          for (int e = 0; e < 8; ++e) o[e] = b < p.B ? __fdividef(gt[e], 1.0f + __expf(-gt[e])) * up[e] : 0.f;
           static_cast<uint4*>(p.y)[static_cast<int64_t>(item / 8) * NB + b] =
               make_uint4(pack2_bf16(o[0], o[1]), pack2_bf16(o[2], o[3]), pack2_bf16(o[4], o[5]), pack2_bf16(o[6], o[7]));
         }
