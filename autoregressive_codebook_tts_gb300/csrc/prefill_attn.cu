@@ -218,8 +218,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_attn_kernel(const __grid_
     mbar_init_fence();
   }
   __syncthreads();
-  grid_wait();   // the rows launch wrote the prompt's cache rows and rotated q rows
   grid_launch_dependents();
+  // start[] and the cache rows below the prompt were final before the rows launch began
+  // (it waits for its own predecessor before it lets this launch start), so they are
+  // read before the dependency wait; the prompt's cache rows and the rotated q rows are
+  // the rows launch's, read after it (the producer waits before the first tile that
+  // holds a prompt row, the consumers before the query rows)
   const int st = __ldcg(p.start + b);
   // the item's window ends with its last query's: [0, start + t0 + nq)
   const int nv_max = min(max(st + t0 + nq, 1), p.capacity);
@@ -235,9 +239,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_attn_kernel(const __grid_
     // ---------------------------------------------------------------- producer
     if (lane == 0) {
       int issued = 0;
-      bool ok = true;
+      bool ok = true, waited = false;
       const int box_bytes = br * D * static_cast<int>(sizeof(KvT));
       for (; issued < ntiles; ++issued) {
+        if (!waited && c0 + (issued + 1) * kTile > st) {
+          grid_wait();
+          waited = true;
+        }
         const int s = issued % kStages;
         if (issued >= kStages && !mbar_wait(&empty[s], static_cast<uint32_t>((issued / kStages) - 1) & 1u)) {
           ok = false;
@@ -278,6 +286,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_attn_kernel(const __grid_
   }
 
   // ------------------------------------------------------------------ consumers
+  grid_wait();   // the rows launch normed and rotated the query rows
   // the warp's 8 query rows (row r = t_local * G + h), zero past the prompt
   float* sqw = sq + warp * 8 * D;
   for (int e = lane; e < 8 * D / 4; e += 32) {

@@ -255,8 +255,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_attn_tc_kernel(const __gr
   tc_fence_after();
   const uint32_t tmem = *s_tmem;
   const uint32_t tO = tmem + 2 * kN;   // S(t) at tmem + (t & 1) * kN
-  grid_wait();   // the rows launch wrote the prompt's cache rows and rotated q rows
   grid_launch_dependents();
+  // start[] and the cache rows below the prompt were final before the rows launch began
+  // (it waits for its own predecessor before it lets this launch start), so they are
+  // read before the dependency wait; the prompt's cache rows and the rotated q rows are
+  // the rows launch's, read after it (the producer waits before the first tile that
+  // holds a prompt row, the softmax warps before the query rows)
   const int st = __ldcg(p.start + b);
   const int nv_max = min(max(st + t0 + nq, 1), p.capacity);
   const int ch_len = prefill_chunk_len(nv_max, p.n_ch);
@@ -269,9 +273,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_attn_tc_kernel(const __gr
     // K(t) goes into its stage once S(t - kNK) is done, V(t) once O += P(t - kNV) V(t - kNV) is
     if (lane == 0 && ntiles > 0) {
       int nk = 0, nvv = 0;   // K and V tiles issued
-      bool ok = true;
+      bool ok = true, waited = false;
       for (int i = 0; i < ntiles; ++i) {
         const int r0 = c0 + i * kN;
+        if (!waited && r0 + kN > st) {
+          grid_wait();
+          waited = true;
+        }
         int row;
         if (!p.paged) {
           row = (b * p.n_kv_heads + g) * p.capacity + r0;
@@ -391,6 +399,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_attn_tc_kernel(const __gr
     const int lim = tl < nq ? min(min(max(raw, 1), p.capacity), c1) : c1;
     if (w == 0 && ch == 0 && g == 0 && h == 0 && tl < nq && (raw < 1 || raw > p.capacity))
       set_err(p.err, TTS_EFLAG_NVALID);
+    grid_wait();   // the rows launch normed and rotated the query rows
     // the query rows, split into bf16 value and remainder, in the swizzled A layout:
     // warp k takes rows 16k..16k+15, one coalesced 512-byte row per load (lane j holds
     // columns 4j..4j+3: 64-column chunk j / 16, 16-byte unit (j % 16) / 2, half j % 2)

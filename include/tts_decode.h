@@ -32,9 +32,11 @@
  *     only on shapes and capacity, never on device data such as cur_len, so a
  *     sequence of calls can be captured in a CUDA graph and replayed with fixed
  *     addresses.
- *   - Kernels are launched with programmatic stream serialisation: each kernel waits
- *     for the previous kernel on the stream before touching its inputs (one
- *     documented opt-in exception, TTS_KV_PREFETCH_BEFORE_WAIT below).
+ *   - Kernels are launched with programmatic stream serialisation: a call touches its
+ *     inputs only after the work enqueued before it on the stream has finished (its
+ *     first kernel waits for the previous kernel; a later kernel of the same call may
+ *     read the call's inputs as soon as that wait is behind it); one documented opt-in
+ *     exception, TTS_KV_PREFETCH_BEFORE_WAIT below.
  *   - The returned tts_status reports errors found on the host, before any launch
  *     (null pointers, bad shapes, misalignment, short workspace, launch failure).
  *     Nothing is launched when it is not TTS_OK.
