@@ -159,6 +159,30 @@ bool multi_query_prefill(const tts_kv_desc* d, int T) {
          rows < (int64_t{1} << 31);
 }
 
+// The prefill workspace: the attention's own part (split or chunk partials), then the
+// normed and rotated q rows [B T][Hq D] f32 at a 256-byte boundary (the caller's q rows
+// are read only).
+struct PrefillWs {
+  size_t attn, q_off, total;
+  bool q_rows;
+};
+PrefillWs prefill_ws(const tts_kv_desc* d, int T, int n_splits) {
+  PrefillWs w;
+  const bool mq = multi_query_prefill(d, T);
+  if (mq) {
+    w.attn = prefill_attn_workspace(d->B, T, d->n_kv_heads, d->n_q_heads / d->n_kv_heads, d->head_dim, d->capacity,
+                                    n_splits, sm_count(), prefill_rows(d));
+  } else {
+    tts_kv_desc dq = *d;  // the B*T queries take the place of the streams
+    dq.B = d->B * T;
+    w.attn = tts_decode_attn_workspace_size(&dq, n_splits);
+  }
+  w.q_rows = true;
+  w.q_off = round256(w.attn);
+  w.total = w.q_rows ? w.q_off + round256(static_cast<size_t>(d->B) * T * d->n_q_heads * d->head_dim * 4) : w.attn;
+  return w;
+}
+
 }  // namespace
 
 extern "C" {
@@ -398,15 +422,8 @@ tts_status tts_decode_step(const float* q, const float* k, const float* v, int64
 
 size_t tts_prefill_workspace_size(const tts_kv_desc* d, int32_t T, int32_t n_splits) {
   if (check_desc(d) != TTS_OK || T < 1 || static_cast<int64_t>(d->B) * T > 65535) return 0;
-  if (multi_query_prefill(d, T)) {
-    // the chunk results of the multi-query kernel (none with one chunk per item)
-    const size_t w = prefill_attn_workspace(d->B, T, d->n_kv_heads, d->n_q_heads / d->n_kv_heads, d->head_dim,
-                                            d->capacity, n_splits, sm_count(), prefill_rows(d));
-    return w > 256 ? w : 256;
-  }
-  tts_kv_desc dq = *d;  // the B*T queries take the place of the streams
-  dq.B = d->B * T;
-  return tts_decode_attn_workspace_size(&dq, n_splits);
+  const size_t w = prefill_ws(d, T, n_splits).total;
+  return w > 256 ? w : 256;
 }
 
 int32_t tts_prefill_launch_count(const tts_kv_desc* d, int32_t T, int32_t n_splits) {
@@ -420,7 +437,7 @@ int32_t tts_prefill_launch_count(const tts_kv_desc* d, int32_t T, int32_t n_spli
   return merged ? 2 : 3;
 }
 
-tts_status tts_prefill_step(float* q, const float* k, const float* v, int64_t row_stride,
+tts_status tts_prefill_step(const float* q, const float* k, const float* v, int64_t row_stride,
                             const float* gamma_q, const float* gamma_k, float eps,
                             const float* rope_cs, int32_t rope_max_pos, void* k_cache,
                             void* v_cache, const tts_kv_desc* d, const int32_t* start_pos,
@@ -438,6 +455,14 @@ tts_status tts_prefill_step(float* q, const float* k, const float* v, int64_t ro
   AttnParams p = {};
   int used = 0;
   PrefillAttnParams pp = {};
+  const PrefillWs pw = prefill_ws(d, T, n_splits);
+  float* q_rows = nullptr;  // the normed q rows, for the paths that read them from memory
+  if (pw.q_rows) {
+    if (workspace == nullptr) return TTS_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return TTS_ERR_ALIGN;
+    if (ws_bytes < pw.total) return TTS_ERR_WORKSPACE;
+    q_rows = reinterpret_cast<float*>(static_cast<unsigned char*>(workspace) + pw.q_off);
+  }
   if (mq) {
     if (k_cache == nullptr || v_cache == nullptr) return TTS_ERR_NULL;
     if (!aligned16(k_cache) || !aligned16(v_cache)) return TTS_ERR_ALIGN;
@@ -468,6 +493,7 @@ tts_status tts_prefill_step(float* q, const float* k, const float* v, int64_t ro
   cudaStream_t s = as_stream(stream);
   PrefillRowsParams rp = {};
   rp.q = q;
+  rp.q_out = q_rows;
   rp.k = k;
   rp.v = v;
   rp.row_stride = row_stride;
@@ -495,8 +521,8 @@ tts_status tts_prefill_step(float* q, const float* k, const float* v, int64_t ro
   st = from_cuda(launch_prefill_rows(rp, s));
   if (st != TTS_OK) return st;
   if (mq) {
-    pp.q = q;
-    pp.q_stride = row_stride;
+    pp.q = q_rows;
+    pp.q_stride = static_cast<int64_t>(d->n_q_heads) * d->head_dim;
     pp.start = start_pos;
     pp.B = d->B;
     pp.T = T;
@@ -514,8 +540,8 @@ tts_status tts_prefill_step(float* q, const float* k, const float* v, int64_t ro
     return from_cuda(launch_prefill_attn(pp, k_cache, v_cache, d->kv_dtype == TTS_BF16, d->head_dim,
                                          d->n_q_heads / d->n_kv_heads, s));
   }
-  p.q = q;
-  p.q_stride = row_stride;
+  p.q = q_rows;
+  p.q_stride = static_cast<int64_t>(d->n_q_heads) * d->head_dim;
   p.lens = start_pos;
   p.q_per_stream = T;
   p.lens_add = 1;  // query t's window is [0, start + t + 1)

@@ -103,7 +103,8 @@ struct AttnParams {
 // Prefill rows: for query row r = b * T + t (position start[b] + t), q RMS-normed and
 // rotated in place, k normed and rotated into the cache, v copied into the cache.
 struct PrefillRowsParams {
-  float* q;
+  const float* q;
+  float* q_out;         // the normed and rotated q rows [B T][Hq D], dense; nullptr: q skipped
   const float* k;
   const float* v;
   int64_t row_stride;   // floats between consecutive rows r of q, k and v
@@ -197,7 +198,7 @@ __host__ __device__ inline int prefill_chunk_len(int nv_max, int n_ch) {
   return (per + kPrefillTile - 1) / kPrefillTile * kPrefillTile;
 }
 struct PrefillAttnParams {
-  const float* q;
+  const float* q;               // the normed and rotated q rows (the rows launch's)
   int64_t q_stride;
   const int32_t* start;         // [B]
   int B, T, n_q_heads, n_kv_heads, capacity;

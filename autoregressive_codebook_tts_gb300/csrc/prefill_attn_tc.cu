@@ -29,7 +29,10 @@
 // and V tiles with 3-D tensor-map loads (one per tile and operand), warp 9 allocates
 // tensor memory and issues the products.  In the last tile, V rows past the chunk are
 // zeroed before their product (a cache tail may hold anything).
-// Every wait is bounded; on expiry TTS_EFLAG_TIMEOUT is set and the CTA winds down.
+// The K/V tiles below the prompt stream before the dependency wait (they were final
+// before the rows launch let this one start); the producer waits before the first tile
+// that holds prompt rows, the softmax warps before the query rows (both the rows
+// launch's).  Every wait is bounded; on expiry TTS_EFLAG_TIMEOUT is set and the CTA winds down.
 #include <cstdint>
 #include <mutex>
 
@@ -399,11 +402,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_attn_tc_kernel(const __gr
     const int lim = tl < nq ? min(min(max(raw, 1), p.capacity), c1) : c1;
     if (w == 0 && ch == 0 && g == 0 && h == 0 && tl < nq && (raw < 1 || raw > p.capacity))
       set_err(p.err, TTS_EFLAG_NVALID);
-    grid_wait();   // the rows launch normed and rotated the query rows
-    // the query rows, split into bf16 value and remainder, in the swizzled A layout:
-    // warp k takes rows 16k..16k+15, one coalesced 512-byte row per load (lane j holds
-    // columns 4j..4j+3: 64-column chunk j / 16, 16-byte unit (j % 16) / 2, half j % 2)
+    // the query rows (normed and rotated by the rows launch: read after the dependency
+    // wait), split into bf16 value and remainder in the swizzled A layout: warp k takes
+    // rows 16k..16k+15, one coalesced 512-byte row per load (lane j holds columns
+    // 4j..4j+3: 64-column chunk j / 16, 16-byte unit (j % 16) / 2, half j % 2)
     {
+      grid_wait();
       float4 v[16];
 #pragma unroll
       for (int i = 0; i < 16; ++i) {

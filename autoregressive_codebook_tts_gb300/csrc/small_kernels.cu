@@ -169,9 +169,9 @@ __global__ void __launch_bounds__(kSetRowsThreads) set_rows_kernel(const SetRows
 // ---------------------------------------------------------------------------
 // Prefill rows ("qwentts.cpp ... src/pipeline-tts.h", KV cache section: the prefill
 // writes the prompt's positions into the cache).  Row r = b * T + t sits at position
-// start[b] + t: its q heads are RMS-normed and rotated in place (the attention reads
-// them), its k heads normed, rotated and written into the cache, its v heads written
-// as they are.  One group of D/4 lanes per head row, as in the standalone norm.
+// start[b] + t: its q heads are RMS-normed and rotated into q_out (the attention reads
+// them there; the caller's q rows are left as they are), its k heads normed, rotated and
+// written into the cache, its v heads written as they are.  One group of D/4 lanes per head row, as in the standalone norm.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void store4(float* dst, const float (&x)[4]) {
   *reinterpret_cast<float4*>(dst) = make_float4(x[0], x[1], x[2], x[3]);
@@ -197,13 +197,17 @@ __global__ void __launch_bounds__(kNormWarps * 32) prefill_rows_kernel(const Pre
   if (!pos_ok && row == 0 && (lane % LPR) == 0) set_err(p.err, TTS_EFLAG_POS_RANGE);
   const int rpos = min(max(pos, 0), p.max_pos - 1);
   const int kind = row < Hq ? 0 : (row < Hq + Hkv ? 1 : 2);  // q, k, v
+  // q rows nobody reads from here are skipped: a warp whose rows are all such leaves;
+  // otherwise they run the norm's shuffles on zeros and store nothing
+  const bool skip = kind == 0 && p.q_out == nullptr;
+  if (__all_sync(kFull, skip)) return;
   const int e0 = (lane % LPR) * EPL;
   const int64_t base = static_cast<int64_t>(r) * p.row_stride;
   const float* src = kind == 0 ? p.q + base + static_cast<int64_t>(row) * D
                    : kind == 1 ? p.k + base + static_cast<int64_t>(row - Hq) * D
                                : p.v + base + static_cast<int64_t>(row - Hq - Hkv) * D;
   float x[EPL] = {0.f, 0.f, 0.f, 0.f};
-  if (live) {
+  if (live && !skip) {
     const float4 v = __ldcg(reinterpret_cast<const float4*>(src + e0));
     x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
   }
@@ -217,7 +221,9 @@ __global__ void __launch_bounds__(kNormWarps * 32) prefill_rows_kernel(const Pre
   norm_rope_regs<EPL, 1, LPR>(y, gam, cs, p.eps, lane % LPR, D);
   if (!live) return;
   if (kind == 0) {
-    *reinterpret_cast<float4*>(p.q + base + static_cast<int64_t>(row) * D + e0) = make_float4(y[0], y[1], y[2], y[3]);
+    if (!skip)
+      *reinterpret_cast<float4*>(p.q_out + static_cast<int64_t>(r) * Hq * D + static_cast<int64_t>(row) * D + e0) =
+          make_float4(y[0], y[1], y[2], y[3]);
     return;
   }
   if (!pos_ok) return;

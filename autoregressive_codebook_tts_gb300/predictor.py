@@ -18,8 +18,7 @@ replays several frames per graph launch.  One frame of B streams, in the order o
 Everything here is argument marshalling: buffers are allocated once, and ``enqueue``
 only issues ``tts_frame_embed``, ``tts_prefill_step``, ``tts_sample_embed`` (the sampler
 with the gather of the drawn code), ``tts_sample``, ``tts_decode_step`` and
-``tts_counter_advance`` calls (plus one device copy of the
-prefill rows, which the prefill norms in place).  The QKV projection and the
+``tts_counter_advance`` calls.  The QKV projection and the
 output heads sit outside this path, so the q/k/v rows of every (position, layer) and
 the logits of every sub-step are inputs.  Sampler draw j of a frame uses the Philox
 counter words (counter, stream, j, 0); the counter moves by one per frame.
@@ -38,8 +37,7 @@ class PredictorFrames:
 
     tables: 15 device tensors [vocab][hidden] (group table j for sub-code j).
     pre: [L][2B][width] f32, the prefill rows (row b*2 + t, width = (Hq + 2 Hkv) D,
-        laid out [q | k | v]).  The prefill norms q in place, so each frame first copies
-        these rows into a working buffer, as the projection would write fresh ones.
+        laid out [q | k | v]), read only.
     qkv: [16][L][B][width] f32, the rows of positions 2..15 (entries 0 and 1 unused).
     logits: [15][B][vocab] f32 (logits[j - 1] decides sub-code j).
     gq, gk: [L][D] f32.
@@ -58,8 +56,7 @@ class PredictorFrames:
         self.slots = slots
         self.tabs = [tts.tables([t]) for t in tables]
         self._tables = tables
-        self.pre_src, self.qkv, self.logits, self.gq, self.gk = pre, qkv, logits, gq, gk
-        self.pre = torch.empty_like(pre)
+        self.pre, self.qkv, self.logits, self.gq, self.gk = pre, qkv, logits, gq, gk
         D = head_dim
         self.caches = [(torch.zeros(B, n_kv_heads, capacity, D, device=device),
                         torch.zeros(B, n_kv_heads, capacity, D, device=device)) for _ in range(layers)]
@@ -94,11 +91,6 @@ class PredictorFrames:
         qd, kd = Hq * D, Hkv * D
         codes = self.codes[s]
         ef = self.err
-        if stream is None:
-            self.pre.copy_(self.pre_src, non_blocking=True)
-        else:
-            with torch.cuda.stream(stream):
-                self.pre.copy_(self.pre_src, non_blocking=True)
         tts.tts_frame_embed(self.tabs[0], codes[:, 0:1], None, self.emb[s, 0], ef, stream=stream)
         for l in range(L):
             rows = self.pre[l]

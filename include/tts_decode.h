@@ -294,20 +294,21 @@ tts_status tts_decode_step_noalloc(const float* q, const float* k, const float* 
  * Prefill: T new positions per stream in one call ([P-pipeline], KV-cache section:
  * the prefill writes the prompt's rows from the reset position, causally).  Row t of
  * stream b sits at position p = start_pos[b] + t, t < T:
- *   q'[b][t] = norm_rope(q[b][t], gamma_q, p), written back into q (in place)
+ *   q'[b][t] = norm_rope(q[b][t], gamma_q, p)
  *   K[b][.][p] = cvt(norm_rope(k[b][t], gamma_k, p)),  V[b][.][p] = cvt(v[b][t])
  *   out[b][t] = attention of q'[b][t] over [0, p + 1)
  * so every query sees the rows before the prompt and the prompt's rows up to its own.
  * With start_pos = 0 it is the prefill after a cache reset.
  *   q, k, v: device f32 rows, row r = b*T + t at ptr + r*row_stride (heads contiguous;
- *        they may be strided views of one projection row).  k and v are read only.
+ *        they may be strided views of one projection row), read only.
  *   out: device f32 [B][T][Hq][D], dense.
  *   start_pos: device int32 [B].  A position outside [0, capacity) or [0, rope_max_pos)
  *        is not written and sets TTS_EFLAG_POS_RANGE; a window past capacity is clamped
  *        and sets TTS_EFLAG_NVALID.  Paged: a page id outside [0, n_pages) skips that
  *        row's write and sets TTS_EFLAG_PAGE.
  *   workspace: at least tts_prefill_workspace_size(desc, T, n_splits) bytes, otherwise
- *        as for tts_decode_attn (its B x T queries take the place of its B streams).
+ *        as for tts_decode_attn (its B x T queries take the place of its B streams); it
+ *        also holds the normed q rows on the paths that read them from memory.
  * Launches on `stream`: the rows, then the attention.  T < 8: the attention runs the
  * B*T queries one by one (as tts_decode_attn).  T >= 8 (and, paged, pages of 8 rows or
  * more): blocks of queries of a stream share every K/V tile of their window (bf16
@@ -324,7 +325,7 @@ size_t tts_prefill_workspace_size(const tts_kv_desc* desc, int32_t T, int32_t n_
  * or 3); 0 for arguments it would reject as shapes.  For counting a graph's nodes. */
 int32_t tts_prefill_launch_count(const tts_kv_desc* desc, int32_t T, int32_t n_splits);
 
-tts_status tts_prefill_step(float* q, const float* k, const float* v, int64_t row_stride,
+tts_status tts_prefill_step(const float* q, const float* k, const float* v, int64_t row_stride,
                             const float* gamma_q, const float* gamma_k, float eps,
                             const float* rope_cs, int32_t rope_max_pos, void* k_cache,
                             void* v_cache, const tts_kv_desc* desc, const int32_t* start_pos,
