@@ -3,8 +3,9 @@
 // prefill writes the prompt's rows, query t of stream b sees positions
 // [0, start[b] + t + 1)).  A work item is 128 query rows (128 / G queries of a stream
 // times the G q heads of one kv head), the MMA's M; its window is cut on the device into
-// n_ch chunks of whole tiles, one CTA per (item, chunk), merged by
-// prefill_combine_kernel as for the CUDA-core kernel.
+// n_ch chunks of whole tiles, one CTA per (item, chunk).  The chunks merge inside a
+// thread-block cluster (2..8 chunks whose clusters the device keeps resident at once:
+// distributed shared memory, chunk order) or in prefill_combine_kernel after the launch.
 //
 // Per 64-row tile of the chunk (N = 64 cache rows):
 //   S = Q_hi K^T + Q_lo K^T          two K-major bf16 products (K = D = 128), the query
@@ -32,7 +33,8 @@
 // The K/V tiles below the prompt stream before the dependency wait (they were final
 // before the rows launch let this one start); the producer waits before the first tile
 // that holds prompt rows, the softmax warps before the query rows (both the rows
-// launch's).  Every wait is bounded; on expiry TTS_EFLAG_TIMEOUT is set and the CTA winds down.
+// launch's).  Every wait is bounded; on expiry TTS_EFLAG_TIMEOUT is set and the CTA
+// winds down.
 #include <cstdint>
 #include <mutex>
 
