@@ -304,7 +304,7 @@ def prefill_workspace(desc: TtsKvDesc, T: int, n_splits=0, device="cuda", stream
 def tts_prefill_step(q, k, v, gamma_q, gamma_k, eps, cs, max_pos, k_cache, v_cache,
                      desc: TtsKvDesc, start_pos, T, scale, out, ws, n_splits=0, err_flag=None,
                      stream=None):
-    """q, k, v: [B*T, ...] row views (row r = b*T + t); q is normed in place."""
+    """q, k, v: [B*T, ...] row views (row r = b*T + t), read only."""
     stride = _row_stride(q)
     assert k.stride(0) == stride and v.stride(0) == stride, "q, k, v rows must share one stride"
     _check(_lib.tts_prefill_step(_ptr(q), _ptr(k), _ptr(v), stride, _ptr(gamma_q), _ptr(gamma_k),
