@@ -3,8 +3,8 @@
 // options table, "Lean Talker frame": one-kernel counter RNG).
 //
 // One CTA per stream.  The logits row is staged in shared memory as order-preserving
-// integer keys; the k-th largest is found by a radix selection (four 8-bit passes of
-// a shared-memory histogram, three barriers a pass).  After the first pass one scan of
+// integer keys; the k-th largest is found by a radix selection (four 8-bit passes, each
+// counting into one shared-memory histogram per warp; three barriers a pass).  After the first pass one scan of
 // the row takes every key whose top byte is above the selected digit as a candidate and
 // lists the indices of those with the selected top byte; the other three passes and the
 // rest of the gather run over that list only.  Ties at the threshold go to the lowest
