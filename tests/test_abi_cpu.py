@@ -72,6 +72,18 @@ def test_decode_layer_launch_count(tts):
     assert tts.tts_decode_layer_launch_count(tts.kv_desc(4, 16, 8, 96, 4096, "f32")) == 0
 
 
+def test_prefill_workspace_holds_the_normed_q_rows(tts):
+    # every prefill path reads its normed q rows from the workspace (the caller's q is read
+    # only), after the attention's own part, at a 256-byte boundary
+    for dt in ("f32", "bf16"):
+        for B, T in ((1, 2), (4, 7), (1, 128), (2, 33)):
+            d = tts.kv_desc(B, 16, 8, 128, 4096, dt)
+            need = tts.tts_prefill_workspace_size(d, T, 0)
+            assert need >= B * T * 16 * 128 * 4
+            assert tts.tts_prefill_workspace_size(d, T, 1) >= B * T * 16 * 128 * 4
+    assert tts.tts_prefill_workspace_size(tts.kv_desc(1, 16, 8, 128, 4096, "f32"), 0, 0) == 0
+
+
 def _call_attn(tts, desc, q=16, k=16, v=16, nv=16, out=16, ws=256, ws_bytes=1 << 20, n_splits=0):
     P = ctypes.c_void_p
     return tts._lib.tts_decode_attn(P(q) if q else None, desc.n_q_heads * desc.head_dim,
