@@ -249,3 +249,53 @@ def test_paged_prefill_never_reads_entries_past_the_window(tts, T):
     for a, b in zip(*results):
         assert torch.equal(a.view(torch.int16) if a.dtype == torch.bfloat16 else a.view(torch.int32),
                            b.view(torch.int16) if b.dtype == torch.bfloat16 else b.view(torch.int32))
+
+
+@pytest.mark.parametrize("kv_dtype,T,n_splits", [("bf16", 100, 0), ("bf16", 100, 16), ("f32", 40, 0)])
+def test_prefill_graph_replay_equals_eager(tts, kv_dtype, T, n_splits):
+    """Two layers' prefill steps captured in a graph replay to the eager bytes: the
+    tensor-core kernel with its chunks merged in clusters (default) or by the combine
+    launch (16 chunks), and the CUDA-core kernel."""
+    w = W.workload("talker", layers=1, kv_dtype=kv_dtype)
+    B, Hq, Hkv, D = w.B, w.n_q_heads, w.n_kv_heads, w.head_dim
+    cs = rope_table(tts, w.capacity, D, w.rope_base)
+    layers = [Layer(w, seed=90 + l, cur_len=[2000]) for l in range(2)]
+    rows = [W.qkv(B * T, Hq, Hkv, D, 95 + l)[0].cuda() for l in range(2)]
+    qd, kd = Hq * D, Hkv * D
+    desc = layers[0].desc(tts)
+    ws = tts.prefill_workspace(desc, T, n_splits)
+    outs = [torch.empty(B, T, Hq, D, device="cuda") for _ in range(2)]
+    start = torch.full((B,), 2000, dtype=torch.int32, device="cuda")
+    ef = torch.zeros(1, dtype=torch.int32, device="cuda")
+    caches0 = [(L.d_K.clone(), L.d_V.clone()) for L in layers]
+
+    def step():
+        for l, L in enumerate(layers):
+            r = rows[l]
+            tts.tts_prefill_step(r[:, :qd], r[:, qd:qd + kd], r[:, qd + kd:], L.d_gq, L.d_gk, w.eps, cs,
+                                 w.capacity, L.d_K, L.d_V, desc, start, T, scale_of(w), outs[l], ws,
+                                 n_splits, ef)
+
+    step()
+    torch.cuda.synchronize()
+    eager = [o.clone() for o in outs]
+    eager_k = [L.d_K.clone() for L in layers]
+    for (k0, v0), L in zip(caches0, layers):
+        L.d_K.copy_(k0)
+        L.d_V.copy_(v0)
+    for o in outs:
+        o.fill_(float("nan"))
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        step()
+    g.replay()
+    torch.cuda.synchronize()
+    assert ef.item() == 0
+    for a, b in zip(eager, outs):
+        assert torch.equal(a, b)
+    # the caches bit for bit (their tails hold NaN poison, so compare the bits)
+    ibits = torch.int16 if eager_k[0].dtype == torch.bfloat16 else torch.int32
+    for a, L in zip(eager_k, layers):
+        assert torch.equal(a.view(ibits), L.d_K.view(ibits))
