@@ -109,3 +109,49 @@ def test_decode_layer_rejects_more_than_32_streams(tts):
         tts.tts_decode_layer(h, lw, 1e-6, cs, 4096, K, K, desc, cur, 0.1,
                              tts.layer_scratch(desc, 2048, 6144), 0)
     assert e.value.status == 2
+
+
+@pytest.mark.parametrize("B", [1, 32])
+def test_decode_layer_graph_replay_equals_eager(tts, B):
+    """Two layers captured in a graph replay to the eager bytes: the projections' column
+    ranges are summed in a fixed order and the attention's splits merged in a fixed order,
+    so nothing depends on timing."""
+    w = W.workload("talker", B=B, layers=1, capacity=512)
+    H, I, Hq, Hkv, D = w.hidden, 3 * w.hidden, w.n_q_heads, w.n_kv_heads, w.head_dim
+    cur = [(b * 37 + 5) % 500 for b in range(B)]
+    layers = [Layer(w, seed=120 + l, cur_len=cur, poison=True) for l in range(2)]
+    lws, keep = [], []
+    for l in range(2):
+        d = {k: v.cuda() for k, v in _weights(H, I, Hq, Hkv, D, 130 + l).items()}
+        keep.append(d)
+        lws.append(tts.layer_weights(d["w_qkv"], d["w_o"], d["w_gu"], d["w_down"], d["gamma_attn"],
+                                     d["gamma_mlp"], d["gamma_q"], d["gamma_k"]))
+    cs = rope_table(tts, w.capacity, D, w.rope_base)
+    descs = [L.desc(tts) for L in layers]
+    scratch = tts.layer_scratch(descs[0], H, I, 0)
+    ef = torch.zeros(1, dtype=torch.int32, device="cuda")
+    h0 = torch.randn(B, H, generator=torch.Generator().manual_seed(140)).cuda()
+    h = h0.clone()
+    caches0 = [(L.d_K.clone(), L.d_V.clone()) for L in layers]
+
+    def frame():
+        for l, L in enumerate(layers):
+            tts.tts_decode_layer(h, lws[l], w.eps, cs, w.capacity, L.d_K, L.d_V, descs[l], L.d_cur,
+                                 scale_of(w), scratch, 0, ef)
+
+    frame()
+    torch.cuda.synchronize()
+    eager = h.clone()
+    h.copy_(h0)
+    for (k0, v0), L in zip(caches0, layers):
+        L.d_K.copy_(k0)
+        L.d_V.copy_(v0)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        frame()
+    g.replay()
+    torch.cuda.synchronize()
+    assert ef.item() == 0
+    assert torch.equal(eager.view(torch.int32), h.view(torch.int32))
